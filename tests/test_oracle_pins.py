@@ -1,0 +1,489 @@
+"""Pins of the CPU oracle to facts it does not produce itself.
+
+Each test checks the oracle against a closed form, a hand-worked example
+(tests/golden/hand_examples.json), a library routine the step reduces to, an
+invariant, or brute force on tiny inputs.  ``tests/test_oracle_mutations.py``
+plants plausible mistakes in the oracle and checks that these pins catch
+each one, so the functions here must reach the oracle through the module
+attribute ``O`` (which the mutation harness patches).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import csa_synth
+from oracle import csa_oracle as O
+from tests._common import f64, oracle_comp, oracle_layer, oracle_state, rel_err_rows, step_tuple
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")))
+
+
+def _tiny_layer(dtype="f32", ratio=4, **kw):
+    base = dict(dtype=dtype, H=4, D=16, R=8, W=8, ratio=ratio, Hi=3, Di=8, topk=5, X=24)
+    base.update(kw)
+    return O.Layer(**base)
+
+
+def _tiny_comp(layer, d, rng, gate_scale=1.0):
+    L = layer.lanes
+    return O.Compressor(
+        wkv=O.store(rng.standard_normal((L * d, layer.X)) / math.sqrt(layer.X), layer.dtype),
+        wgate=O.store(gate_scale * rng.standard_normal((L * d, layer.X)) / math.sqrt(layer.X), layer.dtype),
+        ape=O.round_f32(rng.standard_normal((layer.ratio, L * d))),
+        norm_w=O.round_f32(1.0 + 0.1 * rng.standard_normal(d)),
+        d=d)
+
+
+def _inv_freq(R, base=10000.0):
+    return (base ** (-2.0 * np.arange(R // 2) / R)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------- storage rounding
+
+def test_round_bf16_matches_torch_cast():
+    """fp32 inputs: single rounding to bf16 equals torch's RNE cast (a library routine)."""
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 10.0 ** rng.integers(-30, 30, 20000),
+                        np.float32([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0, -0.0, 1e-40, -3e-39])
+                        ]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).float().numpy().astype(np.float64)
+    got = O.round_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_round_bf16_is_nearest_for_float64():
+    """float64 inputs: the result is a bf16 value and no bf16 neighbour is closer."""
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(5000) * 3.0
+    r = O.round_bf16(x)
+    assert np.array_equal(torch.from_numpy(r.astype(np.float32)).to(torch.bfloat16).double().numpy(), r)
+    ulp = np.ldexp(1.0, np.frexp(r)[1] - 8)
+    for cand in (r - ulp, r + ulp, r - ulp / 2, r + ulp / 2):
+        c = torch.from_numpy(cand.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        assert np.all(np.abs(x - r) <= np.abs(x - c) + 1e-300)
+
+
+# --------------------------------------------------------------------------- RoPE
+
+def test_rope_hand_example():
+    g = GOLDEN["rope_pair"]
+    out = O.rope(np.array(g["v"]), g["p"], np.float32(g["inv_freq"]))
+    assert np.allclose(out, g["expected"], rtol=0, atol=1e-15)
+    back = O.rope(out, g["p"], np.float32(g["inv_freq"]), inverse=True)
+    assert np.allclose(back, g["v"], rtol=0, atol=1e-15)
+
+
+def test_rope_pairs_are_interleaved_on_last_dims():
+    """Closed form per pair: dims (D-R+2i, D-R+2i+1) rotate by p*inv_freq[i]; others unchanged."""
+    D, R, p = 12, 6, 3
+    invf = np.float32([1.0, 0.25, 0.0625])
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(D)
+    out = O.rope(v, p, invf)
+    assert np.array_equal(out[:D - R], v[:D - R])
+    for i in range(R // 2):
+        th = p * float(invf[i])
+        a, b = v[D - R + 2 * i], v[D - R + 2 * i + 1]
+        assert out[D - R + 2 * i] == pytest.approx(a * math.cos(th) - b * math.sin(th), abs=1e-14)
+        assert out[D - R + 2 * i + 1] == pytest.approx(a * math.sin(th) + b * math.cos(th), abs=1e-14)
+
+
+def test_rope_preserves_norm_and_inverts():
+    rng = np.random.default_rng(4)
+    invf = _inv_freq(16)
+    for p in (0, 1, 7, 1000, 65535):
+        v = rng.standard_normal((5, 64))
+        r = O.rope(v, p, invf)
+        assert np.allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(v, axis=-1), rtol=1e-13)
+        assert np.allclose(O.rope(r, p, invf, inverse=True), v, atol=1e-13)
+
+
+def test_rope_dot_depends_only_on_relative_position():
+    """RoPE(q,p).RoPE(k,t) = RoPE(q,p+s).RoPE(k,t+s); power-of-two frequencies keep fp32 angles exact."""
+    rng = np.random.default_rng(5)
+    invf = np.float32([2.0 ** -e for e in range(8)])
+    q, k = rng.standard_normal(32), rng.standard_normal(32)
+    base = O.rope(q, 9, invf) @ O.rope(k, 4, invf)
+    for s in (1, 5, 100, 4096):
+        assert O.rope(q, 9 + s, invf) @ O.rope(k, 4 + s, invf) == pytest.approx(base, abs=1e-9)
+
+
+def test_rope_angle_is_fp32_product():
+    """R8: theta is fp32(p) * fp32(inv_freq) rounded to fp32 (not the exact product)."""
+    invf = np.float32([0.1234567])
+    p = 70001
+    th = O.rope_angles(p, invf)[0]
+    assert th == float(np.float32(p) * invf[0])
+    assert th != p * float(invf[0])
+    out = O.rope(np.array([1.0, 0.0]), p, invf)
+    assert out[0] == pytest.approx(math.cos(th), abs=1e-15)
+    assert abs(out[0] - math.cos(p * float(invf[0]))) > 1e-5
+
+
+# --------------------------------------------------------------------------- RMSNorm
+
+def test_rms_norm_closed_forms():
+    c, w, eps = 3.0, np.array([1.0, 2.0, -1.0, 0.5]), 1e-6
+    y = O.rms_norm(np.full(4, c), w, eps)
+    assert np.allclose(y, c / math.sqrt(c * c + eps) * w, rtol=1e-15)
+    rng = np.random.default_rng(6)
+    u = rng.standard_normal(64)
+    y = O.rms_norm(u, np.ones(64), 0.0)
+    assert np.mean(y * y) == pytest.approx(1.0, rel=1e-13)
+    assert np.allclose(O.rms_norm(7.5 * u, np.ones(64), 0.0), y, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------- compressor
+
+def test_pool_weights_sum_to_one():
+    rng = np.random.default_rng(7)
+    s = rng.standard_normal((8, 100)) * 5
+    w = O.pool_weights(s)
+    assert np.all(w > 0)
+    assert np.allclose(w.sum(axis=0), 1.0, atol=1e-15)
+    assert np.allclose(O.pool_weights(np.zeros((8, 3))), 1 / 8)
+    ref = scipy.special.softmax(s, axis=0)
+    assert np.allclose(w, ref, rtol=1e-13)
+
+
+def test_compressor_hand_example_overlap_row():
+    g = GOLDEN["compressor_overlap_row1"]
+    layer = _tiny_layer(ratio=4)
+    comp = O.Compressor(wkv=None, wgate=None, ape=np.zeros((4, 2)), norm_w=np.ones(1), d=1)
+    tok = {}
+    for t in range(4):
+        tok[t] = (np.array([g["kv_lane0"][t], -99.0]), np.array([g["gate_lane0"][t], 50.0]))
+    for t in range(4, 8):
+        tok[t] = (np.array([-99.0, g["kv_lane1"][t - 4]]), np.array([50.0, g["gate_lane1"][t - 4]]))
+    kv, s = O.window_entries(layer, comp, 1, tok)
+    u = (O.pool_weights(s) * kv).sum(axis=0)
+    assert u[0] == pytest.approx(g["expected_u"], rel=1e-14)
+
+
+def _entries_pooled(layer, comp, j, tok):
+    kv, s = O.window_entries(layer, comp, j, tok)
+    return (O.pool_weights(s) * kv).sum(axis=0)
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_compressor_constant_and_mean(ratio):
+    """All entries equal v -> pooled v; equal gates and zero APE -> arithmetic mean of the entries."""
+    layer = _tiny_layer(ratio=ratio)
+    L, d, r = layer.lanes, 6, ratio
+    rng = np.random.default_rng(8)
+    comp = O.Compressor(wkv=None, wgate=None, ape=rng.standard_normal((r, L * d)), norm_w=np.ones(d), d=d)
+    v = rng.standard_normal(d)
+    tok = {t: (np.tile(v, L), rng.standard_normal(L * d)) for t in range(3 * r)}
+    for j in range(3):
+        assert np.allclose(_entries_pooled(layer, comp, j, tok), v, rtol=1e-13)
+    comp.ape[:] = 0.0
+    tok = {t: (rng.standard_normal(L * d), np.full(L * d, 0.7)) for t in range(3 * r)}
+    for j in range(3):
+        got = _entries_pooled(layer, comp, j, tok)
+        if L == 1:
+            want = np.mean([tok[t][0] for t in range(j * r, (j + 1) * r)], axis=0)
+        else:
+            cur = [tok[t][0][d:] for t in range(j * r, (j + 1) * r)]
+            prev = [tok[t][0][:d] for t in range((j - 1) * r, j * r)] if j > 0 else []
+            want = np.mean(prev + cur, axis=0)
+        assert np.allclose(got, want, rtol=1e-13)
+
+
+def test_compressor_lane_and_ape_assignment():
+    """R1: previous window through lane 0, current through lane 1, APE indexed by t mod ratio.
+
+    One dominant gate selects exactly one entry: putting it on token t and lane
+    l must return that token's lane-l kv."""
+    layer = _tiny_layer(ratio=4)
+    d, r = 3, 4
+    comp = O.Compressor(wkv=None, wgate=None, ape=np.zeros((r, 2 * d)), norm_w=np.ones(d), d=d)
+    kvs = {t: np.arange(2 * d) + 100.0 * t for t in range(8)}
+    for t_hot, lane in [(0, 0), (2, 0), (3, 0), (4, 1), (7, 1)]:
+        tok = {t: (kvs[t], np.full(2 * d, -40.0)) for t in range(8)}
+        tok[t_hot][1][lane * d:(lane + 1) * d] = 40.0
+        got = _entries_pooled(layer, comp, 1, tok)
+        assert np.allclose(got, kvs[t_hot][lane * d:(lane + 1) * d], rtol=1e-12)
+    # APE: a large APE on slot 2 selects token 4+2 of the current window (lane 1)
+    comp.ape[2, d:] = 80.0
+    tok = {t: (kvs[t], np.zeros(2 * d)) for t in range(8)}
+    assert np.allclose(_entries_pooled(layer, comp, 1, tok), kvs[6][d:], rtol=1e-12)
+    # ... and of the previous window on lane 0 when that lane's APE dominates instead
+    comp.ape[:] = 0.0
+    comp.ape[1, :d] = 80.0
+    assert np.allclose(_entries_pooled(layer, comp, 1, tok), kvs[1][:d], rtol=1e-12)
+    # row 0 has no previous window: only lane 1 of tokens 0..3 contributes
+    comp.ape[:] = 0.0
+    tok = {t: (kvs[t], np.zeros(2 * d)) for t in range(4)}
+    assert np.allclose(_entries_pooled(layer, comp, 0, tok),
+                       np.mean([kvs[t][d:] for t in range(4)], axis=0), rtol=1e-13)
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_compress_streaming_is_chunking_invariant(ratio):
+    """Token-by-token, one-shot and random chunkings give bit-identical state and rows;
+    n_rows == floor(tokens / ratio) after every call; each row equals a from-scratch rebuild."""
+    layer = _tiny_layer(ratio=ratio, X=16)
+    d = 8
+    rng = np.random.default_rng(9)
+    comp = _tiny_comp(layer, d, rng)
+    invf = _inv_freq(layer.R)
+    T = 3 * ratio + 3
+    x = O.store(rng.standard_normal((1, T, layer.X)), layer.dtype)
+    F, cap = layer.frontier_slots, T // ratio + 2
+
+    def run(splits):
+        fr, pool, n = np.zeros((1, F, 2 * layer.lanes * d)), np.zeros((1, cap, d)), np.zeros(1, np.int64)
+        p = 0
+        for s in splits:
+            fr, pool, n, err = O.compress_append(layer, comp, x[:, p:p + s], np.array([p]), fr, pool, n, invf)
+            assert err == 0
+            p += s
+            assert n[0] == p // ratio
+        return fr, pool, n
+
+    one = run([T])
+    for splits in ([1] * T, [ratio - 1, ratio + 2, T - 2 * ratio - 1], [5, 1, T - 6]):
+        other = run(splits)
+        for a, b in zip(one, other):
+            assert np.array_equal(a, b)
+    _, pool, n = one
+    kv, g = O.project(layer, comp, x[0])
+    tok = {t: (kv[t], g[t]) for t in range(T)}
+    for j in range(int(n[0])):
+        lo = max(0, (j - 1) * ratio) if layer.lanes == 2 else j * ratio
+        only = {t: tok[t] for t in range(lo, (j + 1) * ratio)}
+        assert np.array_equal(O.compressor_row(layer, comp, j, only, invf), pool[0, j])
+
+
+def test_compressed_row_is_normed_and_roped_at_window_start():
+    """finalize_row = RoPE(j*r) of RMSNorm(u); rotating back gives a row with unit RMS (w = 1)."""
+    layer = _tiny_layer(ratio=4, dtype="f32")
+    d = 16
+    comp = O.Compressor(wkv=None, wgate=None, ape=None, norm_w=np.ones(d), d=d)
+    invf = _inv_freq(layer.R)
+    rng = np.random.default_rng(10)
+    u = rng.standard_normal(d) * 4
+    for j in (0, 1, 5):
+        row = O.finalize_row(layer, comp, u, j, invf)
+        unrot = O.rope(row, j * 4, invf, inverse=True)
+        assert np.mean(unrot ** 2) == pytest.approx(1.0, rel=1e-5)
+        assert np.allclose(unrot, u / np.sqrt(np.mean(u * u)), rtol=1e-5)
+
+
+def test_compress_refuses_inconsistent_state_and_capacity():
+    layer = _tiny_layer(ratio=4, X=16)
+    rng = np.random.default_rng(11)
+    comp = _tiny_comp(layer, 8, rng)
+    invf = _inv_freq(layer.R)
+    x = O.store(rng.standard_normal((2, 4, 16)), "f32")
+    fr, pool = rng.standard_normal((2, 8, 32)), np.zeros((2, 3, 8))
+    fr2, pool2, n2, err = O.compress_append(layer, comp, x, np.array([4, 8]), fr, pool, np.array([0, 2]), invf)
+    assert err == O.ERR_STATE
+    assert np.array_equal(fr2[0], fr[0]) and np.array_equal(pool2[0], pool[0]) and n2[0] == 0
+    assert n2[1] == 3
+    _, pool3, n3, err = O.compress_append(layer, comp, x, np.array([8, 8]), fr, pool, np.array([2, 2]), invf)
+    assert err == 0
+    _, _, n4, err = O.compress_append(layer, comp, x, np.array([12, 8]), fr, pool3, np.array([3, 2]), invf)
+    assert err == O.ERR_CAPACITY and n4[0] == 3
+
+
+# --------------------------------------------------------------------------- indexer / top-k
+
+def test_indexer_hand_example():
+    g = GOLDEN["indexer_scores"]
+    layer = _tiny_layer(Hi=2, Di=2, R=2, topk=g["topk"])
+    s = O.index_scores(layer, np.array(g["iq"]), np.array(g["iw"]), np.array(g["keys"]), 0, np.float32([1.0]))
+    assert np.allclose(s, g["expected_scores"], rtol=1e-15)
+    assert list(O.topk_select(s, g["topk"])) == g["expected_sel"]
+    s = O.index_scores(layer, np.array(g["iq"]), np.array(g["iw_neg"]), np.array(g["keys"]), 0,
+                       np.float32([1.0]))
+    assert np.allclose(s, g["expected_scores_neg"], rtol=1e-15)
+    assert list(O.topk_select(s, g["topk"])) == g["expected_sel_neg"]
+
+
+def test_indexer_single_head_reduces_to_relu_dot():
+    """Hi = 1 with iw = sqrt(Di): score_j = ReLU(RoPE(q,p) . key_j)."""
+    Di = 16
+    layer = _tiny_layer(Hi=1, Di=Di, R=8, dtype="f32")
+    rng = np.random.default_rng(12)
+    invf = _inv_freq(8)
+    q, keys = rng.standard_normal((1, Di)), rng.standard_normal((30, Di))
+    s = O.index_scores(layer, q, np.array([math.sqrt(Di)]), keys, 17, invf)
+    want = np.maximum(O.round_f32(O.rope(q[0], 17, invf)) @ keys.T, 0.0)
+    assert np.allclose(s, want, rtol=1e-12)
+    assert np.all(s >= 0) and np.any(s == 0)
+
+
+def test_topk_against_full_sort_brute_force():
+    rng = np.random.default_rng(13)
+    for trial in range(300):
+        n = int(rng.integers(1, 40))
+        k = int(rng.integers(1, 12))
+        s = rng.integers(-3, 4, n).astype(np.float64)  # many exact ties
+        want = sorted(sorted(range(n), key=lambda j: (-s[j], j))[:k])
+        assert list(O.topk_select(s, k)) == want
+    s = np.array([0.0, -0.0, 0.0, -1.0])
+    assert list(O.topk_select(s, 2)) == [0, 1]
+
+
+def test_visibility_hand_cases():
+    g = GOLDEN["visibility"]
+    layer = _tiny_layer(ratio=g["ratio"])
+    for p, want in g["cases"]:
+        assert O.visible_rows(layer, g["n"], p) == want
+    # decode sees every row emitted up to and including its own token
+    for p in range(64):
+        n = (p + 1) // 4
+        assert O.visible_rows(layer, n, p) == n
+
+
+# --------------------------------------------------------------------------- attention
+
+def test_attention_hand_example():
+    g = GOLDEN["attention_with_sink"]
+    layer = _tiny_layer(H=1, D=g["D"], scale=g["scale"])
+    o = O.attend(layer, np.array(g["q"]), np.array(g["keys"]), np.array(g["sink"]))
+    assert np.allclose(o, g["expected"], rtol=1e-14)
+
+
+def test_attention_sink_limits():
+    """Sink -inf: plain softmax (scipy); sink 0: o = o_plain * S / (S + 1), S = sum e^logit."""
+    layer = _tiny_layer(H=3, D=16)
+    rng = np.random.default_rng(14)
+    q, keys = rng.standard_normal((3, 16)), rng.standard_normal((11, 16))
+    logits = layer.softmax_scale * q @ keys.T
+    plain = scipy.special.softmax(logits, axis=1) @ keys
+    assert np.allclose(O.attend(layer, q, keys, np.full(3, -np.inf)), plain, rtol=1e-13)
+    S = np.exp(logits).sum(axis=1)
+    assert np.allclose(O.attend(layer, q, keys, np.zeros(3)), plain * (S / (S + 1))[:, None], rtol=1e-13)
+    big = O.attend(layer, 200 * q, keys, np.zeros(3))  # logits in the hundreds: no overflow
+    assert np.all(np.isfinite(big))
+
+
+def test_split_merge_equals_unsplit():
+    layer = _tiny_layer(H=4, D=16)
+    rng = np.random.default_rng(15)
+    q, keys, sink = rng.standard_normal((4, 16)), rng.standard_normal((37, 16)), rng.standard_normal(4)
+    full = O.attend(layer, q, keys, sink)
+    for trial in range(20):
+        cuts = np.sort(rng.integers(0, 38, int(rng.integers(0, 6))))
+        parts = np.split(np.arange(37), cuts)
+        got = O.merge_partials([O.attend_partial(layer, q, keys[ix]) for ix in parts], sink)
+        assert np.allclose(got, full, rtol=1e-12, atol=1e-14)
+
+
+def test_topk_covering_all_rows_equals_dense_attention():
+    """When topk >= visible rows, the indexer path equals attending every row (brute force)."""
+    layer = _tiny_layer(H=4, D=16, R=8, W=8, topk=64, Hi=2, Di=8)
+    rng = np.random.default_rng(16)
+    invf = _inv_freq(8)
+    B, cap, p = 1, 20, 60
+    pool = O.round_f32(rng.standard_normal((B, cap, 16)))
+    window = O.round_f32(rng.standard_normal((B, 8, 16)))
+    q, kv, sink = rng.standard_normal((B, 4, 16)), rng.standard_normal((B, 16)), rng.standard_normal(4)
+    n = np.array([15])
+    sel, n_sel = O.index_topk(layer, rng.standard_normal((B, 2, 8)), rng.standard_normal((B, 2)),
+                              rng.standard_normal((B, cap, 8)), n, np.array([p]), invf)
+    assert n_sel[0] == 15
+    a, w1, _ = O.attend_decode(layer, q, kv, sink, window, pool, n, sel, n_sel, np.array([p]), invf)
+    b, _, _ = O.attend_decode(layer, q, kv, sink, window, pool, n, None, None, np.array([p]), invf)
+    assert np.array_equal(a, b)
+    # brute force: explicit key list, plain softmax with the sink column
+    keys = list(pool[0, :15]) + [w1[0, t % 8] for t in range(p - 7, p + 1)]
+    qr = O.round_f32(O.rope(q[0], p, invf))
+    logits = layer.softmax_scale * qr @ np.array(keys).T
+    full = np.concatenate([logits, sink[:, None]], axis=1)
+    wts = scipy.special.softmax(full, axis=1)[:, :-1]
+    o = O.round_f32(O.rope(O.round_f32(wts @ np.array(keys)), p, invf, inverse=True))
+    assert np.allclose(a[0], o, rtol=1e-6, atol=1e-7)
+
+
+def test_window_holds_the_last_W_tokens():
+    """R4: the window is [p-W+1, p]; early on, ring slots of tokens that do not exist yet are ignored."""
+    layer = _tiny_layer(W=8, D=16, R=8)
+    invf = _inv_freq(8)
+    assert list(O.window_tokens(layer, 3)) == [0, 1, 2, 3]
+    assert list(O.window_tokens(layer, 20)) == list(range(13, 21))
+    pool = np.zeros((1, 4, 16))
+    q = np.zeros((1, 4, 16))
+    kv = np.zeros((1, 16))
+    for p, seen in ((3, False), (5, True)):
+        w = np.zeros((1, 8, 16))
+        w[0, 5] = 1.0  # token 5's slot; at p = 3 it holds stale data that must not be attended
+        kv_p = kv if p != 5 else np.ones((1, 16))
+        out, _, _ = O.attend_decode(layer, q, kv_p, np.full(4, -np.inf), w, pool, np.array([0]), None, None,
+                                    np.array([p]), invf)
+        assert (np.abs(out).max() > 0) == seen
+
+
+# --------------------------------------------------------------------------- decode == prefill
+
+def _decode_vs_prefill(ratio, T, ctx_tokens, topk):
+    """Run a chunk token by token (decode path) and as one prefill chunk; compare."""
+    cfg = csa_synth.CONFIGS[1].replace(ratio=ratio, topk=topk)
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(csa_synth.compressor(cfg, "attn")), None
+    if cfg.has_indexer:
+        ci = oracle_comp(csa_synth.compressor(cfg, "index"))
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    sink = f64(csa_synth.sinks(cfg))
+    cap = (ctx_tokens + T) // ratio + 2
+    st0 = oracle_state(csa_synth.empty_cache(cfg, cap, B=1))
+    # build a context by decoding ctx_tokens of hidden states through the compressors only
+    xs = f64(csa_synth.hidden(cfg, ctx_tokens, B=1))
+    if ctx_tokens:
+        st0["front_a"], st0["pool"], n, _ = O.compress_append(layer, ca, xs, st0["pos"], st0["front_a"],
+                                                              st0["pool"], st0["n_rows"], invf)
+        if ci is not None:
+            st0["front_i"], st0["ikeys"], _, _ = O.compress_append(layer, ci, xs, st0["pos"], st0["front_i"],
+                                                                   st0["ikeys"], st0["n_rows"], invf)
+        st0["n_rows"] = n
+        st0["pos"] = np.array([ctx_tokens])
+        rng = np.random.default_rng(18)
+        st0["window"] = O.round_f32(rng.standard_normal(st0["window"].shape))
+    ch = csa_synth.chunk_inputs(cfg, T)
+    x, q, kv, iq, iw = f64(ch.x), f64(ch.q), f64(ch.kv), f64(ch.iq), f64(ch.iw)
+    # decode path
+    st = {k: (v.copy() if v is not None else None) for k, v in st0.items()}
+    outs, sels = [], []
+    for i in range(T):
+        out, sel, n_sel, err = O.decode_step(layer, ca, ci, st, (x[:, i:i + 1], q[i:i + 1], kv[i:i + 1],
+                                             iq[i:i + 1], iw[i:i + 1]), sink, invf)
+        assert err == 0
+        outs.append(out[0])
+        sels.append(None if sel is None else sel[0, :n_sel[0]])
+    # prefill path
+    pf = {k: (v.copy() if v is not None else None) for k, v in st0.items()}
+    pf["front_a"], pf["pool"], n, _ = O.compress_append(layer, ca, x, pf["pos"], pf["front_a"], pf["pool"],
+                                                        pf["n_rows"], invf)
+    if ci is not None:
+        pf["front_i"], pf["ikeys"], _, _ = O.compress_append(layer, ci, x, pf["pos"], pf["front_i"],
+                                                             pf["ikeys"], pf["n_rows"], invf)
+    out_p, sel_p, nsel_p, win_p = O.attend_prefill_chunk(layer, q, kv, iq, iw, sink, int(pf["pos"][0]),
+                                                         pf["window"][0], pf["pool"][0], pf["ikeys"][0]
+                                                         if ci is not None else None, int(n[0]), invf)
+    assert np.array_equal(st["pool"], pf["pool"])
+    assert np.array_equal(st["window"][0], win_p)
+    assert rel_err_rows(np.stack(outs), out_p) <= 4e-6
+    if cfg.has_indexer:
+        for i in range(T):
+            assert list(sels[i]) == list(sel_p[i, :nsel_p[i]])
+    return np.stack(outs), out_p
+
+
+def test_decode_equals_prefill_from_empty_cache():
+    """Crosses window eviction (W = 32), 16 ratio-4 boundaries and the dense->sparse switch (topk 8)."""
+    _decode_vs_prefill(ratio=4, T=70, ctx_tokens=0, topk=8)
+
+
+def test_decode_equals_prefill_mid_sequence():
+    _decode_vs_prefill(ratio=4, T=37, ctx_tokens=41, topk=6)
+
+
+def test_decode_equals_prefill_ratio128():
+    _decode_vs_prefill(ratio=128, T=140, ctx_tokens=130, topk=16)
