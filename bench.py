@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Bench: one DeepSeek-V4-Flash CSA layer on GB300.
+
+Headline workload: batched decode, 32 sequences with 32768-token caches
+(8192 ratio-4 rows + 128-token window each), Flash shapes, bf16.  One step =
+the whole hot path for every sequence: compress (attention pool), compress
+(index pool), indexer top-k, attention + merge.  Metric: layer-steps/s (one
+step advances all 32 sequences by a token) and the achieved HBM GB/s of the
+step's algorithmic bytes.  Also measured: prefill tok/s of a 4096-token chunk
+on a 65536-token cache.
+
+Timing: CUDA events around each step on the launching stream; the 129 MB L2 is
+flushed (a 512 MB write) before every timed step, outside the events, because
+in a full model 42 other layers run between two steps of this one.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA decode layer-steps/s + achieved HBM GB/s (B=32, 32K ctx); prefill tok/s"
+UNIT = "layer-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            self.path = tempfile.mktemp(suffix=".csv")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(cid: int, budget_s: float, max_steps: int) -> dict:
+    """Time the CPU oracle on one sequence of the workload, stepping until the budget is spent.
+    Runs in its own process with single-threaded BLAS."""
+    import numpy as np
+
+    import csa_synth
+    from oracle import csa_oracle as O
+    cfg = csa_synth.CONFIGS[cid]
+    cap = cfg.ctx // cfg.ratio + max_steps // cfg.ratio + 8
+    host = csa_synth.synth_cache(cfg, cap, B=1)
+    f = lambda t: None if t is None else t.float().numpy().astype(np.float64)  # noqa: E731
+    layer = O.Layer(dtype=cfg.dtype, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
+                    topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+    comp = lambda c: O.Compressor(wkv=f(c.wkv), wgate=f(c.wgate), ape=f(c.ape), norm_w=f(c.norm_w), d=c.d)  # noqa
+    ca = comp(csa_synth.compressor(cfg, "attn"))
+    ci = comp(csa_synth.compressor(cfg, "index")) if cfg.has_indexer else None
+    st = dict(pool=f(host.pool), ikeys=f(host.ikeys), window=f(host.window), front_a=f(host.front_attn),
+              front_i=f(host.front_index), n_rows=host.n_rows.numpy().astype(np.int64),
+              pos=host.pos.numpy().astype(np.int64))
+    sink, invf = f(csa_synth.sinks(cfg)), csa_synth.inv_freq(cfg).numpy()
+    times = []
+    t_all = time.perf_counter()
+    for step in range(max_steps):
+        si = csa_synth.step_inputs(cfg, step, B=1)
+        t0 = time.perf_counter()
+        O.decode_step(layer, ca, ci, st, (f(si.x), f(si.q), f(si.kv), f(si.iq), f(si.iw)), sink, invf)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    per_seq = statistics.mean(times)
+    return {"seq_step_s": per_seq, "steps": len(times), "B": cfg.B,
+            "layer_steps_per_s": 1.0 / (per_seq * cfg.B)}
+
+
+def run_oracle_subprocess(cid: int, budget_s: float, max_steps: int) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(cid), str(budget_s), str(max_steps)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 4 * budget_s))
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("CSA_BENCH_GLOO") is None else "gloo")
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class DecodeWorkload:
+    """Config 3 state, weights and per-step inputs resident on one GPU."""
+
+    def __init__(self, cfg, cap: int, n_inputs: int, device):
+        import torch
+
+        import csa_synth
+        import deepseek_v4_compressed_csa_gb300 as csa
+        self.cfg, self.cap, self.dev = cfg, cap, device
+        self.L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
+                           Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+        d = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
+
+        def comp(c):
+            return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
+        self.ca = comp(csa_synth.compressor(cfg, "attn"))
+        self.ci = comp(csa_synth.compressor(cfg, "index")) if cfg.has_indexer else None
+        host = csa_synth.synth_cache(cfg, cap)
+        self.pool, self.ikeys, self.window = d(host.pool), d(host.ikeys), d(host.window)
+        self.front_a, self.front_i = d(host.front_attn), d(host.front_index)
+        self.n_a, self.n_i, self.pos = d(host.n_rows), d(host.n_rows), d(host.pos)
+        self.sink, self.invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
+        B = cfg.B
+        self.host_inputs = [csa_synth.step_inputs(cfg, i) for i in range(n_inputs)]
+        self.inputs = [{k: d(getattr(si, k)) for k in ("x", "q", "kv", "iq", "iw")} for si in self.host_inputs]
+        self.sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
+        self.n_sel = torch.empty(B, dtype=torch.int32, device=device)
+        self.out = torch.empty(B, cfg.H, cfg.D, dtype=cfg.storage, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=device)  # noqa: E731
+        self.ws_c = u8(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, cap))
+        self.ws_i = u8(csa.workspace_size(self.L, csa.OP_INDEX_TOPK, B, 1, cap))
+        self.ws_a = u8(csa.workspace_size(self.L, csa.OP_ATTEND_DECODE, B, 1, cap))
+        self.csa = csa
+
+    def step(self, inp, ev_index=None):
+        csa, cfg = self.csa, self.cfg
+        csa.compress_append(self.L, self.ca, inp["x"], self.pos, self.front_a, self.pool, self.n_a, self.invf,
+                            ws=self.ws_c, err=self.err)
+        sel = n_sel = None
+        if cfg.has_indexer:
+            csa.compress_append(self.L, self.ci, inp["x"], self.pos, self.front_i, self.ikeys, self.n_i, self.invf,
+                                ws=self.ws_c, err=self.err)
+            if ev_index is not None:
+                ev_index[0].record()
+            csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
+                           self.n_sel, ws=self.ws_i, err=self.err)
+            if ev_index is not None:
+                ev_index[1].record()
+            sel, n_sel = self.sel, self.n_sel
+        csa.attend_decode(self.L, inp["q"], inp["kv"], self.sink, self.window, self.pool, self.n_a, sel, n_sel,
+                          self.pos, self.invf, self.out, ws=self.ws_a, err=self.err)
+        self.pos.add_(1)
+
+
+def step_bytes(cfg, n_rows_mean: float) -> dict:
+    """Algorithmic HBM bytes of one decode step (each byte the step must move once)."""
+    B, e = cfg.B, 2
+    L = cfg.lanes
+    w = (2 * L * cfg.D * cfg.X + (2 * L * cfg.Di * cfg.X if cfg.has_indexer else 0)) * e
+    keys = B * n_rows_mean * cfg.Di * e if cfg.has_indexer else 0
+    rows = B * ((cfg.topk if cfg.has_indexer else n_rows_mean) + cfg.W) * cfg.D * e
+    qo = 2 * B * cfg.H * cfg.D * e
+    small = B * (cfg.X * e + cfg.D * e + cfg.Hi * cfg.Di * e + cfg.Hi * e + cfg.topk * 4)
+    fr = B * 2 * (2 * L * (cfg.D + (cfg.Di if cfg.has_indexer else 0))) * e  # frontier slot write + window row
+    return {"weights": w, "index_keys": keys, "attended_rows": rows, "q_out": qo, "small": small + fr,
+            "total": w + keys + rows + qo + small + fr}
+
+
+def run_ours(args):
+    import torch
+    dist, rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import csa_synth
+    import deepseek_v4_compressed_csa_gb300 as csa
+    csa.load_library()
+    cfg = csa_synth.CONFIGS[3]
+    total_steps = args.warmup + args.steps + args.e2e_steps + 2
+    cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
+    wl = DecodeWorkload(cfg, cap, n_inputs=8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        wl.step(wl.inputs[i % len(wl.inputs)])
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    n_start = wl.n_a.float().mean().item()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evi = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = csa.kernel_launches()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        wl.step(wl.inputs[(args.warmup + i) % len(wl.inputs)], ev_index=evi[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = csa.kernel_launches() - launches0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    idx_ms = [a.elapsed_time(b) for a, b in evi]
+    total_ms = _max_over_ranks(dist, sum(step_ms), dev)
+    assert wl.err.item() == 0, f"device error word {wl.err.item()}"
+    n_end = wl.n_a.float().mean().item()
+
+    # ---- end to end: pinned host inputs -> device, step, output -> pinned host
+    pinned = [{k: getattr(si, k).pin_memory() for k in ("x", "q", "kv", "iq", "iw")} for si in wl.host_inputs]
+    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(v) for k, v in wl.inputs[0].items()}
+    h2d = sum(t.numel() * t.element_size() for t in pinned[0].values())
+    d2h = out_host.numel() * out_host.element_size()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.e2e_steps)]
+    torch.cuda.synchronize()
+    for i in range(args.e2e_steps):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        for k, v in pinned[i % len(pinned)].items():
+            dev_in[k].copy_(v, non_blocking=True)
+        wl.step(dev_in)
+        out_host.copy_(wl.out, non_blocking=True)
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev2), dev) / max(1, args.e2e_steps)
+
+    # ---- prefill chunk (config 5), timed once per repeat from a restored snapshot
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
+
+    hbm, tflops, peak_src = _peaks()
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+    nb = step_bytes(cfg, 0.5 * (n_start + n_end))
+    idx_bytes = cfg.B * 0.5 * (n_start + n_end) * cfg.Di * 2 + cfg.B * (cfg.Hi * cfg.Di * 2 + cfg.Hi * 2 +
+                                                                        cfg.topk * 4)
+    idx_avg_s = statistics.mean(idx_ms) / 1e3
+    result = None
+    if rank == 0:
+        cpu = run_oracle_subprocess(3, args.cpu_budget, 400)
+        result = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": cfg.name, "global_batch": cfg.B * world, "seq_len": cfg.ctx, "B_per_gpu": cfg.B,
+                "heads": cfg.H, "latent": cfg.D, "window": cfg.W, "ratio": cfg.ratio, "index_heads": cfg.Hi,
+                "index_dim": cfg.Di, "topk": cfg.topk, "hidden": cfg.X, "compressed_rows": [n_start, n_end],
+                "tokens_per_s": round(value * cfg.B, 1),
+                "step_algorithmic_bytes": int(nb["total"]),
+                "step_hbm_gbs": round(nb["total"] / (ms_per_step / 1e3) / 1e9, 1),
+                "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
+                "l2": "flushed (512 MB write) before every timed step, outside the events",
+                "prefill": prefill,
+            },
+            "roofline": {
+                "kernel": "csa_index_topk (index-key scan + top-k)", "bound": "hbm",
+                "achieved": round(idx_bytes / idx_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(idx_bytes / idx_avg_s / 1e9 / hbm, 4), "traffic": None,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6800 GB/s", "avg_launch_ms": round(idx_avg_s * 1e3, 5),
+                "algorithmic_bytes_per_launch": int(idx_bytes),
+            },
+            "cpu_baseline": {"value": round(cpu["layer_steps_per_s"], 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"1 of {cfg.B} sequences x {cpu['steps']} decode steps of the same workload, "
+                                       f"float64 numpy oracle, single-threaded BLAS; per-layer-step time = "
+                                       f"{cfg.B} x per-sequence time"},
+            "e2e": {"value": round(world * 1e3 / e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def run_prefill(csa, csa_synth, dev, flush, repeats: int):
+    import torch
+    cfg = csa_synth.CONFIGS[5]
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 8
+    host = csa_synth.synth_cache(cfg, cap)
+    d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
+                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+
+    def comp(c):
+        return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
+    ca, ci = comp(csa_synth.compressor(cfg, "attn")), comp(csa_synth.compressor(cfg, "index"))
+    snap = {k: d(getattr(host, k)) for k in ("pool", "ikeys", "window", "front_attn", "front_index", "n_rows", "pos")}
+    st = {k: v.clone() for k, v in snap.items()}
+    n_i = st["n_rows"].clone()
+    ch = csa_synth.chunk_inputs(cfg)
+    x, q, kv, iq, iw = d(ch.x), d(ch.q), d(ch.kv), d(ch.iq), d(ch.iw)
+    sink, invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
+    out = torch.empty(cfg.T, cfg.H, cfg.D, dtype=cfg.storage, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=dev)  # noqa: E731
+    ws_c = u8(csa.workspace_size(L, csa.OP_COMPRESS, 1, cfg.T, cap))
+    ws_p = u8(csa.workspace_size(L, csa.OP_ATTEND_PREFILL, 1, cfg.T, cap))
+    times = []
+    for r in range(repeats + 1):
+        for k in st:
+            st[k].copy_(snap[k])
+        n_i.copy_(snap["n_rows"])
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        csa.compress_append(L, ca, x, st["pos"], st["front_attn"], st["pool"], st["n_rows"], invf, ws=ws_c, err=err)
+        csa.compress_append(L, ci, x, st["pos"], st["front_index"], st["ikeys"], n_i, invf, ws=ws_c, err=err)
+        csa.attend_prefill_chunk(L, q, kv, iq, iw, sink, cfg.ctx, st["window"][0], st["pool"][0], st["ikeys"][0],
+                                 st["n_rows"], invf, out, ws=ws_p, err=err)
+        e1.record()
+        torch.cuda.synchronize()
+        if r > 0:
+            times.append(e0.elapsed_time(e1))
+    assert err.item() == 0
+    ms = statistics.median(times)
+    nvis_sum = sum(min((cfg.ctx + cfg.T) // 4, (cfg.ctx + i + 1) // 4) for i in range(cfg.T))
+    flops = (nvis_sum * cfg.Hi * cfg.Di * 2 + cfg.T * (cfg.topk + cfg.W) * cfg.H * cfg.D * 4 +
+             cfg.T * cfg.X * (2 * 2 * (cfg.D + cfg.Di)) * 2)
+    _, tflops, _ = _peaks()
+    return {"workload": cfg.name, "tok_per_s": round(cfg.T / (ms / 1e3), 1), "ms_per_chunk": round(ms, 4),
+            "algorithmic_tflop": round(flops / 1e12, 4),
+            "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats}
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = max(5.0, min(120.0, 2.0 * (args.steps + args.warmup)))
+    r = run_oracle_subprocess(3, budget, args.warmup + args.steps)
+    value = r["layer_steps_per_s"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+        "steps": r["steps"], "warmup": 0, "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "flash-decode-b32-ctx32k", "global_batch": 32, "seq_len": 32768},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"1 of 32 sequences x {r['steps']} decode steps (float64 numpy oracle, "
+                                   "single-threaded BLAS), scaled x32 to a layer-step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--prefill-repeats", type=int, default=3)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--oracle-sample", nargs=3, default=None)
+    args = ap.parse_args()
+    if args.oracle_sample:
+        cid, budget, mx = args.oracle_sample
+        print(json.dumps(oracle_sample(int(cid), float(budget), int(mx))))
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

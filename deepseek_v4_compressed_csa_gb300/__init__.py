@@ -1,0 +1,12 @@
+"""One layer of DeepSeek-V4 Compressed Sparse Attention on GB300 (sm_103a).
+
+The compute lives in libcsa.so (hand-written CUDA, C ABI in include/csa.h);
+this package is its thin Python binding.  Importing it does not load the
+library; the first call does, and fails loudly if it was not built.
+"""
+from ._binding import (  # noqa: F401
+    CSA_BF16, CSA_F32, DEV_CAPACITY, DEV_RANGE, DEV_STATE, EXPORTS, LIB_PATH, OP_ATTEND_DECODE,
+    OP_ATTEND_PREFILL, OP_COMPRESS, OP_INDEX_TOPK, Compressor, CSAError, Layer, attend_decode,
+    attend_prefill_chunk, compress_append, frontier_slots, index_topk, kernel_launches, load_library,
+    workspace_size,
+)

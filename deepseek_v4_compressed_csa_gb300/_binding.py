@@ -1,0 +1,219 @@
+"""ctypes binding of libcsa.so: argument marshalling only.
+
+Every function here checks tensor devices, dtypes and shapes, passes raw
+device pointers and the current CUDA stream to the C ABI declared in
+include/csa.h, and turns a non-zero csa_status into an exception.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libcsa.so")
+
+CSA_F32, CSA_BF16 = 0, 1
+OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL = 0, 1, 2, 3
+DEV_CAPACITY, DEV_STATE, DEV_RANGE = 1, 2, 4
+CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
+EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
+           "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string")
+
+
+class CSAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int), ("R", ctypes.c_int),
+                ("W", ctypes.c_int), ("ratio", ctypes.c_int), ("Hi", ctypes.c_int), ("Di", ctypes.c_int),
+                ("topk", ctypes.c_int), ("X", ctypes.c_int), ("scale", ctypes.c_float),
+                ("rms_eps", ctypes.c_float)]
+
+
+class _Comp(ctypes.Structure):
+    _fields_ = [("wkv", ctypes.c_void_p), ("wgate", ctypes.c_void_p), ("ape", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p), ("d", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libcsa.so (built by build.py); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"CSA CUDA library not built: {path} is missing "
+                          "(run deepseek_v4_compressed_csa_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.csa_frontier_slots.argtypes = [i32]
+    lib.csa_frontier_slots.restype = i32
+    lib.csa_kernel_launches.argtypes = []
+    lib.csa_kernel_launches.restype = ctypes.c_ulonglong
+    lib.csa_status_string.argtypes = [i32]
+    lib.csa_status_string.restype = ctypes.c_char_p
+    lib.csa_workspace_size.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.csa_workspace_size.restype = i32
+    lib.csa_compress_append.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp, vp]
+    lib.csa_compress_append.restype = i32
+    lib.csa_index_topk.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.csa_index_topk.restype = i32
+    lib.csa_attend_decode.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.csa_attend_decode.restype = i32
+    lib.csa_attend_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, ctypes.c_int32, vp, vp, vp, i32, vp, vp,
+                                             vp, vp, vp, sz, vp, vp]
+    lib.csa_attend_prefill_chunk.restype = i32
+    _lib = lib
+    return lib
+
+
+@dataclass(frozen=True)
+class Layer:
+    """Mirror of csa_layer.  dtype: torch.bfloat16 or torch.float32 (model dtype)."""
+
+    dtype: torch.dtype
+    H: int
+    D: int
+    R: int
+    W: int
+    ratio: int
+    Hi: int
+    Di: int
+    topk: int
+    X: int
+    scale: float = 0.0
+    rms_eps: float = 1e-6
+
+    @property
+    def lanes(self) -> int:
+        return 2 if self.ratio == 4 else 1
+
+    @property
+    def has_indexer(self) -> bool:
+        return self.ratio == 4
+
+    def _c(self) -> _Layer:
+        code = CSA_BF16 if self.dtype == torch.bfloat16 else CSA_F32
+        return _Layer(code, self.H, self.D, self.R, self.W, self.ratio, self.Hi, self.Di, self.topk, self.X,
+                      float(self.scale), float(self.rms_eps))
+
+
+@dataclass
+class Compressor:
+    """Device weights of one compressor: wkv, wgate [L*d, X] model dtype; ape [ratio, L*d] fp32; norm_w [d] fp32."""
+
+    wkv: torch.Tensor
+    wgate: torch.Tensor
+    ape: torch.Tensor
+    norm_w: torch.Tensor
+    d: int
+
+    def _c(self) -> _Comp:
+        return _Comp(_ptr(self.wkv), _ptr(self.wgate), _ptr(self.ape), _ptr(self.norm_w), self.d)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("CSA tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("CSA tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise CSAError(fn, code)
+
+
+def kernel_launches() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(load_library().csa_kernel_launches())
+
+
+def frontier_slots(ratio: int) -> int:
+    return load_library().csa_frontier_slots(ratio)
+
+
+def workspace_size(layer: Layer, op: int, B: int, T: int, cap: int) -> int:
+    n = ctypes.c_size_t(0)
+    L = layer._c()
+    _check("csa_workspace_size", load_library().csa_workspace_size(ctypes.byref(L), op, B, T, cap, ctypes.byref(n)))
+    return int(n.value)
+
+
+def _ws(layer, op, B, T, cap, ws, device):
+    need = workspace_size(layer, op, B, T, cap)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def _err(err, device):
+    return torch.zeros(1, dtype=torch.int32, device=device) if err is None else err
+
+
+def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_rows, inv_freq, ws=None, err=None,
+                    stream=None):
+    """csa_compress_append; x [B,T,X]; returns the device error word tensor."""
+    B, T = x.shape[0], x.shape[1]
+    cap = pool.shape[1]
+    ws, nb = _ws(layer, OP_COMPRESS, B, T, cap, ws, x.device)
+    err = _err(err, x.device)
+    L, C = layer._c(), comp._c()
+    _check("csa_compress_append", load_library().csa_compress_append(
+        ctypes.byref(L), ctypes.byref(C), _ptr(x), B, T, _ptr(pos), _ptr(frontier), _ptr(pool), cap, _ptr(n_rows),
+        _ptr(inv_freq), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def index_topk(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, ws=None, err=None, stream=None):
+    B, cap = iq.shape[0], ikeys.shape[1]
+    ws, nb = _ws(layer, OP_INDEX_TOPK, B, 1, cap, ws, iq.device)
+    err = _err(err, iq.device)
+    L = layer._c()
+    _check("csa_index_topk", load_library().csa_index_topk(
+        ctypes.byref(L), _ptr(iq), _ptr(iw), B, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
+        _ptr(sel), _ptr(n_sel), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq, out, ws=None,
+                  err=None, stream=None):
+    B, cap = q.shape[0], pool.shape[1]
+    ws, nb = _ws(layer, OP_ATTEND_DECODE, B, 1, cap, ws, q.device)
+    err = _err(err, q.device)
+    L = layer._c()
+    _check("csa_attend_decode", load_library().csa_attend_decode(
+        ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(sink), B, _ptr(window), _ptr(pool), cap, _ptr(n_rows),
+        _ptr(sel), _ptr(n_sel), _ptr(pos), _ptr(inv_freq), _ptr(out), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, window, pool, ikeys, n_rows, inv_freq,
+                         out, sel_out=None, ws=None, err=None, stream=None):
+    T, cap = q.shape[0], pool.shape[-2]
+    ws, nb = _ws(layer, OP_ATTEND_PREFILL, 1, T, cap, ws, q.device)
+    err = _err(err, q.device)
+    L = layer._c()
+    _check("csa_attend_prefill_chunk", load_library().csa_attend_prefill_chunk(
+        ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(iq), _ptr(iw), _ptr(sink), T, int(pos0), _ptr(window),
+        _ptr(pool), _ptr(ikeys), cap, _ptr(n_rows), _ptr(inv_freq), _ptr(out), _ptr(sel_out), _ptr(ws), nb,
+        _ptr(err), _stream(stream)))
+    return err

@@ -1,0 +1,193 @@
+// Gated-pooling compressor: projection, window pooling, RMSNorm, RoPE, emit.
+//
+// Definitions: "DeepSeek-V4-Flash: native deepseek_v4 AR backend" (MTPLX #216),
+// "What V4 adds" (learned gated pooling, overlapping ratio-4 / non-overlapping
+// ratio-128 windows, maintained incrementally) and "Decode path" (pool in fp32,
+// cast back before the norm); "feat: add DeepSeek-V4 (Pro/Flash) model support"
+// (mlx-lm #1189), OmarB97 "Compressed pool rows must be roped at birth" (RoPE
+// at the window start j*ratio) and stepnoy's "Fix" 3 (the chunk tail is carried
+// across calls; the absolute position accumulates).
+//
+// One call = four launches on the caller's stream:
+//   validate   per-sequence state check (n_rows == pos/ratio, capacity) -> flags
+//   project    kv | gate rows of every new token (model dtype) -> workspace
+//   pool_emit  one block per completed window: softmax-weighted sum per
+//              channel, RMSNorm, RoPE, store the row
+//   finish     rewrite the frontier ring with the newest tokens, advance n_rows
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T) {
+  CompressWs w;
+  w.flags = c.take<int32_t>(B);
+  w.proj = c.take<char>((size_t)B * T * 2 * L.lanes * d * esize(L.dtype));
+  return w;
+}
+
+__global__ void k_compress_validate(const int32_t* __restrict__ pos, const int32_t* __restrict__ n_rows, int B,
+                                    int T, int ratio, int cap, int32_t* __restrict__ flags, int32_t* err) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int p0 = pos[b];
+  int ok = 1;
+  if (p0 < 0 || n_rows[b] != p0 / ratio) {
+    atomicOr(err, CSA_DEV_STATE);
+    ok = 0;
+  } else if ((long long)(p0 + (long long)T) / ratio - 1 >= cap) {
+    atomicOr(err, CSA_DEV_CAPACITY);
+    ok = 0;
+  }
+  flags[b] = ok;
+}
+
+// out[tok][o] = sum_k W[o][k] x[tok][k]; W = [wkv ; wgate] (2*Ld rows).  One warp
+// per output feature and NTOK tokens; fp32 accumulation in a fixed order.
+template <typename T, int NTOK>
+__global__ void __launch_bounds__(256) k_project_simt(const T* __restrict__ x, const T* __restrict__ wkv,
+                                                      const T* __restrict__ wg, int ntok, int X, int Ld,
+                                                      T* __restrict__ out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o = blockIdx.x * 8 + warp;
+  if (o >= 2 * Ld) return;
+  const int t0 = blockIdx.y * NTOK;
+  const T* w = (o < Ld) ? wkv + (size_t)o * X : wg + (size_t)(o - Ld) * X;
+  float acc[NTOK];
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) acc[t] = 0.f;
+  for (int k = lane * 8; k < X; k += 256) {
+    float wv[8];
+    load8_nc(w + k, wv);
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      if (t0 + t < ntok) {
+        float xv[8];
+        load8_nc(x + (size_t)(t0 + t) * X + k, xv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[t] = fmaf(wv[e], xv[e], acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) {
+    float v = warp_sum(acc[t]);
+    if (lane == 0 && t0 + t < ntok) out[(size_t)(t0 + t) * 2 * Ld + o] = from_f<T>(v);
+  }
+}
+
+// One block per (completed window i of this call, sequence b).
+template <typename T>
+__global__ void __launch_bounds__(256) k_pool_emit(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos,
+                                                   int T_, int ratio, int lanes, int d, int R, int F,
+                                                   const T* __restrict__ frontier, const T* __restrict__ proj,
+                                                   const float* __restrict__ ape, const float* __restrict__ norm_w,
+                                                   float eps, const float* __restrict__ inv_freq,
+                                                   T* __restrict__ pool, int cap) {
+  extern __shared__ float sm_pool[];  // [d] pooled values, then [d] normed values, + 32 reduction slots
+  float* u = sm_pool;
+  float* y = sm_pool + d;
+  float* red = sm_pool + 2 * d;
+  const int b = blockIdx.y;
+  if (!flags[b]) return;
+  const int p0 = pos[b];
+  const int first = p0 + (ratio - 1 - p0 % ratio);  // first token completing a window
+  const int p = first + blockIdx.x * ratio;
+  if (p >= p0 + T_) return;
+  const int j = (p + 1) / ratio - 1;
+  const int Ld = lanes * d;
+  const size_t rowlen = 2 * (size_t)Ld;
+  const T* fr = frontier + (size_t)b * F * rowlen;
+  const T* pj = proj + (size_t)b * T_ * rowlen;
+
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    // entries (token t, lane l): ratio 4 -> window j-1 via lane 0 (if j >= 1) and window j via lane 1
+    float m = -INFINITY;
+    const int t_lo = (lanes == 2) ? max(0, (j - 1) * ratio) : j * ratio;
+    const int t_hi = (j + 1) * ratio;
+    for (int t = t_lo; t < t_hi; ++t) {
+      const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
+      const T* row = (t < p0) ? fr + (size_t)(t % F) * rowlen : pj + (size_t)(t - p0) * rowlen;
+      float s = to_f(row[Ld + l * d + c]) + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
+      m = fmaxf(m, s);
+    }
+    float num = 0.f, den = 0.f;
+    for (int t = t_lo; t < t_hi; ++t) {
+      const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
+      const T* row = (t < p0) ? fr + (size_t)(t % F) * rowlen : pj + (size_t)(t - p0) * rowlen;
+      float s = to_f(row[Ld + l * d + c]) + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
+      float e = expf(s - m);
+      den += e;
+      num = fmaf(e, to_f(row[l * d + c]), num);
+    }
+    float uc = rnd<T>(num / den);
+    u[c] = uc;
+    ss = fmaf(uc, uc, ss);
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) y[c] = rnd<T>(u[c] * inv * __ldg(norm_w + c));
+  __syncthreads();
+  T* dst = pool + ((size_t)b * cap + j) * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float v = y[c];
+    if (c >= d - R) {
+      const int i = (c - (d - R)) >> 1;
+      float cs, sn;
+      rope_cs(j * ratio, inv_freq, i, &cs, &sn);
+      const float a = y[d - R + 2 * i], bb = y[d - R + 2 * i + 1];
+      v = ((c - (d - R)) & 1) ? fmaf(a, sn, bb * cs) : fmaf(a, cs, -bb * sn);
+    }
+    dst[c] = from_f<T>(v);
+  }
+}
+
+// Rewrite the frontier slots of the newest min(T, F) tokens; block (0, b) advances n_rows.
+template <typename T>
+__global__ void k_compress_finish(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos, int T_,
+                                  int ratio, int F, int rowlen, const T* __restrict__ proj, T* __restrict__ frontier,
+                                  int32_t* __restrict__ n_rows) {
+  const int b = blockIdx.y;
+  if (!flags[b]) return;
+  const int p0 = pos[b];
+  const int keep = min(T_, F);
+  const int t = p0 + T_ - keep + blockIdx.x;
+  const T* src = proj + ((size_t)b * T_ + (t - p0)) * rowlen;
+  T* dst = frontier + ((size_t)b * F + (t % F)) * rowlen;
+  for (int e = threadIdx.x * 8; e < rowlen; e += blockDim.x * 8) copy8<T>(dst + e, src + e);
+  if (blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
+}
+
+template <typename T>
+static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const void* x, int B, int T_,
+                              const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
+                              const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s) {
+  const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
+  k_compress_validate<<<(B + 127) / 128, 128, 0, s>>>(pos, n_rows, B, T_, L.ratio, cap, ws.flags, err); count_launches(1);
+  const int ntok = B * T_;
+  dim3 gp((2 * Ld + 7) / 8, (ntok + 7) / 8);
+  k_project_simt<T, 8><<<gp, 256, 0, s>>>(static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
+                                           static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
+                                           static_cast<T*>(ws.proj)); count_launches(1);
+  const int maxwin = (T_ + L.ratio - 1) / L.ratio;
+  dim3 ge(maxwin, B);
+  size_t smem = (2 * (size_t)d + 32) * sizeof(float);
+  k_pool_emit<T><<<ge, 256, smem, s>>>(ws.flags, pos, T_, L.ratio, L.lanes, d, L.R, L.F,
+                                       static_cast<const T*>(frontier), static_cast<const T*>(ws.proj), comp.ape,
+                                       comp.norm_w, L.eps, inv_freq, static_cast<T*>(pool), cap); count_launches(1);
+  dim3 gf(min(T_, L.F), B);
+  k_compress_finish<T><<<gf, 128, 0, s>>>(ws.flags, pos, T_, L.ratio, L.F, rowlen, static_cast<const T*>(ws.proj),
+                                          static_cast<T*>(frontier), n_rows); count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,
+                            const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
+                            const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s) {
+  if (L.dtype == CSA_BF16)
+    return compress_t<__nv_bfloat16>(L, comp, x, B, T, pos, frontier, pool, cap, n_rows, inv_freq, ws, err, s);
+  return compress_t<float>(L, comp, x, B, T, pos, frontier, pool, cap, n_rows, inv_freq, ws, err, s);
+}
+
+}  // namespace csa

@@ -1,0 +1,248 @@
+// Indexer: ReLU-weighted multi-head scores against the index-key pool and an
+// exact top-k with lower-row tie-break.
+//
+// Definition: "feat: add DeepSeek-V4 (Pro/Flash) model support" (mlx-lm #1189),
+// stepnoy's patch point 3 and aidiffuser's indexer: queries roped at their
+// absolute position, raw head weights with Di^-1/2 * Hi^-1/2 folded in, no
+// sigmoid, ReLU on the logits, sum over heads; OmarB97's visibility rule (row j
+// visible to p iff (j+1)*ratio <= p+1); the selection keeps index_topk rows.
+//
+// Launches: rope the index queries -> scores (one block per query and 64-row
+// tile) -> radix select per query (one block per query).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap) {
+  IndexWs w;
+  w.qr = c.take<float>((size_t)Q * L.Hi * L.Di);
+  w.scores = c.take<float>((size_t)Q * cap);
+  return w;
+}
+
+__device__ __forceinline__ int query_pos(const int32_t* pos, int pos0, int q) { return pos ? pos[q] : pos0 + q; }
+__device__ __forceinline__ int query_seq(const int32_t* pos, int q) { return pos ? q : 0; }
+
+// qr[q][h][:] = RoPE(iq[q][h][:], p_q) rounded to the model dtype, held as fp32.
+template <typename T>
+__global__ void k_rope_iq(const T* __restrict__ iq, int Hi, int Di, int R, const int32_t* __restrict__ pos, int pos0,
+                          const float* __restrict__ inv_freq, float* __restrict__ qr) {
+  const int q = blockIdx.x;
+  const int p = query_pos(pos, pos0, q);
+  for (int e = threadIdx.x; e < Hi * Di; e += blockDim.x) {
+    const int c = e % Di;
+    const T* row = iq + ((size_t)q * Hi + e / Di) * Di;
+    float v = to_f(row[c]);
+    if (c >= Di - R) {
+      const int i = (c - (Di - R)) >> 1;
+      float cs, sn;
+      rope_cs(p, inv_freq, i, &cs, &sn);
+      const float a = to_f(row[Di - R + 2 * i]), b = to_f(row[Di - R + 2 * i + 1]);
+      v = ((c - (Di - R)) & 1) ? fmaf(a, sn, b * cs) : fmaf(a, cs, -b * sn);
+    }
+    qr[(size_t)q * Hi * Di + e] = rnd<T>(v);
+  }
+}
+
+// scores[q][j] for the 64 rows j of tile blockIdx.x.  Thread (hq, kq) owns heads
+// 4hq..4hq+3 of the current 64-head group and rows kq + 16*kk (kk < 4).
+template <typename T>
+__global__ void __launch_bounds__(256) k_index_scores(const float* __restrict__ qr, const T* __restrict__ iw,
+                                                      int Hi, int Di, const T* __restrict__ ikeys, int cap,
+                                                      const int32_t* __restrict__ n_rows,
+                                                      const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
+                                                      float wscale, float* __restrict__ scores) {
+  extern __shared__ float sm_idx[];
+  const int q = blockIdx.y, bseq = query_seq(pos, q);
+  const int p = query_pos(pos, pos0, q);
+  const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
+  const int j0 = blockIdx.x * 64;
+  if (nvis <= topk || j0 >= nvis) return;
+  const int KS = Di + 4;             // padded key row (floats)
+  float* ks = sm_idx;                // [64][KS]
+  float* qs = ks + 64 * KS;          // [64][Di] one head group
+  float* part = qs + 64 * Di;        // [16][64]
+  float* wts = part + 16 * 64;       // [64]
+  const int tid = threadIdx.x, hq = tid >> 4, kq = tid & 15;
+  const T* kbase = ikeys + ((size_t)bseq * cap + j0) * Di;
+  const int nk = min(64, nvis - j0);
+  for (int e = tid * 8; e < 64 * Di; e += 256 * 8) {
+    const int r = e / Di, c = e % Di;
+    float v[8];
+    if (r < nk) load8_nc(kbase + (size_t)r * Di + c, v);
+    else
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < 8; ++i) ks[r * KS + c + i] = v[i];
+  }
+  float tot[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int h0 = 0; h0 < Hi; h0 += 64) {
+    const int hn = min(64, Hi - h0);
+    __syncthreads();
+    for (int e = tid; e < 64 * Di; e += 256) {
+      const int h = e / Di;
+      qs[e] = (h < hn) ? qr[((size_t)q * Hi + h0 + h) * Di + (e % Di)] : 0.f;
+    }
+    if (tid < 64) wts[tid] = (tid < hn) ? to_f(iw[(size_t)q * Hi + h0 + tid]) * wscale : 0.f;
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[a][k] = 0.f;
+    for (int c = 0; c < Di; c += 4) {
+      float4 qv[4], kv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) qv[a] = *reinterpret_cast<const float4*>(qs + (hq * 4 + a) * Di + c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) kv[k] = *reinterpret_cast<const float4*>(ks + (kq + 16 * k) * KS + c);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[a][k] = fmaf(qv[a].x, kv[k].x, acc[a][k]);
+          acc[a][k] = fmaf(qv[a].y, kv[k].y, acc[a][k]);
+          acc[a][k] = fmaf(qv[a].z, kv[k].z, acc[a][k]);
+          acc[a][k] = fmaf(qv[a].w, kv[k].w, acc[a][k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int a = 0; a < 4; ++a) tot[k] = fmaf(wts[hq * 4 + a], fmaxf(acc[a][k], 0.f), tot[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) part[hq * 64 + kq + 16 * k] = tot[k];
+  __syncthreads();
+  if (tid < nk) {
+    float s = 0.f;
+    for (int i = 0; i < 16; ++i) s += part[i * 64 + tid];
+    scores[(size_t)q * cap + j0 + tid] = s;
+  }
+}
+
+// Exclusive prefix count of `flag` over the block (blockDim.x == 1024) plus the block total.
+__device__ __forceinline__ int block_excl_count(int flag, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, flag);
+  const int inwarp = __popc(bal & ((1u << lane) - 1u));
+  __syncthreads();
+  if (lane == 0) warp_tot[wid] = __popc(bal);
+  __syncthreads();
+  if (wid == 0) {
+    int v = warp_tot[lane];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    warp_tot[lane] = incl - v;
+    if (lane == 31) *total = incl;
+  }
+  __syncthreads();
+  return warp_tot[wid] + inwarp;
+}
+
+// Exact top-k of scores[q][0 .. nvis) by (score desc, row asc), written in
+// ascending row order.  Radix select of the k-th largest order key over four
+// 8-bit digits, then one ascending pass that keeps every row above the
+// threshold and the lowest-indexed rows equal to it.
+__global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int cap,
+                                               const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
+                                               int pos0, int ratio, int topk, int32_t* __restrict__ sel,
+                                               int32_t* __restrict__ n_sel) {
+  __shared__ int hist[256];
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int p = query_pos(pos, pos0, q);
+  const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
+  int32_t* out = sel + (size_t)q * topk;
+  if (nvis <= topk) {
+    for (int i = threadIdx.x; i < topk; i += blockDim.x) out[i] = (i < nvis) ? i : -1;
+    if (threadIdx.x == 0) n_sel[q] = max(nvis, 0);
+    return;
+  }
+  const float* sc = scores + (size_t)q * cap;
+  uint32_t prefix = 0, mask = 0;
+  int need = topk;  // rank (1-based, from the top) of the threshold among keys matching prefix
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
+      const uint32_t u = ord_key(sc[j]);
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int c = 0, bkt = 0;
+      for (bkt = 255; bkt >= 0; --bkt) {
+        if (c + hist[bkt] >= need) break;
+        c += hist[bkt];
+      }
+      s_need = need - c;
+      s_prefix = prefix | ((uint32_t)bkt << shift);
+    }
+    __syncthreads();
+    need = s_need;
+    prefix = s_prefix;
+    mask |= 255u << shift;
+  }
+  // prefix = order key of the k-th largest score; take every key above it and
+  // the first `need` keys equal to it (ties to the lower row).
+  int eq_base = 0, out_base = 0;
+  for (int j0 = 0; j0 < nvis; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    uint32_t u = (j < nvis) ? ord_key(sc[j]) : 0u;
+    const int eq = (j < nvis) && (u == prefix);
+    const int gt = (j < nvis) && (u > prefix);
+    const int eq_rank = eq_base + block_excl_count(eq, warp_tot, &s_total);
+    const int eq_tot = s_total;
+    const int take = gt || (eq && eq_rank < need);
+    const int slot = out_base + block_excl_count(take, warp_tot, &s_total);
+    const int take_tot = s_total;
+    if (take && slot < topk) out[slot] = j;
+    eq_base += eq_tot;
+    out_base += take_tot;
+  }
+  for (int i = out_base + threadIdx.x; i < topk; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) n_sel[q] = min(out_base, topk);
+}
+
+template <typename T>
+static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
+                           const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq, int32_t* sel,
+                           int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s) {
+  if (tc_index_supported(L)) {
+    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q : 1, cap, n_rows, pos, pos0, inv_freq, ws.qr,
+                                           ws.scores, err, s);
+    if (e != cudaSuccess) return e;
+    k_topk<<<Q, 1024, 0, s>>>(ws.scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel); count_launches(1);
+    return cudaGetLastError();
+  }
+  k_rope_iq<T><<<Q, 256, 0, s>>>(static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, inv_freq, ws.qr); count_launches(1);
+  const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
+  dim3 g((cap + 63) / 64, Q);
+  size_t smem = (64 * (size_t)(L.Di + 4) + 64 * (size_t)L.Di + 16 * 64 + 64) * sizeof(float);
+  k_index_scores<T><<<g, 256, smem, s>>>(ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
+                                         cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores); count_launches(1);
+  k_topk<<<Q, 1024, 0, s>>>(ws.scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel); count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
+                              const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq,
+                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s) {
+  const int smax = 227 * 1024;
+  if (L.dtype == CSA_BF16) {
+    cudaFuncSetAttribute(k_index_scores<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+    return index_t<__nv_bfloat16>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, inv_freq, sel, n_sel, ws, err, s);
+  }
+  cudaFuncSetAttribute(k_index_scores<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+  return index_t<float>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, inv_freq, sel, n_sel, ws, err, s);
+}
+
+}  // namespace csa

@@ -1,0 +1,93 @@
+// Internal interface between the C-ABI entry points (api.cu) and the kernel
+// translation units.  Host-side only declarations; no torch types anywhere.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+// Validated layer dimensions.
+struct Dims {
+  int dtype, H, D, R, W, ratio, Hi, Di, topk, X;
+  float scale, eps;
+  int lanes;  // 2 when ratio == 4 (overlapping windows), else 1
+  int F;      // frontier ring length in tokens
+  bool has_indexer() const { return ratio == 4; }
+};
+
+// Carves 256-byte aligned sub-buffers out of the caller's workspace; with a
+// null base it only measures.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename E> E* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    E* p = base ? reinterpret_cast<E*>(base + off) : nullptr;
+    off += n * sizeof(E);
+    return p;
+  }
+};
+
+inline size_t esize(int dtype) { return dtype == CSA_BF16 ? 2 : 4; }
+
+// Number of kernels this library has enqueued in this process (diagnostics).
+void count_launches(int n);
+
+// ---- compress.cu
+struct CompressWs {
+  int32_t* flags;  // [B] 1 = sequence valid for this call
+  void* proj;      // [B*T, 2*L*d] model dtype: kv | gate of every new token
+};
+CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T);
+cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,
+                            const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
+                            const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s);
+
+// ---- indexer.cu
+struct IndexWs {
+  float* qr;      // [Q, Hi, Di] roped index queries (model-dtype values held as fp32)
+  float* scores;  // [Q, cap]
+};
+IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap);
+// Scores and top-k for Q queries.  Query q belongs to sequence bseq(q) = (pos != null ? q : 0)
+// at position (pos != null ? pos[q] : pos0 + q); its visible rows are
+// min(n_rows[bseq], (p+1)/ratio).  sel [Q, topk], n_sel [Q].
+cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
+                              const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq,
+                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s);
+
+// ---- tc_indexer.cu (tensor-core scores; bf16, Hi = 64, Di = 128)
+bool tc_index_supported(const Dims& L);
+size_t tc_index_ws(const Dims& L, int Q);
+// scores[q][j] for every q whose visible rows exceed topk; keys of query q are
+// ikeys[pos ? q : 0]; ws needs tc_index_ws() bytes.
+cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
+                                   int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
+                                   const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s);
+
+// ---- attend.cu
+struct AttendWs {
+  void* qr;        // [Q, H, D] roped queries, model dtype
+  void* kvr;       // [T, D] roped chunk kv (prefill only)
+  float* part_ml;  // [Q, S, H, 2] split partial (max, sum)
+  float* part_acc; // [Q, S, H, D] split partial accumulators
+  int S;           // splits per query
+};
+int attend_splits(const Dims& L, bool prefill, bool all_rows, int cap);
+AttendWs carve_attend(Carver& c, const Dims& L, int Q, int S, int T);
+// Decode: Q = B sequences, positions pos[b], window rings window[b].
+cudaError_t launch_attend_decode(const Dims& L, const void* q, const void* kv_new, const float* sink, int B,
+                                 void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                                 const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,
+                                 const AttendWs& ws, int32_t* err, cudaStream_t s);
+// Prefill: T queries of one sequence at pos0 + t.  sel/n_sel from the indexer (or null: all visible rows).
+cudaError_t launch_attend_prefill(const Dims& L, const void* q, const void* kv_new, const float* sink, int T,
+                                  int pos0, void* window, const void* pool, int cap, const int32_t* n_rows,
+                                  const int32_t* sel, const int32_t* n_sel, const float* inv_freq, void* out,
+                                  const AttendWs& ws, int32_t* err, cudaStream_t s);
+
+}  // namespace csa

@@ -1,0 +1,229 @@
+/*
+ * csa.h — C ABI of one layer of DeepSeek-V4 Compressed Sparse Attention (CSA)
+ * on a single GB300 (sm_103a).
+ *
+ * The layer (DeepSeek-V4-Flash shapes) has four parts, each a call here:
+ *   csa_compress_append      gated-pooling compressor: projects tokens, pools
+ *                            ratio-4 overlapping or ratio-128 windows, RMSNorm,
+ *                            RoPE at the window start, appends rows to a pool.
+ *   csa_index_topk           indexer: ReLU-weighted multi-head scores of the
+ *                            query against the index-key pool, exact top-k.
+ *   csa_attend_decode        MQA-shaped attention of H heads over one shared
+ *                            latent (K = V): selected pool rows + sliding
+ *                            window, sink logits, split-K partial softmax and
+ *                            merge, inverse RoPE on the output.
+ *   csa_attend_prefill_chunk the same for a chunk of T queries of one
+ *                            sequence, each with its own causal top-k.
+ *
+ * Definitions follow the pages the method is described on:
+ *   [MTPLX#216]  "DeepSeek-V4-Flash: native deepseek_v4 AR backend"
+ *   [mlx-lm#1189] "feat: add DeepSeek-V4 (Pro/Flash) model support"
+ *   [v41-mlx]    "deepseek-v41-mlx" README
+ *
+ * Conventions for every call
+ *   - Every tensor argument is a DEVICE pointer owned by the caller, dense,
+ *     row-major, 16-byte aligned.  The library never allocates or frees device
+ *     memory and keeps no state between calls.  Scratch memory comes from the
+ *     caller through (ws, ws_bytes); csa_workspace_size() gives the size.
+ *   - Storage dtype (layer->dtype): CSA_BF16 or CSA_F32 for activations,
+ *     weights, pools, windows and outputs ("model dtype").  APE, norm weights,
+ *     sink logits and the RoPE table are always fp32.  Arithmetic is fp32.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  No call synchronises or reads device memory
+ *     on the host, so calls can be captured in a CUDA graph.
+ *   - Errors found on the host are returned synchronously, before anything is
+ *     enqueued (fail closed: nothing is modified).  Errors that depend on
+ *     device-resident values (positions, row counts, indices) are OR-ed into
+ *     the caller's device error word `err` (CSA_DEV_* bits) and the offending
+ *     sequence / row is skipped; no call traps or asserts on the device.
+ *   - RoPE: rope dims are the LAST R dims of a row, rotated as interleaved
+ *     pairs (D-R+2i, D-R+2i+1) by theta_i = (float)p * inv_freq[i] (one fp32
+ *     multiply).  inv_freq is a device fp32 table of R/2 entries, so the
+ *     caller chooses plain or YaRN-scaled frequencies ([mlx-lm#1189], OmarB97
+ *     "RoPE regime is per layer kind": compress layers use base 160000).
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_ARG = 1,         /* null / misaligned pointer, inconsistent or out-of-range sizes */
+  CSA_ERR_UNSUPPORTED = 2, /* valid arguments with no kernel for them (see each call) */
+  CSA_ERR_CUDA = 3,        /* a kernel launch failed (cudaGetLastError after enqueue) */
+  CSA_ERR_WORKSPACE = 4    /* ws_bytes smaller than csa_workspace_size() */
+} csa_status;
+
+enum { CSA_F32 = 0, CSA_BF16 = 1 };
+
+/* bits of the device error word */
+enum {
+  CSA_DEV_CAPACITY = 1, /* a compress call would emit a row at index >= cap: sequence skipped */
+  CSA_DEV_STATE = 2,    /* n_rows[b] != floor(pos[b] / ratio) or pos[b] < 0: sequence skipped */
+  CSA_DEV_RANGE = 4     /* a selected row index outside [0, n_rows[b]): that row is skipped */
+};
+
+/* operation ids for csa_workspace_size */
+enum { CSA_OP_COMPRESS = 0, CSA_OP_INDEX_TOPK = 1, CSA_OP_ATTEND_DECODE = 2, CSA_OP_ATTEND_PREFILL = 3 };
+
+/* One CSA layer.
+ *   H query heads over one latent of D dims (K = V), rope on the last R dims;
+ *   W-token sliding window; compress `ratio` (4: overlapping windows of 8
+ *   tokens through two lanes, with the indexer; any other ratio r: one lane,
+ *   non-overlapping windows of r tokens, no indexer); indexer Hi heads of Di
+ *   dims keeping `topk` rows; hidden size X.
+ *   scale: attention logit scale (the pages' kernels use D^-1/2; 0 selects it).
+ *   rms_eps: RMSNorm epsilon of the compressed rows. */
+typedef struct {
+  int dtype;
+  int H, D, R, W, ratio, Hi, Di, topk, X;
+  float scale;
+  float rms_eps;
+} csa_layer;
+
+/* One compressor (the attention pool's, d = D, or the index pool's, d = Di).
+ * L = 2 lanes when ratio == 4, else 1.
+ *   wkv, wgate [L*d, X] model dtype (out-features x in-features);
+ *   ape  [ratio, L*d] fp32: absolute position embedding added to the gates;
+ *   norm_w [d] fp32: RMSNorm weight.
+ * Lane 0 (first d outputs) pools the previous window, lane 1 the current one
+ * ([mlx-lm#1189], Thump604: "ratio-4 overlap compressor shapes ... ape
+ * (4, 1024) and wkv/wgate (1024, 4096)"). */
+typedef struct {
+  const void* wkv;
+  const void* wgate;
+  const float* ape;
+  const float* norm_w;
+  int d;
+} csa_compressor;
+
+/* Frontier ring length in tokens: 2*ratio when ratio == 4, else ratio. */
+int csa_frontier_slots(int ratio);
+
+/* Bytes of scratch memory `op` needs for batch B (T: tokens per sequence for
+ * CSA_OP_COMPRESS, chunk length for CSA_OP_ATTEND_PREFILL, else ignored) and
+ * pool capacity `cap` rows.  Returns CSA_ERR_ARG on bad dimensions. */
+csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int cap, size_t* bytes);
+
+/* csa_compress_append — append T tokens per sequence to one compressed pool.
+ *
+ * Definition ([MTPLX#216] "What V4 adds": learned gated pooling over
+ * overlapping ratio-4 or non-overlapping ratio-128 windows, maintained
+ * incrementally by prefill and decode alike; [mlx-lm#1189] OmarB97 "Compressed
+ * pool rows must be roped at birth", stepnoy "Fix" 3: the chunk tail is carried
+ * and the absolute position accumulates; [MTPLX#216] "Decode path": the row is
+ * pooled in fp32 and cast back before the norm):
+ *   for token p = pos[b] + i:  kv_p = Wkv x_p,  g_p = Wgate x_p  (model dtype)
+ *   when p = (j+1)*ratio - 1 completes window j:
+ *     entries: ratio 4 -> tokens of window j-1 via lane 0 (absent for j = 0)
+ *              and tokens of window j via lane 1; otherwise window j's tokens;
+ *     per channel c: u_c = sum_e softmax_e(g_e,c + ape[t_e mod ratio][c]) kv_e,c
+ *     row j = RoPE(RMSNorm(u), j*ratio), rounded to the model dtype at each step,
+ *     written to pool[b][j]; n_rows[b] = j + 1.
+ * Arguments
+ *   x        [B, T, X]             model dtype, tokens at pos[b] .. pos[b]+T-1
+ *   pos      [B] int32 (device)    position of x[b][0]; the library never writes it
+ *   frontier [B, F, 2*L*d]         model dtype, F = csa_frontier_slots(ratio): ring of the
+ *                                  projected (kv | gate) rows of the last F tokens, slot t mod F;
+ *                                  read for tokens before pos[b], rewritten for the last tokens
+ *   pool     [B, cap, d]           model dtype, rows [0, n_rows[b]) valid
+ *   n_rows   [B] int32 (device)    in/out; must equal floor(pos[b] / ratio) on entry
+ *   inv_freq [R/2] fp32
+ *   err      int32 (device)        error word (CSA_DEV_STATE, CSA_DEV_CAPACITY); a sequence
+ *                                  that would fail is left entirely unchanged
+ * Call it once for the attention pool and, on ratio-4 layers, once for the
+ * index pool, with the same pos and the same n_rows values. */
+csa_status csa_compress_append(const csa_layer* layer, const csa_compressor* comp, const void* x, int B, int T,
+                               const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
+                               const float* inv_freq, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/* csa_index_topk — the indexer for one decode query per sequence.
+ *
+ * Definition ([mlx-lm#1189] stepnoy's patch point 3 and aidiffuser's indexer:
+ * raw head weights with the scale folded in, no sigmoid, ReLU on the logits,
+ * sum over heads; the index pool accumulates in the cache so its row space is
+ * the attention pool's; OmarB97: row j is visible to position p iff
+ * (j+1)*ratio <= p+1):
+ *   n_vis = min(n_rows[b], floor((pos[b]+1)/ratio))
+ *   q_h   = RoPE(iq[b][h], pos[b])  (model dtype)
+ *   s_j   = sum_h iw[b][h] * Di^-1/2 * Hi^-1/2 * max(q_h . ikeys[b][j], 0),  j < n_vis
+ *   if n_vis <= topk: sel = 0 .. n_vis-1; else the topk largest s_j, ties to
+ *   the lower j.  sel is written in ascending row order, padded with -1.
+ * Arguments
+ *   iq [B, Hi, Di], iw [B, Hi]   model dtype
+ *   ikeys [B, cap, Di]           model dtype index-key pool
+ *   n_rows, pos [B] int32 (device)
+ *   sel [B, topk] int32, n_sel [B] int32 (device outputs)
+ * Requires ratio == 4 (the layers that carry an indexer) and topk <= 4096. */
+csa_status csa_index_topk(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys, int cap,
+                          const int32_t* n_rows, const int32_t* pos, const float* inv_freq, int32_t* sel,
+                          int32_t* n_sel, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/* csa_attend_decode — one decode query per sequence.
+ *
+ * Definition ([MTPLX#216] "What V4 adds": 64 query heads over one 512-dim
+ * latent with per-head sink logits and a 128-token sliding window; [v41-mlx]:
+ * the inverse rope on the attention output, sinks in the softmax denominator
+ * only; [mlx-lm#1189] stepnoy: decode gathers its own top-k rows so the softmax
+ * is not diluted over the whole pool):
+ *   window[b][p mod W] = RoPE(kv_new[b], p)            p = pos[b]
+ *   keys  = pool[b][sel[b][0 .. n_sel[b])]  (sel == NULL: rows 0 .. n_vis-1)
+ *           ++ window tokens t in [max(0, p-W+1), p]
+ *   l_ht  = scale * RoPE(q[b][h], p) . key_t
+ *   o_h   = sum_t e^{l_ht} key_t / (e^{sink[h]} + sum_t e^{l_ht})
+ *   out[b][h] = RoPE^-1(o_h, p)   (model dtype before and after the rotation)
+ * computed as split-K partial softmaxes (m, l, acc) merged in a second pass.
+ * Arguments
+ *   q [B, H, D], kv_new [B, D]   model dtype
+ *   sink [H] fp32
+ *   window [B, W, D]             model dtype ring, slot t mod W (written at slot p mod W)
+ *   pool [B, cap, D]             model dtype
+ *   n_rows, n_sel, pos [B] int32 (device); sel [B, topk] int32 or NULL
+ *   out [B, H, D]                model dtype
+ * A selected index outside [0, n_rows[b]) raises CSA_DEV_RANGE and is skipped. */
+csa_status csa_attend_decode(const csa_layer* layer, const void* q, const void* kv_new, const float* sink, int B,
+                             void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                             const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out, void* ws,
+                             size_t ws_bytes, int32_t* err, void* stream);
+
+/* csa_attend_prefill_chunk — T queries of one sequence at positions pos0 .. pos0+T-1.
+ *
+ * The compressors must already have consumed the chunk (n_rows counts the rows
+ * emitted up to its end).  Each query p attends the pool rows visible to it,
+ * reduced by its OWN top-k when the layer has an indexer and more than topk
+ * rows are visible ([mlx-lm#1189] stepnoy's patch point 3: per-query top-k
+ * AND-ed with the visibility mask; aidiffuser: build the membership from the
+ * index list rather than a dense compare), plus its window tokens: ring
+ * entries for tokens before pos0, the chunk's own kv_new roped at their
+ * positions otherwise.  After the chunk the window ring holds its last W
+ * tokens.  Same formulas as csa_attend_decode / csa_index_topk per query.
+ * Arguments
+ *   q [T, H, D], kv_new [T, D], iq [T, Hi, Di], iw [T, Hi]   model dtype (iq, iw,
+ *                                  ikeys may be NULL when ratio != 4)
+ *   sink [H] fp32; pos0 host int; window [W, D]; pool [cap, D]; ikeys [cap, Di]
+ *   n_rows int32 (device, one value)
+ *   out [T, H, D]; sel_out [T, topk] int32 or NULL (the selected rows, -1 padded)
+ * Requires 1 <= T <= 16384 and ratio == 4 or no indexer use. */
+csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const void* kv_new, const void* iq,
+                                    const void* iw, const float* sink, int T, int32_t pos0, void* window,
+                                    const void* pool, const void* ikeys, int cap, const int32_t* n_rows,
+                                    const float* inv_freq, void* out, int32_t* sel_out, void* ws, size_t ws_bytes,
+                                    int32_t* err, void* stream);
+
+/* Number of kernels this library has enqueued in this process (all calls,
+ * all devices).  Diagnostic only: lets a caller count the launches of a region. */
+unsigned long long csa_kernel_launches(void);
+
+/* Human-readable name of a status code. */
+const char* csa_status_string(csa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

@@ -246,7 +246,7 @@ def compressor_row(layer: Layer, comp: Compressor, j: int, tok: dict, inv_freq) 
     return finalize_row(layer, comp, u, j, inv_freq)
 
 
-def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_rows, inv_freq):
+def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_rows, inv_freq, proj=None):
     """Append T tokens per sequence to one compressed pool (attention or index).
 
     x [B,T,X]; pos [B] position of x[:,0]; frontier [B,F,2*L*d] ring of the
@@ -254,7 +254,10 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
     [B,cap,d]; n_rows [B].  Row j is emitted when token (j+1)*ratio-1 arrives
     (R2), so rows built one token at a time equal rows built from a chunk
     ([mlx-lm#1189] stepnoy "Fix" 3: the chunk tail is buffered and replayed, the
-    absolute position accumulates).  Returns (frontier, pool, n_rows, err).
+    absolute position accumulates).  ``proj`` = (kv [B,T,L*d], g [B,T,L*d])
+    optionally supplies the stored projections of the new tokens instead of
+    computing them from x (so pooling can be checked on given inputs).
+    Returns (frontier, pool, n_rows, err).
     """
     x = np.asarray(x, dtype=np.float64)
     frontier = np.array(frontier, dtype=np.float64)
@@ -263,7 +266,10 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
     B, T, _ = x.shape
     r, F, cap = layer.ratio, layer.frontier_slots, pool.shape[1]
     Ld = layer.lanes * comp.d
-    kv_all, g_all = project(layer, comp, x)
+    if proj is None:
+        kv_all, g_all = project(layer, comp, x)
+    else:
+        kv_all, g_all = (np.asarray(a, dtype=np.float64) for a in proj)
     err = 0
     for b in range(B):
         p0 = int(pos[b])

@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library loads, exports every function include/csa.h declares, and rejects
+bad arguments on the host (synchronously, before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import deepseek_v4_compressed_csa_gb300 as csa
+from deepseek_v4_compressed_csa_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from deepseek_v4_compressed_csa_gb300 import build
+        build.build()
+    return csa.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:[A-Za-z_][A-Za-z0-9_]*[\s*]+)+(csa_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(declared) >= {"csa_compress_append", "csa_index_topk", "csa_attend_decode",
+                             "csa_attend_prefill_chunk", "csa_workspace_size"}
+    for name in declared:
+        assert hasattr(lib, name), f"libcsa.so does not export {name}"
+    assert set(B.EXPORTS) <= set(declared)
+
+
+def _layer(**kw):
+    base = dict(dtype=B.CSA_BF16, H=64, D=512, R=64, W=128, ratio=4, Hi=64, Di=128, topk=512, X=4096, scale=0.0,
+                rms_eps=1e-6)
+    base.update(kw)
+    return B._Layer(*[base[f] for f, _ in B._Layer._fields_])
+
+
+def test_frontier_slots_and_status_strings(lib):
+    assert lib.csa_frontier_slots(4) == 8
+    assert lib.csa_frontier_slots(128) == 128
+    assert lib.csa_status_string(0) == b"CSA_OK"
+    assert b"WORKSPACE" in lib.csa_status_string(4)
+
+
+def test_workspace_sizes(lib):
+    L = _layer()
+    n = ctypes.c_size_t()
+    sizes = {}
+    for op in (B.OP_COMPRESS, B.OP_INDEX_TOPK, B.OP_ATTEND_DECODE, B.OP_ATTEND_PREFILL):
+        assert lib.csa_workspace_size(ctypes.byref(L), op, 32, 4, 8400, ctypes.byref(n)) == 0
+        sizes[op] = n.value
+        assert n.value > 0
+    assert lib.csa_workspace_size(ctypes.byref(L), B.OP_INDEX_TOPK, 64, 1, 8400, ctypes.byref(n)) == 0
+    assert n.value > sizes[B.OP_INDEX_TOPK]
+    assert lib.csa_workspace_size(ctypes.byref(L), 99, 1, 1, 1, ctypes.byref(n)) == B.CSA_ERR_ARG
+    assert lib.csa_workspace_size(ctypes.byref(_layer(D=500)), 0, 1, 1, 1, ctypes.byref(n)) == B.CSA_ERR_ARG
+
+
+FAKE = 0x7f0000000000  # never dereferenced: every call below fails validation first
+
+
+def _compress(lib, L, comp=None, ws_bytes=0, x=FAKE, pos=FAKE, err=FAKE, T=4):
+    comp = comp or B._Comp(FAKE, FAKE, FAKE, FAKE, 512)
+    return lib.csa_compress_append(ctypes.byref(L) if L is not None else None, ctypes.byref(comp), x, 2, T, pos,
+                                   FAKE, FAKE, 100, FAKE, FAKE, FAKE, ws_bytes, err, None)
+
+
+def test_host_validation_fails_closed(lib):
+    L = _layer()
+    assert _compress(lib, None) == B.CSA_ERR_ARG
+    assert _compress(lib, _layer(dtype=7)) == B.CSA_ERR_ARG
+    assert _compress(lib, _layer(R=60)) == B.CSA_ERR_ARG
+    assert _compress(lib, _layer(X=4100)) == B.CSA_ERR_ARG
+    assert _compress(lib, L, comp=B._Comp(FAKE, FAKE, FAKE, FAKE, 100)) == B.CSA_ERR_ARG
+    assert _compress(lib, L, x=FAKE + 2) == B.CSA_ERR_ARG
+    assert _compress(lib, L, x=0) == B.CSA_ERR_ARG
+    assert _compress(lib, L, pos=FAKE + 2) == B.CSA_ERR_ARG
+    assert _compress(lib, L, T=0) == B.CSA_ERR_ARG
+    assert _compress(lib, L, ws_bytes=16) == B.CSA_ERR_WORKSPACE
+    # the index call exists only for layers with an indexer
+    L128 = _layer(ratio=128)
+    assert lib.csa_index_topk(ctypes.byref(L128), FAKE, FAKE, 1, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              1 << 30, FAKE, None) == B.CSA_ERR_UNSUPPORTED
+    # decode attention: selections on a layer without an indexer are rejected
+    assert lib.csa_attend_decode(ctypes.byref(L128), FAKE, FAKE, FAKE, 1, FAKE, FAKE, 10, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_ARG
+    # prefill: chunk length bounds and a too-small workspace
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert lib.csa_attend_prefill_chunk(ctypes.byref(L), *args, 0, 0, FAKE, FAKE, FAKE, 10, FAKE, FAKE, FAKE, None,
+                                        FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_attend_prefill_chunk(ctypes.byref(L), *args, 8, 0, FAKE, FAKE, FAKE, 10, FAKE, FAKE, FAKE, None,
+                                        FAKE, 64, FAKE, None) == B.CSA_ERR_WORKSPACE
+
+
+def test_binding_requires_cuda_tensors(lib):
+    import torch
+    L = csa.Layer(dtype=torch.bfloat16, H=64, D=512, R=64, W=128, ratio=4, Hi=64, Di=128, topk=512, X=4096)
+    with pytest.raises(ValueError):
+        B._ptr(torch.zeros(4))
+    assert csa.workspace_size(L, csa.OP_ATTEND_DECODE, 32, 1, 8400) > 0

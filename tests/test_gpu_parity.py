@@ -1,0 +1,373 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Inputs are the seeded synthetic workloads of csa_synth (configs 1-5 and small
+variants); comparison rules are in tests/_gpu.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import csa_synth
+from oracle import csa_oracle as O
+from tests._common import f64, oracle_comp, oracle_layer, oracle_state
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from tests import _gpu as G
+
+
+def _oracle_seq_state(cache: csa_synth.Cache, b: int) -> dict:
+    st = oracle_state(cache)
+    out = {}
+    for k, v in st.items():
+        out[k] = None if v is None else v[b:b + 1].copy()
+    return out
+
+
+def _step_rows(si: csa_synth.StepInputs, b: int):
+    return (f64(si.x[b:b + 1]), f64(si.q[b:b + 1]), f64(si.kv[b:b + 1]), f64(si.iq[b:b + 1]), f64(si.iw[b:b + 1]))
+
+
+def _seq_projs(run, b):
+    return {k: v[b:b + 1].cpu() for k, v in run.projs.items()}
+
+
+def _oracle_decode_check(layer, ca, ci, st, xs, sink, invf, gpu_out, gpu_sel, gpu_nsel, what, projs):
+    """Advance the oracle state by one token and check the GPU's projections, selection and output for it.
+    ``projs`` are the GPU's projections of this sequence's token (per pool)."""
+    x, q, kv, iq, iw = xs
+    n0 = st["n_rows"].copy()
+    st["front_a"], st["pool"], n_a, e1 = G.oracle_compress_checked(layer, ca, x, st["pos"], st["front_a"],
+                                                                   st["pool"], n0, invf, projs["attn"], what)
+    assert e1 == 0
+    sel = n_sel = None
+    if layer.has_indexer:
+        st["front_i"], st["ikeys"], n_i, e2 = G.oracle_compress_checked(layer, ci, x, st["pos"], st["front_i"],
+                                                                        st["ikeys"], n0, invf, projs["index"], what)
+        assert e2 == 0 and np.array_equal(n_a, n_i)
+        p = int(st["pos"][0])
+        nv = O.visible_rows(layer, int(n_a[0]), p)
+        scores = O.index_scores(layer, iq[0], iw[0], st["ikeys"][0, :nv], p, invf) if nv > layer.topk else None
+        G.check_topk(gpu_sel[:int(gpu_nsel)], scores, layer.topk, nv, what=f"{what} top-k")
+        sel = np.asarray(gpu_sel, dtype=np.int64)[None]
+        n_sel = np.array([int(gpu_nsel)])
+    st["n_rows"] = n_a
+    out, st["window"], err = O.attend_decode(layer, q, kv, sink, st["window"], st["pool"], n_a, sel, n_sel, st["pos"],
+                                             invf)
+    assert err == 0
+    st["pos"] = st["pos"] + 1
+    return G.check_rows(gpu_out, out[0], layer.dtype, what=f"{what} output", R=layer.R)
+
+
+def test_config1_tiny_fp32_decode_256_steps():
+    """Config 1: fp32 storage, 256 decode steps from an empty cache (sparse from step 68), every step checked."""
+    cfg = csa_synth.CONFIGS[1]
+    cap = cfg.steps // cfg.ratio + 2
+    run = G.Runner(cfg)
+    host = csa_synth.empty_cache(cfg, cap)
+    st_g = G.DevCache(host)
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    sink, invf = f64(csa_synth.sinks(cfg)), f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    st_o = _oracle_seq_state(host, 0)
+    worst = 0.0
+    for step in range(cfg.steps):
+        si = csa_synth.step_inputs(cfg, step)
+        out, sel, n_sel = run.decode_step(st_g, si)
+        torch.cuda.synchronize()
+        worst = max(worst, _oracle_decode_check(layer, ca, ci, st_o, _step_rows(si, 0), sink, invf, out[0].cpu(),
+                                                sel[0].cpu().numpy(), n_sel[0].item(), f"step {step}",
+                                                _seq_projs(run, 0)))
+    assert run.err.item() == 0
+    n = int(st_o["n_rows"][0])
+    assert n == cfg.steps // cfg.ratio == st_g.n_rows.item()
+    G.check_pool_rows(st_g.pool[0, :n].cpu(), st_o["pool"][0, :n], "f32", "attention pool", R=cfg.R)
+    G.check_pool_rows(st_g.ikeys[0, :n].cpu(), st_o["ikeys"][0, :n], "f32", "index pool", R=cfg.R)
+    G.check_pool_rows(st_g.window[0].cpu(), st_o["window"][0], "f32", "window")
+    print(f"config 1: worst max-relative output error {worst:.2e}")
+
+
+def test_config2_flash_build_8k_then_decode():
+    """Config 2: compress 8192 seeded hidden tokens into both pools, then one decode step at p = 8192."""
+    cfg = csa_synth.CONFIGS[2]
+    cap = cfg.prefill_tokens // cfg.ratio + 8
+    run = G.Runner(cfg)
+    host = csa_synth.empty_cache(cfg, cap)
+    st_g = G.DevCache(host)
+    xs = csa_synth.hidden(cfg, cfg.prefill_tokens)
+    projs = run.compress(st_g, xs)
+    st_g.pos += cfg.prefill_tokens
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    st_o = _oracle_seq_state(host, 0)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    x = f64(xs)
+    n0 = st_o["n_rows"].copy()
+    st_o["front_a"], st_o["pool"], n_a, e = G.oracle_compress_checked(
+        layer, ca, x, st_o["pos"], st_o["front_a"], st_o["pool"], n0, invf, projs["attn"].cpu(), "8k build attn")
+    st_o["front_i"], st_o["ikeys"], n_i, _ = G.oracle_compress_checked(
+        layer, ci, x, st_o["pos"], st_o["front_i"], st_o["ikeys"], n0, invf, projs["index"].cpu(), "8k build index")
+    st_o["n_rows"], st_o["pos"] = n_a, st_o["pos"] + cfg.prefill_tokens
+    torch.cuda.synchronize()
+    assert e == 0 and int(n_a[0]) == 2048 == st_g.n_rows.item()
+    G.check_pool_rows(st_g.pool[0, :2048].cpu(), st_o["pool"][0, :2048], "bf16", "attention pool", R=cfg.R)
+    G.check_pool_rows(st_g.ikeys[0, :2048].cpu(), st_o["ikeys"][0, :2048], "bf16", "index pool", R=cfg.R)
+    G.check_pool_rows(st_g.front_attn.cpu(), st_o["front_a"], "bf16", "attention frontier")
+    # one decode step; window ring starts empty except what decode appends
+    si = csa_synth.step_inputs(cfg, 0)
+    out, sel, n_sel = run.decode_step(st_g, si)
+    torch.cuda.synchronize()
+    sink = f64(csa_synth.sinks(cfg))
+    # the oracle continues from ITS pools (within 2 ulps of the GPU's)
+    _oracle_decode_check(layer, ca, ci, st_o, _step_rows(si, 0), sink, invf, out[0].cpu(), sel[0].cpu().numpy(),
+                         n_sel[0].item(), "config 2", _seq_projs(run, 0))
+    assert run.err.item() == 0
+
+
+@pytest.mark.parametrize("cid,ctx,steps,seqs", [(3, 32768, 10, (0, 13, 31)), (4, 262144 - 3, 6, (0, 15))])
+def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs):
+    """Configs 3 and 4 at full batch and context: every sequence runs on the GPU; the oracle follows
+    a few of them step by step (window-boundary crossings included)."""
+    cfg = csa_synth.CONFIGS[cid]
+    cap = ctx // cfg.ratio + steps // cfg.ratio + 4
+    run = G.Runner(cfg)
+    host = csa_synth.synth_cache(cfg, cap, ctx=ctx)
+    st_g = G.DevCache(host)
+    layer = oracle_layer(cfg)
+    ca = oracle_comp(run.ca_host)
+    ci = oracle_comp(run.ci_host) if cfg.has_indexer else None
+    sink, invf = f64(csa_synth.sinks(cfg)), f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    st_o = {b: _oracle_seq_state(host, b) for b in seqs}
+    for step in range(steps):
+        si = csa_synth.step_inputs(cfg, step)
+        out, sel, n_sel = run.decode_step(st_g, si)
+        torch.cuda.synchronize()
+        for b in seqs:
+            _oracle_decode_check(layer, ca, ci, st_o[b], _step_rows(si, b), sink, invf, out[b].cpu(),
+                                 None if sel is None else sel[b].cpu().numpy(),
+                                 None if n_sel is None else n_sel[b].item(), f"cfg {cid} seq {b} step {step}",
+                                 _seq_projs(run, b))
+    assert run.err.item() == 0
+    for b in seqs:
+        n = int(st_o[b]["n_rows"][0])
+        assert n == st_g.n_rows[b].item()
+        lo = ctx // cfg.ratio
+        G.check_pool_rows(st_g.pool[b, lo:n].cpu(), st_o[b]["pool"][0, lo:n], "bf16", "new pool rows", R=cfg.R)
+        G.check_pool_rows(st_g.window[b].cpu(), st_o[b]["window"][0], "bf16", "window")
+
+
+def test_config5_prefill_chunk_sampled_queries():
+    """Config 5: a 4096-token chunk on a 65536-token cache.  All emitted rows, the frontier and the window
+    are checked; the per-query selection and output are checked on sampled queries."""
+    cfg = csa_synth.CONFIGS[5]
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
+    run = G.Runner(cfg)
+    host = csa_synth.synth_cache(cfg, cap)
+    st_g = G.DevCache(host)
+    ch = csa_synth.chunk_inputs(cfg)
+    out, sel = run.prefill(st_g, ch, cfg.ctx)
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    sink = f64(csa_synth.sinks(cfg))
+    st = _oracle_seq_state(host, 0)
+    x = f64(ch.x)
+    n0 = st["n_rows"].copy()
+    st["front_a"], st["pool"], n_a, _ = G.oracle_compress_checked(layer, ca, x, st["pos"], st["front_a"],
+                                                                  st["pool"], n0, invf, run.projs["attn"].cpu(),
+                                                                  "chunk attn")
+    st["front_i"], st["ikeys"], _, _ = G.oracle_compress_checked(layer, ci, x, st["pos"], st["front_i"], st["ikeys"],
+                                                                 n0, invf, run.projs["index"].cpu(), "chunk index")
+    n = int(n_a[0])
+    assert n == st_g.n_rows.item() == (cfg.ctx + cfg.T) // 4
+    lo = cfg.ctx // 4
+    G.check_pool_rows(st_g.pool[0, lo:n].cpu(), st["pool"][0, lo:n], "bf16", "chunk pool rows", R=cfg.R)
+    G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), st["ikeys"][0, lo:n], "bf16", "chunk index rows", R=cfg.R)
+    G.check_pool_rows(st_g.front_index.cpu(), st["front_i"], "bf16", "index frontier")
+    q, kv, iq, iw = f64(ch.q), f64(ch.kv), f64(ch.iq), f64(ch.iw)
+    rng = np.random.default_rng(0)
+    queries = sorted(set([0, 1, 2, 3, 4, 126, 127, 128, 129, 2047, 4094, 4095] +
+                         list(rng.integers(0, cfg.T, 8))))
+    window = st["window"][0]
+    pool, ikeys = st["pool"][0], st["ikeys"][0]
+    kvr = [O.store(O.rope(kv[i], cfg.ctx + i, invf), "bf16") for i in range(cfg.T)]
+    gsel = sel.cpu().numpy()
+    gout = out.cpu()
+    for i in queries:
+        p = cfg.ctx + i
+        nv = O.visible_rows(layer, n, p)
+        scores = O.index_scores(layer, iq[i], iw[i], ikeys[:nv], p, invf)
+        rows = gsel[i][gsel[i] >= 0]
+        G.check_topk(rows, scores, layer.topk, nv, what=f"query {i} top-k")
+        win = [window[t % cfg.W] if t < cfg.ctx else kvr[t - cfg.ctx] for t in O.window_tokens(layer, p)]
+        keys = np.concatenate([pool[np.sort(rows)], np.stack(win)])
+        qr = O.store(O.rope(q[i], p, invf), "bf16")
+        o = O.output_rows(layer, O.attend(layer, qr, keys, sink), p, invf)
+        G.check_rows(gout[i], o, "bf16", what=f"query {i} output", R=cfg.R)
+    ring = np.array(window)
+    for t in range(cfg.ctx + cfg.T - cfg.W, cfg.ctx + cfg.T):
+        ring[t % cfg.W] = kvr[t - cfg.ctx]
+    G.check_pool_rows(st_g.window[0].cpu(), ring, "bf16", "window after chunk")
+
+
+def test_gpu_decode_equals_gpu_prefill():
+    """A chunk attended as one prefill call equals the same tokens decoded one at a time (Flash shapes,
+    sparse regime, window eviction inside the chunk, 16 compress boundaries)."""
+    cfg = csa_synth.CONFIGS[5].replace(ctx=8192 + 2, T=64)
+    cap = (cfg.ctx + cfg.T) // 4 + 4
+    host = csa_synth.synth_cache(cfg, cap)
+    run = G.Runner(cfg)
+    ch = csa_synth.chunk_inputs(cfg)
+    st_p = G.DevCache(host)
+    out_p, sel_p = run.prefill(st_p, ch, cfg.ctx)
+    st_d = G.DevCache(host)
+    outs = []
+    for i in range(cfg.T):
+        si = csa_synth.StepInputs(x=ch.x[:, i:i + 1], q=ch.q[i:i + 1], kv=ch.kv[i:i + 1], iq=ch.iq[i:i + 1],
+                                  iw=ch.iw[i:i + 1])
+        o, s, ns = run.decode_step(st_d, si)
+        outs.append(o[0])
+        assert sorted(s[0, :ns[0]].tolist()) == sorted(x for x in sel_p[i].tolist() if x >= 0), f"query {i}"
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    assert torch.equal(st_p.pool, st_d.pool) and torch.equal(st_p.ikeys, st_d.ikeys)
+    assert torch.equal(st_p.window, st_d.window)
+    assert torch.equal(st_p.front_attn, st_d.front_attn)
+    G.check_rows(torch.stack(outs).cpu(), out_p.cpu(), "bf16", what="decode vs prefill", R=cfg.R)
+
+
+def _ragged_cache(cfg, cap, ctxs):
+    host = csa_synth.synth_cache(cfg, cap, B=len(ctxs), ctx=max(ctxs))
+    for b, c in enumerate(ctxs):
+        n = c // cfg.ratio
+        host.pool[b, n:] = 0
+        if host.ikeys is not None:
+            host.ikeys[b, n:] = 0
+        host.n_rows[b] = n
+        host.pos[b] = c
+    return host
+
+
+def test_ragged_batch_edges():
+    """One batch mixing an empty cache, a cache shorter than the window, the dense/sparse threshold
+    (n_vis == topk and topk + 1) and a long cache."""
+    cfg = csa_synth.CONFIGS[3].replace(B=6)
+    ctxs = [0, 3, 100, 2047, 2051, 9000]
+    cap = max(ctxs) // 4 + 8
+    host = _ragged_cache(cfg, cap, ctxs)
+    run = G.Runner(cfg)
+    st_g = G.DevCache(host)
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    sink, invf = f64(csa_synth.sinks(cfg)), f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    st_o = {b: _oracle_seq_state(host, b) for b in range(len(ctxs))}
+    for step in range(5):
+        si = csa_synth.step_inputs(cfg, step, B=len(ctxs))
+        out, sel, n_sel = run.decode_step(st_g, si)
+        torch.cuda.synchronize()
+        for b in range(len(ctxs)):
+            _oracle_decode_check(layer, ca, ci, st_o[b], _step_rows(si, b), sink, invf, out[b].cpu(),
+                                 sel[b].cpu().numpy(), n_sel[b].item(), f"ctx {ctxs[b]} step {step}",
+                                 _seq_projs(run, b))
+    assert run.err.item() == 0
+    assert n_sel.cpu().tolist()[3] == 512  # 2047 + 5 tokens -> 513 rows visible: sparse, 512 kept
+
+
+def test_topk_ties_go_to_lower_rows():
+    """All index keys equal -> all scores tie exactly; the selection must be rows 0 .. topk-1."""
+    cfg = csa_synth.CONFIGS[3].replace(B=2)
+    cap = 1200
+    host = _ragged_cache(cfg, cap, [4000, 4400])
+    host.ikeys[:, :] = host.ikeys[:, :1].clone()
+    run = G.Runner(cfg)
+    st_g = G.DevCache(host)
+    si = csa_synth.step_inputs(cfg, 0, B=2)
+    _, sel, n_sel = run.decode_step(st_g, si)
+    torch.cuda.synchronize()
+    for b in range(2):
+        assert n_sel[b].item() == 512
+        assert sel[b].tolist() == list(range(512))
+
+
+def test_compress_chunking_invariance_gpu():
+    """Any split of the same tokens into compress calls gives bit-identical pools and frontiers."""
+    cfg = csa_synth.CONFIGS[2].replace(B=2)
+    cap = 64
+    xs = csa_synth.hidden(cfg, 77, B=2)
+    run = G.Runner(cfg)
+    results = []
+    for splits in ([77], [1] * 77, [3, 5, 8, 61], [13, 64]):
+        st = G.DevCache(csa_synth.empty_cache(cfg, cap, B=2))
+        p = 0
+        for s in splits:
+            run.compress(st, xs[:, p:p + s])
+            st.pos += s
+            p += s
+        torch.cuda.synchronize()
+        results.append(st)
+    for st in results[1:]:
+        assert torch.equal(st.pool, results[0].pool) and torch.equal(st.ikeys, results[0].ikeys)
+        assert torch.equal(st.front_attn, results[0].front_attn)
+        assert torch.equal(st.n_rows, results[0].n_rows)
+    assert run.err.item() == 0
+
+
+def test_device_errors_fail_closed():
+    """Inconsistent state, capacity overflow and out-of-range selections raise error bits and leave the
+    affected state untouched."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[2].replace(B=2)
+    run = G.Runner(cfg)
+    # state: n_rows inconsistent with pos for sequence 0
+    st = G.DevCache(_ragged_cache(cfg, 40, [40, 40]))
+    st.n_rows[0] = 3
+    before = st.pool.clone(), st.front_attn.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa.compress_append(run.L, run.ca, G.dev(csa_synth.hidden(cfg, 8, B=2)), st.pos, st.front_attn, st.pool,
+                        st.n_rows, run.inv_freq, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == csa.DEV_STATE
+    assert torch.equal(st.pool[0], before[0][0]) and torch.equal(st.front_attn[0], before[1][0])
+    assert st.n_rows.tolist() == [3, 12]
+    # capacity: 40 tokens fill 10 rows of a 10-row pool; 4 more would emit row 10
+    st = G.DevCache(_ragged_cache(cfg, 10, [36, 40]))
+    err.zero_()
+    before = st.pool.clone()
+    csa.compress_append(run.L, run.ca, G.dev(csa_synth.hidden(cfg, 4, B=2)), st.pos, st.front_attn, st.pool,
+                        st.n_rows, run.inv_freq, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == csa.DEV_CAPACITY
+    assert st.n_rows.tolist() == [10, 10] and torch.equal(st.pool[1], before[1])
+    # out-of-range selection
+    st = G.DevCache(_ragged_cache(cfg, 40, [100, 100]))
+    err.zero_()
+    si = csa_synth.step_inputs(cfg, 0, B=2)
+    sel = torch.full((2, cfg.topk), -1, dtype=torch.int32, device="cuda")
+    sel[:, 0] = 5
+    sel[1, 1] = 30  # only 25 rows exist
+    n_sel = torch.tensor([1, 2], dtype=torch.int32, device="cuda")
+    out = torch.empty(2, cfg.H, cfg.D, dtype=torch.bfloat16, device="cuda")
+    csa.attend_decode(run.L, G.dev(si.q), G.dev(si.kv), run.sink, st.window, st.pool, st.n_rows, sel, n_sel, st.pos,
+                      run.inv_freq, out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == csa.DEV_RANGE
+    assert torch.isfinite(out.float()).all()
+
+
+def test_host_validation_raises():
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[2].replace(B=1)
+    run = G.Runner(cfg)
+    st = G.DevCache(csa_synth.empty_cache(cfg, 8, B=1))
+    x = G.dev(csa_synth.hidden(cfg, 4, B=1))
+    bad = csa.Layer(**{**vars(run.L), "D": 500})
+    with pytest.raises(csa.CSAError) as ei:
+        csa.compress_append(bad, run.ca, x, st.pos, st.front_attn, st.pool, st.n_rows, run.inv_freq)
+    assert ei.value.code == 1
+    tiny_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(csa.CSAError) as ei:
+        csa.compress_append(run.L, run.ca, x, st.pos, st.front_attn, st.pool, st.n_rows, run.inv_freq, ws=tiny_ws)
+    assert ei.value.code == 4
