@@ -69,6 +69,15 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s);
 
+// ---- tc_attend.cu (tensor-core attention; bf16, H = 64, D = 512, R = 64)
+bool tc_attend_supported(const Dims& L);
+// Q queries (decode: pos[q], ring[q], pool[q]; prefill: pos == null, positions pos0 + q, batch 1, chunk rows
+// kvr), S key splits per query: S > 1 writes (m, l, acc) partials, S == 1 the final output.
+cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, const void* ring, const void* kvr,
+                             const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows, const int32_t* pos,
+                             int pos0, int cap, const float* sink, const float* inv_freq, int Q, int S,
+                             float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
+
 // ---- attend.cu
 struct AttendWs {
   void* qr;        // [Q, H, D] roped queries, model dtype
