@@ -101,7 +101,11 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
   switch (op) {
     case CSA_OP_COMPRESS:
       if (T < 1) return CSA_ERR_ARG;
-      *bytes = ws_compress(L, L.D > L.Di ? L.D : L.Di, B, T);
+      *bytes = ws_compress(L, L.D, B, T);
+      if (L.has_indexer()) {
+        const size_t bi = ws_compress(L, L.Di, B, T);
+        if (bi > *bytes) *bytes = bi;
+      }
       return CSA_OK;
     case CSA_OP_INDEX_TOPK:
       *bytes = ws_index(L, B, cap);

@@ -23,6 +23,9 @@ CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T) {
   CompressWs w;
   w.flags = c.take<int32_t>(B);
   w.proj = c.take<char>((size_t)B * T * 2 * L.lanes * d * esize(L.dtype));
+  w.part = nullptr;
+  w.tickets = nullptr;
+  if (tc_project_supported(L, d)) carve_tc_project(c, L, d, B * T, &w.part, &w.tickets);
   return w;
 }
 
@@ -166,10 +169,15 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
   k_compress_validate<<<(B + 127) / 128, 128, 0, s>>>(pos, n_rows, B, T_, L.ratio, cap, ws.flags, err); count_launches(1);
   const int ntok = B * T_;
-  dim3 gp((2 * Ld + 7) / 8, (ntok + 7) / 8);
-  k_project_simt<T, 8><<<gp, 256, 0, s>>>(static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
-                                           static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
-                                           static_cast<T*>(ws.proj)); count_launches(1);
+  if (tc_project_supported(L, d)) {
+    cudaError_t e = launch_tc_project(L, d, x, ntok, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets, err, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    dim3 gp((2 * Ld + 7) / 8, (ntok + 7) / 8);
+    k_project_simt<T, 8><<<gp, 256, 0, s>>>(static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
+                                             static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
+                                             static_cast<T*>(ws.proj)); count_launches(1);
+  }
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
   dim3 ge(maxwin, B);
   size_t smem = (2 * (size_t)d + 32) * sizeof(float);

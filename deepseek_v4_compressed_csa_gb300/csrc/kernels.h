@@ -41,6 +41,8 @@ void count_launches(int n);
 struct CompressWs {
   int32_t* flags;  // [B] 1 = sequence valid for this call
   void* proj;      // [B*T, 2*L*d] model dtype: kv | gate of every new token
+  float* part;     // tensor-core projection: split-K partials (or null)
+  int* tickets;    // tensor-core projection: per-tile arrival counters (or null)
 };
 CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T);
 cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,
@@ -59,6 +61,12 @@ IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap);
 cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
                               const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq,
                               int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s);
+
+// ---- tc_project.cu (tensor-core compressor projections; bf16)
+bool tc_project_supported(const Dims& L, int d);
+void carve_tc_project(Carver& c, const Dims& L, int d, int ntok, float** part, int** tickets);
+cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,
+                              void* proj, float* part, int* tickets, int32_t* err, cudaStream_t s);
 
 // ---- tc_indexer.cu (tensor-core scores; bf16, Hi = 64, Di = 128)
 bool tc_index_supported(const Dims& L);

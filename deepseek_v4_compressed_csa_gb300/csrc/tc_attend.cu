@@ -227,20 +227,33 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
       lsum[tid] = 0.f;
     }
     tc::named_bar(1, kMain);
-    // query block: RoPE on the last 64 dims, bf16, 128-byte swizzled K-major rows (one per head)
-    for (int e = tid; e < kAH * 64; e += kMain) {
-      const int h = e >> 6, c = e & 63;
-      uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)it.q * kAH + h) * kAD + c * 8));
-      if (c >= 56) {
-        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = (c - 56) * 4 + k;
-          const float2 x = __bfloat1622float2(hv[k]);
-          hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
-        }
+    // query block: 128-byte swizzled K-major rows (one per head), copied with cp.async (all in flight),
+    // then RoPE on the last 64 dims in place, in bf16
+    {
+      const uint32_t q_base = tc::smem_u32(qbuf);
+      const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
+#pragma unroll 8
+      for (int e = tid; e < kAH * 64; e += kMain) {
+        const int h = e >> 6, c = e & 63;
+        tc::cp_async16(q_base + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4), qsrc + (size_t)h * kAD + c * 8,
+                       16u);
       }
-      *reinterpret_cast<uint4*>(qbuf + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4)) = raw;
+      tc::cp_async_wait_all();
+    }
+    tc::named_bar(1, kMain);
+#pragma unroll
+    for (int e = tid; e < kAH * 8; e += kMain) {
+      const int h = e >> 3, c = 56 + (e & 7);
+      uint4* slot = reinterpret_cast<uint4*>(qbuf + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4));
+      uint4 raw = *slot;
+      __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = (c - 56) * 4 + k;
+        const float2 x = __bfloat1622float2(hv[k]);
+        hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
+      }
+      *slot = raw;
     }
     tc::fence_proxy_async_smem();
 

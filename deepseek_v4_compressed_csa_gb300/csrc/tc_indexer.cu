@@ -205,27 +205,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_dealloc(tmem, 2 * N);
 }
 
-// qr[q][h][:] = RoPE(iq[q][h][:], p_q) (bf16), wts[q][h] = iw[q][h] * scale
-__global__ void k_tc_index_prep(const __nv_bfloat16* __restrict__ iq, const __nv_bfloat16* __restrict__ iw,
-                                const int32_t* __restrict__ pos, int pos0, int R, const float* __restrict__ inv_freq,
-                                float wscale, __nv_bfloat16* __restrict__ qr, float* __restrict__ wts) {
-  const int q = blockIdx.x;
-  const int p = pos ? pos[q] : pos0 + q;
+// qr[q][h][:] = RoPE(iq[q][h][:], p_q) (bf16), wts[q][h] = iw[q][h] * scale.
+// Block (q, head group of 8): one 16-byte chunk of 8 dims per thread.
+__global__ void __launch_bounds__(128) k_tc_index_prep(const __nv_bfloat16* __restrict__ iq,
+                                                       const __nv_bfloat16* __restrict__ iw,
+                                                       const int32_t* __restrict__ pos, int pos0, int R,
+                                                       const float* __restrict__ inv_freq, float wscale,
+                                                       __nv_bfloat16* __restrict__ qr, float* __restrict__ wts) {
   constexpr int Hi = 64, Di = 128;
-  for (int e = threadIdx.x; e < Hi * Di; e += blockDim.x) {
-    const int c = e % Di;
-    const __nv_bfloat16* row = iq + ((size_t)q * Hi + e / Di) * Di;
-    float v = __bfloat162float(row[c]);
-    if (c >= Di - R) {
-      const int i = (c - (Di - R)) >> 1;
-      float cs, sn;
-      rope_cs(p, inv_freq, i, &cs, &sn);
-      const float x0 = __bfloat162float(row[Di - R + 2 * i]), x1 = __bfloat162float(row[Di - R + 2 * i + 1]);
-      v = ((c - (Di - R)) & 1) ? fmaf(x0, sn, x1 * cs) : fmaf(x0, cs, -x1 * sn);
+  __shared__ float rc[64], rs[64];
+  const int q = blockIdx.x, h0 = blockIdx.y * 8;
+  const int p = pos ? pos[q] : pos0 + q;
+  if (threadIdx.x < R / 2) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
+  __syncthreads();
+  const int h = h0 + (threadIdx.x >> 4), c = threadIdx.x & 15;  // 16 chunks of 8 dims per head row
+  const size_t off = ((size_t)q * Hi + h) * Di + c * 8;
+  uint4 raw = __ldg(reinterpret_cast<const uint4*>(iq + off));
+  if (c * 8 >= Di - R) {
+    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = (c * 8 - (Di - R)) / 2 + k;
+      const float2 x = __bfloat1622float2(hv[k]);
+      hv[k] = __floats2bfloat162_rn(fmaf(x.x, rc[i], -x.y * rs[i]), fmaf(x.x, rs[i], x.y * rc[i]));
     }
-    qr[(size_t)q * Hi * Di + e] = __float2bfloat16_rn(v);
   }
-  if (threadIdx.x < Hi) wts[(size_t)q * Hi + threadIdx.x] = __bfloat162float(iw[(size_t)q * Hi + threadIdx.x]) * wscale;
+  *reinterpret_cast<uint4*>(qr + off) = raw;
+  if (threadIdx.x < 8) wts[(size_t)q * Hi + h0 + threadIdx.x] = __bfloat162float(iw[(size_t)q * Hi + h0 + threadIdx.x]) * wscale;
 }
 
 int g_num_sms = 0;
@@ -251,8 +257,9 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   __nv_bfloat16* qr = c.take<__nv_bfloat16>((size_t)Q * 64 * 128);
   float* wts = c.take<float>((size_t)Q * 64);
   const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
-  k_tc_index_prep<<<Q, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(iq), static_cast<const __nv_bfloat16*>(iw),
-                                    pos, pos0, L.R, inv_freq, wscale, qr, wts);
+  k_tc_index_prep<<<dim3(Q, 8), 128, 0, s>>>(static_cast<const __nv_bfloat16*>(iq),
+                                              static_cast<const __nv_bfloat16*>(iw), pos, pos0, L.R, inv_freq,
+                                              wscale, qr, wts);
   count_launches(1);
   const int G = pos ? 1 : 4;
   CUtensorMap tk, tq;

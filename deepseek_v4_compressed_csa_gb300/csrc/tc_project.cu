@@ -1,0 +1,216 @@
+// Compressor projections on the 5th-generation tensor cores:
+//   proj[tok][o] = sum_k W[o][k] x[tok][k],  W = [wkv ; wgate]  (2*L*d rows), bf16 out.
+// ("DeepSeek-V4-Flash: native deepseek_v4 AR backend", MTPLX #216, "Decode path":
+// projections kept at the model dtype; "feat: add DeepSeek-V4 (Pro/Flash) model
+// support", mlx-lm #1189, Thump604: wkv/wgate (1024, 4096) on ratio-4 layers.)
+//
+// Computed transposed, C^T = W x^T: M = 128 output features per tile (TMEM lane =
+// feature), N = up to 256 tokens, K = hidden size streamed by TMA in 64-wide
+// blocks through a ring of stages.  Decode has few tokens (one per sequence), so
+// the hidden axis is split across CTAs until ~150 CTAs stream the weights; each
+// split writes fp32 partials and the last CTA of a tile (atomic ticket) sums
+// them in split order, so the result does not depend on arrival order.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kPThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+
+struct PjArgs {
+  int ntok, X, Ld, N, n_kblk, splits;  // n_kblk: 64-wide K blocks per split
+  __nv_bfloat16* proj;                 // [ntok, 2*Ld]
+  float* part;                         // [splits, 2*Ld, n_tiles*N] fp32 (splits > 1)
+  int* tickets;                        // [m_tiles * n_tiles] zeroed before the launch
+  int n_cols;                          // n_tiles * N
+  int32_t* err;
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_tc_project(const __grid_constant__ CUtensorMap tm_wkv, const __grid_constant__ CUtensorMap tm_wg,
+                 const __grid_constant__ CUtensorMap tm_x, PjArgs a, int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int N = a.N;
+  const int stage_bytes = kABytes + N * 128;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+  uint64_t* empty = full + stages;
+  uint64_t* acc_full = empty + stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
+  const int m = blockIdx.x, n = blockIdx.y, split = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tcols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, tcols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+  const int k0 = split * a.n_kblk;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* wmap = (m * 128 < a.Ld) ? &tm_wkv : &tm_wg;
+      const int wrow = (m * 128 < a.Ld) ? m * 128 : m * 128 - a.Ld;
+      tc::tma_prefetch(wmap);
+      tc::tma_prefetch(&tm_x);
+      int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int kb = 0; kb < a.n_kblk; ++kb) {
+        const int s = kb % stages;
+        const uint32_t ph = (kb / stages) & 1;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1)) { failed = true; break; }
+        uint8_t* st = smem + s * stage_bytes;
+        tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tc::tma_load_2d(st, wmap, &full[s], (k0 + kb) * 64, wrow);
+        tc::tma_load_2d(st + kABytes, &tm_x, &full[s], (k0 + kb) * 64, n * N);
+        ++issued[s];
+      }
+      for (int s = 0; s < stages; ++s)
+        if (issued[s] && !tc::mbar_wait(&full[s], (issued[s] - 1) & 1)) failed = true;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, N);
+      for (int kb = 0; kb < a.n_kblk; ++kb) {
+        const int s = kb % stages;
+        if (!tc::mbar_wait(&full[s], (kb / stages) & 1)) { failed = true; break; }
+        tc::fence_after_sync();
+        const uint32_t ab = tc::smem_u32(smem + s * stage_bytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem, tc::sdesc_kmajor_sw128(ab + k * 32), tc::sdesc_kmajor_sw128(ab + kABytes + k * 32),
+                       idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(acc_full);  // also retires every MMA before the epilogue and the dealloc
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int o = m * 128 + quarter * 32 + lane;  // output feature of this thread
+    if (!tc::mbar_wait(acc_full, 0)) failed = true;
+    tc::fence_after_sync();
+    if (!failed) {
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t u[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c0, u);
+        tc::tmem_wait_ld();
+        if (a.splits == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int tok = n * N + c0 + i;
+            if (tok < a.ntok) a.proj[(size_t)tok * 2 * a.Ld + o] = __float2bfloat16_rn(__uint_as_float(u[i]));
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)split * 2 * a.Ld + o) * a.n_cols + n * N + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                 __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+        }
+      }
+    }
+  }
+  if (failed) atomicOr(a.err, tc::kErrTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, tcols);
+  if (a.splits == 1) return;
+  // split-K fix-up: the last CTA of the tile sums every split's partials in split order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int t = atomicAdd(&a.tickets[m * gridDim.y + n], 1);
+    *s_last = (t == a.splits - 1);
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < 128 * N; e += blockDim.x) {
+    const int r = e / N, c = e % N;
+    const int o = m * 128 + r, tok = n * N + c;
+    if (tok >= a.ntok) continue;
+    float acc = 0.f;
+    for (int s = 0; s < a.splits; ++s) acc += __ldcg(a.part + ((size_t)s * 2 * a.Ld + o) * a.n_cols + tok);
+    a.proj[(size_t)tok * 2 * a.Ld + o] = __float2bfloat16_rn(acc);
+  }
+}
+
+int g_sms_pj = 0;
+
+struct PjPlan {
+  int N, n_tiles, m_tiles, splits;
+};
+
+PjPlan plan_project(const Dims& L, int d, int ntok) {
+  PjPlan p;
+  const int Ld = L.lanes * d;
+  p.N = ntok >= 256 ? 256 : ((ntok + 31) / 32) * 32;  // multiple of 32: the epilogue drains 32 columns at a time
+  p.n_tiles = (ntok + p.N - 1) / p.N;
+  p.m_tiles = 2 * Ld / 128;
+  const int base = p.m_tiles * p.n_tiles;
+  const int kblk = L.X / 64;
+  p.splits = 1;
+  while (base * p.splits * 2 <= 160 && p.splits * 2 <= kblk && (kblk % (p.splits * 2)) == 0) p.splits *= 2;
+  return p;
+}
+
+}  // namespace
+
+bool tc_project_supported(const Dims& L, int d) {
+  return L.dtype == CSA_BF16 && L.X % 64 == 0 && (2 * L.lanes * d) % 128 == 0;
+}
+
+void carve_tc_project(Carver& c, const Dims& L, int d, int ntok, float** part, int** tickets) {
+  const PjPlan p = plan_project(L, d, ntok);
+  if (p.splits > 1) {
+    *part = c.take<float>((size_t)p.splits * 2 * L.lanes * d * p.n_tiles * p.N);
+    *tickets = c.take<int>((size_t)p.m_tiles * p.n_tiles);
+  } else {
+    *part = nullptr;
+    *tickets = nullptr;
+  }
+}
+
+cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,
+                              void* proj, float* part, int* tickets, int32_t* err, cudaStream_t s) {
+  const PjPlan p = plan_project(L, d, ntok);
+  const int Ld = L.lanes * d;
+  CUtensorMap tw, tg, tx;
+  if (!make_tmap_2d_bf16(&tw, wkv, Ld, L.X, (uint64_t)L.X * 2, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d_bf16(&tg, wgate, Ld, L.X, (uint64_t)L.X * 2, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d_bf16(&tx, x, ntok, L.X, (uint64_t)L.X * 2, p.N)) return cudaErrorInvalidValue;
+  PjArgs a{};
+  a.ntok = ntok; a.X = L.X; a.Ld = Ld; a.N = p.N; a.splits = p.splits; a.n_kblk = L.X / 64 / p.splits;
+  a.proj = static_cast<__nv_bfloat16*>(proj); a.part = part; a.tickets = tickets;
+  a.n_cols = p.n_tiles * p.N; a.err = err;
+  if (p.splits > 1) {
+    cudaMemsetAsync(tickets, 0, (size_t)p.m_tiles * p.n_tiles * sizeof(int), s);
+  }
+  const int stage_bytes = kABytes + p.N * 128;
+  const int stages = min(8, min(a.n_kblk, (200 * 1024) / stage_bytes));
+  const size_t smem = 1024 + (size_t)stages * stage_bytes + 256;
+  cudaFuncSetAttribute(k_tc_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(p.m_tiles, p.n_tiles, p.splits);
+  k_tc_project<<<grid, kPThreads, smem, s>>>(tw, tg, tx, a, stages);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace csa
