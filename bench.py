@@ -241,16 +241,16 @@ class DecodeWorkload:
         torch.cuda.synchronize()
 
     def replay(self, i, ev=None):
-        gc, gx, ga = self.graphs[i % len(self.graphs)]
-        if ev is not None:
-            ev[0].record()
-        gc.replay()
-        if ev is not None:
-            ev[1].record()
-        gx.replay()
-        if ev is not None:
-            ev[2].record()
-        ga.replay()
+        """Step i: the three phase graphs (or, eagerly, the same calls); events before each phase and after."""
+        if self.graphs is None:
+            inp = self.inputs[i % len(self.inputs)]
+            phases = [lambda: self.compress(inp), lambda: self.index(inp), lambda: self.attend(inp)]
+        else:
+            phases = [g.replay for g in self.graphs[i % len(self.graphs)]]
+        for k, run in enumerate(phases):
+            if ev is not None:
+                ev[k].record()
+            run()
         if ev is not None:
             ev[3].record()
 
@@ -286,7 +286,10 @@ def run_ours(args):
 
     wl.step(wl.inputs[0])  # first calls outside capture (one-time host set-up inside the library)
     torch.cuda.synchronize()
-    wl.capture()  # capturing does not run anything: the graphs replay the steps below
+    if args.eager:
+        wl.graphs = None  # same kernels launched one by one (for profilers that do not follow graphs)
+    else:
+        wl.capture()  # capturing does not run anything: the graphs replay the steps below
     for i in range(args.warmup):
         wl.replay(i)
     torch.cuda.synchronize()
@@ -367,7 +370,8 @@ def run_ours(args):
                 "step_hbm_gbs": round(nb["total"] / (ms_per_step / 1e3) / 1e9, 1),
                 "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
                 "l2": "flushed (512 MB write) before every timed step, outside the events",
-                "launch": "each step = 3 CUDA graph replays (compress x2 | indexer | attention)",
+                "launch": ("kernels launched one by one" if args.eager else
+                           "each step = 3 CUDA graph replays (compress x2 | indexer | attention)"),
                 "prefill": prefill,
             },
             "roofline": {
@@ -475,6 +479,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--prefill-repeats", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--oracle-sample", nargs=3, default=None)
     args = ap.parse_args()

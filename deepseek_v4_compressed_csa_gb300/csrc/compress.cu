@@ -8,12 +8,14 @@
 // at the window start j*ratio) and stepnoy's "Fix" 3 (the chunk tail is carried
 // across calls; the absolute position accumulates).
 //
-// One call = four launches on the caller's stream:
-//   validate   per-sequence state check (n_rows == pos/ratio, capacity) -> flags
+// One call = two or three launches on the caller's stream:
 //   project    kv | gate rows of every new token (model dtype) -> workspace
-//   pool_emit  one block per completed window: softmax-weighted sum per
-//              channel, RMSNorm, RoPE, store the row
-//   finish     rewrite the frontier ring with the newest tokens, advance n_rows
+//   pool_emit  one block per completed window: per-sequence state check
+//              (n_rows == pos/ratio, capacity), softmax-weighted sum per channel,
+//              RMSNorm, RoPE, store the row; for a single new token it also
+//              writes the token's frontier slot and advances n_rows
+//   finish     (chunks) rewrite the frontier ring with the newest tokens,
+//              advance n_rows
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,22 +29,6 @@ CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T) {
   w.tickets = nullptr;
   if (tc_project_supported(L, d)) carve_tc_project(c, L, d, B * T, &w.part, &w.tickets);
   return w;
-}
-
-__global__ void k_compress_validate(const int32_t* __restrict__ pos, const int32_t* __restrict__ n_rows, int B,
-                                    int T, int ratio, int cap, int32_t* __restrict__ flags, int32_t* err) {
-  int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  int p0 = pos[b];
-  int ok = 1;
-  if (p0 < 0 || n_rows[b] != p0 / ratio) {
-    atomicOr(err, CSA_DEV_STATE);
-    ok = 0;
-  } else if ((long long)(p0 + (long long)T) / ratio - 1 >= cap) {
-    atomicOr(err, CSA_DEV_CAPACITY);
-    ok = 0;
-  }
-  flags[b] = ok;
 }
 
 // out[tok][o] = sum_k W[o][k] x[tok][k]; W = [wkv ; wgate] (2*Ld rows).  One warp
@@ -80,10 +66,23 @@ __global__ void __launch_bounds__(256) k_project_simt(const T* __restrict__ x, c
 }
 
 // One block per (completed window i of this call, sequence b).
+// Per-sequence state check of a compress call: n_rows == pos/ratio and every
+// row the call emits fits the pool.  Returns the error bit (0 = valid).
+__device__ __forceinline__ int compress_state_error(int p0, int n, int T_, int ratio, int cap) {
+  if (p0 < 0 || n != p0 / ratio) return CSA_DEV_STATE;
+  if ((long long)(p0 + (long long)T_) / ratio - 1 >= cap) return CSA_DEV_CAPACITY;
+  return 0;
+}
+
+// One block per (completed window i of this call, sequence b).  Block (0, b)
+// publishes the sequence's validity (flags[b], error word).  With fuse_finish
+// (single-token calls) it also writes the new token's frontier slot and advances
+// n_rows: a single new token's slot never holds a token some window still reads.
 template <typename T>
-__global__ void __launch_bounds__(256) k_pool_emit(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos,
+__global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, const int32_t* __restrict__ pos,
+                                                   int32_t* __restrict__ n_rows, int32_t* err, int fuse_finish,
                                                    int T_, int ratio, int lanes, int d, int R, int F,
-                                                   const T* __restrict__ frontier, const T* __restrict__ proj,
+                                                   T* __restrict__ frontier, const T* __restrict__ proj,
                                                    const float* __restrict__ ape, const float* __restrict__ norm_w,
                                                    float eps, const float* __restrict__ inv_freq,
                                                    T* __restrict__ pool, int cap) {
@@ -92,11 +91,28 @@ __global__ void __launch_bounds__(256) k_pool_emit(const int32_t* __restrict__ f
   float* y = sm_pool + d;
   float* red = sm_pool + 2 * d;
   const int b = blockIdx.y;
-  if (!flags[b]) return;
   const int p0 = pos[b];
+  const int bad = compress_state_error(p0, n_rows[b], T_, ratio, cap);
+  if (blockIdx.x == 0) {
+    __syncthreads();  // every thread of this block has read n_rows before thread 0 may advance it
+    if (threadIdx.x == 0) {
+      flags[b] = !bad;
+      if (bad) atomicOr(err, bad);
+    }
+    if (fuse_finish && !bad) {
+      const int rowlen = 2 * lanes * d;
+      const T* src = proj + (size_t)b * rowlen;
+      T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
+      for (int e = threadIdx.x * 8; e < rowlen; e += blockDim.x * 8) copy8<T>(dst + e, src + e);
+    }
+  }
+  if (bad) return;
   const int first = p0 + (ratio - 1 - p0 % ratio);  // first token completing a window
   const int p = first + blockIdx.x * ratio;
-  if (p >= p0 + T_) return;
+  if (p >= p0 + T_) {
+    if (fuse_finish && blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
+    return;
+  }
   const int j = (p + 1) / ratio - 1;
   const int Ld = lanes * d;
   const size_t rowlen = 2 * (size_t)Ld;
@@ -144,6 +160,7 @@ __global__ void __launch_bounds__(256) k_pool_emit(const int32_t* __restrict__ f
     }
     dst[c] = from_f<T>(v);
   }
+  if (fuse_finish && blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
 }
 
 // Rewrite the frontier slots of the newest min(T, F) tokens; block (0, b) advances n_rows.
@@ -167,7 +184,6 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
                               const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                               const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s) {
   const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
-  k_compress_validate<<<(B + 127) / 128, 128, 0, s>>>(pos, n_rows, B, T_, L.ratio, cap, ws.flags, err); count_launches(1);
   const int ntok = B * T_;
   if (tc_project_supported(L, d)) {
     cudaError_t e = launch_tc_project(L, d, x, ntok, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets, err, s);
@@ -181,12 +197,16 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
   dim3 ge(maxwin, B);
   size_t smem = (2 * (size_t)d + 32) * sizeof(float);
-  k_pool_emit<T><<<ge, 256, smem, s>>>(ws.flags, pos, T_, L.ratio, L.lanes, d, L.R, L.F,
-                                       static_cast<const T*>(frontier), static_cast<const T*>(ws.proj), comp.ape,
+  const int fuse = (T_ == 1);
+  k_pool_emit<T><<<ge, 256, smem, s>>>(ws.flags, pos, n_rows, err, fuse, T_, L.ratio, L.lanes, d, L.R, L.F,
+                                       static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape,
                                        comp.norm_w, L.eps, inv_freq, static_cast<T*>(pool), cap); count_launches(1);
-  dim3 gf(min(T_, L.F), B);
-  k_compress_finish<T><<<gf, 128, 0, s>>>(ws.flags, pos, T_, L.ratio, L.F, rowlen, static_cast<const T*>(ws.proj),
-                                          static_cast<T*>(frontier), n_rows); count_launches(1);
+  if (!fuse) {
+    dim3 gf(min(T_, L.F), B);
+    k_compress_finish<T><<<gf, 128, 0, s>>>(ws.flags, pos, T_, L.ratio, L.F, rowlen,
+                                            static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows);
+    count_launches(1);
+  }
   return cudaGetLastError();
 }
 

@@ -212,6 +212,122 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
   if (threadIdx.x == 0) n_sel[q] = min(out_base, topk);
 }
 
+// Inclusive prefix sum over the 1024 threads of the block (one value each).
+__device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __syncthreads();
+  if (lane == 31) warp_tot[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  return v + (wid > 0 ? warp_tot[wid - 1] : 0);
+}
+
+// Exact top-k with the keys resident in shared memory: radix select of the
+// k-th largest order key over digits of 11, 11 and 10 bits (2048-bin
+// histograms; the bucket holding the k-th key is found by a block-wide scan
+// over the bins in descending order), then one ascending pass that keeps the
+// keys above the threshold and the lowest-indexed keys equal to it.
+__global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ scores, int cap,
+                                                    const int32_t* __restrict__ n_rows,
+                                                    const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
+                                                    int32_t* __restrict__ sel, int32_t* __restrict__ n_sel) {
+  extern __shared__ uint32_t sm_keys[];  // [cap] keys, then hist[2048]
+  int* hist = reinterpret_cast<int*>(sm_keys + cap);
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int p = query_pos(pos, pos0, q);
+  const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
+  int32_t* out = sel + (size_t)q * topk;
+  if (nvis <= topk) {
+    for (int i = threadIdx.x; i < topk; i += blockDim.x) out[i] = (i < nvis) ? i : -1;
+    if (threadIdx.x == 0) n_sel[q] = max(nvis, 0);
+    return;
+  }
+  const float* sc = scores + (size_t)q * cap;
+  for (int j = threadIdx.x; j < nvis; j += blockDim.x) sm_keys[j] = ord_key(__ldg(sc + j));
+  uint32_t prefix = 0, mask = 0;
+  int need = topk;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
+      const uint32_t u = sm_keys[j];
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1);
+    }
+    __syncthreads();
+    // thread t owns bins 2047-2t and 2046-2t (descending order)
+    const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
+    const int c_hi = hist[b_hi], c_lo = hist[b_lo];
+    const int incl = block_incl_scan(c_hi + c_lo, warp_tot);
+    const int excl = incl - c_hi - c_lo;
+    if (excl < need && need <= incl) {
+      if (excl + c_hi >= need) {
+        s_prefix = prefix | ((uint32_t)b_hi << shift);
+        s_need = need - excl;
+      } else {
+        s_prefix = prefix | ((uint32_t)b_lo << shift);
+        s_need = need - excl - c_hi;
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= dmask << shift;
+  }
+  int eq_base = 0, out_base = 0;
+  for (int j0 = 0; j0 < nvis; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    const uint32_t u = (j < nvis) ? sm_keys[j] : 0u;
+    const int eq = (j < nvis) && (u == prefix);
+    const int gt = (j < nvis) && (u > prefix);
+    const int eq_rank = eq_base + block_excl_count(eq, warp_tot, &s_total);
+    const int eq_tot = s_total;
+    const int take = gt || (eq && eq_rank < need);
+    const int slot = out_base + block_excl_count(take, warp_tot, &s_total);
+    const int take_tot = s_total;
+    if (take && slot < topk) out[slot] = j;
+    eq_base += eq_tot;
+    out_base += take_tot;
+  }
+  for (int i = out_base + threadIdx.x; i < topk; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) n_sel[q] = min(out_base, topk);
+}
+
+constexpr int kTopkSmemMaxCap = 52 * 1024;
+
+static void launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
+                        int pos0, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
+  if (cap <= kTopkSmemMaxCap) {
+    const size_t smem = (size_t)cap * 4 + 2048 * 4;
+    cudaFuncSetAttribute(k_topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_topk_smem<<<Q, 1024, smem, s>>>(scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+  } else {
+    k_topk<<<Q, 1024, 0, s>>>(scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+  }
+  count_launches(1);
+}
+
 template <typename T>
 static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
                            const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq, int32_t* sel,
@@ -220,7 +336,7 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
     cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q : 1, cap, n_rows, pos, pos0, inv_freq, ws.qr,
                                            ws.scores, err, s);
     if (e != cudaSuccess) return e;
-    k_topk<<<Q, 1024, 0, s>>>(ws.scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel); count_launches(1);
+    launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
     return cudaGetLastError();
   }
   k_rope_iq<T><<<Q, 256, 0, s>>>(static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, inv_freq, ws.qr); count_launches(1);
@@ -229,7 +345,7 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
   size_t smem = (64 * (size_t)(L.Di + 4) + 64 * (size_t)L.Di + 16 * 64 + 64) * sizeof(float);
   k_index_scores<T><<<g, 256, smem, s>>>(ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
                                          cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores); count_launches(1);
-  k_topk<<<Q, 1024, 0, s>>>(ws.scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel); count_launches(1);
+  launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kPThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kMaxSplits = 8;
 
 struct PjArgs {
   int ntok, X, Ld, N, n_kblk, splits;  // n_kblk: 64-wide K blocks per split
@@ -142,13 +143,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   if (!*s_last) return;
   __threadfence();
-  for (int e = threadIdx.x; e < 128 * N; e += blockDim.x) {
-    const int r = e / N, c = e % N;
+  // 4 tokens per task; every split's float4 is loaded before the (split-ordered) sum
+  for (int e = threadIdx.x; e < 128 * (N / 4); e += blockDim.x) {
+    const int r = e / (N / 4), c = (e % (N / 4)) * 4;
     const int o = m * 128 + r, tok = n * N + c;
-    if (tok >= a.ntok) continue;
-    float acc = 0.f;
-    for (int s = 0; s < a.splits; ++s) acc += __ldcg(a.part + ((size_t)s * 2 * a.Ld + o) * a.n_cols + tok);
-    a.proj[(size_t)tok * 2 * a.Ld + o] = __float2bfloat16_rn(acc);
+    float4 v[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < a.splits)
+        v[s] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)s * 2 * a.Ld + o) * a.n_cols + tok));
+    float4 acc = v[0];
+#pragma unroll
+    for (int s = 1; s < kMaxSplits; ++s)
+      if (s < a.splits) {
+        acc.x += v[s].x;
+        acc.y += v[s].y;
+        acc.z += v[s].z;
+        acc.w += v[s].w;
+      }
+    const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (tok + i < a.ntok) a.proj[(size_t)(tok + i) * 2 * a.Ld + o] = __float2bfloat16_rn(f[i]);
   }
 }
 
@@ -167,7 +183,7 @@ PjPlan plan_project(const Dims& L, int d, int ntok) {
   const int base = p.m_tiles * p.n_tiles;
   const int kblk = L.X / 64;
   p.splits = 1;
-  while (base * p.splits * 2 <= 160 && p.splits * 2 <= kblk && (kblk % (p.splits * 2)) == 0) p.splits *= 2;
+  while (base * p.splits * 2 <= 160 && p.splits * 2 <= kMaxSplits && (kblk % (p.splits * 2)) == 0) p.splits *= 2;
   return p;
 }
 
