@@ -22,7 +22,8 @@ DEV_CAPACITY, DEV_STATE, DEV_RANGE = 1, 2, 4
 CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
-           "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string")
+           "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
+           "csa_index_topk_static")
 
 
 class CSAError(RuntimeError):
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_compress_append.restype = i32
     lib.csa_index_topk.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.csa_index_topk.restype = i32
+    lib.csa_static_scratch_bytes.argtypes = []
+    lib.csa_static_scratch_bytes.restype = sz
+    lib.csa_index_topk_static.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_index_topk_static.restype = i32
     lib.csa_attend_decode.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.csa_attend_decode.restype = i32
     lib.csa_attend_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, ctypes.c_int32, vp, vp, vp, i32, vp, vp,
@@ -192,6 +197,21 @@ def index_topk(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, w
         ctypes.byref(L), _ptr(iq), _ptr(iw), B, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
         _ptr(sel), _ptr(n_sel), _ptr(ws), nb, _ptr(err), _stream(stream)))
     return err
+
+
+def index_topk_static(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err=None, stream=None):
+    """csa_index_topk_static: the decode indexer with the library's own fixed scratch array (no workspace)."""
+    B, cap = iq.shape[0], ikeys.shape[1]
+    err = _err(err, iq.device)
+    L = layer._c()
+    _check("csa_index_topk_static", load_library().csa_index_topk_static(
+        ctypes.byref(L), _ptr(iq), _ptr(iw), B, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
+        _ptr(sel), _ptr(n_sel), _ptr(err), _stream(stream)))
+    return err
+
+
+def static_scratch_bytes() -> int:
+    return int(load_library().csa_static_scratch_bytes())
 
 
 def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq, out, ws=None,

@@ -216,6 +216,33 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                     const float* inv_freq, void* out, int32_t* sel_out, void* ws, size_t ws_bytes,
                                     int32_t* err, void* stream);
 
+/* csa_index_topk_static — csa_index_topk without a caller-supplied workspace.
+ *
+ * No counterpart in the paper: this is a calling convention, not a step of the
+ * method.  Some callers cannot allocate device memory at the point where they
+ * run the indexer: code running inside a region whose allocator is frozen (a
+ * serving engine that reserves all device memory up front and hands out no
+ * scratch, or a runtime that forbids cudaMalloc and its implicit device-wide
+ * synchronisation on a latency-critical decode path), or a plain C caller with
+ * no allocator of its own.  This entry point takes its scratch memory from a
+ * file-scope device array of csa_static_scratch_bytes() bytes (4 MiB) inside
+ * the library; it allocates and frees nothing.
+ *   - Arguments, results and errors are those of csa_index_topk, without ws.
+ *   - Returns CSA_ERR_WORKSPACE when the call needs more scratch than the array
+ *     holds (csa_workspace_size(..., CSA_OP_INDEX_TOPK, B, 1, cap) bytes; about
+ *     B * (Hi*Di*4 + cap*4) — e.g. 32 sequences with 8400-row pools fit).
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array: calls whose kernels overlap
+ *     on the GPU (different streams without ordering) race on it.  Calls in one
+ *     stream are ordered and safe.  Nothing in the array needs to start at zero;
+ *     it keeps the last call's contents.
+ *   - Every GPU that loads the library holds the array until the process exits. */
+size_t csa_static_scratch_bytes(void);
+csa_status csa_index_topk_static(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys,
+                                 int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
+                                 int32_t* sel, int32_t* n_sel, int32_t* err, void* stream);
+
 /* Number of kernels this library has enqueued in this process (all calls,
  * all devices).  Diagnostic only: lets a caller count the launches of a region. */
 unsigned long long csa_kernel_launches(void);
