@@ -376,17 +376,14 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
                             const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
                             const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,
                             const AttendWs& ws, int32_t* err, cudaStream_t s) {
+  if (tc_attend_supported(L)) {
+    cudaError_t e = launch_tc_attend(L, q, pool, window, nullptr, kv_new, sel, n_sel, n_rows, pos, 0, cap, sink,
+                                     inv_freq, B, ws.S, ws.part_ml, ws.part_acc, out, err, s);
+    if (e != cudaSuccess || ws.S == 1) return e;
+    return launch_tc_merge(L, ws.part_ml, ws.part_acc, ws.S, B, sink, pos, inv_freq, out, s);
+  }
   k_window_append<T><<<B, 128, 0, s>>>(static_cast<const T*>(kv_new), static_cast<T*>(window), L.W, L.D, L.R, pos,
                                        inv_freq); count_launches(1);
-  if (tc_attend_supported(L)) {
-    cudaError_t e = launch_tc_attend(L, q, pool, window, nullptr, sel, n_sel, n_rows, pos, 0, cap, sink, inv_freq, B,
-                                     ws.S, ws.part_ml, ws.part_acc, out, err, s);
-    if (e != cudaSuccess || ws.S == 1) return e;
-    dim3 gm(L.H, B);
-    k_attend_merge<T><<<gm, max(32, min(1024, L.D / 8)), ws.S * sizeof(float), s>>>(
-        ws.part_ml, ws.part_acc, ws.S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out)); count_launches(1);
-    return cudaGetLastError();
-  }
   k_rope_rows<T><<<B, 256, 0, s>>>(static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, pos, 0,
                                    inv_freq); count_launches(1);
   AttnArgs a{};
@@ -405,8 +402,8 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   k_rope_rows<T><<<T_, 256, 0, s>>>(static_cast<const T*>(kv_new), static_cast<T*>(ws.kvr), 1, L.D, L.R, nullptr,
                                     pos0, inv_freq); count_launches(1);
   if (tc_attend_supported(L)) {
-    cudaError_t e = launch_tc_attend(L, q, pool, window, ws.kvr, sel, n_sel, n_rows, nullptr, pos0, cap, sink,
-                                     inv_freq, T_, 1, nullptr, nullptr, out, err, s);
+    cudaError_t e = launch_tc_attend(L, q, pool, window, ws.kvr, nullptr, sel, n_sel, n_rows, nullptr, pos0, cap,
+                                     sink, inv_freq, T_, 1, nullptr, nullptr, out, err, s);
     if (e != cudaSuccess) return e;
     k_window_store_chunk<T><<<min(T_, L.W), 64, 0, s>>>(static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
                                                         L.D, T_, pos0); count_launches(1);

@@ -81,10 +81,14 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
 bool tc_attend_supported(const Dims& L);
 // Q queries (decode: pos[q], ring[q], pool[q]; prefill: pos == null, positions pos0 + q, batch 1, chunk rows
 // kvr), S key splits per query: S > 1 writes (m, l, acc) partials, S == 1 the final output.
-cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, const void* ring, const void* kvr,
-                             const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows, const int32_t* pos,
-                             int pos0, int cap, const float* sink, const float* inv_freq, int Q, int S,
-                             float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
+// Decode passes kv_new: the CTA that owns the new token's row ropes it and writes its ring slot.
+cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, void* ring, const void* kvr,
+                             const void* kv_new, const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
+                             const int32_t* pos, int pos0, int cap, const float* sink, const float* inv_freq, int Q,
+                             int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
+// Merge of decode split partials for H % 8 == 0, D == 512 (one warp per head, 16 dims per lane).
+cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
+                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s);
 
 // ---- attend.cu
 struct AttendWs {

@@ -64,6 +64,8 @@ struct AtArgs {
   const __nv_bfloat16* pool;  // [B, cap, 512]
   const __nv_bfloat16* ring;  // [B, W, 512]
   const __nv_bfloat16* kvr;   // [T, 512] roped chunk rows (prefill) or null
+  const __nv_bfloat16* kv_new;  // [B, 512] decode: the new token before RoPE (written to the ring here)
+  __nv_bfloat16* ring_out;      // decode: the ring, for the new token's slot
   const int32_t* sel;         // [Q, topk] or null
   const int32_t* n_sel;
   const int32_t* n_rows;
@@ -227,9 +229,10 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
       lsum[tid] = 0.f;
     }
     tc::named_bar(1, kMain);
-    // query block: 128-byte swizzled K-major rows (one per head), copied with cp.async (all in flight),
-    // then RoPE on the last 64 dims in place, in bf16
-    {
+    // query block: 128-byte swizzled K-major rows (one per head), copied with cp.async; the copy is waited
+    // for together with the first tile's rows, then RoPE is applied in place (bf16)
+    const bool q_pending_init = it.t_end > it.t_begin;
+    if (q_pending_init) {
       const uint32_t q_base = tc::smem_u32(qbuf);
       const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
 #pragma unroll 8
@@ -238,24 +241,8 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
         tc::cp_async16(q_base + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4), qsrc + (size_t)h * kAD + c * 8,
                        16u);
       }
-      tc::cp_async_wait_all();
     }
-    tc::named_bar(1, kMain);
-#pragma unroll
-    for (int e = tid; e < kAH * 8; e += kMain) {
-      const int h = e >> 3, c = 56 + (e & 7);
-      uint4* slot = reinterpret_cast<uint4*>(qbuf + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4));
-      uint4 raw = *slot;
-      __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = (c - 56) * 4 + k;
-        const float2 x = __bfloat1622float2(hv[k]);
-        hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
-      }
-      *slot = raw;
-    }
-    tc::fence_proxy_async_smem();
+    bool q_pending = q_pending_init;
 
     for (int t = it.t_begin; t < it.t_end; ++t) {
       const uint32_t par = n_tiles_done & 1;
@@ -272,8 +259,10 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
             else atomicOr(a.err, CSA_DEV_RANGE);
           } else {
             const int tok = it.p - it.nwin + 1 + (r - it.nsel);
-            ptr = (a.kvr && tok >= a.pos0) ? a.kvr + (size_t)(tok - a.pos0) * kAD
-                                           : a.ring + ((size_t)it.b * a.W + (tok % a.W)) * kAD;
+            if (a.kv_new && tok == it.p) ptr = a.kv_new + (size_t)it.b * kAD;  // roped below, also into the ring
+            else
+              ptr = (a.kvr && tok >= a.pos0) ? a.kvr + (size_t)(tok - a.pos0) * kAD
+                                             : a.ring + ((size_t)it.b * a.W + (tok % a.W)) * kAD;
           }
         }
         rowp[tid] = ptr;
@@ -281,10 +270,31 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
       tc::named_bar(1, kMain);
       // ---- gather: warp w copies rows 32w .. 32w+31, 2 x 512 contiguous bytes per instruction
       const uint32_t r_base = tc::smem_u32(rows);
+      const __nv_bfloat16* cur = (a.kv_new && it.p >= 0) ? a.kv_new + (size_t)it.b * kAD : nullptr;
 #pragma unroll 4
       for (int rr = 0; rr < 32; ++rr) {
         const int r = warp * 32 + rr;
         const __nv_bfloat16* src = rowp[r];
+        if (cur && src == cur) {
+          // the new token: RoPE at p, into the tile and into its ring slot
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = lane + 32 * hh;
+            uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
+            if (c >= 56) {
+              __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int i = (c - 56) * 4 + k;
+                const float2 x = __bfloat1622float2(hv[k]);
+                hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
+              }
+            }
+            *reinterpret_cast<uint4*>(rows + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = raw;
+            *reinterpret_cast<uint4*>(a.ring_out + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + c * 8) = raw;
+          }
+          continue;
+        }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int c = lane + 32 * hh;
@@ -294,6 +304,24 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
         }
       }
       tc::cp_async_wait_all();
+      if (q_pending) {
+        tc::named_bar(1, kMain);  // every thread's share of the query block has landed
+#pragma unroll
+        for (int e = tid; e < kAH * 8; e += kMain) {
+          const int h = e >> 3, c = 56 + (e & 7);
+          uint4* slot = reinterpret_cast<uint4*>(qbuf + (c >> 3) * kQBox + h * 128 + (((c & 7) ^ (h & 7)) << 4));
+          uint4 raw = *slot;
+          __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i = (c - 56) * 4 + k;
+            const float2 x = __bfloat1622float2(hv[k]);
+            hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
+          }
+          *slot = raw;
+        }
+        q_pending = false;
+      }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       tc::mbar_arrive(rows_full);
@@ -469,16 +497,89 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
   if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Merge of S split partials for 8 heads of one query: warp w owns head 8*blockIdx.x + w, lane owns latent
+// dims 16*lane .. 16*lane+15.  M = max(z, m_s); Z = e^{z-M} + sum_s l_s e^{m_s-M}; o = sum_s acc_s e^{m_s-M} / Z;
+// bf16; inverse RoPE on the last 64 dims; bf16.  Every split's float4 loads are issued before they are used.
+__global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part_ml, const float* __restrict__ part_acc,
+                                                  int S, const float* __restrict__ sink, const int32_t* __restrict__ pos,
+                                                  const float* __restrict__ inv_freq, __nv_bfloat16* __restrict__ out) {
+  __shared__ float rc[32], rs[32];
+  const int q = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + warp;
+  const int p = pos[q];
+  if (threadIdx.x < 32) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
+  // split statistics: lane s holds split s (S <= 32 handled in rounds of 32)
+  const float z = sink[h];
+  float M = z;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    const float m = s < S ? part_ml[(((size_t)q * S + s) * kAH + h) * 2] : -INFINITY;
+    M = fmaxf(M, warp_max(m));
+  }
+  float Z = expf(z - M);
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    float t = 0.f;
+    if (s < S) {
+      const size_t idx = ((size_t)q * S + s) * kAH + h;
+      const float m = part_ml[idx * 2];
+      t = m == -INFINITY ? 0.f : part_ml[idx * 2 + 1] * expf(m - M);
+    }
+    Z += warp_sum(t);
+  }
+  float v[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) v[e] = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const size_t idx = ((size_t)q * S + s) * kAH + h;
+    const float m = __ldg(part_ml + idx * 2);
+    if (m == -INFINITY) continue;
+    const float f = expf(m - M);
+    const float4* pa = reinterpret_cast<const float4*>(part_acc + idx * kAD + lane * 16);
+    float4 x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = __ldcg(pa + k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[4 * k] = fmaf(x[k].x, f, v[4 * k]);
+      v[4 * k + 1] = fmaf(x[k].y, f, v[4 * k + 1]);
+      v[4 * k + 2] = fmaf(x[k].z, f, v[4 * k + 2]);
+      v[4 * k + 3] = fmaf(x[k].w, f, v[4 * k + 3]);
+    }
+  }
+  __syncthreads();
+  const float invZ = 1.0f / Z;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) v[e] = rnd<__nv_bfloat16>(v[e] * invZ);
+  const int d0 = lane * 16;
+  if (d0 >= kAD - 64) {
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int i = (d0 + e - (kAD - 64)) >> 1;
+      const float x0 = v[e], x1 = v[e + 1];
+      v[e] = fmaf(x0, rc[i], x1 * rs[i]);
+      v[e + 1] = fmaf(-x0, rs[i], x1 * rc[i]);
+    }
+  }
+  uint4 pk[2];
+  __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) hv[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+  uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)q * kAH + h) * kAD + d0);
+  dst[0] = pk[0];
+  dst[1] = pk[1];
+}
+
 int g_sms_at = 0;
 
 }  // namespace
 
 bool tc_attend_supported(const Dims& L) { return L.dtype == CSA_BF16 && L.H == 64 && L.D == 512 && L.R == 64; }
 
-cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, const void* ring, const void* kvr,
-                             const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows, const int32_t* pos,
-                             int pos0, int cap, const float* sink, const float* inv_freq, int Q, int S,
-                             float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s) {
+cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, void* ring, const void* kvr,
+                             const void* kv_new, const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
+                             const int32_t* pos, int pos0, int cap, const float* sink, const float* inv_freq, int Q,
+                             int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s) {
   if (!g_sms_at) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -489,6 +590,8 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, con
   a.pool = static_cast<const __nv_bfloat16*>(pool);
   a.ring = static_cast<const __nv_bfloat16*>(ring);
   a.kvr = static_cast<const __nv_bfloat16*>(kvr);
+  a.kv_new = static_cast<const __nv_bfloat16*>(kv_new);
+  a.ring_out = static_cast<__nv_bfloat16*>(ring);
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq;
   a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.ratio = L.ratio; a.Q = Q; a.S = S;
   a.scale2 = L.scale * 1.4426950408889634f;
@@ -499,6 +602,15 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, con
   const int grid = pos ? items : min(items, g_sms_at);
   cudaFuncSetAttribute(k_tc_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAt);
   k_tc_attend<<<grid, kThreadsAt, kSmemAt, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
+                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s) {
+  (void)L;
+  k_tc_merge<<<dim3(kAH / 8, Q), 256, 0, s>>>(part_ml, part_acc, S, sink, pos, inv_freq,
+                                               static_cast<__nv_bfloat16*>(out));
   count_launches(1);
   return cudaGetLastError();
 }
