@@ -322,6 +322,8 @@ def run_ours(args):
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     idx_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    phase_us = {name: round(1e3 * statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev), 2)
+                for k, name in enumerate(("compress_x2", "index_topk", "attend"))}
     total_ms = _max_over_ranks(dist, sum(step_ms), dev)
     assert wl.err.item() == 0, f"device error word {wl.err.item()}"
     n_end = wl.n_a.float().mean().item()
@@ -379,6 +381,7 @@ def run_ours(args):
                 "step_hbm_gbs": round(nb["total"] / (ms_per_step / 1e3) / 1e9, 1),
                 "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
                 "l2": "flushed (512 MB write) before every timed step, outside the events",
+                "phase_us": phase_us,
                 "launch": ("kernels launched one by one" if args.eager else
                            "each step = 3 CUDA graph replays (compress x2 on two streams | indexer | attention)"),
                 "prefill": prefill,

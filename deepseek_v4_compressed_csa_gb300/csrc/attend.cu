@@ -52,6 +52,8 @@ AttendWs carve_attend(Carver& c, const Dims& L, int Q, int S, int T) {
 template <typename T>
 __global__ void k_rope_rows(const T* __restrict__ src, T* __restrict__ dst, int rows_per_q, int D, int R,
                             const int32_t* __restrict__ pos, int pos0, const float* __restrict__ inv_freq) {
+  pdl_trigger();
+  pdl_wait();
   const int q = blockIdx.x;
   const int p = pos ? pos[q] : pos0 + q;
   const size_t base = (size_t)q * rows_per_q * D;
@@ -74,6 +76,8 @@ __global__ void k_rope_rows(const T* __restrict__ src, T* __restrict__ dst, int 
 template <typename T>
 __global__ void k_window_append(const T* __restrict__ kv, T* __restrict__ window, int W, int D, int R,
                                 const int32_t* __restrict__ pos, const float* __restrict__ inv_freq) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int p = pos[b];
   if (p < 0) return;
@@ -96,6 +100,8 @@ __global__ void k_window_append(const T* __restrict__ kv, T* __restrict__ window
 template <typename T>
 __global__ void k_window_store_chunk(const T* __restrict__ kvr, T* __restrict__ window, int W, int D, int T_,
                                      int pos0) {
+  pdl_trigger();
+  pdl_wait();
   const int keep = min(T_, W);
   const int t = pos0 + T_ - keep + blockIdx.x;
   for (int e = threadIdx.x * 8; e < D; e += blockDim.x * 8)
@@ -124,6 +130,8 @@ struct AttnArgs {
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_attend_simt(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char sm_attn[];
   const int D = a.D, KS = D + 8;
   T* qs = reinterpret_cast<T*>(sm_attn);                 // [kHG][D]
@@ -306,6 +314,8 @@ template <typename T>
 __global__ void k_attend_merge(const float* __restrict__ part_ml, const float* __restrict__ part_acc, int S, int H,
                                int D, int R, const float* __restrict__ sink, const int32_t* __restrict__ pos,
                                int pos0, const float* __restrict__ inv_freq, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm_merge[];  // [S] scale factors
   const int h = blockIdx.x, q = blockIdx.y;
   const int p = pos ? pos[q] : pos0 + q;
@@ -361,12 +371,12 @@ static cudaError_t run_attend(AttnArgs& a, int Q, cudaStream_t s) {
   const size_t smem = attend_smem<T>(a.D);
   cudaFuncSetAttribute(k_attend_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 g((a.H + kHG - 1) / kHG, a.S, Q);
-  k_attend_simt<T><<<g, 256, smem, s>>>(a); count_launches(1);
+  CSA_LAUNCH(k_attend_simt<T>, dim3(g), dim3(256), smem, s, a);
   if (a.S > 1) {
     dim3 gm(a.H, Q);
     const int thr = max(32, min(1024, a.D / 8));
-    k_attend_merge<T><<<gm, thr, a.S * sizeof(float), s>>>(a.part_ml, a.part_acc, a.S, a.H, a.D, a.R, a.sink,
-                                                           a.pos, a.pos0, a.inv_freq, static_cast<T*>(a.out)); count_launches(1);
+    CSA_LAUNCH(k_attend_merge<T>, dim3(gm), dim3(thr), a.S * sizeof(float), s, a.part_ml, a.part_acc, a.S, a.H, a.D, a.R, a.sink,
+                                                           a.pos, a.pos0, a.inv_freq, static_cast<T*>(a.out));
   }
   return cudaGetLastError();
 }
@@ -380,12 +390,15 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
     cudaError_t e = launch_tc_attend(L, q, pool, window, nullptr, kv_new, sel, n_sel, n_rows, pos, 0, cap, sink,
                                      inv_freq, B, ws.S, ws.part_ml, ws.part_acc, out, err, s);
     if (e != cudaSuccess || ws.S == 1) return e;
-    return launch_tc_merge(L, ws.part_ml, ws.part_acc, ws.S, B, sink, pos, inv_freq, out, s);
+    if (ws.S <= 32) return launch_tc_merge(L, ws.part_ml, ws.part_acc, ws.S, B, sink, pos, inv_freq, out, s);
+    CSA_LAUNCH(k_attend_merge<T>, dim3(L.H, B), dim3(max(32, min(1024, L.D / 8))), ws.S * sizeof(float), s,
+               ws.part_ml, ws.part_acc, ws.S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out));
+    return cudaGetLastError();
   }
-  k_window_append<T><<<B, 128, 0, s>>>(static_cast<const T*>(kv_new), static_cast<T*>(window), L.W, L.D, L.R, pos,
-                                       inv_freq); count_launches(1);
-  k_rope_rows<T><<<B, 256, 0, s>>>(static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, pos, 0,
-                                   inv_freq); count_launches(1);
+  CSA_LAUNCH(k_window_append<T>, dim3(B), dim3(128), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(window), L.W, L.D, L.R, pos,
+                                       inv_freq);
+  CSA_LAUNCH(k_rope_rows<T>, dim3(B), dim3(256), 0, s, static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, pos, 0,
+                                   inv_freq);
   AttnArgs a{};
   a.qr = ws.qr; a.pool = pool; a.ring = window; a.kvr = nullptr; a.sel = sel; a.n_sel = n_sel;
   a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq; a.pos0 = 0; a.cap = cap;
@@ -399,18 +412,18 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
                              void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
                              const int32_t* n_sel, const float* inv_freq, void* out, const AttendWs& ws,
                              int32_t* err, cudaStream_t s) {
-  k_rope_rows<T><<<T_, 256, 0, s>>>(static_cast<const T*>(kv_new), static_cast<T*>(ws.kvr), 1, L.D, L.R, nullptr,
-                                    pos0, inv_freq); count_launches(1);
+  CSA_LAUNCH(k_rope_rows<T>, dim3(T_), dim3(256), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(ws.kvr), 1, L.D, L.R, nullptr,
+                                    pos0, inv_freq);
   if (tc_attend_supported(L)) {
     cudaError_t e = launch_tc_attend(L, q, pool, window, ws.kvr, nullptr, sel, n_sel, n_rows, nullptr, pos0, cap,
                                      sink, inv_freq, T_, 1, nullptr, nullptr, out, err, s);
     if (e != cudaSuccess) return e;
-    k_window_store_chunk<T><<<min(T_, L.W), 64, 0, s>>>(static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
-                                                        L.D, T_, pos0); count_launches(1);
+    CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.W)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
+                                                        L.D, T_, pos0);
     return cudaGetLastError();
   }
-  k_rope_rows<T><<<T_, 256, 0, s>>>(static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, nullptr, pos0,
-                                    inv_freq); count_launches(1);
+  CSA_LAUNCH(k_rope_rows<T>, dim3(T_), dim3(256), 0, s, static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, nullptr, pos0,
+                                    inv_freq);
   AttnArgs a{};
   a.qr = ws.qr; a.pool = pool; a.ring = window; a.kvr = ws.kvr; a.sel = sel; a.n_sel = n_sel;
   a.n_rows = n_rows; a.pos = nullptr; a.sink = sink; a.inv_freq = inv_freq; a.pos0 = pos0; a.cap = cap;
@@ -418,8 +431,8 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   a.S = ws.S; a.part_ml = ws.part_ml; a.part_acc = ws.part_acc; a.out = out; a.err = err;
   cudaError_t e = run_attend<T>(a, T_, s);
   if (e != cudaSuccess) return e;
-  k_window_store_chunk<T><<<min(T_, L.W), 64, 0, s>>>(static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
-                                                      L.D, T_, pos0); count_launches(1);
+  CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.W)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
+                                                      L.D, T_, pos0);
   return cudaGetLastError();
 }
 

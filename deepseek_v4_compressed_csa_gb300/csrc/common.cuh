@@ -80,6 +80,14 @@ __device__ __forceinline__ void rope_cs(int p, const float* inv_freq, int i, flo
   sincosf(th, s, c);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel is launched with programmatic stream serialization: it lets the
+// next kernel in the stream start its prologue early (trigger), and itself
+// touches no global memory written or read by its predecessor before the
+// predecessor has completed (wait).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -37,6 +37,8 @@ template <typename T, int NTOK>
 __global__ void __launch_bounds__(256) k_project_simt(const T* __restrict__ x, const T* __restrict__ wkv,
                                                       const T* __restrict__ wg, int ntok, int X, int Ld,
                                                       T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int o = blockIdx.x * 8 + warp;
   if (o >= 2 * Ld) return;
@@ -85,14 +87,19 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
                                                    T* __restrict__ frontier, const T* __restrict__ proj,
                                                    const float* __restrict__ ape, const float* __restrict__ norm_w,
                                                    float eps, const float* __restrict__ inv_freq,
-                                                   T* __restrict__ pool, int cap) {
-  extern __shared__ float sm_pool[];  // [d] pooled values, then [d] normed values, + 32 reduction slots
+                                                   T* __restrict__ pool, int cap, const float* __restrict__ part,
+                                                   int splits, int part_stride) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ float sm_pool[];  // [d] pooled, [d] normed, 32 reduction slots, [2*L*d] new token (part)
   float* u = sm_pool;
   float* y = sm_pool + d;
   float* red = sm_pool + 2 * d;
+  float* cur = sm_pool + 2 * d + 32;
   const int b = blockIdx.y;
   const int p0 = pos[b];
   const int bad = compress_state_error(p0, n_rows[b], T_, ratio, cap);
+  const int rowlen = 2 * lanes * d;
   if (blockIdx.x == 0) {
     __syncthreads();  // every thread of this block has read n_rows before thread 0 may advance it
     if (threadIdx.x == 0) {
@@ -100,10 +107,31 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
       if (bad) atomicOr(err, bad);
     }
     if (fuse_finish && !bad) {
-      const int rowlen = 2 * lanes * d;
-      const T* src = proj + (size_t)b * rowlen;
       T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
-      for (int e = threadIdx.x * 8; e < rowlen; e += blockDim.x * 8) copy8<T>(dst + e, src + e);
+      if (part) {
+        // single new token with split-K partials: sum them in split order, round once to the model dtype
+        for (int e = threadIdx.x * 4; e < rowlen; e += blockDim.x * 4) {
+          float4 acc = __ldcg(reinterpret_cast<const float4*>(part + (size_t)b * rowlen + e));
+          for (int sp = 1; sp < splits; ++sp) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)sp * part_stride + b) * rowlen + e));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const T r = from_f<T>(f[i]);
+            dst[e + i] = r;
+            cur[e + i] = to_f(r);
+          }
+        }
+        __syncthreads();
+      } else {
+        const T* src = proj + (size_t)b * rowlen;
+        for (int e = threadIdx.x * 8; e < rowlen; e += blockDim.x * 8) copy8<T>(dst + e, src + e);
+      }
     }
   }
   if (bad) return;
@@ -115,7 +143,6 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
   }
   const int j = (p + 1) / ratio - 1;
   const int Ld = lanes * d;
-  const size_t rowlen = 2 * (size_t)Ld;
   const T* fr = frontier + (size_t)b * F * rowlen;
   const T* pj = proj + (size_t)b * T_ * rowlen;
 
@@ -127,18 +154,33 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
     const int t_hi = (j + 1) * ratio;
     for (int t = t_lo; t < t_hi; ++t) {
       const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
-      const T* row = (t < p0) ? fr + (size_t)(t % F) * rowlen : pj + (size_t)(t - p0) * rowlen;
-      float s = to_f(row[Ld + l * d + c]) + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
+      float g;
+      if (t < p0) g = to_f(fr[(size_t)(t % F) * rowlen + Ld + l * d + c]);
+      else if (part) g = cur[Ld + l * d + c];
+      else g = to_f(pj[(size_t)(t - p0) * rowlen + Ld + l * d + c]);
+      const float s = g + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
       m = fmaxf(m, s);
     }
     float num = 0.f, den = 0.f;
     for (int t = t_lo; t < t_hi; ++t) {
       const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
-      const T* row = (t < p0) ? fr + (size_t)(t % F) * rowlen : pj + (size_t)(t - p0) * rowlen;
-      float s = to_f(row[Ld + l * d + c]) + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
+      float g, kv;
+      if (t < p0) {
+        const T* row = fr + (size_t)(t % F) * rowlen;
+        g = to_f(row[Ld + l * d + c]);
+        kv = to_f(row[l * d + c]);
+      } else if (part) {
+        g = cur[Ld + l * d + c];
+        kv = cur[l * d + c];
+      } else {
+        const T* row = pj + (size_t)(t - p0) * rowlen;
+        g = to_f(row[Ld + l * d + c]);
+        kv = to_f(row[l * d + c]);
+      }
+      const float s = g + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
       float e = expf(s - m);
       den += e;
-      num = fmaf(e, to_f(row[l * d + c]), num);
+      num = fmaf(e, kv, num);
     }
     float uc = rnd<T>(num / den);
     u[c] = uc;
@@ -168,6 +210,8 @@ template <typename T>
 __global__ void k_compress_finish(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos, int T_,
                                   int ratio, int F, int rowlen, const T* __restrict__ proj, T* __restrict__ frontier,
                                   int32_t* __restrict__ n_rows) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   if (!flags[b]) return;
   const int p0 = pos[b];
@@ -185,27 +229,36 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
                               const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s) {
   const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
   const int ntok = B * T_;
+  const int fuse = (T_ == 1);
+  // single new token per sequence with split-K partials: the pooling kernel sums them (no fix-up pass)
+  const float* part = nullptr;
+  int splits = 1, part_stride = 0;
   if (tc_project_supported(L, d)) {
-    cudaError_t e = launch_tc_project(L, d, x, ntok, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets, err, s);
+    splits = tc_project_splits(L, d, ntok);
+    const bool consumer_sums = fuse && splits > 1;
+    if (consumer_sums) {
+      part = ws.part;
+      part_stride = tc_project_cols(L, d, ntok);
+    }
+    cudaError_t e = launch_tc_project(L, d, x, ntok, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets,
+                                      !consumer_sums, err, s);
     if (e != cudaSuccess) return e;
   } else {
     dim3 gp((2 * Ld + 7) / 8, (ntok + 7) / 8);
-    k_project_simt<T, 8><<<gp, 256, 0, s>>>(static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
+    CSA_LAUNCH(k_project_simt<T, 8>, dim3(gp), dim3(256), 0, s, static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
                                              static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
-                                             static_cast<T*>(ws.proj)); count_launches(1);
+                                             static_cast<T*>(ws.proj));
   }
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
   dim3 ge(maxwin, B);
-  size_t smem = (2 * (size_t)d + 32) * sizeof(float);
-  const int fuse = (T_ == 1);
-  k_pool_emit<T><<<ge, 256, smem, s>>>(ws.flags, pos, n_rows, err, fuse, T_, L.ratio, L.lanes, d, L.R, L.F,
-                                       static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape,
-                                       comp.norm_w, L.eps, inv_freq, static_cast<T*>(pool), cap); count_launches(1);
+  const size_t smem = (2 * (size_t)d + 32 + (part ? (size_t)rowlen : 0)) * sizeof(float);
+  CSA_LAUNCH(k_pool_emit<T>, dim3(ge), dim3(256), smem, s, ws.flags, pos, n_rows, err, fuse, T_, L.ratio, L.lanes, d,
+             L.R, L.F, static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape, comp.norm_w, L.eps,
+             inv_freq, static_cast<T*>(pool), cap, part, splits, part_stride);
   if (!fuse) {
     dim3 gf(min(T_, L.F), B);
-    k_compress_finish<T><<<gf, 128, 0, s>>>(ws.flags, pos, T_, L.ratio, L.F, rowlen,
+    CSA_LAUNCH(k_compress_finish<T>, dim3(gf), dim3(128), 0, s, ws.flags, pos, T_, L.ratio, L.F, rowlen,
                                             static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows);
-    count_launches(1);
   }
   return cudaGetLastError();
 }

@@ -28,6 +28,8 @@ __device__ __forceinline__ int query_seq(const int32_t* pos, int q) { return pos
 template <typename T>
 __global__ void k_rope_iq(const T* __restrict__ iq, int Hi, int Di, int R, const int32_t* __restrict__ pos, int pos0,
                           const float* __restrict__ inv_freq, float* __restrict__ qr) {
+  pdl_trigger();
+  pdl_wait();
   const int q = blockIdx.x;
   const int p = query_pos(pos, pos0, q);
   for (int e = threadIdx.x; e < Hi * Di; e += blockDim.x) {
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256) k_index_scores(const float* __restrict__ 
                                                       const int32_t* __restrict__ n_rows,
                                                       const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
                                                       float wscale, float* __restrict__ scores) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm_idx[];
   const int q = blockIdx.y, bseq = query_seq(pos, q);
   const int p = query_pos(pos, pos0, q);
@@ -152,6 +156,8 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
                                                const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
                                                int pos0, int ratio, int topk, int32_t* __restrict__ sel,
                                                int32_t* __restrict__ n_sel) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int hist[256];
   __shared__ int warp_tot[32];
   __shared__ int s_total;
@@ -245,6 +251,8 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
                                                     const int32_t* __restrict__ n_rows,
                                                     const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
                                                     int32_t* __restrict__ sel, int32_t* __restrict__ n_sel) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t sm_keys[];  // [cap] keys, then hist[2048]
   int* hist = reinterpret_cast<int*>(sm_keys + cap);
   __shared__ int warp_tot[32];
@@ -295,37 +303,80 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
     need = s_need;
     mask |= dmask << shift;
   }
-  int eq_base = 0, out_base = 0;
-  for (int j0 = 0; j0 < nvis; j0 += blockDim.x) {
-    const int j = j0 + threadIdx.x;
-    const uint32_t u = (j < nvis) ? sm_keys[j] : 0u;
-    const int eq = (j < nvis) && (u == prefix);
-    const int gt = (j < nvis) && (u > prefix);
-    const int eq_rank = eq_base + block_excl_count(eq, warp_tot, &s_total);
-    const int eq_tot = s_total;
-    const int take = gt || (eq && eq_rank < need);
-    const int slot = out_base + block_excl_count(take, warp_tot, &s_total);
-    const int take_tot = s_total;
-    if (take && slot < topk) out[slot] = j;
-    eq_base += eq_tot;
-    out_base += take_tot;
+  // Compaction in ascending row order: warp w owns the contiguous keys [w*per, (w+1)*per).  Pass 1 counts
+  // each warp's keys above / equal to the threshold, one warp turns the counts into output offsets (the
+  // lowest-indexed equal keys are the ones kept), pass 2 writes the rows.
+  __shared__ int w_gt[32], w_eq[32], w_out[32], w_eqbase[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int per = ((nvis + 31) / 32 + 31) & ~31;
+  const int lo = wid * per, hi = min(nvis, lo + per);
+  int gt_n = 0, eq_n = 0;
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t u = j < hi ? sm_keys[j] : 0u;
+    gt_n += __popc(__ballot_sync(0xffffffffu, j < hi && u > prefix));
+    eq_n += __popc(__ballot_sync(0xffffffffu, j < hi && u == prefix));
   }
-  for (int i = out_base + threadIdx.x; i < topk; i += blockDim.x) out[i] = -1;
-  if (threadIdx.x == 0) n_sel[q] = min(out_base, topk);
+  if (lane == 0) {
+    w_gt[wid] = gt_n;
+    w_eq[wid] = eq_n;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    const int e = w_eq[lane];
+    int ei = e;  // inclusive prefix of equal keys
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, ei, o);
+      if (lane >= o) ei += n;
+    }
+    const int eq_before = ei - e;
+    const int eq_taken = max(0, min(e, need - eq_before));
+    const int t = w_gt[lane] + eq_taken;
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += n;
+    }
+    w_out[lane] = ti - t;
+    w_eqbase[lane] = eq_before;
+    if (lane == 31) s_total = ti;
+  }
+  __syncthreads();
+  int slot = w_out[wid], eq_rank = w_eqbase[wid];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t u = j < hi ? sm_keys[j] : 0u;
+    const bool eq = j < hi && u == prefix;
+    const unsigned eqb = __ballot_sync(0xffffffffu, eq);
+    const bool take = (j < hi && u > prefix) || (eq && eq_rank + __popc(eqb & lt) < need);
+    const unsigned tb = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int o = slot + __popc(tb & lt);
+      if (o < topk) out[o] = j;
+    }
+    slot += __popc(tb);
+    eq_rank += __popc(eqb);
+  }
+  const int total = s_total;
+  for (int i2 = total + threadIdx.x; i2 < topk; i2 += blockDim.x) out[i2] = -1;
+  if (threadIdx.x == 0) n_sel[q] = min(total, topk);
 }
 
 constexpr int kTopkSmemMaxCap = 52 * 1024;
 
-static void launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
+static cudaError_t launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
                         int pos0, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
   if (cap <= kTopkSmemMaxCap) {
     const size_t smem = (size_t)cap * 4 + 2048 * 4;
     cudaFuncSetAttribute(k_topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_topk_smem<<<Q, 1024, smem, s>>>(scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+    CSA_LAUNCH(k_topk_smem, dim3(Q), dim3(1024), smem, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
   } else {
-    k_topk<<<Q, 1024, 0, s>>>(scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+    CSA_LAUNCH(k_topk, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
   }
-  count_launches(1);
+  return cudaSuccess;
 }
 
 template <typename T>
@@ -336,17 +387,15 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
     cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q : 1, cap, n_rows, pos, pos0, inv_freq, ws.qr,
                                            ws.scores, err, s);
     if (e != cudaSuccess) return e;
-    launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
-    return cudaGetLastError();
+    return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
   }
-  k_rope_iq<T><<<Q, 256, 0, s>>>(static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, inv_freq, ws.qr); count_launches(1);
+  CSA_LAUNCH(k_rope_iq<T>, dim3(Q), dim3(256), 0, s, static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, inv_freq, ws.qr);
   const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
   dim3 g((cap + 63) / 64, Q);
   size_t smem = (64 * (size_t)(L.Di + 4) + 64 * (size_t)L.Di + 16 * 64 + 64) * sizeof(float);
-  k_index_scores<T><<<g, 256, smem, s>>>(ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
-                                         cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores); count_launches(1);
-  launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
-  return cudaGetLastError();
+  CSA_LAUNCH(k_index_scores<T>, dim3(g), dim3(256), smem, s, ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
+                                         cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores);
+  return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
 }
 
 cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,

@@ -37,6 +37,29 @@ inline size_t esize(int dtype) { return dtype == CSA_BF16 ? 2 : 4; }
 // Number of kernels this library has enqueued in this process (diagnostics).
 void count_launches(int n);
 
+// Launch with programmatic stream serialization (see pdl_trigger / pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+#define CSA_LAUNCH(...)                           \
+  do {                                            \
+    cudaError_t csa_e_ = launch_pdl(__VA_ARGS__); \
+    if (csa_e_ != cudaSuccess) return csa_e_;     \
+  } while (0)
+
 // ---- compress.cu
 struct CompressWs {
   int32_t* flags;  // [B] 1 = sequence valid for this call
@@ -65,8 +88,13 @@ cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int
 // ---- tc_project.cu (tensor-core compressor projections; bf16)
 bool tc_project_supported(const Dims& L, int d);
 void carve_tc_project(Carver& c, const Dims& L, int d, int ntok, float** part, int** tickets);
+// K splits the projection of ntok tokens uses (1: proj is written directly).
+int tc_project_splits(const Dims& L, int d, int ntok);
+// Padded token count (rows of each split's partial block).
+int tc_project_cols(const Dims& L, int d, int ntok);
+// fixup = false (splits > 1): the fp32 partials [splits, ntok (padded), 2*L*d] are left for the consumer.
 cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,
-                              void* proj, float* part, int* tickets, int32_t* err, cudaStream_t s);
+                              void* proj, float* part, int* tickets, bool fixup, int32_t* err, cudaStream_t s);
 
 // ---- tc_indexer.cu (tensor-core scores; bf16, Hi = 64, Di = 128)
 bool tc_index_supported(const Dims& L);

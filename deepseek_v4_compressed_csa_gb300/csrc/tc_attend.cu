@@ -125,6 +125,7 @@ __device__ __forceinline__ Item make_item(const AtArgs& a, int item) {
 }
 
 __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* rows = smem;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
     tc::mbar_init(plo_full, kMain);
     tc::fence_mbar_init();
   }
+  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 4) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
@@ -173,8 +175,8 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
   uint32_t n_tiles_done = 0;         // tiles processed by this CTA: parity of every barrier
 
   for (int item = blockIdx.x; item < a.Q * a.S && !failed; item += gridDim.x) {
-    const Item it = make_item(a, item);
     if (warp == 4) {
+      const Item it = make_item(a, item);
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         constexpr uint32_t id_qk = tc::idesc_bf16(128, 64);
@@ -218,23 +220,12 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
     }
 
     // ------------------------------------------------------------ main warps (128 threads)
-    if (tid < 32) {
-      float c, s;
-      rope_cs(it.p, a.inv_freq, tid, &c, &s);
-      rcos[tid] = c;
-      rsin[tid] = s;
-    }
-    if (tid < 64) {
-      mref[tid] = -INFINITY;
-      lsum[tid] = 0.f;
-    }
-    tc::named_bar(1, kMain);
-    // query block: 128-byte swizzled K-major rows (one per head), copied with cp.async; the copy is waited
-    // for together with the first tile's rows, then RoPE is applied in place (bf16)
-    const bool q_pending_init = it.t_end > it.t_begin;
-    if (q_pending_init) {
+    // The query block depends on nothing but the item, so its copy is issued first: 128-byte swizzled
+    // K-major rows (one per head) by cp.async, waited for with the first tile's rows, then roped in place.
+    const int qi = item / a.S, si = item % a.S;
+    {
       const uint32_t q_base = tc::smem_u32(qbuf);
-      const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
+      const __nv_bfloat16* qsrc = a.q + (size_t)qi * kAH * kAD;
 #pragma unroll 8
       for (int e = tid; e < kAH * 64; e += kMain) {
         const int h = e >> 6, c = e & 63;
@@ -242,7 +233,17 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
                        16u);
       }
     }
-    bool q_pending = q_pending_init;
+    // selection of this thread's row of the split's first tile, loaded alongside the item's counters
+    // (valid when the split starts at tile si, i.e. one tile per split; reloaded otherwise)
+    const int spec_r = si * kAR + tid;
+    const int spec_j = (a.sel && spec_r < a.topk) ? a.sel[(size_t)qi * a.topk + spec_r] : 0;
+    const Item it = make_item(a, item);
+    if (tid < 64) {
+      mref[tid] = -INFINITY;
+      lsum[tid] = 0.f;
+    }
+    bool q_pending = true;
+    bool table_ready = false;
 
     for (int t = it.t_begin; t < it.t_end; ++t) {
       const uint32_t par = n_tiles_done & 1;
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
         const __nv_bfloat16* ptr = nullptr;
         if (tid < nr) {
           if (r < it.nsel) {
-            const int j = a.sel ? a.sel[(size_t)it.q * a.topk + r] : r;
+            const int j = !a.sel ? r : (r == spec_r ? spec_j : a.sel[(size_t)it.q * a.topk + r]);
             if (j >= 0 && j < it.nrows) ptr = a.pool + ((size_t)it.b * a.cap + j) * kAD;
             else atomicOr(a.err, CSA_DEV_RANGE);
           } else {
@@ -275,12 +276,35 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
       for (int rr = 0; rr < 32; ++rr) {
         const int r = warp * 32 + rr;
         const __nv_bfloat16* src = rowp[r];
-        if (cur && src == cur) {
-          // the new token: RoPE at p, into the tile and into its ring slot
+        if (cur && src == cur) continue;  // the new token: roped below
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = lane + 32 * hh;
+          const uint32_t dst = r_base + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          tc::cp_async16(dst, src ? static_cast<const void*>(src + c * 8) : static_cast<const void*>(a.pool),
+                         src ? 16u : 0u);
+        }
+      }
+      // RoPE table of this query's position, computed while the copies are in flight
+      if (!table_ready) {
+        if (tid < 32) {
+          float c, sn;
+          rope_cs(it.p, a.inv_freq, tid, &c, &sn);
+          rcos[tid] = c;
+          rsin[tid] = sn;
+        }
+        tc::named_bar(1, kMain);
+        table_ready = true;
+      }
+      {
+        // the new token (decode): RoPE at p, into the tile and into its ring slot (the slot belongs to the
+        // token leaving the window, which no CTA reads)
+        const int cur_row = it.nsel + it.nwin - 1 - r0;
+        if (cur && cur_row >= 0 && cur_row < nr && rowp[cur_row] == cur && warp == (cur_row >> 5)) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int c = lane + 32 * hh;
-            uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + c * 8));
+            uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + c * 8));
             if (c >= 56) {
               __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
 #pragma unroll
@@ -290,17 +314,9 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
                 hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
               }
             }
-            *reinterpret_cast<uint4*>(rows + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = raw;
+            *reinterpret_cast<uint4*>(rows + (c >> 3) * kBox + cur_row * 128 + (((c & 7) ^ (cur_row & 7)) << 4)) = raw;
             *reinterpret_cast<uint4*>(a.ring_out + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + c * 8) = raw;
           }
-          continue;
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int c = lane + 32 * hh;
-          const uint32_t dst = r_base + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          tc::cp_async16(dst, src ? static_cast<const void*>(src + c * 8) : static_cast<const void*>(a.pool),
-                         src ? 16u : 0u);
         }
       }
       tc::cp_async_wait_all();
@@ -430,6 +446,13 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
       ++n_tiles_done;
     }
     if (failed) break;
+    if (q_pending) tc::cp_async_wait_all();  // an item without rows still owns its query copy
+    if (!table_ready && tid < 32) {
+      float c, sn;
+      rope_cs(it.p, a.inv_freq, tid, &c, &sn);
+      rcos[tid] = c;
+      rsin[tid] = sn;
+    }
     tc::named_bar(1, kMain);
     // ---- epilogue: thread owns latent dim d = 128 m + tid of each O^T tile
     const bool any = it.t_end > it.t_begin;
@@ -466,7 +489,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
           for (int h = 0; h < 64; ++h) u[h] = 0u;
         }
         __nv_bfloat16* dst = a.out + (size_t)it.q * kAH * kAD + d;
-#pragma unroll 8
+#pragma unroll
         for (int h = 0; h < 64; ++h) {
           const float z2 = a.sink[h] * 1.4426950408889634f;
           const float mr = mref[h];
@@ -503,48 +526,47 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
 __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part_ml, const float* __restrict__ part_acc,
                                                   int S, const float* __restrict__ sink, const int32_t* __restrict__ pos,
                                                   const float* __restrict__ inv_freq, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float rc[32], rs[32];
   const int q = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 8 + warp;
   const int p = pos[q];
   if (threadIdx.x < 32) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
-  // split statistics: lane s holds split s (S <= 32 handled in rounds of 32)
+  // split statistics: lane s holds split s (S <= 32)
   const float z = sink[h];
-  float M = z;
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s = s0 + lane;
-    const float m = s < S ? part_ml[(((size_t)q * S + s) * kAH + h) * 2] : -INFINITY;
-    M = fmaxf(M, warp_max(m));
-  }
-  float Z = expf(z - M);
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s = s0 + lane;
-    float t = 0.f;
-    if (s < S) {
-      const size_t idx = ((size_t)q * S + s) * kAH + h;
-      const float m = part_ml[idx * 2];
-      t = m == -INFINITY ? 0.f : part_ml[idx * 2 + 1] * expf(m - M);
-    }
-    Z += warp_sum(t);
-  }
+  const size_t base = (size_t)q * S * kAH + h;
+  const float m_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2) : -INFINITY;
+  const float l_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2 + 1) : 0.f;
+  const float M = fmaxf(z, warp_max(m_l));
+  const float f_l = m_l == -INFINITY ? 0.f : expf(m_l - M);
+  const float Z = expf(z - M) + warp_sum(l_l * f_l);
   float v[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) v[e] = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const size_t idx = ((size_t)q * S + s) * kAH + h;
-    const float m = __ldg(part_ml + idx * 2);
-    if (m == -INFINITY) continue;
-    const float f = expf(m - M);
-    const float4* pa = reinterpret_cast<const float4*>(part_acc + idx * kAD + lane * 16);
-    float4 x[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = __ldcg(pa + k);
+  for (int s0 = 0; s0 < S; s0 += 4) {
+    float4 x[4][4];
+    float f[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      v[4 * k] = fmaf(x[k].x, f, v[4 * k]);
-      v[4 * k + 1] = fmaf(x[k].y, f, v[4 * k + 1]);
-      v[4 * k + 2] = fmaf(x[k].z, f, v[4 * k + 2]);
-      v[4 * k + 3] = fmaf(x[k].w, f, v[4 * k + 3]);
+      f[k] = __shfl_sync(0xffffffffu, f_l, (s0 + k) & 31);
+      if (s0 + k < S && f[k] != 0.f) {
+        const float4* pa = reinterpret_cast<const float4*>(part_acc + (base + (size_t)(s0 + k) * kAH) * kAD + lane * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[k][c] = __ldcg(pa + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (s0 + k < S && f[k] != 0.f) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          v[4 * c] = fmaf(x[k][c].x, f[k], v[4 * c]);
+          v[4 * c + 1] = fmaf(x[k][c].y, f[k], v[4 * c + 1]);
+          v[4 * c + 2] = fmaf(x[k][c].z, f[k], v[4 * c + 2]);
+          v[4 * c + 3] = fmaf(x[k][c].w, f[k], v[4 * c + 3]);
+        }
+      }
     }
   }
   __syncthreads();
@@ -601,17 +623,16 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
   const int items = Q * S;
   const int grid = pos ? items : min(items, g_sms_at);
   cudaFuncSetAttribute(k_tc_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAt);
-  k_tc_attend<<<grid, kThreadsAt, kSmemAt, s>>>(a);
-  count_launches(1);
+  CSA_LAUNCH(k_tc_attend, dim3(grid), dim3(kThreadsAt), kSmemAt, s, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
                             const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s) {
   (void)L;
-  k_tc_merge<<<dim3(kAH / 8, Q), 256, 0, s>>>(part_ml, part_acc, S, sink, pos, inv_freq,
+  if (S > 32) return cudaErrorNotSupported;  // callers use the generic merge beyond 32 splits
+  CSA_LAUNCH(k_tc_merge, dim3(dim3(kAH / 8, Q)), dim3(256), 0, s, part_ml, part_acc, S, sink, pos, inv_freq,
                                                static_cast<__nv_bfloat16*>(out));
-  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
                       IdxArgs a) {
+  pdl_trigger();
   constexpr int N = 64 * G;
   constexpr int QBYTES = N * 128 * 2;
   extern __shared__ uint8_t smem_raw[];
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_mbar_init();
   }
+  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 2 * N);
     tc::tmem_relinquish();
@@ -212,6 +214,8 @@ __global__ void __launch_bounds__(128) k_tc_index_prep(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ pos, int pos0, int R,
                                                        const float* __restrict__ inv_freq, float wscale,
                                                        __nv_bfloat16* __restrict__ qr, float* __restrict__ wts) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int Hi = 64, Di = 128;
   __shared__ float rc[64], rs[64];
   const int q = blockIdx.x, h0 = blockIdx.y * 8;
@@ -257,10 +261,9 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   __nv_bfloat16* qr = c.take<__nv_bfloat16>((size_t)Q * 64 * 128);
   float* wts = c.take<float>((size_t)Q * 64);
   const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
-  k_tc_index_prep<<<dim3(Q, 8), 128, 0, s>>>(static_cast<const __nv_bfloat16*>(iq),
+  CSA_LAUNCH(k_tc_index_prep, dim3(dim3(Q, 8)), dim3(128), 0, s, static_cast<const __nv_bfloat16*>(iq),
                                               static_cast<const __nv_bfloat16*>(iw), pos, pos0, L.R, inv_freq,
                                               wscale, qr, wts);
-  count_launches(1);
   const int G = pos ? 1 : 4;
   CUtensorMap tk, tq;
   if (!make_tmap_2d_bf16(&tk, ikeys, (uint64_t)Bk * cap, 128, 256, kTileRows)) return cudaErrorInvalidValue;
@@ -274,12 +277,12 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   const size_t smem = 1024 + (size_t)64 * G * 128 * 2 + (size_t)kStages * kTileBytes + 256;
   if (G == 1) {
     cudaFuncSetAttribute(k_tc_index_scores<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_tc_index_scores<1><<<grid, kThreads, smem, s>>>(tk, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<1>, dim3(grid), dim3(kThreads), smem, s, tk, tq, a);
   } else {
     cudaFuncSetAttribute(k_tc_index_scores<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_tc_index_scores<4><<<grid, kThreads, smem, s>>>(tk, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<4>, dim3(grid), dim3(kThreads), smem, s, tk, tq, a);
   }
-  count_launches(1);
+  
   return cudaGetLastError();
 }
 

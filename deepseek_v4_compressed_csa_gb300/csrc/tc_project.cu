@@ -25,15 +25,17 @@ constexpr int kMaxSplits = 8;
 struct PjArgs {
   int ntok, X, Ld, N, n_kblk, splits;  // n_kblk: 64-wide K blocks per split
   __nv_bfloat16* proj;                 // [ntok, 2*Ld]
-  float* part;                         // [splits, 2*Ld, n_tiles*N] fp32 (splits > 1)
+  float* part;                         // [splits, n_tiles*N, 2*Ld] fp32 (splits > 1)
   int* tickets;                        // [m_tiles * n_tiles] zeroed before the launch
   int n_cols;                          // n_tiles * N
+  int fixup;                           // splits > 1: 1 = sum the partials here; 0 = the consumer sums them
   int32_t* err;
 };
 
 __global__ void __launch_bounds__(kPThreads, 1)
     k_tc_project(const __grid_constant__ CUtensorMap tm_wkv, const __grid_constant__ CUtensorMap tm_wg,
                  const __grid_constant__ CUtensorMap tm_x, PjArgs a, int stages) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = a.N;
@@ -55,6 +57,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc::mbar_init(acc_full, 1);
     tc::fence_mbar_init();
   }
+  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, tcols);
     tc::tmem_relinquish();
@@ -119,11 +122,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (tok < a.ntok) a.proj[(size_t)tok * 2 * a.Ld + o] = __float2bfloat16_rn(__uint_as_float(u[i]));
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)split * 2 * a.Ld + o) * a.n_cols + n * N + c0);
+          float* dst = a.part + ((size_t)split * a.n_cols + n * N + c0) * 2 * a.Ld + o;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                                 __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+          for (int i = 0; i < 32; ++i) dst[(size_t)i * 2 * a.Ld] = __uint_as_float(u[i]);
         }
       }
     }
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, tcols);
-  if (a.splits == 1) return;
+  if (a.splits == 1 || !a.fixup) return;
   // split-K fix-up: the last CTA of the tile sums every split's partials in split order
   __threadfence();
   __syncthreads();
@@ -143,15 +144,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   if (!*s_last) return;
   __threadfence();
-  // 4 tokens per task; every split's float4 is loaded before the (split-ordered) sum
-  for (int e = threadIdx.x; e < 128 * (N / 4); e += blockDim.x) {
-    const int r = e / (N / 4), c = (e % (N / 4)) * 4;
-    const int o = m * 128 + r, tok = n * N + c;
+  // 4 features per task; every split's float4 is loaded before the (split-ordered) sum
+  for (int e = threadIdx.x; e < N * 32; e += blockDim.x) {
+    const int c = e / 32, o = m * 128 + (e % 32) * 4, tok = n * N + c;
+    if (tok >= a.ntok) continue;
     float4 v[kMaxSplits];
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
       if (s < a.splits)
-        v[s] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)s * 2 * a.Ld + o) * a.n_cols + tok));
+        v[s] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)s * a.n_cols + tok) * 2 * a.Ld + o));
     float4 acc = v[0];
 #pragma unroll
     for (int s = 1; s < kMaxSplits; ++s)
@@ -161,14 +162,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         acc.z += v[s].z;
         acc.w += v[s].w;
       }
-    const float f[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (tok + i < a.ntok) a.proj[(size_t)(tok + i) * 2 * a.Ld + o] = __float2bfloat16_rn(f[i]);
+    __nv_bfloat16* dst = a.proj + (size_t)tok * 2 * a.Ld + o;
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x, acc.y);
+    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z, acc.w);
   }
 }
-
-int g_sms_pj = 0;
 
 struct PjPlan {
   int N, n_tiles, m_tiles, splits;
@@ -204,8 +202,14 @@ void carve_tc_project(Carver& c, const Dims& L, int d, int ntok, float** part, i
   }
 }
 
+int tc_project_splits(const Dims& L, int d, int ntok) { return plan_project(L, d, ntok).splits; }
+int tc_project_cols(const Dims& L, int d, int ntok) {
+  const PjPlan p = plan_project(L, d, ntok);
+  return p.n_tiles * p.N;
+}
+
 cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,
-                              void* proj, float* part, int* tickets, int32_t* err, cudaStream_t s) {
+                              void* proj, float* part, int* tickets, bool fixup, int32_t* err, cudaStream_t s) {
   const PjPlan p = plan_project(L, d, ntok);
   const int Ld = L.lanes * d;
   CUtensorMap tw, tg, tx;
@@ -215,8 +219,8 @@ cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, con
   PjArgs a{};
   a.ntok = ntok; a.X = L.X; a.Ld = Ld; a.N = p.N; a.splits = p.splits; a.n_kblk = L.X / 64 / p.splits;
   a.proj = static_cast<__nv_bfloat16*>(proj); a.part = part; a.tickets = tickets;
-  a.n_cols = p.n_tiles * p.N; a.err = err;
-  if (p.splits > 1) {
+  a.n_cols = p.n_tiles * p.N; a.fixup = fixup ? 1 : 0; a.err = err;
+  if (p.splits > 1 && fixup) {
     cudaMemsetAsync(tickets, 0, (size_t)p.m_tiles * p.n_tiles * sizeof(int), s);
   }
   const int stage_bytes = kABytes + p.N * 128;
@@ -224,8 +228,7 @@ cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, con
   const size_t smem = 1024 + (size_t)stages * stage_bytes + 256;
   cudaFuncSetAttribute(k_tc_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.m_tiles, p.n_tiles, p.splits);
-  k_tc_project<<<grid, kPThreads, smem, s>>>(tw, tg, tx, a, stages);
-  count_launches(1);
+  CSA_LAUNCH(k_tc_project, dim3(grid), dim3(kPThreads), smem, s, tw, tg, tx, a, stages);
   return cudaGetLastError();
 }
 

@@ -185,8 +185,9 @@ class Runner:
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def compress(self, st: DevCache, x):
-        """Both compress calls; returns the GPU's projections of the new tokens per pool, read back from
-        the call's workspace (layout: [B] int32 flags, then 256-byte aligned [B*T, 2*L*d] projections)."""
+        """Both compress calls; returns the GPU's projections of the new tokens per pool.  A single new token's
+        projection is read from its frontier slot (slot pos mod F); a chunk's from the call's workspace
+        (layout: [B] int32 flags, then 256-byte aligned [B*T, 2*L*d] projections)."""
         x = dev(x)
         B, T = x.shape[0], x.shape[1]
         n0 = st.n_rows.clone()
@@ -199,10 +200,14 @@ class Runner:
             ws = torch.zeros(csa.workspace_size(self.L, csa.OP_COMPRESS, B, T, pool.shape[1]), dtype=torch.uint8,
                              device="cuda")
             csa.compress_append(self.L, comp, x, st.pos, front, pool, n, self.inv_freq, ws=ws, err=self.err)
-            off = (4 * B + 255) // 256 * 256
             width = 2 * self.cfg.lanes * comp.d
-            raw = ws[off:off + B * T * width * es]
-            projs[name] = raw.view(self.cfg.storage).view(B, T, width).clone()
+            if T == 1:
+                slots = (st.pos.long() % front.shape[1])
+                projs[name] = front[torch.arange(B, device=front.device), slots].view(B, 1, width).clone()
+            else:
+                off = (4 * B + 255) // 256 * 256
+                raw = ws[off:off + B * T * width * es]
+                projs[name] = raw.view(self.cfg.storage).view(B, T, width).clone()
         return projs
 
     def decode_step(self, st: DevCache, si: csa_synth.StepInputs):
