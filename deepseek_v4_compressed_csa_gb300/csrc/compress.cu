@@ -111,14 +111,21 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
       if (part) {
         // single new token with split-K partials: sum them in split order, round once to the model dtype
         for (int e = threadIdx.x * 4; e < rowlen; e += blockDim.x * 4) {
-          float4 acc = __ldcg(reinterpret_cast<const float4*>(part + (size_t)b * rowlen + e));
-          for (int sp = 1; sp < splits; ++sp) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)sp * part_stride + b) * rowlen + e));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-          }
+          constexpr int kMaxSplits = 8;  // the projection never splits further
+          float4 v[kMaxSplits];
+#pragma unroll
+          for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < splits)
+              v[sp] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)sp * part_stride + b) * rowlen + e));
+          float4 acc = v[0];
+#pragma unroll
+          for (int sp = 1; sp < kMaxSplits; ++sp)
+            if (sp < splits) {
+              acc.x += v[sp].x;
+              acc.y += v[sp].y;
+              acc.z += v[sp].z;
+              acc.w += v[sp].w;
+            }
           const float f[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -147,40 +154,50 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
   const T* pj = proj + (size_t)b * T_ * rowlen;
 
   float ss = 0.f;
+  const int t_lo = (lanes == 2) ? max(0, (j - 1) * ratio) : j * ratio;
+  const int t_hi = (j + 1) * ratio;
   for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    // entries (token t, lane l): ratio 4 -> window j-1 via lane 0 (if j >= 1) and window j via lane 1
-    float m = -INFINITY;
-    const int t_lo = (lanes == 2) ? max(0, (j - 1) * ratio) : j * ratio;
-    const int t_hi = (j + 1) * ratio;
-    for (int t = t_lo; t < t_hi; ++t) {
-      const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
-      float g;
-      if (t < p0) g = to_f(fr[(size_t)(t % F) * rowlen + Ld + l * d + c]);
-      else if (part) g = cur[Ld + l * d + c];
-      else g = to_f(pj[(size_t)(t - p0) * rowlen + Ld + l * d + c]);
-      const float s = g + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
-      m = fmaxf(m, s);
-    }
-    float num = 0.f, den = 0.f;
-    for (int t = t_lo; t < t_hi; ++t) {
-      const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
-      float g, kv;
-      if (t < p0) {
-        const T* row = fr + (size_t)(t % F) * rowlen;
-        g = to_f(row[Ld + l * d + c]);
-        kv = to_f(row[l * d + c]);
-      } else if (part) {
-        g = cur[Ld + l * d + c];
-        kv = cur[l * d + c];
-      } else {
-        const T* row = pj + (size_t)(t - p0) * rowlen;
-        g = to_f(row[Ld + l * d + c]);
-        kv = to_f(row[l * d + c]);
+    // entries (token t, lane l): ratio 4 -> window j-1 via lane 0 (if j >= 1) and window j via lane 1.
+    // Chunks of 8 entries: every load of a chunk is issued before its first use; online softmax across chunks.
+    float m = -INFINITY, num = 0.f, den = 0.f;
+    for (int t0 = t_lo; t0 < t_hi; t0 += 8) {
+      float sv[8], kv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k;
+        sv[k] = -INFINITY;
+        kv[k] = 0.f;
+        if (t < t_hi) {
+          const int l = (lanes == 2 && t >= j * ratio) ? 1 : 0;
+          float g;
+          if (t < p0) {
+            const T* row = fr + (size_t)(t % F) * rowlen;
+            g = to_f(row[Ld + l * d + c]);
+            kv[k] = to_f(row[l * d + c]);
+          } else if (part) {
+            g = cur[Ld + l * d + c];
+            kv[k] = cur[l * d + c];
+          } else {
+            const T* row = pj + (size_t)(t - p0) * rowlen;
+            g = to_f(row[Ld + l * d + c]);
+            kv[k] = to_f(row[l * d + c]);
+          }
+          sv[k] = g + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
+        }
       }
-      const float s = g + __ldg(ape + (size_t)(t % ratio) * Ld + l * d + c);
-      float e = expf(s - m);
-      den += e;
-      num = fmaf(e, kv, num);
+      float cm = m;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cm = fmaxf(cm, sv[k]);
+      const float al = (m == -INFINITY) ? 0.f : expf(m - cm);
+      num *= al;
+      den *= al;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float e = (sv[k] == -INFINITY) ? 0.f : expf(sv[k] - cm);
+        den += e;
+        num = fmaf(e, kv[k], num);
+      }
+      m = cm;
     }
     float uc = rnd<T>(num / den);
     u[c] = uc;
