@@ -118,6 +118,18 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
                             const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s);
 
+// ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
+bool tc_attend_decode_supported(const Dims& L);
+// Key splits per query for Q queries of at most max_rows rows: a split is one chunk of <= 160 rows where the
+// workspace allows, more splits while every CTA still fits one wave; never more than max_splits.
+int tc_attend_decode_splits(int Q, int max_rows, int max_splits);
+// One CTA per (query, split).  S > 1 writes (m, l, acc) partials (merge follows), S == 1 the final output.
+// The new token kv_new[b] is roped in-kernel and written to ring slot pos[b] % W.
+cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,
+                                    const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
+                                    const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
+                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
+
 // ---- attend.cu
 struct AttendWs {
   void* qr;        // [Q, H, D] roped queries, model dtype

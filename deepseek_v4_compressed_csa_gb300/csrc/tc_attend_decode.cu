@@ -1,0 +1,568 @@
+// Decode attention on the 5th-generation tensor cores for the Flash shapes (64
+// query heads over one 512-dim latent, K = V, bf16, RoPE on the last 64 dims):
+// one CTA per (query, key split) of up to 160 rows.
+//
+// Definitions: "DeepSeek-V4-Flash: native deepseek_v4 AR backend" (MTPLX #216),
+// "What V4 adds" (MQA-shaped MLA with per-head sink logits) and "Decode path"
+// (bf16 in/out, fp32 softmax state, the probability block cast to bf16 before
+// the PV product); "deepseek-v41-mlx" README (inverse rope on the output, sinks
+// in the denominator only).
+//
+// Why 160 rows: a decode query attends to topk + W = 640 rows; four splits of
+// 160 put a batch of 32 on 128 CTAs, one wave of the 152 SMs, where 128-row
+// splits would need 160 CTAs and a second wave.  The rows of a chunk (selected
+// pool rows, then window tokens, the newest one roped here) are gathered with
+// cp.async into one 160-row, 128-byte-swizzled shared tile that serves both as K
+// (K-major) and as V^T (MN-major), so each row is read from memory once.
+//   QK       S^T = K Q^T twice, M = 128 (TMEM lanes), N = 64 heads, K = 512:
+//            rows 0-127 and rows 32-159 (only lanes 96-127 of the second are used);
+//   softmax  thread = row (warp 3 also takes rows 128-159); per-head column max
+//            and sum by a warp reduce-scatter and a 4-warp combine; the reference
+//            max is raised only when a chunk exceeds it by 2^8 (O rescaled in TMEM);
+//   PV       O^T += V^T P^T: M = 128 latent dims x 4 tiles, N = 64 heads, K = the
+//            chunk's rows.  Once both score products have retired, the query's
+//            shared memory holds P^T as two bf16 parts, P_hi = bf16(P) and
+//            P_lo = bf16(P - P_hi), multiplied in turn (~16 bits of P).
+// With one split the epilogue finalises the output (sink, normalisation, bf16,
+// inverse RoPE, bf16); with several it writes (m, l, acc) partials for the merge
+// kernel.  A split longer than 160 rows takes several chunks and copies the
+// query again for each.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kCR = 160;                 // rows per chunk
+constexpr int kAD = 512;                 // latent dims
+constexpr int kAH = 64;                  // heads
+constexpr int kBox = kCR * 128;          // 64 dims x 160 rows (20 KB)
+constexpr int kRowsBytes = 8 * kBox;     // 160 KB
+constexpr int kQBox = kAH * 128;         // 64 dims x 64 heads (8 KB)
+constexpr int kQBytes = 8 * kQBox;       // 64 KB
+constexpr int kPPart = kCR * 128;        // P^T part: 160 rows x 64 heads, MN-major (20 KB)
+constexpr int kMain = 128;               // gather / softmax / epilogue threads (warps 0-3)
+constexpr int kThreads = kMain + 32;     // + warp 4: TMEM owner and MMA issuer
+constexpr int kGatherRows = kCR / 4;     // rows gathered by each main warp
+constexpr int kTmemCols = 512;           // S^T rows 0-127: cols 0-63; rows 32-159: 64-127; O^T: 128-383
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleAt = 8.f;        // log2 headroom before O is rescaled
+
+// shared memory: rows | query (after the score products: P_hi, P_lo, column reductions) | small state
+constexpr int kOffQ = kRowsBytes;
+constexpr int kOffRed = kOffQ + 2 * kPPart;     // [4][64] column maxima
+constexpr int kOffRedSum = kOffRed + 4 * 64 * 4;
+static_assert(kOffRedSum + 4 * 64 * 4 <= kOffQ + kQBytes, "reductions fit in the query region");
+constexpr int kOffMref = kOffQ + kQBytes;
+constexpr int kOffLsum = kOffMref + 64 * 4;
+constexpr int kOffAlpha = kOffLsum + 64 * 4;
+constexpr int kOffRope = kOffAlpha + 64 * 4;    // cos[32], sin[32]
+constexpr int kOffRowc = kOffRope + 64 * 4;     // [160] row codes
+constexpr int kOffFlag = kOffRowc + kCR * 4;
+constexpr int kOffBars = kOffFlag + 16;         // 4 mbarriers
+constexpr int kOffTmem = kOffBars + 8 * 8;
+constexpr int kSmem = kOffTmem + 16 + 1024;     // + alignment slack
+static_assert(kSmem <= 232448, "shared memory per block");
+
+// row codes: >= 0 pool row (b * cap + j); kRowNone: empty; kRowNew: the new token; <= kRowRing0: ring row
+constexpr int kRowNone = -1;
+constexpr int kRowNew = -2;
+constexpr int kRowRing0 = -3;
+
+struct DecArgs {
+  const __nv_bfloat16* q;       // [Q, 64, 512] queries before RoPE
+  const __nv_bfloat16* pool;    // [B, cap, 512]
+  __nv_bfloat16* ring;          // [B, W, 512]; the new token is written to slot pos % W
+  const __nv_bfloat16* kv_new;  // [B, 512] the new token before RoPE
+  const int32_t* sel;           // [Q, topk] or null (every visible row)
+  const int32_t* n_sel;
+  const int32_t* n_rows;
+  const int32_t* pos;
+  const float* sink;
+  const float* inv_freq;
+  int cap, topk, W, ratio, S;
+  float scale2;                 // softmax scale * log2(e)
+  float* part_ml;
+  float* part_acc;
+  __nv_bfloat16* out;
+  int32_t* err;
+};
+
+// Reduce 64 columns over the 32 lanes of a warp; lane L returns columns 2L, 2L+1.
+template <bool kMax>
+__device__ __forceinline__ float2 reduce_scatter64(float (&v)[64]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int half = 32 >> st, mask = 16 >> st;
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, mask);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return make_float2(v[0], v[1]);
+}
+
+struct Item {
+  int q, s, b, p, nsel, nwin, nrows, r_begin, r_end;
+};
+
+__device__ __forceinline__ Item make_item(const DecArgs& a) {
+  Item it;
+  it.q = blockIdx.x / a.S;
+  it.s = blockIdx.x % a.S;
+  it.b = it.q;
+  it.p = a.pos[it.q];
+  it.nrows = min(a.n_rows[it.b], a.cap);
+  it.nsel = a.sel ? min(max(a.n_sel[it.q], 0), a.topk) : max(0, min(it.nrows, (it.p + 1) / a.ratio));
+  it.nwin = it.p >= 0 ? min(a.W, it.p + 1) : 0;
+  const int total = it.nsel + it.nwin;
+  const int per = (total + a.S - 1) / a.S;
+  it.r_begin = min(total, it.s * per);
+  it.r_end = min(total, it.r_begin + per);
+  return it;
+}
+
+// Code of row r (0 .. nsel+nwin-1) of the item; an out-of-range selection is reported and left empty.
+__device__ __forceinline__ int row_code(const DecArgs& a, const Item& it, int r) {
+  if (r < it.nsel) {
+    const int j = a.sel ? a.sel[(size_t)it.q * a.topk + r] : r;
+    if (j >= 0 && j < it.nrows) return it.b * a.cap + j;
+    atomicOr(a.err, CSA_DEV_RANGE);
+    return kRowNone;
+  }
+  const int tok = it.p - it.nwin + 1 + (r - it.nsel);
+  if (tok == it.p) return kRowNew;
+  return kRowRing0 - (it.b * a.W + tok % a.W);
+}
+
+__device__ __forceinline__ const __nv_bfloat16* code_ptr(const DecArgs& a, int code) {
+  if (code >= 0) return a.pool + (size_t)code * kAD;
+  if (code <= kRowRing0) return a.ring + (size_t)(kRowRing0 - code) * kAD;
+  return nullptr;
+}
+
+__device__ __forceinline__ void rope8(uint4& raw, int c, const float* rcos, const float* rsin) {
+  __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int f = (c - 56) * 4 + k;
+    const float2 x = __bfloat1622float2(hv[k]);
+    hv[k] = __floats2bfloat162_rn(fmaf(x.x, rcos[f], -x.y * rsin[f]), fmaf(x.x, rsin[f], x.y * rcos[f]));
+  }
+}
+
+// probabilities of one row into both P^T parts (MN-major, 128-byte swizzle); returns them in pe (fp32)
+__device__ __forceinline__ void write_p(uint8_t* pbuf, int row, const float (&sv)[64], const float* mref,
+                                        float (&pe)[64]) {
+#pragma unroll
+  for (int h = 0; h < 64; ++h) {
+    const float ref = mref[h] == -INFINITY ? 0.f : mref[h];
+    pe[h] = sv[h] == -INFINITY ? 0.f : exp2f(sv[h] - ref);
+  }
+  uint8_t* dst = pbuf + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 hi, lo;
+    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&hi);
+    __nv_bfloat162* lv = reinterpret_cast<__nv_bfloat162*>(&lo);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      hv[k] = __floats2bfloat162_rn(pe[8 * j + 2 * k], pe[8 * j + 2 * k + 1]);
+      const float2 back = __bfloat1622float2(hv[k]);
+      lv[k] = __floats2bfloat162_rn(pe[8 * j + 2 * k] - back.x, pe[8 * j + 2 * k + 1] - back.y);
+    }
+    const int off = (j ^ (row & 7)) << 4;
+    *reinterpret_cast<uint4*>(dst + off) = hi;
+    *reinterpret_cast<uint4*>(dst + kPPart + off) = lo;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* rows = smem;
+  uint8_t* qbuf = smem + kOffQ;
+  uint8_t* pbuf = qbuf;  // P^T parts reuse the query region once the score products have retired
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
+  float* mref = reinterpret_cast<float*>(smem + kOffMref);
+  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* rcos = reinterpret_cast<float*>(smem + kOffRope);
+  float* rsin = rcos + 32;
+  int* rowc = reinterpret_cast<int*>(smem + kOffRowc);
+  int* flag = reinterpret_cast<int*>(smem + kOffFlag);
+  uint64_t* rows_full = reinterpret_cast<uint64_t*>(smem + kOffBars);  // rows and roped query in place
+  uint64_t* s_full = rows_full + 1;    // both score products retired
+  uint64_t* p_full = rows_full + 2;    // both P parts written
+  uint64_t* pv_done = rows_full + 3;   // PV retired: rows and P regions free, O complete
+  uint64_t* drain = rows_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    tc::mbar_init(rows_full, kMain);
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(p_full, kMain);
+    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(drain, 1);
+    tc::fence_mbar_init();
+  }
+  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  if (warp == 4) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_s = tmem;         // S^T, rows 0-127 (cols 0-63) and rows 32-159 (cols 64-127)
+  const uint32_t tm_o = tmem + 128;   // O^T, 4 x 64 columns
+  const Item it = make_item(a);
+  const int nchunks = (it.r_end - it.r_begin + kCR - 1) / kCR;
+  bool failed = false;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_bf16(128, 64);
+      constexpr uint32_t id_pv = tc::idesc_bf16(128, 64, true, true);
+      const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf), p_base = tc::smem_u32(pbuf);
+      for (int c = 0; c < nchunks; ++c) {
+        const uint32_t par = c & 1;
+        const int nr = min(kCR, it.r_end - it.r_begin - c * kCR);
+        if (!tc::mbar_wait(rows_full, par)) { failed = true; break; }
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int half = 0; half < (nr > 128 ? 2 : 1); ++half) {
+          const uint32_t a_off = half ? 32 * 128 : 0;  // rows 32-159: four 8-row atoms further
+#pragma unroll 8
+          for (int k = 0; k < 32; ++k) {
+            const uint64_t ad = tc::sdesc_kmajor_sw128(r_base + (k >> 2) * kBox + a_off + (k & 3) * 32);
+            const uint64_t bd = tc::sdesc_kmajor_sw128(q_base + (k >> 2) * kQBox + (k & 3) * 32);
+            tc::mma_bf16(tm_s + 64 * half, ad, bd, id_qk, k > 0);
+          }
+        }
+        tc::mma_commit(s_full);
+        if (!tc::mbar_wait(p_full, par)) { failed = true; break; }
+        tc::fence_after_sync();
+        const int ksteps = (nr + 15) >> 4;
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll 1
+            for (int kk = 0; kk < ksteps; ++kk) {
+              const uint64_t ad = tc::sdesc_mnmajor_sw128(r_base + 2 * m * kBox + kk * 2048, kBox, 1024);
+              const uint64_t bd = tc::sdesc_mnmajor_sw128(p_base + part * kPPart + kk * 2048, 8192, 1024);
+              tc::mma_bf16(tm_o + 64 * m, ad, bd, id_pv, (c | part | kk) != 0);
+            }
+          }
+        }
+        tc::mma_commit(pv_done);
+      }
+    }
+    __syncwarp();
+    failed = __shfl_sync(0xffffffffu, (int)failed, 0) != 0;
+  } else {
+    // ------------------------------------------------------------ main warps (128 threads)
+    const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
+    const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
+    const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
+    const int last_row = it.nsel + it.nwin - 1;  // the new token (when p >= 0)
+    auto copy_query = [&]() {  // 64 head rows of 512 dims, K-major swizzled
+#pragma unroll 8
+      for (int e = tid; e < kAH * 64; e += kMain) {
+        const int h = e >> 6, ch = e & 63;
+        tc::cp_async16(q_base + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4),
+                       qsrc + (size_t)h * kAD + ch * 8, 16u);
+      }
+    };
+    copy_query();
+    if (tid < 64) {
+      mref[tid] = -INFINITY;
+      lsum[tid] = 0.f;
+    }
+    bool table_ready = false;
+    const int row = tid;
+
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t par = c & 1;
+      const int r0 = it.r_begin + c * kCR;
+      const int nr = min(kCR, it.r_end - r0);
+      if (c > 0) copy_query();  // the previous chunk's P overwrote it
+      for (int r = tid; r < kCR; r += kMain) rowc[r] = r < nr ? row_code(a, it, r0 + r) : kRowNone;
+      tc::named_bar(1, kMain);
+      // ---- gather: warp w copies rows 40w .. 40w+39, 2 x 512 contiguous bytes per instruction
+      const int cur_row = (it.p >= 0) ? last_row - r0 : -1;
+#pragma unroll 4
+      for (int rr = 0; rr < kGatherRows; ++rr) {
+        const int r = warp * kGatherRows + rr;
+        const int code = rowc[r];
+        if (code == kRowNew) continue;  // roped below
+        const __nv_bfloat16* src = code_ptr(a, code);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ch = lane + 32 * hh;
+          const uint32_t dst = r_base + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          tc::cp_async16(dst, src ? static_cast<const void*>(src + ch * 8) : static_cast<const void*>(a.pool),
+                         src ? 16u : 0u);
+        }
+      }
+      // RoPE table of this query's position, computed while the copies are in flight
+      if (!table_ready) {
+        if (tid < 32) {
+          float cs, sn;
+          rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
+          rcos[tid] = cs;
+          rsin[tid] = sn;
+        }
+        tc::named_bar(1, kMain);
+        table_ready = true;
+      }
+      // the new token: RoPE at p, into the tile and into its ring slot (the slot belongs to the token leaving
+      // the window, which no CTA reads)
+      if (cur_row >= 0 && cur_row < nr && warp == cur_row / kGatherRows) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ch = lane + 32 * hh;
+          uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
+          if (ch >= 56) rope8(raw, ch, rcos, rsin);
+          *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
+          *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
+        }
+      }
+      tc::cp_async_wait_all();
+      tc::named_bar(1, kMain);  // every thread's share of the query block has landed
+#pragma unroll
+      for (int e = tid; e < kAH * 8; e += kMain) {
+        const int h = e >> 3, ch = 56 + (e & 7);
+        uint4* slot = reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4));
+        uint4 raw = *slot;
+        rope8(raw, ch, rcos, rsin);
+        *slot = raw;
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(rows_full);
+      // ---- scores of this thread's row (and, in warp 3, of row 128 + lane)
+      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(s_full, par))) { failed = true; break; }
+      tc::fence_after_sync();
+      const bool two = warp == 3 && nr > 128;
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      float sv[64];
+      float cp[64];
+      {
+        uint32_t u[64];
+        tc::tmem_ld32(tm_s + lane_base, u);
+        tc::tmem_ld32(tm_s + lane_base + 32, u + 32);
+        tc::tmem_wait_ld();
+        const bool valid = row < nr && rowc[row] != kRowNone;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) sv[h] = valid ? __uint_as_float(u[h]) * a.scale2 : -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) cp[h] = sv[h];
+        if (two) {
+          tc::tmem_ld32(tm_s + 64 + lane_base, u);
+          tc::tmem_ld32(tm_s + 96 + lane_base, u + 32);
+          tc::tmem_wait_ld();
+          const bool valid2 = 128 + lane < nr && rowc[128 + lane] != kRowNone;
+#pragma unroll
+          for (int h = 0; h < 64; ++h) cp[h] = fmaxf(cp[h], valid2 ? __uint_as_float(u[h]) * a.scale2 : -INFINITY);
+        }
+      }
+      {
+        const float2 m2 = reduce_scatter64<true>(cp);
+        red[warp * 64 + 2 * lane] = m2.x;
+        red[warp * 64 + 2 * lane + 1] = m2.y;
+      }
+      if (tid == 0) *flag = 0;
+      tc::named_bar(1, kMain);
+      if (tid < 64) {
+        const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+        const float old = mref[tid];
+        float nw = old;
+        if (old == -INFINITY || mt > old + kRescaleAt) nw = mt;
+        float al = 1.f;
+        if (old != -INFINITY && nw != old) {
+          al = exp2f(old - nw);
+          atomicOr(flag, 1);
+        }
+        alpha[tid] = al;
+        mref[tid] = nw;
+        lsum[tid] *= al;
+      }
+      tc::named_bar(1, kMain);
+      if (*flag) {
+        // raise the reference max: O^T (earlier chunks, all retired) *= alpha per head
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t ta = tm_o + 64 * m + lane_base;
+          uint32_t u[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            tc::tmem_ld32(ta + 32 * half, u);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha[32 * half + i]);
+            tc::tmem_st32(ta + 32 * half, u);
+          }
+        }
+        tc::tmem_wait_st();
+      }
+      // ---- probabilities (fp32 for the sums, bf16 hi + lo for the PV product)
+      float pe[64];
+      write_p(pbuf, row, sv, mref, pe);
+      if (two) {
+        uint32_t u[64];
+        tc::tmem_ld32(tm_s + 64 + lane_base, u);
+        tc::tmem_ld32(tm_s + 96 + lane_base, u + 32);
+        tc::tmem_wait_ld();
+        const bool valid2 = 128 + lane < nr && rowc[128 + lane] != kRowNone;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) sv[h] = valid2 ? __uint_as_float(u[h]) * a.scale2 : -INFINITY;
+        float pe2[64];
+        write_p(pbuf, 128 + lane, sv, mref, pe2);
+#pragma unroll
+        for (int h = 0; h < 64; ++h) pe[h] += pe2[h];
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(p_full);
+      {
+        const float2 s2 = reduce_scatter64<false>(pe);
+        red_sum[warp * 64 + 2 * lane] = s2.x;
+        red_sum[warp * 64 + 2 * lane + 1] = s2.y;
+      }
+      tc::named_bar(1, kMain);
+      if (tid < 64) lsum[tid] += (red_sum[tid] + red_sum[64 + tid]) + (red_sum[128 + tid] + red_sum[192 + tid]);
+      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(pv_done, par))) { failed = true; break; }
+      tc::fence_after_sync();
+    }
+    tc::cp_async_wait_all();
+    if (!table_ready && tid < 32) {
+      float cs, sn;
+      rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
+      rcos[tid] = cs;
+      rsin[tid] = sn;
+    }
+    tc::named_bar(1, kMain);
+    if (!failed) {
+      // ---- epilogue: thread owns latent dim d = 128 m + tid of each O^T tile
+      const bool any = nchunks > 0;
+      if (a.S > 1) {
+        if (tid < 64) {
+          const size_t idx = ((size_t)it.q * a.S + it.s) * kAH + tid;
+          a.part_ml[idx * 2] = mref[tid] == -INFINITY ? -INFINITY : mref[tid] * kLn2;
+          a.part_ml[idx * 2 + 1] = lsum[tid];
+        }
+        if (any) {
+          for (int m = 0; m < 4; ++m) {
+            const int d = 128 * m + tid;
+            uint32_t u[64];
+            const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
+            tc::tmem_ld32(ta, u);
+            tc::tmem_ld32(ta + 32, u + 32);
+            tc::tmem_wait_ld();
+            float* dst = a.part_acc + (((size_t)it.q * a.S + it.s) * kAH) * kAD + d;
+#pragma unroll
+            for (int h = 0; h < 64; ++h) dst[(size_t)h * kAD] = __uint_as_float(u[h]);
+          }
+        }
+      } else {
+        for (int m = 0; m < 4; ++m) {
+          const int d = 128 * m + tid;
+          uint32_t u[64];
+          if (any) {
+            const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
+            tc::tmem_ld32(ta, u);
+            tc::tmem_ld32(ta + 32, u + 32);
+            tc::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int h = 0; h < 64; ++h) u[h] = 0u;
+          }
+          __nv_bfloat16* dst = a.out + (size_t)it.q * kAH * kAD + d;
+#pragma unroll
+          for (int h = 0; h < 64; ++h) {
+            const float z2 = a.sink[h] * 1.4426950408889634f;
+            const float mr = mref[h];
+            const float M2 = fmaxf(z2, mr);
+            const float f = mr == -INFINITY ? 0.f : exp2f(mr - M2);
+            const float Z = exp2f(z2 - M2) + lsum[h] * f;
+            float o = rnd<__nv_bfloat16>(__uint_as_float(u[h]) * (f / Z));
+            const float partner = __shfl_xor_sync(0xffffffffu, o, 1);
+            if (d >= kAD - 64) {
+              const int i = (d - (kAD - 64)) >> 1;
+              o = (d & 1) ? fmaf(-partner, rsin[i], o * rcos[i]) : fmaf(o, rcos[i], partner * rsin[i]);
+            }
+            dst[(size_t)h * kAD] = __float2bfloat16_rn(o);
+          }
+        }
+      }
+    }
+  }
+  if (failed) atomicOr(a.err, tc::kErrTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  // retire every MMA before tensor memory is released
+  if (warp == 4 && lane == 0) {
+    tc::mma_commit(drain);
+    if (!tc::mbar_wait(drain, 0)) atomicOr(a.err, tc::kErrTimeout);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+int g_sms_dec = 0;
+
+}  // namespace
+
+bool tc_attend_decode_supported(const Dims& L) {
+  return L.dtype == CSA_BF16 && L.H == kAH && L.D == kAD && L.R == 64;
+}
+
+// Splits per query for at most max_rows rows per query: enough that a split is one chunk (<= 160 rows), more
+// (up to one per 128 rows) while every CTA still fits one wave of the device's SMs; never above max_splits.
+int tc_attend_decode_splits(int Q, int max_rows, int max_splits) {
+  if (!g_sms_dec) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms_dec, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const int s_min = (max_rows + kCR - 1) / kCR;
+  const int s_tiles = (max_rows + 127) / 128;
+  const int s_fit = g_sms_dec / max(1, Q);
+  return max(1, min(max_splits, max(s_min, min(s_fit, s_tiles))));
+}
+
+cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,
+                                    const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
+                                    const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
+                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s) {
+  DecArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.pool = static_cast<const __nv_bfloat16*>(pool);
+  a.ring = static_cast<__nv_bfloat16*>(ring);
+  a.kv_new = static_cast<const __nv_bfloat16*>(kv_new);
+  a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq;
+  a.cap = cap; a.topk = L.topk; a.W = L.W; a.ratio = L.ratio; a.S = S;
+  a.scale2 = L.scale * 1.4426950408889634f;
+  a.part_ml = part_ml; a.part_acc = part_acc;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.err = err;
+  cudaFuncSetAttribute(k_tc_attend_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  CSA_LAUNCH(k_tc_attend_decode, dim3(Q * S), dim3(kThreads), kSmem, s, a);
+  return cudaGetLastError();
+}
+
+}  // namespace csa
