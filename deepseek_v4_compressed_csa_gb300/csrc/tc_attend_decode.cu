@@ -15,10 +15,12 @@
 // cp.async into one 160-row, 128-byte-swizzled shared tile that serves both as K
 // (K-major) and as V^T (MN-major), so each row is read from memory once.
 //   QK       S^T = K Q^T twice, M = 128 (TMEM lanes), N = 64 heads, K = 512:
-//            rows 0-127 and rows 32-159 (only lanes 96-127 of the second are used);
-//   softmax  thread = row (warp 3 also takes rows 128-159); per-head column max
-//            and sum by a warp reduce-scatter and a 4-warp combine; the reference
-//            max is raised only when a chunk exceeds it by 2^8 (O rescaled in TMEM);
+//            rows 0-127, and rows 128-255 of which lanes 0-31 (rows 128-159) are
+//            used (the rest read neighbouring, initialised shared memory);
+//   softmax  five warps, thread = row (warp 4 reads lanes 0-31 of the second
+//            product); per-head column max and sum by a warp reduce-scatter and a
+//            5-warp combine; the reference max is raised only when a chunk exceeds
+//            it by 2^8 (O rescaled in TMEM);
 //   PV       O^T += V^T P^T: M = 128 latent dims x 4 tiles, N = 64 heads, K = the
 //            chunk's rows.  Once both score products have retired, the query's
 //            shared memory holds P^T as two bf16 parts, P_hi = bf16(P) and
@@ -43,18 +45,19 @@ constexpr int kRowsBytes = 8 * kBox;     // 160 KB
 constexpr int kQBox = kAH * 128;         // 64 dims x 64 heads (8 KB)
 constexpr int kQBytes = 8 * kQBox;       // 64 KB
 constexpr int kPPart = kCR * 128;        // P^T part: 160 rows x 64 heads, MN-major (20 KB)
-constexpr int kMain = 128;               // gather / softmax / epilogue threads (warps 0-3)
-constexpr int kThreads = kMain + 32;     // + warp 4: TMEM owner and MMA issuer
-constexpr int kGatherRows = kCR / 4;     // rows gathered by each main warp
-constexpr int kTmemCols = 512;           // S^T rows 0-127: cols 0-63; rows 32-159: 64-127; O^T: 128-383
+constexpr int kMainWarps = kCR / 32;     // gather / softmax threads: one per row (warps 0-4)
+constexpr int kMain = 32 * kMainWarps;
+constexpr int kMmaWarp = kMainWarps;     // TMEM owner and MMA issuer
+constexpr int kThreads = kMain + 32;
+constexpr int kTmemCols = 512;           // S^T rows 0-127: cols 0-63; rows 128-255: 64-127; O^T: 128-383
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleAt = 8.f;        // log2 headroom before O is rescaled
 
 // shared memory: rows | query (after the score products: P_hi, P_lo, column reductions) | small state
 constexpr int kOffQ = kRowsBytes;
-constexpr int kOffRed = kOffQ + 2 * kPPart;     // [4][64] column maxima
-constexpr int kOffRedSum = kOffRed + 4 * 64 * 4;
-static_assert(kOffRedSum + 4 * 64 * 4 <= kOffQ + kQBytes, "reductions fit in the query region");
+constexpr int kOffRed = kOffQ + 2 * kPPart;     // [5][64] column maxima
+constexpr int kOffRedSum = kOffRed + kMainWarps * 64 * 4;
+static_assert(kOffRedSum + kMainWarps * 64 * 4 <= kOffQ + kQBytes, "reductions fit in the query region");
 constexpr int kOffMref = kOffQ + kQBytes;
 constexpr int kOffLsum = kOffMref + 64 * 4;
 constexpr int kOffAlpha = kOffLsum + 64 * 4;
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     tc::fence_mbar_init();
   }
   pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -225,13 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s = tmem;         // S^T, rows 0-127 (cols 0-63) and rows 32-159 (cols 64-127)
+  const uint32_t tm_s = tmem;         // S^T, rows 0-127 (cols 0-63) and rows 128-255 (cols 64-127)
   const uint32_t tm_o = tmem + 128;   // O^T, 4 x 64 columns
   const Item it = make_item(a);
   const int nchunks = (it.r_end - it.r_begin + kCR - 1) / kCR;
   bool failed = false;
 
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = tc::idesc_bf16(128, 64);
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         tc::fence_after_sync();
 #pragma unroll 1
         for (int half = 0; half < (nr > 128 ? 2 : 1); ++half) {
-          const uint32_t a_off = half ? 32 * 128 : 0;  // rows 32-159: four 8-row atoms further
+          const uint32_t a_off = half ? 128 * 128 : 0;  // rows 128-255: sixteen 8-row atoms further
 #pragma unroll 8
           for (int k = 0; k < 32; ++k) {
             const uint64_t ad = tc::sdesc_kmajor_sw128(r_base + (k >> 2) * kBox + a_off + (k & 3) * 32);
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     __syncwarp();
     failed = __shfl_sync(0xffffffffu, (int)failed, 0) != 0;
   } else {
-    // ------------------------------------------------------------ main warps (128 threads)
+    // ------------------------------------------------------------ main warps (160 threads, one per row)
     const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
     const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
     const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
@@ -302,11 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       if (c > 0) copy_query();  // the previous chunk's P overwrote it
       for (int r = tid; r < kCR; r += kMain) rowc[r] = r < nr ? row_code(a, it, r0 + r) : kRowNone;
       tc::named_bar(1, kMain);
-      // ---- gather: warp w copies rows 40w .. 40w+39, 2 x 512 contiguous bytes per instruction
+      // ---- gather: warp w copies rows 32w .. 32w+31, 2 x 512 contiguous bytes per instruction
       const int cur_row = (it.p >= 0) ? last_row - r0 : -1;
 #pragma unroll 4
-      for (int rr = 0; rr < kGatherRows; ++rr) {
-        const int r = warp * kGatherRows + rr;
+      for (int rr = 0; rr < 32; ++rr) {
+        const int r = warp * 32 + rr;
         const int code = rowc[r];
         if (code == kRowNew) continue;  // roped below
         const __nv_bfloat16* src = code_ptr(a, code);
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       }
       // the new token: RoPE at p, into the tile and into its ring slot (the slot belongs to the token leaving
       // the window, which no CTA reads)
-      if (cur_row >= 0 && cur_row < nr && warp == cur_row / kGatherRows) {
+      if (cur_row >= 0 && cur_row < nr && warp == (cur_row >> 5)) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int ch = lane + 32 * hh;
@@ -354,32 +357,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       tc::mbar_arrive(rows_full);
-      // ---- scores of this thread's row (and, in warp 3, of row 128 + lane)
+      // ---- scores of this thread's row: rows 0-127 in the first product, rows 128-159 in lanes 0-31 of the
+      // second (read by warp 4, whose TMEM lane quarter is lanes 0-31)
       if (tc::named_bar_any(2, kMain, !tc::mbar_wait(s_full, par))) { failed = true; break; }
       tc::fence_after_sync();
-      const bool two = warp == 3 && nr > 128;
-      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
       float sv[64];
       float cp[64];
-      {
+      if (warp < 4 || nr > 128) {
+        const uint32_t ta = warp < 4 ? tm_s + ((uint32_t)(warp * 32) << 16) : tm_s + 64;
         uint32_t u[64];
-        tc::tmem_ld32(tm_s + lane_base, u);
-        tc::tmem_ld32(tm_s + lane_base + 32, u + 32);
+        tc::tmem_ld32(ta, u);
+        tc::tmem_ld32(ta + 32, u + 32);
         tc::tmem_wait_ld();
         const bool valid = row < nr && rowc[row] != kRowNone;
 #pragma unroll
         for (int h = 0; h < 64; ++h) sv[h] = valid ? __uint_as_float(u[h]) * a.scale2 : -INFINITY;
+      } else {
 #pragma unroll
-        for (int h = 0; h < 64; ++h) cp[h] = sv[h];
-        if (two) {
-          tc::tmem_ld32(tm_s + 64 + lane_base, u);
-          tc::tmem_ld32(tm_s + 96 + lane_base, u + 32);
-          tc::tmem_wait_ld();
-          const bool valid2 = 128 + lane < nr && rowc[128 + lane] != kRowNone;
-#pragma unroll
-          for (int h = 0; h < 64; ++h) cp[h] = fmaxf(cp[h], valid2 ? __uint_as_float(u[h]) * a.scale2 : -INFINITY);
-        }
+        for (int h = 0; h < 64; ++h) sv[h] = -INFINITY;
       }
+#pragma unroll
+      for (int h = 0; h < 64; ++h) cp[h] = sv[h];
       {
         const float2 m2 = reduce_scatter64<true>(cp);
         red[warp * 64 + 2 * lane] = m2.x;
@@ -388,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       if (tid == 0) *flag = 0;
       tc::named_bar(1, kMain);
       if (tid < 64) {
-        const float mt = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+        float mt = red[tid];
+#pragma unroll
+        for (int w = 1; w < kMainWarps; ++w) mt = fmaxf(mt, red[64 * w + tid]);
         const float old = mref[tid];
         float nw = old;
         if (old == -INFINITY || mt > old + kRescaleAt) nw = mt;
@@ -402,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         lsum[tid] *= al;
       }
       tc::named_bar(1, kMain);
-      if (*flag) {
+      if (*flag && warp < 4) {
         // raise the reference max: O^T (earlier chunks, all retired) *= alpha per head
         for (int m = 0; m < 4; ++m) {
-          const uint32_t ta = tm_o + 64 * m + lane_base;
+          const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
           uint32_t u[32];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -421,19 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       // ---- probabilities (fp32 for the sums, bf16 hi + lo for the PV product)
       float pe[64];
       write_p(pbuf, row, sv, mref, pe);
-      if (two) {
-        uint32_t u[64];
-        tc::tmem_ld32(tm_s + 64 + lane_base, u);
-        tc::tmem_ld32(tm_s + 96 + lane_base, u + 32);
-        tc::tmem_wait_ld();
-        const bool valid2 = 128 + lane < nr && rowc[128 + lane] != kRowNone;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) sv[h] = valid2 ? __uint_as_float(u[h]) * a.scale2 : -INFINITY;
-        float pe2[64];
-        write_p(pbuf, 128 + lane, sv, mref, pe2);
-#pragma unroll
-        for (int h = 0; h < 64; ++h) pe[h] += pe2[h];
-      }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       tc::mbar_arrive(p_full);
@@ -443,7 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         red_sum[warp * 64 + 2 * lane + 1] = s2.y;
       }
       tc::named_bar(1, kMain);
-      if (tid < 64) lsum[tid] += (red_sum[tid] + red_sum[64 + tid]) + (red_sum[128 + tid] + red_sum[192 + tid]);
+      if (tid < 64) {
+        float st = red_sum[tid];
+#pragma unroll
+        for (int w = 1; w < kMainWarps; ++w) st += red_sum[64 * w + tid];
+        lsum[tid] += st;
+      }
       if (tc::named_bar_any(2, kMain, !tc::mbar_wait(pv_done, par))) { failed = true; break; }
       tc::fence_after_sync();
     }
@@ -455,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       rsin[tid] = sn;
     }
     tc::named_bar(1, kMain);
-    if (!failed) {
-      // ---- epilogue: thread owns latent dim d = 128 m + tid of each O^T tile
+    if (!failed && warp < 4) {
+      // ---- epilogue (warps 0-3): thread owns latent dim d = 128 m + tid of each O^T tile
       const bool any = nchunks > 0;
       if (a.S > 1) {
         if (tid < 64) {
@@ -514,13 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   tc::fence_before_sync();
   __syncthreads();
   // retire every MMA before tensor memory is released
-  if (warp == 4 && lane == 0) {
+  if (warp == kMmaWarp && lane == 0) {
     tc::mma_commit(drain);
     if (!tc::mbar_wait(drain, 0)) atomicOr(a.err, tc::kErrTimeout);
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 4) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 int g_sms_dec = 0;
