@@ -386,15 +386,25 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
                             const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
                             const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,
                             const AttendWs& ws, int32_t* err, cudaStream_t s) {
-  if (tc_attend_decode_supported(L)) {
-    // the workspace holds ws.S partials per query; any split count up to it fits
-    const int S = tc_attend_decode_splits(B, (sel ? L.topk : cap) + L.W, ws.S);
+  // the workspace holds ws.S partials per query; the one-chunk decode kernel needs splits of <= 160 rows, which
+  // it always has except for a layer with an indexer called without a selection (every visible row)
+  const int S = tc_attend_decode_supported(L) ? tc_attend_decode_splits(B, (sel ? L.topk : cap) + L.W, ws.S) : 0;
+  if (S > 0) {
     cudaError_t e = launch_tc_attend_decode(L, q, pool, window, kv_new, sel, n_sel, n_rows, pos, cap, sink, inv_freq,
                                             B, S, ws.part_ml, ws.part_acc, out, err, s);
     if (e != cudaSuccess || S == 1) return e;
     if (S <= 32) return launch_tc_merge(L, ws.part_ml, ws.part_acc, S, B, sink, pos, inv_freq, out, s);
     CSA_LAUNCH(k_attend_merge<T>, dim3(L.H, B), dim3(max(32, min(1024, L.D / 8))), S * sizeof(float), s,
                ws.part_ml, ws.part_acc, S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out));
+    return cudaGetLastError();
+  }
+  if (tc_attend_supported(L)) {
+    cudaError_t e = launch_tc_attend(L, q, pool, window, nullptr, kv_new, sel, n_sel, n_rows, pos, 0, cap, sink,
+                                     inv_freq, B, ws.S, ws.part_ml, ws.part_acc, out, err, s);
+    if (e != cudaSuccess || ws.S == 1) return e;
+    if (ws.S <= 32) return launch_tc_merge(L, ws.part_ml, ws.part_acc, ws.S, B, sink, pos, inv_freq, out, s);
+    CSA_LAUNCH(k_attend_merge<T>, dim3(L.H, B), dim3(max(32, min(1024, L.D / 8))), ws.S * sizeof(float), s,
+               ws.part_ml, ws.part_acc, ws.S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out));
     return cudaGetLastError();
   }
   CSA_LAUNCH(k_window_append<T>, dim3(B), dim3(128), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(window), L.W, L.D, L.R, pos,

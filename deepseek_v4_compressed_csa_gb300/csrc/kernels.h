@@ -120,8 +120,8 @@ cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* pa
 
 // ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_decode_supported(const Dims& L);
-// Key splits per query for Q queries of at most max_rows rows: a split is one chunk of <= 160 rows where the
-// workspace allows, more splits while every CTA still fits one wave; never more than max_splits.
+// Key splits per query for Q queries of at most max_rows rows: every split <= 160 rows, more splits while every
+// CTA still fits one wave; 0 when max_splits cannot hold enough splits.
 int tc_attend_decode_splits(int Q, int max_rows, int max_splits);
 // One CTA per (query, split).  S > 1 writes (m, l, acc) partials (merge follows), S == 1 the final output.
 // The new token kv_new[b] is roped in-kernel and written to ring slot pos[b] % W.

@@ -10,25 +10,25 @@
 //
 // Why 160 rows: a decode query attends to topk + W = 640 rows; four splits of
 // 160 put a batch of 32 on 128 CTAs, one wave of the 152 SMs, where 128-row
-// splits would need 160 CTAs and a second wave.  The rows of a chunk (selected
-// pool rows, then window tokens, the newest one roped here) are gathered with
-// cp.async into one 160-row, 128-byte-swizzled shared tile that serves both as K
-// (K-major) and as V^T (MN-major), so each row is read from memory once.
+// splits would need 160 CTAs and a second wave.  Each CTA takes its split's rows
+// (selected pool rows, then window tokens, the newest one roped here) as one
+// chunk, gathered with cp.async into one 160-row, 128-byte-swizzled shared tile
+// that serves both as K (K-major) and as V^T (MN-major), so each row is read from
+// memory once.
 //   QK       S^T = K Q^T twice, M = 128 (TMEM lanes), N = 64 heads, K = 512:
 //            rows 0-127, and rows 128-255 of which lanes 0-31 (rows 128-159) are
 //            used (the rest read neighbouring, initialised shared memory);
 //   softmax  five warps, thread = row (warp 4 reads lanes 0-31 of the second
 //            product); per-head column max and sum by a warp reduce-scatter and a
-//            5-warp combine; the reference max is raised only when a chunk exceeds
-//            it by 2^8 (O rescaled in TMEM);
-//   PV       O^T += V^T P^T: M = 128 latent dims x 4 tiles, N = 64 heads, K = the
-//            chunk's rows.  Once both score products have retired, the query's
-//            shared memory holds P^T as two bf16 parts, P_hi = bf16(P) and
-//            P_lo = bf16(P - P_hi), multiplied in turn (~16 bits of P).
+//            5-warp combine;
+//   PV       O^T = V^T [P_hi | P_lo]^T: M = 128 latent dims x 4 tiles, N = 2 x 64,
+//            K = the chunk's rows.  Once both score products have retired, the
+//            query's shared memory holds P^T as two bf16 parts side by side,
+//            P_hi = bf16(P) and P_lo = bf16(P - P_hi), so one read of V serves both
+//            and the epilogue adds the two halves (~16 bits of P in the product).
 // With one split the epilogue finalises the output (sink, normalisation, bf16,
 // inverse RoPE, bf16); with several it writes (m, l, acc) partials for the merge
-// kernel.  A split longer than 160 rows takes several chunks and copies the
-// query again for each.
+// kernel.  Splits are never longer than 160 rows (the caller picks enough).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -49,9 +49,8 @@ constexpr int kMainWarps = kCR / 32;     // gather / softmax threads: one per ro
 constexpr int kMain = 32 * kMainWarps;
 constexpr int kMmaWarp = kMainWarps;     // TMEM owner and MMA issuer
 constexpr int kThreads = kMain + 32;
-constexpr int kTmemCols = 512;           // S^T rows 0-127: cols 0-63; rows 128-255: 64-127; O^T: 128-383
+constexpr int kTmemCols = 512;           // S^T (cols 0-127), then O^T over all 512 (hi | lo per 128-dim tile)
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleAt = 8.f;        // log2 headroom before O is rescaled
 
 // shared memory: rows | query (after the score products: P_hi, P_lo, column reductions) | small state
 constexpr int kOffQ = kRowsBytes;
@@ -60,11 +59,9 @@ constexpr int kOffRedSum = kOffRed + kMainWarps * 64 * 4;
 static_assert(kOffRedSum + kMainWarps * 64 * 4 <= kOffQ + kQBytes, "reductions fit in the query region");
 constexpr int kOffMref = kOffQ + kQBytes;
 constexpr int kOffLsum = kOffMref + 64 * 4;
-constexpr int kOffAlpha = kOffLsum + 64 * 4;
-constexpr int kOffRope = kOffAlpha + 64 * 4;    // cos[32], sin[32]
+constexpr int kOffRope = kOffLsum + 64 * 4;     // cos[32], sin[32]
 constexpr int kOffRowc = kOffRope + 64 * 4;     // [160] row codes
-constexpr int kOffFlag = kOffRowc + kCR * 4;
-constexpr int kOffBars = kOffFlag + 16;         // 4 mbarriers
+constexpr int kOffBars = kOffRowc + kCR * 4;    // 5 mbarriers
 constexpr int kOffTmem = kOffBars + 8 * 8;
 constexpr int kSmem = kOffTmem + 16 + 1024;     // + alignment slack
 static_assert(kSmem <= 232448, "shared memory per block");
@@ -132,10 +129,11 @@ __device__ __forceinline__ Item make_item(const DecArgs& a) {
   return it;
 }
 
-// Code of row r (0 .. nsel+nwin-1) of the item; an out-of-range selection is reported and left empty.
-__device__ __forceinline__ int row_code(const DecArgs& a, const Item& it, int r) {
+// Code of row r (0 .. nsel+nwin-1) of the item, j = sel[q][r] when r < nsel and a selection is given; an
+// out-of-range selection is reported and left empty.
+__device__ __forceinline__ int row_code(const DecArgs& a, const Item& it, int r, int j) {
   if (r < it.nsel) {
-    const int j = a.sel ? a.sel[(size_t)it.q * a.topk + r] : r;
+    if (!a.sel) j = r;
     if (j >= 0 && j < it.nrows) return it.b * a.cap + j;
     atomicOr(a.err, CSA_DEV_RANGE);
     return kRowNone;
@@ -198,15 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
   float* mref = reinterpret_cast<float*>(smem + kOffMref);
   float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
-  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
   float* rcos = reinterpret_cast<float*>(smem + kOffRope);
   float* rsin = rcos + 32;
   int* rowc = reinterpret_cast<int*>(smem + kOffRowc);
-  int* flag = reinterpret_cast<int*>(smem + kOffFlag);
   uint64_t* rows_full = reinterpret_cast<uint64_t*>(smem + kOffBars);  // rows and roped query in place
   uint64_t* s_full = rows_full + 1;    // both score products retired
   uint64_t* p_full = rows_full + 2;    // both P parts written
-  uint64_t* pv_done = rows_full + 3;   // PV retired: rows and P regions free, O complete
+  uint64_t* pv_done = rows_full + 3;   // PV retired
   uint64_t* drain = rows_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
 
@@ -228,22 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s = tmem;         // S^T, rows 0-127 (cols 0-63) and rows 128-255 (cols 64-127)
-  const uint32_t tm_o = tmem + 128;   // O^T, 4 x 64 columns
+  const uint32_t tm_s = tmem;  // S^T: rows 0-127 in cols 0-63, rows 128-255 in cols 64-127
+  const uint32_t tm_o = tmem;  // O^T tile m: cols 128m + (0-63: P_hi part, 64-127: P_lo part); overwrites S^T
   const Item it = make_item(a);
-  const int nchunks = (it.r_end - it.r_begin + kCR - 1) / kCR;
+  const int nr = min(kCR, it.r_end - it.r_begin);
   bool failed = false;
 
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && nr > 0) {
       constexpr uint32_t id_qk = tc::idesc_bf16(128, 64);
-      constexpr uint32_t id_pv = tc::idesc_bf16(128, 64, true, true);
+      constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, true, true);
       const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf), p_base = tc::smem_u32(pbuf);
-      for (int c = 0; c < nchunks; ++c) {
-        const uint32_t par = c & 1;
-        const int nr = min(kCR, it.r_end - it.r_begin - c * kCR);
-        if (!tc::mbar_wait(rows_full, par)) { failed = true; break; }
+      do {
+        if (!tc::mbar_wait(rows_full, 0)) { failed = true; break; }
         tc::fence_after_sync();
 #pragma unroll 1
         for (int half = 0; half < (nr > 128 ? 2 : 1); ++half) {
@@ -256,113 +250,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
           }
         }
         tc::mma_commit(s_full);
-        if (!tc::mbar_wait(p_full, par)) { failed = true; break; }
+        if (!tc::mbar_wait(p_full, 0)) { failed = true; break; }
         tc::fence_after_sync();
+        // O^T tile m += V^T [P_hi | P_lo]^T: one read of V serves both parts (N = 2 x 64)
         const int ksteps = (nr + 15) >> 4;
-#pragma unroll 1
-        for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 4; ++m) {
 #pragma unroll 1
-            for (int kk = 0; kk < ksteps; ++kk) {
-              const uint64_t ad = tc::sdesc_mnmajor_sw128(r_base + 2 * m * kBox + kk * 2048, kBox, 1024);
-              const uint64_t bd = tc::sdesc_mnmajor_sw128(p_base + part * kPPart + kk * 2048, 8192, 1024);
-              tc::mma_bf16(tm_o + 64 * m, ad, bd, id_pv, (c | part | kk) != 0);
-            }
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = tc::sdesc_mnmajor_sw128(r_base + 2 * m * kBox + kk * 2048, kBox, 1024);
+            const uint64_t bd = tc::sdesc_mnmajor_sw128(p_base + kk * 2048, kPPart, 1024);
+            tc::mma_bf16(tm_o + 128 * m, ad, bd, id_pv, kk > 0);
           }
         }
         tc::mma_commit(pv_done);
-      }
+      } while (false);
     }
     __syncwarp();
     failed = __shfl_sync(0xffffffffu, (int)failed, 0) != 0;
   } else {
     // ------------------------------------------------------------ main warps (160 threads, one per row)
     const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
-    const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
-    const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
+    const int row = tid;
     const int last_row = it.nsel + it.nwin - 1;  // the new token (when p >= 0)
-    auto copy_query = [&]() {  // 64 head rows of 512 dims, K-major swizzled
+    if (it.r_end - it.r_begin > kCR && tid == 0) atomicOr(a.err, CSA_DEV_STATE);  // callers keep splits <= 160
+    // this thread's selection is loaded before the query copies are issued, so the two overlap
+    const int r_abs = it.r_begin + row;
+    const int j_sel = (a.sel && row < nr && r_abs < it.nsel) ? a.sel[(size_t)it.q * a.topk + r_abs] : 0;
+    {
+      const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
 #pragma unroll 8
       for (int e = tid; e < kAH * 64; e += kMain) {
         const int h = e >> 6, ch = e & 63;
         tc::cp_async16(q_base + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4),
                        qsrc + (size_t)h * kAD + ch * 8, 16u);
       }
-    };
-    copy_query();
-    if (tid < 64) {
-      mref[tid] = -INFINITY;
-      lsum[tid] = 0.f;
     }
-    bool table_ready = false;
-    const int row = tid;
-
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t par = c & 1;
-      const int r0 = it.r_begin + c * kCR;
-      const int nr = min(kCR, it.r_end - r0);
-      if (c > 0) copy_query();  // the previous chunk's P overwrote it
-      for (int r = tid; r < kCR; r += kMain) rowc[r] = r < nr ? row_code(a, it, r0 + r) : kRowNone;
-      tc::named_bar(1, kMain);
-      // ---- gather: warp w copies rows 32w .. 32w+31, 2 x 512 contiguous bytes per instruction
-      const int cur_row = (it.p >= 0) ? last_row - r0 : -1;
+    rowc[row] = row < nr ? row_code(a, it, r_abs, j_sel) : kRowNone;
+    tc::named_bar(1, kMain);
+    // ---- gather: warp w copies rows 32w .. 32w+31, 2 x 512 contiguous bytes per instruction
+    const int cur_row = (it.p >= 0) ? last_row - it.r_begin : -1;
 #pragma unroll 4
-      for (int rr = 0; rr < 32; ++rr) {
-        const int r = warp * 32 + rr;
-        const int code = rowc[r];
-        if (code == kRowNew) continue;  // roped below
-        const __nv_bfloat16* src = code_ptr(a, code);
+    for (int rr = 0; rr < 32; ++rr) {
+      const int r = warp * 32 + rr;
+      const int code = rowc[r];
+      if (code == kRowNew) continue;  // roped below
+      const __nv_bfloat16* src = code_ptr(a, code);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int ch = lane + 32 * hh;
-          const uint32_t dst = r_base + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          tc::cp_async16(dst, src ? static_cast<const void*>(src + ch * 8) : static_cast<const void*>(a.pool),
-                         src ? 16u : 0u);
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        const int ch = lane + 32 * hh;
+        const uint32_t dst = r_base + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        tc::cp_async16(dst, src ? static_cast<const void*>(src + ch * 8) : static_cast<const void*>(a.pool),
+                       src ? 16u : 0u);
       }
-      // RoPE table of this query's position, computed while the copies are in flight
-      if (!table_ready) {
-        if (tid < 32) {
-          float cs, sn;
-          rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
-          rcos[tid] = cs;
-          rsin[tid] = sn;
-        }
-        tc::named_bar(1, kMain);
-        table_ready = true;
-      }
-      // the new token: RoPE at p, into the tile and into its ring slot (the slot belongs to the token leaving
-      // the window, which no CTA reads)
-      if (cur_row >= 0 && cur_row < nr && warp == (cur_row >> 5)) {
+    }
+    // RoPE table of this query's position, computed while the copies are in flight
+    if (tid < 32) {
+      float cs, sn;
+      rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
+      rcos[tid] = cs;
+      rsin[tid] = sn;
+    }
+    tc::named_bar(1, kMain);
+    // the new token: RoPE at p, into the tile and into its ring slot (the slot belongs to the token leaving the
+    // window, which no CTA reads)
+    if (cur_row >= 0 && cur_row < nr && warp == (cur_row >> 5)) {
+      const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int ch = lane + 32 * hh;
-          uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
-          if (ch >= 56) rope8(raw, ch, rcos, rsin);
-          *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
-          *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        const int ch = lane + 32 * hh;
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
+        if (ch >= 56) rope8(raw, ch, rcos, rsin);
+        *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
+        *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
       }
-      tc::cp_async_wait_all();
-      tc::named_bar(1, kMain);  // every thread's share of the query block has landed
+    }
+    tc::cp_async_wait_all();
+    tc::named_bar(1, kMain);  // every thread's share of the query block has landed
 #pragma unroll
-      for (int e = tid; e < kAH * 8; e += kMain) {
-        const int h = e >> 3, ch = 56 + (e & 7);
-        uint4* slot = reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4));
-        uint4 raw = *slot;
-        rope8(raw, ch, rcos, rsin);
-        *slot = raw;
+    for (int e = tid; e < kAH * 8; e += kMain) {
+      const int h = e >> 3, ch = 56 + (e & 7);
+      uint4* slot = reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4));
+      uint4 raw = *slot;
+      rope8(raw, ch, rcos, rsin);
+      *slot = raw;
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    tc::mbar_arrive(rows_full);
+    do {
+      if (nr <= 0) {
+        if (tid < 64) {
+          mref[tid] = -INFINITY;
+          lsum[tid] = 0.f;
+        }
+        break;
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(rows_full);
-      // ---- scores of this thread's row: rows 0-127 in the first product, rows 128-159 in lanes 0-31 of the
-      // second (read by warp 4, whose TMEM lane quarter is lanes 0-31)
-      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(s_full, par))) { failed = true; break; }
+      // ---- scores of this thread's row: rows 0-127 from the first product, rows 128-159 from lanes 0-31 of
+      // the second (read by warp 4, whose TMEM lane quarter is lanes 0-31)
+      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(s_full, 0))) { failed = true; break; }
       tc::fence_after_sync();
       float sv[64];
-      float cp[64];
       if (warp < 4 || nr > 128) {
         const uint32_t ta = warp < 4 ? tm_s + ((uint32_t)(warp * 32) << 16) : tm_s + 64;
         uint32_t u[64];
@@ -376,48 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
 #pragma unroll
         for (int h = 0; h < 64; ++h) sv[h] = -INFINITY;
       }
-#pragma unroll
-      for (int h = 0; h < 64; ++h) cp[h] = sv[h];
       {
+        float cp[64];
+#pragma unroll
+        for (int h = 0; h < 64; ++h) cp[h] = sv[h];
         const float2 m2 = reduce_scatter64<true>(cp);
         red[warp * 64 + 2 * lane] = m2.x;
         red[warp * 64 + 2 * lane + 1] = m2.y;
       }
-      if (tid == 0) *flag = 0;
       tc::named_bar(1, kMain);
       if (tid < 64) {
         float mt = red[tid];
 #pragma unroll
         for (int w = 1; w < kMainWarps; ++w) mt = fmaxf(mt, red[64 * w + tid]);
-        const float old = mref[tid];
-        float nw = old;
-        if (old == -INFINITY || mt > old + kRescaleAt) nw = mt;
-        float al = 1.f;
-        if (old != -INFINITY && nw != old) {
-          al = exp2f(old - nw);
-          atomicOr(flag, 1);
-        }
-        alpha[tid] = al;
-        mref[tid] = nw;
-        lsum[tid] *= al;
+        mref[tid] = mt;
       }
       tc::named_bar(1, kMain);
-      if (*flag && warp < 4) {
-        // raise the reference max: O^T (earlier chunks, all retired) *= alpha per head
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
-          uint32_t u[32];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            tc::tmem_ld32(ta + 32 * half, u);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha[32 * half + i]);
-            tc::tmem_st32(ta + 32 * half, u);
-          }
-        }
-        tc::tmem_wait_st();
-      }
       // ---- probabilities (fp32 for the sums, bf16 hi + lo for the PV product)
       float pe[64];
       write_p(pbuf, row, sv, mref, pe);
@@ -434,54 +396,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         float st = red_sum[tid];
 #pragma unroll
         for (int w = 1; w < kMainWarps; ++w) st += red_sum[64 * w + tid];
-        lsum[tid] += st;
+        lsum[tid] = st;
       }
-      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(pv_done, par))) { failed = true; break; }
+      if (tc::named_bar_any(2, kMain, !tc::mbar_wait(pv_done, 0))) { failed = true; break; }
       tc::fence_after_sync();
-    }
+    } while (false);
     tc::cp_async_wait_all();
-    if (!table_ready && tid < 32) {
-      float cs, sn;
-      rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
-      rcos[tid] = cs;
-      rsin[tid] = sn;
-    }
     tc::named_bar(1, kMain);
     if (!failed && warp < 4) {
-      // ---- epilogue (warps 0-3): thread owns latent dim d = 128 m + tid of each O^T tile
-      const bool any = nchunks > 0;
+      // ---- epilogue (warps 0-3): thread owns latent dim d = 128 m + tid of each O^T tile; O = hi + lo parts
+      auto load_o = [&](int m, float (&o)[64]) {
+        if (nr <= 0) {
+#pragma unroll
+          for (int h = 0; h < 64; ++h) o[h] = 0.f;
+          return;
+        }
+        const uint32_t ta = tm_o + 128 * m + ((uint32_t)(warp * 32) << 16);
+        uint32_t u[64];
+        tc::tmem_ld32(ta, u);
+        tc::tmem_ld32(ta + 32, u + 32);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 64; ++h) o[h] = __uint_as_float(u[h]);
+        tc::tmem_ld32(ta + 64, u);
+        tc::tmem_ld32(ta + 96, u + 32);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 64; ++h) o[h] += __uint_as_float(u[h]);
+      };
       if (a.S > 1) {
         if (tid < 64) {
           const size_t idx = ((size_t)it.q * a.S + it.s) * kAH + tid;
           a.part_ml[idx * 2] = mref[tid] == -INFINITY ? -INFINITY : mref[tid] * kLn2;
           a.part_ml[idx * 2 + 1] = lsum[tid];
         }
-        if (any) {
+        if (nr > 0) {
           for (int m = 0; m < 4; ++m) {
-            const int d = 128 * m + tid;
-            uint32_t u[64];
-            const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
-            tc::tmem_ld32(ta, u);
-            tc::tmem_ld32(ta + 32, u + 32);
-            tc::tmem_wait_ld();
-            float* dst = a.part_acc + (((size_t)it.q * a.S + it.s) * kAH) * kAD + d;
+            float o[64];
+            load_o(m, o);
+            float* dst = a.part_acc + (((size_t)it.q * a.S + it.s) * kAH) * kAD + 128 * m + tid;
 #pragma unroll
-            for (int h = 0; h < 64; ++h) dst[(size_t)h * kAD] = __uint_as_float(u[h]);
+            for (int h = 0; h < 64; ++h) dst[(size_t)h * kAD] = o[h];
           }
         }
       } else {
         for (int m = 0; m < 4; ++m) {
           const int d = 128 * m + tid;
-          uint32_t u[64];
-          if (any) {
-            const uint32_t ta = tm_o + 64 * m + ((uint32_t)(warp * 32) << 16);
-            tc::tmem_ld32(ta, u);
-            tc::tmem_ld32(ta + 32, u + 32);
-            tc::tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int h = 0; h < 64; ++h) u[h] = 0u;
-          }
+          float o[64];
+          load_o(m, o);
           __nv_bfloat16* dst = a.out + (size_t)it.q * kAH * kAD + d;
 #pragma unroll
           for (int h = 0; h < 64; ++h) {
@@ -490,13 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
             const float M2 = fmaxf(z2, mr);
             const float f = mr == -INFINITY ? 0.f : exp2f(mr - M2);
             const float Z = exp2f(z2 - M2) + lsum[h] * f;
-            float o = rnd<__nv_bfloat16>(__uint_as_float(u[h]) * (f / Z));
-            const float partner = __shfl_xor_sync(0xffffffffu, o, 1);
+            float v = rnd<__nv_bfloat16>(o[h] * (f / Z));
+            const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
             if (d >= kAD - 64) {
               const int i = (d - (kAD - 64)) >> 1;
-              o = (d & 1) ? fmaf(-partner, rsin[i], o * rcos[i]) : fmaf(o, rcos[i], partner * rsin[i]);
+              v = (d & 1) ? fmaf(-partner, rsin[i], v * rcos[i]) : fmaf(v, rcos[i], partner * rsin[i]);
             }
-            dst[(size_t)h * kAD] = __float2bfloat16_rn(o);
+            dst[(size_t)h * kAD] = __float2bfloat16_rn(v);
           }
         }
       }
@@ -524,17 +486,19 @@ bool tc_attend_decode_supported(const Dims& L) {
 }
 
 // Splits per query for at most max_rows rows per query: enough that a split is one chunk (<= 160 rows), more
-// (up to one per 128 rows) while every CTA still fits one wave of the device's SMs; never above max_splits.
+// (up to one per 128 rows) while every CTA still fits one wave of the device's SMs.  0 when max_splits (the
+// workspace's partial capacity) cannot hold enough.
 int tc_attend_decode_splits(int Q, int max_rows, int max_splits) {
   if (!g_sms_dec) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_sms_dec, cudaDevAttrMultiProcessorCount, dev);
   }
-  const int s_min = (max_rows + kCR - 1) / kCR;
+  const int s_min = max(1, (max_rows + kCR - 1) / kCR);
+  if (s_min > max_splits) return 0;
   const int s_tiles = (max_rows + 127) / 128;
   const int s_fit = g_sms_dec / max(1, Q);
-  return max(1, min(max_splits, max(s_min, min(s_fit, s_tiles))));
+  return min(max_splits, max(s_min, min(s_fit, s_tiles)));
 }
 
 cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,

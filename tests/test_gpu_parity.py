@@ -276,6 +276,33 @@ def test_ragged_batch_edges():
     assert n_sel.cpu().tolist()[3] == 512  # 2047 + 5 tokens -> 513 rows visible: sparse, 512 kept
 
 
+def test_decode_without_selection_attends_every_visible_row():
+    """A layer with an indexer called without a selection attends to every visible row: up to 1300 rows per
+    query here, more than the workspace's splits can hold in 160-row chunks, so the multi-tile kernel serves
+    it.  Checked against the oracle's attention over all visible rows."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=3)
+    ctxs = [1000, 3001, 5202]
+    cap = max(ctxs) // 4 + 8
+    host = _ragged_cache(cfg, cap, ctxs)
+    run = G.Runner(cfg)
+    st_g = G.DevCache(host)
+    layer = oracle_layer(cfg)
+    st_o = oracle_state(host)
+    sink, invf = f64(csa_synth.sinks(cfg)), f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    si = csa_synth.step_inputs(cfg, 0, B=len(ctxs))
+    out = torch.empty(len(ctxs), cfg.H, cfg.D, dtype=cfg.storage, device="cuda")
+    csa.attend_decode(run.L, G.dev(si.q), G.dev(si.kv), run.sink, st_g.window, st_g.pool, st_g.n_rows, None, None,
+                      st_g.pos, run.inv_freq, out, err=run.err)
+    ref, window, err = O.attend_decode(layer, f64(si.q), f64(si.kv), sink, st_o["window"], st_o["pool"],
+                                       st_o["n_rows"], None, None, st_o["pos"], invf)
+    torch.cuda.synchronize()
+    assert err == 0 and run.err.item() == 0
+    for b in range(len(ctxs)):
+        G.check_rows(out[b].cpu(), ref[b], layer.dtype, what=f"ctx {ctxs[b]} output", R=layer.R)
+        G.check_pool_rows(st_g.window[b].cpu(), window[b], "bf16", "window")  # the new token's ring slot
+
+
 def test_topk_ties_go_to_lower_rows():
     """All index keys equal -> all scores tie exactly; the selection must be rows 0 .. topk-1."""
     cfg = csa_synth.CONFIGS[3].replace(B=2)
