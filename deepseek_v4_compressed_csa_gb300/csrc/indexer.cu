@@ -365,11 +365,109 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   if (threadIdx.x == 0) n_sel[q] = min(total, topk);
 }
 
+// Exact top-k with every key in registers, for up to kTopkRegKeys x 1024 visible rows: thread t owns the
+// contiguous rows [K t, K t + K), K = ceil(n_vis / 1024), so the final pass writes the kept rows in ascending
+// order with two block scans.  The threshold is found by the same 11/11/10-bit radix select as k_topk_smem
+// (2048-bin shared histograms, double-buffered so the next pass's bins are cleared during the current one).
+constexpr int kTopkRegKeys = 16;
+
+__global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ scores, int cap,
+                                                   const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
+                                                   int pos0, int ratio, int topk, int32_t* __restrict__ sel,
+                                                   int32_t* __restrict__ n_sel) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int hist[2][2048];
+  __shared__ int warp_tot[32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int p = query_pos(pos, pos0, q);
+  const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
+  int32_t* out = sel + (size_t)q * topk;
+  if (nvis <= topk) {
+    for (int i = threadIdx.x; i < topk; i += blockDim.x) out[i] = (i < nvis) ? i : -1;
+    if (threadIdx.x == 0) n_sel[q] = max(nvis, 0);
+    return;
+  }
+  const int K = (nvis + 1023) >> 10;
+  const int r0 = threadIdx.x * K;
+  const float* sc = scores + (size_t)q * cap + r0;
+  uint32_t uk[kTopkRegKeys];
+#pragma unroll
+  for (int i = 0; i < kTopkRegKeys; ++i) uk[i] = (i < K && r0 + i < nvis) ? ord_key(__ldg(sc + i)) : 0u;
+  hist[0][2 * threadIdx.x] = 0;
+  hist[0][2 * threadIdx.x + 1] = 0;
+  __syncthreads();
+  uint32_t prefix = 0, mask = 0;
+  int need = topk;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    int* h = hist[pass & 1];
+#pragma unroll
+    for (int i = 0; i < kTopkRegKeys; ++i)
+      if (i < K && r0 + i < nvis && (uk[i] & mask) == prefix) atomicAdd(&h[(uk[i] >> shift) & dmask], 1);
+    hist[(pass + 1) & 1][2 * threadIdx.x] = 0;  // the next pass's bins
+    hist[(pass + 1) & 1][2 * threadIdx.x + 1] = 0;
+    __syncthreads();
+    // thread t owns bins 2047-2t and 2046-2t (descending order)
+    const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
+    const int c_hi = h[b_hi], c_lo = h[b_lo];
+    const int incl = block_incl_scan(c_hi + c_lo, warp_tot);
+    const int excl = incl - c_hi - c_lo;
+    if (excl < need && need <= incl) {
+      if (excl + c_hi >= need) {
+        s_prefix = prefix | ((uint32_t)b_hi << shift);
+        s_need = need - excl;
+      } else {
+        s_prefix = prefix | ((uint32_t)b_lo << shift);
+        s_need = need - excl - c_hi;
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= dmask << shift;
+  }
+  // prefix = order key of the k-th largest score: keep every key above it and the `need` lowest-indexed keys
+  // equal to it, in ascending row order
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkRegKeys; ++i) {
+    const bool v = i < K && r0 + i < nvis;
+    gt += (v && uk[i] > prefix) ? 1 : 0;
+    eq += (v && uk[i] == prefix) ? 1 : 0;
+  }
+  const int eq_before = block_incl_scan(eq, warp_tot) - eq;
+  const int take = gt + max(0, min(eq, need - eq_before));
+  int o = block_incl_scan(take, warp_tot) - take;
+  const int total = warp_tot[31];
+  int eq_rank = eq_before;
+#pragma unroll
+  for (int i = 0; i < kTopkRegKeys; ++i) {
+    const bool v = i < K && r0 + i < nvis;
+    bool keep = v && uk[i] > prefix;
+    if (v && uk[i] == prefix) keep = eq_rank++ < need;
+    if (keep) {
+      if (o < topk) out[o] = r0 + i;
+      ++o;
+    }
+  }
+  for (int i = total + threadIdx.x; i < topk; i += blockDim.x) out[i] = -1;
+  if (threadIdx.x == 0) n_sel[q] = min(total, topk);
+}
+
 constexpr int kTopkSmemMaxCap = 52 * 1024;
 
 static cudaError_t launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
                         int pos0, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
-  if (cap <= kTopkSmemMaxCap) {
+  if (cap <= kTopkRegKeys * 1024) {
+    CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+  } else if (cap <= kTopkSmemMaxCap) {
     const size_t smem = (size_t)cap * 4 + 2048 * 4;
     cudaFuncSetAttribute(k_topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     CSA_LAUNCH(k_topk_smem, dim3(Q), dim3(1024), smem, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);

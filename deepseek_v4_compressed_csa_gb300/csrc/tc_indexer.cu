@@ -13,10 +13,13 @@
 // G = 4 queries of one sequence per MMA (N = 256), so a key tile is read once
 // per 4 queries.
 //
-// One persistent CTA per SM, 6 warps: warp 0 issues TMA loads (a resident
-// query block plus a 4-stage ring of 32 KB key tiles), warp 1 owns tensor
-// memory and issues the MMAs from one thread, warps 2-5 drain the two TMEM
-// accumulators and write fp32 scores.
+// One persistent CTA per SM, 8 warps: warp 0 issues TMA loads of a ring of 32 KB
+// key tiles, warp 1 owns tensor memory and issues the MMAs from one thread,
+// warps 2-5 drain the TMEM accumulators and write fp32 scores, warps 6-7 build
+// each query block in shared memory (RoPE at the query's position, bf16, the
+// 128-byte-swizzled K-major layout) and its scaled head weights, so no separate
+// preparation pass runs before the scan.  Decode keeps two query blocks and
+// four accumulators in flight.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -25,16 +28,35 @@ namespace csa {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * 128 * 2;  // 128 rows x 128 bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+constexpr int kPrepThreads = 64;                 // warps 6-7
+
+template <int G>
+struct IdxCfg {
+  static constexpr int N = 64 * G;               // MMA N: 64 heads x G queries
+  static constexpr int kQBytes = N * 128 * 2;    // one query block: 2 boxes of N rows x 128 B
+  static constexpr int kQSlots = G == 1 ? 2 : 1;
+  static constexpr int kStages = 4;
+  static constexpr int kAcc = G == 1 ? 4 : 2;    // TMEM accumulators of N columns
+  static constexpr int kOffK = kQSlots * kQBytes;
+  static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights
+  static constexpr int kOffRope = kOffW + kQSlots * N * 4;     // [G][32] cos, [G][32] sin
+  static constexpr int kOffBars = kOffRope + G * 64 * 4;
+  static constexpr int kNumBars = 2 * kStages + 3 * kQSlots + 2 * kAcc + 1;
+  static constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
+};
 
 struct IdxArgs {
+  const __nv_bfloat16* iq;  // [Q, 64, 128] index queries before RoPE
+  const __nv_bfloat16* iw;  // [Q, 64] head weights
+  const float* inv_freq;
+  float wscale;             // Di^-1/2 Hi^-1/2
+  int R;
   const int32_t* n_rows;
   const int32_t* pos;  // decode positions [Q] or null (prefill: pos0 + q)
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
-  const float* wts;  // [Q, 64] head weights (iw * scale)
   float* scores;     // [Q, cap]
   int32_t* err;
 };
@@ -44,51 +66,85 @@ __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
   const int b = a.pos ? q : 0;
   return min(min(a.n_rows[b], a.cap), (idx_qpos(a, q) + 1) / a.ratio);
 }
-// rows that group g must score (its last query sees the most rows); 0 if the
-// group's queries keep every visible row anyway
-__device__ __forceinline__ int group_rows(const IdxArgs& a, int g) {
+// tiles that group g must score (its last query sees the most rows); 0 if the group's queries keep every
+// visible row anyway
+__device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
   const int qlast = min(a.Q - 1, g * a.G + a.G - 1);
   const int nv = idx_nvis(a, qlast);
-  return nv > a.topk ? nv : 0;
+  return nv > a.topk ? (nv + kTileRows - 1) / kTileRows : 0;
 }
+
+// The CTA's work items are (group, tile) pairs it..i_end-1; a group's tiles past its visible rows are skipped.
+// Every role walks the same sequence: first unskipped item at or after `it`, or i_end.  The walker keeps
+// plain copies of the two fields it needs (a reference to the kernel's parameters would move them to local
+// memory) and the tile count of the last group it looked at.
+struct Walker {
+  int tpg, i_end, g_cached, nt_cached;
+  __device__ Walker(int tiles_per_group, int e) : tpg(tiles_per_group), i_end(e), g_cached(-1), nt_cached(0) {}
+  __device__ __forceinline__ int next(const IdxArgs& a, int it) {
+    while (it < i_end) {
+      const int g = it / tpg, t = it - g * tpg;
+      if (g != g_cached) {
+        g_cached = g;
+        nt_cached = group_tiles(a, g);
+      }
+      if (t < nt_cached) return it;
+      it = (g + 1) * tpg;
+    }
+    return i_end;
+  }
+  // whether item `it` is the last of its group in this CTA's sequence
+  __device__ __forceinline__ bool last_of_group(const IdxArgs& a, int it) {
+    const int nxt = next(a, it + 1);
+    return nxt >= i_end || nxt / tpg != it / tpg;
+  }
+};
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
-                      IdxArgs a) {
+    k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, IdxArgs a) {
+  using C = IdxCfg<G>;
+  constexpr int N = C::N;
   pdl_trigger();
-  constexpr int N = 64 * G;
-  constexpr int QBYTES = N * 128 * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qbuf = smem;                  // [2 boxes][N rows][128 B]
-  uint8_t* kbuf = smem + QBYTES;         // [kStages][2 boxes][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(kbuf + kStages * kTileBytes);
-  uint64_t* full = bars;                 // [kStages]
-  uint64_t* empty = bars + kStages;      // [kStages]
-  uint64_t* q_full = bars + 2 * kStages;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* acc_full = q_full + 2;       // [2]
-  uint64_t* acc_empty = q_full + 4;      // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 6);
+  uint8_t* qbuf = smem;                  // [kQSlots][2 boxes][N rows][128 B]
+  uint8_t* kbuf = smem + C::kOffK;       // [kStages][2 boxes][128 rows][128 B]
+  float* wbuf = reinterpret_cast<float*>(smem + C::kOffW);
+  float* rcos = reinterpret_cast<float*>(smem + C::kOffRope);
+  float* rsin = rcos + G * 32;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;                        // [kStages] key tile landed
+  uint64_t* empty = full + C::kStages;          // [kStages] key tile consumed
+  uint64_t* q_full = empty + C::kStages;        // [kQSlots] query block and weights written
+  uint64_t* q_empty = q_full + C::kQSlots;      // [kQSlots] last MMA of the group retired
+  uint64_t* w_empty = q_empty + C::kQSlots;     // [kQSlots] epilogue done with the group's weights
+  uint64_t* acc_full = w_empty + C::kQSlots;    // [kAcc]
+  uint64_t* acc_empty = acc_full + C::kAcc;     // [kAcc]
+  uint64_t* drain = acc_empty + C::kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int s = 0; s < C::kQSlots; ++s) {
+      tc::mbar_init(&q_full[s], kPrepThreads);
+      tc::mbar_init(&q_empty[s], 1);
+      tc::mbar_init(&w_empty[s], 4);
+    }
+    for (int i = 0; i < C::kAcc; ++i) {
       tc::mbar_init(&acc_full[i], 1);
       tc::mbar_init(&acc_empty[i], 128);
     }
+    tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
   }
   pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 2 * N);
+    tc::tmem_alloc(tmem_slot, C::kAcc * N);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -97,145 +153,230 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
-  const int i_begin = blockIdx.x * per, i_end = min(a.n_items, i_begin + per);
+  const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
+  Walker wk(a.tiles_per_group, i_end);
   bool failed = false;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ key tiles (TMA)
     if (lane == 0) {
       tc::tma_prefetch(&tm_keys);
-      tc::tma_prefetch(&tm_q);
-      int cur_g = -1, stage = 0, n_q = 0;
+      int stage = 0;
       uint32_t phase = 0;
-      int issued[kStages] = {0, 0, 0, 0};
-      for (int it = i_begin; it < i_end && !failed; ++it) {
+      int issued[C::kStages];
+#pragma unroll
+      for (int s = 0; s < C::kStages; ++s) issued[s] = 0;
+      for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
         const int g = it / a.tiles_per_group, t = it % a.tiles_per_group;
-        if (t * kTileRows >= group_rows(a, g)) continue;
-        if (g != cur_g) {
-          if (cur_g >= 0 && !tc::mbar_wait(q_empty, (n_q - 1) & 1)) { failed = true; break; }
-          tc::mbar_arrive_expect_tx(q_full, QBYTES);
-          tc::tma_load_2d(qbuf, &tm_q, q_full, 0, g * N);
-          tc::tma_load_2d(qbuf + QBYTES / 2, &tm_q, q_full, 64, g * N);
-          cur_g = g;
-          ++n_q;
-        }
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
         const int krow = (a.pos ? g : 0) * a.cap + t * kTileRows;
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
         tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
         ++issued[stage];
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
-      // drain: every load issued must land before the CTA may exit
-      for (int s = 0; s < kStages; ++s)
+      // every load issued must land before the CTA may exit
+      for (int s = 0; s < C::kStages; ++s)
         if (issued[s] && !tc::mbar_wait(&full[s], (issued[s] - 1) & 1)) failed = true;
-      if (n_q && !tc::mbar_wait(q_full, (n_q - 1) & 1)) failed = true;
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16(128, N);
-      int cur_g = -1, stage = 0, acc = 0, n_q = 0, n_acc[2] = {0, 0};
+      int cur_g = -1, k = -1, stage = 0, acc = 0;
+      int n_acc[C::kAcc];
+#pragma unroll
+      for (int i = 0; i < C::kAcc; ++i) n_acc[i] = 0;
       uint32_t phase = 0;
-      for (int it = i_begin; it < i_end; ++it) {
-        const int g = it / a.tiles_per_group, t = it % a.tiles_per_group;
-        if (t * kTileRows >= group_rows(a, g)) continue;
+      for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
+        const int g = it / a.tiles_per_group;
         if (g != cur_g) {
-          if (cur_g >= 0) tc::mma_commit(q_empty);
-          if (!tc::mbar_wait(q_full, n_q & 1)) { failed = true; break; }
+          ++k;
           cur_g = g;
-          ++n_q;
+          if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
         }
         if (!tc::mbar_wait(&full[stage], phase)) { failed = true; break; }
         if (!tc::mbar_wait(&acc_empty[acc], (n_acc[acc] & 1) ^ 1)) { failed = true; break; }
         tc::fence_after_sync();
         const uint32_t a_base = tc::smem_u32(kbuf + stage * kTileBytes);
-        const uint32_t b_base = tc::smem_u32(qbuf);
+        const uint32_t b_base = tc::smem_u32(qbuf + (k % C::kQSlots) * C::kQBytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = tc::sdesc_kmajor_sw128(a_base + (k >> 2) * (kTileBytes / 2) + (k & 3) * 32);
-          const uint64_t bd = tc::sdesc_kmajor_sw128(b_base + (k >> 2) * (QBYTES / 2) + (k & 3) * 32);
-          tc::mma_bf16(tmem + acc * N, ad, bd, idesc, k > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = tc::sdesc_kmajor_sw128(a_base + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+          const uint64_t bd = tc::sdesc_kmajor_sw128(b_base + (kk >> 2) * (C::kQBytes / 2) + (kk & 3) * 32);
+          tc::mma_bf16(tmem + acc * N, ad, bd, idesc, kk > 0);
         }
         tc::mma_commit(&empty[stage]);
         tc::mma_commit(&acc_full[acc]);
+        if (wk.last_of_group(a, it)) tc::mma_commit(&q_empty[k % C::kQSlots]);
         ++n_acc[acc];
-        acc ^= 1;
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++acc == C::kAcc) acc = 0;
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
-      // make sure every MMA has retired before tensor memory is released
-      if (n_q > 0) {
-        tc::mma_commit(q_empty);
-        if (!tc::mbar_wait(q_empty, (n_q - 1) & 1)) failed = true;
-      }
+      // every MMA retires before tensor memory is released
+      tc::mma_commit(drain);
+      if (!tc::mbar_wait(drain, 0)) failed = true;
     }
-  } else {
-    // epilogue: warp w drains TMEM lanes 32*(w%4) .. +31
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue: warp w drains TMEM lanes 32*(w%4)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    int acc = 0, n_acc[2] = {0, 0};
-    for (int it = i_begin; it < i_end; ++it) {
+    int cur_g = -1, k = -1, acc = 0;
+    int n_acc[C::kAcc];
+#pragma unroll
+    for (int i = 0; i < C::kAcc; ++i) n_acc[i] = 0;
+    int nv[G];
+    for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
       const int g = it / a.tiles_per_group, t = it % a.tiles_per_group;
-      if (t * kTileRows >= group_rows(a, g)) continue;
+      if (g != cur_g) {
+        ++k;
+        cur_g = g;
+        if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
+#pragma unroll
+        for (int qq = 0; qq < G; ++qq) nv[qq] = g * G + qq < a.Q ? idx_nvis(a, g * G + qq) : 0;
+      }
       if (!tc::mbar_wait(&acc_full[acc], n_acc[acc] & 1)) { failed = true; break; }
       tc::fence_after_sync();
       const int j = t * kTileRows + row;
+      const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
 #pragma unroll
       for (int qq = 0; qq < G; ++qq) {
-        const int q = g * G + qq;
         uint32_t v[64];
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * N + qq * 64;
         tc::tmem_ld32(taddr, v);
         tc::tmem_ld32(taddr + 32, v + 32);
         tc::tmem_wait_ld();
-        if (q < a.Q) {
-          const float* w = a.wts + (size_t)q * 64;
-          float s = 0.f;
+        float s = 0.f;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) s = fmaf(__ldg(w + h), fmaxf(__uint_as_float(v[h]), 0.f), s);
-          if (j < idx_nvis(a, q)) a.scores[(size_t)q * a.cap + j] = s;
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 w = w4[qq * 16 + h4];
+          s = fmaf(w.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), s);
+          s = fmaf(w.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s);
+          s = fmaf(w.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s);
+          s = fmaf(w.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s);
         }
+        if (j < nv[qq]) a.scores[(size_t)(g * G + qq) * a.cap + j] = s;
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&acc_empty[acc]);
+      if (wk.last_of_group(a, it)) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&w_empty[k % C::kQSlots]);
+      }
       ++n_acc[acc];
-      acc ^= 1;
+      if (++acc == C::kAcc) acc = 0;
+    }
+  } else {
+    // ------------------------------------------------------------ query blocks (warps 6-7)
+    // Everything the first query block needs (positions, frequencies, head weights and the first batch of query
+    // chunks) is requested for the CTA's first group before the walk that confirms it, so the whole preparation
+    // costs about one memory round trip.  16 chunks of 8 dims per head row; each thread takes 16 (G = 1) or 64
+    // (G = 4) chunks, in batches of 16 whose loads are all issued before any is used.
+    constexpr int kBatch = 16;
+    constexpr int kChunks = G * 64 * 16;
+    const int pt = threadIdx.x - 192;
+    struct Pre {
+      uint4 raw[kBatch];
+      float wv[G];
+      float th_freq;
+      int p;
+    };
+    auto load_first = [&](int g, Pre& pre) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = pt + b * kPrepThreads;
+        const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
+        pre.raw[b] = (e < kChunks && q < a.Q)
+                         ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
+                         : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int e = pt + i * kPrepThreads, q = g * G + e / 64;
+        pre.wv[i] = q < a.Q ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
+      }
+      // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
+      pre.th_freq = __ldg(a.inv_freq + (pt & 31));
+      const int q0 = g * G + pt / 32;
+      pre.p = (pt < G * 32 && q0 < a.Q) ? idx_qpos(a, q0) : 0;
+    };
+    auto rope_store = [&](uint8_t* qb, int e0, uint4 (&raw)[kBatch], int g) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = e0 + b * kPrepThreads;
+        if (e >= kChunks) break;
+        const int qq = e >> 10, h = (e >> 4) & 63, c = e & 15, row = qq * 64 + h;
+        if (c * 8 >= 128 - a.R && g * G + qq < a.Q) {
+          __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw[b]);
+#pragma unroll
+          for (int kq = 0; kq < 4; ++kq) {
+            const int i = qq * 32 + (c * 8 - (128 - a.R)) / 2 + kq;
+            const float2 x = __bfloat1622float2(hv[kq]);
+            hv[kq] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
+          }
+        }
+        *reinterpret_cast<uint4*>(qb + (c >> 3) * (C::kQBytes / 2) + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+            raw[b];
+      }
+    };
+    // the first two groups of the range are requested up front (before the key stream saturates memory and
+    // stretches every round trip)
+    Pre pre_a, pre_b;
+    const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
+    const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
+    if (i_begin < i_end) load_first(g0, pre_a);
+    if (g1 >= 0) load_first(g1, pre_b);
+    int k = -1;
+    for (int it = wk.next(a, i_begin); it < i_end;
+         it = wk.next(a, (it / a.tiles_per_group + 1) * a.tiles_per_group)) {
+      const int g = it / a.tiles_per_group;
+      ++k;
+      const int slot = k % C::kQSlots, use = k / C::kQSlots;
+      if (use > 0) {
+        const bool ok = tc::mbar_wait(&q_empty[slot], (use - 1) & 1) && tc::mbar_wait(&w_empty[slot], (use - 1) & 1);
+        if (tc::named_bar_any(3, kPrepThreads, !ok)) { failed = true; break; }
+      } else {
+        tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
+      }
+      Pre& pre = g == g1 ? pre_b : pre_a;
+      if (g != g0 && g != g1) load_first(g, pre_a);  // a later group: request it now
+      // RoPE table (G x 32 entries) from the preloaded position and frequency
+      for (int e = pt; e < G * 32; e += kPrepThreads) {
+        int p = pre.p;
+        float f = pre.th_freq;
+        if (e != pt) {  // G = 4: the second entry of this thread
+          const int q = g * G + e / 32;
+          p = q < a.Q ? idx_qpos(a, q) : 0;
+          f = __ldg(a.inv_freq + (e & 31));
+        }
+        sincosf(__fmul_rn((float)p, f), &rsin[e], &rcos[e]);
+      }
+      tc::named_bar(3, kPrepThreads);
+      uint8_t* qb = qbuf + slot * C::kQBytes;
+      rope_store(qb, pt, pre.raw, g);
+      for (int e0 = pt + kPrepThreads * kBatch; e0 < kChunks; e0 += kPrepThreads * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + b * kPrepThreads;
+          const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
+          raw[b] = (e < kChunks && q < a.Q)
+                       ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
+                       : make_uint4(0, 0, 0, 0);
+        }
+        rope_store(qb, e0, raw, g);
+      }
+#pragma unroll
+      for (int i = 0; i < G; ++i) wbuf[slot * N + pt + i * kPrepThreads] = pre.wv[i] * a.wscale;
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&q_full[slot]);
     }
   }
   if (failed) atomicOr(a.err, tc::kErrTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 2 * N);
-}
-
-// qr[q][h][:] = RoPE(iq[q][h][:], p_q) (bf16), wts[q][h] = iw[q][h] * scale.
-// Block (q, head group of 8): one 16-byte chunk of 8 dims per thread.
-__global__ void __launch_bounds__(128) k_tc_index_prep(const __nv_bfloat16* __restrict__ iq,
-                                                       const __nv_bfloat16* __restrict__ iw,
-                                                       const int32_t* __restrict__ pos, int pos0, int R,
-                                                       const float* __restrict__ inv_freq, float wscale,
-                                                       __nv_bfloat16* __restrict__ qr, float* __restrict__ wts) {
-  pdl_trigger();
-  pdl_wait();
-  constexpr int Hi = 64, Di = 128;
-  __shared__ float rc[64], rs[64];
-  const int q = blockIdx.x, h0 = blockIdx.y * 8;
-  const int p = pos ? pos[q] : pos0 + q;
-  if (threadIdx.x < R / 2) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
-  __syncthreads();
-  const int h = h0 + (threadIdx.x >> 4), c = threadIdx.x & 15;  // 16 chunks of 8 dims per head row
-  const size_t off = ((size_t)q * Hi + h) * Di + c * 8;
-  uint4 raw = __ldg(reinterpret_cast<const uint4*>(iq + off));
-  if (c * 8 >= Di - R) {
-    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = (c * 8 - (Di - R)) / 2 + k;
-      const float2 x = __bfloat1622float2(hv[k]);
-      hv[k] = __floats2bfloat162_rn(fmaf(x.x, rc[i], -x.y * rs[i]), fmaf(x.x, rs[i], x.y * rc[i]));
-    }
-  }
-  *reinterpret_cast<uint4*>(qr + off) = raw;
-  if (threadIdx.x < 8) wts[(size_t)q * Hi + h0 + threadIdx.x] = __bfloat162float(iw[(size_t)q * Hi + h0 + threadIdx.x]) * wscale;
+  if (warp == 1) tc::tmem_dealloc(tmem, C::kAcc * N);
 }
 
 int g_num_sms = 0;
@@ -252,37 +393,35 @@ size_t tc_index_ws(const Dims& L, int Q) {
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s) {
+  (void)ws;
   if (!g_num_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  Carver c(ws);
-  __nv_bfloat16* qr = c.take<__nv_bfloat16>((size_t)Q * 64 * 128);
-  float* wts = c.take<float>((size_t)Q * 64);
-  const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
-  CSA_LAUNCH(k_tc_index_prep, dim3(dim3(Q, 8)), dim3(128), 0, s, static_cast<const __nv_bfloat16*>(iq),
-                                              static_cast<const __nv_bfloat16*>(iw), pos, pos0, L.R, inv_freq,
-                                              wscale, qr, wts);
   const int G = pos ? 1 : 4;
-  CUtensorMap tk, tq;
+  CUtensorMap tk;
   if (!make_tmap_2d_bf16(&tk, ikeys, (uint64_t)Bk * cap, 128, 256, kTileRows)) return cudaErrorInvalidValue;
-  if (!make_tmap_2d_bf16(&tq, qr, (uint64_t)Q * 64, 128, 256, 64 * G)) return cudaErrorInvalidValue;
   IdxArgs a{};
+  a.iq = static_cast<const __nv_bfloat16*>(iq);
+  a.iw = static_cast<const __nv_bfloat16*>(iw);
+  a.inv_freq = inv_freq;
+  a.wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
+  a.R = L.R;
   a.n_rows = n_rows; a.pos = pos; a.pos0 = pos0; a.ratio = L.ratio; a.topk = L.topk; a.cap = cap; a.Q = Q;
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
   a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
-  a.wts = wts; a.scores = scores; a.err = err;
+  a.scores = scores; a.err = err;
   const int grid = min(g_num_sms, a.n_items);
-  const size_t smem = 1024 + (size_t)64 * G * 128 * 2 + (size_t)kStages * kTileBytes + 256;
   if (G == 1) {
-    cudaFuncSetAttribute(k_tc_index_scores<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    CSA_LAUNCH(k_tc_index_scores<1>, dim3(grid), dim3(kThreads), smem, s, tk, tq, a);
+    constexpr int smem = IdxCfg<1>::kSmem;
+    cudaFuncSetAttribute(k_tc_index_scores<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<1>, dim3(grid), dim3(kThreads), smem, s, tk, a);
   } else {
-    cudaFuncSetAttribute(k_tc_index_scores<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    CSA_LAUNCH(k_tc_index_scores<4>, dim3(grid), dim3(kThreads), smem, s, tk, tq, a);
+    constexpr int smem = IdxCfg<4>::kSmem;
+    cudaFuncSetAttribute(k_tc_index_scores<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<4>, dim3(grid), dim3(kThreads), smem, s, tk, a);
   }
-  
   return cudaGetLastError();
 }
 
