@@ -165,12 +165,13 @@ def _max_over_ranks(dist, value: float, device) -> float:
 class DecodeWorkload:
     """Config 3 state, weights and per-step inputs resident on one GPU."""
 
-    def __init__(self, cfg, cap: int, n_inputs: int, device):
+    def __init__(self, cfg, cap: int, n_inputs: int, device, serial_indexer: bool = False):
         import torch
 
         import csa_synth
         import deepseek_v4_compressed_csa_gb300 as csa
         self.cfg, self.cap, self.dev = cfg, cap, device
+        self.serial_indexer = serial_indexer
         self.L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
                            Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
         d = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
@@ -195,14 +196,16 @@ class DecodeWorkload:
         self.ws_c = u8(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, cap))
         self.ws_c2 = u8(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, cap))  # the concurrent second call
         self.side = torch.cuda.Stream(device)
+        self.side2 = torch.cuda.Stream(device)
+        self.pool_ready = torch.cuda.Event()
         self.ws_i = u8(csa.workspace_size(self.L, csa.OP_INDEX_TOPK, B, 1, cap))
         self.ws_a = u8(csa.workspace_size(self.L, csa.OP_ATTEND_DECODE, B, 1, cap))
         self.csa = csa
 
     def front(self, inp):
-        """Phase 1: the index pool's compress call and the indexer on the main stream, and concurrently,
-        on a second stream, the attention pool's compress call (only the attention phase needs its row).
-        Each concurrent call has its own workspace."""
+        """Phase 1: the two compress calls on two side streams, and on the main stream the indexer in its
+        overlapped form: its scan of the rows complete before the token runs while the index pool's compress
+        call runs, and its selection waits for that call's event.  Each concurrent call has its own workspace."""
         import torch
         csa = self.csa
         main = torch.cuda.current_stream()
@@ -210,11 +213,20 @@ class DecodeWorkload:
         with torch.cuda.stream(self.side):
             csa.compress_append(self.L, self.ca, inp["x"], self.pos, self.front_a, self.pool, self.n_a, self.invf,
                                 ws=self.ws_c2, err=self.err)
-        if self.cfg.has_indexer:
+        if self.cfg.has_indexer and self.serial_indexer:
             csa.compress_append(self.L, self.ci, inp["x"], self.pos, self.front_i, self.ikeys, self.n_i, self.invf,
                                 ws=self.ws_c, err=self.err)
             csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
                            self.n_sel, ws=self.ws_i, err=self.err)
+        elif self.cfg.has_indexer:
+            self.side2.wait_stream(main)
+            with torch.cuda.stream(self.side2):
+                csa.compress_append(self.L, self.ci, inp["x"], self.pos, self.front_i, self.ikeys, self.n_i,
+                                    self.invf, ws=self.ws_c, err=self.err)
+                self.pool_ready.record(self.side2)
+            csa.index_topk_overlapped(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf,
+                                      self.sel, self.n_sel, pool_ready=self.pool_ready, ws=self.ws_i, err=self.err)
+            main.wait_stream(self.side2)
         main.wait_stream(self.side)
 
     def attend(self, inp):
@@ -228,9 +240,9 @@ class DecodeWorkload:
         self.front(inp)
         self.attend(inp)
 
-    def capture(self):
-        """One CUDA graph per phase (compress + indexer, attention) and per input set; the bench records
-        events between the phase graphs."""
+    def capture(self, per_phase: bool = False):
+        """Per input set, one CUDA graph holding the whole step (both phases), or with per_phase one graph per
+        phase (compress + indexer | attention) so that events can separate them."""
         import torch
         self.graphs = []
         s = torch.cuda.Stream()
@@ -238,28 +250,30 @@ class DecodeWorkload:
         with torch.cuda.stream(s):
             for inp in self.inputs:
                 gs = []
-                for phase in (self.front, self.attend):
+                parts = ((self.front, self.attend),) if not per_phase else ((self.front,), (self.attend,))
+                for part in parts:
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
-                        phase(inp)
+                        for fn in part:
+                            fn(inp)
                     gs.append(g)
                 self.graphs.append(gs)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
 
     def replay(self, i, ev=None):
-        """Step i: the two phase graphs (or, eagerly, the same calls); events before each phase and after."""
+        """Step i: its graph(s) (or, eagerly, the same calls); an event before each graph and one after."""
         if self.graphs is None:
             inp = self.inputs[i % len(self.inputs)]
-            phases = [lambda: self.front(inp), lambda: self.attend(inp)]
+            parts = [lambda: self.step(inp)]
         else:
-            phases = [g.replay for g in self.graphs[i % len(self.graphs)]]
-        for k, run in enumerate(phases):
+            parts = [g.replay for g in self.graphs[i % len(self.graphs)]]
+        for k, run in enumerate(parts):
             if ev is not None:
                 ev[k].record()
             run()
         if ev is not None:
-            ev[2].record()
+            ev[len(parts)].record()
 
 
 def step_bytes(cfg, n_rows_mean: float) -> dict:
@@ -287,7 +301,7 @@ def run_ours(args):
     cfg = csa_synth.CONFIGS[3]
     total_steps = args.warmup + args.steps + args.e2e_steps + 4
     cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
-    wl = DecodeWorkload(cfg, cap, n_inputs=8, device=dev)
+    wl = DecodeWorkload(cfg, cap, n_inputs=8, device=dev, serial_indexer=not args.overlapped_indexer)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -304,7 +318,7 @@ def run_ours(args):
         dist.barrier()
     n_start = wl.n_a.float().mean().item()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    ev = [(mk(), mk(), mk()) for _ in range(args.steps)]
+    ev = [(mk(), mk()) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     launches0 = csa.kernel_launches()
@@ -318,10 +332,7 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    front_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    phase_us = {name: round(1e3 * statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev), 2)
-                for k, name in enumerate(("compress_x2_and_index", "attend"))}
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     total_ms = _max_over_ranks(dist, sum(step_ms), dev)
     assert wl.err.item() == 0, f"device error word {wl.err.item()}"
     n_end = wl.n_a.float().mean().item()
@@ -331,6 +342,23 @@ def run_ours(args):
     torch.cuda.synchronize()
     launches = (csa.kernel_launches() - k0) * args.steps
     del launches0
+
+    # ---- diagnostic (not the headline): the same steps as two graphs, events between the phases
+    phase_us = None
+    if not args.eager:
+        wl.capture(per_phase=True)
+        n_diag = min(args.steps, 16)
+        evd = [(mk(), mk(), mk()) for _ in range(n_diag)]
+        for i in range(3):
+            wl.replay(i)
+        torch.cuda.synchronize()
+        for i in range(n_diag):
+            flush.zero_()
+            wl.replay(i, ev=evd[i])
+        torch.cuda.synchronize()
+        phase_us = {name: round(1e3 * statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evd), 2)
+                    for k, name in enumerate(("compress_x2_and_index", "attend"))}
+        wl.capture()
 
     # ---- end to end: pinned host inputs -> the graphs' input buffers, step, output -> pinned host
     pinned = [{k: getattr(si, k).pin_memory() for k in ("x", "q", "kv", "iq", "iw")} for si in wl.host_inputs]
@@ -360,10 +388,7 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = world * args.steps / (total_ms / 1e3)
     nb = step_bytes(cfg, 0.5 * (n_start + n_end))
-    # phase 1 moves the compressor weights of both pools, every visible index key, and the small per-token terms
-    front_bytes = (nb["weights"] + nb["index_keys"] +
-                   cfg.B * (cfg.X * 2 + cfg.Hi * cfg.Di * 2 + cfg.Hi * 2 + cfg.topk * 4))
-    front_avg_s = statistics.mean(front_ms) / 1e3
+    step_avg_s = ms_per_step / 1e3
     result = None
     if rank == 0:
         cpu = run_oracle_subprocess(3, args.cpu_budget, 400)
@@ -381,18 +406,22 @@ def run_ours(args):
                 "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
                 "l2": "flushed (512 MB write) before every timed step, outside the events",
                 "phase_us": phase_us,
+                "phase_us_note": ("diagnostic run of the same steps as two graphs (compress x2 + indexer | "
+                                  "attention), events between them; each includes its graph's launch latency"),
                 "launch": ("kernels launched one by one" if args.eager else
-                           "each step = 2 CUDA graph replays (compress x2 + indexer, two streams | attention)"),
+                           "each step = 1 CUDA graph replay (three streams in phase 1: both compress calls on "
+                           "side streams, the overlapped indexer on the main stream)"),
                 "prefill": prefill,
             },
             "roofline": {
-                "kernel": ("phase 1 graph: csa_compress_append x2 (attention pool on a second stream) + "
-                           "csa_index_topk (projection weights + index-key scan + top-k)"), "bound": "hbm",
-                "achieved": round(front_bytes / front_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(front_bytes / front_avg_s / 1e9 / hbm, 4), "traffic": None,
+                "kernel": ("decode step graph: every kernel of one step (compress x2, index scan + top-k, "
+                           "attention + merge); algorithmic bytes = weights + index keys + attended rows + "
+                           "q/out + small terms"), "bound": "hbm",
+                "achieved": round(nb["total"] / step_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(nb["total"] / step_avg_s / 1e9 / hbm, 4), "traffic": None,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                else "fallback 6800 GB/s", "avg_launch_ms": round(front_avg_s * 1e3, 5),
-                "algorithmic_bytes_per_launch": int(front_bytes),
+                else "fallback 6800 GB/s", "avg_launch_ms": round(ms_per_step, 5),
+                "algorithmic_bytes_per_launch": int(nb["total"]),
             },
             "cpu_baseline": {"value": round(cpu["layer_steps_per_s"], 5), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"1 of {cfg.B} sequences x {cpu['steps']} decode steps of the same workload, "
@@ -492,6 +521,9 @@ def main():
     ap.add_argument("--prefill-repeats", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
+    ap.add_argument("--overlapped-indexer", action="store_true",
+                    help="run csa_index_topk_overlapped beside the index pool's compress call instead of "
+                         "csa_index_topk after it on one stream")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--oracle-sample", nargs=3, default=None)
     args = ap.parse_args()

@@ -23,7 +23,7 @@ CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
-           "csa_index_topk_static")
+           "csa_index_topk_static", "csa_index_topk_overlapped")
 
 
 class CSAError(RuntimeError):
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_compress_append.restype = i32
     lib.csa_index_topk.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.csa_index_topk.restype = i32
+    lib.csa_index_topk_overlapped.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.csa_index_topk_overlapped.restype = i32
     lib.csa_static_scratch_bytes.argtypes = []
     lib.csa_static_scratch_bytes.restype = sz
     lib.csa_index_topk_static.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
@@ -196,6 +198,21 @@ def index_topk(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, w
     _check("csa_index_topk", load_library().csa_index_topk(
         ctypes.byref(L), _ptr(iq), _ptr(iw), B, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
         _ptr(sel), _ptr(n_sel), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def index_topk_overlapped(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, pool_ready=None, ws=None,
+                          err=None, stream=None):
+    """csa_index_topk_overlapped: the scan of the rows complete before the token is enqueued at once; the
+    rest waits for `pool_ready` (a torch.cuda.Event recorded after the index pool's compress call)."""
+    B, cap = iq.shape[0], ikeys.shape[1]
+    ws, nb = _ws(layer, OP_INDEX_TOPK, B, 1, cap, ws, iq.device)
+    err = _err(err, iq.device)
+    L = layer._c()
+    ev = pool_ready.cuda_event if pool_ready is not None else None
+    _check("csa_index_topk_overlapped", load_library().csa_index_topk_overlapped(
+        ctypes.byref(L), _ptr(iq), _ptr(iw), B, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
+        _ptr(sel), _ptr(n_sel), _ptr(ws), nb, _ptr(err), _stream(stream), ev))
     return err
 
 

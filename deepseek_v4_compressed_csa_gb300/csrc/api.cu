@@ -159,6 +159,26 @@ csa_status csa_index_topk(const csa_layer* layer, const void* iq, const void* iw
                                        static_cast<cudaStream_t>(stream)));
 }
 
+csa_status csa_index_topk_overlapped(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys,
+                                     int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
+                                     int32_t* sel, int32_t* n_sel, void* ws, size_t ws_bytes, int32_t* err,
+                                     void* stream, void* pool_ready) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
+  if (B < 1 || cap < 1) return CSA_ERR_ARG;
+  if (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
+  if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(sel) || !dev_i32(n_sel) || !dev_i32(err)) return CSA_ERR_ARG;
+  const size_t need = ws_index(L, B, cap);
+  if (ws_bytes < need || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  IndexWs w = carve_index(c, L, B, cap);
+  return cuda_status(launch_index_topk_overlapped(L, iq, iw, B, ikeys, cap, n_rows, pos, inv_freq, sel, n_sel, w,
+                                                  err, static_cast<cudaStream_t>(stream),
+                                                  static_cast<cudaEvent_t>(pool_ready)));
+}
+
 csa_status csa_attend_decode(const csa_layer* layer, const void* q, const void* kv_new, const float* sink, int B,
                              void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
                              const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out, void* ws,

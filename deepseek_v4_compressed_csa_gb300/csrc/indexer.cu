@@ -371,16 +371,52 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
 // (2048-bin shared histograms, double-buffered so the next pass's bins are cleared during the current one).
 constexpr int kTopkRegKeys = 16;
 
+// Scores of rows jr[0], jr[1] (-1: none) of query q from the roped queries qr [Q,64,128] (bf16) and the scaled
+// head weights w [Q,64]: thread t takes head t/16, dims 8 (t%16) .. +7; heads are summed in order by one thread.
+// Every thread of the block calls it (two block barriers).
+__device__ __forceinline__ void score_rows(const __nv_bfloat16* __restrict__ qr, const float* __restrict__ w,
+                                           const __nv_bfloat16* __restrict__ keys, int q, const int (&jr)[2],
+                                           float (&part)[2][64], float* out) {
+  const int h = threadIdx.x >> 4, sub = threadIdx.x & 15;
+  float qv[8];
+  load8(qr + ((size_t)q * 64 + h) * 128 + sub * 8, qv);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (jr[r] < 0) continue;
+    float kv[8];
+    load8(keys + (size_t)jr[r] * 128 + sub * 8, kv);
+    float d = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d = fmaf(qv[i], kv[i], d);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (sub == 0) part[r][h] = d;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 && jr[threadIdx.x] >= 0) {
+    float sc = 0.f;
+    for (int hh = 0; hh < 64; ++hh) sc = fmaf(w[(size_t)q * 64 + hh], fmaxf(part[threadIdx.x][hh], 0.f), sc);
+    out[threadIdx.x] = sc;
+  }
+  __syncthreads();
+}
+
+// qr / w / keys non-null: the scan before this kernel covered rows < floor(p/ratio) only (it ran while the index
+// pool's compress call for this token could still write); the rows that call may have written (row
+// floor(p/ratio) and row n_rows-1) are scored here and replace what the score buffer holds for them.
 __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ scores, int cap,
                                                    const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
                                                    int pos0, int ratio, int topk, int32_t* __restrict__ sel,
-                                                   int32_t* __restrict__ n_sel) {
+                                                   int32_t* __restrict__ n_sel, const __nv_bfloat16* __restrict__ qr,
+                                                   const float* __restrict__ w, const __nv_bfloat16* __restrict__ keys) {
   pdl_trigger();
   pdl_wait();
   __shared__ int hist[2][2048];
   __shared__ int warp_tot[32];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
+  __shared__ float part[2][64];
+  __shared__ float new_score[2];
   const int q = blockIdx.x, bseq = query_seq(pos, q);
   const int p = query_pos(pos, pos0, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
@@ -396,6 +432,18 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
   uint32_t uk[kTopkRegKeys];
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) uk[i] = (i < K && r0 + i < nvis) ? ord_key(__ldg(sc + i)) : 0u;
+  if (qr) {
+    const int j0 = min(cap, p / ratio), jl = min(n_rows[bseq], cap) - 1;
+    const int jr[2] = {j0 < nvis ? j0 : -1, (jl >= 0 && jl < nvis && jl != j0) ? jl : -1};
+    score_rows(qr, w, keys + (size_t)bseq * cap * 128, q, jr, part, new_score);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (jr[r] < 0) continue;
+#pragma unroll
+      for (int i = 0; i < kTopkRegKeys; ++i)
+        if (i < K && r0 + i == jr[r]) uk[i] = ord_key(new_score[r]);
+    }
+  }
   hist[0][2 * threadIdx.x] = 0;
   hist[0][2 * threadIdx.x + 1] = 0;
   __syncthreads();
@@ -466,7 +514,9 @@ constexpr int kTopkSmemMaxCap = 52 * 1024;
 static cudaError_t launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
                         int pos0, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
   if (cap <= kTopkRegKeys * 1024) {
-    CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+    CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel,
+               static_cast<const __nv_bfloat16*>(nullptr), static_cast<const float*>(nullptr),
+               static_cast<const __nv_bfloat16*>(nullptr));
   } else if (cap <= kTopkSmemMaxCap) {
     const size_t smem = (size_t)cap * 4 + 2048 * 4;
     cudaFuncSetAttribute(k_topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -494,6 +544,31 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
   CSA_LAUNCH(k_index_scores<T>, dim3(g), dim3(256), smem, s, ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
                                          cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores);
   return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
+}
+
+cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys,
+                                         int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
+                                         int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err,
+                                         cudaStream_t s, cudaEvent_t ready) {
+  if (!tc_index_supported(L) || cap > kTopkRegKeys * 1024) {
+    if (ready) {
+      const cudaError_t e = cudaStreamWaitEvent(s, ready, 0);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_index_topk(L, iq, iw, Q, ikeys, cap, n_rows, pos, 0, inv_freq, sel, n_sel, ws, err, s);
+  }
+  cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, Q, cap, n_rows, pos, 0, inv_freq, ws.qr, ws.scores,
+                                         err, s, true);
+  if (e != cudaSuccess) return e;
+  if (ready) {
+    e = cudaStreamWaitEvent(s, ready, 0);
+    if (e != cudaSuccess) return e;
+  }
+  const auto* qr = reinterpret_cast<const __nv_bfloat16*>(ws.qr);
+  const auto* w = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws.qr) + (size_t)Q * 64 * 128 * 2);
+  CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, ws.scores, cap, n_rows, pos, 0, L.ratio, L.topk, sel, n_sel, qr,
+             w, static_cast<const __nv_bfloat16*>(ikeys));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,

@@ -78,6 +78,14 @@ struct IndexWs {
   float* scores;  // [Q, cap]
 };
 IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap);
+// The indexer in two stages around `ready` (an event recorded after the index pool's compress call for the same
+// token, possibly on another stream; null: no wait): the scan of the rows complete before the token, then,
+// after the event, the rows that call may have written and the selection.  Decode, tensor-core shapes only;
+// otherwise the whole call waits for the event and runs as launch_index_topk.
+cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys,
+                                         int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
+                                         int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err,
+                                         cudaStream_t s, cudaEvent_t ready);
 // Scores and top-k for Q queries.  Query q belongs to sequence bseq(q) = (pos != null ? q : 0)
 // at position (pos != null ? pos[q] : pos0 + q); its visible rows are
 // min(n_rows[bseq], (p+1)/ratio).  sel [Q, topk], n_sel [Q].
@@ -101,9 +109,12 @@ bool tc_index_supported(const Dims& L);
 size_t tc_index_ws(const Dims& L, int Q);
 // scores[q][j] for every q whose visible rows exceed topk; keys of query q are
 // ikeys[pos ? q : 0]; ws needs tc_index_ws() bytes.
+// overlap (decode only): score only rows < floor(pos/ratio) without reading n_rows, and leave the roped
+// queries (bf16 [Q,64,128]) and scaled head weights (fp32 [Q,64]) at the start of ws for the selection stage.
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
-                                   const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s);
+                                   const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s,
+                                   bool overlap = false);
 
 // ---- tc_attend.cu (tensor-core attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_supported(const Dims& L);

@@ -165,6 +165,29 @@ csa_status csa_index_topk(const csa_layer* layer, const void* iq, const void* iw
                           const int32_t* n_rows, const int32_t* pos, const float* inv_freq, int32_t* sel,
                           int32_t* n_sel, void* ws, size_t ws_bytes, int32_t* err, void* stream);
 
+/* csa_index_topk_overlapped — csa_index_topk split around the index pool's
+ * compress call for the same token, so that the scan of the cached index keys
+ * (the bulk of the call) runs while that compress call runs on another stream.
+ * The pages define the same selection as csa_index_topk and have no such split:
+ * it is a scheduling form of that call, with identical outputs up to the
+ * floating-point order of the two rows scored in its second stage.
+ *   stage 1 (enqueued on `stream` at once): s_j for rows j < floor(pos[b]/ratio),
+ *     the rows complete before the token; reads neither n_rows nor any index-key
+ *     row the concurrent compress call may write;
+ *   then `stream` waits for `pool_ready` (a cudaEvent_t recorded after
+ *     csa_compress_append for the index pool and this token; NULL: no wait);
+ *   stage 2: s_j for row floor(pos[b]/ratio) and row n_rows[b]-1 (the rows that
+ *     call may have written), then the selection exactly as csa_index_topk.
+ * Arguments, workspace (CSA_OP_INDEX_TOPK) and errors as csa_index_topk; the
+ * caller orders the compress call after any earlier use of the index pool, and
+ * must not start another call that writes ikeys or n_rows for these sequences
+ * before this one completes.  Shapes the tensor-core scan does not cover, or
+ * cap > 16384, run the whole call after the event. */
+csa_status csa_index_topk_overlapped(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys,
+                                     int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
+                                     int32_t* sel, int32_t* n_sel, void* ws, size_t ws_bytes, int32_t* err,
+                                     void* stream, void* pool_ready);
+
 /* csa_attend_decode — one decode query per sequence.
  *
  * Definition ([MTPLX#216] "What V4 adds": 64 query heads over one 512-dim

@@ -210,16 +210,47 @@ class Runner:
                 projs[name] = raw.view(self.cfg.storage).view(B, T, width).clone()
         return projs
 
-    def decode_step(self, st: DevCache, si: csa_synth.StepInputs):
+    def compress_and_index_overlapped(self, st: DevCache, si: csa_synth.StepInputs, sel, n_sel):
+        """The index pool's compress call on a second stream while csa_index_topk_overlapped scans on the main
+        stream (after the attention pool's compress call), joined by an event; sets self.projs."""
+        x = dev(si.x)
+        B = x.shape[0]
+        n_idx = st.n_rows.clone()
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(main)
+        ready = torch.cuda.Event()
+        mk = lambda pool: torch.zeros(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, pool.shape[1]),  # noqa: E731
+                                      dtype=torch.uint8, device="cuda")
+        ws_i, ws_a = mk(st.ikeys), mk(st.pool)
+        with torch.cuda.stream(side):
+            csa.compress_append(self.L, self.ci, x, st.pos, st.front_index, st.ikeys, n_idx, self.inv_freq, ws=ws_i,
+                                err=self.err)
+            ready.record(side)
+        csa.compress_append(self.L, self.ca, x, st.pos, st.front_attn, st.pool, st.n_rows, self.inv_freq, ws=ws_a,
+                            err=self.err)
+        csa.index_topk_overlapped(self.L, dev(si.iq), dev(si.iw), st.ikeys, n_idx, st.pos, self.inv_freq, sel, n_sel,
+                                  pool_ready=ready, err=self.err)
+        main.wait_stream(side)
+        slots = st.pos.long() % st.front_attn.shape[1]
+        rows = torch.arange(B, device="cuda")
+        self.projs = {"attn": st.front_attn[rows, slots].view(B, 1, -1).clone(),
+                      "index": st.front_index[rows, slots].view(B, 1, -1).clone()}
+
+    def decode_step(self, st: DevCache, si: csa_synth.StepInputs, overlap: bool = False):
         cfg = self.cfg
         B = si.q.shape[0]
-        self.projs = self.compress(st, si.x)
         sel = n_sel = None
         if cfg.has_indexer:
             sel = torch.empty(B, cfg.topk, dtype=torch.int32, device="cuda")
             n_sel = torch.empty(B, dtype=torch.int32, device="cuda")
-            csa.index_topk(self.L, dev(si.iq), dev(si.iw), st.ikeys, st.n_rows, st.pos, self.inv_freq, sel, n_sel,
-                           err=self.err)
+        if overlap and cfg.has_indexer:
+            self.compress_and_index_overlapped(st, si, sel, n_sel)
+        else:
+            self.projs = self.compress(st, si.x)
+            if cfg.has_indexer:
+                csa.index_topk(self.L, dev(si.iq), dev(si.iw), st.ikeys, st.n_rows, st.pos, self.inv_freq, sel,
+                               n_sel, err=self.err)
         out = torch.empty(B, cfg.H, cfg.D, dtype=cfg.storage, device="cuda")
         csa.attend_decode(self.L, dev(si.q), dev(si.kv), self.sink, st.window, st.pool, st.n_rows, sel, n_sel,
                           st.pos, self.inv_freq, out, err=self.err)

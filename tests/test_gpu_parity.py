@@ -125,10 +125,13 @@ def test_config2_flash_build_8k_then_decode():
     assert run.err.item() == 0
 
 
-@pytest.mark.parametrize("cid,ctx,steps,seqs", [(3, 32768, 10, (0, 13, 31)), (4, 262144 - 3, 6, (0, 15))])
-def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs):
+@pytest.mark.parametrize("cid,ctx,steps,seqs,overlap", [(3, 32768, 10, (0, 13, 31), False),
+                                                         (3, 32768 + 1, 6, (5, 30), True),
+                                                         (4, 262144 - 3, 6, (0, 15), False)])
+def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs, overlap):
     """Configs 3 and 4 at full batch and context: every sequence runs on the GPU; the oracle follows
-    a few of them step by step (window-boundary crossings included)."""
+    a few of them step by step (window-boundary crossings included).  The second case drives the indexer
+    through csa_index_topk_overlapped, the form the bench times."""
     cfg = csa_synth.CONFIGS[cid]
     cap = ctx // cfg.ratio + steps // cfg.ratio + 4
     run = G.Runner(cfg)
@@ -141,7 +144,7 @@ def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs):
     st_o = {b: _oracle_seq_state(host, b) for b in seqs}
     for step in range(steps):
         si = csa_synth.step_inputs(cfg, step)
-        out, sel, n_sel = run.decode_step(st_g, si)
+        out, sel, n_sel = run.decode_step(st_g, si, overlap=overlap)
         torch.cuda.synchronize()
         for b in seqs:
             _oracle_decode_check(layer, ca, ci, st_o[b], _step_rows(si, b), sink, invf, out[b].cpu(),
@@ -251,9 +254,11 @@ def _ragged_cache(cfg, cap, ctxs):
     return host
 
 
-def test_ragged_batch_edges():
+@pytest.mark.parametrize("overlap", [False, True], ids=["one_stream", "overlapped_indexer"])
+def test_ragged_batch_edges(overlap):
     """One batch mixing an empty cache, a cache shorter than the window, the dense/sparse threshold
-    (n_vis == topk and topk + 1) and a long cache."""
+    (n_vis == topk and topk + 1) and a long cache; with csa_index_topk, and with csa_index_topk_overlapped
+    scanning while the index pool's compress call runs on another stream (some steps emit a row)."""
     cfg = csa_synth.CONFIGS[3].replace(B=6)
     ctxs = [0, 3, 100, 2047, 2051, 9000]
     cap = max(ctxs) // 4 + 8
@@ -266,7 +271,7 @@ def test_ragged_batch_edges():
     st_o = {b: _oracle_seq_state(host, b) for b in range(len(ctxs))}
     for step in range(5):
         si = csa_synth.step_inputs(cfg, step, B=len(ctxs))
-        out, sel, n_sel = run.decode_step(st_g, si)
+        out, sel, n_sel = run.decode_step(st_g, si, overlap=overlap)
         torch.cuda.synchronize()
         for b in range(len(ctxs)):
             _oracle_decode_check(layer, ca, ci, st_o[b], _step_rows(si, b), sink, invf, out[b].cpu(),
