@@ -59,10 +59,8 @@ struct IdxArgs {
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
   float* scores;     // [Q, cap]
   int32_t* err;
-  // decode scan that overlaps the index pool's compress call for the same token: only rows complete before
-  // the query's position are scored (n_rows is not read), and the roped queries and scaled head weights are
-  // left in qr_out / w_out for the selection stage, which scores the rows that call may write
-  int overlap;
+  // overlapped decode scan (kernel instance kOverlap): the roped queries and scaled head weights, left for the
+  // selection stage
   __nv_bfloat16* qr_out;  // [Q, 64, 128]
   float* w_out;           // [Q, 64]
 };
@@ -72,17 +70,21 @@ __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
   const int b = a.pos ? q : 0;
   return min(min(a.n_rows[b], a.cap), (idx_qpos(a, q) + 1) / a.ratio);
 }
-// rows this scan scores for query q (overlapped decode scan: the rows complete before the query's token)
+// Rows this scan scores for query q.  The overlapped decode scan, which runs while the index pool's compress
+// call for the same token may still write, takes the rows complete before the query's token and does not read
+// n_rows; the selection stage scores the rows that call may write.
+template <bool kOverlap>
 __device__ __forceinline__ int scan_rows(const IdxArgs& a, int q) {
-  return a.overlap ? min(a.cap, idx_qpos(a, q) / a.ratio) : idx_nvis(a, q);
+  return kOverlap ? min(a.cap, idx_qpos(a, q) / a.ratio) : idx_nvis(a, q);
 }
 // tiles that group g must score (its last query sees the most rows); 0 if the group's queries keep every
 // visible row anyway
+template <bool kOverlap>
 __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
   const int qlast = min(a.Q - 1, g * a.G + a.G - 1);
-  if (a.overlap) {  // bound on the visible rows once the concurrent compress call has run
+  if (kOverlap) {  // bound on the visible rows once the concurrent compress call has run
     if (min(a.cap, (idx_qpos(a, qlast) + 1) / a.ratio) <= a.topk) return 0;
-    return (scan_rows(a, qlast) + kTileRows - 1) / kTileRows;
+    return (scan_rows<kOverlap>(a, qlast) + kTileRows - 1) / kTileRows;
   }
   const int nv = idx_nvis(a, qlast);
   return nv > a.topk ? (nv + kTileRows - 1) / kTileRows : 0;
@@ -92,6 +94,7 @@ __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
 // Every role walks the same sequence: first unskipped item at or after `it`, or i_end.  The walker keeps
 // plain copies of the two fields it needs (a reference to the kernel's parameters would move them to local
 // memory) and the tile count of the last group it looked at.
+template <bool kOverlap>
 struct Walker {
   int tpg, i_end, g_cached, nt_cached;
   __device__ Walker(int tiles_per_group, int e) : tpg(tiles_per_group), i_end(e), g_cached(-1), nt_cached(0) {}
@@ -100,7 +103,7 @@ struct Walker {
       const int g = it / tpg, t = it - g * tpg;
       if (g != g_cached) {
         g_cached = g;
-        nt_cached = group_tiles(a, g);
+        nt_cached = group_tiles<kOverlap>(a, g);
       }
       if (t < nt_cached) return it;
       it = (g + 1) * tpg;
@@ -114,10 +117,8 @@ struct Walker {
   }
 };
 
-// Decode (G = 1) keeps to 128 registers a thread, so that the compress kernels running concurrently on other
-// streams (a projection CTA, a pooling CTA) still find registers on the SMs this persistent scan holds.
-template <int G>
-__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
+template <int G, bool kOverlap>
+__global__ void __launch_bounds__(kThreads, 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, IdxArgs a) {
   using C = IdxCfg<G>;
   constexpr int N = C::N;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
 
   const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
   const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
-  Walker wk(a.tiles_per_group, i_end);
+  Walker<kOverlap> wk(a.tiles_per_group, i_end);
   bool failed = false;
 
   if (warp == 0) {
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
         cur_g = g;
         if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
 #pragma unroll
-        for (int qq = 0; qq < G; ++qq) nv[qq] = g * G + qq < a.Q ? scan_rows(a, g * G + qq) : 0;
+        for (int qq = 0; qq < G; ++qq) nv[qq] = g * G + qq < a.Q ? scan_rows<kOverlap>(a, g * G + qq) : 0;
       }
       if (!tc::mbar_wait(&acc_full[acc], n_acc[acc] & 1)) { failed = true; break; }
       tc::fence_after_sync();
@@ -334,18 +335,17 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
         }
         *reinterpret_cast<uint4*>(qb + (c >> 3) * (C::kQBytes / 2) + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
             raw[b];
-        if (a.overlap && g * G + qq < a.Q)  // every CTA preparing this query writes the same bytes
+        if (kOverlap && g * G + qq < a.Q)  // every CTA preparing this query writes the same bytes
           *reinterpret_cast<uint4*>(a.qr_out + ((size_t)(g * G + qq) * 64 + h) * 128 + c * 8) = raw[b];
       }
     };
-    // the first group of the range is requested up front and the second is prefetched into L2 (before the key
-    // stream saturates memory and stretches every round trip)
-    Pre pre_a;
+    // the first two groups of the range are requested up front (before the key stream saturates memory and
+    // stretches every round trip)
+    Pre pre_a, pre_b;
     const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
     const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
     if (i_begin < i_end) load_first(g0, pre_a);
-    if (g1 >= 0 && pt < 32 * G && g1 * G + pt / 32 < a.Q)  // 512 B a thread: 32 threads per query block
-      tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + pt * 2) * 128, 512);
+    if (g1 >= 0) load_first(g1, pre_b);
     int k = -1;
     for (int it = wk.next(a, i_begin); it < i_end;
          it = wk.next(a, (it / a.tiles_per_group + 1) * a.tiles_per_group)) {
@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
       } else {
         tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
       }
-      Pre& pre = pre_a;
-      if (g != g0) load_first(g, pre_a);  // a later group: request it now
+      Pre& pre = g == g1 ? pre_b : pre_a;
+      if (g != g0 && g != g1) load_first(g, pre_a);  // a later group: request it now
       // RoPE table (G x 32 entries) from the preloaded position and frequency
       for (int e = pt; e < G * 32; e += kPrepThreads) {
         int p = pre.p;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
         const float w = pre.wv[i] * a.wscale;
         wbuf[slot * N + pt + i * kPrepThreads] = w;
         const int e = pt + i * kPrepThreads;
-        if (a.overlap && g * G + e / 64 < a.Q) a.w_out[(size_t)(g * G) * 64 + e] = w;
+        if (kOverlap && g * G + e / 64 < a.Q) a.w_out[(size_t)(g * G) * 64 + e] = w;
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&q_full[slot]);
@@ -436,21 +436,24 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
   a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
   a.scores = scores; a.err = err;
-  a.overlap = overlap ? 1 : 0;
   if (overlap) {
     if (!pos || G != 1) return cudaErrorInvalidValue;
     a.qr_out = static_cast<__nv_bfloat16*>(ws);
     a.w_out = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)Q * 64 * 128 * 2);
   }
   const int grid = min(g_num_sms, a.n_items);
-  if (G == 1) {
+  if (G == 1 && overlap) {
     constexpr int smem = IdxCfg<1>::kSmem;
-    cudaFuncSetAttribute(k_tc_index_scores<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+    cudaFuncSetAttribute(k_tc_index_scores<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+  } else if (G == 1) {
+    constexpr int smem = IdxCfg<1>::kSmem;
+    cudaFuncSetAttribute(k_tc_index_scores<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(kThreads), smem, s, tk, a);
   } else {
     constexpr int smem = IdxCfg<4>::kSmem;
-    cudaFuncSetAttribute(k_tc_index_scores<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<4>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+    cudaFuncSetAttribute(k_tc_index_scores<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(kThreads), smem, s, tk, a);
   }
   return cudaGetLastError();
 }
