@@ -172,6 +172,9 @@ class DecodeWorkload:
         import deepseek_v4_compressed_csa_gb300 as csa
         self.cfg, self.cap, self.dev = cfg, cap, device
         self.serial_indexer = serial_indexer
+        # where the main stream joins the attention pool's compress call (one-stream indexer order): before the
+        # indexer, or after it (then attention has two predecessors)
+        self.join_before_index = False
         self.L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
                            Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
         d = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
@@ -203,9 +206,10 @@ class DecodeWorkload:
         self.csa = csa
 
     def front(self, inp):
-        """Phase 1: the two compress calls on two side streams, and on the main stream the indexer in its
-        overlapped form: its scan of the rows complete before the token runs while the index pool's compress
-        call runs, and its selection waits for that call's event.  Each concurrent call has its own workspace."""
+        """Phase 1: the attention pool's compress call on a side stream; on the main stream the index pool's
+        compress call and then the indexer (or, with overlapped_indexer, the index pool's call on a second side
+        stream and csa_index_topk_overlapped beside it, its selection waiting for that call's event).  Each
+        concurrent call has its own workspace."""
         import torch
         csa = self.csa
         main = torch.cuda.current_stream()
@@ -216,6 +220,8 @@ class DecodeWorkload:
         if self.cfg.has_indexer and self.serial_indexer:
             csa.compress_append(self.L, self.ci, inp["x"], self.pos, self.front_i, self.ikeys, self.n_i, self.invf,
                                 ws=self.ws_c, err=self.err)
+            if self.join_before_index:
+                main.wait_stream(self.side)
             csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
                            self.n_sel, ws=self.ws_i, err=self.err)
         elif self.cfg.has_indexer:
@@ -227,7 +233,8 @@ class DecodeWorkload:
             csa.index_topk_overlapped(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf,
                                       self.sel, self.n_sel, pool_ready=self.pool_ready, ws=self.ws_i, err=self.err)
             main.wait_stream(self.side2)
-        main.wait_stream(self.side)
+        if not (self.cfg.has_indexer and self.serial_indexer and self.join_before_index):
+            main.wait_stream(self.side)
 
     def attend(self, inp):
         """Phase 2: attention over the selected rows and the window, merge; then the caller advances pos."""

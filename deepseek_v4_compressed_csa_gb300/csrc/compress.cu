@@ -111,21 +111,28 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
       if (part) {
         // single new token with split-K partials: sum them in split order, round once to the model dtype
         for (int e = threadIdx.x * 4; e < rowlen; e += blockDim.x * 4) {
-          constexpr int kMaxSplits = 8;  // the projection never splits further
-          float4 v[kMaxSplits];
+          // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
+          constexpr int kBatch = 8;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s0 = 0; s0 < splits; s0 += kBatch) {
+            float4 v[kBatch];
 #pragma unroll
-          for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < splits)
-              v[sp] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)sp * part_stride + b) * rowlen + e));
-          float4 acc = v[0];
+            for (int i = 0; i < kBatch; ++i)
+              if (s0 + i < splits)
+                v[i] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + i) * part_stride + b) * rowlen + e));
 #pragma unroll
-          for (int sp = 1; sp < kMaxSplits; ++sp)
-            if (sp < splits) {
-              acc.x += v[sp].x;
-              acc.y += v[sp].y;
-              acc.z += v[sp].z;
-              acc.w += v[sp].w;
-            }
+            for (int i = 0; i < kBatch; ++i)
+              if (s0 + i < splits) {
+                if (s0 + i == 0) {
+                  acc = v[i];
+                } else {
+                  acc.x += v[i].x;
+                  acc.y += v[i].y;
+                  acc.z += v[i].z;
+                  acc.w += v[i].w;
+                }
+              }
+          }
           const float f[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {

@@ -522,7 +522,9 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
 
 // Merge of S split partials for 8 heads of one query: warp w owns head 8*blockIdx.x + w, lane owns latent
 // dims 16*lane .. 16*lane+15.  M = max(z, m_s); Z = e^{z-M} + sum_s l_s e^{m_s-M}; o = sum_s acc_s e^{m_s-M} / Z;
-// bf16; inverse RoPE on the last 64 dims; bf16.  Every split's float4 loads are issued before they are used.
+// bf16; inverse RoPE on the last 64 dims; bf16.  The first four splits' accumulators are requested together with
+// the split statistics (one memory round trip for S <= 4); a split that holds no rows (m = -inf) has weight 0 and
+// its accumulator, which it did not write, is not used.
 __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part_ml, const float* __restrict__ part_acc,
                                                   int S, const float* __restrict__ sink, const int32_t* __restrict__ pos,
                                                   const float* __restrict__ inv_freq, __nv_bfloat16* __restrict__ out) {
@@ -531,13 +533,25 @@ __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part
   __shared__ float rc[32], rs[32];
   const int q = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 8 + warp;
-  const int p = pos[q];
-  if (threadIdx.x < 32) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
-  // split statistics: lane s holds split s (S <= 32)
-  const float z = sink[h];
   const size_t base = (size_t)q * S * kAH + h;
+  float4 x[4][4];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (s0 + k < S) {
+        const float4* pa = reinterpret_cast<const float4*>(part_acc + (base + (size_t)(s0 + k) * kAH) * kAD + lane * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[k][c] = __ldcg(pa + c);
+      }
+    }
+  };
+  load_batch(0);
+  // split statistics: lane s holds split s (S <= 32)
   const float m_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2) : -INFINITY;
   const float l_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2 + 1) : 0.f;
+  const float z = sink[h];
+  const int p = pos[q];
+  if (threadIdx.x < 32) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
   const float M = fmaxf(z, warp_max(m_l));
   const float f_l = m_l == -INFINITY ? 0.f : expf(m_l - M);
   const float Z = expf(z - M) + warp_sum(l_l * f_l);
@@ -545,26 +559,17 @@ __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part
 #pragma unroll
   for (int e = 0; e < 16; ++e) v[e] = 0.f;
   for (int s0 = 0; s0 < S; s0 += 4) {
-    float4 x[4][4];
-    float f[4];
+    if (s0 > 0) load_batch(s0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      f[k] = __shfl_sync(0xffffffffu, f_l, (s0 + k) & 31);
-      if (s0 + k < S && f[k] != 0.f) {
-        const float4* pa = reinterpret_cast<const float4*>(part_acc + (base + (size_t)(s0 + k) * kAH) * kAD + lane * 16);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) x[k][c] = __ldcg(pa + c);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (s0 + k < S && f[k] != 0.f) {
+      const float f = __shfl_sync(0xffffffffu, f_l, (s0 + k) & 31);
+      if (s0 + k < S && f != 0.f) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          v[4 * c] = fmaf(x[k][c].x, f[k], v[4 * c]);
-          v[4 * c + 1] = fmaf(x[k][c].y, f[k], v[4 * c + 1]);
-          v[4 * c + 2] = fmaf(x[k][c].z, f[k], v[4 * c + 2]);
-          v[4 * c + 3] = fmaf(x[k][c].w, f[k], v[4 * c + 3]);
+          v[4 * c] = fmaf(x[k][c].x, f, v[4 * c]);
+          v[4 * c + 1] = fmaf(x[k][c].y, f, v[4 * c + 1]);
+          v[4 * c + 2] = fmaf(x[k][c].z, f, v[4 * c + 2]);
+          v[4 * c + 3] = fmaf(x[k][c].w, f, v[4 * c + 3]);
         }
       }
     }

@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kPThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kMaxSplits = 8;
+constexpr int kMaxSplits = 16;
 
 struct PjArgs {
   int ntok, X, Ld, N, n_kblk, splits;  // n_kblk: 64-wide K blocks per split
@@ -148,20 +148,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
   for (int e = threadIdx.x; e < N * 32; e += blockDim.x) {
     const int c = e / 32, o = m * 128 + (e % 32) * 4, tok = n * N + c;
     if (tok >= a.ntok) continue;
-    float4 v[kMaxSplits];
+    constexpr int kBatch = 8;  // each batch's loads are issued before its adds; the sum stays in split order
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < a.splits; s0 += kBatch) {
+      float4 v[kBatch];
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
-      if (s < a.splits)
-        v[s] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)s * a.n_cols + tok) * 2 * a.Ld + o));
-    float4 acc = v[0];
+      for (int i = 0; i < kBatch; ++i)
+        if (s0 + i < a.splits)
+          v[i] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)(s0 + i) * a.n_cols + tok) * 2 * a.Ld + o));
 #pragma unroll
-    for (int s = 1; s < kMaxSplits; ++s)
-      if (s < a.splits) {
-        acc.x += v[s].x;
-        acc.y += v[s].y;
-        acc.z += v[s].z;
-        acc.w += v[s].w;
-      }
+      for (int i = 0; i < kBatch; ++i)
+        if (s0 + i < a.splits) {
+          if (s0 + i == 0) {
+            acc = v[i];
+          } else {
+            acc.x += v[i].x;
+            acc.y += v[i].y;
+            acc.z += v[i].z;
+            acc.w += v[i].w;
+          }
+        }
+    }
     __nv_bfloat16* dst = a.proj + (size_t)tok * 2 * a.Ld + o;
     *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x, acc.y);
     *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z, acc.w);
