@@ -207,6 +207,11 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// arrive at hardware barrier `id` without waiting (the waiting side uses named_bar with the same count)
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // barrier among `nthreads` threads that also ORs a predicate across them: every
 // participant gets the same answer (keeps error exits uniform)
 __device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {

@@ -117,8 +117,11 @@ struct Walker {
   }
 };
 
+// Decode (G = 1) keeps to 128 registers a thread: the compress calls' small kernels running beside the scan
+// on other streams (a pooling CTA: 256 threads x 64 registers) must still fit on the SMs it holds, or the
+// scan's remaining CTAs wait for them to finish.
 template <int G, bool kOverlap>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, IdxArgs a) {
   using C = IdxCfg<G>;
   constexpr int N = C::N;
@@ -176,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ key tiles (TMA)
+    // the query-block warps request their inputs first: issued behind a full ring of key tiles, those few
+    // loads would wait in the same queues, and the first MMA waits for them
+    tc::named_bar(4, 32 + kPrepThreads);
     if (lane == 0) {
       tc::tma_prefetch(&tm_keys);
       int stage = 0;
@@ -339,13 +345,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(a.qr_out + ((size_t)(g * G + qq) * 64 + h) * 128 + c * 8) = raw[b];
       }
     };
-    // the first two groups of the range are requested up front (before the key stream saturates memory and
-    // stretches every round trip)
+    // the first group of the range is requested up front (before the key stream saturates memory and stretches
+    // every round trip); the second is requested too where registers allow (prefill), else prefetched into L2
+    constexpr bool kPreloadSecond = G != 1;
     Pre pre_a, pre_b;
     const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
     const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
     if (i_begin < i_end) load_first(g0, pre_a);
-    if (g1 >= 0) load_first(g1, pre_b);
+    if (g1 >= 0) {
+      if (kPreloadSecond) {
+        load_first(g1, pre_b);
+      } else if (pt < 32 * G && g1 * G + pt / 32 < a.Q) {  // 512 B a thread: 32 threads per query block
+        tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + pt * 2) * 128, 512);
+      }
+    }
+    tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
     for (int it = wk.next(a, i_begin); it < i_end;
          it = wk.next(a, (it / a.tiles_per_group + 1) * a.tiles_per_group)) {
@@ -358,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
       }
-      Pre& pre = g == g1 ? pre_b : pre_a;
-      if (g != g0 && g != g1) load_first(g, pre_a);  // a later group: request it now
+      const bool second = kPreloadSecond && g == g1;
+      Pre& pre = second ? pre_b : pre_a;
+      if (g != g0 && !second) load_first(g, pre_a);  // a later group: request it now
       // RoPE table (G x 32 entries) from the preloaded position and frequency
       for (int e = pt; e < G * 32; e += kPrepThreads) {
         int p = pre.p;
