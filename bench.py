@@ -190,7 +190,25 @@ class DecodeWorkload:
         self.sink, self.invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
         B = cfg.B
         self.host_inputs = [csa_synth.step_inputs(cfg, i) for i in range(n_inputs)]
-        self.inputs = [{k: d(getattr(si, k)) for k in ("x", "q", "kv", "iq", "iw")} for si in self.host_inputs]
+        # each input set lives in one packed device buffer (256-byte aligned fields), so that a step's inputs
+        # can arrive from pinned host memory in a single copy
+        names = ("x", "q", "kv", "iq", "iw")
+        t0 = self.host_inputs[0]
+        self.fields, off = [], 0
+        for k in names:
+            t = getattr(t0, k)
+            nb = t.numel() * t.element_size()
+            self.fields.append((k, off, nb, t.dtype, tuple(t.shape)))
+            off = (off + nb + 255) // 256 * 256
+        self.packed_bytes = off
+        self.packed = [torch.empty(off, dtype=torch.uint8, device=device) for _ in self.host_inputs]
+        self.inputs = []
+        for buf, si in zip(self.packed, self.host_inputs):
+            views = {}
+            for k, o, nb, dt, shape in self.fields:
+                views[k] = buf[o:o + nb].view(dt).view(shape)
+                views[k].copy_(getattr(si, k))
+            self.inputs.append(views)
         self.sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
         self.n_sel = torch.empty(B, dtype=torch.int32, device=device)
         self.out = torch.empty(B, cfg.H, cfg.D, dtype=cfg.storage, device=device)
@@ -204,6 +222,14 @@ class DecodeWorkload:
         self.ws_i = u8(csa.workspace_size(self.L, csa.OP_INDEX_TOPK, B, 1, cap))
         self.ws_a = u8(csa.workspace_size(self.L, csa.OP_ATTEND_DECODE, B, 1, cap))
         self.csa = csa
+
+    def packed_host(self, i):
+        """Input set i packed as in its device buffer, in pinned host memory."""
+        import torch
+        h = torch.zeros(self.packed_bytes, dtype=torch.uint8).pin_memory()
+        for k, o, nb, dt, shape in self.fields:
+            h[o:o + nb].view(dt).view(shape).copy_(getattr(self.host_inputs[i], k))
+        return h
 
     def front(self, inp):
         """Phase 1: the attention pool's compress call on a side stream; on the main stream the index pool's
@@ -367,10 +393,11 @@ def run_ours(args):
                     for k, name in enumerate(("compress_x2_and_index", "attend"))}
         wl.capture()
 
-    # ---- end to end: pinned host inputs -> the graphs' input buffers, step, output -> pinned host
-    pinned = [{k: getattr(si, k).pin_memory() for k in ("x", "q", "kv", "iq", "iw")} for si in wl.host_inputs]
+    # ---- end to end: a step's inputs from pinned host memory in one copy (the five inputs packed as in the
+    # graphs' input buffer), the step, its output back to pinned host memory
+    pinned = [wl.packed_host(i) for i in range(len(wl.host_inputs))]
     out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in pinned[0].values())
+    h2d = wl.packed_bytes  # the bytes the one copy moves (fields plus alignment padding)
     d2h = out_host.numel() * out_host.element_size()
     ev2 = [(mk(), mk()) for _ in range(args.e2e_steps)]
     torch.cuda.synchronize()
@@ -378,8 +405,7 @@ def run_ours(args):
         flush.zero_()
         ev2[i][0].record(stream)
         k = i % len(pinned)
-        for name, v in pinned[k].items():
-            wl.inputs[k][name].copy_(v, non_blocking=True)
+        wl.packed[k].copy_(pinned[k], non_blocking=True)
         wl.replay(k)
         out_host.copy_(wl.out, non_blocking=True)
         ev2[i][1].record(stream)
