@@ -229,6 +229,177 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
   if (fuse_finish && blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
 }
 
+// One new token per sequence, its projection as split-K partials (the decode step of a ratio-4 layer with two
+// lanes): one block per sequence.  Same arithmetic as k_pool_emit, with its memory requests in two rounds:
+// norm weights, APE and RoPE frequencies do not depend on the position and are requested with it; the
+// partials and the window's seven older frontier entries are requested together once it is known (a token
+// that completes a window has p = 3 mod 4, so its window covers tokens p-7 .. p in a fixed lane / APE order).
+constexpr int kTokChans = 2;  // channels per thread: d <= 512
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ flags, const int32_t* __restrict__ pos,
+                                                         int32_t* __restrict__ n_rows, int32_t* err, int d, int R,
+                                                         int F, T* __restrict__ frontier,
+                                                         const float* __restrict__ ape,
+                                                         const float* __restrict__ norm_w, float eps,
+                                                         const float* __restrict__ inv_freq, T* __restrict__ pool,
+                                                         int cap, const float* __restrict__ part, int splits,
+                                                         int part_stride) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int ratio = 4, lanes = 2, kEnt = ratio * lanes;
+  extern __shared__ float sm_tok[];  // [2*L*d] the new token, [d] pooled, [d] normed, 32 reduction slots, [R] rope
+  const int Ld = lanes * d, rowlen = 2 * Ld;
+  float* cur = sm_tok;
+  float* u = cur + rowlen;
+  float* y = u + d;
+  float* red = y + d;
+  float* rc = red + 32;
+  float* rs = rc + R / 2;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  // round 1: the position with everything that does not depend on it
+  const int p0 = pos[b];
+  const int n = n_rows[b];
+  float nw[kTokChans], ap[kTokChans][kEnt];
+#pragma unroll
+  for (int i = 0; i < kTokChans; ++i) {
+    const int c = tid + 256 * i;
+    nw[i] = c < d ? __ldg(norm_w + c) : 0.f;
+#pragma unroll
+    for (int e = 0; e < kEnt; ++e)  // entry e: token p-7+e, APE row e mod ratio, lane e / ratio
+      ap[i][e] = c < d ? __ldg(ape + (size_t)(e % ratio) * Ld + (e / ratio) * d + c) : 0.f;
+  }
+  const float fq = tid < R / 2 ? __ldg(inv_freq + tid) : 0.f;
+  const int bad = compress_state_error(p0, n, 1, ratio, cap);
+  __syncthreads();  // every thread has read n_rows before thread 0 may advance it
+  if (tid == 0) {
+    flags[b] = !bad;
+    if (bad) atomicOr(err, bad);
+  }
+  if (bad) return;
+  const bool completes = (p0 + 1) % ratio == 0;
+  const int j = (p0 + 1) / ratio - 1;
+  // round 2: the partials of the new token and, if it completes window j, the window's older entries
+  const T* fr = frontier + (size_t)b * F * rowlen;
+  float g[kTokChans][kEnt - 1], kv[kTokChans][kEnt - 1];
+  if (completes) {
+#pragma unroll
+    for (int i = 0; i < kTokChans; ++i) {
+      const int c = tid + 256 * i;
+#pragma unroll
+      for (int e = 0; e < kEnt - 1; ++e) {
+        const int t = p0 - (kEnt - 1) + e;
+        g[i][e] = 0.f;
+        kv[i][e] = 0.f;
+        if (c < d && t >= 0) {
+          const T* row = fr + (size_t)(t % F) * rowlen + (e / ratio) * d + c;
+          g[i][e] = to_f(row[Ld]);
+          kv[i][e] = to_f(row[0]);
+        }
+      }
+    }
+  }
+  {
+    T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
+    for (int e = tid * 4; e < rowlen; e += 256 * 4) {
+      // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
+      constexpr int kBatch = 8;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < splits; s0 += kBatch) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          if (s0 + i < splits)
+            v[i] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + i) * part_stride + b) * rowlen + e));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          if (s0 + i < splits) {
+            if (s0 + i == 0) {
+              acc = v[i];
+            } else {
+              acc.x += v[i].x;
+              acc.y += v[i].y;
+              acc.z += v[i].z;
+              acc.w += v[i].w;
+            }
+          }
+      }
+      const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const T r = from_f<T>(f[i]);
+        dst[e + i] = r;
+        cur[e + i] = to_f(r);
+      }
+    }
+  }
+  if (tid < R / 2) {
+    float cs, sn;
+    sincosf(__fmul_rn((float)(j * ratio), fq), &sn, &cs);
+    rc[tid] = cs;
+    rs[tid] = sn;
+  }
+  __syncthreads();
+  if (!completes) {
+    if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
+    return;
+  }
+  // window j: entries p-7 .. p (lane 0 for window j-1, lane 1 for window j); the last is the new token
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kTokChans; ++i) {
+    const int c = tid + 256 * i;
+    if (c >= d) continue;
+    float sv[kEnt], kk[kEnt];
+#pragma unroll
+    for (int e = 0; e < kEnt; ++e) {
+      const int t = p0 - (kEnt - 1) + e;
+      if (t < 0) {
+        sv[e] = -INFINITY;
+        kk[e] = 0.f;
+      } else if (e == kEnt - 1) {
+        sv[e] = cur[Ld + d + c] + ap[i][e];
+        kk[e] = cur[d + c];
+      } else {
+        sv[e] = g[i][e] + ap[i][e];
+        kk[e] = kv[i][e];
+      }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kEnt; ++e) m = fmaxf(m, sv[e]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int e = 0; e < kEnt; ++e) {
+      const float x = (sv[e] == -INFINITY) ? 0.f : expf(sv[e] - m);
+      den += x;
+      num = fmaf(x, kk[e], num);
+    }
+    const float uc = rnd<T>(num / den);
+    u[c] = uc;
+    ss = fmaf(uc, uc, ss);
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int i = 0; i < kTokChans; ++i) {
+    const int c = tid + 256 * i;
+    if (c < d) y[c] = rnd<T>(u[c] * inv * nw[i]);
+  }
+  __syncthreads();
+  T* dst = pool + ((size_t)b * cap + j) * d;
+  for (int c = tid; c < d; c += 256) {
+    float v = y[c];
+    if (c >= d - R) {
+      const int i = (c - (d - R)) >> 1;
+      const float a = y[d - R + 2 * i], bb = y[d - R + 2 * i + 1];
+      v = ((c - (d - R)) & 1) ? fmaf(a, rs[i], bb * rc[i]) : fmaf(a, rc[i], -bb * rs[i]);
+    }
+    dst[c] = from_f<T>(v);
+  }
+  if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
+}
+
 // Rewrite the frontier slots of the newest min(T, F) tokens; block (0, b) advances n_rows.
 template <typename T>
 __global__ void k_compress_finish(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos, int T_,
@@ -272,6 +443,13 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
     CSA_LAUNCH(k_project_simt<T, 8>, dim3(gp), dim3(256), 0, s, static_cast<const T*>(x), static_cast<const T*>(comp.wkv),
                                              static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
                                              static_cast<T*>(ws.proj));
+  }
+  if (part && L.ratio == 4 && L.lanes == 2 && L.F == 8 && d <= 256 * kTokChans) {
+    const size_t smem = ((size_t)rowlen + 2 * (size_t)d + 32 + L.R) * sizeof(float);
+    CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(256), smem, s, ws.flags, pos, n_rows, err, d, L.R, L.F,
+               static_cast<T*>(frontier), comp.ape, comp.norm_w, L.eps, inv_freq, static_cast<T*>(pool), cap,
+               part, splits, part_stride);
+    return cudaGetLastError();
   }
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
   dim3 ge(maxwin, B);
