@@ -427,8 +427,8 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   CSA_LAUNCH(k_rope_rows<T>, dim3(T_), dim3(256), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(ws.kvr), 1, L.D, L.R, nullptr,
                                     pos0, inv_freq);
   if (tc_attend_supported(L)) {
-    cudaError_t e = launch_tc_attend(L, q, pool, window, ws.kvr, nullptr, sel, n_sel, n_rows, nullptr, pos0, cap,
-                                     sink, inv_freq, T_, 1, nullptr, nullptr, out, err, s);
+    cudaError_t e = launch_tc_attend_prefill(L, q, pool, window, ws.kvr, sel, n_sel, n_rows, pos0, cap, sink,
+                                             inv_freq, T_, out, err, s);
     if (e != cudaSuccess) return e;
     CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.W)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
                                                         L.D, T_, pos0);

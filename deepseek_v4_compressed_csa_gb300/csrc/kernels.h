@@ -129,6 +129,14 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
                             const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s);
 
+// ---- tc_attend_prefill.cu (tensor-core chunked-prefill attention; bf16, H = 64, D = 512, R = 64)
+// T queries of one sequence at positions pos0 + q; the chunk's roped rows kvr [T, D], the ring before the
+// chunk, pool [cap, D]; persistent CTAs (one per SM) finalise the output.  Requires tc_attend_supported(L).
+cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* pool, const void* ring,
+                                     const void* kvr, const int32_t* sel, const int32_t* n_sel,
+                                     const int32_t* n_rows, int pos0, int cap, const float* sink,
+                                     const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s);
+
 // ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_decode_supported(const Dims& L);
 // Key splits per query for Q queries of at most max_rows rows: every split <= 160 rows, more splits while every

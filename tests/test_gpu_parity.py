@@ -160,18 +160,9 @@ def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs, overlap):
         G.check_pool_rows(st_g.window[b].cpu(), st_o[b]["window"][0], "bf16", "window")
 
 
-def test_config5_prefill_chunk_sampled_queries():
-    """Config 5: a 4096-token chunk on a 65536-token cache.  All emitted rows, the frontier and the window
-    are checked; the per-query selection and output are checked on sampled queries."""
-    cfg = csa_synth.CONFIGS[5]
-    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
-    run = G.Runner(cfg)
-    host = csa_synth.synth_cache(cfg, cap)
-    st_g = G.DevCache(host)
-    ch = csa_synth.chunk_inputs(cfg)
-    out, sel = run.prefill(st_g, ch, cfg.ctx)
-    torch.cuda.synchronize()
-    assert run.err.item() == 0
+def _check_prefill(cfg, run, host, ch, out, sel, queries):
+    """Oracle check of one prefill chunk on a single-sequence cache: every emitted row of both pools, the index
+    frontier and the window after the chunk; the selection and output of each query in ``queries``."""
     layer = oracle_layer(cfg)
     ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
     invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
@@ -184,21 +175,16 @@ def test_config5_prefill_chunk_sampled_queries():
                                                                   "chunk attn")
     st["front_i"], st["ikeys"], _, _ = G.oracle_compress_checked(layer, ci, x, st["pos"], st["front_i"], st["ikeys"],
                                                                  n0, invf, run.projs["index"].cpu(), "chunk index")
+    T = ch.q.shape[0]
     n = int(n_a[0])
-    assert n == st_g.n_rows.item() == (cfg.ctx + cfg.T) // 4
     lo = cfg.ctx // 4
-    G.check_pool_rows(st_g.pool[0, lo:n].cpu(), st["pool"][0, lo:n], "bf16", "chunk pool rows", R=cfg.R)
-    G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), st["ikeys"][0, lo:n], "bf16", "chunk index rows", R=cfg.R)
-    G.check_pool_rows(st_g.front_index.cpu(), st["front_i"], "bf16", "index frontier")
     q, kv, iq, iw = f64(ch.q), f64(ch.kv), f64(ch.iq), f64(ch.iw)
-    rng = np.random.default_rng(0)
-    queries = sorted(set([0, 1, 2, 3, 4, 126, 127, 128, 129, 2047, 4094, 4095] +
-                         list(rng.integers(0, cfg.T, 8))))
     window = st["window"][0]
     pool, ikeys = st["pool"][0], st["ikeys"][0]
-    kvr = [O.store(O.rope(kv[i], cfg.ctx + i, invf), "bf16") for i in range(cfg.T)]
+    kvr = [O.store(O.rope(kv[i], cfg.ctx + i, invf), "bf16") for i in range(T)]
     gsel = sel.cpu().numpy()
     gout = out.cpu()
+    worst = 0.0
     for i in queries:
         p = cfg.ctx + i
         nv = O.visible_rows(layer, n, p)
@@ -209,11 +195,58 @@ def test_config5_prefill_chunk_sampled_queries():
         keys = np.concatenate([pool[np.sort(rows)], np.stack(win)])
         qr = O.store(O.rope(q[i], p, invf), "bf16")
         o = O.output_rows(layer, O.attend(layer, qr, keys, sink), p, invf)
-        G.check_rows(gout[i], o, "bf16", what=f"query {i} output", R=cfg.R)
+        worst = max(worst, G.check_rows(gout[i], o, "bf16", what=f"query {i} output", R=cfg.R))
     ring = np.array(window)
-    for t in range(cfg.ctx + cfg.T - cfg.W, cfg.ctx + cfg.T):
+    for t in range(max(cfg.ctx, cfg.ctx + T - cfg.W), cfg.ctx + T):
         ring[t % cfg.W] = kvr[t - cfg.ctx]
+    return st, n, lo, ring, worst
+
+
+def test_config5_prefill_chunk_sampled_queries():
+    """Config 5: a 4096-token chunk on a 65536-token cache.  All emitted rows, the frontier and the window
+    are checked; the per-query selection and output are checked on sampled queries."""
+    cfg = csa_synth.CONFIGS[5]
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
+    run = G.Runner(cfg)
+    host = csa_synth.synth_cache(cfg, cap)
+    st_g = G.DevCache(host)
+    ch = csa_synth.chunk_inputs(cfg)
+    out, sel = run.prefill(st_g, ch, cfg.ctx)
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    rng = np.random.default_rng(0)
+    queries = sorted(set([0, 1, 2, 3, 4, 126, 127, 128, 129, 151, 152, 153, 303, 304, 2047, 4094, 4095] +
+                         list(rng.integers(0, cfg.T, 12))))
+    st, n, lo, ring, _ = _check_prefill(cfg, run, host, ch, out, sel, queries)
+    assert n == st_g.n_rows.item() == (cfg.ctx + cfg.T) // 4
+    G.check_pool_rows(st_g.pool[0, lo:n].cpu(), st["pool"][0, lo:n], "bf16", "chunk pool rows", R=cfg.R)
+    G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), st["ikeys"][0, lo:n], "bf16", "chunk index rows", R=cfg.R)
+    G.check_pool_rows(st_g.front_index.cpu(), st["front_i"], "bf16", "index frontier")
     G.check_pool_rows(st_g.window[0].cpu(), ring, "bf16", "window after chunk")
+
+
+def test_prefill_every_query_with_late_dominant_rows():
+    """Every query of a 300-token chunk (two or more queries per CTA of the chunk kernel) against the oracle.
+    The kv row of every third token is 4x the query of head (token mod 64): that head's logit on its own
+    token, the last row of the query's last tile, is ~2^130 above the rest, so the running reference max is
+    raised after earlier tiles were accumulated (the rescale of O and of the sums)."""
+    cfg = csa_synth.CONFIGS[5].replace(ctx=8192 + 2, T=300)
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
+    run = G.Runner(cfg)
+    host = csa_synth.synth_cache(cfg, cap)
+    st_g = G.DevCache(host)
+    ch = csa_synth.chunk_inputs(cfg)
+    kv = ch.kv.clone()
+    for i in range(0, cfg.T, 3):
+        kv[i] = (4 * ch.q[i, i % cfg.H].float()).to(kv.dtype)
+    ch = csa_synth.StepInputs(x=ch.x, q=ch.q, kv=kv, iq=ch.iq, iw=ch.iw)
+    out, sel = run.prefill(st_g, ch, cfg.ctx)
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    _, n, _, ring, worst = _check_prefill(cfg, run, host, ch, out, sel, range(cfg.T))
+    assert n == st_g.n_rows.item()
+    G.check_pool_rows(st_g.window[0].cpu(), ring, "bf16", "window after chunk")
+    print(f"prefill, every query: worst max-relative output error {worst:.2e}")
 
 
 def test_gpu_decode_equals_gpu_prefill():
