@@ -263,23 +263,37 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
       tc::fence_after_sync();
       const int j = t * kTileRows + row;
       const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
+      // two queries' columns per TMEM round trip (one wait covers both loads)
 #pragma unroll
-      for (int qq = 0; qq < G; ++qq) {
-        uint32_t v[64];
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * N + qq * 64;
-        tc::tmem_ld32(taddr, v);
-        tc::tmem_ld32(taddr + 32, v + 32);
-        tc::tmem_wait_ld();
-        float s = 0.f;
+      for (int qp = 0; qp < G; qp += 2) {
+        constexpr int kPer = G > 1 ? 2 : 1;
+        uint32_t v[kPer][64];
 #pragma unroll
-        for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 w = w4[qq * 16 + h4];
-          s = fmaf(w.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), s);
-          s = fmaf(w.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s);
-          s = fmaf(w.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s);
-          s = fmaf(w.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s);
+        for (int u = 0; u < kPer; ++u) {
+          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * N + (qp + u) * 64;
+          tc::tmem_ld32(taddr, v[u]);
+          tc::tmem_ld32(taddr + 32, v[u] + 32);
         }
-        if (j < nv[qq]) a.scores[(size_t)(g * G + qq) * a.cap + j] = s;
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int qq = qp + u;
+          // four partial sums (heads h = 0, 1, 2, 3 mod 4, each in increasing h) as two packed fp32 pairs, then
+          // (p0 + p1) + (p2 + p3): four independent chains instead of one of 64 dependent FMAs
+          float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int h4 = 0; h4 < 16; ++h4) {
+            const float4 w = w4[qq * 16 + h4];
+            const float2 r01 = make_float2(fmaxf(__uint_as_float(v[u][4 * h4]), 0.f),
+                                           fmaxf(__uint_as_float(v[u][4 * h4 + 1]), 0.f));
+            const float2 r23 = make_float2(fmaxf(__uint_as_float(v[u][4 * h4 + 2]), 0.f),
+                                           fmaxf(__uint_as_float(v[u][4 * h4 + 3]), 0.f));
+            s01 = __ffma2_rn(make_float2(w.x, w.y), r01, s01);
+            s23 = __ffma2_rn(make_float2(w.z, w.w), r23, s23);
+          }
+          const float s = (s01.x + s01.y) + (s23.x + s23.y);
+          if (j < nv[qq]) a.scores[(size_t)(g * G + qq) * a.cap + j] = s;
+        }
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&acc_empty[acc]);
