@@ -559,7 +559,17 @@ def main():
                          "csa_index_topk after it on one stream")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--oracle-sample", nargs=3, default=None)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the 4096-token prefill chunk (for profiling its kernels); prints its record")
     args = ap.parse_args()
+    if args.prefill_only:
+        import torch
+        import csa_synth
+        import deepseek_v4_compressed_csa_gb300 as csa
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        print(json.dumps(run_prefill(csa, csa_synth, dev, flush, args.prefill_repeats)))
+        return
     if args.oracle_sample:
         cid, budget, mx = args.oracle_sample
         print(json.dumps(oracle_sample(int(cid), float(budget), int(mx))))

@@ -30,8 +30,7 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * 128 * 2;  // 128 rows x 128 bf16
-constexpr int kThreads = 256;
-constexpr int kPrepThreads = 64;                 // warps 6-7
+constexpr int kPrepThreads = 64;                 // the last two warps
 
 template <int G>
 struct IdxCfg {
@@ -46,6 +45,12 @@ struct IdxCfg {
   static constexpr int kOffBars = kOffRope + G * 64 * 4;
   static constexpr int kNumBars = 2 * kStages + 3 * kQSlots + 2 * kAcc + 1;
   static constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
+  // warps: 0 TMA, 1 MMA, 2 .. 2 + kEpiWarps - 1 epilogue, then two query-block warps.  A prefill tile has four
+  // queries' columns to reduce: eight epilogue warps, two per TMEM lane quarter, take two queries each.
+  static constexpr int kEpiWarps = G == 1 ? 4 : 8;
+  static constexpr int kQPerWarp = G / (kEpiWarps / 4);
+  static constexpr int kPrepWarp0 = 2 + kEpiWarps;
+  static constexpr int kThreads = 32 * kPrepWarp0 + kPrepThreads;
 };
 
 struct IdxArgs {
@@ -121,7 +126,7 @@ struct Walker {
 // on other streams (a pooling CTA: 256 threads x 64 registers) must still fit on the SMs it holds, or the
 // scan's remaining CTAs wait for them to finish.
 template <int G, bool kOverlap>
-__global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
+__global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, IdxArgs a) {
   using C = IdxCfg<G>;
   constexpr int N = C::N;
@@ -153,11 +158,11 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
     for (int s = 0; s < C::kQSlots; ++s) {
       tc::mbar_init(&q_full[s], kPrepThreads);
       tc::mbar_init(&q_empty[s], 1);
-      tc::mbar_init(&w_empty[s], 4);
+      tc::mbar_init(&w_empty[s], C::kEpiWarps);
     }
     for (int i = 0; i < C::kAcc; ++i) {
       tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_empty[i], 128);
+      tc::mbar_init(&acc_empty[i], 32 * C::kEpiWarps);
     }
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
       tc::mma_commit(drain);
       if (!tc::mbar_wait(drain, 0)) failed = true;
     }
-  } else if (warp < 6) {
+  } else if (warp < C::kPrepWarp0) {
     // ------------------------------------------------------------ epilogue: warp w drains TMEM lanes 32*(w%4)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -263,10 +268,10 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
       tc::fence_after_sync();
       const int j = t * kTileRows + row;
       const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
-      // two queries' columns per TMEM round trip (one wait covers both loads)
-#pragma unroll
-      for (int qp = 0; qp < G; qp += 2) {
-        constexpr int kPer = G > 1 ? 2 : 1;
+      // this warp's queries (kQPerWarp of them) in one TMEM round trip (one wait covers every load)
+      {
+        constexpr int kPer = C::kQPerWarp;
+        const int qp = ((warp - 2) >> 2) * kPer;
         uint32_t v[kPer][64];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
@@ -310,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
     // chunks) is requested for the CTA's first group before the walk that confirms it, so the whole preparation
     // costs about one memory round trip.  16 chunks of 8 dims per head row; each thread takes 16 (G = 1) or 64
     // (G = 4) chunks, in batches of 16 whose loads are all issued before any is used.
-    constexpr int kBatch = 16;
+    constexpr int kBatch = G == 1 ? 16 : 8;  // prefill: fewer registers (twelve warps share the register file)
     constexpr int kChunks = G * 64 * 16;
-    const int pt = threadIdx.x - 192;
+    const int pt = threadIdx.x - 32 * C::kPrepWarp0;
     struct Pre {
       uint4 raw[kBatch];
       float wv[G];
@@ -360,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
       }
     };
     // the first group of the range is requested up front (before the key stream saturates memory and stretches
-    // every round trip); the second is requested too where registers allow (prefill), else prefetched into L2
-    constexpr bool kPreloadSecond = G != 1;
+    // every round trip); the second is prefetched into L2
+    constexpr bool kPreloadSecond = false;
     Pre pre_a, pre_b;
     const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
     const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
@@ -369,8 +374,9 @@ __global__ void __launch_bounds__(kThreads, G == 1 ? 2 : 1)
     if (g1 >= 0) {
       if (kPreloadSecond) {
         load_first(g1, pre_b);
-      } else if (pt < 32 * G && g1 * G + pt / 32 < a.Q) {  // 512 B a thread: 32 threads per query block
-        tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + pt * 2) * 128, 512);
+      } else {
+        for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
+          if (g1 * G + e / 32 < a.Q) tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + e * 2) * 128, 512);
       }
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
@@ -474,15 +480,15 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   if (G == 1 && overlap) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, a);
   } else if (G == 1) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, a);
   } else {
     constexpr int smem = IdxCfg<4>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(IdxCfg<4>::kThreads), smem, s, tk, a);
   }
   return cudaGetLastError();
 }
