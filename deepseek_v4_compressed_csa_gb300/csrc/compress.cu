@@ -246,7 +246,6 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
                                                          int cap, const float* __restrict__ part, int splits,
                                                          int part_stride) {
   pdl_trigger();
-  pdl_wait();
   constexpr int ratio = 4, lanes = 2, kEnt = ratio * lanes;
   extern __shared__ float sm_tok[];  // [2*L*d] the new token, [d] pooled, [d] normed, 32 reduction slots, [R] rope
   const int Ld = lanes * d, rowlen = 2 * Ld;
@@ -257,9 +256,9 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
   float* rc = red + 32;
   float* rs = rc + R / 2;
   const int b = blockIdx.x, tid = threadIdx.x;
-  // round 1: the position with everything that does not depend on it
+  // before the preceding kernel has completed: the position (a step input) and the layer's constants, which no
+  // kernel writes
   const int p0 = pos[b];
-  const int n = n_rows[b];
   float nw[kTokChans], ap[kTokChans][kEnt];
 #pragma unroll
   for (int i = 0; i < kTokChans; ++i) {
@@ -270,16 +269,12 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
       ap[i][e] = c < d ? __ldg(ape + (size_t)(e % ratio) * Ld + (e / ratio) * d + c) : 0.f;
   }
   const float fq = tid < R / 2 ? __ldg(inv_freq + tid) : 0.f;
-  const int bad = compress_state_error(p0, n, 1, ratio, cap);
-  __syncthreads();  // every thread has read n_rows before thread 0 may advance it
-  if (tid == 0) {
-    flags[b] = !bad;
-    if (bad) atomicOr(err, bad);
-  }
-  if (bad) return;
+  pdl_wait();
+  // one round of requests: n_rows, the partials of the new token and, if it completes window j, the window's
+  // older entries; nothing is written before the state check
+  const int n = n_rows[b];
   const bool completes = (p0 + 1) % ratio == 0;
   const int j = (p0 + 1) / ratio - 1;
-  // round 2: the partials of the new token and, if it completes window j, the window's older entries
   const T* fr = frontier + (size_t)b * F * rowlen;
   float g[kTokChans][kEnt - 1], kv[kTokChans][kEnt - 1];
   if (completes) {
@@ -299,39 +294,32 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
       }
     }
   }
-  {
-    T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
-    for (int e = tid * 4; e < rowlen; e += 256 * 4) {
-      // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
-      constexpr int kBatch = 8;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < splits; s0 += kBatch) {
-        float4 v[kBatch];
+  for (int e = tid * 4; e < rowlen; e += 256 * 4) {
+    // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
+    constexpr int kBatch = 8;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < splits; s0 += kBatch) {
+      float4 v[kBatch];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-          if (s0 + i < splits)
-            v[i] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + i) * part_stride + b) * rowlen + e));
+      for (int i = 0; i < kBatch; ++i)
+        if (s0 + i < splits)
+          v[i] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + i) * part_stride + b) * rowlen + e));
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-          if (s0 + i < splits) {
-            if (s0 + i == 0) {
-              acc = v[i];
-            } else {
-              acc.x += v[i].x;
-              acc.y += v[i].y;
-              acc.z += v[i].z;
-              acc.w += v[i].w;
-            }
+      for (int i = 0; i < kBatch; ++i)
+        if (s0 + i < splits) {
+          if (s0 + i == 0) {
+            acc = v[i];
+          } else {
+            acc.x += v[i].x;
+            acc.y += v[i].y;
+            acc.z += v[i].z;
+            acc.w += v[i].w;
           }
-      }
-      const float f[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const T r = from_f<T>(f[i]);
-        dst[e + i] = r;
-        cur[e + i] = to_f(r);
-      }
+        }
     }
+    const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[e + i] = to_f(from_f<T>(f[i]));  // the token in the model dtype
   }
   if (tid < R / 2) {
     float cs, sn;
@@ -339,7 +327,17 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
     rc[tid] = cs;
     rs[tid] = sn;
   }
-  __syncthreads();
+  const int bad = compress_state_error(p0, n, 1, ratio, cap);
+  __syncthreads();  // every thread has read n_rows before thread 0 may advance it; the token is in shared memory
+  if (tid == 0) {
+    flags[b] = !bad;
+    if (bad) atomicOr(err, bad);
+  }
+  if (bad) return;
+  {
+    T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
+    for (int e = tid; e < rowlen; e += 256) dst[e] = from_f<T>(cur[e]);
+  }
   if (!completes) {
     if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
     return;

@@ -167,6 +167,44 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
   }
+  // Query-block warps: everything the first query block needs (positions, frequencies, head weights and the first
+  // batch of query chunks) is requested before the preceding kernel has completed: these are step inputs and
+  // constants that no kernel writes.  16 chunks of 8 dims per head row; each thread takes 16 (G = 1) or 64 (G = 4)
+  // chunks, in batches whose loads are all issued before any is used.
+  constexpr int kBatch = G == 1 ? 16 : 8;  // prefill: fewer registers (twelve warps share the register file)
+  constexpr int kChunks = G * 64 * 16;
+  const int pt = threadIdx.x - 32 * C::kPrepWarp0;
+  struct Pre {
+    uint4 raw[kBatch];
+    float wv[G];
+    float th_freq;
+    int p;
+  };
+  auto load_first = [&](int g, Pre& pre) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = pt + b * kPrepThreads;
+      const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
+      pre.raw[b] = (e < kChunks && q < a.Q)
+                       ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
+                       : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int e = pt + i * kPrepThreads, q = g * G + e / 64;
+      pre.wv[i] = q < a.Q ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
+    }
+    // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
+    pre.th_freq = __ldg(a.inv_freq + (pt & 31));
+    const int q0 = g * G + pt / 32;
+    pre.p = (pt < G * 32 && q0 < a.Q) ? idx_qpos(a, q0) : 0;
+  };
+  const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
+  const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
+  Pre pre_a, pre_b;
+  const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
+  const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
+  if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
   pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::kAcc * N);
@@ -177,8 +215,6 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
-  const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
   Walker<kOverlap> wk(a.tiles_per_group, i_end);
   bool failed = false;
 
@@ -310,39 +346,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       if (++acc == C::kAcc) acc = 0;
     }
   } else {
-    // ------------------------------------------------------------ query blocks (warps 6-7)
-    // Everything the first query block needs (positions, frequencies, head weights and the first batch of query
-    // chunks) is requested for the CTA's first group before the walk that confirms it, so the whole preparation
-    // costs about one memory round trip.  16 chunks of 8 dims per head row; each thread takes 16 (G = 1) or 64
-    // (G = 4) chunks, in batches of 16 whose loads are all issued before any is used.
-    constexpr int kBatch = G == 1 ? 16 : 8;  // prefill: fewer registers (twelve warps share the register file)
-    constexpr int kChunks = G * 64 * 16;
-    const int pt = threadIdx.x - 32 * C::kPrepWarp0;
-    struct Pre {
-      uint4 raw[kBatch];
-      float wv[G];
-      float th_freq;
-      int p;
-    };
-    auto load_first = [&](int g, Pre& pre) {
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int e = pt + b * kPrepThreads;
-        const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
-        pre.raw[b] = (e < kChunks && q < a.Q)
-                         ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
-                         : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        const int e = pt + i * kPrepThreads, q = g * G + e / 64;
-        pre.wv[i] = q < a.Q ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
-      }
-      // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
-      pre.th_freq = __ldg(a.inv_freq + (pt & 31));
-      const int q0 = g * G + pt / 32;
-      pre.p = (pt < G * 32 && q0 < a.Q) ? idx_qpos(a, q0) : 0;
-    };
+    // ------------------------------------------------------------ query blocks (the last two warps)
+    // The first group's inputs were requested before the wait above (load_first), so its preparation costs about
+    // one memory round trip, overlapped with the preceding kernel.
     auto rope_store = [&](uint8_t* qb, int e0, uint4 (&raw)[kBatch], int g) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
@@ -367,10 +373,6 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     // the first group of the range is requested up front (before the key stream saturates memory and stretches
     // every round trip); the second is prefetched into L2
     constexpr bool kPreloadSecond = false;
-    Pre pre_a, pre_b;
-    const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
-    const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-    if (i_begin < i_end) load_first(g0, pre_a);
     if (g1 >= 0) {
       if (kPreloadSecond) {
         load_first(g1, pre_b);
