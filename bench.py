@@ -267,7 +267,7 @@ class DecodeWorkload:
         sel, n_sel = (self.sel, self.n_sel) if self.cfg.has_indexer else (None, None)
         self.csa.attend_decode(self.L, inp["q"], inp["kv"], self.sink, self.window, self.pool, self.n_a, sel, n_sel,
                                self.pos, self.invf, self.out, ws=self.ws_a, err=self.err)
-        self.pos.add_(1)
+        self.csa.advance_positions(self.pos, 1)
 
     def step(self, inp):
         self.front(inp)

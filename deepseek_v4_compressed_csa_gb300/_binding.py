@@ -23,7 +23,7 @@ CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
-           "csa_index_topk_static", "csa_index_topk_overlapped")
+           "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions")
 
 
 class CSAError(RuntimeError):
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_attend_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, ctypes.c_int32, vp, vp, vp, i32, vp, vp,
                                              vp, vp, vp, sz, vp, vp]
     lib.csa_attend_prefill_chunk.restype = i32
+    lib.csa_advance_positions.argtypes = [vp, i32, i32, vp]
+    lib.csa_advance_positions.restype = i32
     _lib = lib
     return lib
 
@@ -152,6 +154,12 @@ def _check(fn: str, code: int):
 def kernel_launches() -> int:
     """Kernels enqueued by the library so far in this process."""
     return int(load_library().csa_kernel_launches())
+
+
+def advance_positions(pos, by: int = 1, stream=None):
+    """pos[b] += by for every sequence (int32 device tensor), on the library's launch path."""
+    _check("csa_advance_positions", load_library().csa_advance_positions(_ptr(pos), pos.numel(), by,
+                                                                         _stream(stream)))
 
 
 def frontier_slots(ratio: int) -> int:

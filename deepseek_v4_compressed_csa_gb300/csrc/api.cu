@@ -236,4 +236,10 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                            L.has_indexer() ? sel : nullptr, n_sel, inv_freq, out, aw, err, s));
 }
 
+csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream) {
+  if (B < 0 || (B > 0 && !pos)) return CSA_ERR_ARG;
+  if (B == 0) return CSA_OK;
+  return cuda_status(launch_advance_positions(pos, B, by, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

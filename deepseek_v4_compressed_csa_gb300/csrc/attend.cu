@@ -448,6 +448,20 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   return cudaGetLastError();
 }
 
+// pos[b] += by: the decode loop's position advance, launched with programmatic serialisation like every kernel
+// here, so it starts while the step's last kernel drains and only its store waits for it
+__global__ void k_advance_positions(int32_t* __restrict__ pos, int B, int by) {
+  pdl_trigger();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  if (b < B) pos[b] += by;
+}
+
+cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s) {
+  CSA_LAUNCH(k_advance_positions, dim3((B + 255) / 256), dim3(256), 0, s, pos, B, by);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attend_decode(const Dims& L, const void* q, const void* kv_new, const float* sink, int B,
                                  void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
                                  const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,

@@ -129,6 +129,9 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
                             const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s);
 
+// ---- attend.cu: pos[b] += by for b < B
+cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s);
+
 // ---- tc_attend_prefill.cu (tensor-core chunked-prefill attention; bf16, H = 64, D = 512, R = 64)
 // T queries of one sequence at positions pos0 + q; the chunk's roped rows kvr [T, D], the ring before the
 // chunk, pool [cap, D]; persistent CTAs (one per SM) finalise the output.  Requires tc_attend_supported(L).

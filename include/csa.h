@@ -266,6 +266,16 @@ csa_status csa_index_topk_static(const csa_layer* layer, const void* iq, const v
                                  int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
                                  int32_t* sel, int32_t* n_sel, int32_t* err, void* stream);
 
+/* Advance the positions of B sequences by `by` tokens: pos[b] += by, in one kernel
+ * on `stream` (a device array of B int32, caller-owned).  A decode loop calls it
+ * after the step's last library call (csa_attend_decode), since every call of a
+ * step reads pos; it is not part of the method ("Decode path": the position of
+ * the next token), only the loop's bookkeeping, launched like the library's
+ * other kernels so that it may start while the step's last kernel finishes.
+ * Errors: CSA_ERR_ARG for a null pos, B < 0; CSA_ERR_CUDA if the launch fails.
+ * B == 0 enqueues nothing. */
+csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream);
+
 /* Number of kernels this library has enqueued in this process (all calls,
  * all devices).  Diagnostic only: lets a caller count the launches of a region. */
 unsigned long long csa_kernel_launches(void);

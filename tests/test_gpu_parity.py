@@ -422,6 +422,18 @@ def test_device_errors_fail_closed():
     assert torch.isfinite(out.float()).all()
 
 
+def test_advance_positions():
+    """csa_advance_positions adds `by` to every position (more sequences than one block holds), and leaves the
+    array alone for B = 0."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    pos = torch.arange(300, dtype=torch.int32, device="cuda") * 7 - 5
+    want = pos.clone() + 3
+    csa.advance_positions(pos, 3)
+    csa.advance_positions(pos[:0], 9)
+    torch.cuda.synchronize()
+    assert torch.equal(pos, want)
+
+
 def test_host_validation_raises():
     import deepseek_v4_compressed_csa_gb300 as csa
     cfg = csa_synth.CONFIGS[2].replace(B=1)
