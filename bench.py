@@ -216,6 +216,8 @@ class DecodeWorkload:
         u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=device)  # noqa: E731
         self.ws_c = u8(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, cap))
         self.ws_c2 = u8(csa.workspace_size(self.L, csa.OP_COMPRESS, B, 1, cap))  # the concurrent second call
+        self.pair = cfg.has_indexer  # both pools through csa_compress_append_pair
+        self.ws_pair = u8(csa.workspace_size(self.L, csa.OP_COMPRESS_PAIR, B, 1, cap)) if self.pair else None
         self.side = torch.cuda.Stream(device)
         self.side2 = torch.cuda.Stream(device)
         self.pool_ready = torch.cuda.Event()
@@ -232,13 +234,22 @@ class DecodeWorkload:
         return h
 
     def front(self, inp):
-        """Phase 1: the attention pool's compress call on a side stream; on the main stream the index pool's
-        compress call and then the indexer (or, with overlapped_indexer, the index pool's call on a second side
-        stream and csa_index_topk_overlapped beside it, its selection waiting for that call's event).  Each
-        concurrent call has its own workspace."""
+        """Phase 1: both pools' compress call (csa_compress_append_pair) and the indexer on one stream; with
+        pair off, the attention pool's compress call on a side stream and, on the main stream, the index pool's
+        call and the indexer (or, with overlapped_indexer, the index pool's call on a second side stream and
+        csa_index_topk_overlapped beside it, its selection waiting for that call's event).  Each concurrent
+        call has its own workspace."""
         import torch
         csa = self.csa
         main = torch.cuda.current_stream()
+        if self.cfg.has_indexer and self.serial_indexer and self.pair:
+            # both pools in one call (one projection grid, one pooling launch), then the indexer: one stream, so
+            # every kernel of the step follows its predecessor by programmatic launch
+            csa.compress_append_pair(self.L, self.ca, self.ci, inp["x"], self.pos, self.front_a, self.pool, self.n_a,
+                                     self.front_i, self.ikeys, self.n_i, self.invf, ws=self.ws_pair, err=self.err)
+            csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
+                           self.n_sel, ws=self.ws_i, err=self.err)
+            return
         self.side.wait_stream(main)
         with torch.cuda.stream(self.side):
             csa.compress_append(self.L, self.ca, inp["x"], self.pos, self.front_a, self.pool, self.n_a, self.invf,
@@ -335,6 +346,7 @@ def run_ours(args):
     total_steps = args.warmup + args.steps + args.e2e_steps + 4
     cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
     wl = DecodeWorkload(cfg, cap, n_inputs=8, device=dev, serial_indexer=not args.overlapped_indexer)
+    wl.pair = wl.pair and not args.two_streams
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -554,6 +566,8 @@ def main():
     ap.add_argument("--prefill-repeats", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
+    ap.add_argument("--two-streams", action="store_true",
+                    help="the two compress calls separately, the attention pool's on a side stream")
     ap.add_argument("--overlapped-indexer", action="store_true",
                     help="run csa_index_topk_overlapped beside the index pool's compress call instead of "
                          "csa_index_topk after it on one stream")

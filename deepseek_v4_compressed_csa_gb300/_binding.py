@@ -17,13 +17,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libcsa.so")
 
 CSA_F32, CSA_BF16 = 0, 1
-OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL = 0, 1, 2, 3
+OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL, OP_COMPRESS_PAIR = 0, 1, 2, 3, 4
 DEV_CAPACITY, DEV_STATE, DEV_RANGE = 1, 2, 4
 CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
-           "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions")
+           "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions",
+           "csa_compress_append_pair")
 
 
 class CSAError(RuntimeError):
@@ -80,6 +81,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_attend_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, i32, ctypes.c_int32, vp, vp, vp, i32, vp, vp,
                                              vp, vp, vp, sz, vp, vp]
     lib.csa_attend_prefill_chunk.restype = i32
+    lib.csa_compress_append_pair.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp,
+                                             sz, vp, vp]
+    lib.csa_compress_append_pair.restype = i32
     lib.csa_advance_positions.argtypes = [vp, i32, i32, vp]
     lib.csa_advance_positions.restype = i32
     _lib = lib
@@ -195,6 +199,21 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
     _check("csa_compress_append", load_library().csa_compress_append(
         ctypes.byref(L), ctypes.byref(C), _ptr(x), B, T, _ptr(pos), _ptr(frontier), _ptr(pool), cap, _ptr(n_rows),
         _ptr(inv_freq), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def compress_append_pair(layer: Layer, comp_a: Compressor, comp_i: Compressor, x, pos, frontier_a, pool_a, n_rows_a,
+                         frontier_i, pool_i, n_rows_i, inv_freq, ws=None, err=None, stream=None):
+    """csa_compress_append_pair (attention pool, then index pool, same tokens); returns the error word tensor."""
+    B, T = x.shape[0], x.shape[1]
+    cap_a, cap_i = pool_a.shape[1], pool_i.shape[1]
+    ws, nb = _ws(layer, OP_COMPRESS_PAIR, B, T, max(cap_a, cap_i), ws, x.device)
+    err = _err(err, x.device)
+    L, Ca, Ci = layer._c(), comp_a._c(), comp_i._c()
+    _check("csa_compress_append_pair", load_library().csa_compress_append_pair(
+        ctypes.byref(L), ctypes.byref(Ca), ctypes.byref(Ci), _ptr(x), B, T, _ptr(pos), _ptr(frontier_a),
+        _ptr(pool_a), cap_a, _ptr(n_rows_a), _ptr(frontier_i), _ptr(pool_i), cap_i, _ptr(n_rows_i), _ptr(inv_freq),
+        _ptr(ws), nb, _ptr(err), _stream(stream)))
     return err
 
 

@@ -46,6 +46,12 @@ size_t ws_compress(const Dims& L, int d, int B, int T) {
   carve_compress(c, L, d, B, T);
   return c.off;
 }
+size_t ws_compress_pair(const Dims& L, int B, int T) {
+  Carver c(nullptr);
+  carve_compress(c, L, L.D, B, T);
+  carve_compress(c, L, L.Di, B, T);
+  return c.off;
+}
 size_t ws_index(const Dims& L, int B, int cap) {
   Carver c(nullptr);
   carve_index(c, L, B, cap);
@@ -107,6 +113,10 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
         if (bi > *bytes) *bytes = bi;
       }
       return CSA_OK;
+    case CSA_OP_COMPRESS_PAIR:
+      if (T < 1 || !L.has_indexer()) return CSA_ERR_ARG;
+      *bytes = ws_compress_pair(L, B, T);
+      return CSA_OK;
     case CSA_OP_INDEX_TOPK:
       *bytes = ws_index(L, B, cap);
       return CSA_OK;
@@ -121,24 +131,54 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
   return CSA_ERR_ARG;
 }
 
+// Argument checks shared by the one-pool and two-pool compress calls.
+static bool compress_args_ok(const Dims& L, const csa_compressor* comp, int B, int T, int cap, const void* frontier,
+                             const void* pool, const int32_t* n_rows) {
+  if (!comp || B < 1 || T < 1 || cap < 1) return false;
+  if (comp->d < L.R || comp->d % 8 || (comp->d != L.D && comp->d != L.Di)) return false;
+  if (!dev_tensor(comp->wkv) || !dev_tensor(comp->wgate) || !dev_tensor(comp->ape) || !dev_tensor(comp->norm_w))
+    return false;
+  return dev_tensor(frontier) && dev_tensor(pool) && dev_i32(n_rows);
+}
+
 csa_status csa_compress_append(const csa_layer* layer, const csa_compressor* comp, const void* x, int B, int T,
                                const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                                const float* inv_freq, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
-  if (!comp || B < 1 || T < 1 || cap < 1) return CSA_ERR_ARG;
-  if (comp->d < L.R || comp->d % 8 || (comp->d != L.D && comp->d != L.Di)) return CSA_ERR_ARG;
-  if (!dev_tensor(comp->wkv) || !dev_tensor(comp->wgate) || !dev_tensor(comp->ape) || !dev_tensor(comp->norm_w))
-    return CSA_ERR_ARG;
-  if (!dev_tensor(x) || !dev_tensor(frontier) || !dev_tensor(pool) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
-  if (!dev_i32(pos) || !dev_i32(n_rows) || !dev_i32(err)) return CSA_ERR_ARG;
+  if (!compress_args_ok(L, comp, B, T, cap, frontier, pool, n_rows)) return CSA_ERR_ARG;
+  if (!dev_tensor(x) || !dev_tensor(inv_freq) || !dev_i32(pos) || !dev_i32(err)) return CSA_ERR_ARG;
   const size_t need = ws_compress(L, comp->d, B, T);
   if (ws_bytes < need || (need && !dev_tensor(ws))) return CSA_ERR_WORKSPACE;
   Carver c(ws);
   CompressWs w = carve_compress(c, L, comp->d, B, T);
   return cuda_status(launch_compress(L, *comp, x, B, T, pos, frontier, pool, cap, n_rows, inv_freq, w, err,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_append_pair(const csa_layer* layer, const csa_compressor* comp_a,
+                                    const csa_compressor* comp_i, const void* x, int B, int T, const int32_t* pos,
+                                    void* frontier_a, void* pool_a, int cap_a, int32_t* n_rows_a, void* frontier_i,
+                                    void* pool_i, int cap_i, int32_t* n_rows_i, const float* inv_freq, void* ws,
+                                    size_t ws_bytes, int32_t* err, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
+  if (!compress_args_ok(L, comp_a, B, T, cap_a, frontier_a, pool_a, n_rows_a) ||
+      !compress_args_ok(L, comp_i, B, T, cap_i, frontier_i, pool_i, n_rows_i))
+    return CSA_ERR_ARG;
+  if (comp_a->d != L.D || comp_i->d != L.Di) return CSA_ERR_ARG;
+  if (!dev_tensor(x) || !dev_tensor(inv_freq) || !dev_i32(pos) || !dev_i32(err)) return CSA_ERR_ARG;
+  const size_t need = ws_compress_pair(L, B, T);
+  if (ws_bytes < need || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  const CompressWs wa = carve_compress(c, L, L.D, B, T);
+  const CompressWs wi = carve_compress(c, L, L.Di, B, T);
+  return cuda_status(launch_compress_pair(L, *comp_a, *comp_i, x, B, T, pos, frontier_a, pool_a, cap_a, n_rows_a,
+                                          frontier_i, pool_i, cap_i, n_rows_i, inv_freq, wa, wi, err,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_index_topk(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys, int cap,

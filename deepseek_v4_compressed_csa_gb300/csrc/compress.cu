@@ -236,16 +236,37 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
 // that completes a window has p = 3 mod 4, so its window covers tokens p-7 .. p in a fixed lane / APE order).
 constexpr int kTokChans = 2;  // channels per thread: d <= 512
 
+// One pool's side of a single-token pooling launch.
 template <typename T>
-__global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ flags, const int32_t* __restrict__ pos,
-                                                         int32_t* __restrict__ n_rows, int32_t* err, int d, int R,
-                                                         int F, T* __restrict__ frontier,
-                                                         const float* __restrict__ ape,
-                                                         const float* __restrict__ norm_w, float eps,
-                                                         const float* __restrict__ inv_freq, T* __restrict__ pool,
-                                                         int cap, const float* __restrict__ part, int splits,
-                                                         int part_stride) {
+struct TokPool {
+  int32_t* flags;
+  int32_t* n_rows;
+  T* frontier;
+  const float* ape;
+  const float* norm_w;
+  T* pool;
+  const float* part;
+  int d, cap, splits, part_stride;
+};
+
+// Blocks [0, B) serve pool pa, blocks [B, 2B) (when launched) pool pb: a ratio-4 layer's two pools of the same
+// tokens in one launch.
+template <typename T>
+__global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<T> pb, int B,
+                                                         const int32_t* __restrict__ pos, int32_t* err, int R, int F,
+                                                         float eps, const float* __restrict__ inv_freq) {
   pdl_trigger();
+  // this block's pool, field by field (a reference to one of the two parameters would move them to local memory)
+  const bool second = blockIdx.x >= (unsigned)B;
+  int32_t* __restrict__ flags = second ? pb.flags : pa.flags;
+  int32_t* __restrict__ n_rows = second ? pb.n_rows : pa.n_rows;
+  T* __restrict__ frontier = second ? pb.frontier : pa.frontier;
+  const float* __restrict__ ape = second ? pb.ape : pa.ape;
+  const float* __restrict__ norm_w = second ? pb.norm_w : pa.norm_w;
+  T* __restrict__ pool = second ? pb.pool : pa.pool;
+  const float* __restrict__ part = second ? pb.part : pa.part;
+  const int d = second ? pb.d : pa.d, cap = second ? pb.cap : pa.cap;
+  const int splits = second ? pb.splits : pa.splits, part_stride = second ? pb.part_stride : pa.part_stride;
   constexpr int ratio = 4, lanes = 2, kEnt = ratio * lanes;
   extern __shared__ float sm_tok[];  // [2*L*d] the new token, [d] pooled, [d] normed, 32 reduction slots, [R] rope
   const int Ld = lanes * d, rowlen = 2 * Ld;
@@ -255,7 +276,7 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(int32_t* __restrict__ f
   float* red = y + d;
   float* rc = red + 32;
   float* rs = rc + R / 2;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int b = blockIdx.x - (second ? B : 0), tid = threadIdx.x;
   // before the preceding kernel has completed: the position (a step input) and the layer's constants, which no
   // kernel writes
   const int p0 = pos[b];
@@ -444,9 +465,9 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   }
   if (part && L.ratio == 4 && L.lanes == 2 && L.F == 8 && d <= 256 * kTokChans) {
     const size_t smem = ((size_t)rowlen + 2 * (size_t)d + 32 + L.R) * sizeof(float);
-    CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(256), smem, s, ws.flags, pos, n_rows, err, d, L.R, L.F,
-               static_cast<T*>(frontier), comp.ape, comp.norm_w, L.eps, inv_freq, static_cast<T*>(pool), cap,
-               part, splits, part_stride);
+    const TokPool<T> tp{ws.flags, n_rows, static_cast<T*>(frontier), comp.ape, comp.norm_w, static_cast<T*>(pool),
+                        part, d, cap, splits, part_stride};
+    CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(256), smem, s, tp, tp, B, pos, err, L.R, L.F, L.eps, inv_freq);
     return cudaGetLastError();
   }
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
@@ -461,6 +482,43 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
                                             static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows);
   }
   return cudaGetLastError();
+}
+
+// Both pools of a ratio-4 layer.  One token per sequence on the tensor-core path: the two projections as one
+// grid and the two pooling steps as one launch; otherwise the two calls in turn.
+static cudaError_t compress_pair_token(const Dims& L, const csa_compressor& ca, const csa_compressor& ci,
+                                       const void* x, int B, const int32_t* pos, void* fa, void* pa, int cap_a,
+                                       int32_t* na, void* fi, void* pi, int cap_i, int32_t* ni,
+                                       const float* inv_freq, const CompressWs& wa, const CompressWs& wi,
+                                       int32_t* err, cudaStream_t s, int sa, int si) {
+  using T = __nv_bfloat16;
+  cudaError_t e = launch_tc_project_pair(L, ca.d, ca.wkv, ca.wgate, wa.part, ci.d, ci.wkv, ci.wgate, wi.part, x, B,
+                                         sa, si, err, s);
+  if (e != cudaSuccess) return e;
+  const TokPool<T> ta{wa.flags, na, static_cast<T*>(fa), ca.ape, ca.norm_w, static_cast<T*>(pa), wa.part, ca.d,
+                      cap_a, sa, tc_project_cols(L, ca.d, B)};
+  const TokPool<T> tb{wi.flags, ni, static_cast<T*>(fi), ci.ape, ci.norm_w, static_cast<T*>(pi), wi.part, ci.d,
+                      cap_i, si, tc_project_cols(L, ci.d, B)};
+  const int dm = max(ca.d, ci.d);
+  const size_t smem = ((size_t)2 * L.lanes * dm + 2 * (size_t)dm + 32 + L.R) * sizeof(float);
+  CSA_LAUNCH(k_pool_emit_token<T>, dim3(2 * B), dim3(256), smem, s, ta, tb, B, pos, err, L.R, L.F, L.eps, inv_freq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const csa_compressor& ci, const void* x,
+                                 int B, int T, const int32_t* pos, void* fa, void* pa, int cap_a, int32_t* na,
+                                 void* fi, void* pi, int cap_i, int32_t* ni, const float* inv_freq,
+                                 const CompressWs& wa, const CompressWs& wi, int32_t* err, cudaStream_t s) {
+  int sa = 0, si = 0;
+  const bool token = T == 1 && L.dtype == CSA_BF16 && L.ratio == 4 && L.lanes == 2 && L.F == 8 && ca.d <= 512 &&
+                     ci.d <= 512 && tc_project_supported(L, ca.d) && tc_project_supported(L, ci.d) && wa.part &&
+                     wi.part && plan_project_pair(L, ca.d, ci.d, B, &sa, &si);
+  if (token)
+    return compress_pair_token(L, ca, ci, x, B, pos, fa, pa, cap_a, na, fi, pi, cap_i, ni, inv_freq, wa, wi, err, s,
+                               sa, si);
+  cudaError_t e = launch_compress(L, ca, x, B, T, pos, fa, pa, cap_a, na, inv_freq, wa, err, s);
+  if (e != cudaSuccess) return e;
+  return launch_compress(L, ci, x, B, T, pos, fi, pi, cap_i, ni, inv_freq, wi, err, s);
 }
 
 cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,

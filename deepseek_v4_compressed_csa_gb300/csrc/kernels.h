@@ -68,6 +68,11 @@ struct CompressWs {
   int* tickets;    // tensor-core projection: per-tile arrival counters (or null)
 };
 CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T);
+// The attention pool (ca, workspace wa) and the index pool (ci, wi) of one call's tokens.
+cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const csa_compressor& ci, const void* x,
+                                 int B, int T, const int32_t* pos, void* fa, void* pa, int cap_a, int32_t* na,
+                                 void* fi, void* pi, int cap_i, int32_t* ni, const float* inv_freq,
+                                 const CompressWs& wa, const CompressWs& wi, int32_t* err, cudaStream_t s);
 cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,
                             const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                             const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s);
@@ -103,6 +108,12 @@ int tc_project_cols(const Dims& L, int d, int ntok);
 // fixup = false (splits > 1): the fp32 partials [splits, ntok (padded), 2*L*d] are left for the consumer.
 cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,
                               void* proj, float* part, int* tickets, bool fixup, int32_t* err, cudaStream_t s);
+// The index pool's and the attention pool's single-token projections as one grid (partials only; the pooling
+// kernel sums them).  plan_project_pair picks the split counts (false: use two launches).
+bool plan_project_pair(const Dims& L, int d0, int d1, int ntok, int* s0, int* s1);
+cudaError_t launch_tc_project_pair(const Dims& L, int d0, const void* wkv0, const void* wg0, float* part0, int d1,
+                                   const void* wkv1, const void* wg1, float* part1, const void* x, int ntok, int s0,
+                                   int s1, int32_t* err, cudaStream_t s);
 
 // ---- tc_indexer.cu (tensor-core scores; bf16, Hi = 64, Di = 128)
 bool tc_index_supported(const Dims& L);

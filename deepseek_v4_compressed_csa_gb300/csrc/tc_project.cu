@@ -32,20 +32,17 @@ struct PjArgs {
   int32_t* err;
 };
 
-__global__ void __launch_bounds__(kPThreads, 1)
-    k_tc_project(const __grid_constant__ CUtensorMap tm_wkv, const __grid_constant__ CUtensorMap tm_wg,
-                 const __grid_constant__ CUtensorMap tm_x, PjArgs a, int stages) {
-  pdl_trigger();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// One (feature tile m, token tile n, split) of one projection: TMA ring, MMA, epilogue to proj or partials.
+// Returns after the CTA's TMEM is released.
+__device__ __forceinline__ void project_tile(const CUtensorMap* tm_wkv, const CUtensorMap* tm_wg,
+                                             const CUtensorMap* tm_x, const PjArgs& a, int m, int n, int split,
+                                             int stages, uint8_t* smem) {
   const int N = a.N;
   const int stage_bytes = kABytes + N * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   uint64_t* empty = full + stages;
   uint64_t* acc_full = empty + stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  int* s_last = reinterpret_cast<int*>(tmem_slot + 1);
-  const int m = blockIdx.x, n = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tcols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
 
@@ -71,10 +68,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const CUtensorMap* wmap = (m * 128 < a.Ld) ? &tm_wkv : &tm_wg;
+      const CUtensorMap* wmap = (m * 128 < a.Ld) ? tm_wkv : tm_wg;
       const int wrow = (m * 128 < a.Ld) ? m * 128 : m * 128 - a.Ld;
       tc::tma_prefetch(wmap);
-      tc::tma_prefetch(&tm_x);
+      tc::tma_prefetch(tm_x);
       int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int kb = 0; kb < a.n_kblk; ++kb) {
         const int s = kb % stages;
@@ -83,7 +80,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint8_t* st = smem + s * stage_bytes;
         tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
         tc::tma_load_2d(st, wmap, &full[s], (k0 + kb) * 64, wrow);
-        tc::tma_load_2d(st + kABytes, &tm_x, &full[s], (k0 + kb) * 64, n * N);
+        tc::tma_load_2d(st + kABytes, tm_x, &full[s], (k0 + kb) * 64, n * N);
         ++issued[s];
       }
       for (int s = 0; s < stages; ++s)
@@ -133,7 +130,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, tcols);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_tc_project(const __grid_constant__ CUtensorMap tm_wkv, const __grid_constant__ CUtensorMap tm_wg,
+                 const __grid_constant__ CUtensorMap tm_x, PjArgs a, int stages) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int m = blockIdx.x, n = blockIdx.y;
+  project_tile(&tm_wkv, &tm_wg, &tm_x, a, m, n, blockIdx.z, stages, smem);
   if (a.splits == 1 || !a.fixup) return;
+  int* s_last = reinterpret_cast<int*>(smem + stages * (kABytes + a.N * 128) + (2 * stages + 1) * 8 + 4);
+  const int N = a.N;
   // split-K fix-up: the last CTA of the tile sums every split's partials in split order
   __threadfence();
   __syncthreads();
@@ -175,6 +184,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
+// The two projections of one token per sequence (attention pool and index pool, one token tile) in one grid:
+// blocks [0, tiles0) are problem 0 (block = split * m_tiles0 + m), the rest problem 1.  Partials only: the pooling
+// kernel sums them.
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_tc_project_pair(const __grid_constant__ CUtensorMap tm_wkv0, const __grid_constant__ CUtensorMap tm_wg0,
+                      const __grid_constant__ CUtensorMap tm_wkv1, const __grid_constant__ CUtensorMap tm_wg1,
+                      const __grid_constant__ CUtensorMap tm_x, PjArgs a0, PjArgs a1, int m_tiles0, int m_tiles1,
+                      int stages) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tiles0 = m_tiles0 * a0.splits;
+  const int bx = blockIdx.x;
+  if (bx < tiles0)
+    project_tile(&tm_wkv0, &tm_wg0, &tm_x, a0, bx % m_tiles0, 0, bx / m_tiles0, stages, smem);
+  else
+    project_tile(&tm_wkv1, &tm_wg1, &tm_x, a1, (bx - tiles0) % m_tiles1, 0, (bx - tiles0) / m_tiles1, stages, smem);
+}
+
 struct PjPlan {
   int N, n_tiles, m_tiles, splits;
 };
@@ -213,6 +241,56 @@ int tc_project_splits(const Dims& L, int d, int ntok) { return plan_project(L, d
 int tc_project_cols(const Dims& L, int d, int ntok) {
   const PjPlan p = plan_project(L, d, ntok);
   return p.n_tiles * p.N;
+}
+
+// Split counts for the two single-token projections run as one grid: powers of two no larger than each one's own
+// plan (its workspace holds that many partials), at most one CTA per SM in total, the largest per-CTA weight
+// share as small as possible.  False when the pair does not fit one wave even unsplit, or has more than one
+// token tile.
+bool plan_project_pair(const Dims& L, int d0, int d1, int ntok, int* s0, int* s1) {
+  const PjPlan p0 = plan_project(L, d0, ntok), p1 = plan_project(L, d1, ntok);
+  if (p0.n_tiles != 1 || p1.n_tiles != 1) return false;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long best = -1;
+  for (int a = 1; a <= p0.splits; a *= 2)
+    for (int b = 1; b <= p1.splits; b *= 2) {
+      if (p0.m_tiles * a + p1.m_tiles * b > sms) continue;
+      const long share = max((long)L.X / a, (long)L.X / b);  // K per CTA of the heavier problem
+      if (best < 0 || share < best || (share == best && a * p0.m_tiles + b * p1.m_tiles > *s0 * p0.m_tiles + *s1 * p1.m_tiles)) {
+        best = share;
+        *s0 = a;
+        *s1 = b;
+      }
+    }
+  return best >= 0;
+}
+
+cudaError_t launch_tc_project_pair(const Dims& L, int d0, const void* wkv0, const void* wg0, float* part0, int d1,
+                                   const void* wkv1, const void* wg1, float* part1, const void* x, int ntok, int s0,
+                                   int s1, int32_t* err, cudaStream_t s) {
+  const PjPlan p0 = plan_project(L, d0, ntok), p1 = plan_project(L, d1, ntok);
+  const int Ld0 = L.lanes * d0, Ld1 = L.lanes * d1;
+  CUtensorMap tw0, tg0, tw1, tg1, tx;
+  if (!make_tmap_2d_bf16(&tw0, wkv0, Ld0, L.X, (uint64_t)L.X * 2, 128) ||
+      !make_tmap_2d_bf16(&tg0, wg0, Ld0, L.X, (uint64_t)L.X * 2, 128) ||
+      !make_tmap_2d_bf16(&tw1, wkv1, Ld1, L.X, (uint64_t)L.X * 2, 128) ||
+      !make_tmap_2d_bf16(&tg1, wg1, Ld1, L.X, (uint64_t)L.X * 2, 128) ||
+      !make_tmap_2d_bf16(&tx, x, ntok, L.X, (uint64_t)L.X * 2, p0.N))
+    return cudaErrorInvalidValue;
+  PjArgs a0{}, a1{};
+  a0.ntok = ntok; a0.X = L.X; a0.Ld = Ld0; a0.N = p0.N; a0.splits = s0; a0.n_kblk = L.X / 64 / s0;
+  a0.part = part0; a0.n_cols = p0.N; a0.fixup = 0; a0.err = err;
+  a1 = a0;
+  a1.Ld = Ld1; a1.splits = s1; a1.n_kblk = L.X / 64 / s1; a1.part = part1;
+  const int stage_bytes = kABytes + p0.N * 128;
+  const int stages = min(8, min(min(a0.n_kblk, a1.n_kblk), (200 * 1024) / stage_bytes));
+  const size_t smem = 1024 + (size_t)stages * stage_bytes + 256;
+  cudaFuncSetAttribute(k_tc_project_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  CSA_LAUNCH(k_tc_project_pair, dim3(p0.m_tiles * s0 + p1.m_tiles * s1), dim3(kPThreads), smem, s, tw0, tg0, tw1,
+             tg1, tx, a0, a1, p0.m_tiles, p1.m_tiles, stages);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_project(const Dims& L, int d, const void* x, int ntok, const void* wkv, const void* wgate,

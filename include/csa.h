@@ -70,7 +70,13 @@ enum {
 };
 
 /* operation ids for csa_workspace_size */
-enum { CSA_OP_COMPRESS = 0, CSA_OP_INDEX_TOPK = 1, CSA_OP_ATTEND_DECODE = 2, CSA_OP_ATTEND_PREFILL = 3 };
+enum {
+  CSA_OP_COMPRESS = 0,
+  CSA_OP_INDEX_TOPK = 1,
+  CSA_OP_ATTEND_DECODE = 2,
+  CSA_OP_ATTEND_PREFILL = 3,
+  CSA_OP_COMPRESS_PAIR = 4 /* csa_compress_append_pair (ratio-4 layers) */
+};
 
 /* One CSA layer.
  *   H query heads over one latent of D dims (K = V), rope on the last R dims;
@@ -142,6 +148,26 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
 csa_status csa_compress_append(const csa_layer* layer, const csa_compressor* comp, const void* x, int B, int T,
                                const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                                const float* inv_freq, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/* csa_compress_append_pair — both compressed pools of a ratio-4 layer (the
+ * attention pool, comp_a with d = D, and the index pool, comp_i with d = Di) for
+ * the same T tokens per sequence: the arguments, errors and definition of
+ * csa_compress_append for the attention pool and then for the index pool, with
+ * each pool's own frontier, pool, cap and n_rows, and one shared x, pos,
+ * inv_freq and error word.  Results are those two calls' (identical for T > 1;
+ * for one token the projections' fp32 sums may be split differently along the
+ * hidden axis, within the projection's own rounding).  The pages compress both pools from the same hidden
+ * states at the same positions ([MTPLX#216] "What V4 adds": the indexer keeps
+ * its own compressed keys beside the attention pool).  Workspace:
+ * CSA_OP_COMPRESS_PAIR.  With one token per sequence (decode) the two
+ * projections run as one kernel and the two pooling steps as one, so that
+ * neither call waits behind the other; longer chunks run the two calls in turn.
+ * CSA_ERR_UNSUPPORTED on layers without an indexer (ratio != 4). */
+csa_status csa_compress_append_pair(const csa_layer* layer, const csa_compressor* comp_a,
+                                    const csa_compressor* comp_i, const void* x, int B, int T, const int32_t* pos,
+                                    void* frontier_a, void* pool_a, int cap_a, int32_t* n_rows_a, void* frontier_i,
+                                    void* pool_i, int cap_i, int32_t* n_rows_i, const float* inv_freq, void* ws,
+                                    size_t ws_bytes, int32_t* err, void* stream);
 
 /* csa_index_topk — the indexer for one decode query per sequence.
  *

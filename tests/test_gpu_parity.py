@@ -422,6 +422,86 @@ def test_device_errors_fail_closed():
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("B,ctx,steps", [(8, 8192 + 1, 6), (32, 32768 + 2, 4)])
+def test_compress_pair_single_tokens_against_oracle(B, ctx, steps):
+    """csa_compress_append_pair, one token per sequence (both projections in one grid, both pooling steps in
+    one launch), across window completions: each pool's projections and emitted rows against the oracle on
+    sampled sequences (the same rules as the single call); a sequence with an inconsistent row count is refused
+    and left unchanged."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=B, ctx=ctx)
+    cap = (ctx + steps) // 4 + 8
+    host = csa_synth.synth_cache(cfg, cap, B=B)
+    run = G.Runner(cfg)
+    st = G.DevCache(host)
+    st.n_rows[B - 1] -= 3  # state error for the last sequence (its positions only grow: it stays inconsistent)
+    ni = st.n_rows.clone()
+    bad_before = (st.pool[B - 1].clone(), st.ikeys[B - 1].clone(), st.front_attn[B - 1].clone())
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    seqs = [0, B // 2, B - 2]
+    full = oracle_state(host)
+    st_o = {b: {k: None if v is None else v[b:b + 1].copy() for k, v in full.items()} for b in seqs}
+    del full
+    F = st.front_attn.shape[1]
+    for step in range(steps):
+        x = csa_synth.hidden(cfg, 1, B=B, tag=100 + step)
+        slots = st.pos.long() % F
+        csa.compress_append_pair(run.L, run.ca, run.ci, G.dev(x), st.pos, st.front_attn, st.pool, st.n_rows,
+                                 st.front_index, st.ikeys, ni, run.inv_freq, err=run.err)
+        torch.cuda.synchronize()
+        for b in seqs:
+            o = st_o[b]
+            xb = f64(x[b:b + 1])
+            n0 = o["n_rows"].copy()
+            pa = st.front_attn[b, slots[b]].view(1, 1, -1).cpu()
+            pi = st.front_index[b, slots[b]].view(1, 1, -1).cpu()
+            o["front_a"], o["pool"], n_a, e1 = G.oracle_compress_checked(layer, ca, xb, o["pos"], o["front_a"], o["pool"],
+                                                                         n0, invf, pa, f"seq {b} step {step} attn")
+            o["front_i"], o["ikeys"], n_i, e2 = G.oracle_compress_checked(layer, ci, xb, o["pos"], o["front_i"],
+                                                                          o["ikeys"], n0, invf, pi,
+                                                                          f"seq {b} step {step} index")
+            assert e1 == 0 and e2 == 0
+            o["n_rows"], o["pos"] = n_a, o["pos"] + 1
+        st.pos += 1
+    assert run.err.item() == csa.DEV_STATE
+    assert torch.equal(st.n_rows, ni)
+    for b in seqs:
+        o = st_o[b]
+        n = int(o["n_rows"][0])
+        assert n == st.n_rows[b].item()
+        lo = ctx // cfg.ratio
+        G.check_pool_rows(st.pool[b, lo:n].cpu(), o["pool"][0, lo:n], "bf16", f"seq {b} pool rows", R=cfg.R)
+        G.check_pool_rows(st.ikeys[b, lo:n].cpu(), o["ikeys"][0, lo:n], "bf16", f"seq {b} index rows", R=cfg.R)
+    assert torch.equal(st.pool[B - 1], bad_before[0]) and torch.equal(st.ikeys[B - 1], bad_before[1])
+    assert torch.equal(st.front_attn[B - 1], bad_before[2])
+    assert st.n_rows[B - 1].item() == host.n_rows[B - 1].item() - 3
+
+
+def test_compress_pair_chunk_equals_two_calls():
+    """A chunk (T > 1) through csa_compress_append_pair is the two single calls in turn: identical results."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    B, ctx, T = 3, 4096 + 3, 6
+    cfg = csa_synth.CONFIGS[3].replace(B=B, ctx=ctx)
+    host = csa_synth.synth_cache(cfg, (ctx + T) // 4 + 8, B=B)
+    run = G.Runner(cfg)
+    one, two = G.DevCache(host), G.DevCache(host)
+    ni_one, ni_two = one.n_rows.clone(), two.n_rows.clone()
+    x = G.dev(csa_synth.hidden(cfg, T, B=B, tag=7))
+    e1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa.compress_append(run.L, run.ca, x, one.pos, one.front_attn, one.pool, one.n_rows, run.inv_freq, err=e1)
+    csa.compress_append(run.L, run.ci, x, one.pos, one.front_index, one.ikeys, ni_one, run.inv_freq, err=e1)
+    csa.compress_append_pair(run.L, run.ca, run.ci, x, two.pos, two.front_attn, two.pool, two.n_rows,
+                             two.front_index, two.ikeys, ni_two, run.inv_freq, err=e2)
+    torch.cuda.synchronize()
+    assert e1.item() == e2.item() == 0
+    assert torch.equal(one.pool, two.pool) and torch.equal(one.ikeys, two.ikeys)
+    assert torch.equal(one.front_attn, two.front_attn) and torch.equal(one.front_index, two.front_index)
+    assert torch.equal(one.n_rows, two.n_rows) and torch.equal(ni_one, ni_two)
+
+
 def test_advance_positions():
     """csa_advance_positions adds `by` to every position (more sequences than one block holds), and leaves the
     array alone for B = 0."""
