@@ -243,10 +243,21 @@ int tc_project_cols(const Dims& L, int d, int ntok) {
   return p.n_tiles * p.N;
 }
 
+// The pair's CTAs run two per SM (their TMA rings sized to fit), so that both weight streams are in flight at
+// once.  Measured on GB300 for the Flash shapes (B = 32): two CTAs per SM with a 5-stage ring took the decode
+// step from 12.6k to 12.8k layer-steps/s against one CTA per SM with 8 stages.
+constexpr int kPairCtasPerSm = 2;
+
+int pair_stages(int N, int n_kblk_min) {
+  const int stage_bytes = kABytes + N * 128;
+  const int budget = 233472 / kPairCtasPerSm - 1024 - 1024 - 256;  // per-SM shared memory, reserve, slack
+  return max(1, min(8, min(n_kblk_min, budget / stage_bytes)));
+}
+
 // Split counts for the two single-token projections run as one grid: powers of two no larger than each one's own
-// plan (its workspace holds that many partials), at most one CTA per SM in total, the largest per-CTA weight
-// share as small as possible.  False when the pair does not fit one wave even unsplit, or has more than one
-// token tile.
+// plan (its workspace holds that many partials), at most kPairCtasPerSm CTAs per SM in total, the largest
+// per-CTA weight share as small as possible.  False when the pair does not fit one wave even unsplit, or has
+// more than one token tile.
 bool plan_project_pair(const Dims& L, int d0, int d1, int ntok, int* s0, int* s1) {
   const PjPlan p0 = plan_project(L, d0, ntok), p1 = plan_project(L, d1, ntok);
   if (p0.n_tiles != 1 || p1.n_tiles != 1) return false;
@@ -256,7 +267,7 @@ bool plan_project_pair(const Dims& L, int d0, int d1, int ntok, int* s0, int* s1
   long best = -1;
   for (int a = 1; a <= p0.splits; a *= 2)
     for (int b = 1; b <= p1.splits; b *= 2) {
-      if (p0.m_tiles * a + p1.m_tiles * b > sms) continue;
+      if (p0.m_tiles * a + p1.m_tiles * b > kPairCtasPerSm * sms) continue;
       const long share = max((long)L.X / a, (long)L.X / b);  // K per CTA of the heavier problem
       if (best < 0 || share < best || (share == best && a * p0.m_tiles + b * p1.m_tiles > *s0 * p0.m_tiles + *s1 * p1.m_tiles)) {
         best = share;
@@ -285,7 +296,7 @@ cudaError_t launch_tc_project_pair(const Dims& L, int d0, const void* wkv0, cons
   a1 = a0;
   a1.Ld = Ld1; a1.splits = s1; a1.n_kblk = L.X / 64 / s1; a1.part = part1;
   const int stage_bytes = kABytes + p0.N * 128;
-  const int stages = min(8, min(min(a0.n_kblk, a1.n_kblk), (200 * 1024) / stage_bytes));
+  const int stages = pair_stages(p0.N, min(a0.n_kblk, a1.n_kblk));
   const size_t smem = 1024 + (size_t)stages * stage_bytes + 256;
   cudaFuncSetAttribute(k_tc_project_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   CSA_LAUNCH(k_tc_project_pair, dim3(p0.m_tiles * s0 + p1.m_tiles * s1), dim3(kPThreads), smem, s, tw0, tg0, tw1,
