@@ -165,7 +165,11 @@ def _max_over_ranks(dist, value: float, device) -> float:
 class DecodeWorkload:
     """Config 3 state, weights and per-step inputs resident on one GPU."""
 
-    def __init__(self, cfg, cap: int, n_inputs: int, device, serial_indexer: bool = False):
+    def __init__(self, cfg, cap: int, n_inputs: int, device, serial_indexer: bool = False, host=None,
+                 host_comp=None, pos=None, input_tag: int = 0):
+        """host / host_comp: a synthetic cache and compressor weights generated once and copied here (several
+        layers hold copies in distinct device memory); pos: a position tensor shared with other layers;
+        input_tag: offset of this layer's per-step input sets."""
         import torch
 
         import csa_synth
@@ -181,15 +185,20 @@ class DecodeWorkload:
 
         def comp(c):
             return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
-        self.ca = comp(csa_synth.compressor(cfg, "attn"))
-        self.ci = comp(csa_synth.compressor(cfg, "index")) if cfg.has_indexer else None
-        host = csa_synth.synth_cache(cfg, cap)
+        if host_comp is None:
+            host_comp = (csa_synth.compressor(cfg, "attn"), csa_synth.compressor(cfg, "index") if cfg.has_indexer
+                         else None)
+        self.ca = comp(host_comp[0])
+        self.ci = comp(host_comp[1]) if cfg.has_indexer else None
+        if host is None:
+            host = csa_synth.synth_cache(cfg, cap)
         self.pool, self.ikeys, self.window = d(host.pool), d(host.ikeys), d(host.window)
         self.front_a, self.front_i = d(host.front_attn), d(host.front_index)
-        self.n_a, self.n_i, self.pos = d(host.n_rows), d(host.n_rows), d(host.pos)
+        self.n_a, self.n_i = d(host.n_rows), d(host.n_rows)
+        self.pos = d(host.pos) if pos is None else pos
         self.sink, self.invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
         B = cfg.B
-        self.host_inputs = [csa_synth.step_inputs(cfg, i) for i in range(n_inputs)]
+        self.host_inputs = [csa_synth.step_inputs(cfg, input_tag + i) for i in range(n_inputs)]
         # each input set lives in one packed device buffer (256-byte aligned fields), so that a step's inputs
         # can arrive from pinned host memory in a single copy
         names = ("x", "q", "kv", "iq", "iw")
@@ -273,12 +282,14 @@ class DecodeWorkload:
         if not (self.cfg.has_indexer and self.serial_indexer and self.join_before_index):
             main.wait_stream(self.side)
 
-    def attend(self, inp):
-        """Phase 2: attention over the selected rows and the window, merge; then the caller advances pos."""
+    def attend(self, inp, advance: bool = True):
+        """Phase 2: attention over the selected rows and the window, merge; then (advance) the positions move on
+        (in a model step that is done once, after the last layer)."""
         sel, n_sel = (self.sel, self.n_sel) if self.cfg.has_indexer else (None, None)
         self.csa.attend_decode(self.L, inp["q"], inp["kv"], self.sink, self.window, self.pool, self.n_a, sel, n_sel,
                                self.pos, self.invf, self.out, ws=self.ws_a, err=self.err)
-        self.csa.advance_positions(self.pos, 1)
+        if advance:
+            self.csa.advance_positions(self.pos, 1)
 
     def step(self, inp):
         self.front(inp)
@@ -320,6 +331,62 @@ class DecodeWorkload:
             ev[len(parts)].record()
 
 
+class ModelStep:
+    """One decode step of `n_layers` layers, as a model step runs them: each layer its own weights, caches, step
+    inputs and workspaces in distinct device memory (so every layer reads its data cold from HBM, as after the
+    other layers of a model), one shared position tensor advanced once after the last layer.  Each step is one
+    CUDA graph replay holding every layer."""
+
+    def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True):
+        import torch
+
+        import csa_synth
+        host = csa_synth.synth_cache(cfg, cap)
+        host_comp = (csa_synth.compressor(cfg, "attn"), csa_synth.compressor(cfg, "index"))
+        self.layers = []
+        pos = None
+        for i in range(n_layers):
+            wl = DecodeWorkload(cfg, cap, n_inputs, device, serial_indexer=True, host=host, host_comp=host_comp,
+                                pos=pos, input_tag=1000 * i)
+            wl.pair = wl.pair and pair
+            pos = wl.pos
+            self.layers.append(wl)
+        self.pos, self.csa, self.n_inputs = pos, self.layers[0].csa, n_inputs
+        self.graphs = None
+        self.torch = torch
+
+    def step(self, i):
+        for wl in self.layers:
+            inp = wl.inputs[i % self.n_inputs]
+            wl.front(inp)
+            wl.attend(inp, advance=False)
+        self.csa.advance_positions(self.pos, 1)
+
+    def capture(self):
+        torch = self.torch
+        self.graphs = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(self.n_inputs):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                    self.step(i)
+                self.graphs.append(g)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+    def replay(self, i, ev=None):
+        if ev is not None:
+            ev[0].record()
+        if self.graphs is None:
+            self.step(i)
+        else:
+            self.graphs[i % self.n_inputs].replay()
+        if ev is not None:
+            ev[1].record()
+
+
 def step_bytes(cfg, n_rows_mean: float) -> dict:
     """Algorithmic HBM bytes of one decode step (each byte the step must move once)."""
     B, e = cfg.B, 2
@@ -343,21 +410,23 @@ def run_ours(args):
     import deepseek_v4_compressed_csa_gb300 as csa
     csa.load_library()
     cfg = csa_synth.CONFIGS[3]
-    total_steps = args.warmup + args.steps + args.e2e_steps + 4
+    nl = args.layers
+    n_single = args.steps  # the one-layer comparison run (layer 0 alone, one graph per layer-step)
+    total_steps = args.warmup + args.steps + args.e2e_steps + 2 * (args.warmup + n_single) + 24
     cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
-    wl = DecodeWorkload(cfg, cap, n_inputs=8, device=dev, serial_indexer=not args.overlapped_indexer)
-    wl.pair = wl.pair and not args.two_streams
+    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, pair=not args.two_streams)
+    wl = ms.layers[0]
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    wl.step(wl.inputs[0])  # first calls outside capture (one-time host set-up inside the library)
+    ms.step(0)  # first calls outside capture (one-time host set-up inside the library)
     torch.cuda.synchronize()
     if args.eager:
-        wl.graphs = None  # same kernels launched one by one (for profilers that do not follow graphs)
+        ms.graphs = None  # same kernels launched one by one (for profilers that do not follow graphs)
     else:
-        wl.capture()  # capturing does not run anything: the graphs replay the steps below
+        ms.capture()  # capturing does not run anything: the graphs replay the steps below
     for i in range(args.warmup):
-        wl.replay(i)
+        ms.replay(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -366,31 +435,63 @@ def run_ours(args):
     ev = [(mk(), mk()) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
-    launches0 = csa.kernel_launches()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     for i in range(args.steps):
         flush.zero_()
-        wl.replay(args.warmup + i, ev=ev[i])
+        ms.replay(args.warmup + i, ev=ev[i])
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    total_ms = _max_over_ranks(dist, sum(step_ms), dev)
-    assert wl.err.item() == 0, f"device error word {wl.err.item()}"
+    total_ms = _max_over_ranks(dist, sum(e[0].elapsed_time(e[1]) for e in ev), dev)
+    for layer in ms.layers:
+        assert layer.err.item() == 0, f"device error word {layer.err.item()}"
     n_end = wl.n_a.float().mean().item()
-    # kernels per step: counted on one eager step (graph replays enqueue the same kernels)
+    # kernels per model step: counted on one eager step (graph replays enqueue the same kernels)
     k0 = csa.kernel_launches()
-    wl.step(wl.inputs[0])
+    ms.step(0)
     torch.cuda.synchronize()
     launches = (csa.kernel_launches() - k0) * args.steps
-    del launches0
 
-    # ---- diagnostic (not the headline): the same steps as two graphs, events between the phases
+    # ---- end to end: per model step, each layer's inputs from pinned host memory (one copy per layer, its five
+    # inputs packed as in its graph's input buffer), the step, the last layer's output back to pinned memory
+    pinned = [[layer.packed_host(i) for i in range(ms.n_inputs)] for layer in ms.layers]
+    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    h2d = wl.packed_bytes  # per layer-step: the bytes its one copy moves (fields plus alignment padding)
+    d2h = out_host.numel() * out_host.element_size()  # per model step (the last layer's output)
+    ev2 = [(mk(), mk()) for _ in range(args.e2e_steps)]
+    torch.cuda.synchronize()
+    for i in range(args.e2e_steps):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        k = i % ms.n_inputs
+        for layer, pin in zip(ms.layers, pinned):
+            layer.packed[k].copy_(pin[k], non_blocking=True)
+        ms.replay(k)
+        out_host.copy_(ms.layers[-1].out, non_blocking=True)
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev2), dev) / max(1, args.e2e_steps)
+
+    # ---- comparison (not the headline): layer 0 alone, one CUDA graph per layer-step (each step's graph
+    # launch latency falls on that one layer); then the per-phase diagnostic on the same layer.  These advance
+    # the shared positions for layer 0 only, so they run after every model step.
+    single = None
     phase_us = None
     if not args.eager:
+        wl.capture()
+        for i in range(args.warmup):
+            wl.replay(i)
+        ev1 = [(mk(), mk()) for _ in range(n_single)]
+        torch.cuda.synchronize()
+        for i in range(n_single):
+            flush.zero_()
+            wl.replay(i, ev=ev1[i])
+        torch.cuda.synchronize()
+        single_ms = sum(a.elapsed_time(b) for a, b in ev1) / n_single
+        single = {"layer_steps_per_s": round(1e3 / single_ms, 3), "ms_per_layer_step": round(single_ms, 5)}
         wl.capture(per_phase=True)
         n_diag = min(args.steps, 16)
         evd = [(mk(), mk(), mk()) for _ in range(n_diag)]
@@ -403,26 +504,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         phase_us = {name: round(1e3 * statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evd), 2)
                     for k, name in enumerate(("compress_x2_and_index", "attend"))}
-        wl.capture()
-
-    # ---- end to end: a step's inputs from pinned host memory in one copy (the five inputs packed as in the
-    # graphs' input buffer), the step, its output back to pinned host memory
-    pinned = [wl.packed_host(i) for i in range(len(wl.host_inputs))]
-    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
-    h2d = wl.packed_bytes  # the bytes the one copy moves (fields plus alignment padding)
-    d2h = out_host.numel() * out_host.element_size()
-    ev2 = [(mk(), mk()) for _ in range(args.e2e_steps)]
-    torch.cuda.synchronize()
-    for i in range(args.e2e_steps):
-        flush.zero_()
-        ev2[i][0].record(stream)
-        k = i % len(pinned)
-        wl.packed[k].copy_(pinned[k], non_blocking=True)
-        wl.replay(k)
-        out_host.copy_(wl.out, non_blocking=True)
-        ev2[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev2), dev) / max(1, args.e2e_steps)
+        assert wl.err.item() == 0, f"device error word {wl.err.item()}"
 
     # ---- prefill chunk (config 5), timed once per repeat from a restored snapshot
     prefill = None
@@ -430,8 +512,8 @@ def run_ours(args):
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
 
     hbm, tflops, peak_src = _peaks()
-    ms_per_step = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1e3)
+    ms_per_step = total_ms / (args.steps * nl)  # per layer-step
+    value = world * args.steps * nl / (total_ms / 1e3)
     nb = step_bytes(cfg, 0.5 * (n_start + n_end))
     step_avg_s = ms_per_step / 1e3
     result = None
@@ -449,31 +531,42 @@ def run_ours(args):
                 "step_algorithmic_bytes": int(nb["total"]),
                 "step_hbm_gbs": round(nb["total"] / (ms_per_step / 1e3) / 1e9, 1),
                 "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
-                "l2": "flushed (512 MB write) before every timed step, outside the events",
+                "layers_per_step": nl,
+                "layer_steps_timed": args.steps * nl,
+                "model_step": (f"each timed step is one decode step of {nl} layers (distinct weights, caches, inputs "
+                               f"and workspaces: {nl} x ~0.4 GB, every layer's data cold in HBM as after the other "
+                               "layers of a model), one CUDA graph replay; value = layer-steps / time; positions "
+                               "advance once per model step"),
+                "single_layer_graph": single,
+                "l2": ("flushed (512 MB write) before every timed model step, outside the events; within a model "
+                       "step each layer's data is distinct and the step's working set is far above L2"),
                 "phase_us": phase_us,
-                "phase_us_note": ("diagnostic run of the same steps as two graphs (compress x2 + indexer | "
+                "phase_us_note": ("diagnostic: layer 0 alone, its step as two graphs (compress x2 + indexer | "
                                   "attention), events between them; each includes its graph's launch latency"),
                 "launch": ("kernels launched one by one" if args.eager else
-                           "each step = 1 CUDA graph replay (three streams in phase 1: both compress calls on "
-                           "side streams, the overlapped indexer on the main stream)"),
+                           "each model step = 1 CUDA graph replay; per layer one stream: csa_compress_append_pair, "
+                           "csa_index_topk, csa_attend_decode, every kernel after its predecessor by programmatic "
+                           "launch; csa_advance_positions after the last layer"),
                 "prefill": prefill,
             },
             "roofline": {
-                "kernel": ("decode step graph: every kernel of one step (compress x2, index scan + top-k, "
-                           "attention + merge); algorithmic bytes = weights + index keys + attended rows + "
-                           "q/out + small terms"), "bound": "hbm",
+                "kernel": (f"model step graph: every kernel of one decode step of {nl} layers (per layer: both "
+                           "projections, both pooling steps, index scan + top-k, attention + merge); algorithmic "
+                           "bytes per layer = weights + index keys + attended rows + q/out + small terms"),
+                "bound": "hbm",
                 "achieved": round(nb["total"] / step_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(nb["total"] / step_avg_s / 1e9 / hbm, 4), "traffic": None,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                else "fallback 6800 GB/s", "avg_launch_ms": round(ms_per_step, 5),
-                "algorithmic_bytes_per_launch": int(nb["total"]),
+                else "fallback 6800 GB/s", "avg_launch_ms": round(total_ms / args.steps, 5),
+                "algorithmic_bytes_per_launch": int(nb["total"] * nl),
             },
             "cpu_baseline": {"value": round(cpu["layer_steps_per_s"], 5), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"1 of {cfg.B} sequences x {cpu['steps']} decode steps of the same workload, "
                                        f"float64 numpy oracle, single-threaded BLAS; per-layer-step time = "
                                        f"{cfg.B} x per-sequence time"},
-            "e2e": {"value": round(world * 1e3 / e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": {"value": round(world * nl * 1e3 / e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": round(d2h / nl),
+                    "per_model_step": {"layers": nl, "h2d_copies": nl, "h2d_bytes": h2d * nl, "d2h_bytes": d2h}},
             "gpu_launches": int(launches),
             "clocks": clk,
         }
@@ -566,6 +659,8 @@ def main():
     ap.add_argument("--prefill-repeats", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
+    ap.add_argument("--layers", type=int, default=8,
+                    help="layers per model step (each its own weights and caches), one CUDA graph per step")
     ap.add_argument("--two-streams", action="store_true",
                     help="the two compress calls separately, the attention pool's on a side stream")
     ap.add_argument("--overlapped-indexer", action="store_true",
