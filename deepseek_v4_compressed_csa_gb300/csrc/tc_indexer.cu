@@ -95,30 +95,48 @@ __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
   return nv > a.topk ? (nv + kTileRows - 1) / kTileRows : 0;
 }
 
-// The CTA's work items are (group, tile) pairs it..i_end-1; a group's tiles past its visible rows are skipped.
-// Every role walks the same sequence: first unskipped item at or after `it`, or i_end.  The walker keeps
-// plain copies of the two fields it needs (a reference to the kernel's parameters would move them to local
-// memory) and the tile count of the last group it looked at.
+// The CTA's work items are the (group, tile) pairs i_begin .. i_end-1 (item = group * tiles_per_group + tile); a
+// group's tiles past its visible rows are skipped.  Every role walks the same sequence with this iterator: one
+// division when it starts and one tile count per group, so that the MMA thread's per-tile bookkeeping stays a few
+// instructions (a division per tile had cost it ~1k clocks a tile, leaving the tensor pipe idle between tiles).
 template <bool kOverlap>
-struct Walker {
-  int tpg, i_end, g_cached, nt_cached;
-  __device__ Walker(int tiles_per_group, int e) : tpg(tiles_per_group), i_end(e), g_cached(-1), nt_cached(0) {}
-  __device__ __forceinline__ int next(const IdxArgs& a, int it) {
-    while (it < i_end) {
-      const int g = it / tpg, t = it - g * tpg;
-      if (g != g_cached) {
-        g_cached = g;
-        nt_cached = group_tiles<kOverlap>(a, g);
-      }
-      if (t < nt_cached) return it;
-      it = (g + 1) * tpg;
-    }
-    return i_end;
+struct Items {
+  int g, t, t1, g_last, i_end, tpg;
+  // first item at or after i_begin; false if none
+  __device__ __forceinline__ bool start(const IdxArgs& a, int i_begin, int i_end_) {
+    tpg = a.tiles_per_group;
+    i_end = i_end_;
+    g_last = i_begin < i_end ? (i_end - 1) / tpg : -1;
+    g = i_begin < i_end ? i_begin / tpg : 0;
+    t = i_begin - g * tpg;
+    if (g > g_last) return false;
+    bounds(a);
+    return settle(a);
   }
-  // whether item `it` is the last of its group in this CTA's sequence
-  __device__ __forceinline__ bool last_of_group(const IdxArgs& a, int it) {
-    const int nxt = next(a, it + 1);
-    return nxt >= i_end || nxt / tpg != it / tpg;
+  __device__ __forceinline__ bool advance(const IdxArgs& a) {
+    ++t;
+    return settle(a);
+  }
+  // first item of the next group that has one
+  __device__ __forceinline__ bool next_group(const IdxArgs& a) {
+    t = t1;
+    return settle(a);
+  }
+  // the current item is the last of its group in this CTA's range
+  __device__ __forceinline__ bool last_of_group() const { return t == t1 - 1; }
+
+ private:
+  __device__ __forceinline__ void bounds(const IdxArgs& a) {
+    const int hi = (g == g_last) ? i_end - g * tpg : tpg;
+    t1 = min(group_tiles<kOverlap>(a, g), hi);
+  }
+  __device__ __forceinline__ bool settle(const IdxArgs& a) {
+    while (t >= t1) {
+      if (++g > g_last) return false;
+      t = 0;
+      bounds(a);
+    }
+    return true;
   }
 };
 
@@ -215,7 +233,6 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  Walker<kOverlap> wk(a.tiles_per_group, i_end);
   bool failed = false;
 
   if (warp == 0) {
@@ -227,41 +244,40 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       tc::tma_prefetch(&tm_keys);
       int stage = 0;
       uint32_t phase = 0;
-      int issued[C::kStages];
-#pragma unroll
-      for (int s = 0; s < C::kStages; ++s) issued[s] = 0;
-      for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
-        const int g = it / a.tiles_per_group, t = it % a.tiles_per_group;
+      uint32_t used = 0, par_last = 0;  // per stage (bit s): a load was issued; parity of its last phase
+      Items<kOverlap> itr;
+      for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
+        const int g = itr.g, t = itr.t;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
         const int krow = (a.pos ? g : 0) * a.cap + t * kTileRows;
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
         tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
-        ++issued[stage];
+        used |= 1u << stage;
+        par_last = (par_last & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
       // every load issued must land before the CTA may exit
       for (int s = 0; s < C::kStages; ++s)
-        if (issued[s] && !tc::mbar_wait(&full[s], (issued[s] - 1) & 1)) failed = true;
+        if (((used >> s) & 1) && !tc::mbar_wait(&full[s], (par_last >> s) & 1)) failed = true;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16(128, N);
       int cur_g = -1, k = -1, stage = 0, acc = 0;
-      int n_acc[C::kAcc];
-#pragma unroll
-      for (int i = 0; i < C::kAcc; ++i) n_acc[i] = 0;
+      uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
       uint32_t phase = 0;
-      for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
-        const int g = it / a.tiles_per_group;
+      Items<kOverlap> itr;
+      for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
+        const int g = itr.g;
         if (g != cur_g) {
           ++k;
           cur_g = g;
           if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
         }
         if (!tc::mbar_wait(&full[stage], phase)) { failed = true; break; }
-        if (!tc::mbar_wait(&acc_empty[acc], (n_acc[acc] & 1) ^ 1)) { failed = true; break; }
+        if (!tc::mbar_wait(&acc_empty[acc], ((acc_par >> acc) & 1) ^ 1)) { failed = true; break; }
         tc::fence_after_sync();
         const uint32_t a_base = tc::smem_u32(kbuf + stage * kTileBytes);
         const uint32_t b_base = tc::smem_u32(qbuf + (k % C::kQSlots) * C::kQBytes);
@@ -273,8 +289,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         }
         tc::mma_commit(&empty[stage]);
         tc::mma_commit(&acc_full[acc]);
-        if (wk.last_of_group(a, it)) tc::mma_commit(&q_empty[k % C::kQSlots]);
-        ++n_acc[acc];
+        if (itr.last_of_group()) tc::mma_commit(&q_empty[k % C::kQSlots]);
+        acc_par ^= 1u << acc;
         if (++acc == C::kAcc) acc = 0;
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
@@ -287,12 +303,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     int cur_g = -1, k = -1, acc = 0;
-    int n_acc[C::kAcc];
-#pragma unroll
-    for (int i = 0; i < C::kAcc; ++i) n_acc[i] = 0;
+    uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
     int nv[G];
-    for (int it = wk.next(a, i_begin); it < i_end; it = wk.next(a, it + 1)) {
-      const int g = it / a.tiles_per_group, t = it % a.tiles_per_group;
+    Items<kOverlap> itr;
+    for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
+      const int g = itr.g, t = itr.t;
       if (g != cur_g) {
         ++k;
         cur_g = g;
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
 #pragma unroll
         for (int qq = 0; qq < G; ++qq) nv[qq] = g * G + qq < a.Q ? scan_rows<kOverlap>(a, g * G + qq) : 0;
       }
-      if (!tc::mbar_wait(&acc_full[acc], n_acc[acc] & 1)) { failed = true; break; }
+      if (!tc::mbar_wait(&acc_full[acc], (acc_par >> acc) & 1)) { failed = true; break; }
       tc::fence_after_sync();
       const int j = t * kTileRows + row;
       const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
@@ -338,11 +353,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&acc_empty[acc]);
-      if (wk.last_of_group(a, it)) {
+      if (itr.last_of_group()) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&w_empty[k % C::kQSlots]);
       }
-      ++n_acc[acc];
+      acc_par ^= 1u << acc;
       if (++acc == C::kAcc) acc = 0;
     }
   } else {
@@ -383,9 +398,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
-    for (int it = wk.next(a, i_begin); it < i_end;
-         it = wk.next(a, (it / a.tiles_per_group + 1) * a.tiles_per_group)) {
-      const int g = it / a.tiles_per_group;
+    Items<kOverlap> itr;
+    for (bool more = itr.start(a, i_begin, i_end); more; more = itr.next_group(a)) {
+      const int g = itr.g;
       ++k;
       const int slot = k % C::kQSlots, use = k / C::kQSlots;
       if (use > 0) {
