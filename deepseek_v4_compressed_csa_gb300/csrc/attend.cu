@@ -388,7 +388,7 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
                             const AttendWs& ws, int32_t* err, cudaStream_t s) {
   // the workspace holds ws.S partials per query; the one-chunk decode kernel needs splits of <= 160 rows, which
   // it always has except for a layer with an indexer called without a selection (every visible row)
-  const int S = tc_attend_decode_supported(L) ? tc_attend_decode_splits(B, (sel ? L.topk : cap) + L.W, ws.S) : 0;
+  const int S = tc_attend_decode_supported(L) ? tc_attend_decode_splits(B, L.W, sel ? L.topk : cap, ws.S) : 0;
   if (S > 0) {
     cudaError_t e = launch_tc_attend_decode(L, q, pool, window, kv_new, sel, n_sel, n_rows, pos, cap, sink, inv_freq,
                                             B, S, ws.part_ml, ws.part_acc, out, err, s);
@@ -450,8 +450,9 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
 
 // pos[b] += by: the decode loop's position advance, launched with programmatic serialisation like every kernel
 // here, so it starts while the step's last kernel drains and only its store waits for it
+// No early trigger: the next kernel starts once the new positions are written, since kernels read the positions
+// of their step before their own programmatic wait.
 __global__ void k_advance_positions(int32_t* __restrict__ pos, int B, int by) {
-  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   if (b < B) pos[b] += by;

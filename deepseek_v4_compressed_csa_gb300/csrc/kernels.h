@@ -54,6 +54,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   count_launches(1);
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
 #define CSA_LAUNCH(...)                           \
   do {                                            \
     cudaError_t csa_e_ = launch_pdl(__VA_ARGS__); \
@@ -153,9 +154,10 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
 
 // ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_decode_supported(const Dims& L);
-// Key splits per query for Q queries of at most max_rows rows: every split <= 160 rows, more splits while every
-// CTA still fits one wave; 0 when max_splits cannot hold enough splits.
-int tc_attend_decode_splits(int Q, int max_rows, int max_splits);
+// Key splits per query for Q queries over a window of W rows and at most n_max selected rows: each split's window
+// share plus selection share fits one 160-row tile, more splits while every CTA still fits one wave; 0 when
+// max_splits cannot hold enough splits.
+int tc_attend_decode_splits(int Q, int W, int n_max, int max_splits);
 // One CTA per (query, split).  S > 1 writes (m, l, acc) partials (merge follows), S == 1 the final output.
 // The new token kv_new[b] is roped in-kernel and written to ring slot pos[b] % W.
 cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,

@@ -11,8 +11,10 @@
 // Why 160 rows: a decode query attends to topk + W = 640 rows; four splits of
 // 160 put a batch of 32 on 128 CTAs, one wave of the 152 SMs, where 128-row
 // splits would need 160 CTAs and a second wave.  Each CTA takes its split's rows
-// (selected pool rows, then window tokens, the newest one roped here) as one
-// chunk, gathered with cp.async into one 160-row, 128-byte-swizzled shared tile
+// as one chunk: its share of the window tokens (the newest one roped here) and
+// the query block, both copied before the programmatic wait since they depend
+// only on the step's inputs, then its share of the selected pool rows once the
+// selection is known; all gathered with cp.async into one 160-row, 128-byte-swizzled shared tile
 // that serves both as K (K-major) and as V^T (MN-major), so each row is read from
 // memory once.
 //   QK       S^T = K Q^T twice, M = 128 (TMEM lanes), N = 64 heads, K = 512:
@@ -109,8 +111,13 @@ __device__ __forceinline__ float2 reduce_scatter64(float (&v)[64]) {
   return make_float2(v[0], v[1]);
 }
 
+// One (query, split) item.  The split's tile holds its share of the window first (known from the position alone,
+// so it is gathered before the programmatic wait), then its share of the selection (known after it):
+//   rows [0, nw)        window tokens w_begin .. w_begin + nw - 1 (of the query's nwin window tokens);
+//   rows [nw, nw + ns)  selected rows s_begin .. s_begin + ns - 1 (of nsel).
 struct Item {
-  int q, s, b, p, nsel, nwin, nrows, r_begin, r_end;
+  int q, s, b, p, nwin, w_begin, nw;  // before the wait
+  int nrows, nsel, s_begin, ns;       // after it
 };
 
 __device__ __forceinline__ Item make_item(const DecArgs& a) {
@@ -119,28 +126,36 @@ __device__ __forceinline__ Item make_item(const DecArgs& a) {
   it.s = blockIdx.x % a.S;
   it.b = it.q;
   it.p = a.pos[it.q];
-  it.nrows = min(a.n_rows[it.b], a.cap);
-  it.nsel = a.sel ? min(max(a.n_sel[it.q], 0), a.topk) : max(0, min(it.nrows, (it.p + 1) / a.ratio));
   it.nwin = it.p >= 0 ? min(a.W, it.p + 1) : 0;
-  const int total = it.nsel + it.nwin;
-  const int per = (total + a.S - 1) / a.S;
-  it.r_begin = min(total, it.s * per);
-  it.r_end = min(total, it.r_begin + per);
+  const int wper = (it.nwin + a.S - 1) / a.S;
+  it.w_begin = min(it.nwin, it.s * wper);
+  it.nw = min(it.nwin, it.w_begin + wper) - it.w_begin;
+  it.nrows = it.nsel = it.s_begin = it.ns = 0;
   return it;
 }
 
-// Code of row r (0 .. nsel+nwin-1) of the item, j = sel[q][r] when r < nsel and a selection is given; an
-// out-of-range selection is reported and left empty.
-__device__ __forceinline__ int row_code(const DecArgs& a, const Item& it, int r, int j) {
-  if (r < it.nsel) {
-    if (!a.sel) j = r;
-    if (j >= 0 && j < it.nrows) return it.b * a.cap + j;
-    atomicOr(a.err, CSA_DEV_RANGE);
-    return kRowNone;
-  }
-  const int tok = it.p - it.nwin + 1 + (r - it.nsel);
+// the selection share (reads the predecessors' outputs: call after the programmatic wait)
+__device__ __forceinline__ void item_selection(const DecArgs& a, Item& it) {
+  it.nrows = min(a.n_rows[it.b], a.cap);
+  it.nsel = a.sel ? min(max(a.n_sel[it.q], 0), a.topk) : max(0, min(it.nrows, (it.p + 1) / a.ratio));
+  const int sper = (it.nsel + a.S - 1) / a.S;
+  it.s_begin = min(it.nsel, it.s * sper);
+  it.ns = min(it.nsel, it.s_begin + sper) - it.s_begin;
+  if (it.nw + it.ns > kCR) it.ns = max(0, kCR - it.nw);  // callers keep both shares within one tile
+}
+
+// Code of window token w (0 .. nwin-1, oldest first) and of selected row k (0 .. nsel-1; j = sel[q][k] when a
+// selection is given); an out-of-range selection is reported and left empty.
+__device__ __forceinline__ int window_code(const DecArgs& a, const Item& it, int w) {
+  const int tok = it.p - it.nwin + 1 + w;
   if (tok == it.p) return kRowNew;
   return kRowRing0 - (it.b * a.W + tok % a.W);
+}
+__device__ __forceinline__ int selected_code(const DecArgs& a, const Item& it, int k, int j) {
+  if (!a.sel) j = k;
+  if (j >= 0 && j < it.nrows) return it.b * a.cap + j;
+  atomicOr(a.err, CSA_DEV_RANGE);
+  return kRowNone;
 }
 
 __device__ __forceinline__ const __nv_bfloat16* code_ptr(const DecArgs& a, int code) {
@@ -185,6 +200,26 @@ __device__ __forceinline__ void write_p(uint8_t* pbuf, int row, const float (&sv
   }
 }
 
+// Copy tile rows [r0, r1) from their codes (cp.async, 2 x 512 contiguous bytes per warp instruction; rows spread
+// over the main warps); an empty row is zero-filled and the new token is skipped (roped separately).
+__device__ __forceinline__ void gather_rows(const DecArgs& a, const int* rowc, uint32_t r_base, int r0, int r1) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 4
+  for (int r = r0 + warp; r < r1; r += kMainWarps) {
+    const int code = rowc[r];
+    if (code == kRowNew) continue;
+    const __nv_bfloat16* src = code_ptr(a, code);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int ch = lane + 32 * hh;
+      const uint32_t dst = r_base + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      tc::cp_async16(dst, src ? static_cast<const void*>(src + ch * 8) : static_cast<const void*>(a.pool),
+                     src ? 16u : 0u);
+    }
+  }
+}
+
+// S > 1 writes (m, l, acc) partials for the merge kernel; S == 1 finalises directly.
 __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -215,7 +250,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     tc::mbar_init(drain, 1);
     tc::fence_mbar_init();
   }
-  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  Item it = make_item(a);
+  const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
+  if (warp != kMmaWarp) {
+    // ---- before the programmatic wait: the query block, the RoPE table, this split's window rows and the new
+    // token (step inputs and the window ring, which no kernel of this step writes before this one)
+    const int row = tid;
+    {
+      const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
+#pragma unroll 8
+      for (int e = tid; e < kAH * 64; e += kMain) {
+        const int h = e >> 6, ch = e & 63;
+        tc::cp_async16(q_base + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4),
+                       qsrc + (size_t)h * kAD + ch * 8, 16u);
+      }
+    }
+    if (row < it.nw) rowc[row] = window_code(a, it, it.w_begin + row);
+    if (tid < 32) {
+      float cs, sn;
+      rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
+      rcos[tid] = cs;
+      rsin[tid] = sn;
+    }
+    tc::named_bar(1, kMain);
+    gather_rows(a, rowc, r_base, 0, it.nw);
+    // the new token (the window's last): RoPE at p, into the tile and into its ring slot (the slot belongs to the
+    // token leaving the window, which no CTA reads)
+    const int cur_row = (it.nw > 0 && it.w_begin + it.nw == it.nwin) ? it.nw - 1 : -1;
+    if (cur_row >= 0 && warp == cur_row % kMainWarps) {
+      const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int ch = lane + 32 * hh;
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
+        if (ch >= 56) rope8(raw, ch, rcos, rsin);
+        *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
+        *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
+      }
+    }
+    tc::cp_async_wait_all();
+    tc::named_bar(1, kMain);  // every thread's share of the query block has landed
+#pragma unroll
+    for (int e = tid; e < kAH * 8; e += kMain) {
+      const int h = e >> 3, ch = 56 + (e & 7);
+      uint4* slot = reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4));
+      uint4 raw = *slot;
+      rope8(raw, ch, rcos, rsin);
+      *slot = raw;
+    }
+  }
+  pdl_wait();  // predecessors complete: the selection is visible and their tensor memory is free
   if (warp == kMmaWarp) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
@@ -226,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem;  // S^T: rows 0-127 in cols 0-63, rows 128-255 in cols 64-127
   const uint32_t tm_o = tmem;  // O^T tile m: cols 128m + (0-63: P_hi part, 64-127: P_lo part); overwrites S^T
-  const Item it = make_item(a);
-  const int nr = min(kCR, it.r_end - it.r_begin);
+  item_selection(a, it);
+  const int nr = it.nw + it.ns;
   bool failed = false;
 
   if (warp == kMmaWarp) {
@@ -235,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     if (lane == 0 && nr > 0) {
       constexpr uint32_t id_qk = tc::idesc_bf16(128, 64);
       constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, true, true);
-      const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf), p_base = tc::smem_u32(pbuf);
+      const uint32_t p_base = tc::smem_u32(pbuf);
       do {
         if (!tc::mbar_wait(rows_full, 0)) { failed = true; break; }
         tc::fence_after_sync();
@@ -270,71 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     failed = __shfl_sync(0xffffffffu, (int)failed, 0) != 0;
   } else {
     // ------------------------------------------------------------ main warps (160 threads, one per row)
-    const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
     const int row = tid;
-    const int last_row = it.nsel + it.nwin - 1;  // the new token (when p >= 0)
-    if (it.r_end - it.r_begin > kCR && tid == 0) atomicOr(a.err, CSA_DEV_STATE);  // callers keep splits <= 160
-    // this thread's selection is loaded before the query copies are issued, so the two overlap
-    const int r_abs = it.r_begin + row;
-    const int j_sel = (a.sel && row < nr && r_abs < it.nsel) ? a.sel[(size_t)it.q * a.topk + r_abs] : 0;
-    {
-      const __nv_bfloat16* qsrc = a.q + (size_t)it.q * kAH * kAD;
-#pragma unroll 8
-      for (int e = tid; e < kAH * 64; e += kMain) {
-        const int h = e >> 6, ch = e & 63;
-        tc::cp_async16(q_base + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4),
-                       qsrc + (size_t)h * kAD + ch * 8, 16u);
-      }
-    }
-    rowc[row] = row < nr ? row_code(a, it, r_abs, j_sel) : kRowNone;
-    tc::named_bar(1, kMain);
-    // ---- gather: warp w copies rows 32w .. 32w+31, 2 x 512 contiguous bytes per instruction
-    const int cur_row = (it.p >= 0) ? last_row - it.r_begin : -1;
-#pragma unroll 4
-    for (int rr = 0; rr < 32; ++rr) {
-      const int r = warp * 32 + rr;
-      const int code = rowc[r];
-      if (code == kRowNew) continue;  // roped below
-      const __nv_bfloat16* src = code_ptr(a, code);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int ch = lane + 32 * hh;
-        const uint32_t dst = r_base + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        tc::cp_async16(dst, src ? static_cast<const void*>(src + ch * 8) : static_cast<const void*>(a.pool),
-                       src ? 16u : 0u);
-      }
-    }
-    // RoPE table of this query's position, computed while the copies are in flight
-    if (tid < 32) {
-      float cs, sn;
-      rope_cs(it.p, a.inv_freq, tid, &cs, &sn);
-      rcos[tid] = cs;
-      rsin[tid] = sn;
+    // ---- the selection share: codes of rows nw .. 159 (empty past nr), then their copies
+    if (row >= it.nw) {
+      const int k = it.s_begin + (row - it.nw);
+      const int j = (a.sel && row < nr) ? a.sel[(size_t)it.q * a.topk + k] : 0;
+      rowc[row] = row < nr ? selected_code(a, it, k, j) : kRowNone;
     }
     tc::named_bar(1, kMain);
-    // the new token: RoPE at p, into the tile and into its ring slot (the slot belongs to the token leaving the
-    // window, which no CTA reads)
-    if (cur_row >= 0 && cur_row < nr && warp == (cur_row >> 5)) {
-      const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int ch = lane + 32 * hh;
-        uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
-        if (ch >= 56) rope8(raw, ch, rcos, rsin);
-        *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
-        *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
-      }
-    }
+    gather_rows(a, rowc, r_base, it.nw, kCR);
     tc::cp_async_wait_all();
-    tc::named_bar(1, kMain);  // every thread's share of the query block has landed
-#pragma unroll
-    for (int e = tid; e < kAH * 8; e += kMain) {
-      const int h = e >> 3, ch = 56 + (e & 7);
-      uint4* slot = reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + h * 128 + (((ch & 7) ^ (h & 7)) << 4));
-      uint4 raw = *slot;
-      rope8(raw, ch, rcos, rsin);
-      *slot = raw;
-    }
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     tc::mbar_arrive(rows_full);
@@ -485,18 +514,20 @@ bool tc_attend_decode_supported(const Dims& L) {
   return L.dtype == CSA_BF16 && L.H == kAH && L.D == kAD && L.R == 64;
 }
 
-// Splits per query for at most max_rows rows per query: enough that a split is one chunk (<= 160 rows), more
-// (up to one per 128 rows) while every CTA still fits one wave of the device's SMs.  0 when max_splits (the
-// workspace's partial capacity) cannot hold enough.
-int tc_attend_decode_splits(int Q, int max_rows, int max_splits) {
+// Splits per query: the fewest S whose window share ceil(W / S) plus selection share ceil(n_max / S) fit one
+// 160-row tile, more (up to one per 128 rows) while every CTA still fits one wave of the device's SMs.  0 when
+// max_splits (the workspace's partial capacity) cannot hold enough.
+int tc_attend_decode_splits(int Q, int W, int n_max, int max_splits) {
   if (!g_sms_dec) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_sms_dec, cudaDevAttrMultiProcessorCount, dev);
   }
-  const int s_min = max(1, (max_rows + kCR - 1) / kCR);
+  auto fits = [&](int S) { return (W + S - 1) / S + (n_max + S - 1) / S <= kCR; };
+  int s_min = max(1, (W + n_max + kCR - 1) / kCR);
+  while (!fits(s_min)) ++s_min;
   if (s_min > max_splits) return 0;
-  const int s_tiles = (max_rows + 127) / 128;
+  const int s_tiles = (W + n_max + 127) / 128;
   const int s_fit = g_sms_dec / max(1, Q);
   return min(max_splits, max(s_min, min(s_fit, s_tiles)));
 }

@@ -31,6 +31,13 @@
  *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream).  No call synchronises or reads device memory
  *     on the host, so calls can be captured in a CUDA graph.
+ *   - Kernels are launched with programmatic dependent launch: each lets its
+ *     successor in the stream start early and waits for its predecessor before
+ *     reading anything that predecessor chain writes.  Before that wait a
+ *     kernel may read its call's step inputs (queries, new tokens, weights,
+ *     positions) and the window ring, so these must be complete when the call
+ *     is enqueued behind work that does not trigger early (any ordinary kernel
+ *     or copy; csa_advance_positions for pos).
  *   - Errors found on the host are returned synchronously, before anything is
  *     enqueued (fail closed: nothing is modified).  Errors that depend on
  *     device-resident values (positions, row counts, indices) are OR-ed into
@@ -298,6 +305,8 @@ csa_status csa_index_topk_static(const csa_layer* layer, const void* iq, const v
  * step reads pos; it is not part of the method ("Decode path": the position of
  * the next token), only the loop's bookkeeping, launched like the library's
  * other kernels so that it may start while the step's last kernel finishes.
+ * Unlike them it lets the next kernel start only once it has written pos, so
+ * the next step's calls may read pos before their programmatic wait.
  * Errors: CSA_ERR_ARG for a null pos, B < 0; CSA_ERR_CUDA if the launch fails.
  * B == 0 enqueues nothing. */
 csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream);
