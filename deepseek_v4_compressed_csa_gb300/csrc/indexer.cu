@@ -242,6 +242,83 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
   return v + (wid > 0 ? warp_tot[wid - 1] : 0);
 }
 
+// One radix-select step over a complete 2048-bin histogram h (the caller's __syncthreads() separates the
+// histogram from this call, and a second one separates this call from the use of the result): the bins are taken
+// in descending order (thread t owns bins 2047-2t and 2046-2t) and the bin where the running count reaches `need`
+// gives *s_prefix = prefix | bin << shift and *s_need = the count still needed inside that bin.  One block barrier:
+// each warp scans its own 64 bins, then every warp scans the 32 warp totals itself.  Requires 1024 threads.
+__device__ __forceinline__ void select_bin(const int* h, int need, uint32_t prefix, int shift, int* warp_tot,
+                                           uint32_t* s_prefix, int* s_need) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
+  const int c_hi = h[b_hi], c_lo = h[b_lo];
+  int v = c_hi + c_lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[wid] = v;
+  __syncthreads();
+  int t = warp_tot[lane];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, t, o);
+    if (lane >= o) t += n;
+  }
+  const int before = __shfl_sync(0xffffffffu, t, (wid + 31) & 31);
+  const int incl = v + (wid > 0 ? before : 0);
+  const int excl = incl - c_hi - c_lo;
+  if (excl < need && need <= incl) {
+    if (excl + c_hi >= need) {
+      *s_prefix = prefix | ((uint32_t)b_hi << shift);
+      *s_need = need - excl;
+    } else {
+      *s_prefix = prefix | ((uint32_t)b_lo << shift);
+      *s_need = need - excl - c_hi;
+    }
+  }
+}
+
+// The same step with every warp taking the decision itself, so that no barrier follows it: after the one barrier
+// each warp scans the 32 warp totals, finds the warp whose bins hold the crossing and rescans those 64 bins (read
+// from h, which must then stay unchanged until the next block barrier).  Returns the new prefix and need.
+__device__ __forceinline__ void select_bin_every_warp(const int* h, int& need, uint32_t& prefix, int shift,
+                                                      int* warp_tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int v = h[2047 - 2 * threadIdx.x] + h[2046 - 2 * threadIdx.x];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tot[wid] = v;
+  __syncthreads();
+  int t = warp_tot[lane];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, t, o);
+    if (lane >= o) t += n;
+  }
+  const int cw = __ffs(__ballot_sync(0xffffffffu, t >= need)) - 1;  // the crossing warp (the total is >= need)
+  const int base = cw > 0 ? __shfl_sync(0xffffffffu, t, (cw + 31) & 31) : 0;
+  const int b_hi = 2047 - 2 * (32 * cw + lane);
+  const int c_hi = h[b_hi], c_lo = h[b_hi - 1];
+  int u = c_hi + c_lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, u, o);
+    if (lane >= o) u += n;
+  }
+  const int incl = base + u, excl = incl - c_hi - c_lo;
+  const int hl = __ffs(__ballot_sync(0xffffffffu, incl >= need)) - 1;  // the crossing lane
+  const bool in_hi = excl + c_hi >= need;
+  const int new_need = in_hi ? need - excl : need - excl - c_hi;
+  const uint32_t bin = in_hi ? (uint32_t)b_hi : (uint32_t)(b_hi - 1);
+  need = __shfl_sync(0xffffffffu, new_need, hl);
+  prefix |= __shfl_sync(0xffffffffu, bin, hl) << shift;
+}
+
 // Exact top-k with the keys resident in shared memory: radix select of the
 // k-th largest order key over digits of 11, 11 and 10 bits (2048-bin
 // histograms; the bucket holding the k-th key is found by a block-wide scan
@@ -284,20 +361,7 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
       if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1);
     }
     __syncthreads();
-    // thread t owns bins 2047-2t and 2046-2t (descending order)
-    const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
-    const int c_hi = hist[b_hi], c_lo = hist[b_lo];
-    const int incl = block_incl_scan(c_hi + c_lo, warp_tot);
-    const int excl = incl - c_hi - c_lo;
-    if (excl < need && need <= incl) {
-      if (excl + c_hi >= need) {
-        s_prefix = prefix | ((uint32_t)b_hi << shift);
-        s_need = need - excl;
-      } else {
-        s_prefix = prefix | ((uint32_t)b_lo << shift);
-        s_need = need - excl - c_hi;
-      }
-    }
+    select_bin(hist, need, prefix, shift, warp_tot, &s_prefix, &s_need);
     __syncthreads();
     prefix = s_prefix;
     need = s_need;
@@ -367,8 +431,8 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
 
 // Exact top-k with every key in registers, for up to kTopkRegKeys x 1024 visible rows: thread t owns the
 // contiguous rows [K t, K t + K), K = ceil(n_vis / 1024), so the final pass writes the kept rows in ascending
-// order with two block scans.  The threshold is found by the same 11/11/10-bit radix select as k_topk_smem
-// (2048-bin shared histograms, double-buffered so the next pass's bins are cleared during the current one).
+// order with one block scan.  The threshold is found by the same 11/11/10-bit radix select as k_topk_smem
+// (2048-bin shared histograms, one per pass, each cleared during the pass before; two block barriers a pass).
 constexpr int kTopkRegKeys = 16;
 
 // Scores of rows jr[0], jr[1] (-1: none) of query q from the roped queries qr [Q,64,128] (bf16) and the scaled
@@ -411,10 +475,8 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
                                                    const float* __restrict__ w, const __nv_bfloat16* __restrict__ keys) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int hist[2][2048];
+  __shared__ int hist[3][2048];  // pass n counts into hist[n] and clears the next pass's bins
   __shared__ int warp_tot[32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
   __shared__ float part[2][64];
   __shared__ float new_score[2];
   const int q = blockIdx.x, bseq = query_seq(pos, q);
@@ -451,38 +513,28 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
   int need = topk;
   const int shifts[3] = {21, 10, 0};
   const int widths[3] = {11, 11, 10};
+  // two barriers a pass: the histogram is complete; the warp totals are written (every warp then decides alone,
+  // and the bins it rereads are not cleared before the next pass's first barrier)
 #pragma unroll
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass];
     const uint32_t dmask = (1u << widths[pass]) - 1u;
-    int* h = hist[pass & 1];
+    int* h = hist[pass];
 #pragma unroll
     for (int i = 0; i < kTopkRegKeys; ++i)
       if (i < K && r0 + i < nvis && (uk[i] & mask) == prefix) atomicAdd(&h[(uk[i] >> shift) & dmask], 1);
-    hist[(pass + 1) & 1][2 * threadIdx.x] = 0;  // the next pass's bins
-    hist[(pass + 1) & 1][2 * threadIdx.x + 1] = 0;
-    __syncthreads();
-    // thread t owns bins 2047-2t and 2046-2t (descending order)
-    const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
-    const int c_hi = h[b_hi], c_lo = h[b_lo];
-    const int incl = block_incl_scan(c_hi + c_lo, warp_tot);
-    const int excl = incl - c_hi - c_lo;
-    if (excl < need && need <= incl) {
-      if (excl + c_hi >= need) {
-        s_prefix = prefix | ((uint32_t)b_hi << shift);
-        s_need = need - excl;
-      } else {
-        s_prefix = prefix | ((uint32_t)b_lo << shift);
-        s_need = need - excl - c_hi;
-      }
+    if (pass < 2) {  // the next pass's bins
+      hist[pass + 1][2 * threadIdx.x] = 0;
+      hist[pass + 1][2 * threadIdx.x + 1] = 0;
     }
     __syncthreads();
-    prefix = s_prefix;
-    need = s_need;
+    select_bin_every_warp(h, need, prefix, shift, warp_tot);
     mask |= dmask << shift;
   }
   // prefix = order key of the k-th largest score: keep every key above it and the `need` lowest-indexed keys
   // equal to it, in ascending row order
+  // One scan of (keys above << 16 | keys equal) per thread gives both counts before it (each < 2^16): the
+  // thread's first output slot is (above before) + min(equal before, need).
   int gt = 0, eq = 0;
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) {
@@ -490,10 +542,12 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
     gt += (v && uk[i] > prefix) ? 1 : 0;
     eq += (v && uk[i] == prefix) ? 1 : 0;
   }
-  const int eq_before = block_incl_scan(eq, warp_tot) - eq;
-  const int take = gt + max(0, min(eq, need - eq_before));
-  int o = block_incl_scan(take, warp_tot) - take;
-  const int total = warp_tot[31];
+  const int packed = (gt << 16) | eq;
+  const int incl = block_incl_scan(packed, warp_tot);
+  const int before = incl - packed;
+  const int eq_before = before & 0xffff;
+  int o = (before >> 16) + min(eq_before, need);
+  const int total = (warp_tot[31] >> 16) + min(warp_tot[31] & 0xffff, need);
   int eq_rank = eq_before;
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) {
