@@ -37,7 +37,7 @@ struct IdxCfg {
   static constexpr int N = 64 * G;               // MMA N: 64 heads x G queries
   static constexpr int kQBytes = N * 128 * 2;    // one query block: 2 boxes of N rows x 128 B
   static constexpr int kQSlots = G == 1 ? 2 : 1;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = G == 1 ? 5 : 4;  // decode: five 32 KB key tiles in flight (measured best of 4-6)
   static constexpr int kAcc = G == 1 ? 4 : 2;    // TMEM accumulators of N columns
   static constexpr int kOffK = kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights

@@ -54,6 +54,22 @@ __device__ __forceinline__ void project_tile(const CUtensorMap* tm_wkv, const CU
     tc::mbar_init(acc_full, 1);
     tc::fence_mbar_init();
   }
+  const int k0 = split * a.n_kblk;
+  const CUtensorMap* wmap = (m * 128 < a.Ld) ? tm_wkv : tm_wg;
+  const int wrow = (m * 128 < a.Ld) ? m * 128 : m * 128 - a.Ld;
+  // The first fill of the ring is issued before the wait on the preceding kernel (by the thread that initialised
+  // the barriers): weights and tokens are the call's inputs, which no kernel of this library writes.
+  const int n_first = min(stages, a.n_kblk);
+  if (threadIdx.x == 0) {
+    tc::tma_prefetch(wmap);
+    tc::tma_prefetch(tm_x);
+    for (int kb = 0; kb < n_first; ++kb) {
+      uint8_t* st = smem + kb * stage_bytes;
+      tc::mbar_arrive_expect_tx(&full[kb], stage_bytes);
+      tc::tma_load_2d(st, wmap, &full[kb], (k0 + kb) * 64, wrow);
+      tc::tma_load_2d(st + kABytes, tm_x, &full[kb], (k0 + kb) * 64, n * N);
+    }
+  }
   pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, tcols);
@@ -64,16 +80,12 @@ __device__ __forceinline__ void project_tile(const CUtensorMap* tm_wkv, const CU
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
-  const int k0 = split * a.n_kblk;
 
   if (warp == 0) {
     if (lane == 0) {
-      const CUtensorMap* wmap = (m * 128 < a.Ld) ? tm_wkv : tm_wg;
-      const int wrow = (m * 128 < a.Ld) ? m * 128 : m * 128 - a.Ld;
-      tc::tma_prefetch(wmap);
-      tc::tma_prefetch(tm_x);
       int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int kb = 0; kb < a.n_kblk; ++kb) {
+      for (int kb = 0; kb < n_first; ++kb) ++issued[kb];
+      for (int kb = n_first; kb < a.n_kblk; ++kb) {
         const int s = kb % stages;
         const uint32_t ph = (kb / stages) & 1;
         if (!tc::mbar_wait(&empty[s], ph ^ 1)) { failed = true; break; }
