@@ -529,11 +529,14 @@ __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part
                                                   int S, const float* __restrict__ sink, const int32_t* __restrict__ pos,
                                                   const float* __restrict__ inv_freq, __nv_bfloat16* __restrict__ out) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float rc[32], rs[32];
   const int q = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 8 + warp;
   const size_t base = (size_t)q * S * kAH + h;
+  // before the wait: the sink and the RoPE table of the query's position (call inputs)
+  const float z = sink[h];
+  if (threadIdx.x < 32) rope_cs(pos[q], inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
+  pdl_wait();
   float4 x[4][4];
   auto load_batch = [&](int s0) {
 #pragma unroll
@@ -549,9 +552,6 @@ __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part
   // split statistics: lane s holds split s (S <= 32)
   const float m_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2) : -INFINITY;
   const float l_l = lane < S ? __ldcg(part_ml + (base + (size_t)lane * kAH) * 2 + 1) : 0.f;
-  const float z = sink[h];
-  const int p = pos[q];
-  if (threadIdx.x < 32) rope_cs(p, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
   const float M = fmaxf(z, warp_max(m_l));
   const float f_l = m_l == -INFINITY ? 0.f : expf(m_l - M);
   const float Z = expf(z - M) + warp_sum(l_l * f_l);
