@@ -346,19 +346,31 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
     return;
   }
   const float* sc = scores + (size_t)q * cap;
-  for (int j = threadIdx.x; j < nvis; j += blockDim.x) sm_keys[j] = ord_key(__ldg(sc + j));
+  // the first digit's histogram is counted while the keys are stored
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+#pragma unroll 4
+  for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
+    const uint32_t u = ord_key(__ldg(sc + j));
+    sm_keys[j] = u;
+    atomicAdd(&hist[u >> 21], 1);
+  }
   uint32_t prefix = 0, mask = 0;
   int need = topk;
   const int shifts[3] = {21, 10, 0};
   const int widths[3] = {11, 11, 10};
+#pragma unroll
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass];
     const uint32_t dmask = (1u << widths[pass]) - 1u;
-    for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
-      const uint32_t u = sm_keys[j];
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1);
+    if (pass > 0) {
+      for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+#pragma unroll 4
+      for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
+        const uint32_t u = sm_keys[j];
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1);
+      }
     }
     __syncthreads();
     select_bin(hist, need, prefix, shift, warp_tot, &s_prefix, &s_need);
@@ -375,6 +387,7 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   const int per = ((nvis + 31) / 32 + 31) & ~31;
   const int lo = wid * per, hi = min(nvis, lo + per);
   int gt_n = 0, eq_n = 0;
+#pragma unroll 4
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t u = j < hi ? sm_keys[j] : 0u;
@@ -410,6 +423,7 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   __syncthreads();
   int slot = w_out[wid], eq_rank = w_eqbase[wid];
   const unsigned lt = (1u << lane) - 1u;
+#pragma unroll 4
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t u = j < hi ? sm_keys[j] : 0u;
