@@ -11,7 +11,11 @@ on a 65536-token cache.
 
 Timing: CUDA events around each step on the launching stream; the 129 MB L2 is
 flushed (a 512 MB write) before every timed step, outside the events, because
-in a full model 42 other layers run between two steps of this one.
+in a full model 42 other layers run between two steps of this one.  A timed
+step is a model step of --layers layers (default 8), each with its own data.
+The end-to-end figure runs the same model steps through the public calls with
+every layer's inputs copied from pinned host memory and the output read back,
+pipelined as a serving loop (the next step's copies under the current step).
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
 """
