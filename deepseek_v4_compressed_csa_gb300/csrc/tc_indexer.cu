@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   };
   const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
   const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
-  Pre pre_a, pre_b;
+  Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
   if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
@@ -237,8 +237,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ key tiles (TMA)
-    // the query-block warps request their inputs first: issued behind a full ring of key tiles, those few
-    // loads would wait in the same queues, and the first MMA waits for them
+    // the ring starts once the query-block warps have issued their requests (issued behind a full ring of key
+    // tiles, those few loads would wait in the same queues; issuing the first tiles at the programmatic wait
+    // instead, or before it, measured slower)
     tc::named_bar(4, 32 + kPrepThreads);
     if (lane == 0) {
       tc::tma_prefetch(&tm_keys);
@@ -385,16 +386,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
           *reinterpret_cast<uint4*>(a.qr_out + ((size_t)(g * G + qq) * 64 + h) * 128 + c * 8) = raw[b];
       }
     };
-    // the first group of the range is requested up front (before the key stream saturates memory and stretches
+    // the first group of the range was requested up front (before the key stream saturates memory and stretches
     // every round trip); the second is prefetched into L2
-    constexpr bool kPreloadSecond = false;
     if (g1 >= 0) {
-      if (kPreloadSecond) {
-        load_first(g1, pre_b);
-      } else {
-        for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
-          if (g1 * G + e / 32 < a.Q) tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + e * 2) * 128, 512);
-      }
+      for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
+        if (g1 * G + e / 32 < a.Q) tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + e * 2) * 128, 512);
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
@@ -409,9 +405,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       } else {
         tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
       }
-      const bool second = kPreloadSecond && g == g1;
-      Pre& pre = second ? pre_b : pre_a;
-      if (g != g0 && !second) load_first(g, pre_a);  // a later group: request it now
+      Pre& pre = pre_a;
+      if (g != g0) load_first(g, pre_a);  // a later group: request it now
       // RoPE table (G x 32 entries) from the preloaded position and frequency
       for (int e = pt; e < G * 32; e += kPrepThreads) {
         int p = pre.p;
