@@ -9,9 +9,8 @@ primitives (matmul, sort, exp) as single steps, loops over sequences, tokens and
 queries in the order the method defines them.  The only deliberate precision
 loss is the storage rounding the pages fix: activations, caches and outputs are
 held in the model dtype (bf16, or fp32 for the tiny case) while pooling, softmax
-and accumulation run at full precision ("Decode path: reference-faithful bf16
-activation storage", MTPLX #216 "DeepSeek-V4-Flash: native deepseek_v4 AR
-backend": rotary rotates in fp32 and copies back at the model dtype; the
+and accumulation run at full precision (MTPLX #216 "DeepSeek-V4-Flash: native
+deepseek_v4 AR backend", "Decode path", on bf16 activation storage: rotary rotates in fp32 and copies back at the model dtype; the
 compressor pools in fp32 and casts the row back before the norm; the sparse
 attention kernel is bf16 in/out with fp32 accumulation).  Rounding happens at
 exactly these points:
@@ -106,8 +105,8 @@ class Layer:
     @property
     def lanes(self) -> int:
         """Ratio-4 layers pool overlapping windows through two lanes
-        ([mlx-lm#1189], Thump604: "ratio-4 overlap compressor shapes ... ape (4, 1024)
-        and wkv/wgate (1024, 4096)", i.e. 2 x 512); ratio-128 layers use one."""
+        ([mlx-lm#1189], Thump604's fixes: the overlap compressor's ape is [4, 1024]
+        and wkv/wgate [1024, 4096], two lanes of 512); ratio-128 layers use one."""
         return 2 if self.ratio == 4 else 1
 
     @property
@@ -118,8 +117,8 @@ class Layer:
 
     @property
     def has_indexer(self) -> bool:
-        """Only ratio-4 layers carry the top-k indexer ([mlx-lm#1189], machiabeli
-        "v0.2: Indexer topk": ratio-4 layers run the indexer)."""
+        """Only ratio-4 layers carry the top-k indexer ([mlx-lm#1189], machiabeli's
+        v0.2 indexer top-k post: the indexer runs on the ratio-4 layers)."""
         return self.ratio == 4
 
     @property
@@ -150,10 +149,10 @@ def rope(v, p, inv_freq, inverse: bool = False) -> np.ndarray:
     """Rotate the LAST 2*len(inv_freq) dims of v (any leading shape) at position p.
 
     Interleaved pairs: dims (D-R+2i, D-R+2i+1) rotate by theta_i
-    ([mlx-lm#1189] stepnoy: "Rotary dims are the LAST rope.dims"; pairs
+    ([mlx-lm#1189] stepnoy: the rotation acts on the trailing rope dims; pairs
     x0 = rot[..., 0], x1 = rot[..., 1] -> (x0 cos - x1 sin, x0 sin + x1 cos)).
     ``inverse`` rotates by -theta (the output rotation, [mlx-lm#1189] Thump604:
-    "inverse output rotation for the post-attention rope dims").
+    the rope dims of the attention output are rotated back).
     """
     v = np.asarray(v, dtype=np.float64)
     R = 2 * len(inv_freq)
@@ -200,8 +199,8 @@ def window_entries(layer: Layer, comp: Compressor, j: int, tok: dict):
 
     ``tok`` maps absolute token index -> (kv [L*d], g [L*d]).  The score of an
     entry is its gate plus the absolute position embedding of the token's slot
-    in its window, ape[t mod ratio] ([MTPLX#216] "What V4 adds": "learned gated
-    pooling"; [mlx-lm#1189] OmarB97/aidiffuser: rows carry the previous window
+    in its window, ape[t mod ratio] ([MTPLX#216] "What V4 adds": learned gated
+    pooling; [mlx-lm#1189] OmarB97/aidiffuser: rows carry the previous window
     for the ratio-4 overlap transform).
     Ratio 4 (R1): tokens of window j-1 through lane 0 and tokens of window j
     through lane 1; window -1 does not exist, so row 0 pools 4 entries.
@@ -232,8 +231,8 @@ def finalize_row(layer: Layer, comp: Compressor, u, j: int, inv_freq) -> np.ndar
     """Pooled row -> model dtype -> RMSNorm -> model dtype -> RoPE at j*ratio -> model dtype.
 
     ([MTPLX#216] "Decode path": the compressor pools in fp32 and casts the row
-    back before the norm; [mlx-lm#1189] OmarB97 "Compressed pool rows must be
-    roped at birth ... at its window-start position (0, r, 2r, ...)".)
+    back before the norm; [mlx-lm#1189] OmarB97's RoPE fixes: a pool row is
+    rotated when it is emitted, at the position its window starts, 0, r, 2r, ...)
     """
     u = store(u, layer.dtype)
     y = store(rms_norm(u, comp.norm_w, layer.rms_eps), layer.dtype)
@@ -302,7 +301,7 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
 def visible_rows(layer: Layer, n: int, p: int) -> int:
     """Rows visible to the query at absolute position p: row j pools tokens
     [j*r, (j+1)*r - 1], so it is visible iff (j+1)*r <= p+1 ([mlx-lm#1189]
-    OmarB97 "Compressed-row visibility mask"; stepnoy's patch point 1)."""
+    OmarB97's fix of the compressed-row visibility mask; stepnoy's patch point 1)."""
     return int(min(n, (p + 1) // layer.ratio))
 
 
@@ -361,8 +360,8 @@ def attend(layer: Layer, q, keys, sink) -> np.ndarray:
     """Softmax attention of H heads over one shared set of keys (K = V).
 
     q [H, D] (roped, model dtype); keys [N, D]; sink [H].  The sink logit z_h
-    enters the softmax denominator only ([v41-mlx] "sinks in the softmax
-    denominator only"; [MTPLX#216] "per-head sink logits"):
+    enters the softmax denominator only ([v41-mlx]: the sinks are added to the
+    softmax denominator alone; [MTPLX#216] "What V4 adds": one sink logit per head):
         o_h = sum_t e^{l_ht} key_t / (e^{z_h} + sum_t e^{l_ht}),  l_ht = scale q_h . key_t
     """
     q = np.asarray(q, dtype=np.float64)
@@ -457,7 +456,7 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0, window, po
     The compressors have already consumed the whole chunk, so the pool holds
     rows emitted up to the chunk's end; each query attends only the rows
     visible to it, through its OWN top-k ([mlx-lm#1189] stepnoy's patch point
-    3: "per-query top-k via a membership mask AND-ed into the visibility mask";
+    3: each query's own top-k membership is combined with the visibility mask;
     aidiffuser: a membership scatter instead of one shared gathered set).
     Window keys older than the chunk come from the ring; chunk tokens are
     roped at their own positions.  After the chunk the ring holds its last W

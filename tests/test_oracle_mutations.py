@@ -300,6 +300,21 @@ def m_compress_emit_late(layer, comp, x, pos, frontier, pool, n_rows, inv_freq):
     return fr, pl, n, err
 
 
+def m_project_swapped(layer, comp, x):
+    x = np.asarray(x, dtype=np.float64)
+    return O.store(x @ comp.wgate.T, layer.dtype), O.store(x @ comp.wkv.T, layer.dtype)
+
+
+def m_project_transposed(layer, comp, x):
+    x = np.asarray(x, dtype=np.float64)
+    return O.store(x @ comp.wkv, layer.dtype), O.store(x @ comp.wgate, layer.dtype)
+
+
+def m_project_not_stored(layer, comp, x):
+    x = np.asarray(x, dtype=np.float64)
+    return x @ comp.wkv.T, x @ comp.wgate.T
+
+
 def m_store_noop(x, dtype):
     return np.asarray(x, dtype=np.float64)
 
@@ -351,6 +366,9 @@ MUTATIONS = {
     "chunk tail dropped": ("compress_append", m_compress_drop_tail),
     "absolute position reset per call": ("compress_append", m_compress_abs_pos_reset),
     "rows emitted one token late": ("compress_append", m_compress_emit_late),
+    "kv/gate weights swapped": ("project", m_project_swapped),
+    "projection contracts the weights' columns": ("project", m_project_transposed),
+    "projections not rounded to the model dtype": ("project", m_project_not_stored),
     "storage rounding skipped": ("store", m_store_noop),
     "bf16 rounding truncates": ("round_bf16", m_round_bf16_truncate),
 }

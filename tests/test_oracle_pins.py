@@ -165,6 +165,19 @@ def test_compressor_hand_example_overlap_row():
     assert u[0] == pytest.approx(g["expected_u"], rel=1e-14)
 
 
+def test_projection_hand_example():
+    """kv = Wkv x and g = Wgate x with weights stored [out, in], each rounded once to bf16 (a tie to even
+    included): pins which weight feeds which output, the contraction axis and the storage rounding."""
+    g = GOLDEN["projection"]
+    layer = _tiny_layer(dtype="bf16", ratio=4, X=2)
+    comp = O.Compressor(wkv=np.array(g["wkv"]), wgate=np.array(g["wgate"]), ape=np.zeros((4, 2)),
+                        norm_w=np.ones(1), d=1)
+    kv, gate = O.project(layer, comp, np.array(g["x"])[None])  # one sequence of two tokens
+    assert kv.shape == gate.shape == (1, 2, 2)
+    assert np.array_equal(kv[0], np.array(g["expected_kv_bf16"]))
+    assert np.array_equal(gate[0], np.array(g["expected_gate_bf16"]))
+
+
 def _entries_pooled(layer, comp, j, tok):
     kv, s = O.window_entries(layer, comp, j, tok)
     return (O.pool_weights(s) * kv).sum(axis=0)
