@@ -1,9 +1,12 @@
 """ctypes binding of libcsa.so: argument marshalling only.
 
-Every function here checks tensor devices, dtypes and shapes, passes raw
-device pointers and the current CUDA stream to the C ABI declared in
-include/csa.h, and turns a non-zero csa_status into an exception.  All
-arithmetic runs in the library's CUDA kernels; there is no CPU path.
+Every function here checks each tensor's dtype and shape against the layer
+and the call (the C ABI sees only untyped pointers, so a wrong dtype or shape
+would otherwise be read as garbage) and that it is a contiguous CUDA tensor,
+all before anything is allocated or enqueued; then it passes raw device
+pointers and the current CUDA stream to the C ABI declared in include/csa.h
+and turns a non-zero csa_status into an exception.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU path.
 """
 from __future__ import annotations
 
@@ -135,6 +138,39 @@ class Compressor:
         return _Comp(_ptr(self.wkv), _ptr(self.wgate), _ptr(self.ape), _ptr(self.norm_w), self.d)
 
 
+def _expect(name: str, t, dtype: torch.dtype, shape=None, optional: bool = False):
+    """Raise TypeError / ValueError unless ``t`` has ``dtype`` and (when given) exactly ``shape``."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _expect_err(err):
+    if err is not None:
+        _expect("err", err, torch.int32)
+        if err.numel() < 1:
+            raise ValueError("err must hold at least one int32")
+
+
+def _expect_comp(layer: "Layer", comp: "Compressor", which: str):
+    L, d = layer.lanes, comp.d
+    _expect(f"{which}.wkv", comp.wkv, layer.dtype, (L * d, layer.X))
+    _expect(f"{which}.wgate", comp.wgate, layer.dtype, (L * d, layer.X))
+    _expect(f"{which}.ape", comp.ape, torch.float32, (layer.ratio, L * d))
+    _expect(f"{which}.norm_w", comp.norm_w, torch.float32, (d,))
+
+
+def _frontier_len(ratio: int) -> int:
+    return 2 * ratio if ratio == 4 else ratio
+
+
 def _ptr(t: torch.Tensor | None):
     if t is None:
         return None
@@ -162,6 +198,7 @@ def kernel_launches() -> int:
 
 def advance_positions(pos, by: int = 1, stream=None):
     """pos[b] += by for every sequence (int32 device tensor), on the library's launch path."""
+    _expect("pos", pos, torch.int32, (pos.numel(),) if isinstance(pos, torch.Tensor) else None)
     _check("csa_advance_positions", load_library().csa_advance_positions(_ptr(pos), pos.numel(), by,
                                                                          _stream(stream)))
 
@@ -191,8 +228,20 @@ def _err(err, device):
 def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_rows, inv_freq, ws=None, err=None,
                     stream=None):
     """csa_compress_append; x [B,T,X]; returns the device error word tensor."""
+    _expect("x", x, layer.dtype)
+    if x.dim() != 3 or x.shape[2] != layer.X:
+        raise ValueError(f"x: shape {tuple(x.shape)}, expected [B, T, {layer.X}]")
     B, T = x.shape[0], x.shape[1]
+    _expect_comp(layer, comp, "comp")
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 3 or pool.shape[0] != B or pool.shape[2] != comp.d:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {comp.d}]")
     cap = pool.shape[1]
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("frontier", frontier, layer.dtype, (B, _frontier_len(layer.ratio), 2 * layer.lanes * comp.d))
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect_err(err)
     ws, nb = _ws(layer, OP_COMPRESS, B, T, cap, ws, x.device)
     err = _err(err, x.device)
     L, C = layer._c(), comp._c()
@@ -205,7 +254,23 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
 def compress_append_pair(layer: Layer, comp_a: Compressor, comp_i: Compressor, x, pos, frontier_a, pool_a, n_rows_a,
                          frontier_i, pool_i, n_rows_i, inv_freq, ws=None, err=None, stream=None):
     """csa_compress_append_pair (attention pool, then index pool, same tokens); returns the error word tensor."""
+    _expect("x", x, layer.dtype)
+    if x.dim() != 3 or x.shape[2] != layer.X:
+        raise ValueError(f"x: shape {tuple(x.shape)}, expected [B, T, {layer.X}]")
     B, T = x.shape[0], x.shape[1]
+    _expect_comp(layer, comp_a, "comp_a")
+    _expect_comp(layer, comp_i, "comp_i")
+    F = _frontier_len(layer.ratio)
+    for nm, pl, fr, nr, d in (("a", pool_a, frontier_a, n_rows_a, comp_a.d), ("i", pool_i, frontier_i, n_rows_i,
+                                                                               comp_i.d)):
+        _expect(f"pool_{nm}", pl, layer.dtype)
+        if pl.dim() != 3 or pl.shape[0] != B or pl.shape[2] != d:
+            raise ValueError(f"pool_{nm}: shape {tuple(pl.shape)}, expected [{B}, cap, {d}]")
+        _expect(f"frontier_{nm}", fr, layer.dtype, (B, F, 2 * layer.lanes * d))
+        _expect(f"n_rows_{nm}", nr, torch.int32, (B,))
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect_err(err)
     cap_a, cap_i = pool_a.shape[1], pool_i.shape[1]
     ws, nb = _ws(layer, OP_COMPRESS_PAIR, B, T, max(cap_a, cap_i), ws, x.device)
     err = _err(err, x.device)
@@ -217,7 +282,25 @@ def compress_append_pair(layer: Layer, comp_a: Compressor, comp_i: Compressor, x
     return err
 
 
+def _expect_index(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err):
+    _expect("iq", iq, layer.dtype)
+    if iq.dim() != 3 or iq.shape[1:] != (layer.Hi, layer.Di):
+        raise ValueError(f"iq: shape {tuple(iq.shape)}, expected [B, {layer.Hi}, {layer.Di}]")
+    B = iq.shape[0]
+    _expect("iw", iw, layer.dtype, (B, layer.Hi))
+    _expect("ikeys", ikeys, layer.dtype)
+    if ikeys.dim() != 3 or ikeys.shape[0] != B or ikeys.shape[2] != layer.Di:
+        raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [{B}, cap, {layer.Di}]")
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("sel", sel, torch.int32, (B, layer.topk))
+    _expect("n_sel", n_sel, torch.int32, (B,))
+    _expect_err(err)
+
+
 def index_topk(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, ws=None, err=None, stream=None):
+    _expect_index(layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err)
     B, cap = iq.shape[0], ikeys.shape[1]
     ws, nb = _ws(layer, OP_INDEX_TOPK, B, 1, cap, ws, iq.device)
     err = _err(err, iq.device)
@@ -232,6 +315,7 @@ def index_topk_overlapped(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, se
                           err=None, stream=None):
     """csa_index_topk_overlapped: the scan of the rows complete before the token is enqueued at once; the
     rest waits for `pool_ready` (a torch.cuda.Event recorded after the index pool's compress call)."""
+    _expect_index(layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err)
     B, cap = iq.shape[0], ikeys.shape[1]
     ws, nb = _ws(layer, OP_INDEX_TOPK, B, 1, cap, ws, iq.device)
     err = _err(err, iq.device)
@@ -245,6 +329,7 @@ def index_topk_overlapped(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, se
 
 def index_topk_static(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err=None, stream=None):
     """csa_index_topk_static: the decode indexer with the library's own fixed scratch array (no workspace)."""
+    _expect_index(layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, err)
     B, cap = iq.shape[0], ikeys.shape[1]
     err = _err(err, iq.device)
     L = layer._c()
@@ -260,7 +345,24 @@ def static_scratch_bytes() -> int:
 
 def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq, out, ws=None,
                   err=None, stream=None):
-    B, cap = q.shape[0], pool.shape[1]
+    _expect("q", q, layer.dtype)
+    if q.dim() != 3 or q.shape[1:] != (layer.H, layer.D):
+        raise ValueError(f"q: shape {tuple(q.shape)}, expected [B, {layer.H}, {layer.D}]")
+    B = q.shape[0]
+    _expect("kv_new", kv_new, layer.dtype, (B, layer.D))
+    _expect("sink", sink, torch.float32, (layer.H,))
+    _expect("window", window, layer.dtype, (B, layer.W, layer.D))
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 3 or pool.shape[0] != B or pool.shape[2] != layer.D:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {layer.D}]")
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("sel", sel, torch.int32, (B, layer.topk), optional=True)
+    _expect("n_sel", n_sel, torch.int32, (B,), optional=sel is None)
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("out", out, layer.dtype, (B, layer.H, layer.D))
+    _expect_err(err)
+    cap = pool.shape[1]
     ws, nb = _ws(layer, OP_ATTEND_DECODE, B, 1, cap, ws, q.device)
     err = _err(err, q.device)
     L = layer._c()
@@ -272,7 +374,28 @@ def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_se
 
 def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, window, pool, ikeys, n_rows, inv_freq,
                          out, sel_out=None, ws=None, err=None, stream=None):
-    T, cap = q.shape[0], pool.shape[-2]
+    _expect("q", q, layer.dtype)
+    if q.dim() != 3 or q.shape[1:] != (layer.H, layer.D):
+        raise ValueError(f"q: shape {tuple(q.shape)}, expected [T, {layer.H}, {layer.D}]")
+    T = q.shape[0]
+    _expect("kv_new", kv_new, layer.dtype, (T, layer.D))
+    if layer.has_indexer:
+        _expect("iq", iq, layer.dtype, (T, layer.Hi, layer.Di))
+        _expect("iw", iw, layer.dtype, (T, layer.Hi))
+        _expect("ikeys", ikeys, layer.dtype)
+        if ikeys.dim() != 2 or ikeys.shape[1] != layer.Di:
+            raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [cap, {layer.Di}]")
+    _expect("sink", sink, torch.float32, (layer.H,))
+    _expect("window", window, layer.dtype, (layer.W, layer.D))
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 2 or pool.shape[1] != layer.D:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [cap, {layer.D}]")
+    _expect("n_rows", n_rows, torch.int32, (1,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("out", out, layer.dtype, (T, layer.H, layer.D))
+    _expect("sel_out", sel_out, torch.int32, (T, layer.topk), optional=True)
+    _expect_err(err)
+    cap = pool.shape[-2]
     ws, nb = _ws(layer, OP_ATTEND_PREFILL, 1, T, cap, ws, q.device)
     err = _err(err, q.device)
     L = layer._c()

@@ -109,3 +109,56 @@ def test_binding_requires_cuda_tensors(lib):
     with pytest.raises(ValueError):
         B._ptr(torch.zeros(4))
     assert csa.workspace_size(L, csa.OP_ATTEND_DECODE, 32, 1, 8400) > 0
+
+
+def _decode_args(torch, dt=None, **over):
+    """Arguments of attend_decode for B = 2 with the right dtypes and shapes (CPU tensors: nothing here may
+    reach the device), with ``over`` replacing some of them."""
+    dt = dt or torch.bfloat16
+    B_, H, D, W, cap, k = 2, 64, 512, 128, 40, 512
+    a = dict(q=torch.zeros(B_, H, D, dtype=dt), kv_new=torch.zeros(B_, D, dtype=dt),
+             sink=torch.zeros(H, dtype=torch.float32), window=torch.zeros(B_, W, D, dtype=dt),
+             pool=torch.zeros(B_, cap, D, dtype=dt), n_rows=torch.zeros(B_, dtype=torch.int32),
+             sel=torch.zeros(B_, k, dtype=torch.int32), n_sel=torch.zeros(B_, dtype=torch.int32),
+             pos=torch.zeros(B_, dtype=torch.int32), inv_freq=torch.zeros(32, dtype=torch.float32),
+             out=torch.zeros(B_, H, D, dtype=dt))
+    a.update(over)
+    return a
+
+
+def test_binding_checks_dtypes_and_shapes_before_the_device(lib):
+    """The C ABI takes untyped pointers, so the binding checks every tensor's dtype and shape against the layer
+    and the call first: a wrong dtype raises TypeError and a wrong shape ValueError before any allocation, device
+    check or launch (here with CPU tensors, which would otherwise fail only at the device check)."""
+    import torch
+    L = csa.Layer(dtype=torch.bfloat16, H=64, D=512, R=64, W=128, ratio=4, Hi=64, Di=128, topk=512, X=4096)
+    with pytest.raises(ValueError, match="CUDA"):  # everything right: only the device check is left
+        csa.attend_decode(L, **_decode_args(torch))
+    bad_dtype = [("q", torch.zeros(2, 64, 512)), ("sink", torch.zeros(64, dtype=torch.bfloat16)),
+                 ("n_rows", torch.zeros(2, dtype=torch.int64)), ("sel", torch.zeros(2, 512)),
+                 ("inv_freq", torch.zeros(32, dtype=torch.float64)), ("out", torch.zeros(2, 64, 512))]
+    for name, t in bad_dtype:
+        with pytest.raises(TypeError, match=name):
+            csa.attend_decode(L, **_decode_args(torch, **{name: t}))
+    bad_shape = [("q", torch.zeros(2, 64, 256, dtype=torch.bfloat16)),
+                 ("kv_new", torch.zeros(3, 512, dtype=torch.bfloat16)),
+                 ("window", torch.zeros(2, 64, 512, dtype=torch.bfloat16)),
+                 ("sel", torch.zeros(2, 256, dtype=torch.int32)), ("pos", torch.zeros(1, dtype=torch.int32))]
+    for name, t in bad_shape:
+        with pytest.raises(ValueError, match=name):
+            csa.attend_decode(L, **_decode_args(torch, **{name: t}))
+    # the other calls: an fp32 tensor handed to a bf16 layer
+    z = torch.zeros
+    with pytest.raises(TypeError, match="iq"):
+        csa.index_topk(L, z(2, 64, 128), z(2, 64, dtype=torch.bfloat16), z(2, 40, 128, dtype=torch.bfloat16),
+                       z(2, dtype=torch.int32), z(2, dtype=torch.int32), z(32), z(2, 512, dtype=torch.int32),
+                       z(2, dtype=torch.int32))
+    comp = csa.Compressor(wkv=z(1024, 4096, dtype=torch.bfloat16), wgate=z(1024, 4096, dtype=torch.bfloat16),
+                          ape=z(4, 1024), norm_w=z(512), d=512)
+    with pytest.raises(TypeError, match="x"):
+        csa.compress_append(L, comp, z(2, 1, 4096), z(2, dtype=torch.int32), z(2, 8, 2048, dtype=torch.bfloat16),
+                            z(2, 40, 512, dtype=torch.bfloat16), z(2, dtype=torch.int32), z(32))
+    with pytest.raises(ValueError, match="frontier"):
+        csa.compress_append(L, comp, z(2, 1, 4096, dtype=torch.bfloat16), z(2, dtype=torch.int32),
+                            z(2, 4, 2048, dtype=torch.bfloat16), z(2, 40, 512, dtype=torch.bfloat16),
+                            z(2, dtype=torch.int32), z(32))

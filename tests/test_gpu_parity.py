@@ -18,11 +18,9 @@ if torch.cuda.is_available():
 
 
 def _oracle_seq_state(cache: csa_synth.Cache, b: int) -> dict:
-    st = oracle_state(cache)
-    out = {}
-    for k, v in st.items():
-        out[k] = None if v is None else v[b:b + 1].copy()
-    return out
+    """Oracle state of sequence b alone (converted after slicing: a full config-3 cache in float64 is ~1.3 GB)."""
+    one = csa_synth.Cache(**{k: (None if v is None else v[b:b + 1]) for k, v in vars(cache).items()})
+    return oracle_state(one)
 
 
 def _step_rows(si: csa_synth.StepInputs, b: int):
@@ -33,9 +31,21 @@ def _seq_projs(run, b):
     return {k: v[b:b + 1].cpu() for k, v in run.projs.items()}
 
 
-def _oracle_decode_check(layer, ca, ci, st, xs, sink, invf, gpu_out, gpu_sel, gpu_nsel, what, projs):
-    """Advance the oracle state by one token and check the GPU's projections, selection and output for it.
-    ``projs`` are the GPU's projections of this sequence's token (per pool)."""
+def _exact_decode_output(layer, q, sink, window, pool, n_rows, sel, n_sel, p, invf):
+    """The un-rounded oracle output of one decode query: the keys of O.attend_decode (selected rows, then the
+    window tokens, the new token already in the ring), float64 attention, rotated back."""
+    rows = np.arange(O.visible_rows(layer, int(n_rows), p)) if sel is None else \
+        np.asarray(sel[:int(n_sel)], dtype=np.int64)
+    keys = np.concatenate([pool[rows]] +
+                          [window[t % layer.W][None] for t in O.window_tokens(layer, p)])
+    o = O.attend(layer, O.store(O.rope(q, p, invf), layer.dtype), keys, sink)
+    return G.exact_output(o, p, invf)
+
+
+def _oracle_decode_check(layer, ca, ci, st, xs, sink, invf, gpu_out, gpu_sel, gpu_nsel, what, projs, label=None):
+    """Advance the oracle state by one token and check the GPU's projections, selection and output for it
+    (against the rounded and the un-rounded oracle output).  ``projs`` are the GPU's projections of this
+    sequence's token (per pool); ``label`` records the errors under that workload name."""
     x, q, kv, iq, iw = xs
     n0 = st["n_rows"].copy()
     st["front_a"], st["pool"], n_a, e1 = G.oracle_compress_checked(layer, ca, x, st["pos"], st["front_a"],
@@ -56,8 +66,11 @@ def _oracle_decode_check(layer, ca, ci, st, xs, sink, invf, gpu_out, gpu_sel, gp
     out, st["window"], err = O.attend_decode(layer, q, kv, sink, st["window"], st["pool"], n_a, sel, n_sel, st["pos"],
                                              invf)
     assert err == 0
+    p = int(st["pos"][0])
+    exact = _exact_decode_output(layer, q[0], sink, st["window"][0], st["pool"][0], n_a[0],
+                                 None if sel is None else sel[0], None if n_sel is None else n_sel[0], p, invf)
     st["pos"] = st["pos"] + 1
-    return G.check_rows(gpu_out, out[0], layer.dtype, what=f"{what} output", R=layer.R)
+    return G.check_rows(gpu_out, out[0], layer.dtype, what=f"{what} output", R=layer.R, exact=exact, label=label)
 
 
 def test_config1_tiny_fp32_decode_256_steps():
@@ -78,13 +91,19 @@ def test_config1_tiny_fp32_decode_256_steps():
         torch.cuda.synchronize()
         worst = max(worst, _oracle_decode_check(layer, ca, ci, st_o, _step_rows(si, 0), sink, invf, out[0].cpu(),
                                                 sel[0].cpu().numpy(), n_sel[0].item(), f"step {step}",
-                                                _seq_projs(run, 0)))
+                                                _seq_projs(run, 0), label="1 tiny-f32-decode-256"))
     assert run.err.item() == 0
     n = int(st_o["n_rows"][0])
     assert n == cfg.steps // cfg.ratio == st_g.n_rows.item()
     G.check_pool_rows(st_g.pool[0, :n].cpu(), st_o["pool"][0, :n], "f32", "attention pool", R=cfg.R)
     G.check_pool_rows(st_g.ikeys[0, :n].cpu(), st_o["ikeys"][0, :n], "f32", "index pool", R=cfg.R)
     G.check_pool_rows(st_g.window[0].cpu(), st_o["window"][0], "f32", "window")
+    # end to end from x: the oracle pools its own projections of the 256 tokens
+    xs = np.concatenate([f64(csa_synth.step_inputs(cfg, step).x) for step in range(cfg.steps)], axis=1)
+    for name, comp, got in (("attention pool", ca, st_g.pool), ("index pool", ci, st_g.ikeys)):
+        rows, allow = G.pool_from_x_allowance(layer, comp, xs, invf)
+        ratio, share = G.check_pool_from_x(got[0, :n].cpu(), rows, allow, what=f"{name} from x")
+        print(f"config 1 {name} from x: largest |diff| / bound {ratio:.3f}, {100 * share:.1f} % of elements differ")
     print(f"config 1: worst max-relative output error {worst:.2e}")
 
 
@@ -114,6 +133,11 @@ def test_config2_flash_build_8k_then_decode():
     G.check_pool_rows(st_g.pool[0, :2048].cpu(), st_o["pool"][0, :2048], "bf16", "attention pool", R=cfg.R)
     G.check_pool_rows(st_g.ikeys[0, :2048].cpu(), st_o["ikeys"][0, :2048], "bf16", "index pool", R=cfg.R)
     G.check_pool_rows(st_g.front_attn.cpu(), st_o["front_a"], "bf16", "attention frontier")
+    # end to end from x: the oracle pools its own projections of the 8192 tokens (derived bound)
+    for name, comp, got in (("attention pool", ca, st_g.pool), ("index pool", ci, st_g.ikeys)):
+        rows, allow = G.pool_from_x_allowance(layer, comp, x, invf)
+        ratio, share = G.check_pool_from_x(got[0, :2048].cpu(), rows, allow, what=f"{name} from x")
+        print(f"config 2 {name} from x: largest |diff| / bound {ratio:.3f}, {100 * share:.1f} % of elements differ")
     # one decode step; window ring starts empty except what decode appends
     si = csa_synth.step_inputs(cfg, 0)
     out, sel, n_sel = run.decode_step(st_g, si)
@@ -121,7 +145,7 @@ def test_config2_flash_build_8k_then_decode():
     sink = f64(csa_synth.sinks(cfg))
     # the oracle continues from ITS pools (within 2 ulps of the GPU's)
     _oracle_decode_check(layer, ca, ci, st_o, _step_rows(si, 0), sink, invf, out[0].cpu(), sel[0].cpu().numpy(),
-                         n_sel[0].item(), "config 2", _seq_projs(run, 0))
+                         n_sel[0].item(), "config 2", _seq_projs(run, 0), label="2 flash-decode-b1-ctx8k")
     assert run.err.item() == 0
 
 
@@ -150,7 +174,7 @@ def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs, overlap):
             _oracle_decode_check(layer, ca, ci, st_o[b], _step_rows(si, b), sink, invf, out[b].cpu(),
                                  None if sel is None else sel[b].cpu().numpy(),
                                  None if n_sel is None else n_sel[b].item(), f"cfg {cid} seq {b} step {step}",
-                                 _seq_projs(run, b))
+                                 _seq_projs(run, b), label=f"{cid} {cfg.name}")
     assert run.err.item() == 0
     for b in seqs:
         n = int(st_o[b]["n_rows"][0])
@@ -160,46 +184,8 @@ def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs, overlap):
         G.check_pool_rows(st_g.window[b].cpu(), st_o[b]["window"][0], "bf16", "window")
 
 
-def _check_prefill(cfg, run, host, ch, out, sel, queries):
-    """Oracle check of one prefill chunk on a single-sequence cache: every emitted row of both pools, the index
-    frontier and the window after the chunk; the selection and output of each query in ``queries``."""
-    layer = oracle_layer(cfg)
-    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
-    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
-    sink = f64(csa_synth.sinks(cfg))
-    st = _oracle_seq_state(host, 0)
-    x = f64(ch.x)
-    n0 = st["n_rows"].copy()
-    st["front_a"], st["pool"], n_a, _ = G.oracle_compress_checked(layer, ca, x, st["pos"], st["front_a"],
-                                                                  st["pool"], n0, invf, run.projs["attn"].cpu(),
-                                                                  "chunk attn")
-    st["front_i"], st["ikeys"], _, _ = G.oracle_compress_checked(layer, ci, x, st["pos"], st["front_i"], st["ikeys"],
-                                                                 n0, invf, run.projs["index"].cpu(), "chunk index")
-    T = ch.q.shape[0]
-    n = int(n_a[0])
-    lo = cfg.ctx // 4
-    q, kv, iq, iw = f64(ch.q), f64(ch.kv), f64(ch.iq), f64(ch.iw)
-    window = st["window"][0]
-    pool, ikeys = st["pool"][0], st["ikeys"][0]
-    kvr = [O.store(O.rope(kv[i], cfg.ctx + i, invf), "bf16") for i in range(T)]
-    gsel = sel.cpu().numpy()
-    gout = out.cpu()
-    worst = 0.0
-    for i in queries:
-        p = cfg.ctx + i
-        nv = O.visible_rows(layer, n, p)
-        scores = O.index_scores(layer, iq[i], iw[i], ikeys[:nv], p, invf)
-        rows = gsel[i][gsel[i] >= 0]
-        G.check_topk(rows, scores, layer.topk, nv, what=f"query {i} top-k")
-        win = [window[t % cfg.W] if t < cfg.ctx else kvr[t - cfg.ctx] for t in O.window_tokens(layer, p)]
-        keys = np.concatenate([pool[np.sort(rows)], np.stack(win)])
-        qr = O.store(O.rope(q[i], p, invf), "bf16")
-        o = O.output_rows(layer, O.attend(layer, qr, keys, sink), p, invf)
-        worst = max(worst, G.check_rows(gout[i], o, "bf16", what=f"query {i} output", R=cfg.R))
-    ring = np.array(window)
-    for t in range(max(cfg.ctx, cfg.ctx + T - cfg.W), cfg.ctx + T):
-        ring[t % cfg.W] = kvr[t - cfg.ctx]
-    return st, n, lo, ring, worst
+def _check_prefill(cfg, run, host, ch, out, sel, queries, label=None):
+    return G.check_prefill_chunk(cfg, run, host, ch, out, sel, queries, label=label)
 
 
 def test_config5_prefill_chunk_sampled_queries():
@@ -217,7 +203,7 @@ def test_config5_prefill_chunk_sampled_queries():
     rng = np.random.default_rng(0)
     queries = sorted(set([0, 1, 2, 3, 4, 126, 127, 128, 129, 151, 152, 153, 303, 304, 2047, 4094, 4095] +
                          list(rng.integers(0, cfg.T, 12))))
-    st, n, lo, ring, _ = _check_prefill(cfg, run, host, ch, out, sel, queries)
+    st, n, lo, ring, _ = _check_prefill(cfg, run, host, ch, out, sel, queries, label="5 flash-prefill-t4096-ctx64k")
     assert n == st_g.n_rows.item() == (cfg.ctx + cfg.T) // 4
     G.check_pool_rows(st_g.pool[0, lo:n].cpu(), st["pool"][0, lo:n], "bf16", "chunk pool rows", R=cfg.R)
     G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), st["ikeys"][0, lo:n], "bf16", "chunk index rows", R=cfg.R)
@@ -243,7 +229,7 @@ def test_prefill_every_query_with_late_dominant_rows():
     out, sel = run.prefill(st_g, ch, cfg.ctx)
     torch.cuda.synchronize()
     assert run.err.item() == 0
-    _, n, _, ring, worst = _check_prefill(cfg, run, host, ch, out, sel, range(cfg.T))
+    _, n, _, ring, worst = _check_prefill(cfg, run, host, ch, out, sel, range(cfg.T), label="5' prefill T300 ctx8k")
     assert n == st_g.n_rows.item()
     G.check_pool_rows(st_g.window[0].cpu(), ring, "bf16", "window after chunk")
     print(f"prefill, every query: worst max-relative output error {worst:.2e}")
@@ -273,6 +259,175 @@ def test_gpu_decode_equals_gpu_prefill():
     assert torch.equal(st_p.window, st_d.window)
     assert torch.equal(st_p.front_attn, st_d.front_attn)
     G.check_rows(torch.stack(outs).cpu(), out_p.cpu(), "bf16", what="decode vs prefill", R=cfg.R)
+
+
+@pytest.mark.parametrize("case", ["fresh_prompt", "tiny_prompt", "dense_to_sparse", "ratio128"])
+def test_prefill_fresh_prompt_crossing_and_ratio128(case):
+    """Prefill chunks beyond the long-cache workloads, every query checked against the oracle (selection, output
+    rounded and un-rounded), with the rows the chunk emits and the window ring after it:
+      * fresh_prompt: 300 tokens from an empty cache (pos0 = 0): the window fills during the chunk (queries 0-126
+        see fewer than 128 window tokens) and every query is in the dense regime (at most 75 rows visible);
+      * tiny_prompt: 7 tokens from an empty cache (one compressed row, fewer tokens than a 128-row tile);
+      * dense_to_sparse: 400 tokens after 1900: the visible rows go from 475 to 575 and pass topk = 512 at
+        query 151 (position 2051), inside the chunk;
+      * ratio128: a ratio-128 layer (no indexer, every visible row attended), 300 tokens after 262044: a window
+        of 128 tokens completes inside the chunk (row 2047 at position 262143)."""
+    base = csa_synth.CONFIGS[5]
+    if case == "fresh_prompt":
+        cfg = base.replace(ctx=0, T=300)
+    elif case == "tiny_prompt":
+        cfg = base.replace(ctx=0, T=7)
+    elif case == "dense_to_sparse":
+        cfg = base.replace(ctx=1900, T=400)
+    else:
+        cfg = csa_synth.CONFIGS[4].replace(B=1, ctx=262144 - 100, T=300)
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
+    host = csa_synth.synth_cache(cfg, cap, B=1) if cfg.ctx else csa_synth.empty_cache(cfg, cap, B=1)
+    run = G.Runner(cfg)
+    st_g = G.DevCache(host)
+    ch = csa_synth.chunk_inputs(cfg)
+    out, sel = run.prefill(st_g, ch, cfg.ctx)
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    if case == "ratio128":
+        queries = sorted(set(range(0, cfg.T, 3)) | {cfg.T - 1, 98, 99, 100, 227, 228})
+    else:
+        queries = range(cfg.T)
+    st, n, lo, ring, worst = G.check_prefill_chunk(cfg, run, host, ch, out, sel, queries,
+                                                   label=f"prefill {case} (T {cfg.T}, ctx {cfg.ctx}, ratio {cfg.ratio})")
+    assert n == st_g.n_rows.item() == (cfg.ctx + cfg.T) // cfg.ratio
+    G.check_pool_rows(st_g.pool[0, lo:n].cpu(), st["pool"][0, lo:n], "bf16", "chunk pool rows", R=cfg.R)
+    if cfg.has_indexer:
+        G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), st["ikeys"][0, lo:n], "bf16", "chunk index rows", R=cfg.R)
+        nvis = [O.visible_rows(oracle_layer(cfg), n, cfg.ctx + i) for i in range(cfg.T)]
+        dense = [i for i in range(cfg.T) if nvis[i] <= cfg.topk]
+        g_sel = sel.cpu()
+        for i in dense:  # the dense regime selects every visible row, padded with -1
+            assert g_sel[i, :nvis[i]].tolist() == list(range(nvis[i])) and (g_sel[i, nvis[i]:] == -1).all()
+    G.check_pool_rows(st_g.window[0].cpu(), ring, "bf16", "window after chunk")
+    print(f"prefill {case}: worst max-relative output error {worst:.2e}")
+
+
+def test_config5_chunk_equals_4096_decode_steps():
+    """Config 5 in full: the 4096-token chunk on the 65536-token cache as one prefill call, against the same
+    tokens decoded one at a time on the GPU (4096 decode steps through the four calls).
+
+    The two paths project the chunk's tokens with different fp32 summation orders along the hidden axis (one
+    token: split-K partials summed in split order; a 4096-token chunk: one accumulation per tile), so a few
+    projections round to neighbouring bf16 values and the pools need not be bit-identical.  Each path is held to
+    the rules of the other tests instead: its projections against the oracle's, its emitted rows against the
+    oracle pooling its own projections.  The window ring and row counts must be identical.  Where the two
+    selections of a query are the same set, the two outputs must agree within twice the output rule (each is
+    held to the rule against the oracle, and their pools may differ by those rounding flips); where they
+    differ, each set must pass the gap rule against the oracle's scores over its own path's index keys.  Both
+    paths' outputs of those queries and of 48 spread queries are checked against the oracle recomputed with
+    their own set and rows."""
+    cfg = csa_synth.CONFIGS[5]
+    cap = (cfg.ctx + cfg.T) // cfg.ratio + 4
+    host = csa_synth.synth_cache(cfg, cap)
+    run = G.Runner(cfg)
+    ch = csa_synth.chunk_inputs(cfg)
+    st_p = G.DevCache(host)
+    out_p, sel_p = run.prefill(st_p, ch, cfg.ctx)
+    proj_p = {k: v.cpu() for k, v in run.projs.items()}
+    st_d = G.DevCache(host)
+    out_d = torch.empty_like(out_p)
+    sel_d = torch.full_like(sel_p, -1)
+    proj_d = {"attn": [], "index": []}
+    for i in range(cfg.T):
+        si = csa_synth.StepInputs(x=ch.x[:, i:i + 1], q=ch.q[i:i + 1], kv=ch.kv[i:i + 1], iq=ch.iq[i:i + 1],
+                                  iw=ch.iw[i:i + 1])
+        o, s, ns = run.decode_step(st_d, si)
+        out_d[i] = o[0]
+        sel_d[i] = s[0]
+        for k in proj_d:
+            proj_d[k].append(run.projs[k])
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    assert torch.equal(st_p.window, st_d.window)
+    assert torch.equal(st_p.n_rows, st_d.n_rows)
+    proj_d = {k: torch.cat(v, dim=1).cpu() for k, v in proj_d.items()}
+    layer = oracle_layer(cfg)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    sink = f64(csa_synth.sinks(cfg))
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    x = f64(ch.x)
+    n = st_p.n_rows.item()
+    lo = cfg.ctx // cfg.ratio
+    keys_of = {}
+    for name, st_g, pr in (("prefill", st_p, proj_p), ("decode", st_d, proj_d)):
+        o = _oracle_seq_state(host, 0)
+        n0 = o["n_rows"].copy()
+        _, pool_o, _, _ = G.oracle_compress_checked(layer, ca, x, o["pos"], o["front_a"], o["pool"], n0, invf,
+                                                    pr["attn"], f"{name} attn")
+        _, ik_o, _, _ = G.oracle_compress_checked(layer, ci, x, o["pos"], o["front_i"], o["ikeys"], n0, invf,
+                                                  pr["index"], f"{name} index")
+        G.check_pool_rows(st_g.pool[0, lo:n].cpu(), pool_o[0, lo:n], "bf16", f"{name} pool rows", R=cfg.R)
+        G.check_pool_rows(st_g.ikeys[0, lo:n].cpu(), ik_o[0, lo:n], "bf16", f"{name} index rows", R=cfg.R)
+        keys_of[name] = (f64(st_g.pool[0].cpu()), f64(st_g.ikeys[0].cpu()))
+    same_pool = bool(torch.equal(st_p.pool, st_d.pool) and torch.equal(st_p.ikeys, st_d.ikeys))
+    sp, sd = torch.sort(sel_p, dim=1).values, torch.sort(sel_d, dim=1).values
+    assert (sp >= 0).all() and (sd >= 0).all()  # 16384+ rows visible: sparse throughout
+    same = (sp == sd).all(dim=1).cpu()
+    idx_same = torch.nonzero(same).flatten()
+    for k in range(0, len(idx_same), 256):
+        blk = idx_same[k:k + 256].to("cuda")
+        G.check_rows(out_p[blk].cpu(), out_d[blk].cpu(), "bf16", what="decode vs prefill", R=cfg.R, scale=2.0)
+    differ = torch.nonzero(~same).flatten().tolist()
+    n_pool_diff = int((st_p.pool != st_d.pool).sum().item() + (st_p.ikeys != st_d.ikeys).sum().item())
+    print(f"config 5 decode == prefill: pools identical: {same_pool} ({n_pool_diff} elements differ); "
+          f"{len(idx_same)} of {cfg.T} selections identical, {len(differ)} differ")
+    assert len(differ) <= cfg.T // 16, f"{len(differ)} queries selected different sets"
+    window0 = f64(host.window[0])
+    kvr = [O.store(O.rope(f64(ch.kv[i]), cfg.ctx + i, invf), "bf16") for i in range(cfg.T)]
+    sample = sorted(set(differ) | set(range(0, cfg.T, cfg.T // 48)) | {cfg.T - 1})
+    for i in sample:
+        p = cfg.ctx + i
+        nv = O.visible_rows(layer, n, p)
+        win = [window0[t % cfg.W] if t < cfg.ctx else kvr[t - cfg.ctx] for t in O.window_tokens(layer, p)]
+        qr = O.store(O.rope(f64(ch.q[i]), p, invf), "bf16")
+        for name, s_, o_ in (("prefill", sel_p, out_p), ("decode", sel_d, out_d)):
+            pool, ikeys = keys_of[name]
+            rows = s_[i].cpu().numpy()
+            if i in differ:
+                scores = O.index_scores(layer, f64(ch.iq[i]), f64(ch.iw[i]), ikeys[:nv], p, invf)
+                G.check_topk(rows, scores, cfg.topk, nv, what=f"{name} query {i} top-k")
+            keys = np.concatenate([pool[np.sort(rows)], np.stack(win)])
+            o = O.attend(layer, qr, keys, sink)
+            G.check_rows(o_[i].cpu(), O.output_rows(layer, o, p, invf), "bf16", what=f"{name} query {i}",
+                         R=cfg.R, exact=G.exact_output(o, p, invf), label=f"5 {name} path, full-chunk sample")
+
+
+def test_config3_every_sequence_four_steps():
+    """Config 3 at full size with every one of the 32 sequences checked against the oracle for four decode steps
+    (projections, selection under the gap rule, output rounded and un-rounded, emitted rows).  The GPU runs
+    first; the oracle then follows one sequence at a time, so only one sequence's float64 state is held."""
+    cfg = csa_synth.CONFIGS[3]
+    steps = 4  # the fourth token (position 32771) completes a window: one row emitted per sequence
+    cap = cfg.ctx // cfg.ratio + 8
+    host = csa_synth.synth_cache(cfg, cap)
+    run = G.Runner(cfg)
+    st_g = G.DevCache(host)
+    rec = []
+    for step in range(steps):
+        si = csa_synth.step_inputs(cfg, step)
+        out, sel, n_sel = run.decode_step(st_g, si)
+        torch.cuda.synchronize()
+        rec.append((si, out.cpu(), sel.cpu().numpy(), n_sel.cpu().numpy(),
+                    {k: v.cpu() for k, v in run.projs.items()}))
+    assert run.err.item() == 0
+    layer = oracle_layer(cfg)
+    ca, ci = oracle_comp(run.ca_host), oracle_comp(run.ci_host)
+    sink, invf = f64(csa_synth.sinks(cfg)), f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    pool_g = st_g.pool.cpu()
+    for b in range(cfg.B):
+        st_o = _oracle_seq_state(host, b)
+        for step, (si, out, sel, n_sel, projs) in enumerate(rec):
+            _oracle_decode_check(layer, ca, ci, st_o, _step_rows(si, b), sink, invf, out[b], sel[b], n_sel[b],
+                                 f"seq {b} step {step}", {k: v[b:b + 1] for k, v in projs.items()},
+                                 label=f"3 {cfg.name}")
+        lo, n = cfg.ctx // cfg.ratio, int(st_o["n_rows"][0])
+        G.check_pool_rows(pool_g[b, lo:n], st_o["pool"][0, lo:n], "bf16", f"seq {b} new pool rows", R=cfg.R)
 
 
 def _ragged_cache(cfg, cap, ctxs):
@@ -528,3 +683,30 @@ def test_host_validation_raises():
     with pytest.raises(csa.CSAError) as ei:
         csa.compress_append(run.L, run.ca, x, st.pos, st.front_attn, st.pool, st.n_rows, run.inv_freq, ws=tiny_ws)
     assert ei.value.code == 4
+
+
+def test_binding_rejects_wrong_dtype_and_shape_before_any_launch():
+    """On the device too: an fp32 query handed to a bf16 layer, or a selection of the wrong width, raises in the
+    binding and enqueues nothing (the library's launch count and the outputs stay as they were)."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=2)
+    run = G.Runner(cfg)
+    st = G.DevCache(_ragged_cache(cfg, 40, [100, 100]))
+    si = csa_synth.step_inputs(cfg, 0, B=2)
+    sel = torch.zeros(2, cfg.topk, dtype=torch.int32, device="cuda")
+    n_sel = torch.ones(2, dtype=torch.int32, device="cuda")
+    out = torch.full((2, cfg.H, cfg.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    before = csa.kernel_launches()
+    with pytest.raises(TypeError, match="q"):
+        csa.attend_decode(run.L, G.dev(si.q).float(), G.dev(si.kv), run.sink, st.window, st.pool, st.n_rows, sel,
+                          n_sel, st.pos, run.inv_freq, out, err=run.err)
+    with pytest.raises(ValueError, match="sel"):
+        csa.attend_decode(run.L, G.dev(si.q), G.dev(si.kv), run.sink, st.window, st.pool, st.n_rows, sel[:, :100],
+                          n_sel, st.pos, run.inv_freq, out, err=run.err)
+    with pytest.raises(TypeError, match="iw"):
+        csa.index_topk(run.L, G.dev(si.iq), G.dev(si.iw).float(), st.ikeys, st.n_rows, st.pos, run.inv_freq, sel,
+                       n_sel, err=run.err)
+    torch.cuda.synchronize()
+    assert csa.kernel_launches() == before
+    assert (out == 7.0).all() and run.err.item() == 0
