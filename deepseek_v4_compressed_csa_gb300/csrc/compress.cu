@@ -4,8 +4,8 @@
 // "What V4 adds" (learned gated pooling, overlapping ratio-4 / non-overlapping
 // ratio-128 windows, maintained incrementally) and "Decode path" (pool in fp32,
 // cast back before the norm); "feat: add DeepSeek-V4 (Pro/Flash) model support"
-// (mlx-lm #1189), OmarB97 "Compressed pool rows must be roped at birth" (RoPE
-// at the window start j*ratio) and stepnoy's "Fix" 3 (the chunk tail is carried
+// (mlx-lm #1189), OmarB97's RoPE fixes (a pool row is rotated when emitted, at
+// its window start j*ratio) and stepnoy's "Fix" 3 (the chunk tail is carried
 // across calls; the absolute position accumulates).
 //
 // One call = two or three launches on the caller's stream:

@@ -2,9 +2,10 @@
 // fixed-size array that lives in the library image, for callers that cannot
 // allocate device memory (see include/csa.h).  Same kernels and results as
 // csa_index_topk; only the origin of the scratch buffer differs.
-#include <atomic>
+#include <cudaTypedefs.h>
 
 #include "kernels.h"
+#include "scratch_cache.h"
 
 namespace {
 
@@ -14,21 +15,52 @@ constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB
 __device__ __align__(256) unsigned char g_csa_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+csa::ContextAddressCache<kMaxDevices> g_scratch_addr;
 
-// Device address of the scratch array on the current device, looked up once per
-// device (host code cannot use the array's name as a device pointer).
+// Unique id of the calling thread's current CUDA context, or 0 if there is none (yet) or the driver entry points
+// cannot be had.  Taken through the runtime's driver entry-point query, so the library needs no libcuda link.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* f0 = nullptr;
+    void* f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 4000, cudaEnableDefault, &q0) == cudaSuccess &&
+        q0 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f0);
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f1);
+    }
+    resolved = true;
+  }
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context.  Host code cannot use the array's name as
+// a device pointer, so the address is looked up with cudaGetSymbolAddress and cached per device together with the
+// id of the context it belongs to; after a device reset the context id changes and the address is looked up again.
 cudaError_t static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    e = cudaGetSymbolAddress(&p, g_csa_static_scratch);
-    if (e != cudaSuccess || p == nullptr) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+  void* p = nullptr;
+  if (g_scratch_addr.lookup(dev, current_context_id(), &p)) {
+    *out = p;
+    return cudaSuccess;
   }
+  e = cudaGetSymbolAddress(&p, g_csa_static_scratch);  // makes the device's primary context current if needed
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  g_scratch_addr.store(dev, current_context_id(), p);
   *out = p;
   return cudaSuccess;
 }

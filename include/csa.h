@@ -46,8 +46,9 @@
  *   - RoPE: rope dims are the LAST R dims of a row, rotated as interleaved
  *     pairs (D-R+2i, D-R+2i+1) by theta_i = (float)p * inv_freq[i] (one fp32
  *     multiply).  inv_freq is a device fp32 table of R/2 entries, so the
- *     caller chooses plain or YaRN-scaled frequencies ([mlx-lm#1189], OmarB97
- *     "RoPE regime is per layer kind": compress layers use base 160000).
+ *     caller chooses plain or YaRN-scaled frequencies ([mlx-lm#1189], OmarB97's
+ *     RoPE fixes: the rotary setting depends on the layer kind, and compress
+ *     layers use base 160000).
  */
 #ifndef CSA_H
 #define CSA_H
@@ -105,9 +106,10 @@ typedef struct {
  *   wkv, wgate [L*d, X] model dtype (out-features x in-features);
  *   ape  [ratio, L*d] fp32: absolute position embedding added to the gates;
  *   norm_w [d] fp32: RMSNorm weight.
- * Lane 0 (first d outputs) pools the previous window, lane 1 the current one
- * ([mlx-lm#1189], Thump604: "ratio-4 overlap compressor shapes ... ape
- * (4, 1024) and wkv/wgate (1024, 4096)"). */
+ * Lane 0 (first d outputs) pools the previous window, lane 1 the current one.
+ * For the Flash ratio-4 attention pool that makes ape [4, 1024] and wkv, wgate
+ * [1024, 4096] ([mlx-lm#1189], Thump604's fixes, on the overlap compressor's
+ * weight shapes). */
 typedef struct {
   const void* wkv;
   const void* wgate;
@@ -128,8 +130,8 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
  *
  * Definition ([MTPLX#216] "What V4 adds": learned gated pooling over
  * overlapping ratio-4 or non-overlapping ratio-128 windows, maintained
- * incrementally by prefill and decode alike; [mlx-lm#1189] OmarB97 "Compressed
- * pool rows must be roped at birth", stepnoy "Fix" 3: the chunk tail is carried
+ * incrementally by prefill and decode alike; [mlx-lm#1189] OmarB97's RoPE
+ * fixes: a pool row is rotated when emitted; stepnoy "Fix" 3: the chunk tail is carried
  * and the absolute position accumulates; [MTPLX#216] "Decode path": the row is
  * pooled in fp32 and cast back before the norm):
  *   for token p = pos[b] + i:  kv_p = Wkv x_p,  g_p = Wgate x_p  (model dtype)
@@ -288,7 +290,11 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
  *     holds (csa_workspace_size(..., CSA_OP_INDEX_TOPK, B, 1, cap) bytes; about
  *     B * (Hi*Di*4 + cap*4) — e.g. 32 sequences with 8400-row pools fit).
  *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current) and keeps it together with the id of the device's
+ *     CUDA context; make that first call before any stream capture.  A call in
+ *     a context other than the one the address was found in (the device was
+ *     reset and its context created again) looks it up again, since the array
+ *     may then sit elsewhere: that call too should come before any capture.
  *   - Every call on a device shares the one array: calls whose kernels overlap
  *     on the GPU (different streams without ordering) race on it.  Calls in one
  *     stream are ordered and safe.  Nothing in the array needs to start at zero;

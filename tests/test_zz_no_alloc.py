@@ -2,7 +2,11 @@
 
 Its scratch is a fixed array inside the library instead of a caller workspace.  It must select
 exactly the rows csa_index_topk selects (the same integer result), call after call, although the
-array keeps the previous call's contents.  This file is named to be collected last.
+array keeps the previous call's contents, and it must not take device memory: the device's free
+memory (as the driver reports it, so an allocation by the library itself would show, not only one
+through torch's allocator) is the same before and after a call.  The first call on a device may
+load the library's module that holds the array (the driver loads modules lazily), so the strict
+check is on the second call.  This file is named to be collected last.
 """
 import pytest
 import torch
@@ -38,9 +42,15 @@ def test_static_scratch_index_matches_workspace_version():
         nsel = torch.full((B,), -7, dtype=torch.int32, device="cuda")
         torch.cuda.synchronize()
         before = torch.cuda.memory_allocated()
+        free_before = torch.cuda.mem_get_info()[0]
         csa.index_topk_static(L, iq, iw, st.ikeys, st.n_rows, st.pos, invf, sel, nsel, err=err)
         torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
         assert torch.cuda.memory_allocated() == before
+        if call == 0:  # at most the array itself, if this call made the driver load its module
+            assert free_before - free_after <= csa.static_scratch_bytes() + (4 << 20)
+        else:
+            assert free_after == free_before, f"device free memory fell by {free_before - free_after} bytes"
         assert err.item() == 0
         assert torch.equal(nsel, nsel_ref) and (nsel == cfg.topk).all()  # sparse regime: 8192 rows visible
         assert torch.equal(sel, sel_ref)
