@@ -39,6 +39,31 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum, every kernel captured cold) of one decode
+# layer-step of the headline workload and of one prefill chunk, with the hash of the kernel sources the counters
+# were taken on (csrc_digest()); the bench reports them only while the sources still hash the same.
+TRAFFIC = {"csrc_sha256": "925e82e22b2fbf16", "decode_layer_step_bytes": 133_434_000, "prefill_chunk_bytes": 1_232_673_000,
+           "profile": "profiles/traffic_decode_b32_ctx32k_and_prefill_t4096.md"}
+
+
+def csrc_digest() -> str:
+    """sha256 (first 16 hex digits) of the library's kernel sources."""
+    import hashlib
+    d = os.path.join(ROOT, "deepseek_v4_compressed_csa_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(key: str, units: int):
+    if TRAFFIC.get(key) is None or TRAFFIC.get("csrc_sha256") != csrc_digest():
+        return None
+    return int(TRAFFIC[key] * units)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -100,48 +125,93 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(cid: int, budget_s: float, max_steps: int) -> dict:
-    """Time the CPU oracle on one sequence of the workload, stepping until the budget is spent.
-    Runs in its own process with single-threaded BLAS."""
+def oracle_sample(cid: int, seqs: list[int], warmup: int, steps: int, budget_s: float) -> dict:
+    """Time the CPU oracle stepping sequences ``seqs`` of workload ``cid`` through ``warmup`` untimed and up to
+    ``steps`` timed decode steps (stopping early once ``budget_s`` of timed work is spent).  Runs in its own
+    process with single-threaded BLAS; returns the per-step times (the sum over its sequences)."""
     import numpy as np
 
     import csa_synth
     from oracle import csa_oracle as O
     cfg = csa_synth.CONFIGS[cid]
-    cap = cfg.ctx // cfg.ratio + max_steps // cfg.ratio + 8
-    host = csa_synth.synth_cache(cfg, cap, B=1)
+    cap = cfg.ctx // cfg.ratio + (warmup + steps) // cfg.ratio + 8
+    host = csa_synth.synth_cache(cfg, cap, B=max(seqs) + 1)
     f = lambda t: None if t is None else t.float().numpy().astype(np.float64)  # noqa: E731
     layer = O.Layer(dtype=cfg.dtype, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
                     topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
     comp = lambda c: O.Compressor(wkv=f(c.wkv), wgate=f(c.wgate), ape=f(c.ape), norm_w=f(c.norm_w), d=c.d)  # noqa
     ca = comp(csa_synth.compressor(cfg, "attn"))
     ci = comp(csa_synth.compressor(cfg, "index")) if cfg.has_indexer else None
-    st = dict(pool=f(host.pool), ikeys=f(host.ikeys), window=f(host.window), front_a=f(host.front_attn),
-              front_i=f(host.front_index), n_rows=host.n_rows.numpy().astype(np.int64),
-              pos=host.pos.numpy().astype(np.int64))
+    sl = lambda t, b: None if t is None else f(t[b:b + 1])  # noqa: E731
+    states = {b: dict(pool=sl(host.pool, b), ikeys=sl(host.ikeys, b), window=sl(host.window, b),
+                      front_a=sl(host.front_attn, b), front_i=sl(host.front_index, b),
+                      n_rows=host.n_rows[b:b + 1].numpy().astype(np.int64),
+                      pos=host.pos[b:b + 1].numpy().astype(np.int64)) for b in seqs}
+    del host
     sink, invf = f(csa_synth.sinks(cfg)), csa_synth.inv_freq(cfg).numpy()
     times = []
-    t_all = time.perf_counter()
-    for step in range(max_steps):
-        si = csa_synth.step_inputs(cfg, step, B=1)
+    spent = 0.0
+    for step in range(warmup + steps):
+        si = csa_synth.step_inputs(cfg, step, B=max(seqs) + 1)
         t0 = time.perf_counter()
-        O.decode_step(layer, ca, ci, st, (f(si.x), f(si.q), f(si.kv), f(si.iq), f(si.iw)), sink, invf)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_all > budget_s:
-            break
-    per_seq = statistics.mean(times)
-    return {"seq_step_s": per_seq, "steps": len(times), "B": cfg.B,
-            "layer_steps_per_s": 1.0 / (per_seq * cfg.B)}
+        for b in seqs:
+            O.decode_step(layer, ca, ci, states[b], (sl(si.x, b), sl(si.q, b), sl(si.kv, b), sl(si.iq, b),
+                                                     sl(si.iw, b)), sink, invf)
+        dt = time.perf_counter() - t0
+        if step >= warmup:
+            times.append(dt)
+            spent += dt
+            if spent > budget_s:
+                break
+    return {"times": times, "seqs": list(seqs)}
 
 
-def run_oracle_subprocess(cid: int, budget_s: float, max_steps: int) -> dict:
+def cpu_info() -> dict:
+    """Host core count and CPU model (for the CPU-baseline figures)."""
+    import platform
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            k = line.split(":")[0].strip().lower()
+            if k in ("model name", "cpu model", "hardware") and ":" in line:
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith(("model name", "vendor id")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine(),
+            "arch": platform.machine()}
+
+
+def run_oracle_processes(cid: int, groups: list[list[int]], warmup: int, steps: int, budget_s: float) -> dict:
+    """The oracle on len(groups) host cores at once: one process per group of sequences (spawned as fresh
+    interpreters, single-threaded BLAS each), all stepping the same decode steps.  A layer-step's time is the
+    slowest process's time for that step (as if the processes met at a barrier after each step)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(cid), str(budget_s), str(max_steps)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 4 * budget_s))
-    if r.returncode != 0:
-        raise RuntimeError(f"oracle sample failed:\n{r.stderr[-2000:]}")
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    procs = []
+    for g in groups:
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(cid), ",".join(map(str, g)),
+               str(warmup), str(steps), str(budget_s)]
+        procs.append(subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env))
+    results = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=max(900, 6 * budget_s))
+        if pr.returncode != 0:
+            raise RuntimeError(f"oracle sample failed:\n{err[-2000:]}")
+        results.append(json.loads(out.strip().splitlines()[-1]))
+    n = min(len(r["times"]) for r in results)
+    per_step = [max(r["times"][i] for r in results) for i in range(n)]
+    return {"step_s": per_step, "steps": n, "processes": len(groups),
+            "sequences": sum(len(r["seqs"]) for r in results)}
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -255,6 +325,11 @@ class DecodeWorkload:
         import torch
         csa = self.csa
         main = torch.cuda.current_stream()
+        if not self.cfg.has_indexer:
+            # a layer without an indexer (ratio 128): its one compress call, then attention, on one stream
+            csa.compress_append(self.L, self.ca, inp["x"], self.pos, self.front_a, self.pool, self.n_a, self.invf,
+                                ws=self.ws_c, err=self.err)
+            return
         if self.cfg.has_indexer and self.serial_indexer and self.pair:
             # both pools in one call (one projection grid, one pooling launch), then the indexer: one stream, so
             # every kernel of the step follows its predecessor by programmatic launch
@@ -341,12 +416,13 @@ class ModelStep:
     other layers of a model), one shared position tensor advanced once after the last layer.  Each step is one
     CUDA graph replay holding every layer."""
 
-    def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True):
+    def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True, host=None):
         import torch
 
         import csa_synth
-        host = csa_synth.synth_cache(cfg, cap)
-        host_comp = (csa_synth.compressor(cfg, "attn"), csa_synth.compressor(cfg, "index"))
+        host = csa_synth.synth_cache(cfg, cap) if host is None else host
+        host_comp = (csa_synth.compressor(cfg, "attn"),
+                     csa_synth.compressor(cfg, "index") if cfg.has_indexer else None)
         self.layers = []
         pos = None
         for i in range(n_layers):
@@ -405,6 +481,78 @@ def step_bytes(cfg, n_rows_mean: float) -> dict:
             "total": w + keys + rows + qo + small + fr}
 
 
+def time_model_steps(ms, first: int, steps: int, flush) -> list[float]:
+    """CUDA-event times (ms) of `steps` model steps (graph replays), the L2 flushed before each, outside the events."""
+    import torch
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk()) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ms.replay(first + i, ev=ev[i])
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def built_cache_b1(csa, csa_synth, cfg, cap, dev):
+    """Config 2's cache: 8192 seeded hidden tokens compressed into both pools by the library (one chunk call per
+    pool) from an empty cache, copied back as a host cache; the window ring stays as decode will fill it."""
+    import torch
+    host = csa_synth.empty_cache(cfg, cap)
+    d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
+                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+    x = d(csa_synth.hidden(cfg, cfg.prefill_tokens))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = {k: d(getattr(host, k)) for k in ("pool", "ikeys", "front_attn", "front_index", "n_rows", "pos")}
+    n_i = st["n_rows"].clone()
+    for which, front, pool, n in (("attn", "front_attn", "pool", st["n_rows"]), ("index", "front_index", "ikeys", n_i)):
+        c = csa_synth.compressor(cfg, which)
+        comp = csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
+        csa.compress_append(L, comp, x, st["pos"], st[front], st[pool], n, d(csa_synth.inv_freq(cfg)), err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0 and int(st["n_rows"][0]) == cfg.prefill_tokens // cfg.ratio
+    for k in ("pool", "ikeys", "front_attn", "front_index", "n_rows"):
+        getattr(host, k).copy_(st[k].cpu())
+    host.pos[:] = cfg.prefill_tokens
+    return host
+
+
+def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup: int, nl: int) -> dict:
+    """Throughput and HBM fraction of another decode workload as a model step of `nl` layers (config 2: B = 1
+    on an 8K cache the library compressed from seeded hidden states; config 4: ratio 128, B = 16, 256K context,
+    every row attended), timed like the headline."""
+    cfg = csa_synth.CONFIGS[cid]
+    n_ctx = cfg.prefill_tokens if cid == 2 else cfg.ctx
+    cap = n_ctx // cfg.ratio + (warmup + steps + 8) // cfg.ratio + 8
+    host = built_cache_b1(csa, csa_synth, cfg, cap, dev) if cid == 2 else None
+    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, host=host)
+    wl = ms.layers[0]
+    ms.step(0)
+    ms.capture()
+    for i in range(warmup):
+        ms.replay(1 + i)
+    n0 = wl.n_a.float().mean().item()
+    t = time_model_steps(ms, 1 + warmup, steps, flush)
+    n1 = wl.n_a.float().mean().item()
+    for layer in ms.layers:
+        assert layer.err.item() == 0, f"device error word {layer.err.item()}"
+    per = [x / nl for x in t]
+    mean_ms = statistics.mean(per)
+    nb = step_bytes(cfg, 0.5 * (n0 + n1))
+    hbm, _, _ = _peaks()
+    gbs = nb["total"] / (mean_ms / 1e3) / 1e9
+    del ms
+    return {"workload": cfg.name, "B": cfg.B, "context": n_ctx, "ratio": cfg.ratio, "compressed_rows": [n0, n1],
+            "layer_steps_per_s": round(1e3 / mean_ms, 1), "tokens_per_s": round(cfg.B * 1e3 / mean_ms, 1),
+            "us_per_layer_step": round(1e3 * mean_ms, 2),
+            "us_per_layer_step_p10_p50_p90": [round(1e3 * x, 2) for x in _percentiles(per)],
+            "step_algorithmic_bytes": int(nb["total"]), "achieved_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm, 4), "layers_per_step": nl, "steps": steps,
+            "cache": ("compressed from 8192 seeded hidden tokens by the library" if cid == 2 else
+                      "synthetic rows drawn directly (seeded N(0,1))")}
+
+
 def run_ours(args):
     import torch
     dist, rank, world, local = _dist()
@@ -449,7 +597,8 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = _max_over_ranks(dist, sum(e[0].elapsed_time(e[1]) for e in ev), dev)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = _max_over_ranks(dist, sum(step_ms), dev)
     for layer in ms.layers:
         assert layer.err.item() == 0, f"device error word {layer.err.item()}"
     n_end = wl.n_a.float().mean().item()
@@ -534,6 +683,16 @@ def run_ours(args):
     if not args.no_prefill:
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
 
+    # ---- the other decode workloads (configs 2 and 4), each as its own model step of nl layers
+    others = None
+    if not args.no_other_configs:
+        del ms, wl
+        torch.cuda.empty_cache()
+        others = {}
+        for cid in (2, 4):
+            line = decode_config_line(csa, csa_synth, cid, dev, flush, args.steps, args.warmup, nl)
+            others[line["workload"]] = line
+
     hbm, tflops, peak_src = _peaks()
     ms_per_step = total_ms / (args.steps * nl)  # per layer-step
     value = world * args.steps * nl / (total_ms / 1e3)
@@ -541,7 +700,7 @@ def run_ours(args):
     step_avg_s = ms_per_step / 1e3
     result = None
     if rank == 0:
-        cpu = run_oracle_subprocess(3, args.cpu_budget, 400)
+        cpu = cpu_baseline(cfg, args.cpu_budget)
         result = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -556,6 +715,7 @@ def run_ours(args):
                 "step_hbm_frac": round(nb["total"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
                 "layers_per_step": nl,
                 "layer_steps_timed": args.steps * nl,
+                "ms_per_layer_step_p10_p50_p90": [round(x / nl, 5) for x in _percentiles(step_ms)],
                 "model_step": (f"each timed step is one decode step of {nl} layers (distinct weights, caches, inputs "
                                f"and workspaces: {nl} x ~0.4 GB, every layer's data cold in HBM as after the other "
                                "layers of a model), one CUDA graph replay; value = layer-steps / time; positions "
@@ -571,6 +731,7 @@ def run_ours(args):
                            "csa_index_topk, csa_attend_decode, every kernel after its predecessor by programmatic "
                            "launch; csa_advance_positions after the last layer"),
                 "prefill": prefill,
+                "other_decode_workloads": others,
             },
             "roofline": {
                 "kernel": (f"model step graph: every kernel of one decode step of {nl} layers (per layer: both "
@@ -578,15 +739,17 @@ def run_ours(args):
                            "bytes per layer = weights + index keys + attended rows + q/out + small terms"),
                 "bound": "hbm",
                 "achieved": round(nb["total"] / step_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(nb["total"] / step_avg_s / 1e9 / hbm, 4), "traffic": None,
+                "frac": round(nb["total"] / step_avg_s / 1e9 / hbm, 4),
+                "traffic": _traffic("decode_layer_step_bytes", nl),
+                "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum summed over one layer-step's "
+                                   f"kernels x {nl} layers ({TRAFFIC['profile']})" if _traffic(
+                                       "decode_layer_step_bytes", nl) else
+                                   "null: no counters taken on the current kernel sources"),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6800 GB/s", "avg_launch_ms": round(total_ms / args.steps, 5),
                 "algorithmic_bytes_per_launch": int(nb["total"] * nl),
             },
-            "cpu_baseline": {"value": round(cpu["layer_steps_per_s"], 5), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"1 of {cfg.B} sequences x {cpu['steps']} decode steps of the same workload, "
-                                       f"float64 numpy oracle, single-threaded BLAS; per-layer-step time = "
-                                       f"{cfg.B} x per-sequence time"},
+            "cpu_baseline": cpu,
             "e2e": {"value": round(world * nl * 1e3 / e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": round(d2h / nl),
                     "per_model_step": {"layers": nl, "h2d_copies": nl, "h2d_bytes": h2d * nl, "d2h_bytes": d2h},
@@ -648,30 +811,80 @@ def run_prefill(csa, csa_synth, dev, flush, repeats: int):
              cfg.T * cfg.X * (2 * 2 * (cfg.D + cfg.Di)) * 2)
     _, tflops, _ = _peaks()
     return {"workload": cfg.name, "tok_per_s": round(cfg.T / (ms / 1e3), 1), "ms_per_chunk": round(ms, 4),
+            "ms_per_chunk_p10_p50_p90": [round(x, 4) for x in _percentiles(times)],
             "algorithmic_tflop": round(flops / 1e12, 4),
-            "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats}
+            "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats,
+            "dram_traffic_bytes": _traffic("prefill_chunk_bytes", 1)}
+
+
+def cpu_baseline(cfg, budget_s: float) -> dict:
+    """The float64 oracle on this host, on bounded samples of the headline workload: one core stepping one of the
+    32 sequences (the primary figure, scaled x32 to a layer-step), and every core at once (one process per core,
+    the 32 sequences split between them, whole layer-steps)."""
+    info = cpu_info()
+    one = run_oracle_processes(3, [[0]], 1, 400, budget_s)
+    per_seq = statistics.mean(one["step_s"])
+    P = max(1, min(info["nproc"] or 1, cfg.B))
+    groups = [list(range(cfg.B))[k::P] for k in range(P)]
+    allc = run_oracle_processes(3, groups, 1, 40, budget_s / 2)
+    all_step = statistics.mean(allc["step_s"])
+    return {"value": round(1.0 / (per_seq * cfg.B), 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"1 of {cfg.B} sequences x {one['steps']} decode steps of the same workload (after one "
+                      f"untimed step), float64 numpy oracle, single-threaded BLAS; per-layer-step time = {cfg.B} x "
+                      f"the per-sequence time ({1e3 * per_seq:.2f} ms)",
+            "nproc": info["nproc"], "cpu_model": info["cpu_model"], "arch": info["arch"],
+            "all_cores": {"value": round(1.0 / all_step, 5), "unit": UNIT, "cores": P,
+                          "sample": f"all {cfg.B} sequences x {allc['steps']} layer-steps (after one untimed), "
+                                    f"{P} processes of single-threaded BLAS, each stepping {cfg.B // P}-"
+                                    f"{-(-cfg.B // P)} sequences; a layer-step = the slowest process's step",
+                          "ms_per_layer_step": round(1e3 * all_step, 3)}}
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args):
+    """The reference arm: the float64 CPU oracle on the host cores, on the same workload (config 3, B = 32): W
+    untimed and K timed layer-steps, each advancing all 32 sequences by one token, the sequences split over one
+    single-threaded process per core (up to 32).  Under torchrun only rank 0 runs it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    budget = max(5.0, min(120.0, 2.0 * (args.steps + args.warmup)))
-    r = run_oracle_subprocess(3, budget, args.warmup + args.steps)
-    value = r["layer_steps_per_s"]
+    import csa_synth
+    cfg = csa_synth.CONFIGS[3]
+    info = cpu_info()
+    P = max(1, min(info["nproc"] or 1, cfg.B))
+    groups = [list(range(cfg.B))[k::P] for k in range(P)]
+    r = run_oracle_processes(3, groups, args.warmup, args.steps, 3600.0)
+    step_s = r["step_s"]
+    ms = 1e3 * statistics.mean(step_s)
+    value = 1e3 / ms
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
-        "steps": r["steps"], "warmup": 0, "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+        "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "flash-decode-b32-ctx32k", "global_batch": 32, "seq_len": 32768},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"1 of 32 sequences x {r['steps']} decode steps (float64 numpy oracle, "
-                                   "single-threaded BLAS), scaled x32 to a layer-step"},
+        "config": {"workload": cfg.name, "global_batch": cfg.B, "seq_len": cfg.ctx,
+                   "step": f"one decode layer-step: all {cfg.B} sequences advance one token through the four calls",
+                   "ms_per_step_p10_p50_p90": [round(1e3 * x, 3) for x in _percentiles(step_s)]},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": P, "kind": "oracle",
+                         "sample": f"all {cfg.B} sequences x {r['steps']} layer-steps after {args.warmup} untimed, "
+                                   f"float64 numpy oracle, {P} single-threaded processes (the sequences split "
+                                   "between them); a layer-step = the slowest process's step",
+                         "nproc": info["nproc"], "cpu_model": info["cpu_model"], "arch": info["arch"]},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def _percentiles(xs, qs=(10, 50, 90)):
+    v = sorted(xs)
+    if not v:
+        return [None for _ in qs]
+    out = []
+    for q in qs:
+        k = (len(v) - 1) * q / 100.0
+        lo, hi = int(k), min(int(k) + 1, len(v) - 1)
+        out.append(v[lo] + (v[hi] - v[lo]) * (k - lo))
+    return out
 
 
 def main():
@@ -683,6 +896,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--prefill-repeats", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the config-2 (B = 1, 8K) and config-4 (ratio 128, B = 16, 256K) decode lines")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
     ap.add_argument("--layers", type=int, default=8,
                     help="layers per model step (each its own weights and caches), one CUDA graph per step")
@@ -692,7 +907,7 @@ def main():
                     help="run csa_index_topk_overlapped beside the index pool's compress call instead of "
                          "csa_index_topk after it on one stream")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--oracle-sample", nargs=3, default=None)
+    ap.add_argument("--oracle-sample", nargs=5, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the 4096-token prefill chunk (for profiling its kernels); prints its record")
     args = ap.parse_args()
@@ -705,8 +920,9 @@ def main():
         print(json.dumps(run_prefill(csa, csa_synth, dev, flush, args.prefill_repeats)))
         return
     if args.oracle_sample:
-        cid, budget, mx = args.oracle_sample
-        print(json.dumps(oracle_sample(int(cid), float(budget), int(mx))))
+        cid, seqs, warmup, steps, budget = args.oracle_sample
+        print(json.dumps(oracle_sample(int(cid), [int(b) for b in seqs.split(",")], int(warmup), int(steps),
+                                       float(budget))))
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
