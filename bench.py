@@ -250,6 +250,7 @@ class DecodeWorkload:
         import deepseek_v4_compressed_csa_gb300 as csa
         self.cfg, self.cap, self.dev = cfg, cap, device
         self.serial_indexer = serial_indexer
+        self.one_stream_overlap = False
         # where the main stream joins the attention pool's compress call (one-stream indexer order): before the
         # indexer, or after it (then attention has two predecessors)
         self.join_before_index = False
@@ -319,7 +320,7 @@ class DecodeWorkload:
     def front(self, inp):
         """Phase 1: both pools' compress call (csa_compress_append_pair) and the indexer on one stream; with
         pair off, the attention pool's compress call on a side stream and, on the main stream, the index pool's
-        call and the indexer (or, with overlapped_indexer, the index pool's call on a second side stream and
+        call and the indexer (or, with serial_indexer off, the index pool's call on a second side stream and
         csa_index_topk_overlapped beside it, its selection waiting for that call's event).  Each concurrent
         call has its own workspace."""
         import torch
@@ -332,11 +333,17 @@ class DecodeWorkload:
             return
         if self.cfg.has_indexer and self.serial_indexer and self.pair:
             # both pools in one call (one projection grid, one pooling launch), then the indexer: one stream, so
-            # every kernel of the step follows its predecessor by programmatic launch
+            # every kernel of the step follows its predecessor by programmatic launch.  With one_stream_overlap the
+            # indexer is csa_index_topk_overlapped without an event: its scan of the rows complete before the token
+            # runs beside the projection and pooling kernels
             csa.compress_append_pair(self.L, self.ca, self.ci, inp["x"], self.pos, self.front_a, self.pool, self.n_a,
                                      self.front_i, self.ikeys, self.n_i, self.invf, ws=self.ws_pair, err=self.err)
-            csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
-                           self.n_sel, ws=self.ws_i, err=self.err)
+            if self.one_stream_overlap:
+                csa.index_topk_overlapped(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf,
+                                          self.sel, self.n_sel, ws=self.ws_i, err=self.err)
+            else:
+                csa.index_topk(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
+                               self.n_sel, ws=self.ws_i, err=self.err)
             return
         self.side.wait_stream(main)
         with torch.cuda.stream(self.side):
@@ -416,7 +423,8 @@ class ModelStep:
     other layers of a model), one shared position tensor advanced once after the last layer.  Each step is one
     CUDA graph replay holding every layer."""
 
-    def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True, host=None):
+    def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True, host=None,
+                 one_stream_overlap: bool = False):
         import torch
 
         import csa_synth
@@ -429,6 +437,7 @@ class ModelStep:
             wl = DecodeWorkload(cfg, cap, n_inputs, device, serial_indexer=True, host=host, host_comp=host_comp,
                                 pos=pos, input_tag=1000 * i)
             wl.pair = wl.pair and pair
+            wl.one_stream_overlap = one_stream_overlap
             pos = wl.pos
             self.layers.append(wl)
         self.pos, self.csa, self.n_inputs = pos, self.layers[0].csa, n_inputs
@@ -518,7 +527,8 @@ def built_cache_b1(csa, csa_synth, cfg, cap, dev):
     return host
 
 
-def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup: int, nl: int) -> dict:
+def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup: int, nl: int,
+                       overlap: bool = False) -> dict:
     """Throughput and HBM fraction of another decode workload as a model step of `nl` layers (config 2: B = 1
     on an 8K cache the library compressed from seeded hidden states; config 4: ratio 128, B = 16, 256K context,
     every row attended), timed like the headline."""
@@ -526,7 +536,7 @@ def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup:
     n_ctx = cfg.prefill_tokens if cid == 2 else cfg.ctx
     cap = n_ctx // cfg.ratio + (warmup + steps + 8) // cfg.ratio + 8
     host = built_cache_b1(csa, csa_synth, cfg, cap, dev) if cid == 2 else None
-    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, host=host)
+    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, host=host, one_stream_overlap=overlap)
     wl = ms.layers[0]
     ms.step(0)
     ms.capture()
@@ -566,7 +576,8 @@ def run_ours(args):
     n_single = args.steps  # the one-layer comparison run (layer 0 alone, one graph per layer-step)
     total_steps = args.warmup + args.steps + args.e2e_steps + 2 * (args.warmup + n_single) + 24
     cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
-    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, pair=not args.two_streams)
+    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, pair=not args.two_streams,
+                   one_stream_overlap=args.indexer == "overlap")
     wl = ms.layers[0]
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -690,7 +701,8 @@ def run_ours(args):
         torch.cuda.empty_cache()
         others = {}
         for cid in (2, 4):
-            line = decode_config_line(csa, csa_synth, cid, dev, flush, args.steps, args.warmup, nl)
+            line = decode_config_line(csa, csa_synth, cid, dev, flush, args.steps, args.warmup, nl,
+                                      overlap=args.indexer == "overlap")
             others[line["workload"]] = line
 
     hbm, tflops, peak_src = _peaks()
@@ -728,8 +740,12 @@ def run_ours(args):
                                   "attention), events between them; each includes its graph's launch latency"),
                 "launch": ("kernels launched one by one" if args.eager else
                            "each model step = 1 CUDA graph replay; per layer one stream: csa_compress_append_pair, "
-                           "csa_index_topk, csa_attend_decode, every kernel after its predecessor by programmatic "
-                           "launch; csa_advance_positions after the last layer"),
+                           + ("csa_index_topk_overlapped (no event: its scan of the rows complete before the token "
+                              "runs beside the projection and pooling kernels), " if args.indexer == "overlap" else
+                              "csa_index_topk, ") +
+                           "csa_attend_decode, every kernel after its predecessor by programmatic launch; "
+                           "csa_advance_positions after the last layer"),
+                "indexer": args.indexer,
                 "prefill": prefill,
                 "other_decode_workloads": others,
             },
@@ -903,9 +919,9 @@ def main():
                     help="layers per model step (each its own weights and caches), one CUDA graph per step")
     ap.add_argument("--two-streams", action="store_true",
                     help="the two compress calls separately, the attention pool's on a side stream")
-    ap.add_argument("--overlapped-indexer", action="store_true",
-                    help="run csa_index_topk_overlapped beside the index pool's compress call instead of "
-                         "csa_index_topk after it on one stream")
+    ap.add_argument("--indexer", choices=["serial", "overlap"], default="serial",
+                    help="after csa_compress_append_pair on the same stream: csa_index_topk (serial) or "
+                         "csa_index_topk_overlapped without an event, whose scan runs beside the compress kernels")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--oracle-sample", nargs=5, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--prefill-only", action="store_true",

@@ -488,26 +488,32 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
                                                    int32_t* __restrict__ n_sel, const __nv_bfloat16* __restrict__ qr,
                                                    const float* __restrict__ w, const __nv_bfloat16* __restrict__ keys) {
   pdl_trigger();
-  pdl_wait();
   __shared__ int hist[3][2048];  // pass n counts into hist[n] and clears the next pass's bins
-  __shared__ int warp_tot[32];
+  __shared__ int warp_tot[32], warp_tot2[32];
   __shared__ float part[2][64];
   __shared__ float new_score[2];
   const int q = blockIdx.x, bseq = query_seq(pos, q);
+  // The position is a step input (no kernel of the step writes it), so the most rows this query can see, and so
+  // this thread's rows, are known before the wait: the score loads then go out in the same round as n_rows.
   const int p = query_pos(pos, pos0, q);
-  const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
+  const int nv_max = max(0, min(cap, (p + 1) / ratio));
+  const int K = max(1, (nv_max + 1023) >> 10);
+  const int r0 = threadIdx.x * K;
+  const float* sc = scores + (size_t)q * cap + r0;
+  pdl_wait();
+  float fk[kTopkRegKeys];
+#pragma unroll
+  for (int i = 0; i < kTopkRegKeys; ++i) fk[i] = (i < K && r0 + i < nv_max) ? __ldg(sc + i) : 0.f;
+  const int nvis = min(min(n_rows[bseq], cap), nv_max);
   int32_t* out = sel + (size_t)q * topk;
   if (nvis <= topk) {
     for (int i = threadIdx.x; i < topk; i += blockDim.x) out[i] = (i < nvis) ? i : -1;
     if (threadIdx.x == 0) n_sel[q] = max(nvis, 0);
     return;
   }
-  const int K = (nvis + 1023) >> 10;
-  const int r0 = threadIdx.x * K;
-  const float* sc = scores + (size_t)q * cap + r0;
   uint32_t uk[kTopkRegKeys];
 #pragma unroll
-  for (int i = 0; i < kTopkRegKeys; ++i) uk[i] = (i < K && r0 + i < nvis) ? ord_key(__ldg(sc + i)) : 0u;
+  for (int i = 0; i < kTopkRegKeys; ++i) uk[i] = (i < K && r0 + i < nvis) ? ord_key(fk[i]) : 0u;
   if (qr) {
     const int j0 = min(cap, p / ratio), jl = min(n_rows[bseq], cap) - 1;
     const int jr[2] = {j0 < nvis ? j0 : -1, (jl >= 0 && jl < nvis && jl != j0) ? jl : -1};
@@ -557,11 +563,27 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
     eq += (v && uk[i] == prefix) ? 1 : 0;
   }
   const int packed = (gt << 16) | eq;
-  const int incl = block_incl_scan(packed, warp_tot);
-  const int before = incl - packed;
+  // one block barrier: every warp scans the 32 warp totals itself
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = packed;
+#pragma unroll
+  for (int o2 = 1; o2 < 32; o2 <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o2);
+    if (lane >= o2) incl += n;
+  }
+  if (lane == 31) warp_tot2[wid] = incl;
+  __syncthreads();
+  int wt = warp_tot2[lane];
+#pragma unroll
+  for (int o2 = 1; o2 < 32; o2 <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, wt, o2);
+    if (lane >= o2) wt += n;
+  }
+  const int before = (wid > 0 ? __shfl_sync(0xffffffffu, wt, (wid + 31) & 31) : 0) + incl - packed;
+  const int all = __shfl_sync(0xffffffffu, wt, 31);
   const int eq_before = before & 0xffff;
   int o = (before >> 16) + min(eq_before, need);
-  const int total = (warp_tot[31] >> 16) + min(warp_tot[31] & 0xffff, need);
+  const int total = (all >> 16) + min(all & 0xffff, need);
   int eq_rank = eq_before;
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) {

@@ -50,7 +50,8 @@ constexpr int kPPart = kCR * 128;        // P^T part: 160 rows x 64 heads, MN-ma
 constexpr int kMainWarps = kCR / 32;     // gather / softmax threads: one per row (warps 0-4)
 constexpr int kMain = 32 * kMainWarps;
 constexpr int kMmaWarp = kMainWarps;     // TMEM owner and MMA issuer
-constexpr int kThreads = kMain + 32;
+constexpr int kEpiWarps = 8;             // epilogue: every warp, two per TMEM lane quarter (warps 6-7 join there)
+constexpr int kThreads = 32 * kEpiWarps;
 constexpr int kTmemCols = 512;           // S^T (cols 0-127), then O^T over all 512 (hi | lo per 128-dim tile)
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -174,13 +175,26 @@ __device__ __forceinline__ void rope8(uint4& raw, int c, const float* rcos, cons
   }
 }
 
+// 2^x by the hardware approximation (relative error ~2^-22; results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // probabilities of one row into both P^T parts (MN-major, 128-byte swizzle); returns them in pe (fp32)
 __device__ __forceinline__ void write_p(uint8_t* pbuf, int row, const float (&sv)[64], const float* mref,
                                         float (&pe)[64]) {
 #pragma unroll
-  for (int h = 0; h < 64; ++h) {
-    const float ref = mref[h] == -INFINITY ? 0.f : mref[h];
-    pe[h] = sv[h] == -INFINITY ? 0.f : exp2f(sv[h] - ref);
+  for (int h4 = 0; h4 < 16; ++h4) {
+    const float4 r4 = reinterpret_cast<const float4*>(mref)[h4];
+    const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int h = 4 * h4 + k;
+      const float ref = rr[k] == -INFINITY ? 0.f : rr[k];
+      pe[h] = sv[h] == -INFINITY ? 0.f : ex2_approx(sv[h] - ref);
+    }
   }
   uint8_t* dst = pbuf + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   }
   Item it = make_item(a);
   const uint32_t r_base = tc::smem_u32(rows), q_base = tc::smem_u32(qbuf);
-  if (warp != kMmaWarp) {
+  if (warp < kMainWarps) {
     // ---- before the programmatic wait: the query block, the RoPE table, this split's window rows and the new
     // token (step inputs and the window ring, which no kernel of this step writes before this one)
     const int row = tid;
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     }
     __syncwarp();
     failed = __shfl_sync(0xffffffffu, (int)failed, 0) != 0;
-  } else {
+  } else if (warp < kMainWarps) {
     // ------------------------------------------------------------ main warps (160 threads, one per row)
     const int row = tid;
     // ---- the selection share: codes of rows nw .. 159 (empty past nr), then their copies
@@ -432,63 +446,68 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     } while (false);
     tc::cp_async_wait_all();
     tc::named_bar(1, kMain);
-    if (!failed && warp < 4) {
-      // ---- epilogue (warps 0-3): thread owns latent dim d = 128 m + tid of each O^T tile; O = hi + lo parts
-      auto load_o = [&](int m, float (&o)[64]) {
-        if (nr <= 0) {
+  }
+  // ---- epilogue (every warp, once the main warps have seen the PV product retire): warp w reads TMEM lane quarter
+  // w % 4 and takes the O^T tiles {0, 1} (w < 4) or {2, 3} (w >= 4); a thread owns latent dim 128 m + 32 (w % 4) +
+  // lane of each; O = hi + lo parts.  Eight warps halve the partial write of four.
+  failed = __syncthreads_or(failed) != 0;
+  tc::fence_after_sync();
+  if (!failed) {
+    const int quarter = warp & 3, dl = quarter * 32 + lane, m0 = (warp >> 2) * 2;
+    auto load_o = [&](int m, float (&o)[64]) {
+      if (nr <= 0) {
 #pragma unroll
-          for (int h = 0; h < 64; ++h) o[h] = 0.f;
-          return;
-        }
-        const uint32_t ta = tm_o + 128 * m + ((uint32_t)(warp * 32) << 16);
-        uint32_t u[64];
-        tc::tmem_ld32(ta, u);
-        tc::tmem_ld32(ta + 32, u + 32);
-        tc::tmem_wait_ld();
+        for (int h = 0; h < 64; ++h) o[h] = 0.f;
+        return;
+      }
+      const uint32_t ta = tm_o + 128 * m + ((uint32_t)(quarter * 32) << 16);
+      uint32_t u[64];
+      tc::tmem_ld32(ta, u);
+      tc::tmem_ld32(ta + 32, u + 32);
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 64; ++h) o[h] = __uint_as_float(u[h]);
-        tc::tmem_ld32(ta + 64, u);
-        tc::tmem_ld32(ta + 96, u + 32);
-        tc::tmem_wait_ld();
+      for (int h = 0; h < 64; ++h) o[h] = __uint_as_float(u[h]);
+      tc::tmem_ld32(ta + 64, u);
+      tc::tmem_ld32(ta + 96, u + 32);
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 64; ++h) o[h] += __uint_as_float(u[h]);
-      };
-      if (a.S > 1) {
-        if (tid < 64) {
-          const size_t idx = ((size_t)it.q * a.S + it.s) * kAH + tid;
-          a.part_ml[idx * 2] = mref[tid] == -INFINITY ? -INFINITY : mref[tid] * kLn2;
-          a.part_ml[idx * 2 + 1] = lsum[tid];
-        }
-        if (nr > 0) {
-          for (int m = 0; m < 4; ++m) {
-            float o[64];
-            load_o(m, o);
-            float* dst = a.part_acc + (((size_t)it.q * a.S + it.s) * kAH) * kAD + 128 * m + tid;
-#pragma unroll
-            for (int h = 0; h < 64; ++h) dst[(size_t)h * kAD] = o[h];
-          }
-        }
-      } else {
-        for (int m = 0; m < 4; ++m) {
-          const int d = 128 * m + tid;
+      for (int h = 0; h < 64; ++h) o[h] += __uint_as_float(u[h]);
+    };
+    if (a.S > 1) {
+      if (tid < 64) {
+        const size_t idx = ((size_t)it.q * a.S + it.s) * kAH + tid;
+        a.part_ml[idx * 2] = mref[tid] == -INFINITY ? -INFINITY : mref[tid] * kLn2;
+        a.part_ml[idx * 2 + 1] = lsum[tid];
+      }
+      if (nr > 0) {
+        for (int m = m0; m < m0 + 2; ++m) {
           float o[64];
           load_o(m, o);
-          __nv_bfloat16* dst = a.out + (size_t)it.q * kAH * kAD + d;
+          float* dst = a.part_acc + (((size_t)it.q * a.S + it.s) * kAH) * kAD + 128 * m + dl;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            const float z2 = a.sink[h] * 1.4426950408889634f;
-            const float mr = mref[h];
-            const float M2 = fmaxf(z2, mr);
-            const float f = mr == -INFINITY ? 0.f : exp2f(mr - M2);
-            const float Z = exp2f(z2 - M2) + lsum[h] * f;
-            float v = rnd<__nv_bfloat16>(o[h] * (f / Z));
-            const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-            if (d >= kAD - 64) {
-              const int i = (d - (kAD - 64)) >> 1;
-              v = (d & 1) ? fmaf(-partner, rsin[i], v * rcos[i]) : fmaf(v, rcos[i], partner * rsin[i]);
-            }
-            dst[(size_t)h * kAD] = __float2bfloat16_rn(v);
+          for (int h = 0; h < 64; ++h) dst[(size_t)h * kAD] = o[h];
+        }
+      }
+    } else {
+      for (int m = m0; m < m0 + 2; ++m) {
+        const int d = 128 * m + dl;
+        float o[64];
+        load_o(m, o);
+        __nv_bfloat16* dst = a.out + (size_t)it.q * kAH * kAD + d;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) {
+          const float z2 = a.sink[h] * 1.4426950408889634f;
+          const float mr = mref[h];
+          const float M2 = fmaxf(z2, mr);
+          const float f = mr == -INFINITY ? 0.f : exp2f(mr - M2);
+          const float Z = exp2f(z2 - M2) + lsum[h] * f;
+          float v = rnd<__nv_bfloat16>(o[h] * (f / Z));
+          const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+          if (d >= kAD - 64) {
+            const int i = (d - (kAD - 64)) >> 1;
+            v = (d & 1) ? fmaf(-partner, rsin[i], v * rcos[i]) : fmaf(v, rcos[i], partner * rsin[i]);
           }
+          dst[(size_t)h * kAD] = __float2bfloat16_rn(v);
         }
       }
     }

@@ -62,6 +62,7 @@ struct IdxArgs {
   const int32_t* n_rows;
   const int32_t* pos;  // decode positions [Q] or null (prefill: pos0 + q)
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
+  int group_penalty;  // partition weight of a group's query block, in tiles
   float* scores;     // [Q, cap]
   int32_t* err;
   // overlapped decode scan (kernel instance kOverlap): the roped queries and scaled head weights, left for the
@@ -217,13 +218,31 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     const int q0 = g * G + pt / 32;
     pre.p = (pt < G * 32 && q0 < a.Q) ? idx_qpos(a, q0) : 0;
   };
-  const int per = (a.n_items + gridDim.x - 1) / gridDim.x;
-  const int i_begin = min(a.n_items, blockIdx.x * per), i_end = min(a.n_items, i_begin + per);
+  // Static partition of the items, weighted: each group costs its tiles plus group_penalty tile-equivalents (the
+  // query block a CTA must build when its range enters the group), placed before the group's first tile.  A CTA
+  // whose range crosses into a second group therefore gets fewer tiles; measured in the decode step, such CTAs
+  // otherwise finished ~3 us (about three tiles) after the others and held up the successor.
+  int i_begin, i_end;
+  {
+    const int unit = a.tiles_per_group + a.group_penalty;
+    const long long total = (long long)(a.n_items / a.tiles_per_group) * unit;
+    auto item_at = [&](long long x) {  // first item at or after cost position x
+      const int g = (int)(x / unit), r = (int)(x - (long long)g * unit);
+      return g * a.tiles_per_group + max(0, r - a.group_penalty);
+    };
+    const long long x0 = total * blockIdx.x / gridDim.x, x1 = total * (blockIdx.x + 1) / gridDim.x;
+    i_begin = min(a.n_items, item_at(x0));
+    i_end = blockIdx.x + 1 == gridDim.x ? a.n_items : min(a.n_items, item_at(x1));
+  }
   Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
   if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
-  pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
+  // before the token and the step's inputs, and writes only its own scratch, so it runs beside the compress
+  // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
+  // a projection kernel that lets successors start only once all earlier work is complete.)
+  if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::kAcc * N);
     tc::tmem_relinquish();
@@ -448,6 +467,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::kAcc * N);
+  if (kOverlap) pdl_wait();  // complete only after the kernels it ran beside
 }
 
 int g_num_sms = 0;
@@ -482,6 +502,7 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   a.n_rows = n_rows; a.pos = pos; a.pos0 = pos0; a.ratio = L.ratio; a.topk = L.topk; a.cap = cap; a.Q = Q;
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
   a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
+  a.group_penalty = G == 1 ? 3 : 0;
   a.scores = scores; a.err = err;
   if (overlap) {
     if (!pos || G != 1) return cudaErrorInvalidValue;

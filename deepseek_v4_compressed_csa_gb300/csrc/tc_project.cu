@@ -71,6 +71,9 @@ __device__ __forceinline__ void project_tile(const CUtensorMap* tm_wkv, const CU
     }
   }
   pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  // Successors may start only now: everything enqueued before this kernel is complete, so a successor that does
+  // not wait for this kernel (the overlapped index scan) may write scratch memory an earlier call still read.
+  pdl_trigger();
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, tcols);
     tc::tmem_relinquish();
@@ -147,7 +150,6 @@ __device__ __forceinline__ void project_tile(const CUtensorMap* tm_wkv, const CU
 __global__ void __launch_bounds__(kPThreads, 1)
     k_tc_project(const __grid_constant__ CUtensorMap tm_wkv, const __grid_constant__ CUtensorMap tm_wg,
                  const __grid_constant__ CUtensorMap tm_x, PjArgs a, int stages) {
-  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int m = blockIdx.x, n = blockIdx.y;
@@ -204,7 +206,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                       const __grid_constant__ CUtensorMap tm_wkv1, const __grid_constant__ CUtensorMap tm_wg1,
                       const __grid_constant__ CUtensorMap tm_x, PjArgs a0, PjArgs a1, int m_tiles0, int m_tiles1,
                       int stages) {
-  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tiles0 = m_tiles0 * a0.splits;

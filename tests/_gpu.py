@@ -422,14 +422,34 @@ class Runner:
         self.projs = {"attn": st.front_attn[rows, slots].view(B, 1, -1).clone(),
                       "index": st.front_index[rows, slots].view(B, 1, -1).clone()}
 
-    def decode_step(self, st: DevCache, si: csa_synth.StepInputs, overlap: bool = False):
+    def compress_pair_and_index_one_stream(self, st: DevCache, si: csa_synth.StepInputs, sel, n_sel):
+        """Both pools through csa_compress_append_pair, then csa_index_topk_overlapped on the same stream with no
+        event: its scan of the rows complete before the token runs beside the compress call's kernels."""
+        x = dev(si.x)
+        B = x.shape[0]
+        n_idx = st.n_rows.clone()
+        csa.compress_append_pair(self.L, self.ca, self.ci, x, st.pos, st.front_attn, st.pool, st.n_rows,
+                                 st.front_index, st.ikeys, n_idx, self.inv_freq, err=self.err)
+        csa.index_topk_overlapped(self.L, dev(si.iq), dev(si.iw), st.ikeys, n_idx, st.pos, self.inv_freq, sel, n_sel,
+                                  err=self.err)
+        slots = st.pos.long() % st.front_attn.shape[1]
+        rows = torch.arange(B, device="cuda")
+        self.projs = {"attn": st.front_attn[rows, slots].view(B, 1, -1).clone(),
+                      "index": st.front_index[rows, slots].view(B, 1, -1).clone()}
+
+    def decode_step(self, st: DevCache, si: csa_synth.StepInputs, overlap=False):
+        """One decode step.  overlap: False (compress calls, then csa_index_topk), True (the index pool's compress
+        call on a second stream beside csa_index_topk_overlapped, joined by an event) or "one_stream" (the pair
+        call, then csa_index_topk_overlapped on one stream)."""
         cfg = self.cfg
         B = si.q.shape[0]
         sel = n_sel = None
         if cfg.has_indexer:
             sel = torch.empty(B, cfg.topk, dtype=torch.int32, device="cuda")
             n_sel = torch.empty(B, dtype=torch.int32, device="cuda")
-        if overlap and cfg.has_indexer:
+        if overlap == "one_stream" and cfg.has_indexer:
+            self.compress_pair_and_index_one_stream(st, si, sel, n_sel)
+        elif overlap and cfg.has_indexer:
             self.compress_and_index_overlapped(st, si, sel, n_sel)
         else:
             self.projs = self.compress(st, si.x)

@@ -151,11 +151,13 @@ def test_config2_flash_build_8k_then_decode():
 
 @pytest.mark.parametrize("cid,ctx,steps,seqs,overlap", [(3, 32768, 10, (0, 13, 31), False),
                                                          (3, 32768 + 1, 6, (5, 30), True),
+                                                         (3, 32768 + 2, 6, (2, 19, 31), "one_stream"),
                                                          (4, 262144 - 3, 6, (0, 15), False)])
 def test_batched_decode_sampled_sequences(cid, ctx, steps, seqs, overlap):
     """Configs 3 and 4 at full batch and context: every sequence runs on the GPU; the oracle follows
     a few of them step by step (window-boundary crossings included).  The second case drives the indexer
-    through csa_index_topk_overlapped, the form the bench times."""
+    through csa_index_topk_overlapped beside the index pool's compress call on another stream; the third
+    through csa_compress_append_pair and csa_index_topk_overlapped on one stream (the bench's order)."""
     cfg = csa_synth.CONFIGS[cid]
     cap = ctx // cfg.ratio + steps // cfg.ratio + 4
     run = G.Runner(cfg)
@@ -442,11 +444,13 @@ def _ragged_cache(cfg, cap, ctxs):
     return host
 
 
-@pytest.mark.parametrize("overlap", [False, True], ids=["one_stream", "overlapped_indexer"])
+@pytest.mark.parametrize("overlap", [False, True, "one_stream"],
+                         ids=["serial", "overlapped_indexer", "overlapped_one_stream"])
 def test_ragged_batch_edges(overlap):
     """One batch mixing an empty cache, a cache shorter than the window, the dense/sparse threshold
-    (n_vis == topk and topk + 1) and a long cache; with csa_index_topk, and with csa_index_topk_overlapped
-    scanning while the index pool's compress call runs on another stream (some steps emit a row)."""
+    (n_vis == topk and topk + 1) and a long cache; with csa_index_topk, with csa_index_topk_overlapped
+    scanning while the index pool's compress call runs on another stream, and with the pair call followed by
+    csa_index_topk_overlapped on one stream (some steps emit a row)."""
     cfg = csa_synth.CONFIGS[3].replace(B=6)
     ctxs = [0, 3, 100, 2047, 2051, 9000]
     cap = max(ctxs) // 4 + 8
