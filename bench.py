@@ -563,6 +563,38 @@ def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup:
                       "synthetic rows drawn directly (seeded N(0,1))")}
 
 
+def trim_line(csa, csa_synth, dev) -> dict:
+    """Latency of csa_trim for the headline batch (B = 32, rollback 64): one graph of 64 trims (a trim moves no
+    data, so its cost is one small kernel whatever it rewinds), timed with CUDA events."""
+    import torch
+    cfg = csa_synth.CONFIGS[3].replace(rollback=64)
+    L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
+                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps, rollback=cfg.rollback)
+    i32 = lambda v: torch.full((cfg.B,), v, dtype=torch.int32, device=dev)  # noqa: E731
+    pos, n_a, n_i, hw = i32(cfg.ctx), i32(cfg.ctx // 4), i32(cfg.ctx // 4), i32(cfg.ctx)
+    n_back, err = i32(0), torch.zeros(1, dtype=torch.int32, device=dev)
+    reps = 64
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        csa.trim(L, n_back, pos, n_a, n_i, hw, err=err)
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                csa.trim(L, n_back, pos, n_a, n_i, hw, err=err)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return {"batch": cfg.B, "rollback": cfg.rollback, "us_per_trim": round(1e3 * e0.elapsed_time(e1) / reps, 3),
+            "how": f"one CUDA graph of {reps} back-to-back csa_trim calls (B = {cfg.B}), CUDA events"}
+
+
 def run_ours(args):
     import torch
     dist, rank, world, local = _dist()
@@ -694,6 +726,8 @@ def run_ours(args):
     if not args.no_prefill:
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
 
+    trim = trim_line(csa, csa_synth, dev)
+
     # ---- the other decode workloads (configs 2 and 4), each as its own model step of nl layers
     others = None
     if not args.no_other_configs:
@@ -748,6 +782,7 @@ def run_ours(args):
                 "indexer": args.indexer,
                 "prefill": prefill,
                 "other_decode_workloads": others,
+                "trim": trim,
             },
             "roofline": {
                 "kernel": (f"model step graph: every kernel of one decode step of {nl} layers (per layer: both "

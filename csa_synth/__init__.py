@@ -57,6 +57,7 @@ class Config:
     T: int = 0  # prefill chunk length (0: decode workload)
     prefill_tokens: int = 0  # tokens compressed from seeded hidden states before decoding
     rms_eps: float = 1e-6
+    rollback: int = 0  # extra ring slots for exact trims (window W + rollback, frontier + rollback)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -65,7 +66,13 @@ class Config:
 
     @property
     def frontier_slots(self) -> int:
-        return 2 * self.ratio if self.ratio == 4 else self.ratio
+        """Frontier ring slots, the rollback journal included."""
+        return (2 * self.ratio if self.ratio == 4 else self.ratio) + self.rollback
+
+    @property
+    def ring_slots(self) -> int:
+        """Window ring slots: W plus the rollback margin."""
+        return self.W + self.rollback
 
     @property
     def has_indexer(self) -> bool:
@@ -211,7 +218,7 @@ def empty_cache(cfg: Config, cap: int, B: int | None = None) -> Cache:
     return Cache(
         pool=z(B, cap, cfg.D),
         ikeys=z(B, cap, cfg.Di) if cfg.has_indexer else None,
-        window=z(B, cfg.W, cfg.D),
+        window=z(B, cfg.ring_slots, cfg.D),
         front_attn=z(B, F, 2 * L * cfg.D),
         front_index=z(B, F, 2 * L * cfg.Di) if cfg.has_indexer else None,
         n_rows=torch.zeros(B, dtype=torch.int32),
@@ -231,6 +238,8 @@ def synth_cache(cfg: Config, cap: int, B: int | None = None, ctx: int | None = N
     """
     B = cfg.B if B is None else B
     ctx = cfg.ctx if ctx is None else ctx
+    if cfg.rollback:
+        return with_rollback_slots(synth_cache(cfg.replace(rollback=0), cap, B, ctx), cfg, ctx)
     n = ctx // cfg.ratio
     assert n <= cap
     c = empty_cache(cfg, cap, B)
@@ -245,3 +254,24 @@ def synth_cache(cfg: Config, cap: int, B: int | None = None, ctx: int | None = N
     c.n_rows[:] = n
     c.pos[:] = ctx
     return c
+
+
+def with_rollback_slots(cache: Cache, cfg: Config, ctx: int) -> Cache:
+    """The same cache (built without rollback slots, position ctx) in rings with cfg.rollback extra slots: token t's
+    window row moves from slot t mod W to slot t mod (W + rollback), and its frontier entry from slot t mod F0 to
+    t mod (F0 + rollback); the new slots hold zeros (no earlier tokens exist in them)."""
+    out = empty_cache(cfg, cache.pool.shape[1], cache.pool.shape[0])
+    out.pool.copy_(cache.pool)
+    if out.ikeys is not None:
+        out.ikeys.copy_(cache.ikeys)
+    out.n_rows.copy_(cache.n_rows)
+    out.pos.copy_(cache.pos)
+    W, Wr = cfg.W, cfg.ring_slots
+    F0, F = cache.front_attn.shape[1], cfg.frontier_slots
+    for t in range(max(0, ctx - W), ctx):
+        out.window[:, t % Wr] = cache.window[:, t % W]
+    for t in range(max(0, ctx - F0), ctx):
+        out.front_attn[:, t % F] = cache.front_attn[:, t % F0]
+        if out.front_index is not None:
+            out.front_index[:, t % F] = cache.front_index[:, t % F0]
+    return out

@@ -21,13 +21,13 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libcsa.so")
 
 CSA_F32, CSA_BF16 = 0, 1
 OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL, OP_COMPRESS_PAIR = 0, 1, 2, 3, 4
-DEV_CAPACITY, DEV_STATE, DEV_RANGE = 1, 2, 4
+DEV_CAPACITY, DEV_STATE, DEV_RANGE, DEV_ROLLBACK = 1, 2, 4, 8
 CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
            "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions",
-           "csa_compress_append_pair")
+           "csa_compress_append_pair", "csa_trim")
 
 
 class CSAError(RuntimeError):
@@ -40,7 +40,7 @@ class _Layer(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int), ("R", ctypes.c_int),
                 ("W", ctypes.c_int), ("ratio", ctypes.c_int), ("Hi", ctypes.c_int), ("Di", ctypes.c_int),
                 ("topk", ctypes.c_int), ("X", ctypes.c_int), ("scale", ctypes.c_float),
-                ("rms_eps", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("rollback", ctypes.c_int)]
 
 
 class _Comp(ctypes.Structure):
@@ -89,13 +89,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_compress_append_pair.restype = i32
     lib.csa_advance_positions.argtypes = [vp, i32, i32, vp]
     lib.csa_advance_positions.restype = i32
+    lib.csa_trim.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_trim.restype = i32
     _lib = lib
     return lib
 
 
 @dataclass(frozen=True)
 class Layer:
-    """Mirror of csa_layer.  dtype: torch.bfloat16 or torch.float32 (model dtype)."""
+    """Mirror of csa_layer.  dtype: torch.bfloat16 or torch.float32 (model dtype).  rollback: tokens csa_trim may
+    rewind; the window ring then has W + rollback slots and each frontier ring frontier_slots(ratio) + rollback."""
 
     dtype: torch.dtype
     H: int
@@ -109,6 +112,11 @@ class Layer:
     X: int
     scale: float = 0.0
     rms_eps: float = 1e-6
+    rollback: int = 0
+
+    @property
+    def ring_slots(self) -> int:
+        return self.W + self.rollback
 
     @property
     def lanes(self) -> int:
@@ -121,7 +129,7 @@ class Layer:
     def _c(self) -> _Layer:
         code = CSA_BF16 if self.dtype == torch.bfloat16 else CSA_F32
         return _Layer(code, self.H, self.D, self.R, self.W, self.ratio, self.Hi, self.Di, self.topk, self.X,
-                      float(self.scale), float(self.rms_eps))
+                      float(self.scale), float(self.rms_eps), int(self.rollback))
 
 
 @dataclass
@@ -167,8 +175,8 @@ def _expect_comp(layer: "Layer", comp: "Compressor", which: str):
     _expect(f"{which}.norm_w", comp.norm_w, torch.float32, (d,))
 
 
-def _frontier_len(ratio: int) -> int:
-    return 2 * ratio if ratio == 4 else ratio
+def _frontier_len(layer: "Layer") -> int:
+    return (2 * layer.ratio if layer.ratio == 4 else layer.ratio) + layer.rollback
 
 
 def _ptr(t: torch.Tensor | None):
@@ -207,6 +215,21 @@ def frontier_slots(ratio: int) -> int:
     return load_library().csa_frontier_slots(ratio)
 
 
+def trim(layer: Layer, n_back, pos, n_rows_a, n_rows_i, hw, err=None, stream=None):
+    """csa_trim: rewind each sequence b by n_back[b] tokens (int32 device tensors [B]; n_rows_i None for layers
+    without an indexer; hw: the high-water positions, caller-owned).  Returns the device error word tensor."""
+    B = pos.numel() if isinstance(pos, torch.Tensor) else 0
+    for name, t in (("n_back", n_back), ("pos", pos), ("n_rows_a", n_rows_a), ("hw", hw)):
+        _expect(name, t, torch.int32, (B,))
+    _expect("n_rows_i", n_rows_i, torch.int32, (B,), optional=not layer.has_indexer)
+    _expect_err(err)
+    err = _err(err, pos.device)
+    L = layer._c()
+    _check("csa_trim", load_library().csa_trim(ctypes.byref(L), B, _ptr(n_back), _ptr(pos), _ptr(n_rows_a),
+                                               _ptr(n_rows_i), _ptr(hw), _ptr(err), _stream(stream)))
+    return err
+
+
 def workspace_size(layer: Layer, op: int, B: int, T: int, cap: int) -> int:
     n = ctypes.c_size_t(0)
     L = layer._c()
@@ -238,7 +261,7 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
         raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {comp.d}]")
     cap = pool.shape[1]
     _expect("pos", pos, torch.int32, (B,))
-    _expect("frontier", frontier, layer.dtype, (B, _frontier_len(layer.ratio), 2 * layer.lanes * comp.d))
+    _expect("frontier", frontier, layer.dtype, (B, _frontier_len(layer), 2 * layer.lanes * comp.d))
     _expect("n_rows", n_rows, torch.int32, (B,))
     _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
     _expect_err(err)
@@ -260,7 +283,7 @@ def compress_append_pair(layer: Layer, comp_a: Compressor, comp_i: Compressor, x
     B, T = x.shape[0], x.shape[1]
     _expect_comp(layer, comp_a, "comp_a")
     _expect_comp(layer, comp_i, "comp_i")
-    F = _frontier_len(layer.ratio)
+    F = _frontier_len(layer)
     for nm, pl, fr, nr, d in (("a", pool_a, frontier_a, n_rows_a, comp_a.d), ("i", pool_i, frontier_i, n_rows_i,
                                                                                comp_i.d)):
         _expect(f"pool_{nm}", pl, layer.dtype)
@@ -351,7 +374,7 @@ def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_se
     B = q.shape[0]
     _expect("kv_new", kv_new, layer.dtype, (B, layer.D))
     _expect("sink", sink, torch.float32, (layer.H,))
-    _expect("window", window, layer.dtype, (B, layer.W, layer.D))
+    _expect("window", window, layer.dtype, (B, layer.ring_slots, layer.D))
     _expect("pool", pool, layer.dtype)
     if pool.dim() != 3 or pool.shape[0] != B or pool.shape[2] != layer.D:
         raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {layer.D}]")
@@ -386,7 +409,7 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, windo
         if ikeys.dim() != 2 or ikeys.shape[1] != layer.Di:
             raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [cap, {layer.Di}]")
     _expect("sink", sink, torch.float32, (layer.H,))
-    _expect("window", window, layer.dtype, (layer.W, layer.D))
+    _expect("window", window, layer.dtype, (layer.ring_slots, layer.D))
     _expect("pool", pool, layer.dtype)
     if pool.dim() != 2 or pool.shape[1] != layer.D:
         raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [cap, {layer.D}]")

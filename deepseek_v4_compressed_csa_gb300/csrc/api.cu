@@ -29,13 +29,16 @@ csa_status make_dims(const csa_layer* l, Dims* d) {
     if (l->topk < 1 || l->topk > 4096) return CSA_ERR_ARG;
   }
   if (!(l->rms_eps >= 0.f) || !(l->scale >= 0.f)) return CSA_ERR_ARG;
+  if (l->rollback < 0 || l->rollback > (1 << 20)) return CSA_ERR_ARG;
   d->dtype = l->dtype;
   d->H = l->H; d->D = l->D; d->R = l->R; d->W = l->W; d->ratio = l->ratio;
   d->Hi = l->Hi; d->Di = l->Di; d->topk = l->topk; d->X = l->X;
   d->scale = l->scale > 0.f ? l->scale : (float)(1.0 / sqrt((double)l->D));
   d->eps = l->rms_eps;
   d->lanes = (l->ratio == 4) ? 2 : 1;
-  d->F = csa_frontier_slots(l->ratio);
+  d->rollback = l->rollback;
+  d->Wr = l->W + l->rollback;
+  d->F = csa_frontier_slots(l->ratio) + l->rollback;
   return CSA_OK;
 }
 
@@ -274,6 +277,19 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
   }
   return cuda_status(launch_attend_prefill(L, q, kv_new, sink, T, pos0, window, pool, cap, n_rows,
                                            L.has_indexer() ? sel : nullptr, n_sel, inv_freq, out, aw, err, s));
+}
+
+csa_status csa_trim(const csa_layer* layer, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
+                    int32_t* n_rows_i, int32_t* hw, int32_t* err, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (B < 0) return CSA_ERR_ARG;
+  if (B == 0) return CSA_OK;
+  if (!dev_i32(n_back) || !dev_i32(pos) || !dev_i32(n_rows_a) || !dev_i32(hw) || !dev_i32(err)) return CSA_ERR_ARG;
+  if (n_rows_i && !dev_i32(n_rows_i)) return CSA_ERR_ARG;
+  if (L.has_indexer() && !n_rows_i) return CSA_ERR_ARG;
+  return cuda_status(launch_trim(L, B, n_back, pos, n_rows_a, n_rows_i, hw, err, static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream) {

@@ -72,7 +72,7 @@ __global__ void k_rope_rows(const T* __restrict__ src, T* __restrict__ dst, int 
   }
 }
 
-// window[b][pos[b] mod W] = RoPE(kv_new[b], pos[b])
+// window[b][pos[b] mod Wr] = RoPE(kv_new[b], pos[b])  (Wr: ring slots)
 template <typename T>
 __global__ void k_window_append(const T* __restrict__ kv, T* __restrict__ window, int W, int D, int R,
                                 const int32_t* __restrict__ pos, const float* __restrict__ inv_freq) {
@@ -96,7 +96,7 @@ __global__ void k_window_append(const T* __restrict__ kv, T* __restrict__ window
   }
 }
 
-// window[t mod W] = kvr[t - pos0] for the chunk's last min(T, W) tokens
+// window[t mod Wr] = kvr[t - pos0] for the chunk's last min(T, Wr) tokens (Wr: ring slots, W + rollback)
 template <typename T>
 __global__ void k_window_store_chunk(const T* __restrict__ kvr, T* __restrict__ window, int W, int D, int T_,
                                      int pos0) {
@@ -119,7 +119,7 @@ struct AttnArgs {
   const int32_t* pos;   // decode positions [B] or null (prefill: pos0 + q)
   const float* sink;
   const float* inv_freq;
-  int pos0, cap, topk, W, H, D, R, ratio;
+  int pos0, cap, topk, W, Wr, H, D, R, ratio;  // W attended window tokens, Wr ring slots
   float scale;
   int S;
   float* part_ml;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(256) k_attend_simt(AttnArgs a) {
   const int b = prefill ? 0 : q;
   const int p = prefill ? a.pos0 + q : a.pos[q];
   const T* pool = static_cast<const T*>(a.pool) + (size_t)b * a.cap * D;
-  const T* ring = static_cast<const T*>(a.ring) + (size_t)b * a.W * D;
+  const T* ring = static_cast<const T*>(a.ring) + (size_t)b * a.Wr * D;
   const T* kvr = static_cast<const T*>(a.kvr);
   const int nrows_b = min(a.n_rows[b], a.cap);
 
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256) k_attend_simt(AttnArgs a) {
           else if (hg == 0) atomicOr(a.err, CSA_DEV_RANGE);
         } else {
           const int t = p - nwin + 1 + (r - nsel);
-          ptr = (prefill && t >= a.pos0) ? kvr + (size_t)(t - a.pos0) * D : ring + (size_t)(t % a.W) * D;
+          ptr = (prefill && t >= a.pos0) ? kvr + (size_t)(t - a.pos0) * D : ring + (size_t)(t % a.Wr) * D;
         }
       }
       rowp[threadIdx.x] = ptr;
@@ -407,14 +407,14 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
                ws.part_ml, ws.part_acc, ws.S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out));
     return cudaGetLastError();
   }
-  CSA_LAUNCH(k_window_append<T>, dim3(B), dim3(128), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(window), L.W, L.D, L.R, pos,
+  CSA_LAUNCH(k_window_append<T>, dim3(B), dim3(128), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(window), L.Wr, L.D, L.R, pos,
                                        inv_freq);
   CSA_LAUNCH(k_rope_rows<T>, dim3(B), dim3(256), 0, s, static_cast<const T*>(q), static_cast<T*>(ws.qr), L.H, L.D, L.R, pos, 0,
                                    inv_freq);
   AttnArgs a{};
   a.qr = ws.qr; a.pool = pool; a.ring = window; a.kvr = nullptr; a.sel = sel; a.n_sel = n_sel;
   a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq; a.pos0 = 0; a.cap = cap;
-  a.topk = L.topk; a.W = L.W; a.H = L.H; a.D = L.D; a.R = L.R; a.ratio = L.ratio; a.scale = L.scale;
+  a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.H = L.H; a.D = L.D; a.R = L.R; a.ratio = L.ratio; a.scale = L.scale;
   a.S = ws.S; a.part_ml = ws.part_ml; a.part_acc = ws.part_acc; a.out = out; a.err = err;
   return run_attend<T>(a, B, s);
 }
@@ -430,7 +430,7 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
     cudaError_t e = launch_tc_attend_prefill(L, q, pool, window, ws.kvr, sel, n_sel, n_rows, pos0, cap, sink,
                                              inv_freq, T_, out, err, s);
     if (e != cudaSuccess) return e;
-    CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.W)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
+    CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.Wr)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.Wr,
                                                         L.D, T_, pos0);
     return cudaGetLastError();
   }
@@ -439,11 +439,11 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   AttnArgs a{};
   a.qr = ws.qr; a.pool = pool; a.ring = window; a.kvr = ws.kvr; a.sel = sel; a.n_sel = n_sel;
   a.n_rows = n_rows; a.pos = nullptr; a.sink = sink; a.inv_freq = inv_freq; a.pos0 = pos0; a.cap = cap;
-  a.topk = L.topk; a.W = L.W; a.H = L.H; a.D = L.D; a.R = L.R; a.ratio = L.ratio; a.scale = L.scale;
+  a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.H = L.H; a.D = L.D; a.R = L.R; a.ratio = L.ratio; a.scale = L.scale;
   a.S = ws.S; a.part_ml = ws.part_ml; a.part_acc = ws.part_acc; a.out = out; a.err = err;
   cudaError_t e = run_attend<T>(a, T_, s);
   if (e != cudaSuccess) return e;
-  CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.W)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.W,
+  CSA_LAUNCH(k_window_store_chunk<T>, dim3(min(T_, L.Wr)), dim3(64), 0, s, static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.Wr,
                                                       L.D, T_, pos0);
   return cudaGetLastError();
 }
@@ -456,6 +456,40 @@ __global__ void k_advance_positions(int32_t* __restrict__ pos, int B, int by) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   if (b < B) pos[b] += by;
+}
+
+// csa_trim: per sequence, hw = max(hw, pos); refuse (sequence unchanged) unless 0 <= n_back, pos - n_back >= 0,
+// pos - n_back >= hw - rollback and n_rows == pos / ratio; else pos -= n_back and n_rows = pos / ratio in every
+// pool.  ("DeepSeek-V4-Flash: native deepseek_v4 AR backend", MTPLX #216, the MTP / speculative-lane post: an exact
+// trim truncates emitted rows, rebuilds frontiers from a journal and keeps extra window rows, and refuses beyond
+// its bound.)  Like the decode kernels it reads the state after its programmatic wait; it lets the next kernel
+// start only once it has written pos, since kernels read positions before their own wait.
+__global__ void k_trim(int B, const int32_t* __restrict__ n_back, int32_t* __restrict__ pos,
+                       int32_t* __restrict__ n_rows_a, int32_t* __restrict__ n_rows_i, int32_t* __restrict__ hw,
+                       int ratio, int rollback, int32_t* __restrict__ err) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  if (b >= B) return;
+  const int p = pos[b], n = n_back[b], h = max(hw[b], p), np = p - n;
+  if (p < 0 || n_rows_a[b] != p / ratio || (n_rows_i && n_rows_i[b] != p / ratio)) {
+    atomicOr(err, CSA_DEV_STATE);
+    return;
+  }
+  if (n < 0 || np < 0 || np < h - rollback) {
+    atomicOr(err, CSA_DEV_ROLLBACK);
+    return;
+  }
+  hw[b] = h;
+  pos[b] = np;
+  n_rows_a[b] = np / ratio;
+  if (n_rows_i) n_rows_i[b] = np / ratio;
+}
+
+cudaError_t launch_trim(const Dims& L, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
+                        int32_t* n_rows_i, int32_t* hw, int32_t* err, cudaStream_t s) {
+  CSA_LAUNCH(k_trim, dim3((B + 255) / 256), dim3(256), 0, s, B, n_back, pos, n_rows_a, n_rows_i, hw, L.ratio,
+             L.rollback, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s) {

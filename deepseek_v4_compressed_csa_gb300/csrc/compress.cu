@@ -463,7 +463,7 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
                                              static_cast<const T*>(comp.wgate), ntok, L.X, Ld,
                                              static_cast<T*>(ws.proj));
   }
-  if (part && L.ratio == 4 && L.lanes == 2 && L.F == 8 && d <= 256 * kTokChans) {
+  if (part && L.ratio == 4 && L.lanes == 2 && L.F >= 8 && d <= 256 * kTokChans) {
     const size_t smem = ((size_t)rowlen + 2 * (size_t)d + 32 + L.R) * sizeof(float);
     const TokPool<T> tp{ws.flags, n_rows, static_cast<T*>(frontier), comp.ape, comp.norm_w, static_cast<T*>(pool),
                         part, d, cap, splits, part_stride};
@@ -510,7 +510,7 @@ cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const 
                                  void* fi, void* pi, int cap_i, int32_t* ni, const float* inv_freq,
                                  const CompressWs& wa, const CompressWs& wi, int32_t* err, cudaStream_t s) {
   int sa = 0, si = 0;
-  const bool token = T == 1 && L.dtype == CSA_BF16 && L.ratio == 4 && L.lanes == 2 && L.F == 8 && ca.d <= 512 &&
+  const bool token = T == 1 && L.dtype == CSA_BF16 && L.ratio == 4 && L.lanes == 2 && L.F >= 8 && ca.d <= 512 &&
                      ci.d <= 512 && tc_project_supported(L, ca.d) && tc_project_supported(L, ci.d) && wa.part &&
                      wi.part && plan_project_pair(L, ca.d, ci.d, B, &sa, &si);
   if (token)

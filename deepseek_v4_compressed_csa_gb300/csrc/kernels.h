@@ -13,8 +13,10 @@ namespace csa {
 struct Dims {
   int dtype, H, D, R, W, ratio, Hi, Di, topk, X;
   float scale, eps;
-  int lanes;  // 2 when ratio == 4 (overlapping windows), else 1
-  int F;      // frontier ring length in tokens
+  int lanes;     // 2 when ratio == 4 (overlapping windows), else 1
+  int rollback;  // tokens csa_trim may rewind
+  int Wr;        // window ring slots: W + rollback (a query attends its last W tokens)
+  int F;         // frontier ring slots: 2 ratio (ratio 4) or ratio, + rollback (the journal)
   bool has_indexer() const { return ratio == 4; }
 };
 
@@ -143,6 +145,9 @@ cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* pa
 
 // ---- attend.cu: pos[b] += by for b < B
 cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s);
+// ---- attend.cu: csa_trim (rewind B sequences by n_back tokens within the rollback margin)
+cudaError_t launch_trim(const Dims& L, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
+                        int32_t* n_rows_i, int32_t* hw, int32_t* err, cudaStream_t s);
 
 // ---- tc_attend_prefill.cu (tensor-core chunked-prefill attention; bf16, H = 64, D = 512, R = 64)
 // T queries of one sequence at positions pos0 + q; the chunk's roped rows kvr [T, D], the ring before the

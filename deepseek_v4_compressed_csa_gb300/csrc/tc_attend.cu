@@ -73,6 +73,7 @@ struct AtArgs {
   const float* sink;
   const float* inv_freq;
   int pos0, cap, topk, W, ratio, Q, S;
+  int Wr;  // window ring slots (W + rollback); a query attends its last W tokens
   float scale2;               // softmax scale * log2(e)
   float* part_ml;
   float* part_acc;
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
             if (a.kv_new && tok == it.p) ptr = a.kv_new + (size_t)it.b * kAD;  // roped below, also into the ring
             else
               ptr = (a.kvr && tok >= a.pos0) ? a.kvr + (size_t)(tok - a.pos0) * kAD
-                                             : a.ring + ((size_t)it.b * a.W + (tok % a.W)) * kAD;
+                                             : a.ring + ((size_t)it.b * a.Wr + (tok % a.Wr)) * kAD;
           }
         }
         rowp[tid] = ptr;
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
               }
             }
             *reinterpret_cast<uint4*>(rows + (c >> 3) * kBox + cur_row * 128 + (((c & 7) ^ (cur_row & 7)) << 4)) = raw;
-            *reinterpret_cast<uint4*>(a.ring_out + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + c * 8) = raw;
+            *reinterpret_cast<uint4*>(a.ring_out + ((size_t)it.b * a.Wr + (it.p % a.Wr)) * kAD + c * 8) = raw;
           }
         }
       }
@@ -620,7 +621,7 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
   a.kv_new = static_cast<const __nv_bfloat16*>(kv_new);
   a.ring_out = static_cast<__nv_bfloat16*>(ring);
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq;
-  a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.ratio = L.ratio; a.Q = Q; a.S = S;
+  a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.ratio = L.ratio; a.Q = Q; a.S = S;
   a.scale2 = L.scale * 1.4426950408889634f;
   a.part_ml = part_ml; a.part_acc = part_acc;
   a.out = static_cast<__nv_bfloat16*>(out);

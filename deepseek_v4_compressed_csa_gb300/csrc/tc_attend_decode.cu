@@ -86,6 +86,7 @@ struct DecArgs {
   const float* sink;
   const float* inv_freq;
   int cap, topk, W, ratio, S;
+  int Wr;                       // ring slots (W + rollback); the query attends its last W tokens
   float scale2;                 // softmax scale * log2(e)
   float* part_ml;
   float* part_acc;
@@ -150,7 +151,7 @@ __device__ __forceinline__ void item_selection(const DecArgs& a, Item& it) {
 __device__ __forceinline__ int window_code(const DecArgs& a, const Item& it, int w) {
   const int tok = it.p - it.nwin + 1 + w;
   if (tok == it.p) return kRowNew;
-  return kRowRing0 - (it.b * a.W + tok % a.W);
+  return kRowRing0 - (it.b * a.Wr + tok % a.Wr);
 }
 __device__ __forceinline__ int selected_code(const DecArgs& a, const Item& it, int k, int j) {
   if (!a.sel) j = k;
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         uint4 raw = __ldg(reinterpret_cast<const uint4*>(cur + ch * 8));
         if (ch >= 56) rope8(raw, ch, rcos, rsin);
         *reinterpret_cast<uint4*>(rows + (ch >> 3) * kBox + cur_row * 128 + (((ch & 7) ^ (cur_row & 7)) << 4)) = raw;
-        *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.W + (it.p % a.W)) * kAD + ch * 8) = raw;
+        *reinterpret_cast<uint4*>(a.ring + ((size_t)it.b * a.Wr + (it.p % a.Wr)) * kAD + ch * 8) = raw;
       }
     }
     tc::cp_async_wait_all();
@@ -561,7 +562,7 @@ cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* po
   a.ring = static_cast<__nv_bfloat16*>(ring);
   a.kv_new = static_cast<const __nv_bfloat16*>(kv_new);
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.pos = pos; a.sink = sink; a.inv_freq = inv_freq;
-  a.cap = cap; a.topk = L.topk; a.W = L.W; a.ratio = L.ratio; a.S = S;
+  a.cap = cap; a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.ratio = L.ratio; a.S = S;
   a.scale2 = L.scale * 1.4426950408889634f;
   a.part_ml = part_ml; a.part_acc = part_acc;
   a.out = static_cast<__nv_bfloat16*>(out);

@@ -90,6 +90,7 @@ struct PfArgs {
   const float* sink;
   const float* inv_freq;
   int T, pos0, cap, topk, W, ratio;
+  int Wr;                      // ring slots (W + rollback); a query attends its last W tokens
   int chunk_tiles;             // T >= 128: 128-row boxes of the chunk's rows are available
   float scale2;                // softmax scale * log2(e)
   __nv_bfloat16* out;          // [T, 64, 512]
@@ -136,7 +137,7 @@ __device__ __forceinline__ int row_src(const PfArgs& a, int code, int& row) {
       row = tok - a.pos0;
       return kSrcChunk;
     }
-    row = tok % a.W;
+    row = tok % a.Wr;
     return kSrcRing;
   }
   row = 0;
@@ -615,7 +616,7 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
   a.ring = static_cast<const __nv_bfloat16*>(ring);
   a.kvr = static_cast<const __nv_bfloat16*>(kvr);
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.sink = sink; a.inv_freq = inv_freq;
-  a.T = T; a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.ratio = L.ratio;
+  a.T = T; a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.ratio = L.ratio;
   a.scale2 = L.scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.err = err;
@@ -626,7 +627,7 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
   if (!make_tmap_2d_bf16(&tq, q, (uint64_t)T * kAH, kAD, kAD * 2, 64) ||
       !make_tmap_2d_bf16(&tp, pool, (uint64_t)cap, kAD, kAD * 2, 1) ||
       !make_tmap_2d_bf16(&tk, kvr, (uint64_t)T, kAD, kAD * 2, 1) ||
-      !make_tmap_2d_bf16(&tr, ring, (uint64_t)L.W, kAD, kAD * 2, 1) ||
+      !make_tmap_2d_bf16(&tr, ring, (uint64_t)L.Wr, kAD, kAD * 2, 1) ||
       !make_tmap_2d_bf16(&tkt, kvr, (uint64_t)T, kAD, kAD * 2, a.chunk_tiles ? kPR : 1))
     return cudaErrorInvalidValue;
   cudaFuncSetAttribute(k_tc_attend_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

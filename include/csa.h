@@ -74,7 +74,8 @@ enum { CSA_F32 = 0, CSA_BF16 = 1 };
 enum {
   CSA_DEV_CAPACITY = 1, /* a compress call would emit a row at index >= cap: sequence skipped */
   CSA_DEV_STATE = 2,    /* n_rows[b] != floor(pos[b] / ratio) or pos[b] < 0: sequence skipped */
-  CSA_DEV_RANGE = 4     /* a selected row index outside [0, n_rows[b]): that row is skipped */
+  CSA_DEV_RANGE = 4,    /* a selected row index outside [0, n_rows[b]): that row is skipped */
+  CSA_DEV_ROLLBACK = 8  /* csa_trim beyond the rollback margin (or below 0): sequence left unchanged */
 };
 
 /* operation ids for csa_workspace_size */
@@ -93,12 +94,18 @@ enum {
  *   non-overlapping windows of r tokens, no indexer); indexer Hi heads of Di
  *   dims keeping `topk` rows; hidden size X.
  *   scale: attention logit scale (the pages' kernels use D^-1/2; 0 selects it).
- *   rms_eps: RMSNorm epsilon of the compressed rows. */
+ *   rms_eps: RMSNorm epsilon of the compressed rows.
+ *   rollback: tokens csa_trim may rewind (0: none).  The window ring then holds
+ *     W + rollback slots (token t in slot t mod (W + rollback)) and each frontier
+ *     ring csa_frontier_slots(ratio) + rollback slots (its journal of projected
+ *     rows); a query still attends only its last W tokens.  Every call of a layer
+ *     takes buffers of those sizes. */
 typedef struct {
   int dtype;
   int H, D, R, W, ratio, Hi, Di, topk, X;
   float scale;
   float rms_eps;
+  int rollback;
 } csa_layer;
 
 /* One compressor (the attention pool's, d = D, or the index pool's, d = Di).
@@ -118,7 +125,8 @@ typedef struct {
   int d;
 } csa_compressor;
 
-/* Frontier ring length in tokens: 2*ratio when ratio == 4, else ratio. */
+/* Frontier ring length in tokens without a rollback journal: 2*ratio when
+ * ratio == 4, else ratio (a layer with rollback r adds r slots). */
 int csa_frontier_slots(int ratio);
 
 /* Bytes of scratch memory `op` needs for batch B (T: tokens per sequence for
@@ -144,9 +152,10 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
  * Arguments
  *   x        [B, T, X]             model dtype, tokens at pos[b] .. pos[b]+T-1
  *   pos      [B] int32 (device)    position of x[b][0]; the library never writes it
- *   frontier [B, F, 2*L*d]         model dtype, F = csa_frontier_slots(ratio): ring of the
- *                                  projected (kv | gate) rows of the last F tokens, slot t mod F;
- *                                  read for tokens before pos[b], rewritten for the last tokens
+ *   frontier [B, F, 2*L*d]         model dtype, F = csa_frontier_slots(ratio) + layer->rollback:
+ *                                  ring of the projected (kv | gate) rows of the last F tokens,
+ *                                  slot t mod F; read for tokens before pos[b], rewritten for the
+ *                                  last tokens
  *   pool     [B, cap, d]           model dtype, rows [0, n_rows[b]) valid
  *   n_rows   [B] int32 (device)    in/out; must equal floor(pos[b] / ratio) on entry
  *   inv_freq [R/2] fp32
@@ -217,7 +226,16 @@ csa_status csa_index_topk(const csa_layer* layer, const void* iq, const void* iw
  * caller orders the compress call after any earlier use of the index pool, and
  * must not start another call that writes ikeys or n_rows for these sequences
  * before this one completes.  Shapes the tensor-core scan does not cover, or
- * cap > 16384, run the whole call after the event. */
+ * cap > 16384, run the whole call after the event.
+ * One stream, no event: enqueued right after csa_compress_append(_pair) for the
+ * same token on the same stream, with pool_ready NULL, stage 1 runs beside that
+ * call's kernels: it does not wait for the kernels before it (it reads only the
+ * rows complete before the token and the step's inputs, and writes only its
+ * workspace) and waits for them at its end, and the compress call's projection
+ * kernel lets its successors start only once all earlier work in the stream
+ * is complete.  Enqueued behind anything else, stage 1's inputs must be complete
+ * and its workspace free when it is enqueued behind work that does not trigger
+ * early. */
 csa_status csa_index_topk_overlapped(const csa_layer* layer, const void* iq, const void* iw, int B, const void* ikeys,
                                      int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
                                      int32_t* sel, int32_t* n_sel, void* ws, size_t ws_bytes, int32_t* err,
@@ -240,7 +258,8 @@ csa_status csa_index_topk_overlapped(const csa_layer* layer, const void* iq, con
  * Arguments
  *   q [B, H, D], kv_new [B, D]   model dtype
  *   sink [H] fp32
- *   window [B, W, D]             model dtype ring, slot t mod W (written at slot p mod W)
+ *   window [B, Wr, D]            model dtype ring, Wr = W + layer->rollback, slot t mod Wr
+ *                                (written at slot p mod Wr)
  *   pool [B, cap, D]             model dtype
  *   n_rows, n_sel, pos [B] int32 (device); sel [B, topk] int32 or NULL
  *   out [B, H, D]                model dtype
@@ -259,12 +278,12 @@ csa_status csa_attend_decode(const csa_layer* layer, const void* q, const void* 
  * AND-ed with the visibility mask; aidiffuser: build the membership from the
  * index list rather than a dense compare), plus its window tokens: ring
  * entries for tokens before pos0, the chunk's own kv_new roped at their
- * positions otherwise.  After the chunk the window ring holds its last W
- * tokens.  Same formulas as csa_attend_decode / csa_index_topk per query.
+ * positions otherwise.  After the chunk the window ring holds its last
+ * W + rollback tokens.  Same formulas as csa_attend_decode / csa_index_topk per query.
  * Arguments
  *   q [T, H, D], kv_new [T, D], iq [T, Hi, Di], iw [T, Hi]   model dtype (iq, iw,
  *                                  ikeys may be NULL when ratio != 4)
- *   sink [H] fp32; pos0 host int; window [W, D]; pool [cap, D]; ikeys [cap, Di]
+ *   sink [H] fp32; pos0 host int; window [W + rollback, D]; pool [cap, D]; ikeys [cap, Di]
  *   n_rows int32 (device, one value)
  *   out [T, H, D]; sel_out [T, topk] int32 or NULL (the selected rows, -1 padded)
  * Requires 1 <= T <= 16384 and ratio == 4 or no indexer use. */
@@ -273,6 +292,34 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                     const void* pool, const void* ikeys, int cap, const int32_t* n_rows,
                                     const float* inv_freq, void* out, int32_t* sel_out, void* ws, size_t ws_bytes,
                                     int32_t* err, void* stream);
+
+/* csa_trim — rewind sequences by n_back[b] tokens, exactly (speculative decoding:
+ * the rejected draft tokens are taken back).
+ *
+ * Definition ([MTPLX#216], the MTP / speculative-lane post: the cache trim rewinds
+ * every lane exactly; emitted compressed rows are truncated, since a row depends
+ * only on its one completed window; the compressor frontiers are rebuilt from a
+ * bounded journal of their own projected rows; the sliding window keeps
+ * rollback_capacity extra rows, since an evicted row cannot be recovered; asked
+ * to go further, trim refuses instead of clamping).  Here the journal and the
+ * extra window rows are the layer's rollback slots (csa_layer.rollback), so a
+ * trim moves no data: with p = pos[b] and p' = p - n_back[b],
+ *   hw[b]       = max(hw[b], p)          (the highest position the sequence reached)
+ *   refuse      if n_back[b] < 0, p' < 0, p' < hw[b] - rollback, or n_rows[b] != p / ratio
+ *   pos[b]      = p'
+ *   n_rows[b]   = p' / ratio  (for n_rows_a and, when given, n_rows_i)
+ * After it, decoding tokens from p' gives bit for bit what the sequence would
+ * have given had the rewound tokens never been decoded: the frontier ring still
+ * holds the projections of the ratio-window tokens before p', the window ring
+ * the W tokens before p', and pool rows past the new n_rows are rewritten when
+ * their windows complete again.
+ * Arguments (device, int32 [B]): n_back; pos, n_rows_a (attention pool) and
+ * n_rows_i (index pool; NULL for layers without an indexer) in/out; hw in/out,
+ * caller-owned, set to the sequence's position when it starts (0 for a new one).
+ * A refused sequence is left entirely unchanged and CSA_DEV_ROLLBACK (or
+ * CSA_DEV_STATE) is OR-ed into err.  One small kernel on `stream`. */
+csa_status csa_trim(const csa_layer* layer, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
+                    int32_t* n_rows_i, int32_t* hw, int32_t* err, void* stream);
 
 /* csa_index_topk_static — csa_index_topk without a caller-supplied workspace.
  *

@@ -43,6 +43,11 @@ Readings where the pages are silent (each also listed with the design notes):
   R10 a compress call whose sequence state is inconsistent (n_rows !=
       floor(pos/ratio)), or that would emit a row at or beyond the pool
       capacity, changes nothing for that sequence and raises an error bit.
+  R15 rollback: the window ring and the frontier rings may hold extra slots
+      (the rollback margin, whose frontier slots are the journal of projected
+      rows); every ring is indexed modulo its own length, so extra slots change
+      no result.  A trim back to position p' is refused unless p' >= 0 and
+      p' >= (the highest position the sequence reached) - rollback.
 """
 from __future__ import annotations
 
@@ -54,6 +59,7 @@ import numpy as np
 ERR_CAPACITY = 1
 ERR_STATE = 2
 ERR_RANGE = 4
+ERR_ROLLBACK = 8
 
 
 # --------------------------------------------------------------------------
@@ -101,6 +107,7 @@ class Layer:
     X: int
     scale: float | None = None  # default D^-1/2 (R3)
     rms_eps: float = 1e-6  # (R3)
+    rollback: int = 0  # tokens trim() may rewind (R15)
 
     @property
     def lanes(self) -> int:
@@ -253,7 +260,8 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
     [B,cap,d]; n_rows [B].  Row j is emitted when token (j+1)*ratio-1 arrives
     (R2), so rows built one token at a time equal rows built from a chunk
     ([mlx-lm#1189] stepnoy "Fix" 3: the chunk tail is buffered and replayed, the
-    absolute position accumulates).  ``proj`` = (kv [B,T,L*d], g [B,T,L*d])
+    absolute position accumulates).  F is the frontier ring's own length (the
+    base slots, plus the rollback journal when the layer keeps one, R15).  ``proj`` = (kv [B,T,L*d], g [B,T,L*d])
     optionally supplies the stored projections of the new tokens instead of
     computing them from x (so pooling can be checked on given inputs).
     Returns (frontier, pool, n_rows, err).
@@ -263,7 +271,7 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
     pool = np.array(pool, dtype=np.float64)
     n_rows = np.array(n_rows, dtype=np.int64)
     B, T, _ = x.shape
-    r, F, cap = layer.ratio, layer.frontier_slots, pool.shape[1]
+    r, F, cap = layer.ratio, frontier.shape[1], pool.shape[1]
     Ld = layer.lanes * comp.d
     if proj is None:
         kv_all, g_all = project(layer, comp, x)
@@ -421,19 +429,21 @@ def window_tokens(layer: Layer, p: int) -> range:
 def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq):
     """One decode step's attention for every sequence.
 
-    Appends RoPE(kv_new, p) to the window ring (slot p mod W), then attends
-    q roped at p over the selected pool rows (``sel`` None: every visible row,
-    the ratio-128 / dense layers) plus the window tokens [p-W+1, p].
+    Appends RoPE(kv_new, p) to the window ring (slot p mod the ring's length:
+    W, plus the rollback margin when kept, R15), then attends q roped at p over
+    the selected pool rows (``sel`` None: every visible row, the ratio-128 /
+    dense layers) plus the window tokens [p-W+1, p].
     Returns (out [B,H,D], window, err).  A selected index outside [0, n_rows)
     raises ERR_RANGE and is skipped.
     """
     window = np.array(window, dtype=np.float64)
     B = len(pos)
+    Wr = window.shape[1]
     out = np.zeros((B, layer.H, layer.D))
     err = 0
     for b in range(B):
         p = int(pos[b])
-        window[b, p % layer.W] = store(rope(kv_new[b], p, inv_freq), layer.dtype)
+        window[b, p % Wr] = store(rope(kv_new[b], p, inv_freq), layer.dtype)
         if sel is None:
             rows = np.arange(visible_rows(layer, int(n_rows[b]), p))
         else:
@@ -442,7 +452,7 @@ def attend_decode(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_se
             if bad.any():
                 err |= ERR_RANGE
                 rows = rows[~bad]
-        keys = [pool[b][rows]] + [window[b, t % layer.W][None] for t in window_tokens(layer, p)]
+        keys = [pool[b][rows]] + [window[b, t % Wr][None] for t in window_tokens(layer, p)]
         keys = np.concatenate(keys, axis=0)
         qr = store(rope(q[b], p, inv_freq), layer.dtype)
         out[b] = output_rows(layer, attend(layer, qr, keys, sink), p, inv_freq)
@@ -460,14 +470,14 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0, window, po
     aidiffuser: a membership scatter instead of one shared gathered set).
     Window keys older than the chunk come from the ring; chunk tokens are
     roped at their own positions.  After the chunk the ring holds its last W
-    tokens.  ``queries`` optionally restricts which chunk offsets are computed
+    tokens (its last W + rollback when the ring keeps a rollback margin, R15).  ``queries`` optionally restricts which chunk offsets are computed
     (for sampled checks at full size); the others stay zero.
     Returns (out [T,H,D], sel [T,topk] (-1 padding), n_sel [T], window).
     """
     q = np.asarray(q, dtype=np.float64)
     T = q.shape[0]
     window = np.array(window, dtype=np.float64)
-    W, k = layer.W, layer.topk
+    W, Wr, k = layer.W, window.shape[0], layer.topk
     kvr = [store(rope(kv_new[i], pos0 + i, inv_freq), layer.dtype) for i in range(T)]
     out = np.zeros((T, layer.H, layer.D))
     sel = -np.ones((T, k), dtype=np.int64)
@@ -481,12 +491,12 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0, window, po
         if layer.has_indexer:
             sel[i, :len(rows)] = rows
             n_sel[i] = len(rows)
-        win = [window[t % W] if t < pos0 else kvr[t - pos0] for t in window_tokens(layer, p)]
+        win = [window[t % Wr] if t < pos0 else kvr[t - pos0] for t in window_tokens(layer, p)]
         keys = np.concatenate([pool[rows], np.stack(win)], axis=0)
         qr = store(rope(q[i], p, inv_freq), layer.dtype)
         out[i] = output_rows(layer, attend(layer, qr, keys, sink), p, inv_freq)
-    for t in range(max(pos0, pos0 + T - W), pos0 + T):
-        window[t % W] = kvr[t - pos0]
+    for t in range(max(pos0, pos0 + T - Wr), pos0 + T):
+        window[t % Wr] = kvr[t - pos0]
     return out, sel, n_sel, window
 
 
@@ -520,3 +530,38 @@ def decode_step(layer: Layer, comp_a: Compressor, comp_i: Compressor | None, st:
     err |= e
     st["pos"] = np.asarray(st["pos"]) + 1
     return out, sel, n_sel, err
+
+
+# --------------------------------------------------------------------------
+# exact trim (speculative decoding's rejection repair)
+# --------------------------------------------------------------------------
+
+def trim(layer: Layer, st: dict, n_back, hw):
+    """Rewind each sequence b by n_back[b] tokens ([MTPLX#216], the MTP /
+    speculative-lane post: the cache trim rewinds every lane exactly; compressed
+    rows are truncated, since each depends only on its own completed window; the
+    compressor frontiers are rebuilt from a bounded journal of projected rows;
+    the window keeps rollback_capacity extra rows; beyond that bound trim refuses
+    rather than clamps).  With the journal and the extra window rows kept in the
+    rings' rollback slots (R15) nothing is copied: the position and both row
+    counts move back, and the rings and pools keep the older entries the next
+    tokens need.  ``hw`` holds each sequence's highest position so far (updated
+    here); a sequence whose trim is refused keeps its whole state.  Returns the
+    error bits (ERR_ROLLBACK, ERR_STATE)."""
+    err = 0
+    pos = np.array(st["pos"], dtype=np.int64)
+    n_rows = np.array(st["n_rows"], dtype=np.int64)
+    for b in range(len(pos)):
+        p, n = int(pos[b]), int(n_back[b])
+        h = max(int(hw[b]), p)
+        if p < 0 or n_rows[b] != p // layer.ratio:
+            err |= ERR_STATE
+            continue
+        if n < 0 or p - n < 0 or p - n < h - layer.rollback:
+            err |= ERR_ROLLBACK
+            continue
+        hw[b] = h
+        pos[b] = p - n
+        n_rows[b] = (p - n) // layer.ratio
+    st["pos"], st["n_rows"] = pos, n_rows
+    return err

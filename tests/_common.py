@@ -16,7 +16,7 @@ def f64(t):
 
 def oracle_layer(cfg: csa_synth.Config) -> O.Layer:
     return O.Layer(dtype=cfg.dtype, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
-                   Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+                   Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps, rollback=cfg.rollback)
 
 
 def oracle_comp(c: csa_synth.Compressor) -> O.Compressor:

@@ -49,7 +49,7 @@ def dev(t):
 
 def lib_layer(cfg: csa_synth.Config) -> csa.Layer:
     return csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
-                     topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+                     topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps, rollback=cfg.rollback)
 
 
 def lib_comp(c: csa_synth.Compressor) -> csa.Compressor:

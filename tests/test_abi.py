@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(lib):
 
 def _layer(**kw):
     base = dict(dtype=B.CSA_BF16, H=64, D=512, R=64, W=128, ratio=4, Hi=64, Di=128, topk=512, X=4096, scale=0.0,
-                rms_eps=1e-6)
+                rms_eps=1e-6, rollback=0)
     base.update(kw)
     return B._Layer(*[base[f] for f, _ in B._Layer._fields_])
 
@@ -95,6 +95,11 @@ def test_host_validation_fails_closed(lib):
     # decode attention: selections on a layer without an indexer are rejected
     assert lib.csa_attend_decode(ctypes.byref(L128), FAKE, FAKE, FAKE, 1, FAKE, FAKE, 10, FAKE, FAKE, FAKE, FAKE,
                                  FAKE, FAKE, FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_ARG
+    # trim: a negative rollback capacity, null state pointers, a layer with an indexer without its n_rows
+    assert lib.csa_trim(ctypes.byref(_layer(rollback=-1)), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_trim(ctypes.byref(L), 2, FAKE, None, FAKE, FAKE, FAKE, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_trim(ctypes.byref(L), 2, FAKE, FAKE, FAKE, None, FAKE, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_trim(ctypes.byref(L), 0, None, None, None, None, None, None, None) == B.CSA_OK
     # prefill: chunk length bounds and a too-small workspace
     args = (FAKE, FAKE, FAKE, FAKE, FAKE)
     assert lib.csa_attend_prefill_chunk(ctypes.byref(L), *args, 0, 0, FAKE, FAKE, FAKE, 10, FAKE, FAKE, FAKE, None,

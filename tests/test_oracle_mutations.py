@@ -31,8 +31,10 @@ def _pin_functions():
         params = [m for m in marks if m.name == "parametrize"]
         if params:
             argname, values = params[0].args
+            names = [a.strip() for a in argname.split(",")]
             for v in values:
-                out.append((f"{name}[{v}]", fn, {argname: v}))
+                kw = dict(zip(names, v)) if len(names) > 1 else {names[0]: v}
+                out.append((f"{name}[{v}]", fn, kw))
         else:
             out.append((name, fn, {}))
     return out
@@ -315,6 +317,38 @@ def m_project_not_stored(layer, comp, x):
     return x @ comp.wkv.T, x @ comp.wgate.T
 
 
+def m_trim_keeps_rows(layer, st, n_back, hw):
+    n_rows = np.array(st["n_rows"])
+    err = _orig["trim"](layer, st, n_back, hw)
+    st["n_rows"] = n_rows
+    return err
+
+
+def m_trim_margin_off_by_one(layer, st, n_back, hw):
+    wide = O.Layer(**{**vars(layer), "rollback": layer.rollback + 1})
+    return _orig["trim"](wide, st, n_back, hw)
+
+
+def m_trim_forgets_high_water(layer, st, n_back, hw):
+    return _orig["trim"](layer, st, n_back, np.array(st["pos"], dtype=np.int64))
+
+
+def m_window_ring_mod_W(layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq):
+    window = np.array(window, dtype=np.float64)
+    Wr = window.shape[1]
+    if Wr == layer.W:
+        return _orig["attend_decode"](layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq)
+    # reads and writes the ring modulo W instead of its own length
+    small = window[:, :layer.W].copy()
+    for b in range(window.shape[0]):
+        for t in range(max(0, int(pos[b]) - layer.W), int(pos[b])):
+            small[b, t % layer.W] = window[b, t % Wr]
+    out, small, err = _orig["attend_decode"](layer, q, kv_new, sink, small, pool, n_rows, sel, n_sel, pos, inv_freq)
+    p = int(pos[0])
+    window[0, p % layer.W] = small[0, p % layer.W]
+    return out, window, err
+
+
 def m_store_noop(x, dtype):
     return np.asarray(x, dtype=np.float64)
 
@@ -369,6 +403,10 @@ MUTATIONS = {
     "kv/gate weights swapped": ("project", m_project_swapped),
     "projection contracts the weights' columns": ("project", m_project_transposed),
     "projections not rounded to the model dtype": ("project", m_project_not_stored),
+    "trim keeps the row counts": ("trim", m_trim_keeps_rows),
+    "trim margin one token too wide": ("trim", m_trim_margin_off_by_one),
+    "trim forgets the high-water mark": ("trim", m_trim_forgets_high_water),
+    "window ring indexed modulo W": ("attend_decode", m_window_ring_mod_W),
     "storage rounding skipped": ("store", m_store_noop),
     "bf16 rounding truncates": ("round_bf16", m_round_bf16_truncate),
 }

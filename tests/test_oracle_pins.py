@@ -500,3 +500,103 @@ def test_decode_equals_prefill_mid_sequence():
 
 def test_decode_equals_prefill_ratio128():
     _decode_vs_prefill(ratio=128, T=140, ctx_tokens=130, topk=16)
+
+
+# --------------------------------------------------------------------------- exact trim (R15)
+
+def _rollback_setup(ratio, rollback, W=8, topk=5, seed=31):
+    layer = _tiny_layer(ratio=ratio, W=W, topk=topk, rollback=rollback)
+    rng = np.random.default_rng(seed)
+    ca = _tiny_comp(layer, layer.D, rng)
+    ci = _tiny_comp(layer, layer.Di, rng) if layer.has_indexer else None
+    invf = _inv_freq(layer.R)
+    sink = rng.standard_normal(layer.H)
+    return layer, ca, ci, invf, sink, rng
+
+
+def _empty_state(layer, cap, extra):
+    """One sequence's empty state with `extra` rollback slots in every ring."""
+    L = layer.lanes
+    F = layer.frontier_slots + extra
+    return dict(pool=np.zeros((1, cap, layer.D)), ikeys=np.zeros((1, cap, layer.Di)),
+                window=np.zeros((1, layer.W + extra, layer.D)),
+                front_a=np.zeros((1, F, 2 * L * layer.D)), front_i=np.zeros((1, F, 2 * L * layer.Di)),
+                n_rows=np.zeros(1, dtype=np.int64), pos=np.zeros(1, dtype=np.int64))
+
+
+def _tokens(layer, rng, n):
+    return [(rng.standard_normal((1, 1, layer.X)), rng.standard_normal((1, layer.H, layer.D)),
+             rng.standard_normal((1, layer.D)), rng.standard_normal((1, layer.Hi, layer.Di)),
+             rng.standard_normal((1, layer.Hi))) for _ in range(n)]
+
+
+def _decode(layer, ca, ci, st, tok, sink, invf):
+    out, sel, n_sel, err = O.decode_step(layer, ca, ci, st, tok, sink, invf)
+    assert err == 0
+    return out, (None if sel is None else list(sel[0, :n_sel[0]]))
+
+
+@pytest.mark.parametrize("ratio,n_true,drafts", [
+    (4, 40, [(9, 3), (18, 4), (21, 2), (30, 6)]),  # drafts crossing emissions at 12, 20, 24 and 32; dense->sparse at 23
+    (128, 300, [(125, 5), (254, 6)]),               # drafts crossing the ratio-128 emissions at 128 and 256
+])
+def test_trim_then_redecode_equals_never_decoded(ratio, n_true, drafts):
+    """R15 against its definition: decoding k draft tokens, trimming them and decoding the true tokens gives, step
+    for step, exactly the outputs, selections and state of decoding only the true tokens (with or without rollback
+    slots in the rings)."""
+    R = 6
+    layer, ca, ci, invf, sink, rng = _rollback_setup(ratio, R)
+    true = _tokens(layer, rng, n_true)
+    cap = n_true // ratio + 4
+    ref = _empty_state(layer, cap, 0)  # no rollback slots: rings of exactly W / frontier_slots
+    ref_out = [_decode(layer, ca, ci, ref, t, sink, invf) for t in true]
+    st = _empty_state(layer, cap, R)
+    hw = np.zeros(1, dtype=np.int64)
+    at = dict(drafts)
+    for i, t in enumerate(true):
+        if i in at:
+            k = at[i]
+            for d in _tokens(layer, rng, k):
+                _decode(layer, ca, ci, st, d, sink, invf)
+            assert O.trim(layer, st, np.array([k]), hw) == 0
+            assert int(st["pos"][0]) == i and int(st["n_rows"][0]) == i // ratio
+        out, sel = _decode(layer, ca, ci, st, t, sink, invf)
+        assert np.array_equal(out, ref_out[i][0]), f"step {i}"
+        assert sel == ref_out[i][1], f"step {i} selection"
+    n = int(ref["n_rows"][0])
+    assert int(st["n_rows"][0]) == n and int(st["pos"][0]) == n_true
+    assert np.array_equal(st["pool"][:, :n], ref["pool"][:, :n])
+    if layer.has_indexer:
+        assert np.array_equal(st["ikeys"][:, :n], ref["ikeys"][:, :n])
+    Wr, F = layer.W + R, layer.frontier_slots + R
+    for tk in range(n_true - layer.W, n_true):  # the window tokens the next query attends
+        assert np.array_equal(st["window"][0, tk % Wr], ref["window"][0, tk % layer.W])
+    for tk in range(n_true - layer.frontier_slots, n_true):  # the frontier entries the next emission pools
+        assert np.array_equal(st["front_a"][0, tk % F], ref["front_a"][0, tk % layer.frontier_slots])
+
+
+def test_trim_refuses_beyond_the_margin():
+    """R15: a trim past the rollback margin, below position 0, by a negative count, or on an inconsistent state is
+    refused and changes nothing; the margin counts from the highest position reached, so two trims of 4 after
+    decoding 6 draft tokens exceed a margin of 6 even though each alone would not."""
+    layer, ca, ci, invf, sink, rng = _rollback_setup(4, 6)
+    st = _empty_state(layer, 16, 6)
+    hw = np.zeros(1, dtype=np.int64)
+    for t in _tokens(layer, rng, 20):
+        _decode(layer, ca, ci, st, t, sink, invf)
+    snap = {k: v.copy() for k, v in st.items()}
+    for n in (7, 21, -1):
+        assert O.trim(layer, st, np.array([n]), hw) == O.ERR_ROLLBACK
+        assert all(np.array_equal(st[k], snap[k]) for k in st)
+    assert O.trim(layer, st, np.array([4]), hw) == 0 and int(hw[0]) == 20
+    for t in _tokens(layer, rng, 2):  # back to 18, still below the high-water mark 20
+        _decode(layer, ca, ci, st, t, sink, invf)
+    assert O.trim(layer, st, np.array([5]), hw) == O.ERR_ROLLBACK  # 13 < 20 - 6
+    assert O.trim(layer, st, np.array([4]), hw) == 0 and int(st["pos"][0]) == 14
+    st["n_rows"][0] += 1
+    assert O.trim(layer, st, np.array([1]), hw) == O.ERR_STATE
+    zero = _rollback_setup(4, 0)[0]
+    st2 = _empty_state(zero, 16, 0)
+    st2["pos"][0], st2["n_rows"][0] = 8, 2
+    assert O.trim(zero, st2, np.array([1]), np.zeros(1, dtype=np.int64)) == O.ERR_ROLLBACK  # no margin: no trim
+    assert O.trim(zero, st2, np.array([0]), np.zeros(1, dtype=np.int64)) == 0
