@@ -476,6 +476,121 @@ class ModelStep:
             ev[1].record()
 
 
+class ConsumerLayer:
+    """A layer that owns no compressor (DeepSeek-V4.1 cross-layer sharing): its own queries, new token, sinks,
+    window ring and workspaces; the owner's compressed rows, index keys, row counts and positions.  kind "index":
+    its own top-k over the owner's index keys (an index-source layer); "plain": the owner's selection."""
+
+    def __init__(self, owner, kind: str, n_inputs: int, device, tag: int):
+        import torch
+
+        import csa_synth
+        csa, cfg = owner.csa, owner.cfg
+        self.owner, self.kind, self.csa, self.cfg = owner, kind, csa, cfg
+        c = cfg.replace(cid=cfg.cid + 700 + tag)
+        d = lambda t: t.to(device).contiguous()  # noqa: E731
+        self.inputs = []
+        for i in range(n_inputs):
+            si = csa_synth.step_inputs(c, i)
+            self.inputs.append({k: d(getattr(si, k)) for k in ("q", "kv", "iq", "iw")})
+        self.window = owner.window.clone()
+        self.sink = d(csa_synth.sinks(c))
+        B, cap = cfg.B, owner.cap
+        self.sel = torch.empty(B, cfg.topk, dtype=torch.int32, device=device)
+        self.n_sel = torch.empty(B, dtype=torch.int32, device=device)
+        self.out = torch.empty(B, cfg.H, cfg.D, dtype=cfg.storage, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=device)  # noqa: E731
+        self.ws_i = u8(csa.workspace_size(owner.L, csa.OP_INDEX_TOPK, B, 1, cap))
+        self.ws_a = u8(csa.workspace_size(owner.L, csa.OP_ATTEND_DECODE, B, 1, cap))
+
+    def step(self, i):
+        o, csa = self.owner, self.csa
+        inp = self.inputs[i % len(self.inputs)]
+        if self.kind == "index":
+            csa.index_topk(o.L, inp["iq"], inp["iw"], o.ikeys, o.n_i, o.pos, o.invf, self.sel, self.n_sel,
+                           ws=self.ws_i, err=self.err)
+            sel, n_sel = self.sel, self.n_sel
+        else:
+            sel, n_sel = o.sel, o.n_sel
+        csa.attend_decode(o.L, inp["q"], inp["kv"], self.sink, self.window, o.pool, o.n_a, sel, n_sel, o.pos, o.invf,
+                          self.out, ws=self.ws_a, err=self.err)
+
+
+SHARED_PATTERN = ("owner", "plain", "plain", "index", "index", "index", "plain", "plain")
+
+
+def shared_line(csa, csa_synth, dev, flush, steps: int, warmup: int) -> dict:
+    """A DeepSeek-V4.1-style model step of 8 layers sharing one owner's caches (the README's pattern: one
+    compressor-owning layer, then layers consuming its caches, a run of them index-source layers), B = 32 on 32K
+    caches, one CUDA graph per model step, the L2 flushed before each, timed like the headline."""
+    import torch
+    cfg = csa_synth.CONFIGS[3]
+    cap = cfg.ctx // cfg.ratio + (warmup + steps + 8) // cfg.ratio + 8
+    owner = DecodeWorkload(cfg, cap, 4, dev, serial_indexer=True)
+    layers = [ConsumerLayer(owner, k, 4, dev, i) for i, k in enumerate(SHARED_PATTERN) if k != "owner"]
+
+    class _Step:
+        def __init__(self):
+            self.graphs = None
+
+        def step(self, i):
+            inp = owner.inputs[i % 4]
+            owner.front(inp)
+            owner.attend(inp, advance=False)
+            for c in layers:
+                c.step(i)
+            csa.advance_positions(owner.pos, 1)
+
+        def replay(self, i, ev=None):
+            if ev is not None:
+                ev[0].record()
+            self.graphs[i % 4].replay()
+            if ev is not None:
+                ev[1].record()
+
+    ms = _Step()
+    ms.step(0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    ms.graphs = []
+    with torch.cuda.stream(s):
+        for i in range(4):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                ms.step(i)
+            ms.graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for i in range(warmup):
+        ms.replay(1 + i)
+    n0 = owner.n_a.float().mean().item()
+    t = time_model_steps(ms, 1 + warmup, steps, flush)
+    n1 = owner.n_a.float().mean().item()
+    assert owner.err.item() == 0 and all(c.err.item() == 0 for c in layers)
+    nl = len(SHARED_PATTERN)
+    per_step_ms = statistics.mean(t)
+    n = 0.5 * (n0 + n1)
+    full = step_bytes(cfg, n)
+    e = 2
+    rows = full["attended_rows"] + full["q_out"]
+    idx = full["index_keys"] + cfg.B * (cfg.Hi * cfg.Di * e + cfg.Hi * e + cfg.topk * 4)
+    by_kind = {"owner": full["total"], "index": rows + idx, "plain": rows}
+    total = sum(by_kind[k] for k in SHARED_PATTERN)
+    hbm, _, _ = _peaks()
+    gbs = total / (per_step_ms / 1e3) / 1e9
+    del layers, owner
+    return {"pattern": list(SHARED_PATTERN), "layer_steps_per_s": round(nl * 1e3 / per_step_ms, 1),
+            "tokens_per_s": round(cfg.B * nl * 1e3 / per_step_ms, 1), "us_per_layer_step": round(
+                1e3 * per_step_ms / nl, 2), "ms_per_model_step_p10_p50_p90": [round(x, 4) for x in _percentiles(t)],
+            "algorithmic_bytes_per_model_step": int(total),
+            "bytes_by_layer_kind": {k: int(v) for k, v in by_kind.items()},
+            "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "steps": steps,
+            "note": ("layer 0 owns the compressors and index keys; the others attend to its rows with their own "
+                     "queries, sinks and windows, index-source layers through their own top-k over its keys")}
+
+
 def step_bytes(cfg, n_rows_mean: float) -> dict:
     """Algorithmic HBM bytes of one decode step (each byte the step must move once)."""
     B, e = cfg.B, 2
@@ -727,6 +842,7 @@ def run_ours(args):
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
 
     trim = trim_line(csa, csa_synth, dev)
+    shared = None if args.no_other_configs else shared_line(csa, csa_synth, dev, flush, args.steps, args.warmup)
 
     # ---- the other decode workloads (configs 2 and 4), each as its own model step of nl layers
     others = None
@@ -783,6 +899,7 @@ def run_ours(args):
                 "prefill": prefill,
                 "other_decode_workloads": others,
                 "trim": trim,
+                "v41_shared_caches": shared,
             },
             "roofline": {
                 "kernel": (f"model step graph: every kernel of one decode step of {nl} layers (per layer: both "

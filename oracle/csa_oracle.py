@@ -48,6 +48,10 @@ Readings where the pages are silent (each also listed with the design notes):
       rows); every ring is indexed modulo its own length, so extra slots change
       no result.  A trim back to position p' is refused unless p' >= 0 and
       p' >= (the highest position the sequence reached) - rollback.
+  R16 cross-layer sharing (V4.1): a layer without a compressor keeps its own
+      window ring and attends to the most recent owner's compressed rows,
+      through its own top-k over the owner's index keys (index-source layers)
+      or through the owner's selection of the same step (the other layers).
 """
 from __future__ import annotations
 
@@ -565,3 +569,26 @@ def trim(layer: Layer, st: dict, n_back, hw):
         n_rows[b] = (p - n) // layer.ratio
     st["pos"], st["n_rows"] = pos, n_rows
     return err
+
+
+# --------------------------------------------------------------------------
+# cross-layer sharing (DeepSeek-V4.1)
+# --------------------------------------------------------------------------
+
+def consumer_decode_step(layer: Layer, owner: dict, window, step_in, sink, inv_freq, owner_sel=None):
+    """One decode step of a layer that owns no compressor ([v41-mlx], "Cross-layer sharing": a few layers own
+    the KV compressors and index keys and every other layer consumes the most recent owner's caches; the
+    index-source layers score their own queries against the owner's keys).  Reading R16: such a layer keeps its
+    own sliding-window ring (its own kv rows) and attends, with its own queries and sinks, to the owner's
+    compressed rows: through its own top-k over the owner's index keys when it is an index-source layer
+    (``owner_sel`` None), else through the owner's selection of this step (``owner_sel`` = (sel, n_sel)).  It
+    writes none of the owner's state.  ``owner`` holds the owner's pool, ikeys, n_rows after this step's
+    compress calls, and the step's positions.  Returns (out, sel, n_sel, window, err)."""
+    x, q, kv, iq, iw = step_in
+    if owner_sel is None:
+        sel, n_sel = index_topk(layer, iq, iw, owner["ikeys"], owner["n_rows"], owner["pos"], inv_freq)
+    else:
+        sel, n_sel = owner_sel
+    out, window, err = attend_decode(layer, q, kv, sink, window, owner["pool"], owner["n_rows"], sel, n_sel,
+                                     owner["pos"], inv_freq)
+    return out, sel, n_sel, window, err

@@ -349,6 +349,14 @@ def m_window_ring_mod_W(layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel
     return out, window, err
 
 
+def m_consumer_reselects(layer, owner, window, step_in, sink, inv_freq, owner_sel=None):
+    return _orig["consumer_decode_step"](layer, owner, window, step_in, sink, inv_freq, None)
+
+
+def m_consumer_own_window_ignored(layer, owner, window, step_in, sink, inv_freq, owner_sel=None):
+    return _orig["consumer_decode_step"](layer, owner, np.zeros_like(window), step_in, sink, inv_freq, owner_sel)
+
+
 def m_store_noop(x, dtype):
     return np.asarray(x, dtype=np.float64)
 
@@ -407,6 +415,8 @@ MUTATIONS = {
     "trim margin one token too wide": ("trim", m_trim_margin_off_by_one),
     "trim forgets the high-water mark": ("trim", m_trim_forgets_high_water),
     "window ring indexed modulo W": ("attend_decode", m_window_ring_mod_W),
+    "plain consumer re-selects with its own queries": ("consumer_decode_step", m_consumer_reselects),
+    "consumer ignores its own window": ("consumer_decode_step", m_consumer_own_window_ignored),
     "storage rounding skipped": ("store", m_store_noop),
     "bf16 rounding truncates": ("round_bf16", m_round_bf16_truncate),
 }

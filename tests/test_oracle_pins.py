@@ -600,3 +600,43 @@ def test_trim_refuses_beyond_the_margin():
     st2["pos"][0], st2["n_rows"][0] = 8, 2
     assert O.trim(zero, st2, np.array([1]), np.zeros(1, dtype=np.int64)) == O.ERR_ROLLBACK  # no margin: no trim
     assert O.trim(zero, st2, np.array([0]), np.zeros(1, dtype=np.int64)) == 0
+
+
+# --------------------------------------------------------------------------- cross-layer sharing (R16)
+
+def test_consumer_layer_reads_the_owner_caches():
+    """R16: a consumer layer with the owner's own queries, new token and window reproduces the owner's selection and
+    output exactly (as an index-source layer and reusing the owner's selection alike); with its own queries it
+    selects through the owner's keys, equal to the indexer run directly on them; severing the sharing (an empty
+    pool in place of the owner's) changes the output, the negative control of the V4.1 port's tests."""
+    layer, ca, ci, invf, sink, rng = _rollback_setup(4, 0, topk=5)
+    st = _empty_state(layer, 16, 0)
+    for t in _tokens(layer, rng, 40):
+        _decode(layer, ca, ci, st, t, sink, invf)
+    tok = _tokens(layer, rng, 1)[0]
+    win0 = st["window"].copy()
+    out_o, sel_o, nsel_o, _ = O.decode_step(layer, ca, ci, st, tok, sink, invf)
+    owner = dict(pool=st["pool"], ikeys=st["ikeys"], n_rows=st["n_rows"], pos=st["pos"] - 1)
+    pool_before = st["pool"].copy()
+    for owner_sel in (None, (sel_o, nsel_o)):
+        out_c, sel_c, nsel_c, _, err = O.consumer_decode_step(layer, owner, win0.copy(), tok, sink, invf, owner_sel)
+        assert err == 0
+        assert np.array_equal(out_c, out_o) and np.array_equal(sel_c, sel_o)
+    assert np.array_equal(st["pool"], pool_before)
+    own = _tokens(layer, rng, 1)[0]
+    own_win = rng.standard_normal(win0.shape)
+    out_c, sel_c, nsel_c, _, _ = O.consumer_decode_step(layer, owner, own_win, own, sink, invf)
+    s2, n2 = O.index_topk(layer, own[3], own[4], owner["ikeys"], owner["n_rows"], owner["pos"], invf)
+    assert np.array_equal(sel_c, s2) and np.array_equal(nsel_c, n2)
+    out_p, sel_p, _, _, _ = O.consumer_decode_step(layer, owner, own_win, own, sink, invf, (sel_o, nsel_o))
+    assert np.array_equal(sel_p, sel_o)  # a plain consumer attends the owner's selection, not its own
+    keys = np.concatenate([owner["pool"][0][sel_o[0, :nsel_o[0]]]] +
+                          [O.store(O.rope(own[2][0], int(owner["pos"][0]), invf), layer.dtype)[None]
+                           if t == int(owner["pos"][0]) else own_win[0, t % layer.W][None]
+                           for t in O.window_tokens(layer, int(owner["pos"][0]))])
+    qr = O.store(O.rope(own[1][0], int(owner["pos"][0]), invf), layer.dtype)
+    ref = O.output_rows(layer, O.attend(layer, qr, keys, sink), int(owner["pos"][0]), invf)
+    assert np.allclose(out_p[0], ref, rtol=0, atol=0)
+    severed = dict(owner, pool=np.zeros_like(owner["pool"]))
+    out_s, _, _, _, _ = O.consumer_decode_step(layer, severed, own_win, own, sink, invf)
+    assert rel_err_rows(out_s, out_c) > 0.05
