@@ -591,6 +591,114 @@ def shared_line(csa, csa_synth, dev, flush, steps: int, warmup: int) -> dict:
                      "queries, sinks and windows, index-source layers through their own top-k over its keys")}
 
 
+class VerifyLayer:
+    """One layer's state for verify blocks of T tokens per sequence (config 3 shapes, rollback T - 1 + 8)."""
+
+    def __init__(self, cfg, T: int, cap: int, n_inputs: int, device, host, host_comp, pos, tag: int):
+        import torch
+
+        import csa_synth
+        import deepseek_v4_compressed_csa_gb300 as csa
+        self.csa, self.cfg, self.T = csa, cfg, T
+        self.L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
+                           Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps,
+                           rollback=cfg.rollback)
+        d = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
+
+        def comp(c):
+            return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
+        self.ca, self.ci = comp(host_comp[0]), comp(host_comp[1])
+        self.pool, self.ikeys, self.window = d(host.pool), d(host.ikeys), d(host.window)
+        self.front_a, self.front_i = d(host.front_attn), d(host.front_index)
+        self.n_a, self.n_i, self.pos = d(host.n_rows), d(host.n_rows), pos
+        self.sink, self.invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
+        B = cfg.B
+        self.inputs = []
+        for i in range(n_inputs):
+            si = [csa_synth.step_inputs(cfg, tag + T * i + j) for j in range(T)]
+            st = lambda f: d(torch.stack([getattr(x, f) for x in si], dim=1))  # noqa: E731
+            self.inputs.append(dict(x=d(torch.cat([x.x for x in si], dim=1)), q=st("q"), kv=st("kv"), iq=st("iq"),
+                                    iw=st("iw")))
+        self.sel = torch.empty(B, T, cfg.topk, dtype=torch.int32, device=device)
+        self.n_sel = torch.empty(B, T, dtype=torch.int32, device=device)
+        self.out = torch.empty(B, T, cfg.H, cfg.D, dtype=cfg.storage, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=device)  # noqa: E731
+        self.ws_pair = u8(csa.workspace_size(self.L, csa.OP_COMPRESS_PAIR, B, T, cap))
+        self.ws_i = u8(csa.workspace_size(self.L, csa.OP_INDEX_TOPK, B * T, 1, cap))
+        self.ws_a = u8(csa.workspace_size(self.L, csa.OP_ATTEND_DECODE, B * T, 1, cap))
+
+    def step(self, i):
+        csa, inp = self.csa, self.inputs[i % len(self.inputs)]
+        csa.compress_append_pair(self.L, self.ca, self.ci, inp["x"], self.pos, self.front_a, self.pool, self.n_a,
+                                 self.front_i, self.ikeys, self.n_i, self.invf, ws=self.ws_pair, err=self.err)
+        csa.index_topk_verify(self.L, inp["iq"], inp["iw"], self.ikeys, self.n_i, self.pos, self.invf, self.sel,
+                              self.n_sel, ws=self.ws_i, err=self.err)
+        csa.attend_verify(self.L, inp["q"], inp["kv"], self.sink, self.window, self.pool, self.n_a, self.sel,
+                          self.n_sel, self.pos, self.invf, self.out, ws=self.ws_a, err=self.err)
+
+
+def verify_line(csa, csa_synth, dev, flush, steps: int, warmup: int, nl: int, T: int = 4) -> dict:
+    """Verify blocks of T tokens per sequence (a speculative step with T - 1 drafts), B = 32 on 32K caches, as a
+    model step of nl layers in one CUDA graph, the positions advancing by T after the last layer."""
+    import torch
+    cfg = csa_synth.CONFIGS[3].replace(rollback=T - 1 + 8)
+    cap = cfg.ctx // cfg.ratio + T * (warmup + steps + 8) // cfg.ratio + 8
+    host = csa_synth.synth_cache(cfg, cap)
+    host_comp = (csa_synth.compressor(cfg, "attn"), csa_synth.compressor(cfg, "index"))
+    pos = host.pos.to(dev)
+    layers = [VerifyLayer(cfg, T, cap, 4, dev, host, host_comp, pos, 5000 + 100 * i) for i in range(nl)]
+
+    class _Step:
+        graphs = None
+
+        def step(self, i):
+            for layer in layers:
+                layer.step(i)
+            csa.advance_positions(pos, T)
+
+        def replay(self, i, ev=None):
+            if ev is not None:
+                ev[0].record()
+            self.graphs[i % 4].replay()
+            if ev is not None:
+                ev[1].record()
+
+    ms = _Step()
+    ms.step(0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    ms.graphs = []
+    with torch.cuda.stream(s):
+        for i in range(4):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                ms.step(i)
+            ms.graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for i in range(warmup):
+        ms.replay(1 + i)
+    n0 = layers[0].n_a.float().mean().item()
+    t = time_model_steps(ms, 1 + warmup, steps, flush)
+    n1 = layers[0].n_a.float().mean().item()
+    assert all(layer.err.item() == 0 for layer in layers)
+    per = statistics.mean(t) / nl
+    b = step_bytes(cfg, 0.5 * (n0 + n1))
+    # per layer-step: the weights and the index keys once (four queries share each key tile), every query's rows
+    total = b["weights"] + b["index_keys"] + T * (b["attended_rows"] + b["q_out"]) + T * b["small"]
+    hbm, _, _ = _peaks()
+    gbs = total / (per / 1e3) / 1e9
+    del layers
+    return {"T": T, "B": cfg.B, "layer_steps_per_s": round(1e3 / per, 1),
+            "verified_tokens_per_s": round(cfg.B * T * 1e3 / per, 1), "us_per_layer_step": round(1e3 * per, 2),
+            "us_per_layer_step_p10_p50_p90": [round(1e3 * x / nl, 2) for x in _percentiles(t)],
+            "algorithmic_bytes_per_layer_step": int(total), "achieved_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm, 4), "layers_per_step": nl, "steps": steps,
+            "calls": "per layer: csa_compress_append_pair (T tokens), csa_index_topk_verify, csa_attend_verify"}
+
+
 def step_bytes(cfg, n_rows_mean: float) -> dict:
     """Algorithmic HBM bytes of one decode step (each byte the step must move once)."""
     B, e = cfg.B, 2
@@ -843,6 +951,7 @@ def run_ours(args):
 
     trim = trim_line(csa, csa_synth, dev)
     shared = None if args.no_other_configs else shared_line(csa, csa_synth, dev, flush, args.steps, args.warmup)
+    verify = None if args.no_other_configs else verify_line(csa, csa_synth, dev, flush, args.steps, args.warmup, nl)
 
     # ---- the other decode workloads (configs 2 and 4), each as its own model step of nl layers
     others = None
@@ -900,6 +1009,7 @@ def run_ours(args):
                 "other_decode_workloads": others,
                 "trim": trim,
                 "v41_shared_caches": shared,
+                "verify_blocks": verify,
             },
             "roofline": {
                 "kernel": (f"model step graph: every kernel of one decode step of {nl} layers (per layer: both "
@@ -1078,7 +1188,17 @@ def main():
     ap.add_argument("--oracle-sample", nargs=5, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the 4096-token prefill chunk (for profiling its kernels); prints its record")
+    ap.add_argument("--verify-only", action="store_true",
+                    help="time only the verify-block model step (B 32, T 4; for profiling its kernels); prints its record")
     args = ap.parse_args()
+    if args.verify_only:
+        import torch
+        import csa_synth
+        import deepseek_v4_compressed_csa_gb300 as csa
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        print(json.dumps(verify_line(csa, csa_synth, dev, flush, args.steps, args.warmup, args.layers)))
+        return
     if args.prefill_only:
         import torch
         import csa_synth

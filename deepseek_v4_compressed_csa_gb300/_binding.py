@@ -27,7 +27,7 @@ STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_C
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
            "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions",
-           "csa_compress_append_pair", "csa_trim")
+           "csa_compress_append_pair", "csa_trim", "csa_index_topk_verify", "csa_attend_verify")
 
 
 class CSAError(RuntimeError):
@@ -91,6 +91,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_advance_positions.restype = i32
     lib.csa_trim.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_trim.restype = i32
+    lib.csa_index_topk_verify.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.csa_index_topk_verify.restype = i32
+    lib.csa_attend_verify.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.csa_attend_verify.restype = i32
     _lib = lib
     return lib
 
@@ -426,4 +430,63 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, windo
         ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(iq), _ptr(iw), _ptr(sink), T, int(pos0), _ptr(window),
         _ptr(pool), _ptr(ikeys), cap, _ptr(n_rows), _ptr(inv_freq), _ptr(out), _ptr(sel_out), _ptr(ws), nb,
         _ptr(err), _stream(stream)))
+    return err
+
+
+def index_topk_verify(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel, ws=None, err=None,
+                      stream=None):
+    """csa_index_topk_verify: iq [B, T, Hi, Di], iw [B, T, Hi]; sel [B, T, topk], n_sel [B, T]; pos [B] is the
+    position of each block's first token."""
+    _expect("iq", iq, layer.dtype)
+    if iq.dim() != 4 or iq.shape[2:] != (layer.Hi, layer.Di):
+        raise ValueError(f"iq: shape {tuple(iq.shape)}, expected [B, T, {layer.Hi}, {layer.Di}]")
+    B, T = iq.shape[0], iq.shape[1]
+    _expect("iw", iw, layer.dtype, (B, T, layer.Hi))
+    _expect("ikeys", ikeys, layer.dtype)
+    if ikeys.dim() != 3 or ikeys.shape[0] != B or ikeys.shape[2] != layer.Di:
+        raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [{B}, cap, {layer.Di}]")
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("sel", sel, torch.int32, (B, T, layer.topk))
+    _expect("n_sel", n_sel, torch.int32, (B, T))
+    _expect_err(err)
+    cap = ikeys.shape[1]
+    ws, nb = _ws(layer, OP_INDEX_TOPK, B * T, 1, cap, ws, iq.device)
+    err = _err(err, iq.device)
+    L = layer._c()
+    _check("csa_index_topk_verify", load_library().csa_index_topk_verify(
+        ctypes.byref(L), _ptr(iq), _ptr(iw), B, T, _ptr(ikeys), cap, _ptr(n_rows), _ptr(pos), _ptr(inv_freq),
+        _ptr(sel), _ptr(n_sel), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def attend_verify(layer: Layer, q, kv_new, sink, window, pool, n_rows, sel, n_sel, pos, inv_freq, out, ws=None,
+                  err=None, stream=None):
+    """csa_attend_verify: q [B, T, H, D], kv_new [B, T, D], out [B, T, H, D]; the block's tokens are written to the
+    window ring first (the layer needs rollback >= T - 1)."""
+    _expect("q", q, layer.dtype)
+    if q.dim() != 4 or q.shape[2:] != (layer.H, layer.D):
+        raise ValueError(f"q: shape {tuple(q.shape)}, expected [B, T, {layer.H}, {layer.D}]")
+    B, T = q.shape[0], q.shape[1]
+    _expect("kv_new", kv_new, layer.dtype, (B, T, layer.D))
+    _expect("sink", sink, torch.float32, (layer.H,))
+    _expect("window", window, layer.dtype, (B, layer.ring_slots, layer.D))
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 3 or pool.shape[0] != B or pool.shape[2] != layer.D:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {layer.D}]")
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("sel", sel, torch.int32, (B, T, layer.topk))
+    _expect("n_sel", n_sel, torch.int32, (B, T))
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("out", out, layer.dtype, (B, T, layer.H, layer.D))
+    _expect_err(err)
+    cap = pool.shape[1]
+    ws, nb = _ws(layer, OP_ATTEND_DECODE, B * T, 1, cap, ws, q.device)
+    err = _err(err, q.device)
+    L = layer._c()
+    _check("csa_attend_verify", load_library().csa_attend_verify(
+        ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(sink), B, T, _ptr(window), _ptr(pool), cap, _ptr(n_rows),
+        _ptr(sel), _ptr(n_sel), _ptr(pos), _ptr(inv_freq), _ptr(out), _ptr(ws), nb, _ptr(err), _stream(stream)))
     return err

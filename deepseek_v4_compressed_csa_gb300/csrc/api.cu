@@ -279,6 +279,48 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                            L.has_indexer() ? sel : nullptr, n_sel, inv_freq, out, aw, err, s));
 }
 
+csa_status csa_index_topk_verify(const csa_layer* layer, const void* iq, const void* iw, int B, int T,
+                                 const void* ikeys, int cap, const int32_t* n_rows, const int32_t* pos,
+                                 const float* inv_freq, int32_t* sel, int32_t* n_sel, void* ws, size_t ws_bytes,
+                                 int32_t* err, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
+  if (B < 1 || T < 1 || T > 64 || cap < 1 || (long long)B * T > (1 << 20)) return CSA_ERR_ARG;
+  if (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
+  if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(sel) || !dev_i32(n_sel) || !dev_i32(err)) return CSA_ERR_ARG;
+  const size_t need = ws_index(L, B * T, cap);
+  if (ws_bytes < need || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  IndexWs w = carve_index(c, L, B * T, cap);
+  // with device positions the index kernels take the queries per sequence in place of pos0
+  return cuda_status(launch_index_topk(L, iq, iw, B * T, ikeys, cap, n_rows, pos, T, inv_freq, sel, n_sel, w, err,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_attend_verify(const csa_layer* layer, const void* q, const void* kv_new, const float* sink, int B, int T,
+                             void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                             const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out, void* ws,
+                             size_t ws_bytes, int32_t* err, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!L.has_indexer() || !tc_attend_decode_supported(L)) return CSA_ERR_UNSUPPORTED;
+  if (B < 1 || T < 1 || T > 64 || cap < 1 || (long long)B * T > (1 << 20)) return CSA_ERR_ARG;
+  if (T - 1 > L.rollback) return CSA_ERR_ARG;  // the block's later tokens would overwrite window rows still attended
+  if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
+      !dev_tensor(inv_freq) || !dev_tensor(out))
+    return CSA_ERR_ARG;
+  if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(err) || !dev_i32(sel) || !dev_i32(n_sel)) return CSA_ERR_ARG;
+  const size_t need = ws_decode(L, B * T, cap);
+  if (ws_bytes < need || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  AttendWs w = carve_attend(c, L, B * T, attend_splits(L, false, false, cap), 0);
+  return cuda_status(launch_attend_verify(L, q, kv_new, sink, B, T, window, pool, cap, n_rows, sel, n_sel, pos,
+                                          inv_freq, out, w, err, static_cast<cudaStream_t>(stream)));
+}
+
 csa_status csa_trim(const csa_layer* layer, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
                     int32_t* n_rows_i, int32_t* hw, int32_t* err, void* stream) {
   Dims L;

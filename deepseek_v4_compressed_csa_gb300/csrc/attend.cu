@@ -448,6 +448,55 @@ static cudaError_t prefill_t(const Dims& L, const void* q, const void* kv_new, c
   return cudaGetLastError();
 }
 
+// Verify blocks: window[b][(pos[b] + i) mod Wr] = RoPE(kv_new[b][i], pos[b] + i) for the block's T tokens.  It lets
+// the next kernel start only once it has written the ring (no early trigger), since the attention kernel reads
+// window rows before its own programmatic wait.
+template <typename T>
+__global__ void k_window_append_block(const T* __restrict__ kv, T* __restrict__ window, int Wr, int D, int R, int T_,
+                                      const int32_t* __restrict__ pos, const float* __restrict__ inv_freq) {
+  pdl_wait();
+  const int b = blockIdx.x / T_, i = blockIdx.x % T_;
+  const int p = pos[b] + i;
+  if (pos[b] < 0) return;
+  const T* row = kv + (size_t)blockIdx.x * D;
+  T* dst = window + ((size_t)b * Wr + (p % Wr)) * D;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float v = to_f(row[c]);
+    if (c >= D - R) {
+      const int k = (c - (D - R)) >> 1;
+      float cs, sn;
+      rope_cs(p, inv_freq, k, &cs, &sn);
+      const float a = to_f(row[D - R + 2 * k]), bb = to_f(row[D - R + 2 * k + 1]);
+      v = ((c - (D - R)) & 1) ? fmaf(a, sn, bb * cs) : fmaf(a, cs, -bb * sn);
+    }
+    dst[c] = from_f<T>(v);
+  }
+}
+
+cudaError_t launch_attend_verify(const Dims& L, const void* q, const void* kv_new, const float* sink, int B, int T_,
+                                 void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                                 const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,
+                                 const AttendWs& ws, int32_t* err, cudaStream_t s) {
+  const int Q = B * T_;
+  const int S = tc_attend_decode_splits(Q, L.W, L.topk, ws.S);
+  if (S < 1 || S > 32) return cudaErrorNotSupported;
+  CSA_LAUNCH(k_window_append_block<__nv_bfloat16>, dim3(Q), dim3(128), 0, s,
+             static_cast<const __nv_bfloat16*>(kv_new), static_cast<__nv_bfloat16*>(window), L.Wr, L.D, L.R, T_, pos,
+             inv_freq);
+  // Many queries (more than one wave of split items): the pipelined kernel, a CTA per query streaming its tiles,
+  // with no partials to merge.  Few: the split decode kernel, whose items fill the SMs.
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if ((long)Q * S > sms)
+    return launch_tc_attend_prefill(L, q, pool, window, nullptr, sel, n_sel, n_rows, 0, cap, sink, inv_freq, Q, out,
+                                    err, s, pos, T_);
+  cudaError_t e = launch_tc_attend_decode(L, q, pool, window, kv_new, sel, n_sel, n_rows, pos, cap, sink, inv_freq, Q,
+                                          S, ws.part_ml, ws.part_acc, out, err, s, T_, true);
+  if (e != cudaSuccess || S == 1) return e;
+  return launch_tc_merge(L, ws.part_ml, ws.part_acc, S, Q, sink, pos, inv_freq, out, s, T_);
+}
+
 // pos[b] += by: the decode loop's position advance, launched with programmatic serialisation like every kernel
 // here, so it starts while the step's last kernel drains and only its store waits for it
 // No early trigger: the next kernel starts once the new positions are written, since kernels read the positions

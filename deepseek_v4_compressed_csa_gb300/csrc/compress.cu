@@ -419,6 +419,158 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
 }
 
+// A block of 2 <= T <= kBlockMax new tokens per sequence whose projections are split-K partials (a verify block of
+// a ratio-4 layer with two lanes): one CTA per sequence and pool.  The CTA sums each token's partials in split
+// order and rounds it to the model dtype (what the projection's own fix-up would store), holding the block's
+// tokens and the seven frontier entries before it in shared memory, so the frontier is read before any slot is
+// rewritten, whatever its length.  It then writes the newest min(T, F) tokens' frontier slots and pools every
+// window the block completes with the arithmetic of k_pool_emit_token (entries p-7 .. p in lane / APE order):
+// threads 0-255 pool (the others add zeros to the norm's reduction, which leaves it unchanged); all 1024 load,
+// so the partials take about two memory round trips.
+constexpr int kBlockMax = 16;
+constexpr int kBlockOld = 7;  // frontier entries before the block that a window it completes can need
+constexpr int kBlockThreads = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) k_pool_block(TokPool<T> pa, TokPool<T> pb, int B, int T_,
+                                                    const int32_t* __restrict__ pos, int32_t* err, int R, int F,
+                                                    float eps, const float* __restrict__ inv_freq, int ext_stride) {
+  pdl_trigger();
+  const bool second = blockIdx.x >= (unsigned)B;
+  int32_t* __restrict__ flags = second ? pb.flags : pa.flags;
+  int32_t* __restrict__ n_rows = second ? pb.n_rows : pa.n_rows;
+  T* __restrict__ frontier = second ? pb.frontier : pa.frontier;
+  const float* __restrict__ ape = second ? pb.ape : pa.ape;
+  const float* __restrict__ norm_w = second ? pb.norm_w : pa.norm_w;
+  T* __restrict__ pool = second ? pb.pool : pa.pool;
+  const float* __restrict__ part = second ? pb.part : pa.part;
+  const int d = second ? pb.d : pa.d, cap = second ? pb.cap : pa.cap;
+  const int splits = second ? pb.splits : pa.splits, part_stride = second ? pb.part_stride : pa.part_stride;
+  constexpr int ratio = 4, lanes = 2, kEnt = ratio * lanes;
+  // shared: [kBlockOld + T][ext_stride] entries (model dtype) from token p0 - 7 on, [d] pooled, [d] normed,
+  // 32 reduction slots
+  extern __shared__ float sm_blk[];
+  const int Ld = lanes * d, rowlen = 2 * Ld;
+  T* ext = reinterpret_cast<T*>(sm_blk);
+  float* u = reinterpret_cast<float*>(ext + (size_t)(kBlockOld + T_) * ext_stride);
+  float* y = u + d;
+  float* red = y + d;
+  const int b = blockIdx.x - (second ? B : 0), tid = threadIdx.x;
+  const int p0 = pos[b];
+  pdl_wait();
+  const int n = n_rows[b];
+  const int bad = compress_state_error(p0, n, T_, ratio, cap);
+  if (!bad) {
+    // the seven older entries (rows of tokens p0-7 .. p0-1 that exist) and the block's tokens
+    const T* fr = frontier + (size_t)b * F * rowlen;
+    for (int e = tid * 8; e < kBlockOld * rowlen; e += kBlockThreads * 8) {
+      const int k = e / rowlen, c = e % rowlen, t = p0 - kBlockOld + k;
+      if (t >= 0) copy8<T>(ext + (size_t)k * ext_stride + c, fr + (size_t)(t % F) * rowlen + c);
+    }
+    for (int e = tid * 4; e < T_ * rowlen; e += kBlockThreads * 4) {
+      const int i = e / rowlen, c = e % rowlen;
+      // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
+      constexpr int kBatch = 8;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < splits; s0 += kBatch) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+          if (s0 + k < splits)
+            v[k] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(s0 + k) * part_stride + b * T_ + i) *
+                                                                 rowlen + c));
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+          if (s0 + k < splits) {
+            if (s0 + k == 0) {
+              acc = v[k];
+            } else {
+              acc.x += v[k].x;
+              acc.y += v[k].y;
+              acc.z += v[k].z;
+              acc.w += v[k].w;
+            }
+          }
+      }
+      T* dst = ext + (size_t)(kBlockOld + i) * ext_stride + c;
+      dst[0] = from_f<T>(acc.x);
+      dst[1] = from_f<T>(acc.y);
+      dst[2] = from_f<T>(acc.z);
+      dst[3] = from_f<T>(acc.w);
+    }
+  }
+  __syncthreads();  // every thread has read n_rows and the frontier before either is written
+  if (tid == 0) {
+    flags[b] = !bad;
+    if (bad) atomicOr(err, bad);
+  }
+  if (bad) return;
+  {
+    const int keep = min(T_, F);
+    for (int e = tid * 8; e < keep * rowlen; e += kBlockThreads * 8) {
+      const int i = T_ - keep + e / rowlen, c = e % rowlen;
+      copy8<T>(frontier + ((size_t)b * F + (p0 + i) % F) * rowlen + c, ext + (size_t)(kBlockOld + i) * ext_stride + c);
+    }
+  }
+  // windows j completed by the block: token 4j + 3 in [p0, p0 + T), the first j = floor(p0 / 4)
+  for (int j = p0 / ratio; ratio * j + ratio - 1 < p0 + T_; ++j) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kTokChans; ++i) {
+      const int c = tid + 256 * i;
+      if (tid >= 256 || c >= d) continue;
+      float sv[kEnt], kk[kEnt];
+#pragma unroll
+      for (int e = 0; e < kEnt; ++e) {  // entry e: token 4j-4+e, APE row e mod 4, lane e / 4
+        const int t = ratio * j + ratio - kEnt + e;
+        if (t < 0) {
+          sv[e] = -INFINITY;
+          kk[e] = 0.f;
+        } else {
+          const T* row = ext + (size_t)(t - (p0 - kBlockOld)) * ext_stride + (e / ratio) * d + c;
+          sv[e] = to_f(row[Ld]) + __ldg(ape + (size_t)(e % ratio) * Ld + (e / ratio) * d + c);
+          kk[e] = to_f(row[0]);
+        }
+      }
+      float m = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kEnt; ++e) m = fmaxf(m, sv[e]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int e = 0; e < kEnt; ++e) {
+        const float x = (sv[e] == -INFINITY) ? 0.f : expf(sv[e] - m);
+        den += x;
+        num = fmaf(x, kk[e], num);
+      }
+      const float uc = rnd<T>(num / den);
+      u[c] = uc;
+      ss = fmaf(uc, uc, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll
+    for (int i = 0; i < kTokChans; ++i) {
+      const int c = tid + 256 * i;
+      if (tid < 256 && c < d) y[c] = rnd<T>(u[c] * inv * __ldg(norm_w + c));
+    }
+    __syncthreads();
+    T* dst = pool + ((size_t)b * cap + j) * d;
+    for (int c = tid; c < d; c += kBlockThreads) {
+      float v = y[c];
+      if (c >= d - R) {
+        const int i = (c - (d - R)) >> 1;
+        float cs, sn;
+        rope_cs(j * ratio, inv_freq, i, &cs, &sn);
+        const float a = y[d - R + 2 * i], bb = y[d - R + 2 * i + 1];
+        v = ((c - (d - R)) & 1) ? fmaf(a, sn, bb * cs) : fmaf(a, cs, -bb * sn);
+      }
+      dst[c] = from_f<T>(v);
+    }
+    __syncthreads();  // y is rewritten by the next window
+  }
+  if (tid == 0) n_rows[b] = (p0 + T_) / ratio;
+}
+
 // Rewrite the frontier slots of the newest min(T, F) tokens; block (0, b) advances n_rows.
 template <typename T>
 __global__ void k_compress_finish(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos, int T_,
@@ -505,17 +657,44 @@ static cudaError_t compress_pair_token(const Dims& L, const csa_compressor& ca, 
   return cudaGetLastError();
 }
 
+// A verify block (2 <= T <= kBlockMax tokens per sequence, one token tile in all): the two projections as one
+// grid, then k_pool_block for both pools in one launch.
+static cudaError_t compress_pair_block(const Dims& L, const csa_compressor& ca, const csa_compressor& ci,
+                                       const void* x, int B, int T_, const int32_t* pos, void* fa, void* pa,
+                                       int cap_a, int32_t* na, void* fi, void* pi, int cap_i, int32_t* ni,
+                                       const float* inv_freq, const CompressWs& wa, const CompressWs& wi,
+                                       int32_t* err, cudaStream_t s, int sa, int si) {
+  using T = __nv_bfloat16;
+  const int ntok = B * T_;
+  cudaError_t e = launch_tc_project_pair(L, ca.d, ca.wkv, ca.wgate, wa.part, ci.d, ci.wkv, ci.wgate, wi.part, x, ntok,
+                                         sa, si, err, s);
+  if (e != cudaSuccess) return e;
+  const TokPool<T> ta{wa.flags, na, static_cast<T*>(fa), ca.ape, ca.norm_w, static_cast<T*>(pa), wa.part, ca.d,
+                      cap_a, sa, tc_project_cols(L, ca.d, ntok)};
+  const TokPool<T> tb{wi.flags, ni, static_cast<T*>(fi), ci.ape, ci.norm_w, static_cast<T*>(pi), wi.part, ci.d,
+                      cap_i, si, tc_project_cols(L, ci.d, ntok)};
+  const int dm = max(ca.d, ci.d), stride = 2 * L.lanes * dm;
+  const size_t smem = (size_t)(kBlockOld + T_) * stride * sizeof(T) + (2 * (size_t)dm + 32) * sizeof(float);
+  cudaFuncSetAttribute(k_pool_block<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  CSA_LAUNCH(k_pool_block<T>, dim3(2 * B), dim3(kBlockThreads), smem, s, ta, tb, B, T_, pos, err, L.R, L.F, L.eps,
+             inv_freq, stride);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const csa_compressor& ci, const void* x,
                                  int B, int T, const int32_t* pos, void* fa, void* pa, int cap_a, int32_t* na,
                                  void* fi, void* pi, int cap_i, int32_t* ni, const float* inv_freq,
                                  const CompressWs& wa, const CompressWs& wi, int32_t* err, cudaStream_t s) {
   int sa = 0, si = 0;
-  const bool token = T == 1 && L.dtype == CSA_BF16 && L.ratio == 4 && L.lanes == 2 && L.F >= 8 && ca.d <= 512 &&
-                     ci.d <= 512 && tc_project_supported(L, ca.d) && tc_project_supported(L, ci.d) && wa.part &&
-                     wi.part && plan_project_pair(L, ca.d, ci.d, B, &sa, &si);
-  if (token)
+  const bool fused = T <= kBlockMax && L.dtype == CSA_BF16 && L.ratio == 4 && L.lanes == 2 && L.F >= 8 &&
+                     ca.d <= 512 && ci.d <= 512 && tc_project_supported(L, ca.d) && tc_project_supported(L, ci.d) &&
+                     wa.part && wi.part && plan_project_pair(L, ca.d, ci.d, B * T, &sa, &si);
+  if (fused && T == 1)
     return compress_pair_token(L, ca, ci, x, B, pos, fa, pa, cap_a, na, fi, pi, cap_i, ni, inv_freq, wa, wi, err, s,
                                sa, si);
+  if (fused)
+    return compress_pair_block(L, ca, ci, x, B, T, pos, fa, pa, cap_a, na, fi, pi, cap_i, ni, inv_freq, wa, wi, err,
+                               s, sa, si);
   cudaError_t e = launch_compress(L, ca, x, B, T, pos, fa, pa, cap_a, na, inv_freq, wa, err, s);
   if (e != cudaSuccess) return e;
   return launch_compress(L, ci, x, B, T, pos, fi, pi, cap_i, ni, inv_freq, wi, err, s);

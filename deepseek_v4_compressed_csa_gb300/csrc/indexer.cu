@@ -21,8 +21,14 @@ IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap) {
   return w;
 }
 
-__device__ __forceinline__ int query_pos(const int32_t* pos, int pos0, int q) { return pos ? pos[q] : pos0 + q; }
-__device__ __forceinline__ int query_seq(const int32_t* pos, int q) { return pos ? q : 0; }
+// Query q's position and sequence.  With device positions (decode, verify blocks) pos0 carries the number of
+// consecutive queries per sequence (0 or 1: one; T: a verify block of T tokens): query q belongs to sequence
+// q / T at position pos[q / T] + q % T.  Without them (a prefill chunk of one sequence): sequence 0, pos0 + q.
+__device__ __forceinline__ int query_pos(const int32_t* pos, int pos0, int q) {
+  const int t = max(1, pos0);
+  return pos ? pos[q / t] + q % t : pos0 + q;
+}
+__device__ __forceinline__ int query_seq(const int32_t* pos, int pos0, int q) { return pos ? q / max(1, pos0) : 0; }
 
 // qr[q][h][:] = RoPE(iq[q][h][:], p_q) rounded to the model dtype, held as fp32.
 template <typename T>
@@ -58,7 +64,7 @@ __global__ void __launch_bounds__(256) k_index_scores(const float* __restrict__ 
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm_idx[];
-  const int q = blockIdx.y, bseq = query_seq(pos, q);
+  const int q = blockIdx.y, bseq = query_seq(pos, pos0, q);
   const int p = query_pos(pos, pos0, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   const int j0 = blockIdx.x * 64;
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
   __shared__ int s_total;
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
   const int p = query_pos(pos, pos0, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   int32_t* out = sel + (size_t)q * topk;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   __shared__ int s_total;
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
   const int p = query_pos(pos, pos0, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   int32_t* out = sel + (size_t)q * topk;
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
   __shared__ int warp_tot[32], warp_tot2[32];
   __shared__ float part[2][64];
   __shared__ float new_score[2];
-  const int q = blockIdx.x, bseq = query_seq(pos, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
   // The position is a step input (no kernel of the step writes it), so the most rows this query can see, and so
   // this thread's rows, are known before the wait: the score loads then go out in the same round as n_rows.
   const int p = query_pos(pos, pos0, q);
@@ -622,7 +628,8 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
                            const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq, int32_t* sel,
                            int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s) {
   if (tc_index_supported(L)) {
-    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q : 1, cap, n_rows, pos, pos0, inv_freq, ws.qr,
+    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q / max(1, pos0) : 1, cap, n_rows, pos, pos0,
+                                           inv_freq, ws.qr,
                                            ws.scores, err, s);
     if (e != cudaSuccess) return e;
     return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);

@@ -140,8 +140,10 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
                              const int32_t* pos, int pos0, int cap, const float* sink, const float* inv_freq, int Q,
                              int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
 // Merge of decode split partials for H % 8 == 0, D == 512 (one warp per head, 16 dims per lane).
+// qps: consecutive queries per sequence (query q at pos[q / qps] + q % qps).
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
-                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s);
+                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s,
+                            int qps = 1);
 
 // ---- attend.cu: pos[b] += by for b < B
 cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s);
@@ -152,10 +154,13 @@ cudaError_t launch_trim(const Dims& L, int B, const int32_t* n_back, int32_t* po
 // ---- tc_attend_prefill.cu (tensor-core chunked-prefill attention; bf16, H = 64, D = 512, R = 64)
 // T queries of one sequence at positions pos0 + q; the chunk's roped rows kvr [T, D], the ring before the
 // chunk, pool [cap, D]; persistent CTAs (one per SM) finalise the output.  Requires tc_attend_supported(L).
+// With device positions (verify blocks): query q of sequence q / qps at pos[q / qps] + q % qps over pool
+// [B, cap, D] and ring [B, Wr, D], every window token (the block's included) read from the ring; kvr unused.
 cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* pool, const void* ring,
                                      const void* kvr, const int32_t* sel, const int32_t* n_sel,
                                      const int32_t* n_rows, int pos0, int cap, const float* sink,
-                                     const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s);
+                                     const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s,
+                                     const int32_t* pos = nullptr, int qps = 1);
 
 // ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_decode_supported(const Dims& L);
@@ -164,11 +169,14 @@ bool tc_attend_decode_supported(const Dims& L);
 // max_splits cannot hold enough splits.
 int tc_attend_decode_splits(int Q, int W, int n_max, int max_splits);
 // One CTA per (query, split).  S > 1 writes (m, l, acc) partials (merge follows), S == 1 the final output.
-// The new token kv_new[b] is roped in-kernel and written to ring slot pos[b] % W.
+// Decode (qps 1): the new token kv_new[b] is roped in-kernel and written to ring slot pos[b] % Wr.  Verify blocks
+// (qps tokens per sequence, kv_in_ring): query q belongs to sequence q / qps at pos[q / qps] + q % qps and every
+// block token is already in the ring.
 cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,
                                     const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
                                     const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
-                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s);
+                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s,
+                                    int qps = 1, bool kv_in_ring = false);
 
 // ---- attend.cu
 struct AttendWs {
@@ -190,5 +198,11 @@ cudaError_t launch_attend_prefill(const Dims& L, const void* q, const void* kv_n
                                   int pos0, void* window, const void* pool, int cap, const int32_t* n_rows,
                                   const int32_t* sel, const int32_t* n_sel, const float* inv_freq, void* out,
                                   const AttendWs& ws, int32_t* err, cudaStream_t s);
+
+// Verify blocks: T tokens per sequence appended to the window ring (roped), then each attended by its own query.
+cudaError_t launch_attend_verify(const Dims& L, const void* q, const void* kv_new, const float* sink, int B, int T,
+                                 void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                                 const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out,
+                                 const AttendWs& ws, int32_t* err, cudaStream_t s);
 
 }  // namespace csa

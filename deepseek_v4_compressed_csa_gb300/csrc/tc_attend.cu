@@ -528,7 +528,8 @@ __global__ void __launch_bounds__(kThreadsAt, 1) k_tc_attend(AtArgs a) {
 // its accumulator, which it did not write, is not used.
 __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part_ml, const float* __restrict__ part_acc,
                                                   int S, const float* __restrict__ sink, const int32_t* __restrict__ pos,
-                                                  const float* __restrict__ inv_freq, __nv_bfloat16* __restrict__ out) {
+                                                  int qps, const float* __restrict__ inv_freq,
+                                                  __nv_bfloat16* __restrict__ out) {
   pdl_trigger();
   __shared__ float rc[32], rs[32];
   const int q = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(256) k_tc_merge(const float* __restrict__ part
   const size_t base = (size_t)q * S * kAH + h;
   // before the wait: the sink and the RoPE table of the query's position (call inputs)
   const float z = sink[h];
-  if (threadIdx.x < 32) rope_cs(pos[q], inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
+  if (threadIdx.x < 32) rope_cs(pos[q / qps] + q % qps, inv_freq, threadIdx.x, &rc[threadIdx.x], &rs[threadIdx.x]);
   pdl_wait();
   float4 x[4][4];
   auto load_batch = [&](int s0) {
@@ -634,10 +635,11 @@ cudaError_t launch_tc_attend(const Dims& L, const void* q, const void* pool, voi
 }
 
 cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* part_acc, int S, int Q,
-                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s) {
+                            const float* sink, const int32_t* pos, const float* inv_freq, void* out, cudaStream_t s,
+                            int qps) {
   (void)L;
   if (S > 32) return cudaErrorNotSupported;  // callers use the generic merge beyond 32 splits
-  CSA_LAUNCH(k_tc_merge, dim3(dim3(kAH / 8, Q)), dim3(256), 0, s, part_ml, part_acc, S, sink, pos, inv_freq,
+  CSA_LAUNCH(k_tc_merge, dim3(dim3(kAH / 8, Q)), dim3(256), 0, s, part_ml, part_acc, S, sink, pos, qps, inv_freq,
                                                static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }

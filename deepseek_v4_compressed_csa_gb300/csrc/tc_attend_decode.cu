@@ -87,6 +87,8 @@ struct DecArgs {
   const float* inv_freq;
   int cap, topk, W, ratio, S;
   int Wr;                       // ring slots (W + rollback); the query attends its last W tokens
+  int qps;                      // consecutive queries per sequence (a verify block; 1 for decode)
+  int kv_in_ring;               // the new tokens are already in the ring (verify): none is roped here
   float scale2;                 // softmax scale * log2(e)
   float* part_ml;
   float* part_acc;
@@ -126,8 +128,8 @@ __device__ __forceinline__ Item make_item(const DecArgs& a) {
   Item it;
   it.q = blockIdx.x / a.S;
   it.s = blockIdx.x % a.S;
-  it.b = it.q;
-  it.p = a.pos[it.q];
+  it.b = it.q / a.qps;
+  it.p = a.pos[it.b] + it.q % a.qps;
   it.nwin = it.p >= 0 ? min(a.W, it.p + 1) : 0;
   const int wper = (it.nwin + a.S - 1) / a.S;
   it.w_begin = min(it.nwin, it.s * wper);
@@ -150,7 +152,7 @@ __device__ __forceinline__ void item_selection(const DecArgs& a, Item& it) {
 // selection is given); an out-of-range selection is reported and left empty.
 __device__ __forceinline__ int window_code(const DecArgs& a, const Item& it, int w) {
   const int tok = it.p - it.nwin + 1 + w;
-  if (tok == it.p) return kRowNew;
+  if (tok == it.p && !a.kv_in_ring) return kRowNew;
   return kRowRing0 - (it.b * a.Wr + tok % a.Wr);
 }
 __device__ __forceinline__ int selected_code(const DecArgs& a, const Item& it, int k, int j) {
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
     gather_rows(a, rowc, r_base, 0, it.nw);
     // the new token (the window's last): RoPE at p, into the tile and into its ring slot (the slot belongs to the
     // token leaving the window, which no CTA reads)
-    const int cur_row = (it.nw > 0 && it.w_begin + it.nw == it.nwin) ? it.nw - 1 : -1;
+    const int cur_row = (!a.kv_in_ring && it.nw > 0 && it.w_begin + it.nw == it.nwin) ? it.nw - 1 : -1;
     if (cur_row >= 0 && warp == cur_row % kMainWarps) {
       const __nv_bfloat16* cur = a.kv_new + (size_t)it.b * kAD;
 #pragma unroll
@@ -555,8 +557,11 @@ int tc_attend_decode_splits(int Q, int W, int n_max, int max_splits) {
 cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,
                                     const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
                                     const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
-                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s) {
+                                    int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s,
+                                    int qps, bool kv_in_ring) {
   DecArgs a{};
+  a.qps = qps;
+  a.kv_in_ring = kv_in_ring ? 1 : 0;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.pool = static_cast<const __nv_bfloat16*>(pool);
   a.ring = static_cast<__nv_bfloat16*>(ring);

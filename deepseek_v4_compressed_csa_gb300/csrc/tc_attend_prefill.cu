@@ -81,12 +81,14 @@ constexpr int kRowTok0 = -2;
 
 struct PfArgs {
   const __nv_bfloat16* q;      // [T, 64, 512] queries before RoPE
-  const __nv_bfloat16* pool;   // [cap, 512] compressed rows (pool of the one sequence)
-  const __nv_bfloat16* ring;   // [W, 512] window ring before the chunk (token t in slot t % W)
-  const __nv_bfloat16* kvr;    // [T, 512] roped rows of the chunk's tokens
+  const __nv_bfloat16* pool;   // [cap, 512] compressed rows (pool of the one sequence); verify: [B, cap, 512]
+  const __nv_bfloat16* ring;   // [Wr, 512] window ring before the chunk (token t in slot t % Wr); verify: [B, Wr, 512]
+  const __nv_bfloat16* kvr;    // [T, 512] roped rows of the chunk's tokens (unused for verify blocks)
   const int32_t* sel;          // [T, topk] or null (every visible row)
   const int32_t* n_sel;
-  const int32_t* n_rows;       // [1]
+  const int32_t* n_rows;       // [1]; verify: [B]
+  const int32_t* pos;          // null: one chunk at pos0 + q; verify blocks: [B], query q at pos[q / qps] + q % qps
+  int qps;                     // verify: queries per sequence (every window token of the block already in the ring)
   const float* sink;
   const float* inv_freq;
   int T, pos0, cap, topk, W, ratio;
@@ -98,28 +100,34 @@ struct PfArgs {
 };
 
 struct Query {
-  int p, nsel, nwin, nrows, ntiles;
+  int b, p, nsel, nwin, nrows, ntiles;
 };
 
 __device__ __forceinline__ Query query_info(const PfArgs& a, int qi) {
   Query r;
-  r.p = a.pos0 + qi;
-  r.nrows = min(a.n_rows[0], a.cap);
+  r.b = a.pos ? qi / a.qps : 0;
+  r.p = a.pos ? a.pos[r.b] + qi % a.qps : a.pos0 + qi;
+  r.nrows = min(a.n_rows[r.b], a.cap);
   r.nsel = a.sel ? min(max(a.n_sel[qi], 0), a.topk) : max(0, min(r.nrows, (r.p + 1) / a.ratio));
   r.nwin = r.p >= 0 ? min(a.W, r.p + 1) : 0;
   r.ntiles = max(1, (r.nsel + r.nwin + kPR - 1) / kPR);  // a query without rows still finalises a zero output
   return r;
 }
 
-// Code of row r_abs of query qi; j = sel[qi][r_abs] when a selection is given and r_abs < nsel.
+// Code of row r_abs of query qi; j = sel[qi][r_abs] when a selection is given and r_abs < nsel.  A pool row's
+// code is its row in the pool tensor map (b * cap + j); a window token's is kRowTok0 - token for a chunk, and
+// kRowTok0 - (b * Wr + token mod Wr), its ring row, for verify blocks.
 __device__ __forceinline__ int row_code(const PfArgs& a, const Query& qu, int r_abs, int j) {
   if (r_abs < qu.nsel) {
     if (!a.sel) j = r_abs;
-    if (j >= 0 && j < qu.nrows) return j;
+    if (j >= 0 && j < qu.nrows) return qu.b * a.cap + j;
     atomicOr(a.err, CSA_DEV_RANGE);
     return kRowNone;
   }
-  if (r_abs < qu.nsel + qu.nwin) return kRowTok0 - (qu.p - qu.nwin + 1 + (r_abs - qu.nsel));
+  if (r_abs < qu.nsel + qu.nwin) {
+    const int tok = qu.p - qu.nwin + 1 + (r_abs - qu.nsel);
+    return kRowTok0 - (a.pos ? qu.b * a.Wr + tok % a.Wr : tok);
+  }
   return kRowNone;
 }
 
@@ -133,6 +141,10 @@ __device__ __forceinline__ int row_src(const PfArgs& a, int code, int& row) {
   }
   if (code <= kRowTok0) {
     const int tok = kRowTok0 - code;
+    if (a.pos) {
+      row = tok;  // verify blocks: already the ring row
+      return kSrcRing;
+    }
     if (tok >= a.pos0) {
       row = tok - a.pos0;
       return kSrcChunk;
@@ -602,7 +614,8 @@ int g_sms_pf = 0;
 cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* pool, const void* ring,
                                      const void* kvr, const int32_t* sel, const int32_t* n_sel,
                                      const int32_t* n_rows, int pos0, int cap, const float* sink,
-                                     const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s) {
+                                     const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s,
+                                     const int32_t* pos, int qps) {
   if (T <= 0) return cudaSuccess;
   if (cap <= 0) return cudaErrorInvalidValue;
   if (!g_sms_pf) {
@@ -617,17 +630,20 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
   a.kvr = static_cast<const __nv_bfloat16*>(kvr);
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.sink = sink; a.inv_freq = inv_freq;
   a.T = T; a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.ratio = L.ratio;
+  a.pos = pos; a.qps = max(1, qps);
+  const int nseq = pos ? (T + a.qps - 1) / a.qps : 1;
+  if (pos && !kvr) kvr = q;  // verify blocks read no chunk rows: the chunk maps only need a valid address
   a.scale2 = L.scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.err = err;
   // one-row boxes for the row gathers (tile::gather4 and single rows), 64-row boxes for the query blocks
   // and 128-row boxes of the chunk's rows (whole window tiles)
   CUtensorMap tq, tp, tk, tr, tkt;
-  a.chunk_tiles = T >= kPR;
+  a.chunk_tiles = !pos && T >= kPR;
   if (!make_tmap_2d_bf16(&tq, q, (uint64_t)T * kAH, kAD, kAD * 2, 64) ||
-      !make_tmap_2d_bf16(&tp, pool, (uint64_t)cap, kAD, kAD * 2, 1) ||
+      !make_tmap_2d_bf16(&tp, pool, (uint64_t)nseq * cap, kAD, kAD * 2, 1) ||
       !make_tmap_2d_bf16(&tk, kvr, (uint64_t)T, kAD, kAD * 2, 1) ||
-      !make_tmap_2d_bf16(&tr, ring, (uint64_t)L.Wr, kAD, kAD * 2, 1) ||
+      !make_tmap_2d_bf16(&tr, ring, (uint64_t)nseq * L.Wr, kAD, kAD * 2, 1) ||
       !make_tmap_2d_bf16(&tkt, kvr, (uint64_t)T, kAD, kAD * 2, a.chunk_tiles ? kPR : 1))
     return cudaErrorInvalidValue;
   cudaFuncSetAttribute(k_tc_attend_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

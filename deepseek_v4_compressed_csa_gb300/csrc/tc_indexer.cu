@@ -19,7 +19,11 @@
 // each query block in shared memory (RoPE at the query's position, bf16, the
 // 128-byte-swizzled K-major layout) and its scaled head weights, so no separate
 // preparation pass runs before the scan.  Decode keeps two query blocks and
-// four accumulators in flight.
+// four accumulators in flight.  With G = 4 a block (256 head rows, 64 KB) comes
+// in one TMA copy, already in that layout, and its last R dims are roped in
+// place: a CTA of a verify block's scan enters a new group every ~14 tiles, and
+// copying the block through registers took eight dependent load rounds each
+// time, with the one query slot (and so the tensor pipe) waiting.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -43,7 +47,7 @@ struct IdxCfg {
   static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights
   static constexpr int kOffRope = kOffW + kQSlots * N * 4;     // [G][32] cos, [G][32] sin
   static constexpr int kOffBars = kOffRope + G * 64 * 4;
-  static constexpr int kNumBars = 2 * kStages + 3 * kQSlots + 2 * kAcc + 1;
+  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 2 * kAcc + 1;
   static constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
   // warps: 0 TMA, 1 MMA, 2 .. 2 + kEpiWarps - 1 epilogue, then two query-block warps.  A prefill tile has four
   // queries' columns to reduce: eight epilogue warps, two per TMEM lane quarter, take two queries each.
@@ -60,7 +64,8 @@ struct IdxArgs {
   float wscale;             // Di^-1/2 Hi^-1/2
   int R;
   const int32_t* n_rows;
-  const int32_t* pos;  // decode positions [Q] or null (prefill: pos0 + q)
+  const int32_t* pos;  // decode / verify positions [Q / qps] or null (prefill: pos0 + q)
+  int qps;             // consecutive queries per sequence (a verify block of qps tokens; 1 for decode)
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
   int group_penalty;  // partition weight of a group's query block, in tiles
   float* scores;     // [Q, cap]
@@ -71,9 +76,11 @@ struct IdxArgs {
   float* w_out;           // [Q, 64]
 };
 
-__device__ __forceinline__ int idx_qpos(const IdxArgs& a, int q) { return a.pos ? a.pos[q] : a.pos0 + q; }
+__device__ __forceinline__ int idx_qpos(const IdxArgs& a, int q) {
+  return a.pos ? a.pos[q / a.qps] + q % a.qps : a.pos0 + q;
+}
 __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
-  const int b = a.pos ? q : 0;
+  const int b = a.pos ? q / a.qps : 0;
   return min(min(a.n_rows[b], a.cap), (idx_qpos(a, q) + 1) / a.ratio);
 }
 // Rows this scan scores for query q.  The overlapped decode scan, which runs while the index pool's compress
@@ -146,7 +153,8 @@ struct Items {
 // scan's remaining CTAs wait for them to finish.
 template <int G, bool kOverlap>
 __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
-    k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, IdxArgs a) {
+    k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
+                      IdxArgs a) {
   using C = IdxCfg<G>;
   constexpr int N = C::N;
   pdl_trigger();
@@ -166,7 +174,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   uint64_t* acc_full = w_empty + C::kQSlots;    // [kAcc]
   uint64_t* acc_empty = acc_full + C::kAcc;     // [kAcc]
   uint64_t* drain = acc_empty + C::kAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* q_loaded = drain + 1;               // [kQSlots] G = 4: the query block's TMA copy landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_loaded + C::kQSlots);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -199,14 +208,24 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     float th_freq;
     int p;
   };
+  // G = 4: the block of group g by TMA (rows g*256 .. of [Q*64, 128]; rows past the last query read zeros)
+  auto issue_q = [&](int g) {
+    if (pt == 0) {
+      tc::mbar_arrive_expect_tx(&q_loaded[0], C::kQBytes);
+      tc::tma_load_2d(qbuf, &tm_q, &q_loaded[0], 0, g * N);
+      tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, g * N);
+    }
+  };
   auto load_first = [&](int g, Pre& pre) {
+    if constexpr (G != 4) {
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int e = pt + b * kPrepThreads;
-      const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
-      pre.raw[b] = (e < kChunks && q < a.Q)
-                       ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
-                       : make_uint4(0, 0, 0, 0);
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = pt + b * kPrepThreads;
+        const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
+        pre.raw[b] = (e < kChunks && q < a.Q)
+                         ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
+                         : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -237,7 +256,20 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-  if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
+  if (warp >= C::kPrepWarp0 && i_begin < i_end) {
+    if (G == 4) {
+      // this thread issues the block copies: it initialises their barrier itself, ahead of the CTA-wide sync.
+      // The range's first group is copied now; whether it has tiles is known only after the wait (a prefill
+      // chunk's first groups may have none), so the loop below drains this copy if it starts at a later group.
+      if (pt == 0) {
+        tc::mbar_init(&q_loaded[0], 1);
+        tc::fence_mbar_init();
+        tc::tma_prefetch(&tm_q);
+      }
+      issue_q(g0);
+    }
+    load_first(g0, pre_a);
+  }
   // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
   // before the token and the step's inputs, and writes only its own scratch, so it runs beside the compress
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
@@ -269,7 +301,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g, t = itr.t;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
-        const int krow = (a.pos ? g : 0) * a.cap + t * kTileRows;
+        const int krow = (a.pos ? g * G / a.qps : 0) * a.cap + t * kTileRows;  // a group's queries share a sequence
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
         tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
@@ -413,6 +445,14 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
+    int q_pending = (G == 4 && i_begin < i_end) ? g0 : -1;  // G = 4: group whose block copy is in flight
+    uint32_t q_waits = 0;                                  // G = 4: completed phases of q_loaded
+    auto wait_q = [&]() {
+      const bool ok = tc::mbar_wait(&q_loaded[0], q_waits & 1);
+      ++q_waits;
+      q_pending = -1;
+      return ok;
+    };
     Items<kOverlap> itr;
     for (bool more = itr.start(a, i_begin, i_end); more; more = itr.next_group(a)) {
       const int g = itr.g;
@@ -426,6 +466,15 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       }
       Pre& pre = pre_a;
       if (g != g0) load_first(g, pre_a);  // a later group: request it now
+      if constexpr (G == 4) {
+        if (q_pending != g) {
+          // the slot is free (first group, or the previous group's MMAs retired); a copy of a group without
+          // tiles still in flight is drained first
+          if (q_pending >= 0 && tc::named_bar_any(3, kPrepThreads, !wait_q())) { failed = true; break; }
+          issue_q(g);
+          q_pending = g;
+        }
+      }
       // RoPE table (G x 32 entries) from the preloaded position and frequency
       for (int e = pt; e < G * 32; e += kPrepThreads) {
         int p = pre.p;
@@ -439,18 +488,38 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       }
       tc::named_bar(3, kPrepThreads);
       uint8_t* qb = qbuf + slot * C::kQBytes;
-      rope_store(qb, pt, pre.raw, g);
-      for (int e0 = pt + kPrepThreads * kBatch; e0 < kChunks; e0 += kPrepThreads * kBatch) {
-        uint4 raw[kBatch];
+      if constexpr (G == 4) {
+        // RoPE in place on the copied block: 16-byte chunks c >= (128 - R) / 8 of each of the N head rows
+        if (tc::named_bar_any(3, kPrepThreads, !wait_q())) { failed = true; break; }
+        const int c0 = (128 - a.R) / 8, nrc = 16 - c0;
+        for (int e = pt; e < N * nrc; e += kPrepThreads) {
+          const int row = e / nrc, c = c0 + e % nrc, qq = row >> 6;
+          uint4* slot_p =
+              reinterpret_cast<uint4*>(qb + (c >> 3) * (C::kQBytes / 2) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+          uint4 raw = *slot_p;
+          __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int e = e0 + b * kPrepThreads;
-          const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
-          raw[b] = (e < kChunks && q < a.Q)
-                       ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
-                       : make_uint4(0, 0, 0, 0);
+          for (int kq = 0; kq < 4; ++kq) {
+            const int i = qq * 32 + (c * 8 - (128 - a.R)) / 2 + kq;
+            const float2 x = __bfloat1622float2(hv[kq]);
+            hv[kq] = __floats2bfloat162_rn(fmaf(x.x, rcos[i], -x.y * rsin[i]), fmaf(x.x, rsin[i], x.y * rcos[i]));
+          }
+          *slot_p = raw;
         }
-        rope_store(qb, e0, raw, g);
+      } else {
+        rope_store(qb, pt, pre.raw, g);
+        for (int e0 = pt + kPrepThreads * kBatch; e0 < kChunks; e0 += kPrepThreads * kBatch) {
+          uint4 raw[kBatch];
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int e = e0 + b * kPrepThreads;
+            const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
+            raw[b] = (e < kChunks && q < a.Q)
+                         ? __ldg(reinterpret_cast<const uint4*>(a.iq + ((size_t)q * 64 + h) * 128 + c * 8))
+                         : make_uint4(0, 0, 0, 0);
+          }
+          rope_store(qb, e0, raw, g);
+        }
       }
 #pragma unroll
       for (int i = 0; i < G; ++i) {
@@ -462,6 +531,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&q_full[slot]);
     }
+    // a block copy that no group used (a range without tiles) lands before the CTA exits
+    if (G == 4 && q_pending >= 0 && !wait_q()) failed = true;
   }
   if (failed) atomicOr(a.err, tc::kErrTimeout);
   tc::fence_before_sync();
@@ -490,9 +561,13 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  const int G = pos ? 1 : 4;
-  CUtensorMap tk;
+  // queries per MMA: 4 for a prefill chunk and for verify blocks whose length is a multiple of 4 (the block's
+  // queries then share every key tile, one read for four), else 1 (decode)
+  const int G = !pos ? 4 : (pos0 > 1 && pos0 % 4 == 0 ? 4 : 1);
+  CUtensorMap tk, tq;
   if (!make_tmap_2d_bf16(&tk, ikeys, (uint64_t)Bk * cap, 128, 256, kTileRows)) return cudaErrorInvalidValue;
+  // the 4-query instance copies each group's query block (4 x 64 head rows) by TMA
+  if (!make_tmap_2d_bf16(&tq, iq, (uint64_t)Q * 64, 128, 256, 64 * G)) return cudaErrorInvalidValue;
   IdxArgs a{};
   a.iq = static_cast<const __nv_bfloat16*>(iq);
   a.iw = static_cast<const __nv_bfloat16*>(iw);
@@ -500,6 +575,7 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   a.wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
   a.R = L.R;
   a.n_rows = n_rows; a.pos = pos; a.pos0 = pos0; a.ratio = L.ratio; a.topk = L.topk; a.cap = cap; a.Q = Q;
+  a.qps = pos ? max(1, pos0) : 1;  // with device positions pos0 carries the queries per sequence
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
   a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
   a.group_penalty = G == 1 ? 3 : 0;
@@ -513,15 +589,15 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   if (G == 1 && overlap) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, a);
   } else if (G == 1) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, a);
   } else {
     constexpr int smem = IdxCfg<4>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(IdxCfg<4>::kThreads), smem, s, tk, a);
+    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(IdxCfg<4>::kThreads), smem, s, tk, tq, a);
   }
   return cudaGetLastError();
 }

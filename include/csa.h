@@ -293,6 +293,39 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                     const float* inv_freq, void* out, int32_t* sel_out, void* ws, size_t ws_bytes,
                                     int32_t* err, void* stream);
 
+/* csa_index_topk_verify, csa_attend_verify — a verify block: T consecutive tokens
+ * per sequence (a speculative step's last accepted token and its T-1 drafts),
+ * each query with its own causal top-k and attention, B sequences at once.
+ *
+ * Definition ([MTPLX#216], "Benchmark notes" and the MTP post: verification runs
+ * a K+1-wide query block per sequence, the KV projected inside a K+1-wide GEMM;
+ * the per-query semantics are those of a prefill chunk, [mlx-lm#1189] stepnoy's
+ * patch point 3): call csa_compress_append (or _pair) with the block's T tokens
+ * first; then, for query i of sequence b at p = pos[b] + i, the selection and the
+ * output are csa_index_topk's and csa_attend_decode's at position p, with the
+ * rows visible at p (those emitted by tokens <= p) and the window tokens
+ * [p-W+1, p], the block's own earlier tokens included.  csa_attend_verify first
+ * writes all T tokens, roped, to their ring slots (pos[b] + i) mod (W + rollback),
+ * so the layer needs rollback >= T - 1 (else CSA_ERR_ARG): the block's later
+ * tokens must not overwrite window rows its earlier queries attend.  Neither call
+ * advances pos; after verification the caller advances it by T (csa_advance_positions)
+ * and rewinds the rejected drafts with csa_trim.
+ * Arguments as csa_index_topk / csa_attend_decode with one more axis of T queries
+ * per sequence: iq [B, T, Hi, Di], iw [B, T, Hi], q [B, T, H, D], kv_new [B, T, D],
+ * sel [B, T, topk], n_sel [B, T], out [B, T, H, D]; pos [B] is the position of each
+ * block's first token; 1 <= T <= 64.  Workspaces: csa_workspace_size(..,
+ * CSA_OP_INDEX_TOPK, B * T, 1, cap, ..) and (.., CSA_OP_ATTEND_DECODE, B * T, ..).
+ * Tensor-core shapes (bf16, 64 x 512 latent, 64 x 128 indexer) with an indexer
+ * (ratio 4); other layers get CSA_ERR_UNSUPPORTED. */
+csa_status csa_index_topk_verify(const csa_layer* layer, const void* iq, const void* iw, int B, int T,
+                                 const void* ikeys, int cap, const int32_t* n_rows, const int32_t* pos,
+                                 const float* inv_freq, int32_t* sel, int32_t* n_sel, void* ws, size_t ws_bytes,
+                                 int32_t* err, void* stream);
+csa_status csa_attend_verify(const csa_layer* layer, const void* q, const void* kv_new, const float* sink, int B, int T,
+                             void* window, const void* pool, int cap, const int32_t* n_rows, const int32_t* sel,
+                             const int32_t* n_sel, const int32_t* pos, const float* inv_freq, void* out, void* ws,
+                             size_t ws_bytes, int32_t* err, void* stream);
+
 /* csa_trim — rewind sequences by n_back[b] tokens, exactly (speculative decoding:
  * the rejected draft tokens are taken back).
  *

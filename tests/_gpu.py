@@ -395,6 +395,24 @@ class Runner:
                 projs[name] = raw.view(self.cfg.storage).view(B, T, width).clone()
         return projs
 
+    def compress_pair(self, st: DevCache, x):
+        """csa_compress_append_pair (both pools, one call); returns the GPU's projections of the new tokens per
+        pool, read from their frontier slots (slot (pos + i) mod F; the block fits the frontier)."""
+        x = dev(x)
+        B, T = x.shape[0], x.shape[1]
+        F = st.front_attn.shape[1]
+        assert T <= F
+        n_i = st.n_rows.clone()
+        ws = torch.zeros(csa.workspace_size(self.L, csa.OP_COMPRESS_PAIR, B, T, st.pool.shape[1]), dtype=torch.uint8,
+                         device="cuda")
+        csa.compress_append_pair(self.L, self.ca, self.ci, x, st.pos, st.front_attn, st.pool, st.n_rows,
+                                 st.front_index, st.ikeys, n_i, self.inv_freq, ws=ws, err=self.err)
+        torch.cuda.synchronize()
+        assert torch.equal(n_i, st.n_rows)
+        slots = (st.pos.long()[:, None] + torch.arange(T, device="cuda")[None]) % F
+        rows = torch.arange(B, device="cuda")[:, None]
+        return {"attn": st.front_attn[rows, slots].clone(), "index": st.front_index[rows, slots].clone()}
+
     def compress_and_index_overlapped(self, st: DevCache, si: csa_synth.StepInputs, sel, n_sel):
         """The index pool's compress call on a second stream while csa_index_topk_overlapped scans on the main
         stream (after the attention pool's compress call), joined by an event; sets self.projs."""
