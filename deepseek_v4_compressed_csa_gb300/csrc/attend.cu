@@ -390,9 +390,10 @@ static cudaError_t decode_t(const Dims& L, const void* q, const void* kv_new, co
   // it always has except for a layer with an indexer called without a selection (every visible row)
   const int S = tc_attend_decode_supported(L) ? tc_attend_decode_splits(B, L.W, sel ? L.topk : cap, ws.S) : 0;
   if (S > 0) {
+    const bool cluster = tc_attend_decode_cluster(S);
     cudaError_t e = launch_tc_attend_decode(L, q, pool, window, kv_new, sel, n_sel, n_rows, pos, cap, sink, inv_freq,
-                                            B, S, ws.part_ml, ws.part_acc, out, err, s);
-    if (e != cudaSuccess || S == 1) return e;
+                                            B, S, ws.part_ml, ws.part_acc, out, err, s, 1, false, cluster);
+    if (e != cudaSuccess || S == 1 || cluster) return e;
     if (S <= 32) return launch_tc_merge(L, ws.part_ml, ws.part_acc, S, B, sink, pos, inv_freq, out, s);
     CSA_LAUNCH(k_attend_merge<T>, dim3(L.H, B), dim3(max(32, min(1024, L.D / 8))), S * sizeof(float), s,
                ws.part_ml, ws.part_acc, S, L.H, L.D, L.R, sink, pos, 0, inv_freq, static_cast<T*>(out));
@@ -491,9 +492,10 @@ cudaError_t launch_attend_verify(const Dims& L, const void* q, const void* kv_ne
   if ((long)Q * S > sms)
     return launch_tc_attend_prefill(L, q, pool, window, nullptr, sel, n_sel, n_rows, 0, cap, sink, inv_freq, Q, out,
                                     err, s, pos, T_);
+  const bool cluster = tc_attend_decode_cluster(S);
   cudaError_t e = launch_tc_attend_decode(L, q, pool, window, kv_new, sel, n_sel, n_rows, pos, cap, sink, inv_freq, Q,
-                                          S, ws.part_ml, ws.part_acc, out, err, s, T_, true);
-  if (e != cudaSuccess || S == 1) return e;
+                                          S, ws.part_ml, ws.part_acc, out, err, s, T_, true, cluster);
+  if (e != cudaSuccess || S == 1 || cluster) return e;
   return launch_tc_merge(L, ws.part_ml, ws.part_acc, S, Q, sink, pos, inv_freq, out, s, T_);
 }
 

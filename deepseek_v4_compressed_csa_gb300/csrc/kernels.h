@@ -57,6 +57,28 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with thread-block clusters of cluster_x consecutive blocks (grid.x a multiple of cluster_x).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                      int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 #define CSA_LAUNCH(...)                           \
   do {                                            \
     cudaError_t csa_e_ = launch_pdl(__VA_ARGS__); \
@@ -176,7 +198,10 @@ cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* po
                                     const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
                                     const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
                                     int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s,
-                                    int qps = 1, bool kv_in_ring = false);
+                                    int qps = 1, bool kv_in_ring = false, bool cluster = false);
+// Whether S splits can merge inside a cluster (S in {2, 4} and the device places such clusters): the decode
+// kernel then writes the output itself and no merge kernel runs.
+bool tc_attend_decode_cluster(int S);
 
 // ---- attend.cu
 struct AttendWs {

@@ -89,6 +89,7 @@ struct DecArgs {
   int Wr;                       // ring slots (W + rollback); the query attends its last W tokens
   int qps;                      // consecutive queries per sequence (a verify block; 1 for decode)
   int kv_in_ring;               // the new tokens are already in the ring (verify): none is roped here
+  int cluster;                  // S in {2, 4}: the S splits of a query are one cluster and merge through DSMEM
   float scale2;                 // softmax scale * log2(e)
   float* part_ml;
   float* part_acc;
@@ -455,9 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
   // lane of each; O = hi + lo parts.  Eight warps halve the partial write of four.
   failed = __syncthreads_or(failed) != 0;
   tc::fence_after_sync();
-  if (!failed) {
-    const int quarter = warp & 3, dl = quarter * 32 + lane, m0 = (warp >> 2) * 2;
-    auto load_o = [&](int m, float (&o)[64]) {
+  const int quarter = warp & 3, dl = quarter * 32 + lane, m0 = (warp >> 2) * 2;
+  auto load_o = [&](int m, float (&o)[64]) {
       if (nr <= 0) {
 #pragma unroll
         for (int h = 0; h < 64; ++h) o[h] = 0.f;
@@ -476,6 +476,93 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
 #pragma unroll
       for (int h = 0; h < 64; ++h) o[h] += __uint_as_float(u[h]);
     };
+  if (a.cluster) {
+    // The query's S splits are one cluster.  Each leaves its O (hi + lo, fp32), its per-head reference max (natural
+    // log units) and row sum in its own row tile (free once PV retired); after a cluster barrier, rank r merges
+    // dims [r D/S, (r+1) D/S) of all S with the arithmetic of the merge kernel, reading the others' shared memory.
+    // A second barrier keeps every CTA's shared memory in place until the others have read it.  Every thread
+    // reaches both barriers, a failed CTA too (its output is then invalid and the error word says so).
+    float* accs = reinterpret_cast<float*>(rows);  // [64 heads][512]
+    float* mls = accs + kAH * kAD;                 // [64][2]
+    float* tab = mls + 2 * kAH;                    // [64][S + 1]: weights f_s, then 1 / Z
+    const int S = a.S;
+    if (!failed) {
+      if (tid < 64) {
+        mls[2 * tid] = mref[tid] == -INFINITY ? -INFINITY : mref[tid] * kLn2;
+        mls[2 * tid + 1] = lsum[tid];
+      }
+      for (int m = m0; m < m0 + 2; ++m) {
+        float o[64];
+        load_o(m, o);
+#pragma unroll
+        for (int h = 0; h < 64; ++h) accs[h * kAD + 128 * m + dl] = o[h];
+      }
+    }
+    tc::cluster_sync();
+    if (tid < 64) {
+      // M = max(z, m_s); f_s = e^{m_s - M} (0 for a split without rows); Z = e^{z - M} + sum_s l_s f_s
+      const float z = a.sink[tid];
+      float ms[4], ls[4];
+      float M = z;
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp) {
+        if (sp < S) {
+          const float2 v = tc::ld_cluster_f2(tc::cluster_map(mls + 2 * tid, sp));
+          ms[sp] = v.x;
+          ls[sp] = v.y;
+          M = fmaxf(M, v.x);
+        }
+      }
+      float zs = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp) {
+        if (sp < S) {
+          const float f = ms[sp] == -INFINITY ? 0.f : expf(ms[sp] - M);
+          tab[tid * (S + 1) + sp] = f;
+          zs = fmaf(ls[sp], f, zs);
+        }
+      }
+      tab[tid * (S + 1) + S] = 1.0f / (expf(z - M) + zs);
+    }
+    __syncthreads();
+    // warp w: heads 8w .. 8w + 7; lane: 4-dim columns of this rank's slice
+    const int r = it.s, ncol = kAD / 4 / S;
+    for (int hh = 0; hh < 8; ++hh) {
+      const int h = warp * 8 + hh;
+      for (int c = lane; c < ncol; c += 32) {
+        const int d = r * (kAD / S) + 4 * c;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < S; ++sp) {
+          const float f = tab[h * (S + 1) + sp];
+          if (f != 0.f) {
+            const float4 x = tc::ld_cluster_f4(tc::cluster_map(accs + h * kAD + d, sp));
+            v[0] = fmaf(x.x, f, v[0]);
+            v[1] = fmaf(x.y, f, v[1]);
+            v[2] = fmaf(x.z, f, v[2]);
+            v[3] = fmaf(x.w, f, v[3]);
+          }
+        }
+        const float invZ = tab[h * (S + 1) + S];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = rnd<__nv_bfloat16>(v[e] * invZ);
+        if (d >= kAD - 64) {
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int i = (d + e - (kAD - 64)) >> 1;
+            const float x0 = v[e], x1 = v[e + 1];
+            v[e] = fmaf(x0, rcos[i], x1 * rsin[i]);
+            v[e + 1] = fmaf(-x0, rsin[i], x1 * rcos[i]);
+          }
+        }
+        uint2 pk;
+        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&pk);
+        hv[0] = __floats2bfloat162_rn(v[0], v[1]);
+        hv[1] = __floats2bfloat162_rn(v[2], v[3]);
+        *reinterpret_cast<uint2*>(a.out + ((size_t)it.q * kAH + h) * kAD + d) = pk;
+      }
+    }
+    tc::cluster_sync();
+  } else if (!failed) {
     if (a.S > 1) {
       if (tid < 64) {
         const size_t idx = ((size_t)it.q * a.S + it.s) * kAH + tid;
@@ -554,12 +641,39 @@ int tc_attend_decode_splits(int Q, int W, int n_max, int max_splits) {
   return min(max_splits, max(s_min, min(s_fit, s_tiles)));
 }
 
+// Whether the S splits of a query can run as one cluster (S in {2, 4}, and the device can place such a cluster of
+// these CTAs); asked once per S.
+bool tc_attend_decode_cluster(int S) {
+  static int known[5] = {-1, -1, -1, -1, -1};
+  if (S != 2 && S != 4) return false;
+  if (known[S] < 0) {
+    cudaFuncSetAttribute(k_tc_attend_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_tc_attend_decode, &cfg);
+    if (e != cudaSuccess) cudaGetLastError();  // leave no sticky error behind
+    known[S] = (e == cudaSuccess && n > 0) ? 1 : 0;
+  }
+  return known[S] == 1;
+}
+
 cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* pool, void* ring, const void* kv_new,
                                     const int32_t* sel, const int32_t* n_sel, const int32_t* n_rows,
                                     const int32_t* pos, int cap, const float* sink, const float* inv_freq, int Q,
                                     int S, float* part_ml, float* part_acc, void* out, int32_t* err, cudaStream_t s,
-                                    int qps, bool kv_in_ring) {
+                                    int qps, bool kv_in_ring, bool cluster) {
   DecArgs a{};
+  a.cluster = cluster ? 1 : 0;
   a.qps = qps;
   a.kv_in_ring = kv_in_ring ? 1 : 0;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -573,7 +687,13 @@ cudaError_t launch_tc_attend_decode(const Dims& L, const void* q, const void* po
   a.out = static_cast<__nv_bfloat16*>(out);
   a.err = err;
   cudaFuncSetAttribute(k_tc_attend_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  CSA_LAUNCH(k_tc_attend_decode, dim3(Q * S), dim3(kThreads), kSmem, s, a);
+  if (cluster) {
+    if (S != 2 && S != 4) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_pdl_cluster(k_tc_attend_decode, dim3(Q * S), dim3(kThreads), kSmem, s, S, a);
+    if (e != cudaSuccess) return e;
+  } else {
+    CSA_LAUNCH(k_tc_attend_decode, dim3(Q * S), dim3(kThreads), kSmem, s, a);
+  }
   return cudaGetLastError();
 }
 
