@@ -288,9 +288,10 @@ __device__ __forceinline__ void select_bin(const int* h, int need, uint32_t pref
 
 // The same step with every warp taking the decision itself, so that no barrier follows it: after the one barrier
 // each warp scans the 32 warp totals, finds the warp whose bins hold the crossing and rescans those 64 bins (read
-// from h, which must then stay unchanged until the next block barrier).  Returns the new prefix and need.
+// from h, which must then stay unchanged until the next block barrier).  Returns the new prefix and need, and
+// the selected bin's count.
 __device__ __forceinline__ void select_bin_every_warp(const int* h, int& need, uint32_t& prefix, int shift,
-                                                      int* warp_tot) {
+                                                      int* warp_tot, int& bin_count) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int v = h[2047 - 2 * threadIdx.x] + h[2046 - 2 * threadIdx.x];
 #pragma unroll
@@ -321,6 +322,7 @@ __device__ __forceinline__ void select_bin_every_warp(const int* h, int& need, u
   const bool in_hi = excl + c_hi >= need;
   const int new_need = in_hi ? need - excl : need - excl - c_hi;
   const uint32_t bin = in_hi ? (uint32_t)b_hi : (uint32_t)(b_hi - 1);
+  bin_count = __shfl_sync(0xffffffffu, in_hi ? c_hi : c_lo, hl);
   need = __shfl_sync(0xffffffffu, new_need, hl);
   prefix |= __shfl_sync(0xffffffffu, bin, hl) << shift;
 }
@@ -554,19 +556,23 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
       hist[pass + 1][2 * threadIdx.x + 1] = 0;
     }
     __syncthreads();
-    select_bin_every_warp(h, need, prefix, shift, warp_tot);
+    int bin_count;
+    select_bin_every_warp(h, need, prefix, shift, warp_tot, bin_count);
     mask |= dmask << shift;
+    // the selected bin holds exactly the keys still needed: every one of them is kept, so the later digits
+    // decide nothing (the same answer in every warp: all read the same histogram)
+    if (bin_count == need) break;
   }
-  // prefix = order key of the k-th largest score: keep every key above it and the `need` lowest-indexed keys
-  // equal to it, in ascending row order
+  // prefix = the k-th largest order key on the digits decided (mask): keep every key above it there and the
+  // `need` lowest-indexed keys equal to it there, in ascending row order
   // One scan of (keys above << 16 | keys equal) per thread gives both counts before it (each < 2^16): the
   // thread's first output slot is (above before) + min(equal before, need).
   int gt = 0, eq = 0;
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) {
     const bool v = i < K && r0 + i < nvis;
-    gt += (v && uk[i] > prefix) ? 1 : 0;
-    eq += (v && uk[i] == prefix) ? 1 : 0;
+    gt += (v && (uk[i] & mask) > prefix) ? 1 : 0;
+    eq += (v && (uk[i] & mask) == prefix) ? 1 : 0;
   }
   const int packed = (gt << 16) | eq;
   // one block barrier: every warp scans the 32 warp totals itself
@@ -594,8 +600,8 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
 #pragma unroll
   for (int i = 0; i < kTopkRegKeys; ++i) {
     const bool v = i < K && r0 + i < nvis;
-    bool keep = v && uk[i] > prefix;
-    if (v && uk[i] == prefix) keep = eq_rank++ < need;
+    bool keep = v && (uk[i] & mask) > prefix;
+    if (v && (uk[i] & mask) == prefix) keep = eq_rank++ < need;
     if (keep) {
       if (o < topk) out[o] = r0 + i;
       ++o;

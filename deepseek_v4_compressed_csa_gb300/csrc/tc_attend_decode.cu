@@ -525,21 +525,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
       tab[tid * (S + 1) + S] = 1.0f / (expf(z - M) + zs);
     }
     __syncthreads();
-    // warp w: heads 8w .. 8w + 7; lane: 4-dim columns of this rank's slice
+    // warp w: heads 8w .. 8w + 7, four at a time with every split's values requested together (one remote round
+    // trip per four heads; one per head measured slower, and so did a remote store of every value, and fetching
+    // the splits' statistics in the same round); lane: 4-dim columns of this rank's slice.  A split's values are
+    // read whatever its weight (a split without rows left zeros) and added only when the weight is not zero.
     const int r = it.s, ncol = kAD / 4 / S;
-    for (int hh = 0; hh < 8; ++hh) {
-      const int h = warp * 8 + hh;
-      for (int c = lane; c < ncol; c += 32) {
-        const int d = r * (kAD / S) + 4 * c;
+    for (int c = lane; c < ncol; c += 32) {
+      const int d = r * (kAD / S) + 4 * c;
+#pragma unroll 1
+      for (int h0 = warp * 8; h0 < warp * 8 + 8; h0 += 4) {
+        float4 x[4][4];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int sp = 0; sp < 4; ++sp)
+            if (sp < S) x[hh][sp] = tc::ld_cluster_f4(tc::cluster_map(accs + (h0 + hh) * kAD + d, sp));
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+        const int h = h0 + hh;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int sp = 0; sp < S; ++sp) {
-          const float f = tab[h * (S + 1) + sp];
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+          const float f = sp < S ? tab[h * (S + 1) + sp] : 0.f;
           if (f != 0.f) {
-            const float4 x = tc::ld_cluster_f4(tc::cluster_map(accs + h * kAD + d, sp));
-            v[0] = fmaf(x.x, f, v[0]);
-            v[1] = fmaf(x.y, f, v[1]);
-            v[2] = fmaf(x.z, f, v[2]);
-            v[3] = fmaf(x.w, f, v[3]);
+            v[0] = fmaf(x[hh][sp].x, f, v[0]);
+            v[1] = fmaf(x[hh][sp].y, f, v[1]);
+            v[2] = fmaf(x[hh][sp].z, f, v[2]);
+            v[3] = fmaf(x[hh][sp].w, f, v[3]);
           }
         }
         const float invZ = tab[h * (S + 1) + S];
@@ -559,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_attend_decode(DecArgs a) {
         hv[0] = __floats2bfloat162_rn(v[0], v[1]);
         hv[1] = __floats2bfloat162_rn(v[2], v[3]);
         *reinterpret_cast<uint2*>(a.out + ((size_t)it.q * kAH + h) * kAD + d) = pk;
+        }
       }
     }
     tc::cluster_sync();
