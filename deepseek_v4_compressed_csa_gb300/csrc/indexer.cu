@@ -251,10 +251,11 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
 // One radix-select step over a complete 2048-bin histogram h (the caller's __syncthreads() separates the
 // histogram from this call, and a second one separates this call from the use of the result): the bins are taken
 // in descending order (thread t owns bins 2047-2t and 2046-2t) and the bin where the running count reaches `need`
-// gives *s_prefix = prefix | bin << shift and *s_need = the count still needed inside that bin.  One block barrier:
-// each warp scans its own 64 bins, then every warp scans the 32 warp totals itself.  Requires 1024 threads.
+// gives *s_prefix = prefix | bin << shift, *s_need = the count still needed inside that bin and *s_count = the
+// bin's count.  One block barrier: each warp scans its own 64 bins, then every warp scans the 32 warp totals
+// itself.  Requires 1024 threads.
 __device__ __forceinline__ void select_bin(const int* h, int need, uint32_t prefix, int shift, int* warp_tot,
-                                           uint32_t* s_prefix, int* s_need) {
+                                           uint32_t* s_prefix, int* s_need, int* s_count) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int b_hi = 2047 - 2 * threadIdx.x, b_lo = b_hi - 1;
   const int c_hi = h[b_hi], c_lo = h[b_lo];
@@ -279,9 +280,11 @@ __device__ __forceinline__ void select_bin(const int* h, int need, uint32_t pref
     if (excl + c_hi >= need) {
       *s_prefix = prefix | ((uint32_t)b_hi << shift);
       *s_need = need - excl;
+      *s_count = c_hi;
     } else {
       *s_prefix = prefix | ((uint32_t)b_lo << shift);
       *s_need = need - excl - c_hi;
+      *s_count = c_lo;
     }
   }
 }
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
+  __shared__ int s_need, s_count;
   const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
   const int p = query_pos(pos, pos0, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
@@ -381,11 +384,14 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
       }
     }
     __syncthreads();
-    select_bin(hist, need, prefix, shift, warp_tot, &s_prefix, &s_need);
+    select_bin(hist, need, prefix, shift, warp_tot, &s_prefix, &s_need, &s_count);
     __syncthreads();
     prefix = s_prefix;
     need = s_need;
     mask |= dmask << shift;
+    // the selected bin holds exactly the keys still needed: every one is kept, the later digits decide nothing
+    // (read by every thread after the barrier: the same answer everywhere)
+    if (s_count == need) break;
   }
   // Compaction in ascending row order: warp w owns the contiguous keys [w*per, (w+1)*per).  Pass 1 counts
   // each warp's keys above / equal to the threshold, one warp turns the counts into output offsets (the
@@ -399,8 +405,8 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t u = j < hi ? sm_keys[j] : 0u;
-    gt_n += __popc(__ballot_sync(0xffffffffu, j < hi && u > prefix));
-    eq_n += __popc(__ballot_sync(0xffffffffu, j < hi && u == prefix));
+    gt_n += __popc(__ballot_sync(0xffffffffu, j < hi && (u & mask) > prefix));
+    eq_n += __popc(__ballot_sync(0xffffffffu, j < hi && (u & mask) == prefix));
   }
   if (lane == 0) {
     w_gt[wid] = gt_n;
@@ -435,9 +441,9 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t u = j < hi ? sm_keys[j] : 0u;
-    const bool eq = j < hi && u == prefix;
+    const bool eq = j < hi && (u & mask) == prefix;
     const unsigned eqb = __ballot_sync(0xffffffffu, eq);
-    const bool take = (j < hi && u > prefix) || (eq && eq_rank + __popc(eqb & lt) < need);
+    const bool take = (j < hi && (u & mask) > prefix) || (eq && eq_rank + __popc(eqb & lt) < need);
     const unsigned tb = __ballot_sync(0xffffffffu, take);
     if (take) {
       const int o = slot + __popc(tb & lt);
