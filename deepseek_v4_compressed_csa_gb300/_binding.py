@@ -21,13 +21,15 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libcsa.so")
 
 CSA_F32, CSA_BF16 = 0, 1
 OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL, OP_COMPRESS_PAIR = 0, 1, 2, 3, 4
+OP_COMPRESS_VARLEN, OP_ATTEND_PREFILL_VARLEN = 5, 6
 DEV_CAPACITY, DEV_STATE, DEV_RANGE, DEV_ROLLBACK = 1, 2, 4, 8
 CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
 EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "csa_compress_append", "csa_index_topk",
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
            "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions",
-           "csa_compress_append_pair", "csa_trim", "csa_index_topk_verify", "csa_attend_verify")
+           "csa_compress_append_pair", "csa_trim", "csa_index_topk_verify", "csa_attend_verify",
+           "csa_compress_append_varlen", "csa_attend_prefill_varlen")
 
 
 class CSAError(RuntimeError):
@@ -95,6 +97,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_index_topk_verify.restype = i32
     lib.csa_attend_verify.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.csa_attend_verify.restype = i32
+    lib.csa_compress_append_varlen.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, sz, vp, vp]
+    lib.csa_compress_append_varlen.restype = i32
+    lib.csa_attend_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, vp, i32, vp, vp,
+                                              vp, vp, vp, sz, vp, vp]
+    lib.csa_attend_prefill_varlen.restype = i32
     _lib = lib
     return lib
 
@@ -430,6 +437,77 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, windo
         ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(iq), _ptr(iw), _ptr(sink), T, int(pos0), _ptr(window),
         _ptr(pool), _ptr(ikeys), cap, _ptr(n_rows), _ptr(inv_freq), _ptr(out), _ptr(sel_out), _ptr(ws), nb,
         _ptr(err), _stream(stream)))
+    return err
+
+
+def _expect_varlen(cu_seqlens, B: int, N: int, T_max: int):
+    _expect("cu_seqlens", cu_seqlens, torch.int32, (B + 1,))
+    if not 1 <= int(T_max) <= N:
+        raise ValueError(f"T_max = {T_max}: expected 1 <= T_max <= N = {N}")
+
+
+def compress_append_varlen(layer: Layer, comp: Compressor, x, cu_seqlens, T_max: int, pos, frontier, pool, n_rows,
+                           inv_freq, ws=None, err=None, stream=None):
+    """csa_compress_append_varlen; x [N, X] packs B chunks, sequence b's rows cu_seqlens[b] .. cu_seqlens[b+1]-1
+    (device int32 [B+1]); T_max (host) bounds every chunk's length."""
+    _expect("x", x, layer.dtype)
+    if x.dim() != 2 or x.shape[1] != layer.X:
+        raise ValueError(f"x: shape {tuple(x.shape)}, expected [N, {layer.X}]")
+    N = x.shape[0]
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 3 or pool.shape[2] != comp.d:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [B, cap, {comp.d}]")
+    B, cap = pool.shape[0], pool.shape[1]
+    _expect_varlen(cu_seqlens, B, N, T_max)
+    _expect_comp(layer, comp, "comp")
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("frontier", frontier, layer.dtype, (B, _frontier_len(layer), 2 * layer.lanes * comp.d))
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect_err(err)
+    ws, nb = _ws(layer, OP_COMPRESS_VARLEN, B, N, cap, ws, x.device)
+    err = _err(err, x.device)
+    L, C = layer._c(), comp._c()
+    _check("csa_compress_append_varlen", load_library().csa_compress_append_varlen(
+        ctypes.byref(L), ctypes.byref(C), _ptr(x), B, _ptr(cu_seqlens), N, int(T_max), _ptr(pos), _ptr(frontier),
+        _ptr(pool), cap, _ptr(n_rows), _ptr(inv_freq), _ptr(ws), nb, _ptr(err), _stream(stream)))
+    return err
+
+
+def attend_prefill_varlen(layer: Layer, q, kv_new, iq, iw, sink, cu_seqlens, T_max: int, pos, window, pool, ikeys,
+                          n_rows, inv_freq, out, sel_out=None, ws=None, err=None, stream=None):
+    """csa_attend_prefill_varlen; q [N, H, D], kv_new [N, D], iq [N, Hi, Di], iw [N, Hi], out [N, H, D] pack B
+    chunks (rows cu_seqlens[b] .. cu_seqlens[b+1]-1 at positions pos[b] ..); window [B, W+rollback, D], pool
+    [B, cap, D], ikeys [B, cap, Di], n_rows [B]."""
+    _expect("q", q, layer.dtype)
+    if q.dim() != 3 or q.shape[1:] != (layer.H, layer.D):
+        raise ValueError(f"q: shape {tuple(q.shape)}, expected [N, {layer.H}, {layer.D}]")
+    N = q.shape[0]
+    _expect("pool", pool, layer.dtype)
+    if pool.dim() != 3 or pool.shape[2] != layer.D:
+        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [B, cap, {layer.D}]")
+    B, cap = pool.shape[0], pool.shape[1]
+    _expect_varlen(cu_seqlens, B, N, T_max)
+    _expect("kv_new", kv_new, layer.dtype, (N, layer.D))
+    if layer.has_indexer:
+        _expect("iq", iq, layer.dtype, (N, layer.Hi, layer.Di))
+        _expect("iw", iw, layer.dtype, (N, layer.Hi))
+        _expect("ikeys", ikeys, layer.dtype, (B, cap, layer.Di))
+    _expect("sink", sink, torch.float32, (layer.H,))
+    _expect("pos", pos, torch.int32, (B,))
+    _expect("window", window, layer.dtype, (B, layer.ring_slots, layer.D))
+    _expect("n_rows", n_rows, torch.int32, (B,))
+    _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
+    _expect("out", out, layer.dtype, (N, layer.H, layer.D))
+    _expect("sel_out", sel_out, torch.int32, (N, layer.topk), optional=True)
+    _expect_err(err)
+    ws, nb = _ws(layer, OP_ATTEND_PREFILL_VARLEN, B, N, cap, ws, q.device)
+    err = _err(err, q.device)
+    L = layer._c()
+    _check("csa_attend_prefill_varlen", load_library().csa_attend_prefill_varlen(
+        ctypes.byref(L), _ptr(q), _ptr(kv_new), _ptr(iq), _ptr(iw), _ptr(sink), B, _ptr(cu_seqlens), N, int(T_max),
+        _ptr(pos), _ptr(window), _ptr(pool), _ptr(ikeys), cap, _ptr(n_rows), _ptr(inv_freq), _ptr(out), _ptr(sel_out),
+        _ptr(ws), nb, _ptr(err), _stream(stream)))
     return err
 
 

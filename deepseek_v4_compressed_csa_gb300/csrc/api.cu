@@ -74,6 +74,16 @@ void carve_prefill(Carver& c, const Dims& L, int T, int cap, IndexWs* iw, int32_
   }
   *aw = carve_attend(c, L, T, attend_splits(L, true, false, cap), T);
 }
+size_t ws_compress_varlen(const Dims& L, int B, int N) {
+  size_t best = 0;
+  for (int d : {L.D, L.Di}) {
+    if (d == L.Di && !L.has_indexer()) continue;
+    Carver c(nullptr);
+    carve_compress_varlen(c, L, d, B, N);
+    best = c.off > best ? c.off : best;
+  }
+  return best;
+}
 size_t ws_prefill(const Dims& L, int T, int cap) {
   Carver c(nullptr);
   IndexWs iw{};
@@ -127,6 +137,14 @@ csa_status csa_workspace_size(const csa_layer* layer, int op, int B, int T, int 
       *bytes = ws_decode(L, B, cap);
       return CSA_OK;
     case CSA_OP_ATTEND_PREFILL:
+      if (T < 1 || T > 16384) return CSA_ERR_ARG;
+      *bytes = ws_prefill(L, T, cap);
+      return CSA_OK;
+    case CSA_OP_COMPRESS_VARLEN:  // T: the batch's total tokens N
+      if (T < 1 || T > (1 << 20)) return CSA_ERR_ARG;
+      *bytes = ws_compress_varlen(L, B, T);
+      return CSA_OK;
+    case CSA_OP_ATTEND_PREFILL_VARLEN:  // T: the batch's total tokens N
       if (T < 1 || T > 16384) return CSA_ERR_ARG;
       *bytes = ws_prefill(L, T, cap);
       return CSA_OK;
@@ -277,6 +295,68 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
   }
   return cuda_status(launch_attend_prefill(L, q, kv_new, sink, T, pos0, window, pool, cap, n_rows,
                                            L.has_indexer() ? sel : nullptr, n_sel, inv_freq, out, aw, err, s));
+}
+
+// Host-side checks of a packed variable-length batch's sizes (the row table itself is on the device).
+static bool varlen_args_ok(int B, const int32_t* cu_seqlens, int N, int T_max) {
+  return B >= 1 && B <= (1 << 16) && N >= 1 && T_max >= 1 && T_max <= N && dev_i32(cu_seqlens);
+}
+
+csa_status csa_compress_append_varlen(const csa_layer* layer, const csa_compressor* comp, const void* x, int B,
+                                      const int32_t* cu_seqlens, int N, int T_max, const int32_t* pos,
+                                      void* frontier, void* pool, int cap, int32_t* n_rows, const float* inv_freq,
+                                      void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!varlen_args_ok(B, cu_seqlens, N, T_max) || N > (1 << 20)) return CSA_ERR_ARG;
+  if (!compress_args_ok(L, comp, B, 1, cap, frontier, pool, n_rows)) return CSA_ERR_ARG;
+  if (!dev_tensor(x) || !dev_i32(pos) || !dev_tensor(inv_freq) || !dev_i32(err)) return CSA_ERR_ARG;
+  Carver c0(nullptr);
+  carve_compress_varlen(c0, L, comp->d, B, N);
+  if (ws_bytes < c0.off || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  const CompressWs w = carve_compress_varlen(c, L, comp->d, B, N);
+  return cuda_status(launch_compress_varlen(L, *comp, x, B, cu_seqlens, N, T_max, pos, frontier, pool, cap, n_rows,
+                                            inv_freq, w, err, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_attend_prefill_varlen(const csa_layer* layer, const void* q, const void* kv_new, const void* iq,
+                                     const void* iw, const float* sink, int B, const int32_t* cu_seqlens, int N,
+                                     int T_max, const int32_t* pos, void* window, const void* pool,
+                                     const void* ikeys, int cap, const int32_t* n_rows, const float* inv_freq,
+                                     void* out, int32_t* sel_out, void* ws, size_t ws_bytes, int32_t* err,
+                                     void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!varlen_args_ok(B, cu_seqlens, N, T_max) || N > 16384 || cap < 1) return CSA_ERR_ARG;
+  if (!tc_attend_supported(L) || (L.has_indexer() && !tc_index_supported(L))) return CSA_ERR_UNSUPPORTED;
+  if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
+      !dev_tensor(inv_freq) || !dev_tensor(out))
+    return CSA_ERR_ARG;
+  if (!dev_i32(pos) || !dev_i32(n_rows) || !dev_i32(err)) return CSA_ERR_ARG;
+  if (L.has_indexer() && (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys))) return CSA_ERR_ARG;
+  if (sel_out && !dev_i32(sel_out)) return CSA_ERR_ARG;
+  const size_t need = ws_prefill(L, N, cap);
+  if (ws_bytes < need || !dev_tensor(ws)) return CSA_ERR_WORKSPACE;
+  Carver c(ws);
+  IndexWs iws{};
+  int32_t *sel = nullptr, *n_sel = nullptr;
+  AttendWs aw{};
+  carve_prefill(c, L, N, cap, &iws, &sel, &n_sel, &aw);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L.has_indexer()) {
+    if (sel_out) sel = sel_out;
+    cudaError_t e = launch_index_topk(L, iq, iw, N, ikeys, cap, n_rows, pos, B, inv_freq, sel, n_sel, iws, err, s,
+                                      cu_seqlens);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  } else if (sel_out && L.topk > 0) {
+    cudaMemsetAsync(sel_out, 0xff, (size_t)N * L.topk * sizeof(int32_t), s);
+  }
+  return cuda_status(launch_attend_prefill_varlen(L, q, kv_new, sink, B, cu_seqlens, N, T_max, window, pool, cap,
+                                                  n_rows, L.has_indexer() ? sel : nullptr, n_sel, pos, inv_freq,
+                                                  out, aw, err, s));
 }
 
 csa_status csa_index_topk_verify(const csa_layer* layer, const void* iq, const void* iw, int B, int T,

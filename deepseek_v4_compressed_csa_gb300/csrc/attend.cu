@@ -108,6 +108,47 @@ __global__ void k_window_store_chunk(const T* __restrict__ kvr, T* __restrict__ 
     copy8<T>(window + (size_t)(t % W) * D + e, kvr + (size_t)(t - pos0) * D + e);
 }
 
+// Packed variable-length chunks (row table cu [nseq + 1]): kvr[r] = RoPE(kv[r], pos[b] + r - cu[b]) for row r of
+// sequence b.
+template <typename T>
+__global__ void k_rope_rows_varlen(const T* __restrict__ kv, T* __restrict__ kvr, int D, int R,
+                                   const int32_t* __restrict__ pos, const int32_t* __restrict__ cu, int nseq,
+                                   const float* __restrict__ inv_freq) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x, b = varlen_seq(cu, nseq, r);
+  const int p = pos[b] + r - __ldg(cu + b);
+  const T* row = kv + (size_t)r * D;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float v = to_f(row[c]);
+    if (c >= D - R) {
+      const int i = (c - (D - R)) >> 1;
+      float cs, sn;
+      rope_cs(p, inv_freq, i, &cs, &sn);
+      const float a = to_f(row[D - R + 2 * i]), bb = to_f(row[D - R + 2 * i + 1]);
+      v = ((c - (D - R)) & 1) ? fmaf(a, sn, bb * cs) : fmaf(a, cs, -bb * sn);
+    }
+    kvr[(size_t)r * D + c] = from_f<T>(v);
+  }
+}
+
+// Each sequence's last min(T_b, Wr) chunk tokens into its ring: window[b][(pos[b] + i) mod Wr] = kvr[cu[b] + i].
+// A sequence whose row-table entries are inconsistent is left alone (the compress call reports the table).
+template <typename T>
+__global__ void k_window_store_varlen(const T* __restrict__ kvr, T* __restrict__ window, int Wr, int D, int N,
+                                      const int32_t* __restrict__ pos, const int32_t* __restrict__ cu) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y, c0 = cu[b], c1 = cu[b + 1];
+  if (c0 < 0 || c1 > N || c1 < c0) return;
+  const int Tb = c1 - c0, keep = min(Tb, Wr);
+  if ((int)blockIdx.x >= keep) return;
+  const int i = Tb - keep + blockIdx.x, t = pos[b] + i;
+  if (t < 0) return;
+  for (int e = threadIdx.x * 8; e < D; e += blockDim.x * 8)
+    copy8<T>(window + ((size_t)b * Wr + t % Wr) * D + e, kvr + (size_t)(c0 + i) * D + e);
+}
+
 struct AttnArgs {
   const void* qr;       // [Q, H, D] roped queries
   const void* pool;     // [B, cap, D]
@@ -557,6 +598,23 @@ cudaError_t launch_attend_decode(const Dims& L, const void* q, const void* kv_ne
                                    ws, err, s);
   return decode_t<float>(L, q, kv_new, sink, B, window, pool, cap, n_rows, sel, n_sel, pos, inv_freq, out, ws, err,
                          s);
+}
+
+cudaError_t launch_attend_prefill_varlen(const Dims& L, const void* q, const void* kv_new, const float* sink, int B,
+                                         const int32_t* cu, int N, int T_max, void* window, const void* pool, int cap,
+                                         const int32_t* n_rows, const int32_t* sel, const int32_t* n_sel,
+                                         const int32_t* pos, const float* inv_freq, void* out, const AttendWs& ws,
+                                         int32_t* err, cudaStream_t s) {
+  using T = __nv_bfloat16;
+  if (!tc_attend_supported(L)) return cudaErrorNotSupported;
+  CSA_LAUNCH(k_rope_rows_varlen<T>, dim3(N), dim3(128), 0, s, static_cast<const T*>(kv_new), static_cast<T*>(ws.kvr),
+             L.D, L.R, pos, cu, B, inv_freq);
+  cudaError_t e = launch_tc_attend_prefill(L, q, pool, window, ws.kvr, sel, n_sel, n_rows, 0, cap, sink, inv_freq, N,
+                                           out, err, s, pos, B, cu);
+  if (e != cudaSuccess) return e;
+  CSA_LAUNCH(k_window_store_varlen<T>, dim3(max(1, min(T_max, L.Wr)), B), dim3(64), 0, s,
+             static_cast<const T*>(ws.kvr), static_cast<T*>(window), L.Wr, L.D, N, pos, cu);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attend_prefill(const Dims& L, const void* q, const void* kv_new, const float* sink, int T,

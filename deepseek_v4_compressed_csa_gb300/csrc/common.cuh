@@ -72,6 +72,19 @@ template <> __device__ __forceinline__ void zero8<float>(float* dst) {
   reinterpret_cast<float4*>(dst)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// ---------------------------------------------------------------- packed variable-length batches
+// The tokens (queries) of B sequences packed back to back: sequence b owns rows [cu[b], cu[b+1]) of every packed
+// tensor (cu: [B + 1] device int32, cu[0] = 0, non-decreasing, cu[B] = N).  The sequence of row q is the last b
+// with cu[b] <= q (an empty sequence is passed over); the result is always in [0, B).
+__device__ __forceinline__ int varlen_seq(const int32_t* __restrict__ cu, int nseq, int q) {
+  int lo = 0, hi = nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= q) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // ---------------------------------------------------------------- RoPE
 // theta_i = (float)p * inv_freq[i], one fp32 multiply; accurate sincosf
 // (the library is built without fast-math: angles reach ~2.7e5 rad).

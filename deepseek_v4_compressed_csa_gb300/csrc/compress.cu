@@ -21,6 +21,16 @@
 
 namespace csa {
 
+CompressWs carve_compress_varlen(Carver& c, const Dims& L, int d, int B, int N) {
+  CompressWs w;
+  w.flags = c.take<int32_t>(B);
+  w.proj = c.take<char>((size_t)N * 2 * L.lanes * d * esize(L.dtype));
+  w.part = nullptr;
+  w.tickets = nullptr;
+  if (tc_project_supported(L, d)) carve_tc_project(c, L, d, N, &w.part, &w.tickets);
+  return w;
+}
+
 CompressWs carve_compress(Carver& c, const Dims& L, int d, int B, int T) {
   CompressWs w;
   w.flags = c.take<int32_t>(B);
@@ -88,7 +98,8 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
                                                    const float* __restrict__ ape, const float* __restrict__ norm_w,
                                                    float eps, const float* __restrict__ inv_freq,
                                                    T* __restrict__ pool, int cap, const float* __restrict__ part,
-                                                   int splits, int part_stride) {
+                                                   int splits, int part_stride, const int32_t* __restrict__ cu,
+                                                   int N) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm_pool[];  // [d] pooled, [d] normed, 32 reduction slots, [2*L*d] new token (part)
@@ -98,7 +109,15 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
   float* cur = sm_pool + 2 * d + 32;
   const int b = blockIdx.y;
   const int p0 = pos[b];
-  const int bad = compress_state_error(p0, n_rows[b], T_, ratio, cap);
+  // a packed variable-length batch (cu non-null): this sequence's tokens are projection rows cu[b] .. cu[b+1]-1
+  int row0 = b * T_, bad_table = 0;
+  if (cu) {
+    const int c0 = cu[b], c1 = cu[b + 1];
+    bad_table = (c0 < 0 || c1 < c0 || c1 > N) ? CSA_DEV_STATE : 0;
+    row0 = bad_table ? 0 : c0;
+    T_ = bad_table ? 0 : c1 - c0;
+  }
+  const int bad = bad_table ? bad_table : compress_state_error(p0, n_rows[b], T_, ratio, cap);
   const int rowlen = 2 * lanes * d;
   if (blockIdx.x == 0) {
     __syncthreads();  // every thread of this block has read n_rows before thread 0 may advance it
@@ -158,7 +177,7 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
   const int j = (p + 1) / ratio - 1;
   const int Ld = lanes * d;
   const T* fr = frontier + (size_t)b * F * rowlen;
-  const T* pj = proj + (size_t)b * T_ * rowlen;
+  const T* pj = proj + (size_t)row0 * rowlen;
 
   float ss = 0.f;
   const int t_lo = (lanes == 2) ? max(0, (j - 1) * ratio) : j * ratio;
@@ -575,15 +594,24 @@ __global__ void __launch_bounds__(kBlockThreads) k_pool_block(TokPool<T> pa, Tok
 template <typename T>
 __global__ void k_compress_finish(const int32_t* __restrict__ flags, const int32_t* __restrict__ pos, int T_,
                                   int ratio, int F, int rowlen, const T* __restrict__ proj, T* __restrict__ frontier,
-                                  int32_t* __restrict__ n_rows) {
+                                  int32_t* __restrict__ n_rows, const int32_t* __restrict__ cu) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
-  if (!flags[b]) return;
+  if (!flags[b]) return;  // also set for an inconsistent row-table entry
   const int p0 = pos[b];
+  int row0 = b * T_;
+  if (cu) {
+    row0 = cu[b];
+    T_ = cu[b + 1] - row0;
+  }
   const int keep = min(T_, F);
+  if (cu && (int)blockIdx.x >= keep) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
+    return;
+  }
   const int t = p0 + T_ - keep + blockIdx.x;
-  const T* src = proj + ((size_t)b * T_ + (t - p0)) * rowlen;
+  const T* src = proj + ((size_t)row0 + (t - p0)) * rowlen;
   T* dst = frontier + ((size_t)b * F + (t % F)) * rowlen;
   for (int e = threadIdx.x * 8; e < rowlen; e += blockDim.x * 8) copy8<T>(dst + e, src + e);
   if (blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
@@ -627,13 +655,54 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   const size_t smem = (2 * (size_t)d + 32 + (part ? (size_t)rowlen : 0)) * sizeof(float);
   CSA_LAUNCH(k_pool_emit<T>, dim3(ge), dim3(256), smem, s, ws.flags, pos, n_rows, err, fuse, T_, L.ratio, L.lanes, d,
              L.R, L.F, static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape, comp.norm_w, L.eps,
-             inv_freq, static_cast<T*>(pool), cap, part, splits, part_stride);
+             inv_freq, static_cast<T*>(pool), cap, part, splits, part_stride, static_cast<const int32_t*>(nullptr),
+             0);
   if (!fuse) {
     dim3 gf(min(T_, L.F), B);
     CSA_LAUNCH(k_compress_finish<T>, dim3(gf), dim3(128), 0, s, ws.flags, pos, T_, L.ratio, L.F, rowlen,
-                                            static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows);
+                                            static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows,
+               static_cast<const int32_t*>(nullptr));
   }
   return cudaGetLastError();
+}
+
+// A packed variable-length batch: x [N, X] holds B chunks back to back (row table cu, the longest T_max tokens).
+// One projection over the N rows, then per sequence the windows its chunk completes and its frontier slots.
+template <typename T>
+static cudaError_t compress_varlen_t(const Dims& L, const csa_compressor& comp, const void* x, int B,
+                                     const int32_t* cu, int N, int T_max, const int32_t* pos, void* frontier,
+                                     void* pool, int cap, int32_t* n_rows, const float* inv_freq,
+                                     const CompressWs& ws, int32_t* err, cudaStream_t s) {
+  const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
+  if (tc_project_supported(L, d)) {
+    cudaError_t e = launch_tc_project(L, d, x, N, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets, true, err, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    dim3 gp((2 * Ld + 7) / 8, (N + 7) / 8);
+    CSA_LAUNCH(k_project_simt<T, 8>, dim3(gp), dim3(256), 0, s, static_cast<const T*>(x),
+               static_cast<const T*>(comp.wkv), static_cast<const T*>(comp.wgate), N, L.X, Ld,
+               static_cast<T*>(ws.proj));
+  }
+  // windows a chunk of T_max tokens can complete: ceil(T_max / ratio), one more when it starts mid-window
+  const int maxwin = (T_max + L.ratio - 1) / L.ratio + 1;
+  const size_t smem = (2 * (size_t)d + 32) * sizeof(float);
+  CSA_LAUNCH(k_pool_emit<T>, dim3(maxwin, B), dim3(256), smem, s, ws.flags, pos, n_rows, err, 0, 0, L.ratio, L.lanes,
+             d, L.R, L.F, static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape, comp.norm_w, L.eps,
+             inv_freq, static_cast<T*>(pool), cap, static_cast<const float*>(nullptr), 1, 0, cu, N);
+  CSA_LAUNCH(k_compress_finish<T>, dim3(max(1, min(T_max, L.F)), B), dim3(128), 0, s, ws.flags, pos, 0, L.ratio, L.F,
+             rowlen, static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows, cu);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_varlen(const Dims& L, const csa_compressor& comp, const void* x, int B,
+                                   const int32_t* cu, int N, int T_max, const int32_t* pos, void* frontier,
+                                   void* pool, int cap, int32_t* n_rows, const float* inv_freq,
+                                   const CompressWs& ws, int32_t* err, cudaStream_t s) {
+  if (L.dtype == CSA_BF16)
+    return compress_varlen_t<__nv_bfloat16>(L, comp, x, B, cu, N, T_max, pos, frontier, pool, cap, n_rows, inv_freq,
+                                            ws, err, s);
+  return compress_varlen_t<float>(L, comp, x, B, cu, N, T_max, pos, frontier, pool, cap, n_rows, inv_freq, ws, err,
+                                  s);
 }
 
 // Both pools of a ratio-4 layer.  One token per sequence on the tensor-core path: the two projections as one

@@ -23,21 +23,30 @@ IndexWs carve_index(Carver& c, const Dims& L, int Q, int cap) {
 
 // Query q's position and sequence.  With device positions (decode, verify blocks) pos0 carries the number of
 // consecutive queries per sequence (0 or 1: one; T: a verify block of T tokens): query q belongs to sequence
-// q / T at position pos[q / T] + q % T.  Without them (a prefill chunk of one sequence): sequence 0, pos0 + q.
-__device__ __forceinline__ int query_pos(const int32_t* pos, int pos0, int q) {
+// q / T at position pos[q / T] + q % T.  With a packed variable-length batch (cu non-null: the row table, pos0 =
+// the number of sequences) query q belongs to sequence b = varlen_seq(cu, pos0, q) at pos[b] + q - cu[b].
+// Without positions (a prefill chunk of one sequence): sequence 0, pos0 + q.
+__device__ __forceinline__ int query_seq(const int32_t* pos, int pos0, const int32_t* cu, int q) {
+  if (cu) return varlen_seq(cu, pos0, q);
+  return pos ? q / max(1, pos0) : 0;
+}
+__device__ __forceinline__ int query_pos(const int32_t* pos, int pos0, const int32_t* cu, int q) {
+  if (cu) {
+    const int b = varlen_seq(cu, pos0, q);
+    return pos[b] + q - __ldg(cu + b);
+  }
   const int t = max(1, pos0);
   return pos ? pos[q / t] + q % t : pos0 + q;
 }
-__device__ __forceinline__ int query_seq(const int32_t* pos, int pos0, int q) { return pos ? q / max(1, pos0) : 0; }
 
 // qr[q][h][:] = RoPE(iq[q][h][:], p_q) rounded to the model dtype, held as fp32.
 template <typename T>
 __global__ void k_rope_iq(const T* __restrict__ iq, int Hi, int Di, int R, const int32_t* __restrict__ pos, int pos0,
-                          const float* __restrict__ inv_freq, float* __restrict__ qr) {
+                          const int32_t* __restrict__ cu, const float* __restrict__ inv_freq, float* __restrict__ qr) {
   pdl_trigger();
   pdl_wait();
   const int q = blockIdx.x;
-  const int p = query_pos(pos, pos0, q);
+  const int p = query_pos(pos, pos0, cu, q);
   for (int e = threadIdx.x; e < Hi * Di; e += blockDim.x) {
     const int c = e % Di;
     const T* row = iq + ((size_t)q * Hi + e / Di) * Di;
@@ -59,13 +68,14 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_index_scores(const float* __restrict__ qr, const T* __restrict__ iw,
                                                       int Hi, int Di, const T* __restrict__ ikeys, int cap,
                                                       const int32_t* __restrict__ n_rows,
-                                                      const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
+                                                      const int32_t* __restrict__ pos, int pos0,
+                                                      const int32_t* __restrict__ cu, int ratio, int topk,
                                                       float wscale, float* __restrict__ scores) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm_idx[];
-  const int q = blockIdx.y, bseq = query_seq(pos, pos0, q);
-  const int p = query_pos(pos, pos0, q);
+  const int q = blockIdx.y, bseq = query_seq(pos, pos0, cu, q);
+  const int p = query_pos(pos, pos0, cu, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   const int j0 = blockIdx.x * 64;
   if (nvis <= topk || j0 >= nvis) return;
@@ -160,8 +170,8 @@ __device__ __forceinline__ int block_excl_count(int flag, int* warp_tot, int* to
 // threshold and the lowest-indexed rows equal to it.
 __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int cap,
                                                const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
-                                               int pos0, int ratio, int topk, int32_t* __restrict__ sel,
-                                               int32_t* __restrict__ n_sel) {
+                                               int pos0, const int32_t* __restrict__ cu, int ratio, int topk,
+                                               int32_t* __restrict__ sel, int32_t* __restrict__ n_sel) {
   pdl_trigger();
   pdl_wait();
   __shared__ int hist[256];
@@ -169,8 +179,8 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
   __shared__ int s_total;
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
-  const int p = query_pos(pos, pos0, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, cu, q);
+  const int p = query_pos(pos, pos0, cu, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   int32_t* out = sel + (size_t)q * topk;
   if (nvis <= topk) {
@@ -337,7 +347,8 @@ __device__ __forceinline__ void select_bin_every_warp(const int* h, int& need, u
 // keys above the threshold and the lowest-indexed keys equal to it.
 __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ scores, int cap,
                                                     const int32_t* __restrict__ n_rows,
-                                                    const int32_t* __restrict__ pos, int pos0, int ratio, int topk,
+                                                    const int32_t* __restrict__ pos, int pos0,
+                                                    const int32_t* __restrict__ cu, int ratio, int topk,
                                                     int32_t* __restrict__ sel, int32_t* __restrict__ n_sel) {
   pdl_trigger();
   pdl_wait();
@@ -347,8 +358,8 @@ __global__ void __launch_bounds__(1024) k_topk_smem(const float* __restrict__ sc
   __shared__ int s_total;
   __shared__ uint32_t s_prefix;
   __shared__ int s_need, s_count;
-  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
-  const int p = query_pos(pos, pos0, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, cu, q);
+  const int p = query_pos(pos, pos0, cu, q);
   const int nvis = min(min(n_rows[bseq], cap), (p + 1) / ratio);
   int32_t* out = sel + (size_t)q * topk;
   if (nvis <= topk) {
@@ -498,7 +509,8 @@ __device__ __forceinline__ void score_rows(const __nv_bfloat16* __restrict__ qr,
 // floor(p/ratio) and row n_rows-1) are scored here and replace what the score buffer holds for them.
 __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ scores, int cap,
                                                    const int32_t* __restrict__ n_rows, const int32_t* __restrict__ pos,
-                                                   int pos0, int ratio, int topk, int32_t* __restrict__ sel,
+                                                   int pos0, const int32_t* __restrict__ cu, int ratio, int topk,
+                                                   int32_t* __restrict__ sel,
                                                    int32_t* __restrict__ n_sel, const __nv_bfloat16* __restrict__ qr,
                                                    const float* __restrict__ w, const __nv_bfloat16* __restrict__ keys) {
   pdl_trigger();
@@ -506,10 +518,10 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
   __shared__ int warp_tot[32], warp_tot2[32];
   __shared__ float part[2][64];
   __shared__ float new_score[2];
-  const int q = blockIdx.x, bseq = query_seq(pos, pos0, q);
+  const int q = blockIdx.x, bseq = query_seq(pos, pos0, cu, q);
   // The position is a step input (no kernel of the step writes it), so the most rows this query can see, and so
   // this thread's rows, are known before the wait: the score loads then go out in the same round as n_rows.
-  const int p = query_pos(pos, pos0, q);
+  const int p = query_pos(pos, pos0, cu, q);
   const int nv_max = max(0, min(cap, (p + 1) / ratio));
   const int K = max(1, (nv_max + 1023) >> 10);
   const int r0 = threadIdx.x * K;
@@ -620,39 +632,43 @@ __global__ void __launch_bounds__(1024) k_topk_reg(const float* __restrict__ sco
 constexpr int kTopkSmemMaxCap = 52 * 1024;
 
 static cudaError_t launch_topk(const Dims& L, const float* scores, int cap, const int32_t* n_rows, const int32_t* pos,
-                        int pos0, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
+                        int pos0, const int32_t* cu, int Q, int32_t* sel, int32_t* n_sel, cudaStream_t s) {
   if (cap <= kTopkRegKeys * 1024) {
-    CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel,
+    CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, cu, L.ratio, L.topk, sel, n_sel,
                static_cast<const __nv_bfloat16*>(nullptr), static_cast<const float*>(nullptr),
                static_cast<const __nv_bfloat16*>(nullptr));
   } else if (cap <= kTopkSmemMaxCap) {
     const size_t smem = (size_t)cap * 4 + 2048 * 4;
     cudaFuncSetAttribute(k_topk_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    CSA_LAUNCH(k_topk_smem, dim3(Q), dim3(1024), smem, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+    CSA_LAUNCH(k_topk_smem, dim3(Q), dim3(1024), smem, s, scores, cap, n_rows, pos, pos0, cu, L.ratio, L.topk, sel,
+               n_sel);
   } else {
-    CSA_LAUNCH(k_topk, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, L.ratio, L.topk, sel, n_sel);
+    CSA_LAUNCH(k_topk, dim3(Q), dim3(1024), 0, s, scores, cap, n_rows, pos, pos0, cu, L.ratio, L.topk, sel, n_sel);
   }
   return cudaSuccess;
 }
 
 template <typename T>
 static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
-                           const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq, int32_t* sel,
-                           int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s) {
+                           const int32_t* n_rows, const int32_t* pos, int pos0, const int32_t* cu,
+                           const float* inv_freq, int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err,
+                           cudaStream_t s) {
   if (tc_index_supported(L)) {
-    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, pos ? Q / max(1, pos0) : 1, cap, n_rows, pos, pos0,
-                                           inv_freq, ws.qr,
-                                           ws.scores, err, s);
+    // sequences holding the keys: one per query group of a verify block, or the varlen batch's count (pos0)
+    const int Bk = cu ? pos0 : (pos ? Q / max(1, pos0) : 1);
+    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, Bk, cap, n_rows, pos, pos0, inv_freq, ws.qr,
+                                           ws.scores, err, s, false, cu);
     if (e != cudaSuccess) return e;
-    return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
+    return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, cu, Q, sel, n_sel, s);
   }
-  CSA_LAUNCH(k_rope_iq<T>, dim3(Q), dim3(256), 0, s, static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, inv_freq, ws.qr);
+  CSA_LAUNCH(k_rope_iq<T>, dim3(Q), dim3(256), 0, s, static_cast<const T*>(iq), L.Hi, L.Di, L.R, pos, pos0, cu,
+             inv_freq, ws.qr);
   const float wscale = (float)(1.0 / sqrt((double)L.Di * (double)L.Hi));
   dim3 g((cap + 63) / 64, Q);
   size_t smem = (64 * (size_t)(L.Di + 4) + 64 * (size_t)L.Di + 16 * 64 + 64) * sizeof(float);
   CSA_LAUNCH(k_index_scores<T>, dim3(g), dim3(256), smem, s, ws.qr, static_cast<const T*>(iw), L.Hi, L.Di, static_cast<const T*>(ikeys),
-                                         cap, n_rows, pos, pos0, L.ratio, L.topk, wscale, ws.scores);
-  return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, Q, sel, n_sel, s);
+                                         cap, n_rows, pos, pos0, cu, L.ratio, L.topk, wscale, ws.scores);
+  return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, cu, Q, sel, n_sel, s);
 }
 
 cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys,
@@ -675,21 +691,24 @@ cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const vo
   }
   const auto* qr = reinterpret_cast<const __nv_bfloat16*>(ws.qr);
   const auto* w = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws.qr) + (size_t)Q * 64 * 128 * 2);
-  CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, ws.scores, cap, n_rows, pos, 0, L.ratio, L.topk, sel, n_sel, qr,
+  CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, ws.scores, cap, n_rows, pos, 0,
+             static_cast<const int32_t*>(nullptr), L.ratio, L.topk, sel, n_sel, qr,
              w, static_cast<const __nv_bfloat16*>(ikeys));
   return cudaGetLastError();
 }
 
 cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
                               const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq,
-                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s) {
+                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s,
+                              const int32_t* cu) {
   const int smax = 227 * 1024;
   if (L.dtype == CSA_BF16) {
     cudaFuncSetAttribute(k_index_scores<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-    return index_t<__nv_bfloat16>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, inv_freq, sel, n_sel, ws, err, s);
+    return index_t<__nv_bfloat16>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, cu, inv_freq, sel, n_sel, ws, err,
+                                  s);
   }
   cudaFuncSetAttribute(k_index_scores<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-  return index_t<float>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, inv_freq, sel, n_sel, ws, err, s);
+  return index_t<float>(L, iq, iw, Q, ikeys, cap, n_rows, pos, pos0, cu, inv_freq, sel, n_sel, ws, err, s);
 }
 
 }  // namespace csa

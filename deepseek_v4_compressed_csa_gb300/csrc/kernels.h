@@ -101,6 +101,14 @@ cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const 
 cudaError_t launch_compress(const Dims& L, const csa_compressor& comp, const void* x, int B, int T,
                             const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                             const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s);
+// A packed variable-length batch: x [N, X], sequence b's chunk = rows cu[b] .. cu[b+1]-1 at positions pos[b] ..;
+// ws carved for B sequences and N tokens (carve_compress(c, L, d, B, ceil(N / B)) is not enough: use
+// carve_compress_varlen).  A sequence whose row-table entries are inconsistent is flagged CSA_DEV_STATE and left.
+cudaError_t launch_compress_varlen(const Dims& L, const csa_compressor& comp, const void* x, int B,
+                                   const int32_t* cu, int N, int T_max, const int32_t* pos, void* frontier,
+                                   void* pool, int cap, int32_t* n_rows, const float* inv_freq,
+                                   const CompressWs& ws, int32_t* err, cudaStream_t s);
+CompressWs carve_compress_varlen(Carver& c, const Dims& L, int d, int B, int N);
 
 // ---- indexer.cu
 struct IndexWs {
@@ -116,12 +124,14 @@ cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const vo
                                          int cap, const int32_t* n_rows, const int32_t* pos, const float* inv_freq,
                                          int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err,
                                          cudaStream_t s, cudaEvent_t ready);
-// Scores and top-k for Q queries.  Query q belongs to sequence bseq(q) = (pos != null ? q : 0)
-// at position (pos != null ? pos[q] : pos0 + q); its visible rows are
-// min(n_rows[bseq], (p+1)/ratio).  sel [Q, topk], n_sel [Q].
+// Scores and top-k for Q queries.  Query q belongs to sequence bseq(q) at position p(q): without pos, 0 and
+// pos0 + q (one chunk); with pos, q / t and pos[q / t] + q % t, t = max(1, pos0) (decode, verify blocks); with
+// cu (a packed variable-length batch of pos0 sequences, row table cu [pos0 + 1]), the b with cu[b] <= q <
+// cu[b+1] and pos[b] + q - cu[b].  Its visible rows are min(n_rows[bseq], (p+1)/ratio).  sel [Q, topk], n_sel [Q].
 cudaError_t launch_index_topk(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int cap,
                               const int32_t* n_rows, const int32_t* pos, int pos0, const float* inv_freq,
-                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s);
+                              int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err, cudaStream_t s,
+                              const int32_t* cu = nullptr);
 
 // ---- tc_project.cu (tensor-core compressor projections; bf16)
 bool tc_project_supported(const Dims& L, int d);
@@ -150,7 +160,7 @@ size_t tc_index_ws(const Dims& L, int Q);
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s,
-                                   bool overlap = false);
+                                   bool overlap = false, const int32_t* cu = nullptr);
 
 // ---- tc_attend.cu (tensor-core attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_supported(const Dims& L);
@@ -178,11 +188,13 @@ cudaError_t launch_trim(const Dims& L, int B, const int32_t* n_back, int32_t* po
 // chunk, pool [cap, D]; persistent CTAs (one per SM) finalise the output.  Requires tc_attend_supported(L).
 // With device positions (verify blocks): query q of sequence q / qps at pos[q / qps] + q % qps over pool
 // [B, cap, D] and ring [B, Wr, D], every window token (the block's included) read from the ring; kvr unused.
+// With a row table cu (a packed variable-length batch of qps chunks, T = N rows): query q of sequence b at
+// pos[b] + q - cu[b]; tokens before pos[b] from the ring, the chunk's own from kvr [N, D] (roped).
 cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* pool, const void* ring,
                                      const void* kvr, const int32_t* sel, const int32_t* n_sel,
                                      const int32_t* n_rows, int pos0, int cap, const float* sink,
                                      const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s,
-                                     const int32_t* pos = nullptr, int qps = 1);
+                                     const int32_t* pos = nullptr, int qps = 1, const int32_t* cu = nullptr);
 
 // ---- tc_attend_decode.cu (tensor-core decode attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_decode_supported(const Dims& L);
@@ -223,6 +235,15 @@ cudaError_t launch_attend_prefill(const Dims& L, const void* q, const void* kv_n
                                   int pos0, void* window, const void* pool, int cap, const int32_t* n_rows,
                                   const int32_t* sel, const int32_t* n_sel, const float* inv_freq, void* out,
                                   const AttendWs& ws, int32_t* err, cudaStream_t s);
+
+// A packed variable-length batch of B prefill chunks (row table cu [B + 1], N rows, the longest T_max): the rows
+// are roped at their positions into ws.kvr, every query attends, then each sequence's last min(T_b, Wr) rows
+// enter its ring.  Tensor-core shapes only.
+cudaError_t launch_attend_prefill_varlen(const Dims& L, const void* q, const void* kv_new, const float* sink, int B,
+                                         const int32_t* cu, int N, int T_max, void* window, const void* pool, int cap,
+                                         const int32_t* n_rows, const int32_t* sel, const int32_t* n_sel,
+                                         const int32_t* pos, const float* inv_freq, void* out, const AttendWs& ws,
+                                         int32_t* err, cudaStream_t s);
 
 // Verify blocks: T tokens per sequence appended to the window ring (roped), then each attended by its own query.
 cudaError_t launch_attend_verify(const Dims& L, const void* q, const void* kv_new, const float* sink, int B, int T,

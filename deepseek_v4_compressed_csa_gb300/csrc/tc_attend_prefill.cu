@@ -89,6 +89,8 @@ struct PfArgs {
   const int32_t* n_rows;       // [1]; verify: [B]
   const int32_t* pos;          // null: one chunk at pos0 + q; verify blocks: [B], query q at pos[q / qps] + q % qps
   int qps;                     // verify: queries per sequence (every window token of the block already in the ring)
+  const int32_t* cu;           // packed variable-length batch of nseq chunks: row table [nseq + 1], query q of
+  int nseq;                    // sequence b (cu[b] <= q < cu[b+1]) at pos[b] + q - cu[b]; kvr holds every chunk's rows
   const float* sink;
   const float* inv_freq;
   int T, pos0, cap, topk, W, ratio;
@@ -105,8 +107,13 @@ struct Query {
 
 __device__ __forceinline__ Query query_info(const PfArgs& a, int qi) {
   Query r;
-  r.b = a.pos ? qi / a.qps : 0;
-  r.p = a.pos ? a.pos[r.b] + qi % a.qps : a.pos0 + qi;
+  if (a.cu) {
+    r.b = varlen_seq(a.cu, a.nseq, qi);
+    r.p = a.pos[r.b] + qi - __ldg(a.cu + r.b);
+  } else {
+    r.b = a.pos ? qi / a.qps : 0;
+    r.p = a.pos ? a.pos[r.b] + qi % a.qps : a.pos0 + qi;
+  }
   r.nrows = min(a.n_rows[r.b], a.cap);
   r.nsel = a.sel ? min(max(a.n_sel[qi], 0), a.topk) : max(0, min(r.nrows, (r.p + 1) / a.ratio));
   r.nwin = r.p >= 0 ? min(a.W, r.p + 1) : 0;
@@ -116,7 +123,9 @@ __device__ __forceinline__ Query query_info(const PfArgs& a, int qi) {
 
 // Code of row r_abs of query qi; j = sel[qi][r_abs] when a selection is given and r_abs < nsel.  A pool row's
 // code is its row in the pool tensor map (b * cap + j); a window token's is kRowTok0 - token for a chunk, and
-// kRowTok0 - (b * Wr + token mod Wr), its ring row, for verify blocks.
+// kRowTok0 - (b * Wr + token mod Wr), its ring row, for verify blocks; in a variable-length batch, kRowTok0 -
+// its ring row (tokens before the sequence's chunk) or kRowTok0 - (kChunkFlag + its packed chunk row).
+constexpr int kChunkFlag = 1 << 29;
 __device__ __forceinline__ int row_code(const PfArgs& a, const Query& qu, int r_abs, int j) {
   if (r_abs < qu.nsel) {
     if (!a.sel) j = r_abs;
@@ -126,6 +135,12 @@ __device__ __forceinline__ int row_code(const PfArgs& a, const Query& qu, int r_
   }
   if (r_abs < qu.nsel + qu.nwin) {
     const int tok = qu.p - qu.nwin + 1 + (r_abs - qu.nsel);
+    if (a.cu) {
+      const int p0 = a.pos[qu.b];
+      if (tok < p0) return kRowTok0 - (qu.b * a.Wr + tok % a.Wr);
+      const int row = min(max(__ldg(a.cu + qu.b) + (tok - p0), 0), a.T - 1);  // inside the packed rows
+      return kRowTok0 - (kChunkFlag + row);
+    }
     return kRowTok0 - (a.pos ? qu.b * a.Wr + tok % a.Wr : tok);
   }
   return kRowNone;
@@ -141,6 +156,10 @@ __device__ __forceinline__ int row_src(const PfArgs& a, int code, int& row) {
   }
   if (code <= kRowTok0) {
     const int tok = kRowTok0 - code;
+    if (a.cu) {  // variable-length batch: the ring row or the flagged packed chunk row
+      row = tok >= kChunkFlag ? tok - kChunkFlag : tok;
+      return tok >= kChunkFlag ? kSrcChunk : kSrcRing;
+    }
     if (a.pos) {
       row = tok;  // verify blocks: already the ring row
       return kSrcRing;
@@ -615,7 +634,7 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
                                      const void* kvr, const int32_t* sel, const int32_t* n_sel,
                                      const int32_t* n_rows, int pos0, int cap, const float* sink,
                                      const float* inv_freq, int T, void* out, int32_t* err, cudaStream_t s,
-                                     const int32_t* pos, int qps) {
+                                     const int32_t* pos, int qps, const int32_t* cu) {
   if (T <= 0) return cudaSuccess;
   if (cap <= 0) return cudaErrorInvalidValue;
   if (!g_sms_pf) {
@@ -631,7 +650,9 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
   a.sel = sel; a.n_sel = n_sel; a.n_rows = n_rows; a.sink = sink; a.inv_freq = inv_freq;
   a.T = T; a.pos0 = pos0; a.cap = cap; a.topk = L.topk; a.W = L.W; a.Wr = L.Wr; a.ratio = L.ratio;
   a.pos = pos; a.qps = max(1, qps);
-  const int nseq = pos ? (T + a.qps - 1) / a.qps : 1;
+  a.cu = cu; a.nseq = cu ? qps : 0;  // a row table: qps carries the number of sequences
+  if (cu && (!pos || qps < 1 || !kvr)) return cudaErrorInvalidValue;
+  const int nseq = cu ? qps : (pos ? (T + a.qps - 1) / a.qps : 1);
   if (pos && !kvr) kvr = q;  // verify blocks read no chunk rows: the chunk maps only need a valid address
   a.scale2 = L.scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -639,7 +660,7 @@ cudaError_t launch_tc_attend_prefill(const Dims& L, const void* q, const void* p
   // one-row boxes for the row gathers (tile::gather4 and single rows), 64-row boxes for the query blocks
   // and 128-row boxes of the chunk's rows (whole window tiles)
   CUtensorMap tq, tp, tk, tr, tkt;
-  a.chunk_tiles = !pos && T >= kPR;
+  a.chunk_tiles = (!pos || cu) && T >= kPR;
   if (!make_tmap_2d_bf16(&tq, q, (uint64_t)T * kAH, kAD, kAD * 2, 64) ||
       !make_tmap_2d_bf16(&tp, pool, (uint64_t)nseq * cap, kAD, kAD * 2, 1) ||
       !make_tmap_2d_bf16(&tk, kvr, (uint64_t)T, kAD, kAD * 2, 1) ||

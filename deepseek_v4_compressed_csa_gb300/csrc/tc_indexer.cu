@@ -66,6 +66,8 @@ struct IdxArgs {
   const int32_t* n_rows;
   const int32_t* pos;  // decode / verify positions [Q / qps] or null (prefill: pos0 + q)
   int qps;             // consecutive queries per sequence (a verify block of qps tokens; 1 for decode)
+  const int32_t* cu;   // packed variable-length batch: row table [nseq + 1] (queries of sequence b: cu[b] ..), or null
+  int nseq;
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
   int group_penalty;  // partition weight of a group's query block, in tiles
   float* scores;     // [Q, cap]
@@ -76,11 +78,19 @@ struct IdxArgs {
   float* w_out;           // [Q, 64]
 };
 
+__device__ __forceinline__ int idx_seq(const IdxArgs& a, int q) {
+  if (a.cu) return varlen_seq(a.cu, a.nseq, q);
+  return a.pos ? q / a.qps : 0;
+}
 __device__ __forceinline__ int idx_qpos(const IdxArgs& a, int q) {
+  if (a.cu) {
+    const int b = varlen_seq(a.cu, a.nseq, q);
+    return a.pos[b] + q - __ldg(a.cu + b);
+  }
   return a.pos ? a.pos[q / a.qps] + q % a.qps : a.pos0 + q;
 }
 __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
-  const int b = a.pos ? q / a.qps : 0;
+  const int b = idx_seq(a, q);
   return min(min(a.n_rows[b], a.cap), (idx_qpos(a, q) + 1) / a.ratio);
 }
 // Rows this scan scores for query q.  The overlapped decode scan, which runs while the index pool's compress
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g, t = itr.t;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
-        const int krow = (a.pos ? g * G / a.qps : 0) * a.cap + t * kTileRows;  // a group's queries share a sequence
+        const int krow = idx_seq(a, g * G) * a.cap + t * kTileRows;  // a group's queries share a sequence
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
         tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
@@ -555,15 +565,16 @@ size_t tc_index_ws(const Dims& L, int Q) {
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s,
-                                   bool overlap) {
+                                   bool overlap, const int32_t* cu) {
   if (!g_num_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
   }
   // queries per MMA: 4 for a prefill chunk and for verify blocks whose length is a multiple of 4 (the block's
-  // queries then share every key tile, one read for four), else 1 (decode)
-  const int G = !pos ? 4 : (pos0 > 1 && pos0 % 4 == 0 ? 4 : 1);
+  // queries then share every key tile, one read for four), else 1 (decode, and a packed variable-length batch,
+  // whose groups of four could straddle two sequences)
+  const int G = cu ? 1 : (!pos ? 4 : (pos0 > 1 && pos0 % 4 == 0 ? 4 : 1));
   CUtensorMap tk, tq;
   if (!make_tmap_2d_bf16(&tk, ikeys, (uint64_t)Bk * cap, 128, 256, kTileRows)) return cudaErrorInvalidValue;
   // the 4-query instance copies each group's query block (4 x 64 head rows) by TMA
@@ -576,6 +587,9 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   a.R = L.R;
   a.n_rows = n_rows; a.pos = pos; a.pos0 = pos0; a.ratio = L.ratio; a.topk = L.topk; a.cap = cap; a.Q = Q;
   a.qps = pos ? max(1, pos0) : 1;  // with device positions pos0 carries the queries per sequence
+  a.cu = cu;
+  a.nseq = cu ? pos0 : 0;         // ... and with a row table, the number of sequences
+  if (cu && (!pos || pos0 < 1)) return cudaErrorInvalidValue;
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
   a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
   a.group_penalty = G == 1 ? 3 : 0;

@@ -14,6 +14,8 @@
  *                            merge, inverse RoPE on the output.
  *   csa_attend_prefill_chunk the same for a chunk of T queries of one
  *                            sequence, each with its own causal top-k.
+ *   (*_varlen: a packed batch of chunks of different lengths; *_verify: verify
+ *   blocks of T tokens per sequence; csa_trim: rewind for speculative decoding.)
  *
  * Definitions follow the pages the method is described on:
  *   [MTPLX#216]  "DeepSeek-V4-Flash: native deepseek_v4 AR backend"
@@ -84,7 +86,9 @@ enum {
   CSA_OP_INDEX_TOPK = 1,
   CSA_OP_ATTEND_DECODE = 2,
   CSA_OP_ATTEND_PREFILL = 3,
-  CSA_OP_COMPRESS_PAIR = 4 /* csa_compress_append_pair (ratio-4 layers) */
+  CSA_OP_COMPRESS_PAIR = 4, /* csa_compress_append_pair (ratio-4 layers) */
+  CSA_OP_COMPRESS_VARLEN = 5,       /* csa_compress_append_varlen: B sequences, T = N packed tokens */
+  CSA_OP_ATTEND_PREFILL_VARLEN = 6  /* csa_attend_prefill_varlen: B sequences, T = N packed tokens */
 };
 
 /* One CSA layer.
@@ -292,6 +296,45 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
                                     const void* pool, const void* ikeys, int cap, const int32_t* n_rows,
                                     const float* inv_freq, void* out, int32_t* sel_out, void* ws, size_t ws_bytes,
                                     int32_t* err, void* stream);
+
+/* csa_compress_append_varlen, csa_attend_prefill_varlen — a packed batch of
+ * prefill chunks of different lengths (ragged batched prefill): sequence b's
+ * chunk is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of every packed tensor, at
+ * positions pos[b] .. pos[b] + T_b - 1 (T_b = cu_seqlens[b+1] - cu_seqlens[b]).
+ *
+ * Definition: for every sequence, exactly csa_compress_append on its chunk (each
+ * pool), then csa_attend_prefill_chunk on it with pos0 = pos[b] ([MTPLX#216]
+ * "Verification": decode == prefill across chunked prefill and batching).  The
+ * sequences share the launches: one projection over the N packed tokens, and
+ * per-query scoring, top-k and attention over all of them.
+ * Arguments
+ *   x [N, X]; q [N, H, D]; kv_new [N, D]; iq [N, Hi, Di]; iw [N, Hi]   model dtype,
+ *     packed (iq, iw, ikeys may be NULL when ratio != 4)
+ *   cu_seqlens int32 [B + 1] (device): 0 = cu[0] <= cu[1] <= ... <= cu[B] = N
+ *     (an empty chunk is allowed); T_max (host) >= every T_b sizes the grids
+ *   pos int32 [B] (device): each chunk's first position; not advanced here
+ *   frontier, pool, n_rows, window, ikeys: per sequence as for csa_compress_append
+ *     and csa_attend_decode ([B, ...] with pool capacity cap)
+ *   out [N, H, D]; sel_out [N, topk] int32 or NULL
+ * Workspace: csa_workspace_size(.., CSA_OP_COMPRESS_VARLEN, B, N, cap, ..) and
+ *   (.., CSA_OP_ATTEND_PREFILL_VARLEN, B, N, cap, ..).
+ * Errors: as the single-chunk calls; N <= 2^20 for the compress call and
+ *   N <= 16384 for the attention call (CSA_ERR_ARG beyond).  A row-table entry
+ *   with cu[b] < 0, cu[b+1] < cu[b] or cu[b+1] > N is flagged CSA_DEV_STATE by
+ *   the compress call, which leaves that sequence unchanged; every packed row
+ *   index the attention call derives from the table is clamped into [0, N).
+ *   The attention call needs the tensor-core shapes (bf16, H = 64, D = 512,
+ *   R = 64; Hi = 64, Di = 128 with an indexer): CSA_ERR_UNSUPPORTED otherwise. */
+csa_status csa_compress_append_varlen(const csa_layer* layer, const csa_compressor* comp, const void* x, int B,
+                                      const int32_t* cu_seqlens, int N, int T_max, const int32_t* pos,
+                                      void* frontier, void* pool, int cap, int32_t* n_rows, const float* inv_freq,
+                                      void* ws, size_t ws_bytes, int32_t* err, void* stream);
+csa_status csa_attend_prefill_varlen(const csa_layer* layer, const void* q, const void* kv_new, const void* iq,
+                                     const void* iw, const float* sink, int B, const int32_t* cu_seqlens, int N,
+                                     int T_max, const int32_t* pos, void* window, const void* pool,
+                                     const void* ikeys, int cap, const int32_t* n_rows, const float* inv_freq,
+                                     void* out, int32_t* sel_out, void* ws, size_t ws_bytes, int32_t* err,
+                                     void* stream);
 
 /* csa_index_topk_verify, csa_attend_verify — a verify block: T consecutive tokens
  * per sequence (a speculative step's last accepted token and its T-1 drafts),
