@@ -945,9 +945,11 @@ def run_ours(args):
         assert wl.err.item() == 0, f"device error word {wl.err.item()}"
 
     # ---- prefill chunk (config 5), timed once per repeat from a restored snapshot
-    prefill = None
+    prefill = prefill_varlen = None
     if not args.no_prefill:
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
+        if not args.no_other_configs:
+            prefill_varlen = run_prefill_varlen(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
 
     trim = trim_line(csa, csa_synth, dev)
     shared = None if args.no_other_configs else shared_line(csa, csa_synth, dev, flush, args.steps, args.warmup)
@@ -1006,6 +1008,7 @@ def run_ours(args):
                            "csa_advance_positions after the last layer"),
                 "indexer": args.indexer,
                 "prefill": prefill,
+                "prefill_varlen": prefill_varlen,
                 "other_decode_workloads": others,
                 "trim": trim,
                 "v41_shared_caches": shared,
@@ -1093,6 +1096,79 @@ def run_prefill(csa, csa_synth, dev, flush, repeats: int):
             "algorithmic_tflop": round(flops / 1e12, 4),
             "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats,
             "dram_traffic_bytes": _traffic("prefill_chunk_bytes", 1)}
+
+
+# A ragged prefill batch: eight requests' chunks (4096 tokens in all) at contexts from 2K to 64K, packed.
+VARLEN_SPECS = [(65536, 256), (32768, 512), (16384, 384), (8192, 640), (4096, 128), (49152, 1024), (24576, 768),
+                (2048, 384)]
+
+
+def run_prefill_varlen(csa, csa_synth, dev, flush, repeats: int) -> dict:
+    """csa_compress_append_varlen (both pools) + csa_attend_prefill_varlen on VARLEN_SPECS (Flash shapes, each
+    sequence's cache drawn from its own seeded stream), timed from a restored snapshot with the L2 flushed."""
+    import torch
+    cfg = csa_synth.CONFIGS[5]
+    B = len(VARLEN_SPECS)
+    lens = [t for _, t in VARLEN_SPECS]
+    N, T_max = sum(lens), max(lens)
+    cap = max(c + t for c, t in VARLEN_SPECS) // cfg.ratio + 8
+    parts = [csa_synth.synth_cache(cfg.replace(cid=cfg.cid + 300 + b), cap, B=1, ctx=c)
+             for b, (c, _) in enumerate(VARLEN_SPECS)]
+    d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    snap = {k: d(torch.cat([getattr(p, k) for p in parts]))
+            for k in ("pool", "ikeys", "window", "front_attn", "front_index", "n_rows", "pos")}
+    del parts
+    L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
+                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+
+    def comp(c):
+        return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
+    ca, ci = comp(csa_synth.compressor(cfg, "attn")), comp(csa_synth.compressor(cfg, "index"))
+    chunks = [csa_synth.chunk_inputs(cfg.replace(cid=cfg.cid + 400 + b), t) for b, t in enumerate(lens)]
+    x = d(torch.cat([ch.x[0] for ch in chunks]))
+    q, kv, iq, iw = (d(torch.cat([getattr(ch, f) for ch in chunks])) for f in ("q", "kv", "iq", "iw"))
+    cu = torch.tensor([0] + [sum(lens[:i + 1]) for i in range(B)], dtype=torch.int32, device=dev)
+    sink, invf = d(csa_synth.sinks(cfg)), d(csa_synth.inv_freq(cfg))
+    st = {k: v.clone() for k, v in snap.items()}
+    n_i = st["n_rows"].clone()
+    out = torch.empty(N, cfg.H, cfg.D, dtype=cfg.storage, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    u8 = lambda n: torch.empty(max(n, 256), dtype=torch.uint8, device=dev)  # noqa: E731
+    ws_c = u8(csa.workspace_size(L, csa.OP_COMPRESS_VARLEN, B, N, cap))
+    ws_p = u8(csa.workspace_size(L, csa.OP_ATTEND_PREFILL_VARLEN, B, N, cap))
+    times = []
+    for r in range(repeats + 1):
+        for k in st:
+            st[k].copy_(snap[k])
+        n_i.copy_(snap["n_rows"])
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        csa.compress_append_varlen(L, ca, x, cu, T_max, st["pos"], st["front_attn"], st["pool"], st["n_rows"], invf,
+                                   ws=ws_c, err=err)
+        csa.compress_append_varlen(L, ci, x, cu, T_max, st["pos"], st["front_index"], st["ikeys"], n_i, invf,
+                                   ws=ws_c, err=err)
+        csa.attend_prefill_varlen(L, q, kv, iq, iw, sink, cu, T_max, st["pos"], st["window"], st["pool"],
+                                  st["ikeys"], st["n_rows"], invf, out, ws=ws_p, err=err)
+        e1.record()
+        torch.cuda.synchronize()
+        if r > 0:
+            times.append(e0.elapsed_time(e1))
+    assert err.item() == 0
+    ms = statistics.median(times)
+    flops = N * cfg.X * (2 * 2 * (cfg.D + cfg.Di)) * 2
+    for c, t in VARLEN_SPECS:
+        for i in range(t):
+            nvis = min((c + t) // cfg.ratio, (c + i + 1) // cfg.ratio)
+            flops += nvis * cfg.Hi * cfg.Di * 2 + (min(nvis, cfg.topk) + min(cfg.W, c + i + 1)) * cfg.H * cfg.D * 4
+    _, tflops, _ = _peaks()
+    return {"workload": "flash-prefill-varlen-b8-n4096", "requests": [{"context": c, "tokens": t}
+                                                                      for c, t in VARLEN_SPECS],
+            "tok_per_s": round(N / (ms / 1e3), 1), "ms_per_batch": round(ms, 4),
+            "ms_per_batch_p10_p50_p90": [round(x, 4) for x in _percentiles(times)],
+            "algorithmic_tflop": round(flops / 1e12, 4),
+            "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats,
+            "calls": "csa_compress_append_varlen x 2 (attention and index pools), csa_attend_prefill_varlen"}
 
 
 def cpu_baseline(cfg, budget_s: float) -> dict:
@@ -1206,6 +1282,7 @@ def main():
         dev = torch.device("cuda", 0)
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         print(json.dumps(run_prefill(csa, csa_synth, dev, flush, args.prefill_repeats)))
+        print(json.dumps(run_prefill_varlen(csa, csa_synth, dev, flush, args.prefill_repeats)))
         return
     if args.oracle_sample:
         cid, seqs, warmup, steps, budget = args.oracle_sample

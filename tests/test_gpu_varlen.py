@@ -99,3 +99,32 @@ def test_varlen_sizes_refused_on_host():
     with pytest.raises(ValueError):  # a row table of the wrong length
         csa.compress_append_varlen(run.L, run.ca, x, cu[:2], 3, st.pos, st.front_attn, st.pool, st.n_rows,
                                    run.inv_freq)
+
+
+def test_varlen_inconsistent_row_table_is_flagged():
+    """A row-table entry that ends before it starts is flagged CSA_DEV_STATE by the compress call, which leaves that
+    sequence unchanged; the other sequences (even overlapping rows) are processed, and every row index the
+    attention call derives from the table stays inside the packed buffers."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[5]
+    B, N, cap = 3, 8, 1100
+    parts = [_seq_cache(cfg, cap, b, 4000 + 4 * b) for b in range(B)]
+    host = csa_synth.Cache(**{k: None if getattr(parts[0], k) is None else torch.cat([getattr(p, k) for p in parts])
+                              for k in vars(parts[0])})
+    run = G.Runner(cfg)
+    st = G.DevCache(host)
+    cu = torch.tensor([0, 5, 3, 8], dtype=torch.int32, device="cuda")
+    ch = csa_synth.chunk_inputs(cfg.replace(cid=cfg.cid + 90), N)
+    n_i = st.n_rows.clone()
+    csa.compress_append_varlen(run.L, run.ca, G.dev(ch.x[0]), cu, 5, st.pos, st.front_attn, st.pool, st.n_rows,
+                               run.inv_freq, err=run.err)
+    csa.compress_append_varlen(run.L, run.ci, G.dev(ch.x[0]), cu, 5, st.pos, st.front_index, st.ikeys, n_i,
+                               run.inv_freq, err=run.err)
+    out = torch.empty(N, cfg.H, cfg.D, dtype=cfg.storage, device="cuda")
+    csa.attend_prefill_varlen(run.L, G.dev(ch.q), G.dev(ch.kv), G.dev(ch.iq), G.dev(ch.iw), run.sink, cu, 5, st.pos,
+                              st.window, st.pool, st.ikeys, st.n_rows, run.inv_freq, out, err=run.err)
+    torch.cuda.synchronize()
+    assert run.err.item() & csa.DEV_STATE
+    assert st.n_rows.tolist() == [(4000 + 5) // 4, host.n_rows[1].item(), (4008 + 5) // 4]
+    for k in ("pool", "window", "front_attn"):
+        assert torch.equal(getattr(st, k)[1].cpu(), getattr(host, k)[1]), f"flagged sequence changed {k}"
