@@ -253,7 +253,11 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
 // norm weights, APE and RoPE frequencies do not depend on the position and are requested with it; the
 // partials and the window's seven older frontier entries are requested together once it is known (a token
 // that completes a window has p = 3 mod 4, so its window covers tokens p-7 .. p in a fixed lane / APE order).
-constexpr int kTokChans = 2;  // channels per thread: d <= 512
+constexpr int kTokChans = 2;  // channels per pooling thread: d <= 512
+// Threads of a single-token pooling block: all of them load the split-K partials (one round for up to 16 splits at
+// the Flash shapes), the first 256 pool (so the arithmetic, the norm's reduction order included, is the chunk
+// kernel's: the extra warps add zeros to the block sum).
+constexpr int kTokThreads = 512;
 
 // One pool's side of a single-token pooling launch.
 template <typename T>
@@ -271,7 +275,7 @@ struct TokPool {
 // Blocks [0, B) serve pool pa, blocks [B, 2B) (when launched) pool pb: a ratio-4 layer's two pools of the same
 // tokens in one launch.
 template <typename T>
-__global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<T> pb, int B,
+__global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, TokPool<T> pb, int B,
                                                          const int32_t* __restrict__ pos, int32_t* err, int R, int F,
                                                          float eps, const float* __restrict__ inv_freq) {
   pdl_trigger();
@@ -296,13 +300,14 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   float* rc = red + 32;
   float* rs = rc + R / 2;
   const int b = blockIdx.x - (second ? B : 0), tid = threadIdx.x;
+  const int cb = tid < 256 ? tid : (1 << 20);  // pooling channels cb + 256 i on threads 0-255 only
   // before the preceding kernel has completed: the position (a step input) and the layer's constants, which no
   // kernel writes
   const int p0 = pos[b];
   float nw[kTokChans], ap[kTokChans][kEnt];
 #pragma unroll
   for (int i = 0; i < kTokChans; ++i) {
-    const int c = tid + 256 * i;
+    const int c = cb + 256 * i;
     nw[i] = c < d ? __ldg(norm_w + c) : 0.f;
 #pragma unroll
     for (int e = 0; e < kEnt; ++e)  // entry e: token p-7+e, APE row e mod ratio, lane e / ratio
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   if (completes) {
 #pragma unroll
     for (int i = 0; i < kTokChans; ++i) {
-      const int c = tid + 256 * i;
+      const int c = cb + 256 * i;
 #pragma unroll
       for (int e = 0; e < kEnt - 1; ++e) {
         const int t = p0 - (kEnt - 1) + e;
@@ -334,9 +339,9 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
       }
     }
   }
-  for (int e = tid * 4; e < rowlen; e += 256 * 4) {
-    // batches of 8 splits, each batch's loads issued before its adds; the sum stays in split order
-    constexpr int kBatch = 8;
+  for (int e = tid * 4; e < rowlen; e += kTokThreads * 4) {
+    // batches of 16 splits, each batch's loads issued before its adds; the sum stays in split order
+    constexpr int kBatch = 16;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < splits; s0 += kBatch) {
       float4 v[kBatch];
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   if (bad) return;
   {
     T* dst = frontier + ((size_t)b * F + (p0 % F)) * rowlen;
-    for (int e = tid; e < rowlen; e += 256) dst[e] = from_f<T>(cur[e]);
+    for (int e = tid; e < rowlen; e += kTokThreads) dst[e] = from_f<T>(cur[e]);
   }
   if (!completes) {
     if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < kTokChans; ++i) {
-    const int c = tid + 256 * i;
+    const int c = cb + 256 * i;
     if (c >= d) continue;
     float sv[kEnt], kk[kEnt];
 #pragma unroll
@@ -421,12 +426,12 @@ __global__ void __launch_bounds__(256) k_pool_emit_token(TokPool<T> pa, TokPool<
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
 #pragma unroll
   for (int i = 0; i < kTokChans; ++i) {
-    const int c = tid + 256 * i;
+    const int c = cb + 256 * i;
     if (c < d) y[c] = rnd<T>(u[c] * inv * nw[i]);
   }
   __syncthreads();
   T* dst = pool + ((size_t)b * cap + j) * d;
-  for (int c = tid; c < d; c += 256) {
+  for (int c = tid; c < d; c += kTokThreads) {
     float v = y[c];
     if (c >= d - R) {
       const int i = (c - (d - R)) >> 1;
@@ -647,7 +652,8 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
     const size_t smem = ((size_t)rowlen + 2 * (size_t)d + 32 + L.R) * sizeof(float);
     const TokPool<T> tp{ws.flags, n_rows, static_cast<T*>(frontier), comp.ape, comp.norm_w, static_cast<T*>(pool),
                         part, d, cap, splits, part_stride};
-    CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(256), smem, s, tp, tp, B, pos, err, L.R, L.F, L.eps, inv_freq);
+    CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(kTokThreads), smem, s, tp, tp, B, pos, err, L.R, L.F, L.eps,
+               inv_freq);
     return cudaGetLastError();
   }
   const int maxwin = (T_ + L.ratio - 1) / L.ratio;
@@ -722,7 +728,8 @@ static cudaError_t compress_pair_token(const Dims& L, const csa_compressor& ca, 
                       cap_i, si, tc_project_cols(L, ci.d, B)};
   const int dm = max(ca.d, ci.d);
   const size_t smem = ((size_t)2 * L.lanes * dm + 2 * (size_t)dm + 32 + L.R) * sizeof(float);
-  CSA_LAUNCH(k_pool_emit_token<T>, dim3(2 * B), dim3(256), smem, s, ta, tb, B, pos, err, L.R, L.F, L.eps, inv_freq);
+  CSA_LAUNCH(k_pool_emit_token<T>, dim3(2 * B), dim3(kTokThreads), smem, s, ta, tb, B, pos, err, L.R, L.F, L.eps,
+             inv_freq);
   return cudaGetLastError();
 }
 
