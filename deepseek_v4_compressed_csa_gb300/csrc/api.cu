@@ -299,7 +299,9 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
 
 // Host-side checks of a packed variable-length batch's sizes (the row table itself is on the device).
 static bool varlen_args_ok(int B, const int32_t* cu_seqlens, int N, int T_max) {
-  return B >= 1 && B <= (1 << 16) && N >= 1 && T_max >= 1 && T_max <= N && dev_i32(cu_seqlens);
+  // (B + 1 <= 4096 N: the index scan's group table fits the query area of its workspace)
+  return B >= 1 && B <= (1 << 16) && N >= 1 && T_max >= 1 && T_max <= N && (long long)B + 1 <= 4096LL * N &&
+         dev_i32(cu_seqlens);
 }
 
 csa_status csa_compress_append_varlen(const csa_layer* layer, const csa_compressor* comp, const void* x, int B,

@@ -68,6 +68,8 @@ struct IdxArgs {
   int qps;             // consecutive queries per sequence (a verify block of qps tokens; 1 for decode)
   const int32_t* cu;   // packed variable-length batch: row table [nseq + 1] (queries of sequence b: cu[b] ..), or null
   int nseq;
+  const int32_t* gcu;  // G = 4 with a row table: group table [nseq + 1] (sequence b's ceil(T_b / 4) groups start at
+                       // gcu[b]; a group never straddles two sequences), or null
   int pos0, ratio, topk, cap, Q, G, n_items, tiles_per_group;
   int group_penalty;  // partition weight of a group's query block, in tiles
   float* scores;     // [Q, cap]
@@ -89,6 +91,30 @@ __device__ __forceinline__ int idx_qpos(const IdxArgs& a, int q) {
   }
   return a.pos ? a.pos[q / a.qps] + q % a.qps : a.pos0 + q;
 }
+// Group g's first query and query count (<= 0: no such group).  Without a group table: queries g G .. g G + G - 1
+// (those below Q); with one: group k of sequence b (gcu[b] <= g < gcu[b+1]) holds queries cu[b] + 4k .. of its
+// sequence only.
+__device__ __forceinline__ int grp_first(const IdxArgs& a, int g, int& cnt) {
+  if (a.gcu) {
+    int lo = 0, hi = a.nseq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.gcu + mid) <= g) lo = mid; else hi = mid - 1;
+    }
+    const int q0 = __ldg(a.cu + lo) + 4 * (g - __ldg(a.gcu + lo));
+    cnt = g < __ldg(a.gcu + a.nseq) ? min(4, __ldg(a.cu + lo + 1) - q0) : 0;
+    cnt = q0 < 0 ? 0 : min(cnt, a.Q - q0);  // an inconsistent row table never reaches past the packed queries
+    return q0;
+  }
+  cnt = min(a.G, a.Q - g * a.G);
+  return g * a.G;
+}
+// query qq of group g, or -1
+__device__ __forceinline__ int grp_query(const IdxArgs& a, int g, int qq) {
+  int cnt;
+  const int q0 = grp_first(a, g, cnt);
+  return qq < cnt ? q0 + qq : -1;
+}
 __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
   const int b = idx_seq(a, q);
   return min(min(a.n_rows[b], a.cap), (idx_qpos(a, q) + 1) / a.ratio);
@@ -104,7 +130,10 @@ __device__ __forceinline__ int scan_rows(const IdxArgs& a, int q) {
 // visible row anyway
 template <bool kOverlap>
 __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
-  const int qlast = min(a.Q - 1, g * a.G + a.G - 1);
+  int cnt;
+  const int q0 = grp_first(a, g, cnt);
+  if (cnt <= 0) return 0;
+  const int qlast = q0 + cnt - 1;
   if (kOverlap) {  // bound on the visible rows once the concurrent compress call has run
     if (min(a.cap, (idx_qpos(a, qlast) + 1) / a.ratio) <= a.topk) return 0;
     return (scan_rows<kOverlap>(a, qlast) + kTileRows - 1) / kTileRows;
@@ -218,12 +247,15 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     float th_freq;
     int p;
   };
-  // G = 4: the block of group g by TMA (rows g*256 .. of [Q*64, 128]; rows past the last query read zeros)
+  // G = 4: the block of group g by TMA (rows 64 q0 .. + 255 of [Q*64, 128], q0 its first query; rows past the last
+  // query read zeros, rows of another sequence's queries in a group of fewer than four are masked by the epilogue)
   auto issue_q = [&](int g) {
     if (pt == 0) {
+      int cnt;
+      const int q0 = grp_first(a, g, cnt);
       tc::mbar_arrive_expect_tx(&q_loaded[0], C::kQBytes);
-      tc::tma_load_2d(qbuf, &tm_q, &q_loaded[0], 0, g * N);
-      tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, g * N);
+      tc::tma_load_2d(qbuf, &tm_q, &q_loaded[0], 0, q0 * 64);
+      tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
     }
   };
   auto load_first = [&](int g, Pre& pre) {
@@ -239,13 +271,13 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      const int e = pt + i * kPrepThreads, q = g * G + e / 64;
-      pre.wv[i] = q < a.Q ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
+      const int e = pt + i * kPrepThreads, q = grp_query(a, g, e / 64);
+      pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
     }
     // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
     pre.th_freq = __ldg(a.inv_freq + (pt & 31));
-    const int q0 = g * G + pt / 32;
-    pre.p = (pt < G * 32 && q0 < a.Q) ? idx_qpos(a, q0) : 0;
+    const int q0 = pt < G * 32 ? grp_query(a, g, pt / 32) : -1;
+    pre.p = q0 >= 0 ? idx_qpos(a, q0) : 0;
   };
   // Static partition of the items, weighted: each group costs its tiles plus group_penalty tile-equivalents (the
   // query block a CTA must build when its range enters the group), placed before the group's first tile.  A CTA
@@ -266,25 +298,30 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-  if (warp >= C::kPrepWarp0 && i_begin < i_end) {
+  // the first query block: requested before the wait, except with a group table (written by the kernel before)
+  auto start_first = [&]() {
     if (G == 4) {
-      // this thread issues the block copies: it initialises their barrier itself, ahead of the CTA-wide sync.
       // The range's first group is copied now; whether it has tiles is known only after the wait (a prefill
       // chunk's first groups may have none), so the loop below drains this copy if it starts at a later group.
-      if (pt == 0) {
-        tc::mbar_init(&q_loaded[0], 1);
-        tc::fence_mbar_init();
-        tc::tma_prefetch(&tm_q);
-      }
       issue_q(g0);
     }
     load_first(g0, pre_a);
+  };
+  if (warp >= C::kPrepWarp0 && i_begin < i_end) {
+    if (G == 4 && pt == 0) {
+      // this thread issues the block copies: it initialises their barrier itself, ahead of the CTA-wide sync
+      tc::mbar_init(&q_loaded[0], 1);
+      tc::fence_mbar_init();
+      tc::tma_prefetch(&tm_q);
+    }
+    if (!a.gcu) start_first();
   }
   // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
   // before the token and the step's inputs, and writes only its own scratch, so it runs beside the compress
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
   // a projection kernel that lets successors start only once all earlier work is complete.)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) start_first();
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::kAcc * N);
     tc::tmem_relinquish();
@@ -311,7 +348,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g, t = itr.t;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
-        const int krow = idx_seq(a, g * G) * a.cap + t * kTileRows;  // a group's queries share a sequence
+        int cnt;
+        const int krow = idx_seq(a, grp_first(a, g, cnt)) * a.cap + t * kTileRows;  // a group's queries share
+                                                                                   // a sequence
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
         tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
@@ -366,7 +405,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     const int row = quarter * 32 + lane;
     int cur_g = -1, k = -1, acc = 0;
     uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
-    int nv[G];
+    int nv[G], qix[G];
     Items<kOverlap> itr;
     for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
       const int g = itr.g, t = itr.t;
@@ -375,7 +414,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         cur_g = g;
         if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
 #pragma unroll
-        for (int qq = 0; qq < G; ++qq) nv[qq] = g * G + qq < a.Q ? scan_rows<kOverlap>(a, g * G + qq) : 0;
+        for (int qq = 0; qq < G; ++qq) {
+          qix[qq] = grp_query(a, g, qq);
+          nv[qq] = qix[qq] >= 0 ? scan_rows<kOverlap>(a, qix[qq]) : 0;
+        }
       }
       if (!tc::mbar_wait(&acc_full[acc], (acc_par >> acc) & 1)) { failed = true; break; }
       tc::fence_after_sync();
@@ -410,7 +452,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
             s23 = __ffma2_rn(make_float2(w.z, w.w), r23, s23);
           }
           const float s = (s01.x + s01.y) + (s23.x + s23.y);
-          if (j < nv[qq]) a.scores[(size_t)(g * G + qq) * a.cap + j] = s;
+          if (j < nv[qq]) a.scores[(size_t)qix[qq] * a.cap + j] = s;
         }
       }
       tc::fence_before_sync();
@@ -450,8 +492,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     // the first group of the range was requested up front (before the key stream saturates memory and stretches
     // every round trip); the second is prefetched into L2
     if (g1 >= 0) {
+      int cnt1;
+      const int q01 = grp_first(a, g1, cnt1);
       for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
-        if (g1 * G + e / 32 < a.Q) tc::prefetch_l2(a.iq + ((size_t)(g1 * G) * 64 + e * 2) * 128, 512);
+        if (e / 32 < cnt1) tc::prefetch_l2(a.iq + ((size_t)q01 * 64 + e * 2) * 128, 512);
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
@@ -490,8 +534,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         int p = pre.p;
         float f = pre.th_freq;
         if (e != pt) {  // G = 4: the second entry of this thread
-          const int q = g * G + e / 32;
-          p = q < a.Q ? idx_qpos(a, q) : 0;
+          const int q = grp_query(a, g, e / 32);
+          p = q >= 0 ? idx_qpos(a, q) : 0;
           f = __ldg(a.inv_freq + (e & 31));
         }
         sincosf(__fmul_rn((float)p, f), &rsin[e], &rcos[e]);
@@ -553,6 +597,37 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
 
 int g_num_sms = 0;
 
+// gcu[b] = sum over sequences before b of ceil(T_b / 4) (T_b = cu[b+1] - cu[b], an inconsistent entry counted as
+// empty), b = 0 .. nseq: one block, each thread a contiguous share of the sequences, then a block scan.
+__global__ void __launch_bounds__(1024) k_varlen_groups(const int32_t* __restrict__ cu, int nseq,
+                                                        int32_t* __restrict__ gcu) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int wsum[32];
+  const int per = (nseq + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(nseq, (int)threadIdx.x * per), b1 = min(nseq, b0 + per);
+  auto groups = [&](int b) { return (max(0, cu[b + 1] - cu[b]) + 3) / 4; };
+  int mine = 0;
+  for (int b = b0; b < b1; ++b) mine += groups(b);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < wid; ++w) base += wsum[w];
+  int run = base + incl - mine;
+  for (int b = b0; b < b1; ++b) {
+    gcu[b] = run;
+    run += groups(b);
+  }
+  if (threadIdx.x == blockDim.x - 1) gcu[nseq] = run;
+}
+
 }  // namespace
 
 bool tc_index_supported(const Dims& L) { return L.dtype == CSA_BF16 && L.Hi == 64 && L.Di == 128; }
@@ -571,10 +646,10 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  // queries per MMA: 4 for a prefill chunk and for verify blocks whose length is a multiple of 4 (the block's
-  // queries then share every key tile, one read for four), else 1 (decode, and a packed variable-length batch,
-  // whose groups of four could straddle two sequences)
-  const int G = cu ? 1 : (!pos ? 4 : (pos0 > 1 && pos0 % 4 == 0 ? 4 : 1));
+  // queries per MMA: 4 for a prefill chunk, a packed variable-length batch (groups of four of one sequence, from a
+  // group table) and verify blocks whose length is a multiple of 4 (a group's queries share every key tile, one
+  // read for four), else 1 (decode)
+  const int G = cu ? 4 : (!pos ? 4 : (pos0 > 1 && pos0 % 4 == 0 ? 4 : 1));
   CUtensorMap tk, tq;
   if (!make_tmap_2d_bf16(&tk, ikeys, (uint64_t)Bk * cap, 128, 256, kTileRows)) return cudaErrorInvalidValue;
   // the 4-query instance copies each group's query block (4 x 64 head rows) by TMA
@@ -591,7 +666,17 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   a.nseq = cu ? pos0 : 0;         // ... and with a row table, the number of sequences
   if (cu && (!pos || pos0 < 1)) return cudaErrorInvalidValue;
   a.G = G; a.tiles_per_group = (cap + kTileRows - 1) / kTileRows;
-  a.n_items = ((Q + G - 1) / G) * a.tiles_per_group;
+  // groups: Q / G rounded up; with a row table at most (Q + 3 nseq) / 4 (every sequence's last group may be short;
+  // groups past the table's total have no tiles)
+  const long long n_groups = cu ? ((long long)Q + 3LL * a.nseq) / 4 : (Q + G - 1) / G;
+  if (n_groups * a.tiles_per_group > INT32_MAX) return cudaErrorInvalidValue;
+  a.n_items = (int)(n_groups * a.tiles_per_group);
+  if (cu) {
+    // the group table goes into the query-output area of ws, which only the overlapped decode scan uses
+    if (!ws) return cudaErrorInvalidValue;
+    a.gcu = static_cast<const int32_t*>(ws);
+    CSA_LAUNCH(k_varlen_groups, dim3(1), dim3(1024), 0, s, cu, a.nseq, static_cast<int32_t*>(ws));
+  }
   a.group_penalty = G == 1 ? 3 : 0;
   a.scores = scores; a.err = err;
   if (overlap) {
