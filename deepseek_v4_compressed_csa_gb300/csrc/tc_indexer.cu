@@ -94,8 +94,9 @@ __device__ __forceinline__ int idx_qpos(const IdxArgs& a, int q) {
 // Group g's first query and query count (<= 0: no such group).  Without a group table: queries g G .. g G + G - 1
 // (those below Q); with one: group k of sequence b (gcu[b] <= g < gcu[b+1]) holds queries cu[b] + 4k .. of its
 // sequence only.
+template <int G>
 __device__ __forceinline__ int grp_first(const IdxArgs& a, int g, int& cnt) {
-  if (a.gcu) {
+  if (G == 4 && a.gcu) {
     int lo = 0, hi = a.nseq - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -106,13 +107,14 @@ __device__ __forceinline__ int grp_first(const IdxArgs& a, int g, int& cnt) {
     cnt = q0 < 0 ? 0 : min(cnt, a.Q - q0);  // an inconsistent row table never reaches past the packed queries
     return q0;
   }
-  cnt = min(a.G, a.Q - g * a.G);
-  return g * a.G;
+  cnt = min(G, a.Q - g * G);
+  return g * G;
 }
 // query qq of group g, or -1
+template <int G>
 __device__ __forceinline__ int grp_query(const IdxArgs& a, int g, int qq) {
   int cnt;
-  const int q0 = grp_first(a, g, cnt);
+  const int q0 = grp_first<G>(a, g, cnt);
   return qq < cnt ? q0 + qq : -1;
 }
 __device__ __forceinline__ int idx_nvis(const IdxArgs& a, int q) {
@@ -128,10 +130,10 @@ __device__ __forceinline__ int scan_rows(const IdxArgs& a, int q) {
 }
 // tiles that group g must score (its last query sees the most rows); 0 if the group's queries keep every
 // visible row anyway
-template <bool kOverlap>
+template <int G, bool kOverlap>
 __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
   int cnt;
-  const int q0 = grp_first(a, g, cnt);
+  const int q0 = grp_first<G>(a, g, cnt);
   if (cnt <= 0) return 0;
   const int qlast = q0 + cnt - 1;
   if (kOverlap) {  // bound on the visible rows once the concurrent compress call has run
@@ -146,7 +148,7 @@ __device__ __forceinline__ int group_tiles(const IdxArgs& a, int g) {
 // group's tiles past its visible rows are skipped.  Every role walks the same sequence with this iterator: one
 // division when it starts and one tile count per group, so that the MMA thread's per-tile bookkeeping stays a few
 // instructions (a division per tile had cost it ~1k clocks a tile, leaving the tensor pipe idle between tiles).
-template <bool kOverlap>
+template <int G, bool kOverlap>
 struct Items {
   int g, t, t1, g_last, i_end, tpg;
   // first item at or after i_begin; false if none
@@ -175,7 +177,7 @@ struct Items {
  private:
   __device__ __forceinline__ void bounds(const IdxArgs& a) {
     const int hi = (g == g_last) ? i_end - g * tpg : tpg;
-    t1 = min(group_tiles<kOverlap>(a, g), hi);
+    t1 = min(group_tiles<G, kOverlap>(a, g), hi);
   }
   __device__ __forceinline__ bool settle(const IdxArgs& a) {
     while (t >= t1) {
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   auto issue_q = [&](int g) {
     if (pt == 0) {
       int cnt;
-      const int q0 = grp_first(a, g, cnt);
+      const int q0 = grp_first<G>(a, g, cnt);
       tc::mbar_arrive_expect_tx(&q_loaded[0], C::kQBytes);
       tc::tma_load_2d(qbuf, &tm_q, &q_loaded[0], 0, q0 * 64);
       tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
@@ -271,12 +273,12 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      const int e = pt + i * kPrepThreads, q = grp_query(a, g, e / 64);
+      const int e = pt + i * kPrepThreads, q = grp_query<G>(a, g, e / 64);
       pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
     }
     // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
     pre.th_freq = __ldg(a.inv_freq + (pt & 31));
-    const int q0 = pt < G * 32 ? grp_query(a, g, pt / 32) : -1;
+    const int q0 = pt < G * 32 ? grp_query<G>(a, g, pt / 32) : -1;
     pre.p = q0 >= 0 ? idx_qpos(a, q0) : 0;
   };
   // Static partition of the items, weighted: each group costs its tiles plus group_penalty tile-equivalents (the
@@ -298,15 +300,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-  // the first query block: requested before the wait, except with a group table (written by the kernel before)
-  auto start_first = [&]() {
-    if (G == 4) {
-      // The range's first group is copied now; whether it has tiles is known only after the wait (a prefill
-      // chunk's first groups may have none), so the loop below drains this copy if it starts at a later group.
-      issue_q(g0);
-    }
-    load_first(g0, pre_a);
-  };
+  // The first query block is requested before the wait (step inputs), except with a group table, which the
+  // kernel before writes.  G = 4: the range's first group is copied now; whether it has tiles is known only after
+  // the wait (a prefill chunk's first groups may have none), so the loop below drains this copy if it starts at a
+  // later group.
   if (warp >= C::kPrepWarp0 && i_begin < i_end) {
     if (G == 4 && pt == 0) {
       // this thread issues the block copies: it initialises their barrier itself, ahead of the CTA-wide sync
@@ -314,14 +311,22 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       tc::fence_mbar_init();
       tc::tma_prefetch(&tm_q);
     }
-    if (!a.gcu) start_first();
+    if (G != 4 || !a.gcu) {
+      if (G == 4) issue_q(g0);
+      load_first(g0, pre_a);
+    }
   }
   // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
   // before the token and the step's inputs, and writes only its own scratch, so it runs beside the compress
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
   // a projection kernel that lets successors start only once all earlier work is complete.)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
-  if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) start_first();
+  if constexpr (G == 4) {
+    if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) {
+      issue_q(g0);
+      load_first(g0, pre_a);
+    }
+  }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::kAcc * N);
     tc::tmem_relinquish();
@@ -344,12 +349,12 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, par_last = 0;  // per stage (bit s): a load was issued; parity of its last phase
-      Items<kOverlap> itr;
+      Items<G, kOverlap> itr;
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g, t = itr.t;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1)) { failed = true; break; }
         int cnt;
-        const int krow = idx_seq(a, grp_first(a, g, cnt)) * a.cap + t * kTileRows;  // a group's queries share
+        const int krow = idx_seq(a, grp_first<G>(a, g, cnt)) * a.cap + t * kTileRows;  // a group's queries share
                                                                                    // a sequence
         tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
         tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       int cur_g = -1, k = -1, stage = 0, acc = 0;
       uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
       uint32_t phase = 0;
-      Items<kOverlap> itr;
+      Items<G, kOverlap> itr;
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g;
         if (g != cur_g) {
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     int cur_g = -1, k = -1, acc = 0;
     uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
     int nv[G], qix[G];
-    Items<kOverlap> itr;
+    Items<G, kOverlap> itr;
     for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
       const int g = itr.g, t = itr.t;
       if (g != cur_g) {
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         if (!tc::mbar_wait(&q_full[k % C::kQSlots], (k / C::kQSlots) & 1)) { failed = true; break; }
 #pragma unroll
         for (int qq = 0; qq < G; ++qq) {
-          qix[qq] = grp_query(a, g, qq);
+          qix[qq] = grp_query<G>(a, g, qq);
           nv[qq] = qix[qq] >= 0 ? scan_rows<kOverlap>(a, qix[qq]) : 0;
         }
       }
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     // every round trip); the second is prefetched into L2
     if (g1 >= 0) {
       int cnt1;
-      const int q01 = grp_first(a, g1, cnt1);
+      const int q01 = grp_first<G>(a, g1, cnt1);
       for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
         if (e / 32 < cnt1) tc::prefetch_l2(a.iq + ((size_t)q01 * 64 + e * 2) * 128, 512);
     }
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       q_pending = -1;
       return ok;
     };
-    Items<kOverlap> itr;
+    Items<G, kOverlap> itr;
     for (bool more = itr.start(a, i_begin, i_end); more; more = itr.next_group(a)) {
       const int g = itr.g;
       ++k;
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         int p = pre.p;
         float f = pre.th_freq;
         if (e != pt) {  // G = 4: the second entry of this thread
-          const int q = grp_query(a, g, e / 32);
+          const int q = grp_query<G>(a, g, e / 32);
           p = q >= 0 ? idx_qpos(a, q) : 0;
           f = __ldg(a.inv_freq + (e & 31));
         }
