@@ -42,7 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum, every kernel captured cold) of one decode
 # layer-step of the headline workload and of one prefill chunk, with the hash of the kernel sources the counters
 # were taken on (csrc_digest()); the bench reports them only while the sources still hash the same.
-TRAFFIC = {"csrc_sha256": "925e82e22b2fbf16", "decode_layer_step_bytes": 133_434_000, "prefill_chunk_bytes": 1_232_673_000,
+TRAFFIC = {"csrc_sha256": "49c6546013356468", "decode_layer_step_bytes": 116_683_000, "prefill_chunk_bytes": 1_234_840_000,
            "profile": "profiles/traffic_decode_b32_ctx32k_and_prefill_t4096.md"}
 
 
