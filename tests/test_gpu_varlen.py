@@ -128,3 +128,46 @@ def test_varlen_inconsistent_row_table_is_flagged():
     assert st.n_rows.tolist() == [(4000 + 5) // 4, host.n_rows[1].item(), (4008 + 5) // 4]
     for k in ("pool", "window", "front_attn"):
         assert torch.equal(getattr(st, k)[1].cpu(), getattr(host, k)[1]), f"flagged sequence changed {k}"
+
+
+def test_varlen_prefill_ratio128_without_indexer():
+    """The same on a ratio-128 layer (no indexer: every visible row attended): a fresh prompt whose chunk completes
+    row 0, a short chunk, and a chunk that completes row 2047 (position 262143)."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[4].replace(B=1)
+    specs = [(0, 130), (1000, 50), (262144 - 100, 300)]
+    B = len(specs)
+    cap = max(c + t for c, t in specs) // cfg.ratio + 4
+    parts = [_seq_cache(cfg, cap, b, c) for b, (c, _) in enumerate(specs)]
+    host = csa_synth.Cache(**{k: None if getattr(parts[0], k) is None else torch.cat([getattr(p, k) for p in parts])
+                              for k in vars(parts[0])})
+    chunks = [csa_synth.chunk_inputs(cfg.replace(cid=cfg.cid + 80 + b), t) for b, (_, t) in enumerate(specs)]
+    lens = [t for _, t in specs]
+    N, T_max = sum(lens), max(lens)
+    cu_host = [0] + np.cumsum(lens).tolist()
+    run = G.Runner(cfg)
+    st = G.DevCache(host)
+    cu = torch.tensor(cu_host, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(csa.workspace_size(run.L, csa.OP_COMPRESS_VARLEN, B, N, cap), dtype=torch.uint8, device="cuda")
+    csa.compress_append_varlen(run.L, run.ca, G.dev(_packed(chunks, "x")), cu, T_max, st.pos, st.front_attn,
+                               st.pool, st.n_rows, run.inv_freq, ws=ws, err=run.err)
+    width = 2 * cfg.lanes * cfg.D
+    off = (4 * B + 255) // 256 * 256
+    proj = ws[off:off + N * width * 2].view(cfg.storage).view(N, width).clone()
+    out = torch.empty(N, cfg.H, cfg.D, dtype=cfg.storage, device="cuda")
+    sel = torch.empty(N, cfg.topk, dtype=torch.int32, device="cuda")
+    csa.attend_prefill_varlen(run.L, G.dev(_packed(chunks, "q")), G.dev(_packed(chunks, "kv")), None, None,
+                              run.sink, cu, T_max, st.pos, st.window, st.pool, None, st.n_rows, run.inv_freq, out,
+                              sel_out=sel, err=run.err)
+    torch.cuda.synchronize()
+    assert run.err.item() == 0
+    for b, (ctx, T) in enumerate(specs):
+        lo_b, hi_b = cu_host[b], cu_host[b + 1]
+        run.projs = {"attn": proj[lo_b:hi_b][None].cpu()}
+        queries = range(T) if T <= 130 else sorted(set(range(0, T, 3)) | {T - 1, 98, 99, 100, 227, 228})
+        st_o, n, lo, ring, worst = G.check_prefill_chunk(cfg.replace(ctx=ctx, T=T), run, parts[b], chunks[b],
+                                                         out[lo_b:hi_b], sel[lo_b:hi_b], queries,
+                                                         label=f"varlen prefill batch, ratio 128 (B {B})")
+        assert n == st.n_rows[b].item() == (ctx + T) // cfg.ratio, f"seq {b} rows"
+        G.check_pool_rows(st.pool[b, lo:n].cpu(), st_o["pool"][0, lo:n], "bf16", f"seq {b} pool rows", R=cfg.R)
+        G.check_pool_rows(st.window[b].cpu(), ring, "bf16", f"seq {b} window after chunk")

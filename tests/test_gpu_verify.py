@@ -31,11 +31,14 @@ def _block(cfg, B, T, k):
 
 # (B, T, compress call, sequences checked against the oracle).  B 4, T 4: the paired compress's block path, the
 # indexer's 4-query MMA, the split decode attention kernel; T 5: one compress call per pool (chunk path) and the
-# 1-query MMA; B 40: 160 queries, which the pipelined attention kernel takes (one CTA per query, no partials).
+# 1-query MMA; B 40: 160 queries, which the pipelined attention kernel takes (one CTA per query, no partials);
+# T 8: two 4-query groups per sequence; B 2, T 16: 32 queries in 4 splits each, merged in-cluster.
 CASES = {
     "b4_t4_pair": (4, 4, "pair", None),
     "b4_t5_per_pool": (4, 5, "single", None),
     "b40_t4_pair": (40, 4, "pair", (0, 7, 19, 33, 39)),
+    "b8_t8_pair": (8, 8, "pair", (0, 5)),      # two 4-query groups per sequence; pipelined attention
+    "b2_t16_pair": (2, 16, "pair", None),      # the longest block the paired compress fuses; split attention
 }
 
 
