@@ -52,6 +52,17 @@ Readings where the pages are silent (each also listed with the design notes):
       window ring and attends to the most recent owner's compressed rows,
       through its own top-k over the owner's index keys (index-source layers)
       or through the owner's selection of the same step (the other layers).
+  R19 fp8 index keys (the optional key format): the pages name a Hadamard
+      rotation of the indexer's activations and an fp4 activation simulation
+      without fixing a format ([mlx-lm#1189], the indexer thread).  This build's
+      format: every index row and every index-query head (128 values, already
+      in the model dtype) is rotated by the unnormalised 128-point Walsh-Hadamard
+      transform (butterflies of spans 1, 2, .., 64 in fp32), scaled by
+      amax / 448 (fp32) and rounded to E4M3 (nearest even, saturating at 448);
+      a row keeps its 128 codes and its fp32 scale.  The score is the bf16
+      definition with the dot product taken on the decoded values and divided by
+      128 (H H^T = 128 I, so the rotation cancels).  The codes are integers
+      decided in fp32 on both sides, in the same operation order.
 """
 from __future__ import annotations
 
@@ -362,6 +373,93 @@ def index_topk(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq):
         sel[b, :len(rows)] = rows
         n_sel[b] = len(rows)
     return sel, n_sel
+
+
+# --------------------------------------------------------------------------
+# fp8 index keys (R19)
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code) -> np.ndarray:
+    """Value of E4M3 codes (OCP 8-bit floating point: sign, 4 exponent bits of bias 7, 3 mantissa bits; exponent 0
+    holds the subnormals m * 2^-9; S.1111.111 is NaN, there is no infinity)."""
+    c = np.asarray(code, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code of each (finite) value, ties to the even code, magnitudes beyond 448 saturating to 448,
+    the sign bit that of the value (-0 -> 0x80).
+    Written from the format: the representable magnitudes are m * 2^-9 (m = 0..7) and (8 + m) * 2^(e-10)
+    (e = 1..15, m = 0..7, except e = 15, m = 7); the code of a magnitude is its index in that increasing list,
+    so the nearest one, with ties to the even index, is the nearest even-mantissa one."""
+    x = np.asarray(x, dtype=np.float64)
+    mags = e4m3_decode(np.arange(0x7F))  # codes 0x00 .. 0x7E: 0 .. 448, increasing
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, len(mags) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - mags[lo], mags[hi] - a
+    pick = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = pick.astype(np.int64)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.int64)  # the sign is kept, zero's included
+
+
+def fwht_f32(v) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform of 128 values in fp32, butterflies of span 1, 2, 4, .., 64 in that
+    order, (a, b) -> (a + b, a - b) for each pair (i, i + span) with bit `span` of i clear (R19)."""
+    u = np.array(v, dtype=np.float32).copy()
+    n = u.shape[-1]
+    h = 1
+    while h < n:
+        for i in range(n):
+            if i & h == 0:
+                a, b = u[..., i].copy(), u[..., i + h].copy()
+                u[..., i] = a + b
+                u[..., i + h] = a - b
+        h *= 2
+    return u
+
+
+def quantize_fp8_row(v):
+    """(codes [128], scale) of one index row or index-query head already in the model dtype (R19): fp32 rotation,
+    scale = amax / 448 (fp32), codes = E4M3(u / scale); an all-zero row has scale 0 and zero codes."""
+    u = fwht_f32(v)
+    amax = np.float32(np.max(np.abs(u)))
+    if amax == 0:
+        return np.zeros(u.shape[-1], dtype=np.int64), np.float32(0.0)
+    scale = np.float32(amax / np.float32(E4M3_MAX))
+    return e4m3_encode((u / scale).astype(np.float32)), scale
+
+
+def fp8_key_values(codes, scale) -> np.ndarray:
+    """Rotated, quantised key row as float64: decoded codes times the row's scale."""
+    return e4m3_decode(codes) * np.float64(scale)
+
+
+def index_scores_fp8(layer: Layer, q_codes, q_scales, iw, key_codes, key_scales) -> np.ndarray:
+    """score_j = sum_h w_h ReLU(s_q[h] s_k[j] (qc_h . kc_j) / 128), the bf16 definition on the rotated,
+    quantised operands (R19).  q_codes [Hi, 128], q_scales [Hi]; key_codes [n, 128], key_scales [n]."""
+    w = np.asarray(iw, dtype=np.float64) * (layer.Di ** -0.5) * (layer.Hi ** -0.5)
+    qv = e4m3_decode(q_codes)
+    kv = e4m3_decode(key_codes)
+    dots = (qv @ kv.T) * np.asarray(q_scales, dtype=np.float64)[:, None] * np.asarray(key_scales,
+                                                                                     dtype=np.float64)[None, :]
+    return (w[:, None] * np.maximum(dots / 128.0, 0.0)).sum(axis=0)
+
+
+def quantize_fp8_query(layer: Layer, iq, p, inv_freq):
+    """(codes [Hi, 128], scales [Hi]) of the index query at position p: RoPE as for the bf16 scores, the model
+    dtype, then quantize_fp8_row per head."""
+    q = store(rope(iq, p, inv_freq), layer.dtype)
+    out = [quantize_fp8_row(q[h]) for h in range(q.shape[0])]
+    return np.stack([c for c, _ in out]), np.array([s for _, s in out], dtype=np.float32)
 
 
 # --------------------------------------------------------------------------

@@ -368,7 +368,49 @@ def m_round_bf16_truncate(x):
     return np.ldexp(np.trunc(np.ldexp(x, 8 - e)), e - 8)
 
 
+def m_e4m3_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    mags = O.e4m3_decode(np.arange(0x7F))
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, len(mags) - 1)
+    lo = np.maximum(hi - 1, 0)
+    code = np.where(a - mags[lo] < mags[hi] - a, lo, hi).astype(np.int64)
+    return np.where(np.signbit(x), code | 0x80, code)
+
+
+def m_fwht_sign_flipped(v):
+    u = np.array(v, dtype=np.float32).copy()
+    h = 1
+    while h < u.shape[-1]:
+        for i in range(u.shape[-1]):
+            if i & h == 0:
+                a, b = u[..., i].copy(), u[..., i + h].copy()
+                u[..., i], u[..., i + h] = a + b, b - a
+        h *= 2
+    return u
+
+
+def m_fp8_scale_240(v):
+    u = O.fwht_f32(v)
+    amax = np.float32(np.max(np.abs(u)))
+    if amax == 0:
+        return np.zeros(u.shape[-1], dtype=np.int64), np.float32(0.0)
+    scale = np.float32(amax / np.float32(240.0))
+    return O.e4m3_encode((u / scale).astype(np.float32)), scale
+
+
+def m_fp8_scores_no_1_over_128(layer, q_codes, q_scales, iw, key_codes, key_scales):
+    w = np.asarray(iw, dtype=np.float64) * (layer.Di ** -0.5) * (layer.Hi ** -0.5)
+    dots = (O.e4m3_decode(q_codes) @ O.e4m3_decode(key_codes).T) * np.asarray(q_scales)[:, None] * \
+        np.asarray(key_scales)[None, :]
+    return (w[:, None] * np.maximum(dots, 0.0)).sum(axis=0)
+
+
 MUTATIONS = {
+    "e4m3 ties away from zero": ("e4m3_encode", m_e4m3_ties_away),
+    "hadamard butterfly sign flipped": ("fwht_f32", m_fwht_sign_flipped),
+    "fp8 scale amax / 240": ("quantize_fp8_row", m_fp8_scale_240),
+    "fp8 scores without the 1/128": ("index_scores_fp8", m_fp8_scores_no_1_over_128),
     "window keeps W+1 tokens": ("window_tokens", m_window_keep_one_more),
     "window keeps W-1 tokens": ("window_tokens", m_window_keep_one_less),
     "window excludes the query's own token": ("window_tokens", m_window_excludes_self),

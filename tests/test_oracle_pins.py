@@ -640,3 +640,95 @@ def test_consumer_layer_reads_the_owner_caches():
     severed = dict(owner, pool=np.zeros_like(owner["pool"]))
     out_s, _, _, _, _ = O.consumer_decode_step(layer, severed, own_win, own, sink, invf)
     assert rel_err_rows(out_s, out_c) > 0.05
+
+
+# ---------------------------------------------------------------- fp8 index keys (R19)
+
+def test_e4m3_format_values():
+    """E4M3 as the OCP 8-bit floating-point format defines it: bias 7, 3 mantissa bits, subnormals m * 2^-9,
+    S.1111.111 the only NaN encodings, largest finite magnitude 448 = 1.75 * 2^8."""
+    v = O.e4m3_decode(np.arange(256))
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9 and v[0x08] == 2.0 ** -6
+    assert v[0x38] == 1.0 and v[0x39] == 1.125 and v[0xB8] == -1.0 and v[0x58] == 16.0
+    assert set(np.nonzero(np.isnan(v))[0].tolist()) == {0x7F, 0xFF}
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)  # codes 0 .. 0x7E increase strictly
+
+
+def test_e4m3_rounding_ties_to_even_and_saturation():
+    """Every finite code round-trips; midpoints go to the even code; magnitudes past 448 saturate."""
+    c = np.arange(256)
+    v = O.e4m3_decode(c)
+    fin = ~np.isnan(v)
+    assert np.array_equal(O.e4m3_encode(v[fin]), c[fin])
+    mids = [(2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (1.0625, 0x38), (1.1875, 0x3A), (17.0, 0x58),
+            (-1.0625, 0xB8), (432.0, 0x7E), (2.0 ** -6 + 2.0 ** -10, 0x08)]
+    for x, want in mids:
+        assert O.e4m3_encode([x])[0] == want, x
+    # on either side of the midpoint 1.0625 between 1.0 (0x38) and 1.125 (0x39)
+    assert O.e4m3_encode([1.06])[0] == 0x38 and O.e4m3_encode([1.07])[0] == 0x39
+    assert O.e4m3_encode([449.0, 1e6, -1e6]).tolist() == [0x7E, 0x7E, 0xFE]
+
+
+def test_fwht_is_the_hadamard_transform():
+    """The fp32 butterflies equal the Sylvester Hadamard matrix (built independently by scipy) up to fp32 rounding,
+    transform a one-hot into a row of (-1)^popcount(i & k), and applied twice give 128 x exactly on small integers."""
+    import scipy.linalg
+    H = scipy.linalg.hadamard(128).astype(np.float64)
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal(128).astype(np.float32)
+    assert np.max(np.abs(O.fwht_f32(x) - H @ x.astype(np.float64))) < 64 * 2.0 ** -23 * np.abs(x).sum()
+    k = 37
+    sign = np.array([(-1) ** bin(i & k).count("1") for i in range(128)], dtype=np.float64)
+    assert np.array_equal(O.fwht_f32(np.eye(128, dtype=np.float32)[k]), sign)
+    xi = rng.integers(-8, 9, 128).astype(np.float32)
+    assert np.array_equal(O.fwht_f32(O.fwht_f32(xi)), 128 * xi)
+
+
+def test_fp8_row_quantization():
+    """The largest rotated element maps to +-448; every decoded element is within half an E4M3 step of the rotated
+    value (scaled); a zero row keeps scale 0 and zero codes."""
+    rng = np.random.default_rng(7)
+    v = O.store(rng.standard_normal(128), "bf16")
+    codes, scale = O.quantize_fp8_row(v)
+    u = H_apply(v)
+    assert np.max(np.abs(O.e4m3_decode(codes))) == 448.0
+    y = u / np.float64(scale)
+    step = np.where(np.abs(y) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 1e-30))) - 3))
+    assert np.all(np.abs(O.e4m3_decode(codes) - y) <= 0.5 * step + 1e-12 * np.abs(y))
+    c0, s0 = O.quantize_fp8_row(np.zeros(128))
+    assert s0 == 0 and not np.any(c0)
+
+
+def H_apply(v):
+    import scipy.linalg
+    return scipy.linalg.hadamard(128).astype(np.float64) @ np.asarray(v, dtype=np.float64)
+
+
+def test_fp8_scores_equal_the_exact_definition_on_representable_operands():
+    """When the rotated query heads and key rows lie on the E4M3 grid with their largest element at 448 times a
+    power-of-two scale, quantisation loses nothing and the fp8 score equals sum_h w_h ReLU(q_h . k_j) exactly
+    (the rotation cancels: H H^T = 128 I)."""
+    layer = O.Layer(dtype="bf16", H=4, D=16, R=8, W=8, ratio=4, Hi=3, Di=128, topk=2, X=24)
+    rng = np.random.default_rng(23)
+    grid = O.e4m3_decode(np.arange(0x7F))
+
+    def representable(scale):
+        u = rng.choice(grid, 128) * rng.choice([-1.0, 1.0], 128)
+        u[rng.integers(128)] = 448.0
+        return u * scale
+
+    q_rot = np.stack([representable(2.0 ** -6) for _ in range(layer.Hi)])
+    k_rot = np.stack([representable(2.0 ** -7) for _ in range(5)])
+    q = np.stack([O.fwht_f32(r.astype(np.float32)) for r in q_rot]).astype(np.float64) / 128
+    k = np.stack([O.fwht_f32(r.astype(np.float32)) for r in k_rot]).astype(np.float64) / 128
+    qc = [O.quantize_fp8_row(r) for r in q]
+    kc = [O.quantize_fp8_row(r) for r in k]
+    assert all(s == 2.0 ** -6 for _, s in qc) and all(s == 2.0 ** -7 for _, s in kc)
+    iw = rng.standard_normal(layer.Hi)
+    got = O.index_scores_fp8(layer, np.stack([c for c, _ in qc]), np.array([s for _, s in qc]), iw,
+                             np.stack([c for c, _ in kc]), np.array([s for _, s in kc]))
+    w = iw * layer.Di ** -0.5 * layer.Hi ** -0.5
+    want = (w[:, None] * np.maximum(q @ k.T, 0.0)).sum(axis=0)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
