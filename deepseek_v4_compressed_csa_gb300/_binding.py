@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libcsa.so")
 CSA_F32, CSA_BF16 = 0, 1
 OP_COMPRESS, OP_INDEX_TOPK, OP_ATTEND_DECODE, OP_ATTEND_PREFILL, OP_COMPRESS_PAIR = 0, 1, 2, 3, 4
 OP_COMPRESS_VARLEN, OP_ATTEND_PREFILL_VARLEN = 5, 6
+FP8_ROW_BYTES = 144  # CSA_FP8_ROW_BYTES: 128 E4M3 codes, the fp32 scale, 12 zero bytes
 DEV_CAPACITY, DEV_STATE, DEV_RANGE, DEV_ROLLBACK = 1, 2, 4, 8
 CSA_OK, CSA_ERR_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA", 4: "CSA_ERR_WORKSPACE"}
@@ -42,7 +43,7 @@ class _Layer(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int), ("R", ctypes.c_int),
                 ("W", ctypes.c_int), ("ratio", ctypes.c_int), ("Hi", ctypes.c_int), ("Di", ctypes.c_int),
                 ("topk", ctypes.c_int), ("X", ctypes.c_int), ("scale", ctypes.c_float),
-                ("rms_eps", ctypes.c_float), ("rollback", ctypes.c_int)]
+                ("rms_eps", ctypes.c_float), ("rollback", ctypes.c_int), ("index_fp8", ctypes.c_int)]
 
 
 class _Comp(ctypes.Structure):
@@ -109,7 +110,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 @dataclass(frozen=True)
 class Layer:
     """Mirror of csa_layer.  dtype: torch.bfloat16 or torch.float32 (model dtype).  rollback: tokens csa_trim may
-    rewind; the window ring then has W + rollback slots and each frontier ring frontier_slots(ratio) + rollback."""
+    rewind; the window ring then has W + rollback slots and each frontier ring frontier_slots(ratio) + rollback.
+    index_fp8: the index pool holds fp8 rows, a uint8 tensor [B, cap, FP8_ROW_BYTES]."""
 
     dtype: torch.dtype
     H: int
@@ -124,6 +126,7 @@ class Layer:
     scale: float = 0.0
     rms_eps: float = 1e-6
     rollback: int = 0
+    index_fp8: bool = False
 
     @property
     def ring_slots(self) -> int:
@@ -140,7 +143,13 @@ class Layer:
     def _c(self) -> _Layer:
         code = CSA_BF16 if self.dtype == torch.bfloat16 else CSA_F32
         return _Layer(code, self.H, self.D, self.R, self.W, self.ratio, self.Hi, self.Di, self.topk, self.X,
-                      float(self.scale), float(self.rms_eps), int(self.rollback))
+                      float(self.scale), float(self.rms_eps), int(self.rollback), int(self.index_fp8))
+
+    def pool_spec(self, d: int):
+        """(dtype, row length) of a pool with rows of d values: fp8 index rows are FP8_ROW_BYTES bytes."""
+        if self.index_fp8 and d == self.Di:
+            return torch.uint8, FP8_ROW_BYTES
+        return self.dtype, d
 
 
 @dataclass
@@ -184,6 +193,16 @@ def _expect_comp(layer: "Layer", comp: "Compressor", which: str):
     _expect(f"{which}.wgate", comp.wgate, layer.dtype, (L * d, layer.X))
     _expect(f"{which}.ape", comp.ape, torch.float32, (layer.ratio, L * d))
     _expect(f"{which}.norm_w", comp.norm_w, torch.float32, (d,))
+
+
+def _expect_pool(name: str, layer: "Layer", pool, d: int, B=None, dims: int = 3):
+    """pool [B, cap, row] (dims 3) or [cap, row] (dims 2) in the layer's pool format for rows of d values."""
+    dt, row = layer.pool_spec(d)
+    _expect(name, pool, dt)
+    lead = () if B is None or dims == 2 else (B,)
+    if pool.dim() != dims or pool.shape[-1] != row or tuple(pool.shape[:len(lead)]) != lead:
+        want = "[cap, %d]" % row if dims == 2 else "[%s, cap, %d]" % ("B" if B is None else B, row)
+        raise ValueError(f"{name}: shape {tuple(pool.shape)}, expected {want}")
 
 
 def _frontier_len(layer: "Layer") -> int:
@@ -267,9 +286,7 @@ def compress_append(layer: Layer, comp: Compressor, x, pos, frontier, pool, n_ro
         raise ValueError(f"x: shape {tuple(x.shape)}, expected [B, T, {layer.X}]")
     B, T = x.shape[0], x.shape[1]
     _expect_comp(layer, comp, "comp")
-    _expect("pool", pool, layer.dtype)
-    if pool.dim() != 3 or pool.shape[0] != B or pool.shape[2] != comp.d:
-        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [{B}, cap, {comp.d}]")
+    _expect_pool("pool", layer, pool, comp.d, B)
     cap = pool.shape[1]
     _expect("pos", pos, torch.int32, (B,))
     _expect("frontier", frontier, layer.dtype, (B, _frontier_len(layer), 2 * layer.lanes * comp.d))
@@ -297,9 +314,7 @@ def compress_append_pair(layer: Layer, comp_a: Compressor, comp_i: Compressor, x
     F = _frontier_len(layer)
     for nm, pl, fr, nr, d in (("a", pool_a, frontier_a, n_rows_a, comp_a.d), ("i", pool_i, frontier_i, n_rows_i,
                                                                                comp_i.d)):
-        _expect(f"pool_{nm}", pl, layer.dtype)
-        if pl.dim() != 3 or pl.shape[0] != B or pl.shape[2] != d:
-            raise ValueError(f"pool_{nm}: shape {tuple(pl.shape)}, expected [{B}, cap, {d}]")
+        _expect_pool(f"pool_{nm}", layer, pl, d, B)
         _expect(f"frontier_{nm}", fr, layer.dtype, (B, F, 2 * layer.lanes * d))
         _expect(f"n_rows_{nm}", nr, torch.int32, (B,))
     _expect("pos", pos, torch.int32, (B,))
@@ -322,9 +337,7 @@ def _expect_index(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n_sel
         raise ValueError(f"iq: shape {tuple(iq.shape)}, expected [B, {layer.Hi}, {layer.Di}]")
     B = iq.shape[0]
     _expect("iw", iw, layer.dtype, (B, layer.Hi))
-    _expect("ikeys", ikeys, layer.dtype)
-    if ikeys.dim() != 3 or ikeys.shape[0] != B or ikeys.shape[2] != layer.Di:
-        raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [{B}, cap, {layer.Di}]")
+    _expect_pool("ikeys", layer, ikeys, layer.Di, B)
     _expect("n_rows", n_rows, torch.int32, (B,))
     _expect("pos", pos, torch.int32, (B,))
     _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))
@@ -416,9 +429,7 @@ def attend_prefill_chunk(layer: Layer, q, kv_new, iq, iw, sink, pos0: int, windo
     if layer.has_indexer:
         _expect("iq", iq, layer.dtype, (T, layer.Hi, layer.Di))
         _expect("iw", iw, layer.dtype, (T, layer.Hi))
-        _expect("ikeys", ikeys, layer.dtype)
-        if ikeys.dim() != 2 or ikeys.shape[1] != layer.Di:
-            raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [cap, {layer.Di}]")
+        _expect_pool("ikeys", layer, ikeys, layer.Di, dims=2)
     _expect("sink", sink, torch.float32, (layer.H,))
     _expect("window", window, layer.dtype, (layer.ring_slots, layer.D))
     _expect("pool", pool, layer.dtype)
@@ -454,9 +465,7 @@ def compress_append_varlen(layer: Layer, comp: Compressor, x, cu_seqlens, T_max:
     if x.dim() != 2 or x.shape[1] != layer.X:
         raise ValueError(f"x: shape {tuple(x.shape)}, expected [N, {layer.X}]")
     N = x.shape[0]
-    _expect("pool", pool, layer.dtype)
-    if pool.dim() != 3 or pool.shape[2] != comp.d:
-        raise ValueError(f"pool: shape {tuple(pool.shape)}, expected [B, cap, {comp.d}]")
+    _expect_pool("pool", layer, pool, comp.d)
     B, cap = pool.shape[0], pool.shape[1]
     _expect_varlen(cu_seqlens, B, N, T_max)
     _expect_comp(layer, comp, "comp")
@@ -492,7 +501,9 @@ def attend_prefill_varlen(layer: Layer, q, kv_new, iq, iw, sink, cu_seqlens, T_m
     if layer.has_indexer:
         _expect("iq", iq, layer.dtype, (N, layer.Hi, layer.Di))
         _expect("iw", iw, layer.dtype, (N, layer.Hi))
-        _expect("ikeys", ikeys, layer.dtype, (B, cap, layer.Di))
+        _expect_pool("ikeys", layer, ikeys, layer.Di, B)
+        if ikeys.shape[1] != cap:
+            raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [{B}, {cap}, {layer.pool_spec(layer.Di)[1]}]")
     _expect("sink", sink, torch.float32, (layer.H,))
     _expect("pos", pos, torch.int32, (B,))
     _expect("window", window, layer.dtype, (B, layer.ring_slots, layer.D))
@@ -520,9 +531,7 @@ def index_topk_verify(layer: Layer, iq, iw, ikeys, n_rows, pos, inv_freq, sel, n
         raise ValueError(f"iq: shape {tuple(iq.shape)}, expected [B, T, {layer.Hi}, {layer.Di}]")
     B, T = iq.shape[0], iq.shape[1]
     _expect("iw", iw, layer.dtype, (B, T, layer.Hi))
-    _expect("ikeys", ikeys, layer.dtype)
-    if ikeys.dim() != 3 or ikeys.shape[0] != B or ikeys.shape[2] != layer.Di:
-        raise ValueError(f"ikeys: shape {tuple(ikeys.shape)}, expected [{B}, cap, {layer.Di}]")
+    _expect_pool("ikeys", layer, ikeys, layer.Di, B)
     _expect("n_rows", n_rows, torch.int32, (B,))
     _expect("pos", pos, torch.int32, (B,))
     _expect("inv_freq", inv_freq, torch.float32, (layer.R // 2,))

@@ -30,6 +30,10 @@ csa_status make_dims(const csa_layer* l, Dims* d) {
   }
   if (!(l->rms_eps >= 0.f) || !(l->scale >= 0.f)) return CSA_ERR_ARG;
   if (l->rollback < 0 || l->rollback > (1 << 20)) return CSA_ERR_ARG;
+  if (l->index_fp8 != 0 && l->index_fp8 != 1) return CSA_ERR_ARG;
+  // (the index pool is told apart from the attention pool by its row length)
+  if (l->index_fp8 && (l->ratio != 4 || l->dtype != CSA_BF16 || l->Hi != 64 || l->Di != 128 || l->D == l->Di))
+    return CSA_ERR_UNSUPPORTED;
   d->dtype = l->dtype;
   d->H = l->H; d->D = l->D; d->R = l->R; d->W = l->W; d->ratio = l->ratio;
   d->Hi = l->Hi; d->Di = l->Di; d->topk = l->topk; d->X = l->X;
@@ -39,6 +43,7 @@ csa_status make_dims(const csa_layer* l, Dims* d) {
   d->rollback = l->rollback;
   d->Wr = l->W + l->rollback;
   d->F = csa_frontier_slots(l->ratio) + l->rollback;
+  d->ikey_fp8 = l->index_fp8;
   return CSA_OK;
 }
 
@@ -227,7 +232,7 @@ csa_status csa_index_topk_overlapped(const csa_layer* layer, const void* iq, con
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
-  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
+  if (!L.has_indexer() || L.ikey_fp8) return CSA_ERR_UNSUPPORTED;
   if (B < 1 || cap < 1) return CSA_ERR_ARG;
   if (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
   if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(sel) || !dev_i32(n_sel) || !dev_i32(err)) return CSA_ERR_ARG;
@@ -270,6 +275,7 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
+  if (L.ikey_fp8) return CSA_ERR_UNSUPPORTED;  // fp8 index rows are scored for decode queries only
   if (T < 1 || T > 16384 || pos0 < 0 || cap < 1) return CSA_ERR_ARG;
   if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
       !dev_tensor(inv_freq) || !dev_tensor(out))
@@ -333,7 +339,8 @@ csa_status csa_attend_prefill_varlen(const csa_layer* layer, const void* q, cons
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
   if (!varlen_args_ok(B, cu_seqlens, N, T_max) || N > 16384 || cap < 1) return CSA_ERR_ARG;
-  if (!tc_attend_supported(L) || (L.has_indexer() && !tc_index_supported(L))) return CSA_ERR_UNSUPPORTED;
+  if (!tc_attend_supported(L) || (L.has_indexer() && !tc_index_supported(L)) || L.ikey_fp8)
+    return CSA_ERR_UNSUPPORTED;
   if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
       !dev_tensor(inv_freq) || !dev_tensor(out))
     return CSA_ERR_ARG;
@@ -368,7 +375,7 @@ csa_status csa_index_topk_verify(const csa_layer* layer, const void* iq, const v
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
-  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
+  if (!L.has_indexer() || L.ikey_fp8) return CSA_ERR_UNSUPPORTED;
   if (B < 1 || T < 1 || T > 64 || cap < 1 || (long long)B * T > (1 << 20)) return CSA_ERR_ARG;
   if (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
   if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(sel) || !dev_i32(n_sel) || !dev_i32(err)) return CSA_ERR_ARG;

@@ -17,6 +17,7 @@
 //   finish     (chunks) rewrite the frontier ring with the newest tokens,
 //              advance n_rows
 #include "common.cuh"
+#include "fp8_row.cuh"
 #include "kernels.h"
 
 namespace csa {
@@ -77,6 +78,20 @@ __global__ void __launch_bounds__(256) k_project_simt(const T* __restrict__ x, c
   }
 }
 
+// An index row of 128 values in shared memory (model dtype) -> its fp8 row at dst, written by warp 0 once every
+// thread of the block has stored its values (all threads call this).
+__device__ __forceinline__ void store_fp8_row(uint8_t* dst, const float* row) {
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const float4 v = *reinterpret_cast<const float4*>(row + 4 * lane);
+    float u[4] = {v.x, v.y, v.z, v.w};
+    float scale;
+    const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
+    fp8_row_store(dst, lane, packed, scale);
+  }
+}
+
 // One block per (completed window i of this call, sequence b).
 // Per-sequence state check of a compress call: n_rows == pos/ratio and every
 // row the call emits fits the pool.  Returns the error bit (0 = valid).
@@ -99,7 +114,7 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
                                                    float eps, const float* __restrict__ inv_freq,
                                                    T* __restrict__ pool, int cap, const float* __restrict__ part,
                                                    int splits, int part_stride, const int32_t* __restrict__ cu,
-                                                   int N) {
+                                                   int N, int fp8) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm_pool[];  // [d] pooled, [d] normed, 32 reduction slots, [2*L*d] new token (part)
@@ -243,8 +258,12 @@ __global__ void __launch_bounds__(256) k_pool_emit(int32_t* __restrict__ flags, 
       const float a = y[d - R + 2 * i], bb = y[d - R + 2 * i + 1];
       v = ((c - (d - R)) & 1) ? fmaf(a, sn, bb * cs) : fmaf(a, cs, -bb * sn);
     }
-    dst[c] = from_f<T>(v);
+    if (fp8)
+      u[c] = rnd<T>(v);  // the row in the model dtype, then rotated and quantised below
+    else
+      dst[c] = from_f<T>(v);
   }
+  if (fp8) store_fp8_row(reinterpret_cast<uint8_t*>(pool) + ((size_t)b * cap + j) * kFp8RowBytes, u);
   if (fuse_finish && blockIdx.x == 0 && threadIdx.x == 0) n_rows[b] = (p0 + T_) / ratio;
 }
 
@@ -270,6 +289,7 @@ struct TokPool {
   T* pool;
   const float* part;
   int d, cap, splits, part_stride;
+  int fp8;  // the pool holds fp8 index rows (kFp8RowBytes each, pool then points at bytes)
 };
 
 // Blocks [0, B) serve pool pa, blocks [B, 2B) (when launched) pool pb: a ratio-4 layer's two pools of the same
@@ -290,6 +310,7 @@ __global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, 
   const float* __restrict__ part = second ? pb.part : pa.part;
   const int d = second ? pb.d : pa.d, cap = second ? pb.cap : pa.cap;
   const int splits = second ? pb.splits : pa.splits, part_stride = second ? pb.part_stride : pa.part_stride;
+  const int fp8 = second ? pb.fp8 : pa.fp8;
   constexpr int ratio = 4, lanes = 2, kEnt = ratio * lanes;
   extern __shared__ float sm_tok[];  // [2*L*d] the new token, [d] pooled, [d] normed, 32 reduction slots, [R] rope
   const int Ld = lanes * d, rowlen = 2 * Ld;
@@ -438,8 +459,12 @@ __global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, 
       const float a = y[d - R + 2 * i], bb = y[d - R + 2 * i + 1];
       v = ((c - (d - R)) & 1) ? fmaf(a, rs[i], bb * rc[i]) : fmaf(a, rc[i], -bb * rs[i]);
     }
-    dst[c] = from_f<T>(v);
+    if (fp8)
+      u[c] = rnd<T>(v);  // the row in the model dtype, then rotated and quantised below
+    else
+      dst[c] = from_f<T>(v);
   }
+  if (fp8) store_fp8_row(reinterpret_cast<uint8_t*>(pool) + ((size_t)b * cap + j) * kFp8RowBytes, u);
   if (tid == 0) n_rows[b] = (p0 + 1) / ratio;
 }
 
@@ -627,6 +652,7 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
                               const int32_t* pos, void* frontier, void* pool, int cap, int32_t* n_rows,
                               const float* inv_freq, const CompressWs& ws, int32_t* err, cudaStream_t s) {
   const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
+  const int fp8 = L.ikey_fp8 && d == L.Di;  // the index pool of a layer with fp8 index rows
   const int ntok = B * T_;
   const int fuse = (T_ == 1);
   // single new token per sequence with split-K partials: the pooling kernel sums them (no fix-up pass)
@@ -651,7 +677,7 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   if (part && L.ratio == 4 && L.lanes == 2 && L.F >= 8 && d <= 256 * kTokChans) {
     const size_t smem = ((size_t)rowlen + 2 * (size_t)d + 32 + L.R) * sizeof(float);
     const TokPool<T> tp{ws.flags, n_rows, static_cast<T*>(frontier), comp.ape, comp.norm_w, static_cast<T*>(pool),
-                        part, d, cap, splits, part_stride};
+                        part, d, cap, splits, part_stride, fp8};
     CSA_LAUNCH(k_pool_emit_token<T>, dim3(B), dim3(kTokThreads), smem, s, tp, tp, B, pos, err, L.R, L.F, L.eps,
                inv_freq);
     return cudaGetLastError();
@@ -662,7 +688,7 @@ static cudaError_t compress_t(const Dims& L, const csa_compressor& comp, const v
   CSA_LAUNCH(k_pool_emit<T>, dim3(ge), dim3(256), smem, s, ws.flags, pos, n_rows, err, fuse, T_, L.ratio, L.lanes, d,
              L.R, L.F, static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape, comp.norm_w, L.eps,
              inv_freq, static_cast<T*>(pool), cap, part, splits, part_stride, static_cast<const int32_t*>(nullptr),
-             0);
+             0, fp8);
   if (!fuse) {
     dim3 gf(min(T_, L.F), B);
     CSA_LAUNCH(k_compress_finish<T>, dim3(gf), dim3(128), 0, s, ws.flags, pos, T_, L.ratio, L.F, rowlen,
@@ -680,6 +706,7 @@ static cudaError_t compress_varlen_t(const Dims& L, const csa_compressor& comp, 
                                      void* pool, int cap, int32_t* n_rows, const float* inv_freq,
                                      const CompressWs& ws, int32_t* err, cudaStream_t s) {
   const int d = comp.d, Ld = L.lanes * d, rowlen = 2 * Ld;
+  const int fp8 = L.ikey_fp8 && d == L.Di;
   if (tc_project_supported(L, d)) {
     cudaError_t e = launch_tc_project(L, d, x, N, comp.wkv, comp.wgate, ws.proj, ws.part, ws.tickets, true, err, s);
     if (e != cudaSuccess) return e;
@@ -694,7 +721,7 @@ static cudaError_t compress_varlen_t(const Dims& L, const csa_compressor& comp, 
   const size_t smem = (2 * (size_t)d + 32) * sizeof(float);
   CSA_LAUNCH(k_pool_emit<T>, dim3(maxwin, B), dim3(256), smem, s, ws.flags, pos, n_rows, err, 0, 0, L.ratio, L.lanes,
              d, L.R, L.F, static_cast<T*>(frontier), static_cast<const T*>(ws.proj), comp.ape, comp.norm_w, L.eps,
-             inv_freq, static_cast<T*>(pool), cap, static_cast<const float*>(nullptr), 1, 0, cu, N);
+             inv_freq, static_cast<T*>(pool), cap, static_cast<const float*>(nullptr), 1, 0, cu, N, fp8);
   CSA_LAUNCH(k_compress_finish<T>, dim3(max(1, min(T_max, L.F)), B), dim3(128), 0, s, ws.flags, pos, 0, L.ratio, L.F,
              rowlen, static_cast<const T*>(ws.proj), static_cast<T*>(frontier), n_rows, cu);
   return cudaGetLastError();
@@ -723,9 +750,9 @@ static cudaError_t compress_pair_token(const Dims& L, const csa_compressor& ca, 
                                          sa, si, err, s);
   if (e != cudaSuccess) return e;
   const TokPool<T> ta{wa.flags, na, static_cast<T*>(fa), ca.ape, ca.norm_w, static_cast<T*>(pa), wa.part, ca.d,
-                      cap_a, sa, tc_project_cols(L, ca.d, B)};
+                      cap_a, sa, tc_project_cols(L, ca.d, B), 0};
   const TokPool<T> tb{wi.flags, ni, static_cast<T*>(fi), ci.ape, ci.norm_w, static_cast<T*>(pi), wi.part, ci.d,
-                      cap_i, si, tc_project_cols(L, ci.d, B)};
+                      cap_i, si, tc_project_cols(L, ci.d, B), L.ikey_fp8};
   const int dm = max(ca.d, ci.d);
   const size_t smem = ((size_t)2 * L.lanes * dm + 2 * (size_t)dm + 32 + L.R) * sizeof(float);
   CSA_LAUNCH(k_pool_emit_token<T>, dim3(2 * B), dim3(kTokThreads), smem, s, ta, tb, B, pos, err, L.R, L.F, L.eps,
@@ -746,9 +773,9 @@ static cudaError_t compress_pair_block(const Dims& L, const csa_compressor& ca, 
                                          sa, si, err, s);
   if (e != cudaSuccess) return e;
   const TokPool<T> ta{wa.flags, na, static_cast<T*>(fa), ca.ape, ca.norm_w, static_cast<T*>(pa), wa.part, ca.d,
-                      cap_a, sa, tc_project_cols(L, ca.d, ntok)};
+                      cap_a, sa, tc_project_cols(L, ca.d, ntok), 0};
   const TokPool<T> tb{wi.flags, ni, static_cast<T*>(fi), ci.ape, ci.norm_w, static_cast<T*>(pi), wi.part, ci.d,
-                      cap_i, si, tc_project_cols(L, ci.d, ntok)};
+                      cap_i, si, tc_project_cols(L, ci.d, ntok), 0};
   const int dm = max(ca.d, ci.d), stride = 2 * L.lanes * dm;
   const size_t smem = (size_t)(kBlockOld + T_) * stride * sizeof(T) + (2 * (size_t)dm + 32) * sizeof(float);
   cudaFuncSetAttribute(k_pool_block<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -768,7 +795,7 @@ cudaError_t launch_compress_pair(const Dims& L, const csa_compressor& ca, const 
   if (fused && T == 1)
     return compress_pair_token(L, ca, ci, x, B, pos, fa, pa, cap_a, na, fi, pi, cap_i, ni, inv_freq, wa, wi, err, s,
                                sa, si);
-  if (fused)
+  if (fused && !L.ikey_fp8)  // the block kernel writes model-dtype rows only
     return compress_pair_block(L, ca, ci, x, B, T, pos, fa, pa, cap_a, na, fi, pi, cap_i, ni, inv_freq, wa, wi, err,
                                s, sa, si);
   cudaError_t e = launch_compress(L, ca, x, B, T, pos, fa, pa, cap_a, na, inv_freq, wa, err, s);

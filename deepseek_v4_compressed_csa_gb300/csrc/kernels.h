@@ -17,6 +17,7 @@ struct Dims {
   int rollback;  // tokens csa_trim may rewind
   int Wr;        // window ring slots: W + rollback (a query attends its last W tokens)
   int F;         // frontier ring slots: 2 ratio (ratio 4) or ratio, + rollback (the journal)
+  int ikey_fp8;  // index keys as fp8 rows (CSA_FP8_ROW_BYTES each: 128 E4M3 codes of the rotated row, fp32 scale)
   bool has_indexer() const { return ratio == 4; }
 };
 
@@ -160,7 +161,7 @@ size_t tc_index_ws(const Dims& L, int Q);
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s,
-                                   bool overlap = false, const int32_t* cu = nullptr);
+                                   bool overlap = false, const int32_t* cu = nullptr, bool fp8 = false);
 
 // ---- tc_attend.cu (tensor-core attention; bf16, H = 64, D = 512, R = 64)
 bool tc_attend_supported(const Dims& L);

@@ -24,7 +24,9 @@
 // place: a CTA of a verify block's scan enters a new group every ~14 tiles, and
 // copying the block through registers took eight dependent load rounds each
 // time, with the one query slot (and so the tensor pipe) waiting.
+
 #include "common.cuh"
+#include "fp8_row.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -33,15 +35,18 @@ namespace csa {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kTileBytes = kTileRows * 128 * 2;  // 128 rows x 128 bf16
 constexpr int kPrepThreads = 64;                 // the last two warps
 
-template <int G>
+// kFp8: index keys and queries as E4M3 codes (a row of 128 bytes in shared memory, one 128-byte swizzle box)
+template <int G, bool kFp8 = false>
 struct IdxCfg {
   static constexpr int N = 64 * G;               // MMA N: 64 heads x G queries
-  static constexpr int kQBytes = N * 128 * 2;    // one query block: 2 boxes of N rows x 128 B
+  static constexpr int kRowBytes = kFp8 ? 128 : 256;           // a key row or a query head row in shared memory
+  static constexpr int kTileBytes = kTileRows * kRowBytes;     // a key tile: 32 KB (bf16), 16 KB (e4m3)
+  static constexpr int kQBytes = N * kRowBytes;  // one query block (bf16: 2 boxes of N rows x 128 B)
   static constexpr int kQSlots = G == 1 ? 2 : 1;
-  static constexpr int kStages = G == 1 ? 5 : 4;  // decode: five 32 KB key tiles in flight (measured best of 4-6)
+  // decode: five 32 KB key tiles in flight (measured best of 4-6); fp8: the same bytes in eight 16 KB tiles
+  static constexpr int kStages = G == 1 ? (kFp8 ? 8 : 5) : 4;
   static constexpr int kAcc = G == 1 ? 4 : 2;    // TMEM accumulators of N columns
   static constexpr int kOffK = kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights
@@ -78,6 +83,11 @@ struct IdxArgs {
   // selection stage
   __nv_bfloat16* qr_out;  // [Q, 64, 128]
   float* w_out;           // [Q, 64]
+  // fp8 index keys (instance kFp8): the quantised queries [Q, 64, 128] codes and [Q, 64] scales, and the key rows
+  // (kFp8RowBytes each: 128 codes, then the fp32 scale) for the scales
+  const uint8_t* q8;
+  const float* qs;
+  const uint8_t* keys8;
 };
 
 __device__ __forceinline__ int idx_seq(const IdxArgs& a, int q) {
@@ -192,11 +202,11 @@ struct Items {
 // Decode (G = 1) keeps to 128 registers a thread: the compress calls' small kernels running beside the scan
 // on other streams (a pooling CTA: 256 threads x 64 registers) must still fit on the SMs it holds, or the
 // scan's remaining CTAs wait for them to finish.
-template <int G, bool kOverlap>
-__global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
+template <int G, bool kOverlap, bool kFp8 = false>
+__global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
                       IdxArgs a) {
-  using C = IdxCfg<G>;
+  using C = IdxCfg<G, kFp8>;
   constexpr int N = C::N;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -240,8 +250,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   // batch of query chunks) is requested before the preceding kernel has completed: these are step inputs and
   // constants that no kernel writes.  16 chunks of 8 dims per head row; each thread takes 16 (G = 1) or 64 (G = 4)
   // chunks, in batches whose loads are all issued before any is used.
-  constexpr int kBatch = G == 1 ? 16 : 8;  // prefill: fewer registers (twelve warps share the register file)
-  constexpr int kChunks = G * 64 * 16;
+  // fp8: 8 chunks of 16 codes per head row, copied from the quantised queries (no RoPE here: the queries were
+  // roped and quantised by the kernel before)
+  constexpr int kChunksPerRow = kFp8 ? 8 : 16;
+  constexpr int kBatch = G == 1 ? (kFp8 ? 8 : 16) : 8;  // prefill: fewer registers (twelve warps share the file)
+  constexpr int kChunks = G * 64 * kChunksPerRow;
   const int pt = threadIdx.x - 32 * C::kPrepWarp0;
   struct Pre {
     uint4 raw[kBatch];
@@ -261,7 +274,16 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     }
   };
   auto load_first = [&](int g, Pre& pre) {
-    if constexpr (G != 4) {
+    if constexpr (kFp8) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int e = pt + b * kPrepThreads;
+        const int q = g * G + (e >> 9), h = (e >> 3) & 63, c = e & 7;
+        pre.raw[b] = (e < kChunks && q < a.Q)
+                         ? __ldg(reinterpret_cast<const uint4*>(a.q8 + ((size_t)q * 64 + h) * 128 + c * 16))
+                         : make_uint4(0, 0, 0, 0);
+      }
+    } else if constexpr (G != 4) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int e = pt + b * kPrepThreads;
@@ -275,6 +297,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     for (int i = 0; i < G; ++i) {
       const int e = pt + i * kPrepThreads, q = grp_query<G>(a, g, e / 64);
       pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
+      // fp8: the head's query scale and the 1/128 of the unnormalised rotation go into its weight
+      if constexpr (kFp8) pre.wv[i] *= q >= 0 ? __ldg(a.qs + (size_t)q * 64 + (e & 63)) * 0.0078125f : 0.f;
     }
     // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
     pre.th_freq = __ldg(a.inv_freq + (pt & 31));
@@ -300,8 +324,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   Pre pre_a;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-  // The first query block is requested before the wait (step inputs), except with a group table, which the
-  // kernel before writes.  G = 4: the range's first group is copied now; whether it has tiles is known only after
+  // The first query block is requested before the wait (step inputs), except with a group table or fp8 queries,
+  // which the kernel before writes.  G = 4: the range's first group is copied now; whether it has tiles is known only after
   // the wait (a prefill chunk's first groups may have none), so the loop below drains this copy if it starts at a
   // later group.
   if (warp >= C::kPrepWarp0 && i_begin < i_end) {
@@ -311,7 +335,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
       tc::fence_mbar_init();
       tc::tma_prefetch(&tm_q);
     }
-    if (G != 4 || !a.gcu) {
+    if (!kFp8 && (G != 4 || !a.gcu)) {
       if (G == 4) issue_q(g0);
       load_first(g0, pre_a);
     }
@@ -321,6 +345,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
   // a projection kernel that lets successors start only once all earlier work is complete.)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
+  // fp8: the quantised queries and their scales are the preceding kernel's output
+  if constexpr (kFp8) {
+    if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
+  }
   if constexpr (G == 4) {
     if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) {
       issue_q(g0);
@@ -356,9 +384,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         int cnt;
         const int krow = idx_seq(a, grp_first<G>(a, g, cnt)) * a.cap + t * kTileRows;  // a group's queries share
                                                                                    // a sequence
-        tc::mbar_arrive_expect_tx(&full[stage], kTileBytes);
-        tc::tma_load_2d(kbuf + stage * kTileBytes, &tm_keys, &full[stage], 0, krow);
-        tc::tma_load_2d(kbuf + stage * kTileBytes + kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
+        tc::mbar_arrive_expect_tx(&full[stage], C::kTileBytes);
+        tc::tma_load_2d(kbuf + stage * C::kTileBytes, &tm_keys, &full[stage], 0, krow);
+        if constexpr (!kFp8)
+          tc::tma_load_2d(kbuf + stage * C::kTileBytes + C::kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
         used |= 1u << stage;
         par_last = (par_last & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -385,13 +414,23 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
         if (!tc::mbar_wait(&full[stage], phase)) { failed = true; break; }
         if (!tc::mbar_wait(&acc_empty[acc], ((acc_par >> acc) & 1) ^ 1)) { failed = true; break; }
         tc::fence_after_sync();
-        const uint32_t a_base = tc::smem_u32(kbuf + stage * kTileBytes);
+        const uint32_t a_base = tc::smem_u32(kbuf + stage * C::kTileBytes);
         const uint32_t b_base = tc::smem_u32(qbuf + (k % C::kQSlots) * C::kQBytes);
+        if constexpr (kFp8) {
+          // K = 128 E4M3 elements: four 32-element steps inside one 128-byte swizzled row
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = tc::sdesc_kmajor_sw128(a_base + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
-          const uint64_t bd = tc::sdesc_kmajor_sw128(b_base + (kk >> 2) * (C::kQBytes / 2) + (kk & 3) * 32);
-          tc::mma_bf16(tmem + acc * N, ad, bd, idesc, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = tc::sdesc_kmajor_sw128(a_base + kk * 32);
+            const uint64_t bd = tc::sdesc_kmajor_sw128(b_base + kk * 32);
+            tc::mma_f8(tmem + acc * N, ad, bd, tc::idesc_e4m3(128, N), kk > 0);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = tc::sdesc_kmajor_sw128(a_base + (kk >> 2) * (C::kTileBytes / 2) + (kk & 3) * 32);
+            const uint64_t bd = tc::sdesc_kmajor_sw128(b_base + (kk >> 2) * (C::kQBytes / 2) + (kk & 3) * 32);
+            tc::mma_bf16(tmem + acc * N, ad, bd, idesc, kk > 0);
+          }
         }
         tc::mma_commit(&empty[stage]);
         tc::mma_commit(&acc_full[acc]);
@@ -424,9 +463,14 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
           nv[qq] = qix[qq] >= 0 ? scan_rows<kOverlap>(a, qix[qq]) : 0;
         }
       }
+      const int j = t * kTileRows + row;
+      float kscale = 1.f;  // fp8: the key row's scale, requested before the accumulator wait
+      if constexpr (kFp8)
+        kscale = j < nv[0] ? __ldg(reinterpret_cast<const float*>(
+                                 a.keys8 + ((size_t)idx_seq(a, qix[0]) * a.cap + j) * kFp8RowBytes + 128))
+                           : 0.f;
       if (!tc::mbar_wait(&acc_full[acc], (acc_par >> acc) & 1)) { failed = true; break; }
       tc::fence_after_sync();
-      const int j = t * kTileRows + row;
       const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
       // this warp's queries (kQPerWarp of them) in one TMEM round trip (one wait covers every load)
       {
@@ -456,7 +500,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
             s01 = __ffma2_rn(make_float2(w.x, w.y), r01, s01);
             s23 = __ffma2_rn(make_float2(w.z, w.w), r23, s23);
           }
-          const float s = (s01.x + s01.y) + (s23.x + s23.y);
+          float s = (s01.x + s01.y) + (s23.x + s23.y);
+          if constexpr (kFp8) s *= kscale;  // ReLU(k s) = k ReLU(s) for the row's scale k >= 0
           if (j < nv[qq]) a.scores[(size_t)qix[qq] * a.cap + j] = s;
         }
       }
@@ -474,6 +519,16 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     // The first group's inputs were requested before the wait above (load_first), so its preparation costs about
     // one memory round trip, overlapped with the preceding kernel.
     auto rope_store = [&](uint8_t* qb, int e0, uint4 (&raw)[kBatch], int g) {
+      if constexpr (kFp8) {  // codes as they are, into the one 128-byte swizzled box of each head row
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + b * kPrepThreads;
+          if (e >= kChunks) break;
+          const int row = ((e >> 9) << 6) + ((e >> 3) & 63), c = e & 7;
+          *reinterpret_cast<uint4*>(qb + row * 128 + ((c ^ (row & 7)) << 4)) = raw[b];
+        }
+        return;
+      }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int e = e0 + b * kPrepThreads;
@@ -499,8 +554,13 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
     if (g1 >= 0) {
       int cnt1;
       const int q01 = grp_first<G>(a, g1, cnt1);
-      for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
-        if (e / 32 < cnt1) tc::prefetch_l2(a.iq + ((size_t)q01 * 64 + e * 2) * 128, 512);
+      if constexpr (kFp8) {
+        for (int e = pt; e < 16 * G; e += kPrepThreads)  // 512 B a thread: 16 threads per block of codes
+          if (e / 16 < cnt1) tc::prefetch_l2(a.q8 + (size_t)q01 * 8192 + e * 512, 512);
+      } else {
+        for (int e = pt; e < 32 * G; e += kPrepThreads)  // 512 B a thread: 32 threads per query block
+          if (e / 32 < cnt1) tc::prefetch_l2(a.iq + ((size_t)q01 * 64 + e * 2) * 128, 512);
+      }
     }
     tc::named_bar_arrive(4, 32 + kPrepThreads);  // releases the key-tile producer
     int k = -1;
@@ -602,6 +662,47 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, G == 1 ? 2 : 1)
 
 int g_num_sms = 0;
 
+// fp8 index queries (the optional key format): query q's head h, RoPE at pos[q] as for the bf16 scores, rounded
+// to bf16, rotated by the unnormalised 128-point Walsh-Hadamard transform in fp32 (butterflies of span 1, 2, ..,
+// 64 in that order), scaled by amax / 448 and rounded to E4M3 (nearest even, saturating): q8 [Q, 64, 128] codes,
+// qs [Q, 64] scales.  Warp w takes heads 8w .. 8w + 7; lane l holds elements 4l .. 4l + 3 of a head (spans 1 and
+// 2 inside the lane, spans 4 .. 64 between lanes l and l ^ span / 4).
+__global__ void __launch_bounds__(256) k_quant_iq(const __nv_bfloat16* __restrict__ iq,
+                                                  const int32_t* __restrict__ pos, const float* __restrict__ inv_freq,
+                                                  int R, uint8_t* __restrict__ q8, float* __restrict__ qs) {
+  pdl_trigger();
+  pdl_wait();
+  const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = pos[q];
+  for (int h = warp * 8; h < warp * 8 + 8; ++h) {
+    const __nv_bfloat16* src = iq + ((size_t)q * 64 + h) * 128 + 4 * lane;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    __nv_bfloat162 hv[2];
+    memcpy(hv, &raw, sizeof(raw));
+    float u[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i0 = 4 * lane + 2 * k;  // element pair (i0, i0 + 1)
+      const float2 x = __bfloat1622float2(hv[k]);
+      if (i0 >= 128 - R) {
+        float cs, sn;
+        rope_cs(p, inv_freq, (i0 - (128 - R)) >> 1, &cs, &sn);
+        const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(x.x, cs, -x.y * sn), fmaf(x.x, sn, x.y * cs));
+        const float2 y = __bfloat1622float2(r);
+        u[2 * k] = y.x;
+        u[2 * k + 1] = y.y;
+      } else {
+        u[2 * k] = x.x;
+        u[2 * k + 1] = x.y;
+      }
+    }
+    float scale;
+    const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
+    *reinterpret_cast<uint32_t*>(q8 + ((size_t)q * 64 + h) * 128 + 4 * lane) = packed;
+    if (lane == 0) qs[(size_t)q * 64 + h] = scale;
+  }
+}
+
 // gcu[b] = sum over sequences before b of ceil(T_b / 4) (T_b = cu[b+1] - cu[b], an inconsistent entry counted as
 // empty), b = 0 .. nseq: one block, each thread a contiguous share of the sequences, then a block scan.
 __global__ void __launch_bounds__(1024) k_varlen_groups(const int32_t* __restrict__ cu, int nseq,
@@ -645,7 +746,7 @@ size_t tc_index_ws(const Dims& L, int Q) {
 cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw, int Q, const void* ikeys, int Bk,
                                    int cap, const int32_t* n_rows, const int32_t* pos, int pos0,
                                    const float* inv_freq, void* ws, float* scores, int32_t* err, cudaStream_t s,
-                                   bool overlap, const int32_t* cu) {
+                                   bool overlap, const int32_t* cu, bool fp8) {
   if (!g_num_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -690,6 +791,23 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
     a.w_out = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)Q * 64 * 128 * 2);
   }
   const int grid = min(g_num_sms, a.n_items);
+  if (fp8) {
+    // decode only: the quantised queries go into the query-output area of ws, the keys are fp8 rows
+    if (!pos || G != 1 || overlap || cu || !ws) return cudaErrorInvalidValue;
+    auto* q8 = static_cast<uint8_t*>(ws);
+    auto* qsc = reinterpret_cast<float*>(q8 + (size_t)Q * 64 * 128);
+    CSA_LAUNCH(k_quant_iq, dim3(Q), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(iq), pos, inv_freq, L.R, q8,
+               qsc);
+    CUtensorMap tk8;
+    if (!make_tmap_2d_u8(&tk8, ikeys, (uint64_t)Bk * cap, 128, kFp8RowBytes, kTileRows)) return cudaErrorInvalidValue;
+    a.q8 = q8;
+    a.qs = qsc;
+    a.keys8 = static_cast<const uint8_t*>(ikeys);
+    constexpr int smem = IdxCfg<1, true>::kSmem;
+    cudaFuncSetAttribute(k_tc_index_scores<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<1, false, true>, dim3(grid), dim3(IdxCfg<1, true>::kThreads), smem, s, tk8, tq, a);
+    return cudaGetLastError();
+  }
   if (G == 1 && overlap) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

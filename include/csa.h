@@ -103,14 +103,32 @@ enum {
  *     W + rollback slots (token t in slot t mod (W + rollback)) and each frontier
  *     ring csa_frontier_slots(ratio) + rollback slots (its journal of projected
  *     rows); a query still attends only its last W tokens.  Every call of a layer
- *     takes buffers of those sizes. */
+ *     takes buffers of those sizes.
+ *   index_fp8: 0 (index keys in the model dtype) or 1 (fp8 index rows of
+ *     CSA_FP8_ROW_BYTES: the index pool is then a [B, cap, 144] byte tensor that
+ *     csa_compress_append / _pair write and csa_index_topk reads; ratio 4, bf16,
+ *     Hi = 64, Di = 128 only, else CSA_ERR_UNSUPPORTED; the other index calls
+ *     return CSA_ERR_UNSUPPORTED with it). */
 typedef struct {
   int dtype;
   int H, D, R, W, ratio, Hi, Di, topk, X;
   float scale;
   float rms_eps;
   int rollback;
+  int index_fp8;
 } csa_layer;
+
+/* Bytes of one index-key row when layer->index_fp8 = 1: the row (already in
+ * the model dtype, as the bf16 format would store it) rotated by the
+ * unnormalised 128-point Walsh-Hadamard transform (fp32 butterflies of span
+ * 1, 2, .., 64), as 128 E4M3 codes of rotated / scale (nearest even,
+ * saturating), then the fp32 scale = amax / 448 at byte 128, then padding.
+ * The index queries are rotated and quantised per head the same way and a
+ * score is the bf16 definition on the decoded values, divided by 128
+ * ([mlx-lm#1189], the indexer thread: a Hadamard rotation and a low-precision
+ * activation simulation in the indexer, the rotation cancelling in the dot
+ * product; the format itself is this library's choice). */
+#define CSA_FP8_ROW_BYTES 144
 
 /* One compressor (the attention pool's, d = D, or the index pool's, d = Di).
  * L = 2 lanes when ratio == 4, else 1.

@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol(lib):
 
 def _layer(**kw):
     base = dict(dtype=B.CSA_BF16, H=64, D=512, R=64, W=128, ratio=4, Hi=64, Di=128, topk=512, X=4096, scale=0.0,
-                rms_eps=1e-6, rollback=0)
+                rms_eps=1e-6, rollback=0, index_fp8=0)
     base.update(kw)
     return B._Layer(*[base[f] for f, _ in B._Layer._fields_])
 
@@ -167,3 +167,25 @@ def test_binding_checks_dtypes_and_shapes_before_the_device(lib):
         csa.compress_append(L, comp, z(2, 1, 4096, dtype=torch.bfloat16), z(2, dtype=torch.int32),
                             z(2, 4, 2048, dtype=torch.bfloat16), z(2, 40, 512, dtype=torch.bfloat16),
                             z(2, dtype=torch.int32), z(32))
+
+
+def test_fp8_index_rows_host_checks(lib):
+    """index_fp8: 0 or 1; fp8 rows need ratio 4, bf16, Hi = 64, Di = 128 and D != Di; only the decode index call
+    and the compress calls take them, the other index entry points refuse the layer before touching a pointer."""
+    n = ctypes.c_size_t()
+    assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=1)), B.OP_INDEX_TOPK, 32, 1, 8400,
+                                  ctypes.byref(n)) == B.CSA_OK
+    assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=2)), 0, 1, 1, 1, ctypes.byref(n)) == B.CSA_ERR_ARG
+    for bad in (dict(ratio=128), dict(dtype=B.CSA_F32), dict(Hi=32), dict(Di=64, R=64), dict(D=128)):
+        assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=1, **bad)), 0, 1, 1, 1,
+                                      ctypes.byref(n)) == B.CSA_ERR_UNSUPPORTED, bad
+    L8 = _layer(index_fp8=1, rollback=8)
+    assert lib.csa_index_topk_overlapped(ctypes.byref(L8), FAKE, FAKE, 1, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                         FAKE, 1 << 30, FAKE, None, None) == B.CSA_ERR_UNSUPPORTED
+    assert lib.csa_attend_prefill_chunk(ctypes.byref(L8), FAKE, FAKE, FAKE, FAKE, FAKE, 8, 0, FAKE, FAKE, FAKE, 10,
+                                        FAKE, FAKE, FAKE, None, FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_UNSUPPORTED
+    assert lib.csa_index_topk_verify(ctypes.byref(L8), FAKE, FAKE, 1, 4, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_UNSUPPORTED
+    assert lib.csa_attend_prefill_varlen(ctypes.byref(L8), FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, 8, 4, FAKE, FAKE,
+                                         FAKE, FAKE, 10, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, FAKE,
+                                         None) == B.CSA_ERR_UNSUPPORTED

@@ -1,0 +1,185 @@
+"""Index keys as fp8 rows (csa_layer.index_fp8 = 1) on the GPU against the oracle.
+
+The mlx-lm DeepSeek-V4 port's indexer discussion (mlx-lm#1189) rotates the index operands by a Hadamard matrix and
+simulates low-precision activations; this library stores the index pool as E4M3 rows of the rotated keys with one
+fp32 scale per row and quantises the decode query's heads the same way (the oracle's quantize_fp8_row /
+quantize_fp8_query / index_scores_fp8).  Checked here:
+
+  * every fp8 row the compressors write (the chunk kernel and the single-token kernel of the paired call) equals,
+    code for code and bit for bit in its scale, the oracle's quantisation of the row the same kernels write in the
+    model dtype for a bf16 layer fed the same tokens: both sides rotate the same bf16 values with the same fp32
+    butterflies, divide and round to nearest even, so nothing is left to tolerance;
+  * the query codes the index call writes to its workspace: exact at position 0 (RoPE is then the identity on both
+    sides, so the inputs match; an all-zero head gets scale 0 and zero codes); at later positions the GPU's fp32
+    RoPE may land one bf16 ulp away from the oracle's float64 one in a few elements, so most heads must match
+    exactly and every head's scale within 2^-6;
+  * the selection under the gap rule against index_scores_fp8 on the GPU's own key and query codes (identical
+    operands; only the summation order differs), dense (n_vis <= topk) and sparse, at every decode step; the
+    fixed-scratch entry point selects the same rows.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import csa_synth
+from oracle import csa_oracle as O
+from tests._common import f64, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from tests import _gpu as G
+
+ROW = 144  # bytes of an fp8 index row: 128 codes, the fp32 scale, padding
+
+
+def _codes_scales(rows8: torch.Tensor):
+    """uint8 [..., 144] -> (codes int64 [..., 128], scales float32 [...]); checks the zero padding."""
+    a = rows8.cpu().numpy()
+    assert np.all(a[..., 132:] == 0), "padding bytes of an fp8 row are not zero"
+    codes = a[..., :128].astype(np.int64)
+    scales = np.ascontiguousarray(a[..., 128:132]).view(np.float32)[..., 0]
+    return codes, scales
+
+
+def _check_rows_exact(rows8, rows16, what):
+    """fp8 rows against the oracle's quantisation of the bf16 rows the same kernels wrote."""
+    codes, scales = _codes_scales(rows8)
+    ref = f64(rows16).astype(np.float32)
+    for j in range(ref.shape[0]):
+        c, s = O.quantize_fp8_row(ref[j])
+        assert np.float32(s).view(np.uint32) == scales[j].view(np.uint32), f"{what} row {j}: scale {scales[j]} vs {s}"
+        bad = np.nonzero(codes[j] != c)[0]
+        assert bad.size == 0, f"{what} row {j}: {bad.size} codes differ, first at {bad[0]}: {codes[j, bad[0]]:#x} " \
+                              f"vs {c[bad[0]]:#x}"
+
+
+class _State:
+    """Attention pool and index pool state of one layer on the device, from an empty cache."""
+
+    def __init__(self, cfg, cap, fp8):
+        c = csa_synth.empty_cache(cfg, cap)
+        self.pool, self.front_a, self.front_i = G.dev(c.pool), G.dev(c.front_attn), G.dev(c.front_index)
+        self.ikeys = (torch.zeros(cfg.B, cap, ROW, dtype=torch.uint8, device="cuda") if fp8 else G.dev(c.ikeys))
+        self.n_a, self.n_i, self.pos = G.dev(c.n_rows), G.dev(c.n_rows), G.dev(c.pos)
+
+
+def _query_ws(L, B, cap):
+    import deepseek_v4_compressed_csa_gb300 as csa
+    return torch.zeros(csa.workspace_size(L, csa.OP_INDEX_TOPK, B, 1, cap), dtype=torch.uint8, device="cuda")
+
+
+def _ws_queries(ws, B):
+    """The quantised decode queries in the index call's workspace: [B, 64, 128] codes, then [B, 64] fp32 scales."""
+    a = ws.cpu().numpy()
+    codes = a[:B * 64 * 128].reshape(B, 64, 128).astype(np.int64)
+    scales = np.ascontiguousarray(a[B * 64 * 128:B * 64 * 128 + B * 64 * 4]).view(np.float32).reshape(B, 64)
+    return codes, scales
+
+
+def test_fp8_queries_exact_at_position_zero():
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=3, ctx=0)
+    L = dataclasses.replace(G.lib_layer(cfg), index_fp8=True)
+    layer = oracle_layer(cfg)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    cap = 64
+    si = csa_synth.step_inputs(cfg.replace(cid=cfg.cid + 900), 0)
+    iq = si.iq.clone()
+    iq[1, 5] = 0  # an all-zero head: scale 0, zero codes
+    st = _State(cfg, cap, True)
+    sel = torch.empty(cfg.B, cfg.topk, dtype=torch.int32, device="cuda")
+    n_sel = torch.empty(cfg.B, dtype=torch.int32, device="cuda")
+    ws = _query_ws(L, cfg.B, cap)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa.index_topk(L, G.dev(iq), G.dev(si.iw), st.ikeys, st.n_i, st.pos, G.dev(csa_synth.inv_freq(cfg)), sel, n_sel,
+                   ws=ws, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert n_sel.cpu().tolist() == [0] * cfg.B
+    codes, scales = _ws_queries(ws, cfg.B)
+    for b in range(cfg.B):
+        c, s = O.quantize_fp8_query(layer, f64(iq[b]), 0, invf)
+        assert np.array_equal(scales[b].view(np.uint32), s.view(np.uint32)), f"query {b}: scales differ"
+        assert np.array_equal(codes[b], c), f"query {b}: codes differ"
+    assert scales[1, 5] == 0 and not codes[1, 5].any()
+
+
+# (tokens compressed from an empty cache before the decode steps, decode steps): 1023 tokens leave 255 rows
+# (dense: every visible row is selected), 4095 leave 1023 rows (sparse: 512 of 1023 .. 1024).
+CASES = {"dense": (1023, 6), "sparse": (4095, 6)}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_fp8_index_rows_and_selection(case):
+    import deepseek_v4_compressed_csa_gb300 as csa
+    T0, steps = CASES[case]
+    cfg = csa_synth.CONFIGS[3].replace(B=2, ctx=0)
+    L16 = G.lib_layer(cfg)
+    L8 = dataclasses.replace(L16, index_fp8=True)
+    layer = oracle_layer(cfg)
+    invf = f64(csa_synth.inv_freq(cfg)).astype(np.float32)
+    inv_freq = G.dev(csa_synth.inv_freq(cfg))
+    ca = G.lib_comp(csa_synth.compressor(cfg, "attn"))
+    ci = G.lib_comp(csa_synth.compressor(cfg, "index"))
+    cap = (T0 + steps) // 4 + 70  # ragged last tile of 128 rows
+    s16, s8 = _State(cfg, cap, False), _State(cfg, cap, True)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # the cache: one chunk of T0 tokens per sequence through each pool's own compress call (chunk kernel)
+    x = G.dev(csa_synth.hidden(cfg, T0, tag=31))
+    for L, s in ((L16, s16), (L8, s8)):
+        csa.compress_append(L, ca, x, s.pos, s.front_a, s.pool, s.n_a, inv_freq, err=err)
+        csa.compress_append(L, ci, x, s.pos, s.front_i, s.ikeys, s.n_i, inv_freq, err=err)
+        s.pos += T0
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    n0 = T0 // 4
+    assert s8.n_i.cpu().tolist() == [n0] * cfg.B
+    for b in range(cfg.B):
+        _check_rows_exact(s8.ikeys[b, :n0], s16.ikeys[b, :n0], f"chunk, sequence {b}")
+    assert torch.equal(s8.pool, s16.pool)
+    mism, heads = 0, 0
+    for k in range(steps):
+        si = csa_synth.step_inputs(cfg.replace(cid=cfg.cid + 900), k + 1)
+        xk = G.dev(si.x)
+        for L, s in ((L16, s16), (L8, s8)):  # both pools in one call: the single-token kernel
+            csa.compress_append_pair(L, ca, ci, xk, s.pos, s.front_a, s.pool, s.n_a, s.front_i, s.ikeys, s.n_i,
+                                     inv_freq, err=err)
+        sel = torch.empty(cfg.B, cfg.topk, dtype=torch.int32, device="cuda")
+        n_sel = torch.empty(cfg.B, dtype=torch.int32, device="cuda")
+        ws = _query_ws(L8, cfg.B, cap)
+        iq, iw = G.dev(si.iq), G.dev(si.iw)
+        csa.index_topk(L8, iq, iw, s8.ikeys, s8.n_i, s8.pos, inv_freq, sel, n_sel, ws=ws, err=err)
+        sel_s = torch.empty_like(sel)
+        n_sel_s = torch.empty_like(n_sel)
+        csa.index_topk_static(L8, iq, iw, s8.ikeys, s8.n_i, s8.pos, inv_freq, sel_s, n_sel_s, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert torch.equal(sel_s, sel) and torch.equal(n_sel_s, n_sel)
+        n = s8.n_i.cpu().numpy()
+        pos = s8.pos.cpu().numpy()
+        assert np.array_equal(n, s16.n_i.cpu().numpy())
+        if (pos[0] + 1) % 4 == 0:  # the step completed a row: the single-token kernel's fp8 store
+            for b in range(cfg.B):
+                _check_rows_exact(s8.ikeys[b, n[b] - 1:n[b]], s16.ikeys[b, n[b] - 1:n[b]], f"step {k}, seq {b}")
+        qc, qs = _ws_queries(ws, cfg.B)
+        kc, ks = _codes_scales(s8.ikeys)
+        g_sel, g_n = sel.cpu().numpy(), n_sel.cpu().numpy()
+        for b in range(cfg.B):
+            p = int(pos[b])
+            oc, osc = O.quantize_fp8_query(layer, f64(si.iq[b]), p, invf)
+            rel = np.abs(qs[b].astype(np.float64) - osc) / np.maximum(osc, 1e-30)
+            assert rel.max() <= 2.0 ** -6, f"step {k} seq {b}: query scale off by {rel.max()}"
+            same = np.all(qc[b] == oc, axis=1)
+            mism += int((~same).sum())
+            heads += same.size
+            nv = O.visible_rows(layer, int(n[b]), p)
+            rows = g_sel[b][:g_n[b]]
+            scores = O.index_scores_fp8(layer, qc[b], qs[b], f64(si.iw[b]), kc[b, :nv], ks[b, :nv])
+            G.check_topk(rows, scores, layer.topk, nv, what=f"step {k} seq {b} fp8 top-k")
+        s8.pos += 1
+        s16.pos += 1
+    # a head's codes differ only when the fp32 RoPE of one of its elements rounds to the other bf16 neighbour
+    assert mism <= heads // 10, f"{mism} of {heads} query heads quantised differently from the oracle"
