@@ -240,10 +240,11 @@ class DecodeWorkload:
     """Config 3 state, weights and per-step inputs resident on one GPU."""
 
     def __init__(self, cfg, cap: int, n_inputs: int, device, serial_indexer: bool = False, host=None,
-                 host_comp=None, pos=None, input_tag: int = 0):
+                 host_comp=None, pos=None, input_tag: int = 0, index_fp8: bool = False):
         """host / host_comp: a synthetic cache and compressor weights generated once and copied here (several
         layers hold copies in distinct device memory); pos: a position tensor shared with other layers;
-        input_tag: offset of this layer's per-step input sets."""
+        input_tag: offset of this layer's per-step input sets; index_fp8: the index pool as fp8 rows (the
+        cache's model-dtype index rows converted by csa_index_rows_fp8)."""
         import torch
 
         import csa_synth
@@ -255,7 +256,8 @@ class DecodeWorkload:
         # indexer, or after it (then attention has two predecessors)
         self.join_before_index = False
         self.L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi,
-                           Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+                           Di=cfg.Di, topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps,
+                           index_fp8=index_fp8)
         d = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
 
         def comp(c):
@@ -268,6 +270,11 @@ class DecodeWorkload:
         if host is None:
             host = csa_synth.synth_cache(cfg, cap)
         self.pool, self.ikeys, self.window = d(host.pool), d(host.ikeys), d(host.window)
+        if index_fp8:
+            keys = self.ikeys
+            self.ikeys = torch.empty(cfg.B, cap, csa.FP8_ROW_BYTES, dtype=torch.uint8, device=device)
+            csa.index_rows_fp8(self.L, keys, self.ikeys)
+            del keys
         self.front_a, self.front_i = d(host.front_attn), d(host.front_index)
         self.n_a, self.n_i = d(host.n_rows), d(host.n_rows)
         self.pos = d(host.pos) if pos is None else pos
@@ -424,7 +431,7 @@ class ModelStep:
     CUDA graph replay holding every layer."""
 
     def __init__(self, cfg, cap: int, n_inputs: int, device, n_layers: int, pair: bool = True, host=None,
-                 one_stream_overlap: bool = False):
+                 one_stream_overlap: bool = False, index_fp8: bool = False):
         import torch
 
         import csa_synth
@@ -435,7 +442,7 @@ class ModelStep:
         pos = None
         for i in range(n_layers):
             wl = DecodeWorkload(cfg, cap, n_inputs, device, serial_indexer=True, host=host, host_comp=host_comp,
-                                pos=pos, input_tag=1000 * i)
+                                pos=pos, input_tag=1000 * i, index_fp8=index_fp8)
             wl.pair = wl.pair and pair
             wl.one_stream_overlap = one_stream_overlap
             pos = wl.pos
@@ -699,12 +706,14 @@ def verify_line(csa, csa_synth, dev, flush, steps: int, warmup: int, nl: int, T:
             "calls": "per layer: csa_compress_append_pair (T tokens), csa_index_topk_verify, csa_attend_verify"}
 
 
-def step_bytes(cfg, n_rows_mean: float) -> dict:
-    """Algorithmic HBM bytes of one decode step (each byte the step must move once)."""
+def step_bytes(cfg, n_rows_mean: float, index_fp8: bool = False) -> dict:
+    """Algorithmic HBM bytes of one decode step (each byte the step must move once); index_fp8: index-key rows of
+    144 bytes (128 codes and the row's scale) instead of Di model-dtype values."""
     B, e = cfg.B, 2
     L = cfg.lanes
     w = (2 * L * cfg.D * cfg.X + (2 * L * cfg.Di * cfg.X if cfg.has_indexer else 0)) * e
-    keys = B * n_rows_mean * cfg.Di * e if cfg.has_indexer else 0
+    key_row = 144 if index_fp8 else cfg.Di * e
+    keys = B * n_rows_mean * key_row if cfg.has_indexer else 0
     rows = B * ((cfg.topk if cfg.has_indexer else n_rows_mean) + cfg.W) * cfg.D * e
     qo = 2 * B * cfg.H * cfg.D * e
     small = B * (cfg.X * e + cfg.D * e + cfg.Hi * cfg.Di * e + cfg.Hi * e + cfg.topk * 4)
@@ -751,15 +760,17 @@ def built_cache_b1(csa, csa_synth, cfg, cap, dev):
 
 
 def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup: int, nl: int,
-                       overlap: bool = False) -> dict:
+                       overlap: bool = False, index_fp8: bool = False) -> dict:
     """Throughput and HBM fraction of another decode workload as a model step of `nl` layers (config 2: B = 1
     on an 8K cache the library compressed from seeded hidden states; config 4: ratio 128, B = 16, 256K context,
-    every row attended), timed like the headline."""
+    every row attended; config 3 with index_fp8: the headline workload with the index pool as fp8 rows), timed
+    like the headline."""
     cfg = csa_synth.CONFIGS[cid]
     n_ctx = cfg.prefill_tokens if cid == 2 else cfg.ctx
     cap = n_ctx // cfg.ratio + (warmup + steps + 8) // cfg.ratio + 8
     host = built_cache_b1(csa, csa_synth, cfg, cap, dev) if cid == 2 else None
-    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, host=host, one_stream_overlap=overlap)
+    ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, host=host, one_stream_overlap=overlap,
+                   index_fp8=index_fp8)
     wl = ms.layers[0]
     ms.step(0)
     ms.capture()
@@ -772,18 +783,19 @@ def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup:
         assert layer.err.item() == 0, f"device error word {layer.err.item()}"
     per = [x / nl for x in t]
     mean_ms = statistics.mean(per)
-    nb = step_bytes(cfg, 0.5 * (n0 + n1))
+    nb = step_bytes(cfg, 0.5 * (n0 + n1), index_fp8)
     hbm, _, _ = _peaks()
     gbs = nb["total"] / (mean_ms / 1e3) / 1e9
     del ms
-    return {"workload": cfg.name, "B": cfg.B, "context": n_ctx, "ratio": cfg.ratio, "compressed_rows": [n0, n1],
+    return {"workload": cfg.name + (" fp8-index-keys" if index_fp8 else ""), "B": cfg.B, "context": n_ctx, "ratio": cfg.ratio, "compressed_rows": [n0, n1],
             "layer_steps_per_s": round(1e3 / mean_ms, 1), "tokens_per_s": round(cfg.B * 1e3 / mean_ms, 1),
             "us_per_layer_step": round(1e3 * mean_ms, 2),
             "us_per_layer_step_p10_p50_p90": [round(1e3 * x, 2) for x in _percentiles(per)],
             "step_algorithmic_bytes": int(nb["total"]), "achieved_gbs": round(gbs, 1),
             "hbm_frac": round(gbs / hbm, 4), "layers_per_step": nl, "steps": steps,
             "cache": ("compressed from 8192 seeded hidden tokens by the library" if cid == 2 else
-                      "synthetic rows drawn directly (seeded N(0,1))")}
+                      "synthetic rows drawn directly (seeded N(0,1))" + (
+                          "; index rows converted to fp8 rows by csa_index_rows_fp8" if index_fp8 else ""))}
 
 
 def trim_line(csa, csa_synth, dev) -> dict:
@@ -961,9 +973,9 @@ def run_ours(args):
         del ms, wl
         torch.cuda.empty_cache()
         others = {}
-        for cid in (2, 4):
+        for cid, fp8 in ((2, False), (4, False), (3, True)):
             line = decode_config_line(csa, csa_synth, cid, dev, flush, args.steps, args.warmup, nl,
-                                      overlap=args.indexer == "overlap")
+                                      overlap=args.indexer == "overlap" and not fp8, index_fp8=fp8)
             others[line["workload"]] = line
 
     hbm, tflops, peak_src = _peaks()

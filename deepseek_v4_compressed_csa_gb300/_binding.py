@@ -30,7 +30,7 @@ EXPORTS = ("csa_kernel_launches", "csa_frontier_slots", "csa_workspace_size", "c
            "csa_attend_decode", "csa_attend_prefill_chunk", "csa_status_string", "csa_static_scratch_bytes",
            "csa_index_topk_static", "csa_index_topk_overlapped", "csa_advance_positions",
            "csa_compress_append_pair", "csa_trim", "csa_index_topk_verify", "csa_attend_verify",
-           "csa_compress_append_varlen", "csa_attend_prefill_varlen")
+           "csa_compress_append_varlen", "csa_attend_prefill_varlen", "csa_index_rows_fp8")
 
 
 class CSAError(RuntimeError):
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.csa_attend_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, vp, i32, vp, vp,
                                               vp, vp, vp, sz, vp, vp]
     lib.csa_attend_prefill_varlen.restype = i32
+    lib.csa_index_rows_fp8.argtypes = [vp, vp, ctypes.c_longlong, vp, vp]
+    lib.csa_index_rows_fp8.restype = i32
     _lib = lib
     return lib
 
@@ -239,6 +241,19 @@ def advance_positions(pos, by: int = 1, stream=None):
     _expect("pos", pos, torch.int32, (pos.numel(),) if isinstance(pos, torch.Tensor) else None)
     _check("csa_advance_positions", load_library().csa_advance_positions(_ptr(pos), pos.numel(), by,
                                                                          _stream(stream)))
+
+
+def index_rows_fp8(layer: Layer, src, dst, stream=None):
+    """csa_index_rows_fp8: src [..., Di] model-dtype index rows -> dst [..., FP8_ROW_BYTES] uint8 fp8 rows (same
+    leading shape); the layer has index_fp8 set."""
+    _expect("src", src, layer.dtype)
+    if src.dim() < 1 or src.shape[-1] != layer.Di:
+        raise ValueError(f"src: shape {tuple(src.shape)}, expected [..., {layer.Di}]")
+    _expect("dst", dst, torch.uint8, tuple(src.shape[:-1]) + (FP8_ROW_BYTES,))
+    n = src.numel() // layer.Di
+    L = layer._c()
+    _check("csa_index_rows_fp8", load_library().csa_index_rows_fp8(ctypes.byref(L), _ptr(src), n, _ptr(dst),
+                                                                   _stream(stream)))
 
 
 def frontier_slots(ratio: int) -> int:

@@ -429,4 +429,15 @@ csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream) {
   return cuda_status(launch_advance_positions(pos, B, by, static_cast<cudaStream_t>(stream)));
 }
 
+csa_status csa_index_rows_fp8(const csa_layer* layer, const void* src, long long n, void* dst, void* stream) {
+  Dims L;
+  csa_status st = make_dims(layer, &L);
+  if (st != CSA_OK) return st;
+  if (!L.ikey_fp8) return CSA_ERR_UNSUPPORTED;
+  if (n < 0 || n > (1LL << 34)) return CSA_ERR_ARG;
+  if (n == 0) return CSA_OK;
+  if (!dev_tensor(src) || !dev_tensor(dst)) return CSA_ERR_ARG;
+  return cuda_status(launch_index_rows_fp8(src, n, dst, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

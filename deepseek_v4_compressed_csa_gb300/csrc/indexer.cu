@@ -10,6 +10,7 @@
 // Launches: rope the index queries -> scores (one block per query and 64-row
 // tile) -> radix select per query (one block per query).
 #include "common.cuh"
+#include "fp8_row.cuh"
 #include "kernels.h"
 
 namespace csa {
@@ -702,6 +703,32 @@ cudaError_t launch_index_topk_overlapped(const Dims& L, const void* iq, const vo
   CSA_LAUNCH(k_topk_reg, dim3(Q), dim3(1024), 0, s, ws.scores, cap, n_rows, pos, 0,
              static_cast<const int32_t*>(nullptr), L.ratio, L.topk, sel, n_sel, qr,
              w, static_cast<const __nv_bfloat16*>(ikeys));
+  return cudaGetLastError();
+}
+
+// Rows of 128 bf16 values -> fp8 index rows (the format the pooling kernels write): one warp per row, lane l
+// takes values 4l .. 4l+3.
+__global__ void __launch_bounds__(256) k_index_rows_fp8(const __nv_bfloat16* __restrict__ src, long long n,
+                                                        uint8_t* __restrict__ dst) {
+  pdl_trigger();
+  pdl_wait();
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;  // a whole warp leaves together
+  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src + r * 128 + 4 * lane));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const float2 v0 = __bfloat1622float2(h[0]), v1 = __bfloat1622float2(h[1]);
+  float u[4] = {v0.x, v0.y, v1.x, v1.y};
+  float scale;
+  const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
+  fp8_row_store(dst + r * kFp8RowBytes, lane, packed, scale);
+}
+
+cudaError_t launch_index_rows_fp8(const void* src, long long n, void* dst, cudaStream_t s) {
+  const long long blocks = (n + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  CSA_LAUNCH(k_index_rows_fp8, dim3((unsigned)blocks), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), n,
+             static_cast<uint8_t*>(dst));
   return cudaGetLastError();
 }
 

@@ -180,6 +180,8 @@ cudaError_t launch_tc_merge(const Dims& L, const float* part_ml, const float* pa
 
 // ---- attend.cu: pos[b] += by for b < B
 cudaError_t launch_advance_positions(int32_t* pos, int B, int by, cudaStream_t s);
+// n rows of 128 bf16 values (src) -> n fp8 index rows of kFp8RowBytes (dst)
+cudaError_t launch_index_rows_fp8(const void* src, long long n, void* dst, cudaStream_t s);
 // ---- attend.cu: csa_trim (rewind B sequences by n_back tokens within the rollback margin)
 cudaError_t launch_trim(const Dims& L, int B, const int32_t* n_back, int32_t* pos, int32_t* n_rows_a,
                         int32_t* n_rows_i, int32_t* hw, int32_t* err, cudaStream_t s);

@@ -665,42 +665,46 @@ int g_num_sms = 0;
 // fp8 index queries (the optional key format): query q's head h, RoPE at pos[q] as for the bf16 scores, rounded
 // to bf16, rotated by the unnormalised 128-point Walsh-Hadamard transform in fp32 (butterflies of span 1, 2, ..,
 // 64 in that order), scaled by amax / 448 and rounded to E4M3 (nearest even, saturating): q8 [Q, 64, 128] codes,
-// qs [Q, 64] scales.  Warp w takes heads 8w .. 8w + 7; lane l holds elements 4l .. 4l + 3 of a head (spans 1 and
-// 2 inside the lane, spans 4 .. 64 between lanes l and l ^ span / 4).
-__global__ void __launch_bounds__(256) k_quant_iq(const __nv_bfloat16* __restrict__ iq,
-                                                  const int32_t* __restrict__ pos, const float* __restrict__ inv_freq,
-                                                  int R, uint8_t* __restrict__ q8, float* __restrict__ qs) {
+// qs [Q, 64] scales.  Block (q, quarter): 16 warps, one head each (heads 16 quarter ..); lane l holds elements
+// 4l .. 4l + 3.  Everything up to the stores reads step inputs only (queries, positions, frequencies), so it runs
+// before the programmatic wait, beside the preceding kernels; the stores wait for them (the workspace may still
+// be read by an earlier call).
+constexpr int kQuantHeads = 16;
+__global__ void __launch_bounds__(32 * kQuantHeads) k_quant_iq(const __nv_bfloat16* __restrict__ iq,
+                                                               const int32_t* __restrict__ pos,
+                                                               const float* __restrict__ inv_freq, int R,
+                                                               uint8_t* __restrict__ q8, float* __restrict__ qs) {
   pdl_trigger();
-  pdl_wait();
-  const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = pos[q];
-  for (int h = warp * 8; h < warp * 8 + 8; ++h) {
-    const __nv_bfloat16* src = iq + ((size_t)q * 64 + h) * 128 + 4 * lane;
-    const uint2 raw = *reinterpret_cast<const uint2*>(src);
-    __nv_bfloat162 hv[2];
-    memcpy(hv, &raw, sizeof(raw));
-    float u[4];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i0 = 4 * lane + 2 * k;  // element pair (i0, i0 + 1)
-      const float2 x = __bfloat1622float2(hv[k]);
-      if (i0 >= 128 - R) {
-        float cs, sn;
-        rope_cs(p, inv_freq, (i0 - (128 - R)) >> 1, &cs, &sn);
-        const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(x.x, cs, -x.y * sn), fmaf(x.x, sn, x.y * cs));
-        const float2 y = __bfloat1622float2(r);
-        u[2 * k] = y.x;
-        u[2 * k + 1] = y.y;
-      } else {
-        u[2 * k] = x.x;
-        u[2 * k + 1] = x.y;
-      }
-    }
-    float scale;
-    const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
-    *reinterpret_cast<uint32_t*>(q8 + ((size_t)q * 64 + h) * 128 + 4 * lane) = packed;
-    if (lane == 0) qs[(size_t)q * 64 + h] = scale;
+  __shared__ float rc[64], rs[64];
+  const int q = blockIdx.x, h = blockIdx.y * kQuantHeads + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(iq + ((size_t)q * 64 + h) * 128 + 4 * lane));
+  if (threadIdx.x < R / 2) {
+    const int p = __ldg(pos + q);
+    sincosf(__fmul_rn((float)p, __ldg(inv_freq + threadIdx.x)), &rs[threadIdx.x], &rc[threadIdx.x]);
   }
+  __syncthreads();
+  const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  float u[4];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i0 = 4 * lane + 2 * k;  // element pair (i0, i0 + 1)
+    const float2 x = __bfloat1622float2(hv[k]);
+    if (i0 >= 128 - R) {
+      const int i = (i0 - (128 - R)) >> 1;
+      const float2 y = __bfloat1622float2(
+          __floats2bfloat162_rn(fmaf(x.x, rc[i], -x.y * rs[i]), fmaf(x.x, rs[i], x.y * rc[i])));
+      u[2 * k] = y.x;
+      u[2 * k + 1] = y.y;
+    } else {
+      u[2 * k] = x.x;
+      u[2 * k + 1] = x.y;
+    }
+  }
+  float scale;
+  const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
+  pdl_wait();
+  *reinterpret_cast<uint32_t*>(q8 + ((size_t)q * 64 + h) * 128 + 4 * lane) = packed;
+  if (lane == 0) qs[(size_t)q * 64 + h] = scale;
 }
 
 // gcu[b] = sum over sequences before b of ceil(T_b / 4) (T_b = cu[b+1] - cu[b], an inconsistent entry counted as
@@ -796,8 +800,8 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
     if (!pos || G != 1 || overlap || cu || !ws) return cudaErrorInvalidValue;
     auto* q8 = static_cast<uint8_t*>(ws);
     auto* qsc = reinterpret_cast<float*>(q8 + (size_t)Q * 64 * 128);
-    CSA_LAUNCH(k_quant_iq, dim3(Q), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(iq), pos, inv_freq, L.R, q8,
-               qsc);
+    CSA_LAUNCH(k_quant_iq, dim3(Q, 64 / kQuantHeads), dim3(32 * kQuantHeads), 0, s,
+               static_cast<const __nv_bfloat16*>(iq), pos, inv_freq, L.R, q8, qsc);
     CUtensorMap tk8;
     if (!make_tmap_2d_u8(&tk8, ikeys, (uint64_t)Bk * cap, 128, kFp8RowBytes, kTileRows)) return cudaErrorInvalidValue;
     a.q8 = q8;

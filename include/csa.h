@@ -458,6 +458,21 @@ csa_status csa_index_topk_static(const csa_layer* layer, const void* iq, const v
  * B == 0 enqueues nothing. */
 csa_status csa_advance_positions(int32_t* pos, int B, int by, void* stream);
 
+/* csa_index_rows_fp8 — index-key rows in the model dtype to fp8 index rows.
+ *
+ * src: n rows of Di = 128 bf16 values (an index pool written with index_fp8 = 0,
+ * or rows from elsewhere; device, 16-byte aligned, caller-owned, read only);
+ * dst: n rows of CSA_FP8_ROW_BYTES bytes (device, 16-byte aligned, caller-owned,
+ * written).  Each row becomes exactly the row csa_compress_append would store
+ * for it in a layer with index_fp8 = 1 (rotation, scale, E4M3 codes, zero
+ * padding; see CSA_FP8_ROW_BYTES), so a cache built in the model dtype can be
+ * carried over to the fp8 format.  Not a step of the method: a format
+ * conversion.  The layer must have index_fp8 = 1 (else CSA_ERR_UNSUPPORTED).
+ * Errors: CSA_ERR_ARG for n < 0 or n > 2^34, a null or misaligned pointer;
+ * CSA_ERR_CUDA if the launch fails.  n == 0 enqueues nothing.  One kernel on
+ * `stream`; src and dst must not overlap. */
+csa_status csa_index_rows_fp8(const csa_layer* layer, const void* src, long long n, void* dst, void* stream);
+
 /* Number of kernels this library has enqueued in this process (all calls,
  * all devices).  Diagnostic only: lets a caller count the launches of a region. */
 unsigned long long csa_kernel_launches(void);

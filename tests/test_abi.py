@@ -189,3 +189,12 @@ def test_fp8_index_rows_host_checks(lib):
     assert lib.csa_attend_prefill_varlen(ctypes.byref(L8), FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, 8, 4, FAKE, FAKE,
                                          FAKE, FAKE, 10, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, FAKE,
                                          None) == B.CSA_ERR_UNSUPPORTED
+
+
+def test_index_rows_fp8_host_checks(lib):
+    L8, L16 = _layer(index_fp8=1), _layer()
+    assert lib.csa_index_rows_fp8(ctypes.byref(L16), FAKE, 4, FAKE, None) == B.CSA_ERR_UNSUPPORTED
+    assert lib.csa_index_rows_fp8(ctypes.byref(L8), FAKE, -1, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_index_rows_fp8(ctypes.byref(L8), FAKE + 8, 4, FAKE, None) == B.CSA_ERR_ARG
+    assert lib.csa_index_rows_fp8(ctypes.byref(L8), FAKE, 4, None, None) == B.CSA_ERR_ARG
+    assert lib.csa_index_rows_fp8(ctypes.byref(L8), None, 0, None, None) == B.CSA_OK  # nothing to do

@@ -107,6 +107,26 @@ def test_fp8_queries_exact_at_position_zero():
     assert scales[1, 5] == 0 and not codes[1, 5].any()
 
 
+def test_index_rows_fp8_conversion():
+    """csa_index_rows_fp8 on seeded rows, with an all-zero row, rows scaled far up and down (E4M3 subnormal codes,
+    bf16 subnormal inputs) and a row with one dominant element (every other code small): bit-exact."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=2, ctx=4 * 300)
+    L = dataclasses.replace(G.lib_layer(cfg), index_fp8=True)
+    src = csa_synth.synth_cache(cfg, 300).ikeys.clone()  # [2, 300, 128] seeded N(0,1), bf16
+    src[0, 0] = 0
+    src[0, 1] *= 1e30
+    src[0, 2] *= 1e-38
+    src[1, 3] *= 1e-3
+    src[1, 3, 17] = 1e3
+    dst = torch.zeros(2, 300, ROW, dtype=torch.uint8, device="cuda")
+    csa.index_rows_fp8(L, G.dev(src), dst)
+    torch.cuda.synchronize()
+    _check_rows_exact(dst.view(-1, ROW), src.view(-1, 128), "converted")
+    codes, scales = _codes_scales(dst[0, 0])
+    assert scales == 0 and not codes.any()
+
+
 # (tokens compressed from an empty cache before the decode steps, decode steps): 1023 tokens leave 255 rows
 # (dense: every visible row is selected), 4095 leave 1023 rows (sparse: 512 of 1023 .. 1024).
 CASES = {"dense": (1023, 6), "sparse": (4095, 6)}
@@ -140,6 +160,9 @@ def test_fp8_index_rows_and_selection(case):
     for b in range(cfg.B):
         _check_rows_exact(s8.ikeys[b, :n0], s16.ikeys[b, :n0], f"chunk, sequence {b}")
     assert torch.equal(s8.pool, s16.pool)
+    conv = torch.zeros(cfg.B, n0, ROW, dtype=torch.uint8, device="cuda")
+    csa.index_rows_fp8(L8, s16.ikeys[:, :n0].contiguous(), conv)
+    assert torch.equal(conv, s8.ikeys[:, :n0]), "csa_index_rows_fp8 differs from the compress kernels' fp8 rows"
     mism, heads = 0, 0
     for k in range(steps):
         si = csa_synth.step_inputs(cfg.replace(cid=cfg.cid + 900), k + 1)
