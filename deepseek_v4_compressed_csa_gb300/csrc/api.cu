@@ -32,7 +32,8 @@ csa_status make_dims(const csa_layer* l, Dims* d) {
   if (l->rollback < 0 || l->rollback > (1 << 20)) return CSA_ERR_ARG;
   if (l->index_fp8 != 0 && l->index_fp8 != 1) return CSA_ERR_ARG;
   // (the index pool is told apart from the attention pool by its row length)
-  if (l->index_fp8 && (l->ratio != 4 || l->dtype != CSA_BF16 || l->Hi != 64 || l->Di != 128 || l->D == l->Di))
+  if (l->index_fp8 && (l->ratio != 4 || l->dtype != CSA_BF16 || l->Hi != 64 || l->Di != 128 || l->D == l->Di ||
+                       l->R > 64 || l->R % 8))
     return CSA_ERR_UNSUPPORTED;
   d->dtype = l->dtype;
   d->H = l->H; d->D = l->D; d->R = l->R; d->W = l->W; d->ratio = l->ratio;

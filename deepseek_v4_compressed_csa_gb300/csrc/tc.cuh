@@ -20,6 +20,30 @@
 namespace csa {
 namespace tc {
 
+// Read-only global loads issued where they are written.  An ordinary non-coherent load (__ldg) may be moved by
+// the compiler to its first use, past barriers and the programmatic-launch wait, and a batch of them then runs as
+// one round trip per use; these stay in place, so a batch is in flight together.
+__device__ __forceinline__ uint4 ld_nc_v4_now(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_nc_v2_now(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32_now(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_nc_u16_now(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
 // error bit for a wait that ran out of time (kept apart from the CSA_DEV_* API bits)
 constexpr int kErrTimeout = 1 << 16;
 
@@ -310,8 +334,9 @@ __device__ __forceinline__ uint32_t elect_one_lane() { return (threadIdx.x & 31)
 // box of box_rows x 64 columns and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
                        uint32_t box_rows);
-// The same for a byte matrix: boxes of 128 bytes x box_rows rows, 128-byte swizzle.
+// The same for a byte matrix: boxes of box_cols bytes (a multiple of 16; at most 128 with the 128-byte swizzle,
+// 256 without) x box_rows rows.
 bool make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
-                     uint32_t box_rows);
+                     uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 }  // namespace csa

@@ -51,8 +51,14 @@ struct IdxCfg {
   static constexpr int kOffK = kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights
   static constexpr int kOffRope = kOffW + kQSlots * N * 4;     // [G][32] cos, [G][32] sin
-  static constexpr int kOffBars = kOffRope + G * 64 * 4;
-  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 2 * kAcc + 1;
+  // fp8: the key rows' scales (bytes 128-143 of each row, 16 B a row) by a second TMA copy per tile into a ring
+  // of kStages + kAcc slots: the producer refills a slot only once the epilogue is done with it (it has waited for
+  // the MMA kStages tiles back, which waited for the epilogue kAcc tiles before that)
+  static constexpr int kScaleSlots = kFp8 ? kStages + kAcc : 0;
+  static constexpr int kScaleBytes = kTileRows * 16;
+  static constexpr int kOffS = kOffRope + G * 64 * 4;
+  static constexpr int kOffBars = kOffS + kScaleSlots * kScaleBytes;
+  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 2 * kAcc + 1 + kScaleSlots;
   static constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
   // warps: 0 TMA, 1 MMA, 2 .. 2 + kEpiWarps - 1 epilogue, then two query-block warps.  A prefill tile has four
   // queries' columns to reduce: eight epilogue warps, two per TMEM lane quarter, take two queries each.
@@ -83,11 +89,9 @@ struct IdxArgs {
   // selection stage
   __nv_bfloat16* qr_out;  // [Q, 64, 128]
   float* w_out;           // [Q, 64]
-  // fp8 index keys (instance kFp8): the quantised queries [Q, 64, 128] codes and [Q, 64] scales, and the key rows
-  // (kFp8RowBytes each: 128 codes, then the fp32 scale) for the scales
+  // fp8 index keys (instance kFp8): the quantised queries, q8 [Q, 64, 128] codes and qs [Q, 64] scales
   const uint8_t* q8;
   const float* qs;
-  const uint8_t* keys8;
 };
 
 __device__ __forceinline__ int idx_seq(const IdxArgs& a, int q) {
@@ -205,7 +209,7 @@ struct Items {
 template <int G, bool kOverlap, bool kFp8 = false>
 __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     k_tc_index_scores(const __grid_constant__ CUtensorMap tm_keys, const __grid_constant__ CUtensorMap tm_q,
-                      IdxArgs a) {
+                      const __grid_constant__ CUtensorMap tm_ks, IdxArgs a) {
   using C = IdxCfg<G, kFp8>;
   constexpr int N = C::N;
   pdl_trigger();
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   float* wbuf = reinterpret_cast<float*>(smem + C::kOffW);
   float* rcos = reinterpret_cast<float*>(smem + C::kOffRope);
   float* rsin = rcos + G * 32;
+  uint8_t* sbuf = smem + C::kOffS;  // fp8: [kScaleSlots][128 rows][16 B], the row's scale first
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* full = bars;                        // [kStages] key tile landed
   uint64_t* empty = full + C::kStages;          // [kStages] key tile consumed
@@ -226,7 +231,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   uint64_t* acc_empty = acc_full + C::kAcc;     // [kAcc]
   uint64_t* drain = acc_empty + C::kAcc;
   uint64_t* q_loaded = drain + 1;               // [kQSlots] G = 4: the query block's TMA copy landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_loaded + C::kQSlots);
+  uint64_t* s_full = q_loaded + C::kQSlots;     // [kScaleSlots] fp8: a tile's key scales landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + C::kScaleSlots);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -244,6 +250,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       tc::mbar_init(&acc_empty[i], 32 * C::kEpiWarps);
     }
     tc::mbar_init(drain, 1);
+    for (int i = 0; i < C::kScaleSlots; ++i) tc::mbar_init(&s_full[i], 1);
     tc::fence_mbar_init();
   }
   // Query-block warps: everything the first query block needs (positions, frequencies, head weights and the first
@@ -259,6 +266,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   struct Pre {
     uint4 raw[kBatch];
     float wv[G];
+    float qsv;  // fp8: the scale of head pt
     float th_freq;
     int p;
   };
@@ -273,17 +281,18 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
     }
   };
-  auto load_first = [&](int g, Pre& pre) {
-    if constexpr (kFp8) {
+  // fp8 (G = 1): group g's codes and head pt's scale, the preceding kernel's output (so after the wait); loads
+  // that stay where they are written (the second group's must not be moved behind the key stream)
+  auto load_codes = [&](int g, Pre& pre) {
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int e = pt + b * kPrepThreads;
-        const int q = g * G + (e >> 9), h = (e >> 3) & 63, c = e & 7;
-        pre.raw[b] = (e < kChunks && q < a.Q)
-                         ? __ldg(reinterpret_cast<const uint4*>(a.q8 + ((size_t)q * 64 + h) * 128 + c * 16))
-                         : make_uint4(0, 0, 0, 0);
-      }
-    } else if constexpr (G != 4) {
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = pt + b * kPrepThreads, h = (e >> 3) & 63, c = e & 7;
+      pre.raw[b] = tc::ld_nc_v4_now(a.q8 + ((size_t)g * 64 + h) * 128 + c * 16);
+    }
+    pre.qsv = __uint_as_float(tc::ld_nc_u32_now(a.qs + (size_t)g * 64 + pt));
+  };
+  auto load_first = [&](int g, Pre& pre) {
+    if constexpr (!kFp8 && G != 4) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int e = pt + b * kPrepThreads;
@@ -297,11 +306,9 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     for (int i = 0; i < G; ++i) {
       const int e = pt + i * kPrepThreads, q = grp_query<G>(a, g, e / 64);
       pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
-      // fp8: the head's query scale and the 1/128 of the unnormalised rotation go into its weight
-      if constexpr (kFp8) pre.wv[i] *= q >= 0 ? __ldg(a.qs + (size_t)q * 64 + (e & 63)) * 0.0078125f : 0.f;
     }
     // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
-    pre.th_freq = __ldg(a.inv_freq + (pt & 31));
+    pre.th_freq = (pt & 31) < a.R / 2 ? __ldg(a.inv_freq + (pt & 31)) : 0.f;
     const int q0 = pt < G * 32 ? grp_query<G>(a, g, pt / 32) : -1;
     pre.p = q0 >= 0 ? idx_qpos(a, q0) : 0;
   };
@@ -321,7 +328,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     i_begin = min(a.n_items, item_at(x0));
     i_end = blockIdx.x + 1 == gridDim.x ? a.n_items : min(a.n_items, item_at(x1));
   }
-  Pre pre_a;
+  Pre pre_a, pre_b;  // pre_b: fp8, the range's second group
+  bool g1_loaded = false;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
   // The first query block is requested before the wait (step inputs), except with a group table or fp8 queries,
@@ -335,9 +343,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       tc::fence_mbar_init();
       tc::tma_prefetch(&tm_q);
     }
-    if (!kFp8 && (G != 4 || !a.gcu)) {
+    if (G != 4 || !a.gcu) {
       if (G == 4) issue_q(g0);
       load_first(g0, pre_a);
+      if (kFp8 && g1 >= 0) load_first(g1, pre_b);  // fp8: the second group's weights and position too
     }
   }
   // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
@@ -345,9 +354,16 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
   // a projection kernel that lets successors start only once all earlier work is complete.)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
-  // fp8: the quantised queries and their scales are the preceding kernel's output
+  // fp8: the quantised queries and their scales are the preceding kernel's output; the codes of the range's first
+  // two groups are requested now, before the key stream starts (a load issued behind the stream took ~10 us)
   if constexpr (kFp8) {
-    if (warp >= C::kPrepWarp0 && i_begin < i_end) load_first(g0, pre_a);
+    if (warp >= C::kPrepWarp0 && i_begin < i_end) {
+      load_codes(g0, pre_a);
+      if (g1 >= 0) {
+        load_codes(g1, pre_b);
+        g1_loaded = true;
+      }
+    }
   }
   if constexpr (G == 4) {
     if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) {
@@ -374,9 +390,12 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     tc::named_bar(4, 32 + kPrepThreads);
     if (lane == 0) {
       tc::tma_prefetch(&tm_keys);
+      if constexpr (kFp8) tc::tma_prefetch(&tm_ks);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, par_last = 0;  // per stage (bit s): a load was issued; parity of its last phase
+      int n_items = 0;                  // fp8: items issued (scale slot n_items % kScaleSlots)
+      uint32_t s_used = 0, s_par = 0;   // fp8: per scale slot, as used / par_last
       Items<G, kOverlap> itr;
       for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
         const int g = itr.g, t = itr.t;
@@ -388,6 +407,15 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
         tc::tma_load_2d(kbuf + stage * C::kTileBytes, &tm_keys, &full[stage], 0, krow);
         if constexpr (!kFp8)
           tc::tma_load_2d(kbuf + stage * C::kTileBytes + C::kTileBytes / 2, &tm_keys, &full[stage], 64, krow);
+        if constexpr (kFp8) {
+          const int ss = n_items % C::kScaleSlots;
+          const uint32_t sp = (uint32_t)(n_items / C::kScaleSlots) & 1;
+          tc::mbar_arrive_expect_tx(&s_full[ss], C::kScaleBytes);
+          tc::tma_load_2d(sbuf + ss * C::kScaleBytes, &tm_ks, &s_full[ss], 128, krow);
+          s_used |= 1u << ss;
+          s_par = (s_par & ~(1u << ss)) | (sp << ss);
+          ++n_items;
+        }
         used |= 1u << stage;
         par_last = (par_last & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -395,6 +423,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       // every load issued must land before the CTA may exit
       for (int s = 0; s < C::kStages; ++s)
         if (((used >> s) & 1) && !tc::mbar_wait(&full[s], (par_last >> s) & 1)) failed = true;
+      for (int s = 0; s < C::kScaleSlots; ++s)
+        if (((s_used >> s) & 1) && !tc::mbar_wait(&s_full[s], (s_par >> s) & 1)) failed = true;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -450,6 +480,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     int cur_g = -1, k = -1, acc = 0;
     uint32_t acc_par = 0;  // bit i: parity of accumulator i's uses so far
     int nv[G], qix[G];
+    int n_done = 0;  // fp8: items taken (scale slot n_done % kScaleSlots)
     Items<G, kOverlap> itr;
     for (bool more = itr.start(a, i_begin, i_end); more; more = itr.advance(a)) {
       const int g = itr.g, t = itr.t;
@@ -464,11 +495,13 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
         }
       }
       const int j = t * kTileRows + row;
-      float kscale = 1.f;  // fp8: the key row's scale, requested before the accumulator wait
-      if constexpr (kFp8)
-        kscale = j < nv[0] ? __ldg(reinterpret_cast<const float*>(
-                                 a.keys8 + ((size_t)idx_seq(a, qix[0]) * a.cap + j) * kFp8RowBytes + 128))
-                           : 0.f;
+      float kscale = 1.f;  // fp8: the key row's scale, from the tile's scale slot
+      if constexpr (kFp8) {
+        const int ss = n_done % C::kScaleSlots;
+        if (!tc::mbar_wait(&s_full[ss], (uint32_t)(n_done / C::kScaleSlots) & 1)) { failed = true; break; }
+        kscale = *reinterpret_cast<const float*>(sbuf + ss * C::kScaleBytes + row * 16);
+        ++n_done;
+      }
       if (!tc::mbar_wait(&acc_full[acc], (acc_par >> acc) & 1)) { failed = true; break; }
       tc::fence_after_sync();
       const float4* w4 = reinterpret_cast<const float4*>(wbuf + (k % C::kQSlots) * N);
@@ -583,8 +616,12 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       } else {
         tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
       }
-      Pre& pre = pre_a;
-      if (g != g0) load_first(g, pre_a);  // a later group: request it now
+      const bool from_b = kFp8 && g == g1 && g1_loaded;  // fp8: the second group, requested after the wait
+      Pre& pre = from_b ? pre_b : pre_a;
+      if (g != g0 && !from_b) {  // a later group: request it now
+        load_first(g, pre_a);
+        if constexpr (kFp8) load_codes(g, pre_a);
+      }
       if constexpr (G == 4) {
         if (q_pending != g) {
           // the slot is free (first group, or the previous group's MMAs retired); a copy of a group without
@@ -594,14 +631,14 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
           q_pending = g;
         }
       }
-      // RoPE table (G x 32 entries) from the preloaded position and frequency
-      for (int e = pt; e < G * 32; e += kPrepThreads) {
+      // RoPE table (G x 32 entries) from the preloaded position and frequency (fp8: roped before quantisation)
+      for (int e = pt; !kFp8 && e < G * 32; e += kPrepThreads) {
         int p = pre.p;
         float f = pre.th_freq;
         if (e != pt) {  // G = 4: the second entry of this thread
           const int q = grp_query<G>(a, g, e / 32);
           p = q >= 0 ? idx_qpos(a, q) : 0;
-          f = __ldg(a.inv_freq + (e & 31));
+          f = (e & 31) < a.R / 2 ? __ldg(a.inv_freq + (e & 31)) : 0.f;
         }
         sincosf(__fmul_rn((float)p, f), &rsin[e], &rcos[e]);
       }
@@ -642,7 +679,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       }
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const float w = pre.wv[i] * a.wscale;
+        // fp8: the head's query scale and the 1/128 of the unnormalised rotation go into its weight
+        const float w = (kFp8 ? pre.wv[i] * (pre.qsv * 0.0078125f) : pre.wv[i]) * a.wscale;
         wbuf[slot * N + pt + i * kPrepThreads] = w;
         const int e = pt + i * kPrepThreads;
         if (kOverlap && g * G + e / 64 < a.Q) a.w_out[(size_t)(g * G) * 64 + e] = w;
@@ -740,7 +778,10 @@ __global__ void __launch_bounds__(1024) k_varlen_groups(const int32_t* __restric
 
 }  // namespace
 
-bool tc_index_supported(const Dims& L) { return L.dtype == CSA_BF16 && L.Hi == 64 && L.Di == 128; }
+// (RoPE on whole 16-byte chunks of a head row, with one 32-entry table per query)
+bool tc_index_supported(const Dims& L) {
+  return L.dtype == CSA_BF16 && L.Hi == 64 && L.Di == 128 && L.R <= 64 && L.R % 8 == 0;
+}
 
 size_t tc_index_ws(const Dims& L, int Q) {
   (void)L;
@@ -802,28 +843,31 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
     auto* qsc = reinterpret_cast<float*>(q8 + (size_t)Q * 64 * 128);
     CSA_LAUNCH(k_quant_iq, dim3(Q, 64 / kQuantHeads), dim3(32 * kQuantHeads), 0, s,
                static_cast<const __nv_bfloat16*>(iq), pos, inv_freq, L.R, q8, qsc);
-    CUtensorMap tk8;
-    if (!make_tmap_2d_u8(&tk8, ikeys, (uint64_t)Bk * cap, 128, kFp8RowBytes, kTileRows)) return cudaErrorInvalidValue;
+    // the key rows' codes (bytes 0-127, swizzled) and scales (bytes 128-143) by two tensor maps
+    CUtensorMap tk8, tks;
+    if (!make_tmap_2d_u8(&tk8, ikeys, (uint64_t)Bk * cap, kFp8RowBytes, kFp8RowBytes, 128, kTileRows, true) ||
+        !make_tmap_2d_u8(&tks, ikeys, (uint64_t)Bk * cap, kFp8RowBytes, kFp8RowBytes, 16, kTileRows, false))
+      return cudaErrorInvalidValue;
     a.q8 = q8;
     a.qs = qsc;
-    a.keys8 = static_cast<const uint8_t*>(ikeys);
     constexpr int smem = IdxCfg<1, true>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, false, true>, dim3(grid), dim3(IdxCfg<1, true>::kThreads), smem, s, tk8, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<1, false, true>, dim3(grid), dim3(IdxCfg<1, true>::kThreads), smem, s, tk8, tq, tks,
+               a);
     return cudaGetLastError();
   }
   if (G == 1 && overlap) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<1, true>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, tk, a);
   } else if (G == 1) {
     constexpr int smem = IdxCfg<1>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tq, tk, a);
   } else {
     constexpr int smem = IdxCfg<4>::kSmem;
     cudaFuncSetAttribute(k_tc_index_scores<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(IdxCfg<4>::kThreads), smem, s, tk, tq, a);
+    CSA_LAUNCH(k_tc_index_scores<4, false>, dim3(grid), dim3(IdxCfg<4>::kThreads), smem, s, tk, tq, tk, a);
   }
   return cudaGetLastError();
 }

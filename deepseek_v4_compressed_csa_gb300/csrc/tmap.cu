@@ -32,7 +32,7 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
 }
 
 bool make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
-                     uint32_t box_rows) {
+                     uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -44,15 +44,16 @@ bool make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u) || box_rows == 0 || box_rows > 256 ||
-      cols < 128)
+      box_cols == 0 || (box_cols & 15u) || box_cols > (swizzle128 ? 128u : 256u) || cols < box_cols)
     return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
-  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -107,7 +107,8 @@ enum {
  *   index_fp8: 0 (index keys in the model dtype) or 1 (fp8 index rows of
  *     CSA_FP8_ROW_BYTES: the index pool is then a [B, cap, 144] byte tensor that
  *     csa_compress_append / _pair write and csa_index_topk reads; ratio 4, bf16,
- *     Hi = 64, Di = 128 only, else CSA_ERR_UNSUPPORTED; the other index calls
+ *     Hi = 64, Di = 128 (D != 128), R <= 64 and a multiple of 8 only, else
+ *     CSA_ERR_UNSUPPORTED; the other index calls
  *     return CSA_ERR_UNSUPPORTED with it). */
 typedef struct {
   int dtype;

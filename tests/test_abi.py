@@ -176,7 +176,7 @@ def test_fp8_index_rows_host_checks(lib):
     assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=1)), B.OP_INDEX_TOPK, 32, 1, 8400,
                                   ctypes.byref(n)) == B.CSA_OK
     assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=2)), 0, 1, 1, 1, ctypes.byref(n)) == B.CSA_ERR_ARG
-    for bad in (dict(ratio=128), dict(dtype=B.CSA_F32), dict(Hi=32), dict(Di=64, R=64), dict(D=128)):
+    for bad in (dict(ratio=128), dict(dtype=B.CSA_F32), dict(Hi=32), dict(Di=64, R=64), dict(D=128), dict(R=72)):
         assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=1, **bad)), 0, 1, 1, 1,
                                       ctypes.byref(n)) == B.CSA_ERR_UNSUPPORTED, bad
     L8 = _layer(index_fp8=1, rollback=8)
