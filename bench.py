@@ -42,7 +42,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum, every kernel captured cold) of one decode
 # layer-step of the headline workload and of one prefill chunk, with the hash of the kernel sources the counters
 # were taken on (csrc_digest()); the bench reports them only while the sources still hash the same.
-TRAFFIC = {"csrc_sha256": "49c6546013356468", "decode_layer_step_bytes": 116_683_000, "prefill_chunk_bytes": 1_234_840_000,
+TRAFFIC = {"csrc_sha256": "8205bc1683e3de69", "decode_layer_step_bytes": 116_686_000,
+           "decode_fp8_layer_step_bytes": 87_500_000, "prefill_chunk_bytes": 1_234_392_000,
            "profile": "profiles/traffic_decode_b32_ctx32k_and_prefill_t4096.md"}
 
 
@@ -793,6 +794,7 @@ def decode_config_line(csa, csa_synth, cid: int, dev, flush, steps: int, warmup:
             "us_per_layer_step_p10_p50_p90": [round(1e3 * x, 2) for x in _percentiles(per)],
             "step_algorithmic_bytes": int(nb["total"]), "achieved_gbs": round(gbs, 1),
             "hbm_frac": round(gbs / hbm, 4), "layers_per_step": nl, "steps": steps,
+            "dram_traffic_bytes_per_layer_step": _traffic("decode_fp8_layer_step_bytes", 1) if index_fp8 else None,
             "cache": ("compressed from 8192 seeded hidden tokens by the library" if cid == 2 else
                       "synthetic rows drawn directly (seeded N(0,1))" + (
                           "; index rows converted to fp8 rows by csa_index_rows_fp8" if index_fp8 else ""))}
@@ -844,7 +846,7 @@ def run_ours(args):
     total_steps = args.warmup + args.steps + args.e2e_steps + 2 * (args.warmup + n_single) + 24
     cap = cfg.ctx // cfg.ratio + total_steps // cfg.ratio + 8
     ms = ModelStep(cfg, cap, n_inputs=4, device=dev, n_layers=nl, pair=not args.two_streams,
-                   one_stream_overlap=args.indexer == "overlap")
+                   one_stream_overlap=args.indexer == "overlap", index_fp8=args.index_fp8)
     wl = ms.layers[0]
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -981,7 +983,8 @@ def run_ours(args):
     hbm, tflops, peak_src = _peaks()
     ms_per_step = total_ms / (args.steps * nl)  # per layer-step
     value = world * args.steps * nl / (total_ms / 1e3)
-    nb = step_bytes(cfg, 0.5 * (n_start + n_end))
+    nb = step_bytes(cfg, 0.5 * (n_start + n_end), args.index_fp8)
+    tkey = "decode_fp8_layer_step_bytes" if args.index_fp8 else "decode_layer_step_bytes"
     step_avg_s = ms_per_step / 1e3
     result = None
     if rank == 0:
@@ -1019,6 +1022,7 @@ def run_ours(args):
                            "csa_attend_decode, every kernel after its predecessor by programmatic launch; "
                            "csa_advance_positions after the last layer"),
                 "indexer": args.indexer,
+                "index_fp8": bool(args.index_fp8),
                 "prefill": prefill,
                 "prefill_varlen": prefill_varlen,
                 "other_decode_workloads": others,
@@ -1033,10 +1037,9 @@ def run_ours(args):
                 "bound": "hbm",
                 "achieved": round(nb["total"] / step_avg_s / 1e9, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(nb["total"] / step_avg_s / 1e9 / hbm, 4),
-                "traffic": _traffic("decode_layer_step_bytes", nl),
+                "traffic": _traffic(tkey, nl),
                 "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum summed over one layer-step's "
-                                   f"kernels x {nl} layers ({TRAFFIC['profile']})" if _traffic(
-                                       "decode_layer_step_bytes", nl) else
+                                   f"kernels x {nl} layers ({TRAFFIC['profile']})" if _traffic(tkey, nl) else
                                    "null: no counters taken on the current kernel sources"),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6800 GB/s", "avg_launch_ms": round(total_ms / args.steps, 5),
@@ -1265,6 +1268,9 @@ def main():
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the config-2 (B = 1, 8K) and config-4 (ratio 128, B = 16, 256K) decode lines")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one instead of CUDA graphs")
+    ap.add_argument("--index-fp8", action="store_true",
+                    help="the headline workload with fp8 index rows (diagnostic and profiling; the default line and "
+                         "its other_decode_workloads entry are unchanged)")
     ap.add_argument("--layers", type=int, default=8,
                     help="layers per model step (each its own weights and caches), one CUDA graph per step")
     ap.add_argument("--two-streams", action="store_true",
