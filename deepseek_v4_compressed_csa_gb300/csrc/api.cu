@@ -276,7 +276,6 @@ csa_status csa_attend_prefill_chunk(const csa_layer* layer, const void* q, const
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
-  if (L.ikey_fp8) return CSA_ERR_UNSUPPORTED;  // fp8 index rows are scored for decode queries only
   if (T < 1 || T > 16384 || pos0 < 0 || cap < 1) return CSA_ERR_ARG;
   if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
       !dev_tensor(inv_freq) || !dev_tensor(out))
@@ -340,8 +339,7 @@ csa_status csa_attend_prefill_varlen(const csa_layer* layer, const void* q, cons
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
   if (!varlen_args_ok(B, cu_seqlens, N, T_max) || N > 16384 || cap < 1) return CSA_ERR_ARG;
-  if (!tc_attend_supported(L) || (L.has_indexer() && !tc_index_supported(L)) || L.ikey_fp8)
-    return CSA_ERR_UNSUPPORTED;
+  if (!tc_attend_supported(L) || (L.has_indexer() && !tc_index_supported(L))) return CSA_ERR_UNSUPPORTED;
   if (!dev_tensor(q) || !dev_tensor(kv_new) || !dev_i32(sink) || !dev_tensor(window) || !dev_tensor(pool) ||
       !dev_tensor(inv_freq) || !dev_tensor(out))
     return CSA_ERR_ARG;
@@ -376,7 +374,7 @@ csa_status csa_index_topk_verify(const csa_layer* layer, const void* iq, const v
   Dims L;
   csa_status st = make_dims(layer, &L);
   if (st != CSA_OK) return st;
-  if (!L.has_indexer() || L.ikey_fp8) return CSA_ERR_UNSUPPORTED;
+  if (!L.has_indexer()) return CSA_ERR_UNSUPPORTED;
   if (B < 1 || T < 1 || T > 64 || cap < 1 || (long long)B * T > (1 << 20)) return CSA_ERR_ARG;
   if (!dev_tensor(iq) || !dev_i32(iw) || !dev_tensor(ikeys) || !dev_tensor(inv_freq)) return CSA_ERR_ARG;
   if (!dev_i32(n_rows) || !dev_i32(pos) || !dev_i32(sel) || !dev_i32(n_sel) || !dev_i32(err)) return CSA_ERR_ARG;

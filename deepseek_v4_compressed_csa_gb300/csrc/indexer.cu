@@ -654,19 +654,12 @@ static cudaError_t index_t(const Dims& L, const void* iq, const void* iw, int Q,
                            const int32_t* n_rows, const int32_t* pos, int pos0, const int32_t* cu,
                            const float* inv_freq, int32_t* sel, int32_t* n_sel, const IndexWs& ws, int32_t* err,
                            cudaStream_t s) {
-  if (L.ikey_fp8) {
-    // fp8 index rows: single decode queries (one per sequence) on the tensor-core path only
-    if (!pos || pos0 > 1 || cu || !tc_index_supported(L)) return cudaErrorNotSupported;
-    cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, Q, cap, n_rows, pos, 0, inv_freq, ws.qr, ws.scores,
-                                           err, s, false, nullptr, true);
-    if (e != cudaSuccess) return e;
-    return launch_topk(L, ws.scores, cap, n_rows, pos, 0, nullptr, Q, sel, n_sel, s);
-  }
+  if (L.ikey_fp8 && !tc_index_supported(L)) return cudaErrorNotSupported;  // fp8 rows: tensor-core scan only
   if (tc_index_supported(L)) {
     // sequences holding the keys: one per query group of a verify block, or the varlen batch's count (pos0)
     const int Bk = cu ? pos0 : (pos ? Q / max(1, pos0) : 1);
     cudaError_t e = launch_tc_index_scores(L, iq, iw, Q, ikeys, Bk, cap, n_rows, pos, pos0, inv_freq, ws.qr,
-                                           ws.scores, err, s, false, cu);
+                                           ws.scores, err, s, false, cu, L.ikey_fp8 != 0);
     if (e != cudaSuccess) return e;
     return launch_topk(L, ws.scores, cap, n_rows, pos, pos0, cu, Q, sel, n_sel, s);
   }

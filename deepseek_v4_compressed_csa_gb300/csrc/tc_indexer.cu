@@ -46,7 +46,7 @@ struct IdxCfg {
   static constexpr int kQBytes = N * kRowBytes;  // one query block (bf16: 2 boxes of N rows x 128 B)
   static constexpr int kQSlots = G == 1 ? 2 : 1;
   // decode: five 32 KB key tiles in flight (measured best of 4-6); fp8: the same bytes in eight 16 KB tiles
-  static constexpr int kStages = G == 1 ? (kFp8 ? 8 : 5) : 4;
+  static constexpr int kStages = G == 1 ? (kFp8 ? 8 : 5) : (kFp8 ? 8 : 4);
   static constexpr int kAcc = G == 1 ? 4 : 2;    // TMEM accumulators of N columns
   static constexpr int kOffK = kQSlots * kQBytes;
   static constexpr int kOffW = kOffK + kStages * kTileBytes;   // [kQSlots][N] head weights
@@ -89,9 +89,11 @@ struct IdxArgs {
   // selection stage
   __nv_bfloat16* qr_out;  // [Q, 64, 128]
   float* w_out;           // [Q, 64]
-  // fp8 index keys (instance kFp8): the quantised queries, q8 [Q, 64, 128] codes and qs [Q, 64] scales
+  // fp8 index keys (instance kFp8): the quantised queries, q8 [Q, 64, 128] codes and qs [Q, 64] scales; G = 4 takes
+  // the head weights with the scale and the 1/128 folded in, w8 [Q, 64] (iw qs / 128)
   const uint8_t* q8;
   const float* qs;
+  const float* w8;
 };
 
 __device__ __forceinline__ int idx_seq(const IdxArgs& a, int q) {
@@ -278,7 +280,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       const int q0 = grp_first<G>(a, g, cnt);
       tc::mbar_arrive_expect_tx(&q_loaded[0], C::kQBytes);
       tc::tma_load_2d(qbuf, &tm_q, &q_loaded[0], 0, q0 * 64);
-      tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
+      if constexpr (!kFp8)  // fp8: one 128-byte box of codes per head row
+        tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
     }
   };
   // fp8 (G = 1): group g's codes and head pt's scale, the preceding kernel's output (so after the wait); loads
@@ -305,7 +308,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int e = pt + i * kPrepThreads, q = grp_query<G>(a, g, e / 64);
-      pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
+      if constexpr (kFp8 && G == 4)  // the folded weights, the preceding kernel's output (load_first runs after the wait)
+        pre.wv[i] = q >= 0 ? a.w8[(size_t)q * 64 + (e & 63)] : 0.f;
+      else
+        pre.wv[i] = q >= 0 ? __bfloat162float(a.iw[(size_t)q * 64 + (e & 63)]) : 0.f;
     }
     // RoPE table entry e = pt (G = 1: threads 0-31) or pt, pt + 64 (G = 4: two per thread, see below)
     pre.th_freq = (pt & 31) < a.R / 2 ? __ldg(a.inv_freq + (pt & 31)) : 0.f;
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       tc::fence_mbar_init();
       tc::tma_prefetch(&tm_q);
     }
-    if (G != 4 || !a.gcu) {
+    if (G != 4 || !(a.gcu || kFp8)) {
       if (G == 4) issue_q(g0);
       load_first(g0, pre_a);
       if (kFp8 && g1 >= 0) load_first(g1, pre_b);  // fp8: the second group's weights and position too
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   // fp8: the quantised queries and their scales are the preceding kernel's output; the codes of the range's first
   // two groups are requested now, before the key stream starts (a load issued behind the stream took ~10 us)
-  if constexpr (kFp8) {
+  if constexpr (kFp8 && G == 1) {
     if (warp >= C::kPrepWarp0 && i_begin < i_end) {
       load_codes(g0, pre_a);
       if (g1 >= 0) {
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     }
   }
   if constexpr (G == 4) {
-    if (a.gcu && warp >= C::kPrepWarp0 && i_begin < i_end) {
+    if ((a.gcu || kFp8) && warp >= C::kPrepWarp0 && i_begin < i_end) {
       issue_q(g0);
       load_first(g0, pre_a);
     }
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       Pre& pre = from_b ? pre_b : pre_a;
       if (g != g0 && !from_b) {  // a later group: request it now
         load_first(g, pre_a);
-        if constexpr (kFp8) load_codes(g, pre_a);
+        if constexpr (kFp8 && G == 1) load_codes(g, pre_a);
       }
       if constexpr (G == 4) {
         if (q_pending != g) {
@@ -645,10 +651,11 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       tc::named_bar(3, kPrepThreads);
       uint8_t* qb = qbuf + slot * C::kQBytes;
       if constexpr (G == 4) {
-        // RoPE in place on the copied block: 16-byte chunks c >= (128 - R) / 8 of each of the N head rows
+        // RoPE in place on the copied block: 16-byte chunks c >= (128 - R) / 8 of each of the N head rows (fp8:
+        // the codes were roped before quantisation)
         if (tc::named_bar_any(3, kPrepThreads, !wait_q())) { failed = true; break; }
         const int c0 = (128 - a.R) / 8, nrc = 16 - c0;
-        for (int e = pt; e < N * nrc; e += kPrepThreads) {
+        for (int e = pt; !kFp8 && e < N * nrc; e += kPrepThreads) {
           const int row = e / nrc, c = c0 + e % nrc, qq = row >> 6;
           uint4* slot_p =
               reinterpret_cast<uint4*>(qb + (c >> 3) * (C::kQBytes / 2) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
@@ -680,7 +687,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         // fp8: the head's query scale and the 1/128 of the unnormalised rotation go into its weight
-        const float w = (kFp8 ? pre.wv[i] * (pre.qsv * 0.0078125f) : pre.wv[i]) * a.wscale;
+        // (G = 4: the folded weights already hold them)
+        const float w = (kFp8 && G == 1 ? pre.wv[i] * (pre.qsv * 0.0078125f) : pre.wv[i]) * a.wscale;
         wbuf[slot * N + pt + i * kPrepThreads] = w;
         const int e = pt + i * kPrepThreads;
         if (kOverlap && g * G + e / 64 < a.Q) a.w_out[(size_t)(g * G) * 64 + e] = w;
@@ -703,21 +711,32 @@ int g_num_sms = 0;
 // fp8 index queries (the optional key format): query q's head h, RoPE at pos[q] as for the bf16 scores, rounded
 // to bf16, rotated by the unnormalised 128-point Walsh-Hadamard transform in fp32 (butterflies of span 1, 2, ..,
 // 64 in that order), scaled by amax / 448 and rounded to E4M3 (nearest even, saturating): q8 [Q, 64, 128] codes,
-// qs [Q, 64] scales.  Block (q, quarter): 16 warps, one head each (heads 16 quarter ..); lane l holds elements
-// 4l .. 4l + 3.  Everything up to the stores reads step inputs only (queries, positions, frequencies), so it runs
+// qs [Q, 64] scales, and (w8 non-null) the head weights with the scale and the 1/128 of the unnormalised rotation
+// folded in, w8 [Q, 64] = iw qs / 128.  Query q's position as the scan takes it (pos, pos0, qps, cu: see
+// idx_qpos).  Block (q, quarter): 16 warps, one head each (heads 16 quarter ..); lane l holds elements 4l .. 4l + 3.  Everything up to the stores reads step inputs only (queries, positions, frequencies), so it runs
 // before the programmatic wait, beside the preceding kernels; the stores wait for them (the workspace may still
 // be read by an earlier call).
 constexpr int kQuantHeads = 16;
 __global__ void __launch_bounds__(32 * kQuantHeads) k_quant_iq(const __nv_bfloat16* __restrict__ iq,
-                                                               const int32_t* __restrict__ pos,
+                                                               const __nv_bfloat16* __restrict__ iw,
+                                                               const int32_t* __restrict__ pos, int pos0, int qps,
+                                                               const int32_t* __restrict__ cu, int nseq,
                                                                const float* __restrict__ inv_freq, int R,
-                                                               uint8_t* __restrict__ q8, float* __restrict__ qs) {
+                                                               uint8_t* __restrict__ q8, float* __restrict__ qs,
+                                                               float* __restrict__ w8) {
   pdl_trigger();
   __shared__ float rc[64], rs[64];
   const int q = blockIdx.x, h = blockIdx.y * kQuantHeads + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const uint2 raw = __ldg(reinterpret_cast<const uint2*>(iq + ((size_t)q * 64 + h) * 128 + 4 * lane));
+  const float wh = w8 ? __bfloat162float(iw[(size_t)q * 64 + h]) : 0.f;
   if (threadIdx.x < R / 2) {
-    const int p = __ldg(pos + q);
+    int p;
+    if (cu) {
+      const int b = varlen_seq(cu, nseq, q);
+      p = __ldg(pos + b) + q - __ldg(cu + b);
+    } else {
+      p = pos ? __ldg(pos + q / qps) + q % qps : pos0 + q;
+    }
     sincosf(__fmul_rn((float)p, __ldg(inv_freq + threadIdx.x)), &rs[threadIdx.x], &rc[threadIdx.x]);
   }
   __syncthreads();
@@ -742,7 +761,10 @@ __global__ void __launch_bounds__(32 * kQuantHeads) k_quant_iq(const __nv_bfloat
   const uint32_t packed = fp8_rotate_quantize(u, lane, &scale);
   pdl_wait();
   *reinterpret_cast<uint32_t*>(q8 + ((size_t)q * 64 + h) * 128 + 4 * lane) = packed;
-  if (lane == 0) qs[(size_t)q * 64 + h] = scale;
+  if (lane == 0) {
+    qs[(size_t)q * 64 + h] = scale;
+    if (w8) w8[(size_t)q * 64 + h] = wh * (scale * 0.0078125f);
+  }
 }
 
 // gcu[b] = sum over sequences before b of ceil(T_b / 4) (T_b = cu[b+1] - cu[b], an inconsistent entry counted as
@@ -837,23 +859,37 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
   }
   const int grid = min(g_num_sms, a.n_items);
   if (fp8) {
-    // decode only: the quantised queries go into the query-output area of ws, the keys are fp8 rows
-    if (!pos || G != 1 || overlap || cu || !ws) return cudaErrorInvalidValue;
-    auto* q8 = static_cast<uint8_t*>(ws);
+    // the quantised queries go into the query-output area of ws (after the group table, if any): codes
+    // [Q, 64, 128], scales [Q, 64] and, for 4-query groups, the folded head weights [Q, 64]; the keys are fp8 rows
+    if (overlap || !ws) return cudaErrorInvalidValue;
+    const size_t off = cu ? ((size_t)(a.nseq + 1) * 4 + 255) / 256 * 256 : 0;
+    auto* q8 = static_cast<uint8_t*>(ws) + off;
     auto* qsc = reinterpret_cast<float*>(q8 + (size_t)Q * 64 * 128);
+    float* w8 = G == 4 ? qsc + (size_t)Q * 64 : nullptr;
     CSA_LAUNCH(k_quant_iq, dim3(Q, 64 / kQuantHeads), dim3(32 * kQuantHeads), 0, s,
-               static_cast<const __nv_bfloat16*>(iq), pos, inv_freq, L.R, q8, qsc);
-    // the key rows' codes (bytes 0-127, swizzled) and scales (bytes 128-143) by two tensor maps
-    CUtensorMap tk8, tks;
+               static_cast<const __nv_bfloat16*>(iq), static_cast<const __nv_bfloat16*>(iw), pos, pos0, a.qps, cu,
+               a.nseq, inv_freq, L.R, q8, qsc, w8);
+    // the key rows' codes (bytes 0-127, swizzled) and scales (bytes 128-143) by two tensor maps; 4-query groups
+    // copy their 256 code rows by TMA too
+    CUtensorMap tk8, tks, tq8;
     if (!make_tmap_2d_u8(&tk8, ikeys, (uint64_t)Bk * cap, kFp8RowBytes, kFp8RowBytes, 128, kTileRows, true) ||
-        !make_tmap_2d_u8(&tks, ikeys, (uint64_t)Bk * cap, kFp8RowBytes, kFp8RowBytes, 16, kTileRows, false))
+        !make_tmap_2d_u8(&tks, ikeys, (uint64_t)Bk * cap, kFp8RowBytes, kFp8RowBytes, 16, kTileRows, false) ||
+        !make_tmap_2d_u8(&tq8, q8, (uint64_t)Q * 64, 128, 128, 128, 64 * G, true))
       return cudaErrorInvalidValue;
     a.q8 = q8;
     a.qs = qsc;
-    constexpr int smem = IdxCfg<1, true>::kSmem;
-    cudaFuncSetAttribute(k_tc_index_scores<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    CSA_LAUNCH(k_tc_index_scores<1, false, true>, dim3(grid), dim3(IdxCfg<1, true>::kThreads), smem, s, tk8, tq, tks,
-               a);
+    a.w8 = w8;
+    if (G == 1) {
+      constexpr int smem = IdxCfg<1, true>::kSmem;
+      cudaFuncSetAttribute(k_tc_index_scores<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      CSA_LAUNCH(k_tc_index_scores<1, false, true>, dim3(grid), dim3(IdxCfg<1, true>::kThreads), smem, s, tk8, tq8,
+                 tks, a);
+    } else {
+      constexpr int smem = IdxCfg<4, true>::kSmem;
+      cudaFuncSetAttribute(k_tc_index_scores<4, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      CSA_LAUNCH(k_tc_index_scores<4, false, true>, dim3(grid), dim3(IdxCfg<4, true>::kThreads), smem, s, tk8, tq8,
+                 tks, a);
+    }
     return cudaGetLastError();
   }
   if (G == 1 && overlap) {

@@ -105,11 +105,12 @@ enum {
  *     rows); a query still attends only its last W tokens.  Every call of a layer
  *     takes buffers of those sizes.
  *   index_fp8: 0 (index keys in the model dtype) or 1 (fp8 index rows of
- *     CSA_FP8_ROW_BYTES: the index pool is then a [B, cap, 144] byte tensor that
- *     csa_compress_append / _pair write and csa_index_topk reads; ratio 4, bf16,
- *     Hi = 64, Di = 128 (D != 128), R <= 64 and a multiple of 8 only, else
- *     CSA_ERR_UNSUPPORTED; the other index calls
- *     return CSA_ERR_UNSUPPORTED with it). */
+ *     CSA_FP8_ROW_BYTES: the index pool, written by the compress calls and read
+ *     by every index call (csa_index_topk, _verify, csa_attend_prefill_chunk,
+ *     _varlen), is then a [B, cap, 144] byte tensor (a prefill chunk's ikeys
+ *     [cap, 144]); ratio 4, bf16, Hi = 64, Di = 128 (D != 128), R <= 64 only,
+ *     else CSA_ERR_UNSUPPORTED; csa_index_topk_overlapped returns
+ *     CSA_ERR_UNSUPPORTED with it). */
 typedef struct {
   int dtype;
   int H, D, R, W, ratio, Hi, Di, topk, X;

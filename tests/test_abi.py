@@ -170,8 +170,8 @@ def test_binding_checks_dtypes_and_shapes_before_the_device(lib):
 
 
 def test_fp8_index_rows_host_checks(lib):
-    """index_fp8: 0 or 1; fp8 rows need ratio 4, bf16, Hi = 64, Di = 128 and D != Di; only the decode index call
-    and the compress calls take them, the other index entry points refuse the layer before touching a pointer."""
+    """index_fp8: 0 or 1; fp8 rows need ratio 4, bf16, Hi = 64, Di = 128, R <= 64 and D != Di; the overlapped index
+    call refuses such a layer before touching a pointer."""
     n = ctypes.c_size_t()
     assert lib.csa_workspace_size(ctypes.byref(_layer(index_fp8=1)), B.OP_INDEX_TOPK, 32, 1, 8400,
                                   ctypes.byref(n)) == B.CSA_OK
@@ -182,13 +182,6 @@ def test_fp8_index_rows_host_checks(lib):
     L8 = _layer(index_fp8=1, rollback=8)
     assert lib.csa_index_topk_overlapped(ctypes.byref(L8), FAKE, FAKE, 1, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE,
                                          FAKE, 1 << 30, FAKE, None, None) == B.CSA_ERR_UNSUPPORTED
-    assert lib.csa_attend_prefill_chunk(ctypes.byref(L8), FAKE, FAKE, FAKE, FAKE, FAKE, 8, 0, FAKE, FAKE, FAKE, 10,
-                                        FAKE, FAKE, FAKE, None, FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_UNSUPPORTED
-    assert lib.csa_index_topk_verify(ctypes.byref(L8), FAKE, FAKE, 1, 4, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                     FAKE, 1 << 30, FAKE, None) == B.CSA_ERR_UNSUPPORTED
-    assert lib.csa_attend_prefill_varlen(ctypes.byref(L8), FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, 8, 4, FAKE, FAKE,
-                                         FAKE, FAKE, 10, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, FAKE,
-                                         None) == B.CSA_ERR_UNSUPPORTED
 
 
 def test_index_rows_fp8_host_checks(lib):

@@ -206,3 +206,123 @@ def test_fp8_index_rows_and_selection(case):
         s16.pos += 1
     # a head's codes differ only when the fp32 RoPE of one of its elements rounds to the other bf16 neighbour
     assert mism <= heads // 10, f"{mism} of {heads} query heads quantised differently from the oracle"
+
+
+def _fp8_cache(cfg, T0, cap, tag):
+    """Both pools of B sequences from T0 seeded tokens each, the index pool as fp8 rows (the chunk kernel)."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    L8 = dataclasses.replace(G.lib_layer(cfg), index_fp8=True)
+    ca = G.lib_comp(csa_synth.compressor(cfg, "attn"))
+    ci = G.lib_comp(csa_synth.compressor(cfg, "index"))
+    s = _State(cfg, cap, True)
+    s.window = G.dev(csa_synth.empty_cache(cfg, cap).window)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    inv_freq = G.dev(csa_synth.inv_freq(cfg))
+    if T0:
+        x = G.dev(csa_synth.hidden(cfg, T0, tag=tag))
+        csa.compress_append(L8, ca, x, s.pos, s.front_a, s.pool, s.n_a, inv_freq, err=err)
+        csa.compress_append(L8, ci, x, s.pos, s.front_i, s.ikeys, s.n_i, inv_freq, err=err)
+        s.pos += T0
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return L8, ca, ci, s, err, inv_freq
+
+
+def _check_queries(layer, ws, off, Q, iws, ikeys_b, n_rows, positions, sel, n_sel, what):
+    """Selections of Q queries (query i of sequence seq[i] at position positions[i]) against the fp8 scores on the
+    GPU's own query codes (in ws at byte off) and key codes."""
+    a = ws.cpu().numpy()[off:]
+    qc = a[:Q * 64 * 128].reshape(Q, 64, 128).astype(np.int64)
+    qs = np.ascontiguousarray(a[Q * 64 * 128:Q * 64 * 128 + Q * 256]).view(np.float32).reshape(Q, 64)
+    g_sel, g_n = sel.cpu().numpy().reshape(Q, -1), n_sel.cpu().numpy().reshape(Q)
+    for i in range(Q):
+        kc, ks = _codes_scales(ikeys_b(i))
+        nv = O.visible_rows(layer, int(n_rows(i)), int(positions[i]))
+        scores = O.index_scores_fp8(layer, qc[i], qs[i], iws[i], kc[:nv], ks[:nv])
+        G.check_topk(g_sel[i][:g_n[i]], scores, layer.topk, nv, what=f"{what} query {i}")
+
+
+@pytest.mark.parametrize("T", [4, 5])
+def test_fp8_verify_blocks(T):
+    """Verify blocks on fp8 rows: T = 4 scores four queries per product (the 4-query instance), T = 5 one."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=2, ctx=0, rollback=T - 1 + 4)
+    T0 = 2047
+    cap = (T0 + 3 * T) // 4 + 40
+    L8, ca, ci, s, err, inv_freq = _fp8_cache(cfg, T0, cap, 51)
+    layer = oracle_layer(cfg)
+    for k in range(2):  # the second block crosses 512 visible rows for some queries
+        blk = [csa_synth.step_inputs(cfg.replace(cid=cfg.cid + 960 + k), i) for i in range(T)]
+        x = G.dev(torch.cat([b.x for b in blk], dim=1))
+        csa.compress_append_pair(L8, ca, ci, x, s.pos, s.front_a, s.pool, s.n_a, s.front_i, s.ikeys, s.n_i, inv_freq,
+                                 err=err)
+        iq = torch.stack([b.iq for b in blk], 1)
+        iw = torch.stack([b.iw for b in blk], 1)
+        sel = torch.empty(cfg.B, T, cfg.topk, dtype=torch.int32, device="cuda")
+        n_sel = torch.empty(cfg.B, T, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(csa.workspace_size(L8, csa.OP_INDEX_TOPK, cfg.B * T, 1, cap), dtype=torch.uint8,
+                         device="cuda")
+        csa.index_topk_verify(L8, G.dev(iq), G.dev(iw), s.ikeys, s.n_i, s.pos, inv_freq, sel, n_sel, ws=ws, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        pos = s.pos.cpu().numpy()
+        n = s.n_i.cpu().numpy()
+        Q = cfg.B * T
+        _check_queries(layer, ws, 0, Q, f64(iw).reshape(Q, -1), lambda i: s.ikeys[i // T], lambda i: n[i // T],
+                       [pos[i // T] + i % T for i in range(Q)], sel, n_sel, f"verify block {k}")
+        csa.advance_positions(s.pos, T)
+
+
+def test_fp8_prefill_chunk_and_varlen():
+    """A prefill chunk (one sequence) and a packed batch on fp8 rows, both through the 4-query instance (the packed
+    batch from its group table); selections against the fp8 scores on the GPU's codes."""
+    import deepseek_v4_compressed_csa_gb300 as csa
+    cfg = csa_synth.CONFIGS[3].replace(B=1, ctx=0)
+    T0, T = 2099, 41
+    cap = (T0 + T) // 4 + 30
+    L8, ca, ci, s, err, inv_freq = _fp8_cache(cfg, T0, cap, 52)
+    layer = oracle_layer(cfg)
+    ch = csa_synth.chunk_inputs(cfg.replace(cid=cfg.cid + 970), T)
+    x = G.dev(ch.x)
+    n_i = s.n_i
+    csa.compress_append(L8, ca, x, s.pos, s.front_a, s.pool, s.n_a, inv_freq, err=err)
+    csa.compress_append(L8, ci, x, s.pos, s.front_i, s.ikeys, n_i, inv_freq, err=err)
+    out = torch.empty(T, cfg.H, cfg.D, dtype=cfg.storage, device="cuda")
+    sel = torch.empty(T, cfg.topk, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(csa.workspace_size(L8, csa.OP_ATTEND_PREFILL, 1, T, cap), dtype=torch.uint8, device="cuda")
+    csa.attend_prefill_chunk(L8, G.dev(ch.q), G.dev(ch.kv), G.dev(ch.iq), G.dev(ch.iw), G.dev(csa_synth.sinks(cfg)),
+                             T0, s.window[0], s.pool[0], s.ikeys[0], s.n_a, inv_freq, out, sel_out=sel, ws=ws, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    n = int(s.n_a.item())
+    n_sel = torch.tensor([int((sel[i] >= 0).sum()) for i in range(T)], dtype=torch.int32)
+    _check_queries(layer, ws, 0, T, f64(ch.iw), lambda i: s.ikeys[0], lambda i: n, [T0 + i for i in range(T)], sel,
+                   n_sel, "prefill")
+    # a packed batch: a sequence of 2099 tokens takes 9 more, one of 2051 takes 30, one empty chunk in between
+    cfgv = csa_synth.CONFIGS[3].replace(B=3, ctx=0)
+    lens = [9, 0, 30]
+    T0v = 2099
+    capv = (T0v + 40) // 4 + 30
+    L8, ca, ci, sv, err, inv_freq = _fp8_cache(cfgv, T0v, capv, 53)
+    N = sum(lens)
+    cu = torch.tensor([0, 9, 9, 39], dtype=torch.int32, device="cuda")
+    chv = csa_synth.chunk_inputs(cfgv.replace(cid=cfgv.cid + 980), N)
+    xv = G.dev(chv.x[0])
+    csa.compress_append_varlen(L8, ca, xv, cu, max(lens), sv.pos, sv.front_a, sv.pool, sv.n_a, inv_freq, err=err)
+    csa.compress_append_varlen(L8, ci, xv, cu, max(lens), sv.pos, sv.front_i, sv.ikeys, sv.n_i, inv_freq, err=err)
+    out = torch.empty(N, cfgv.H, cfgv.D, dtype=cfgv.storage, device="cuda")
+    sel = torch.empty(N, cfgv.topk, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(csa.workspace_size(L8, csa.OP_ATTEND_PREFILL_VARLEN, 3, N, capv), dtype=torch.uint8,
+                     device="cuda")
+    csa.attend_prefill_varlen(L8, G.dev(chv.q), G.dev(chv.kv), G.dev(chv.iq), G.dev(chv.iw),
+                              G.dev(csa_synth.sinks(cfgv)), cu, max(lens), sv.pos, sv.window, sv.pool, sv.ikeys, sv.n_a,
+                              inv_freq, out, sel_out=sel, ws=ws, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    seq = [0] * 9 + [2] * 30
+    posq = [T0v + i for i in range(9)] + [T0v + i for i in range(30)]
+    nv = sv.n_a.cpu().numpy()
+    n_sel = torch.tensor([int((sel[i] >= 0).sum()) for i in range(N)], dtype=torch.int32)
+    off = (4 * 4 + 255) // 256 * 256  # the group table of 3 + 1 entries comes first
+    _check_queries(layer, ws, off, N, f64(chv.iw), lambda i: sv.ikeys[seq[i]], lambda i: nv[seq[i]], posq, sel, n_sel,
+                   "varlen")
