@@ -959,11 +959,12 @@ def run_ours(args):
         assert wl.err.item() == 0, f"device error word {wl.err.item()}"
 
     # ---- prefill chunk (config 5), timed once per repeat from a restored snapshot
-    prefill = prefill_varlen = None
+    prefill = prefill_varlen = prefill_fp8 = None
     if not args.no_prefill:
         prefill = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
         if not args.no_other_configs:
             prefill_varlen = run_prefill_varlen(csa, csa_synth, dev, flush, repeats=args.prefill_repeats)
+            prefill_fp8 = run_prefill(csa, csa_synth, dev, flush, repeats=args.prefill_repeats, index_fp8=True)
 
     trim = trim_line(csa, csa_synth, dev)
     shared = None if args.no_other_configs else shared_line(csa, csa_synth, dev, flush, args.steps, args.warmup)
@@ -1025,6 +1026,7 @@ def run_ours(args):
                 "index_fp8": bool(args.index_fp8),
                 "prefill": prefill,
                 "prefill_varlen": prefill_varlen,
+                "prefill_fp8_index_keys": prefill_fp8,
                 "other_decode_workloads": others,
                 "trim": trim,
                 "v41_shared_caches": shared,
@@ -1061,19 +1063,25 @@ def run_ours(args):
     return result
 
 
-def run_prefill(csa, csa_synth, dev, flush, repeats: int):
+def run_prefill(csa, csa_synth, dev, flush, repeats: int, index_fp8: bool = False):
+    """One 4096-token chunk on a 64K cache (both compress calls + csa_attend_prefill_chunk), timed from a restored
+    snapshot; index_fp8: the index pool as fp8 rows (the cache's bf16 rows converted by csa_index_rows_fp8)."""
     import torch
     cfg = csa_synth.CONFIGS[5]
     cap = (cfg.ctx + cfg.T) // cfg.ratio + 8
     host = csa_synth.synth_cache(cfg, cap)
     d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
     L = csa.Layer(dtype=cfg.storage, H=cfg.H, D=cfg.D, R=cfg.R, W=cfg.W, ratio=cfg.ratio, Hi=cfg.Hi, Di=cfg.Di,
-                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps)
+                  topk=cfg.topk, X=cfg.X, scale=cfg.scale, rms_eps=cfg.rms_eps, index_fp8=index_fp8)
 
     def comp(c):
         return csa.Compressor(wkv=d(c.wkv), wgate=d(c.wgate), ape=d(c.ape), norm_w=d(c.norm_w), d=c.d)
     ca, ci = comp(csa_synth.compressor(cfg, "attn")), comp(csa_synth.compressor(cfg, "index"))
     snap = {k: d(getattr(host, k)) for k in ("pool", "ikeys", "window", "front_attn", "front_index", "n_rows", "pos")}
+    if index_fp8:
+        rows = torch.empty(snap["ikeys"].shape[:-1] + (csa.FP8_ROW_BYTES,), dtype=torch.uint8, device=dev)
+        csa.index_rows_fp8(L, snap["ikeys"], rows)
+        snap["ikeys"] = rows
     st = {k: v.clone() for k, v in snap.items()}
     n_i = st["n_rows"].clone()
     ch = csa_synth.chunk_inputs(cfg)
@@ -1106,11 +1114,13 @@ def run_prefill(csa, csa_synth, dev, flush, repeats: int):
     flops = (nvis_sum * cfg.Hi * cfg.Di * 2 + cfg.T * (cfg.topk + cfg.W) * cfg.H * cfg.D * 4 +
              cfg.T * cfg.X * (2 * 2 * (cfg.D + cfg.Di)) * 2)
     _, tflops, _ = _peaks()
-    return {"workload": cfg.name, "tok_per_s": round(cfg.T / (ms / 1e3), 1), "ms_per_chunk": round(ms, 4),
-            "ms_per_chunk_p10_p50_p90": [round(x, 4) for x in _percentiles(times)],
+    return {"workload": cfg.name + (" fp8-index-keys" if index_fp8 else ""), "tok_per_s": round(cfg.T / (ms / 1e3), 1),
+            "ms_per_chunk": round(ms, 4), "ms_per_chunk_p10_p50_p90": [round(x, 4) for x in _percentiles(times)],
             "algorithmic_tflop": round(flops / 1e12, 4),
             "tensor_frac": round(flops / (ms / 1e3) / 1e12 / tflops, 4), "repeats": repeats,
-            "dram_traffic_bytes": _traffic("prefill_chunk_bytes", 1)}
+            "tensor_frac_note": ("the same bf16-equivalent flop count and bf16 peak; the index products here are "
+                                 "e4m3 (twice the bf16 rate)") if index_fp8 else None,
+            "dram_traffic_bytes": None if index_fp8 else _traffic("prefill_chunk_bytes", 1)}
 
 
 # A ragged prefill batch: eight requests' chunks (4096 tokens in all) at contexts from 2K to 64K, packed.
@@ -1301,6 +1311,7 @@ def main():
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         print(json.dumps(run_prefill(csa, csa_synth, dev, flush, args.prefill_repeats)))
         print(json.dumps(run_prefill_varlen(csa, csa_synth, dev, flush, args.prefill_repeats)))
+        print(json.dumps(run_prefill(csa, csa_synth, dev, flush, args.prefill_repeats, index_fp8=True)))
         return
     if args.oracle_sample:
         cid, seqs, warmup, steps, budget = args.oracle_sample
