@@ -284,6 +284,13 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
         tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
     }
   };
+  // G = 1, bf16 (not overlapped): query g's block, already roped by the kernel before (k_rope_iq16), copied by TMA
+  // into slot `slot`
+  auto issue_q1 = [&](int g, int slot) {
+    tc::mbar_arrive_expect_tx(&q_loaded[slot], C::kQBytes);
+    tc::tma_load_2d(qbuf + slot * C::kQBytes, &tm_q, &q_loaded[slot], 0, g * 64);
+    tc::tma_load_2d(qbuf + slot * C::kQBytes + C::kQBytes / 2, &tm_q, &q_loaded[slot], 64, g * 64);
+  };
   // fp8 (G = 1): group g's codes and head pt's scale, the preceding kernel's output (so after the wait); loads
   // that stay where they are written (the second group's must not be moved behind the key stream)
   auto load_codes = [&](int g, Pre& pre) {
@@ -294,10 +301,11 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     }
     pre.qsv = __uint_as_float(tc::ld_nc_u32_now(a.qs + (size_t)g * 64 + pt));
   };
-  auto load_first = [&](int g, Pre& pre) {
+  // (rows = false: everything but the query rows)
+  auto load_first = [&](int g, Pre& pre, bool rows = true) {
     if constexpr (!kFp8 && G != 4) {
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
+      for (int b = 0; b < kBatch && rows; ++b) {
         const int e = pt + b * kPrepThreads;
         const int q = g * G + (e >> 10), h = (e >> 4) & 63, c = e & 15;
         pre.raw[b] = (e < kChunks && q < a.Q)
@@ -334,8 +342,13 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     i_begin = min(a.n_items, item_at(x0));
     i_end = blockIdx.x + 1 == gridDim.x ? a.n_items : min(a.n_items, item_at(x1));
   }
-  Pre pre_a, pre_b;  // pre_b: fp8, the range's second group
-  bool g1_loaded = false;
+  Pre pre_a, pre_b;  // pre_b: the range's second group (fp8, or bf16 with roped copies)
+  bool g1_loaded = false, q_copies = false;
+  // bf16 decode (G = 1, not overlapped): the queries come roped from the kernel before, and the blocks of the range's
+  // first two groups are copied by TMA right after the wait, before the key stream starts; the query warps then
+  // only write the head weights (measured: behind the stream a load round trip takes ~10 us and 16 KB of
+  // shared-memory stores ~8 us, so a block built there started a CTA's scan ~8 us after its wait)
+  constexpr bool kRopedCopy = G == 1 && !kFp8 && !kOverlap;
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
   // The first query block is requested before the wait (step inputs), except with a group table or fp8 queries,
@@ -343,16 +356,17 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   // the wait (a prefill chunk's first groups may have none), so the loop below drains this copy if it starts at a
   // later group.
   if (warp >= C::kPrepWarp0 && i_begin < i_end) {
-    if (G == 4 && pt == 0) {
-      // this thread issues the block copies: it initialises their barrier itself, ahead of the CTA-wide sync
-      tc::mbar_init(&q_loaded[0], 1);
+    if ((G == 4 || kRopedCopy) && pt == 0) {
+      // this thread issues the block copies: it initialises their barriers itself, ahead of the CTA-wide sync
+      for (int sl = 0; sl < C::kQSlots; ++sl) tc::mbar_init(&q_loaded[sl], 1);
       tc::fence_mbar_init();
       tc::tma_prefetch(&tm_q);
     }
     if (G != 4 || !(a.gcu || kFp8)) {
       if (G == 4) issue_q(g0);
-      load_first(g0, pre_a);
-      if (kFp8 && g1 >= 0) load_first(g1, pre_b);  // fp8: the second group's weights and position too
+      load_first(g0, pre_a, !kRopedCopy);
+      // fp8 and roped copies: the second group's weights and position too
+      if ((kFp8 || kRopedCopy) && g1 >= 0) load_first(g1, pre_b, false);
     }
   }
   // The overlapped decode scan does not wait for its predecessors here: it reads only index-key rows complete
@@ -375,6 +389,16 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     if ((a.gcu || kFp8) && warp >= C::kPrepWarp0 && i_begin < i_end) {
       issue_q(g0);
       load_first(g0, pre_a);
+    }
+  }
+  if constexpr (kRopedCopy) {
+    if (warp >= C::kPrepWarp0 && i_begin < i_end) {
+      if (pt == 0) {
+        issue_q1(g0, 0);
+        if (g1 >= 0) issue_q1(g1, 1);
+      }
+      q_copies = true;
+      g1_loaded = g1 >= 0;
     }
   }
   if (warp == 1) {
@@ -622,6 +646,25 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
       } else {
         tc::named_bar(3, kPrepThreads);  // the previous group's RoPE table is no longer read
       }
+      if constexpr (kRopedCopy) {
+        if (k == 0) {  // both copies land before any slot is written or read
+          const bool ok = tc::mbar_wait(&q_loaded[0], 0) && (!g1_loaded || tc::mbar_wait(&q_loaded[1], 0));
+          if (tc::named_bar_any(3, kPrepThreads, !ok)) { failed = true; break; }
+          q_copies = false;  // landed
+        }
+        if ((k == 0 && g == g0) || (k == 1 && g == g1 && g1_loaded)) {
+          wbuf[slot * N + pt] = (k == 0 ? pre_a : pre_b).wv[0] * a.wscale;  // the block was copied into this slot
+        } else {  // a range that skips its first group, or a third group: the block is built here
+          load_first(g, pre_a);
+          if (pt < 32) sincosf(__fmul_rn((float)pre_a.p, pre_a.th_freq), &rsin[pt], &rcos[pt]);
+          tc::named_bar(3, kPrepThreads);
+          rope_store(qbuf + slot * C::kQBytes, pt, pre_a.raw, g);
+          wbuf[slot * N + pt] = pre_a.wv[0] * a.wscale;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&q_full[slot]);
+        continue;
+      }
       const bool from_b = kFp8 && g == g1 && g1_loaded;  // fp8: the second group, requested after the wait
       Pre& pre = from_b ? pre_b : pre_a;
       if (g != g0 && !from_b) {  // a later group: request it now
@@ -698,6 +741,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
     }
     // a block copy that no group used (a range without tiles) lands before the CTA exits
     if (G == 4 && q_pending >= 0 && !wait_q()) failed = true;
+    if (kRopedCopy && q_copies) {
+      if (!tc::mbar_wait(&q_loaded[0], 0)) failed = true;
+      if (g1_loaded && !tc::mbar_wait(&q_loaded[1], 0)) failed = true;
+    }
   }
   if (failed) atomicOr(a.err, tc::kErrTimeout);
   tc::fence_before_sync();
@@ -765,6 +812,38 @@ __global__ void __launch_bounds__(32 * kQuantHeads) k_quant_iq(const __nv_bfloat
     qs[(size_t)q * 64 + h] = scale;
     if (w8) w8[(size_t)q * 64 + h] = wh * (scale * 0.0078125f);
   }
+}
+
+// Roped bf16 index queries for the one-query scan: qr [Q, 64, 128], query q at pos[q / qps] + q % qps, its last R
+// dims roped (the scan's arithmetic: fp32 angle, sincosf, one fused multiply-add a component, bf16).  Block (q,
+// quarter): 16 warps, one head each; lane l holds elements 4l .. 4l + 3.  Everything up to the stores reads step
+// inputs only, so it runs before the programmatic wait, beside the preceding kernels.
+__global__ void __launch_bounds__(32 * kQuantHeads) k_rope_iq16(const __nv_bfloat16* __restrict__ iq,
+                                                                const int32_t* __restrict__ pos, int qps,
+                                                                const float* __restrict__ inv_freq, int R,
+                                                                __nv_bfloat16* __restrict__ qr) {
+  pdl_trigger();
+  __shared__ float rc[64], rs[64];
+  const int q = blockIdx.x, h = blockIdx.y * kQuantHeads + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const size_t off = ((size_t)q * 64 + h) * 128 + 4 * lane;
+  uint2 raw = __ldg(reinterpret_cast<const uint2*>(iq + off));
+  if (threadIdx.x < R / 2) {
+    const int p = __ldg(pos + q / qps) + q % qps;
+    sincosf(__fmul_rn((float)p, __ldg(inv_freq + threadIdx.x)), &rs[threadIdx.x], &rc[threadIdx.x]);
+  }
+  __syncthreads();
+  __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i0 = 4 * lane + 2 * k;  // element pair (i0, i0 + 1)
+    if (i0 >= 128 - R) {
+      const int i = (i0 - (128 - R)) >> 1;
+      const float2 x = __bfloat1622float2(hv[k]);
+      hv[k] = __floats2bfloat162_rn(fmaf(x.x, rc[i], -x.y * rs[i]), fmaf(x.x, rs[i], x.y * rc[i]));
+    }
+  }
+  pdl_wait();
+  *reinterpret_cast<uint2*>(qr + off) = raw;
 }
 
 // gcu[b] = sum over sequences before b of ceil(T_b / 4) (T_b = cu[b+1] - cu[b], an inconsistent entry counted as
@@ -890,6 +969,19 @@ cudaError_t launch_tc_index_scores(const Dims& L, const void* iq, const void* iw
       CSA_LAUNCH(k_tc_index_scores<4, false, true>, dim3(grid), dim3(IdxCfg<4, true>::kThreads), smem, s, tk8, tq8,
                  tks, a);
     }
+    return cudaGetLastError();
+  }
+  if (G == 1 && !overlap) {
+    // the queries roped by a kernel of their own into the query-output area of ws, copied into the scan by TMA
+    if (!pos || !ws) return cudaErrorInvalidValue;
+    auto* qr16 = static_cast<__nv_bfloat16*>(ws);
+    CSA_LAUNCH(k_rope_iq16, dim3(Q, 64 / kQuantHeads), dim3(32 * kQuantHeads), 0, s,
+               static_cast<const __nv_bfloat16*>(iq), pos, a.qps, inv_freq, L.R, qr16);
+    CUtensorMap tqr;
+    if (!make_tmap_2d_bf16(&tqr, qr16, (uint64_t)Q * 64, 128, 256, 64)) return cudaErrorInvalidValue;
+    constexpr int smem = IdxCfg<1>::kSmem;
+    cudaFuncSetAttribute(k_tc_index_scores<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    CSA_LAUNCH(k_tc_index_scores<1, false>, dim3(grid), dim3(IdxCfg<1>::kThreads), smem, s, tk, tqr, tk, a);
     return cudaGetLastError();
   }
   if (G == 1 && overlap) {
