@@ -284,18 +284,19 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
         tc::tma_load_2d(qbuf + C::kQBytes / 2, &tm_q, &q_loaded[0], 64, q0 * 64);
     }
   };
-  // G = 1, bf16 (not overlapped): query g's block, already roped by the kernel before (k_rope_iq16), copied by TMA
-  // into slot `slot`
+  // G = 1 (not overlapped): query g's block, already roped (bf16, k_rope_iq16) or quantised (fp8, k_quant_iq) by
+  // the kernel before, copied by TMA into slot `slot`
   auto issue_q1 = [&](int g, int slot) {
     tc::mbar_arrive_expect_tx(&q_loaded[slot], C::kQBytes);
     tc::tma_load_2d(qbuf + slot * C::kQBytes, &tm_q, &q_loaded[slot], 0, g * 64);
-    tc::tma_load_2d(qbuf + slot * C::kQBytes + C::kQBytes / 2, &tm_q, &q_loaded[slot], 64, g * 64);
+    if constexpr (!kFp8)  // fp8: one 128-byte box of codes per head row
+      tc::tma_load_2d(qbuf + slot * C::kQBytes + C::kQBytes / 2, &tm_q, &q_loaded[slot], 64, g * 64);
   };
   // fp8 (G = 1): group g's codes and head pt's scale, the preceding kernel's output (so after the wait); loads
   // that stay where they are written (the second group's must not be moved behind the key stream)
-  auto load_codes = [&](int g, Pre& pre) {
+  auto load_codes = [&](int g, Pre& pre, bool codes = true) {
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
+    for (int b = 0; b < kBatch && codes; ++b) {
       const int e = pt + b * kPrepThreads, h = (e >> 3) & 63, c = e & 7;
       pre.raw[b] = tc::ld_nc_v4_now(a.q8 + ((size_t)g * 64 + h) * 128 + c * 16);
     }
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   // first two groups are copied by TMA right after the wait, before the key stream starts; the query warps then
   // only write the head weights (measured: behind the stream a load round trip takes ~10 us and 16 KB of
   // shared-memory stores ~8 us, so a block built there started a CTA's scan ~8 us after its wait)
-  constexpr bool kRopedCopy = G == 1 && !kFp8 && !kOverlap;
+  constexpr bool kRopedCopy = G == 1 && !kOverlap;  // (fp8: the codes of k_quant_iq, the same way)
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
   // The first query block is requested before the wait (step inputs), except with a group table or fp8 queries,
@@ -376,13 +377,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
   // fp8: the quantised queries and their scales are the preceding kernel's output; the codes of the range's first
   // two groups are requested now, before the key stream starts (a load issued behind the stream took ~10 us)
-  if constexpr (kFp8 && G == 1) {
+  if constexpr (kFp8 && G == 1) {  // the head scales (the codes come by TMA, below)
     if (warp >= C::kPrepWarp0 && i_begin < i_end) {
-      load_codes(g0, pre_a);
-      if (g1 >= 0) {
-        load_codes(g1, pre_b);
-        g1_loaded = true;
-      }
+      load_codes(g0, pre_a, false);
+      if (g1 >= 0) load_codes(g1, pre_b, false);
     }
   }
   if constexpr (G == 4) {
@@ -652,14 +650,19 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
           if (tc::named_bar_any(3, kPrepThreads, !ok)) { failed = true; break; }
           q_copies = false;  // landed
         }
+        // fp8: the head's query scale and the 1/128 of the unnormalised rotation go into its weight
+        auto weight = [&](const Pre& pc) {
+          return (kFp8 ? pc.wv[0] * (pc.qsv * 0.0078125f) : pc.wv[0]) * a.wscale;
+        };
         if ((k == 0 && g == g0) || (k == 1 && g == g1 && g1_loaded)) {
-          wbuf[slot * N + pt] = (k == 0 ? pre_a : pre_b).wv[0] * a.wscale;  // the block was copied into this slot
+          wbuf[slot * N + pt] = weight(k == 0 ? pre_a : pre_b);  // the block was copied into this slot
         } else {  // a range that skips its first group, or a third group: the block is built here
           load_first(g, pre_a);
-          if (pt < 32) sincosf(__fmul_rn((float)pre_a.p, pre_a.th_freq), &rsin[pt], &rcos[pt]);
+          if constexpr (kFp8) load_codes(g, pre_a);
+          if (!kFp8 && pt < 32) sincosf(__fmul_rn((float)pre_a.p, pre_a.th_freq), &rsin[pt], &rcos[pt]);
           tc::named_bar(3, kPrepThreads);
           rope_store(qbuf + slot * C::kQBytes, pt, pre_a.raw, g);
-          wbuf[slot * N + pt] = pre_a.wv[0] * a.wscale;
+          wbuf[slot * N + pt] = weight(pre_a);
         }
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(&q_full[slot]);
