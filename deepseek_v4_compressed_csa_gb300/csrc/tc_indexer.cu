@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   constexpr bool kRopedCopy = G == 1 && !kOverlap;  // (fp8: the codes of k_quant_iq, the same way)
   const int g0 = min(i_begin, a.n_items - 1) / a.tiles_per_group;
   const int g1 = (g0 + 1) * a.tiles_per_group < i_end ? g0 + 1 : -1;
-  // The first query block is requested before the wait (step inputs), except with a group table or fp8 queries,
-  // which the kernel before writes.  G = 4: the range's first group is copied now; whether it has tiles is known only after
+  // The first query block is requested before the wait (step inputs), except with a group table, fp8 queries or
+  // roped copies (G = 1), which the kernel before writes.  G = 4: the range's first group is copied now; whether it has tiles is known only after
   // the wait (a prefill chunk's first groups may have none), so the loop below drains this copy if it starts at a
   // later group.
   if (warp >= C::kPrepWarp0 && i_begin < i_end) {
@@ -375,9 +375,9 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
   // call's kernels; it waits for them at its end instead, so that its successor's wait covers them.  (It follows
   // a projection kernel that lets successors start only once all earlier work is complete.)
   if (!kOverlap) pdl_wait();  // predecessor complete: its outputs are visible and its tensor memory is free
-  // fp8: the quantised queries and their scales are the preceding kernel's output; the codes of the range's first
-  // two groups are requested now, before the key stream starts (a load issued behind the stream took ~10 us)
-  if constexpr (kFp8 && G == 1) {  // the head scales (the codes come by TMA, below)
+  // fp8: the quantised queries and their scales are the preceding kernel's output; the head scales of the range's
+  // first two groups are requested now, before the key stream starts (a load issued behind the stream took ~10 us)
+  if constexpr (kFp8 && G == 1) {  // (the codes come by TMA, below)
     if (warp >= C::kPrepWarp0 && i_begin < i_end) {
       load_codes(g0, pre_a, false);
       if (g1 >= 0) load_codes(g1, pre_b, false);
@@ -668,12 +668,8 @@ __global__ void __launch_bounds__(IdxCfg<G, kFp8>::kThreads, G == 1 ? 2 : 1)
         tc::mbar_arrive(&q_full[slot]);
         continue;
       }
-      const bool from_b = kFp8 && g == g1 && g1_loaded;  // fp8: the second group, requested after the wait
-      Pre& pre = from_b ? pre_b : pre_a;
-      if (g != g0 && !from_b) {  // a later group: request it now
-        load_first(g, pre_a);
-        if constexpr (kFp8 && G == 1) load_codes(g, pre_a);
-      }
+      Pre& pre = pre_a;
+      if (g != g0) load_first(g, pre_a);  // a later group: request it now
       if constexpr (G == 4) {
         if (q_pending != g) {
           // the slot is free (first group, or the previous group's MMAs retired); a copy of a group without
@@ -763,9 +759,10 @@ int g_num_sms = 0;
 // 64 in that order), scaled by amax / 448 and rounded to E4M3 (nearest even, saturating): q8 [Q, 64, 128] codes,
 // qs [Q, 64] scales, and (w8 non-null) the head weights with the scale and the 1/128 of the unnormalised rotation
 // folded in, w8 [Q, 64] = iw qs / 128.  Query q's position as the scan takes it (pos, pos0, qps, cu: see
-// idx_qpos).  Block (q, quarter): 16 warps, one head each (heads 16 quarter ..); lane l holds elements 4l .. 4l + 3.  Everything up to the stores reads step inputs only (queries, positions, frequencies), so it runs
-// before the programmatic wait, beside the preceding kernels; the stores wait for them (the workspace may still
-// be read by an earlier call).
+// idx_qpos).  Block (q, quarter): 16 warps, one head each (heads 16 quarter ..); lane l holds elements 4l .. 4l + 3.
+// Everything up to the stores reads step inputs only (queries, positions, frequencies), so it runs before the
+// programmatic wait, beside the preceding kernels; the stores wait for them (the workspace may still be read by an
+// earlier call).
 constexpr int kQuantHeads = 16;
 __global__ void __launch_bounds__(32 * kQuantHeads) k_quant_iq(const __nv_bfloat16* __restrict__ iq,
                                                                const __nv_bfloat16* __restrict__ iw,
