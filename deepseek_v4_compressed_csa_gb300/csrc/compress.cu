@@ -278,6 +278,22 @@ constexpr int kTokChans = 2;  // channels per pooling thread: d <= 512
 // kernel's: the extra warps add zeros to the block sum).
 constexpr int kTokThreads = 512;
 
+// The bits of one element, by a load the compiler keeps where it is written, and their fp32 value (a bf16 is the
+// high half of its fp32).  The single-token kernel loads the window's older entries this way, every load issued
+// before any is used: converted as each arrived, the loads went out one after another.
+__device__ __forceinline__ uint32_t ld_bits_now(const __nv_bfloat16* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_bits_now(const float* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float bits_f(uint32_t v, const __nv_bfloat16*) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bits_f(uint32_t v, const float*) { return __uint_as_float(v); }
+
 // One pool's side of a single-token pooling launch.
 template <typename T>
 struct TokPool {
@@ -337,12 +353,13 @@ __global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, 
   const float fq = tid < R / 2 ? __ldg(inv_freq + tid) : 0.f;
   pdl_wait();
   // one round of requests: n_rows, the partials of the new token and, if it completes window j, the window's
-  // older entries; nothing is written before the state check
+  // older entries (their bits, converted where the pooling uses them; this kernel writes no slot it reads them
+  // from); nothing is written before the state check
   const int n = n_rows[b];
   const bool completes = (p0 + 1) % ratio == 0;
   const int j = (p0 + 1) / ratio - 1;
   const T* fr = frontier + (size_t)b * F * rowlen;
-  float g[kTokChans][kEnt - 1], kv[kTokChans][kEnt - 1];
+  uint32_t g[kTokChans][kEnt - 1], kv[kTokChans][kEnt - 1];
   if (completes) {
 #pragma unroll
     for (int i = 0; i < kTokChans; ++i) {
@@ -350,12 +367,12 @@ __global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, 
 #pragma unroll
       for (int e = 0; e < kEnt - 1; ++e) {
         const int t = p0 - (kEnt - 1) + e;
-        g[i][e] = 0.f;
-        kv[i][e] = 0.f;
+        g[i][e] = 0u;
+        kv[i][e] = 0u;
         if (c < d && t >= 0) {
           const T* row = fr + (size_t)(t % F) * rowlen + (e / ratio) * d + c;
-          g[i][e] = to_f(row[Ld]);
-          kv[i][e] = to_f(row[0]);
+          g[i][e] = ld_bits_now(row + Ld);
+          kv[i][e] = ld_bits_now(row);
         }
       }
     }
@@ -425,8 +442,8 @@ __global__ void __launch_bounds__(kTokThreads) k_pool_emit_token(TokPool<T> pa, 
         sv[e] = cur[Ld + d + c] + ap[i][e];
         kk[e] = cur[d + c];
       } else {
-        sv[e] = g[i][e] + ap[i][e];
-        kk[e] = kv[i][e];
+        sv[e] = bits_f(g[i][e], fr) + ap[i][e];
+        kk[e] = bits_f(kv[i][e], fr);
       }
     }
     float m = -INFINITY;
