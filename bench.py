@@ -42,8 +42,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum, every kernel captured cold) of one decode
 # layer-step of the headline workload and of one prefill chunk, with the hash of the kernel sources the counters
 # were taken on (csrc_digest()); the bench reports them only while the sources still hash the same.
-TRAFFIC = {"csrc_sha256": "3067eea87744158b", "decode_layer_step_bytes": 117_480_000,
-           "decode_fp8_layer_step_bytes": 87_534_000, "prefill_chunk_bytes": 1_233_679_000,
+TRAFFIC = {"csrc_sha256": "36a6e608430072f3", "decode_layer_step_bytes": 117_480_000,
+           "decode_fp8_layer_step_bytes": 87_534_000, "prefill_chunk_bytes": 1_234_002_000,
            "profile": "profiles/traffic_decode_b32_ctx32k_and_prefill_t4096.md"}
 
 
