@@ -226,6 +226,12 @@ def _dist():
     return None, 0, 1, 0
 
 
+def whole_job_rate(world: int, units_per_rank: float, slowest_ms: float) -> float:
+    """Units per second of the whole job: each of the world's replicas processes units_per_rank units in the timed
+    region, whose length is the slowest rank's (the max over ranks)."""
+    return world * units_per_rank / (slowest_ms / 1e3)
+
+
 def _max_over_ranks(dist, value: float, device) -> float:
     if dist is None:
         return value
@@ -983,7 +989,7 @@ def run_ours(args):
 
     hbm, tflops, peak_src = _peaks()
     ms_per_step = total_ms / (args.steps * nl)  # per layer-step
-    value = world * args.steps * nl / (total_ms / 1e3)
+    value = whole_job_rate(world, args.steps * nl, total_ms)
     nb = step_bytes(cfg, 0.5 * (n_start + n_end), args.index_fp8)
     tkey = "decode_fp8_layer_step_bytes" if args.index_fp8 else "decode_layer_step_bytes"
     step_avg_s = ms_per_step / 1e3
@@ -1048,7 +1054,7 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": int(nb["total"] * nl),
             },
             "cpu_baseline": cpu,
-            "e2e": {"value": round(world * nl * 1e3 / e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": round(whole_job_rate(world, nl, e2e_ms), 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": round(d2h / nl),
                     "per_model_step": {"layers": nl, "h2d_copies": nl, "h2d_bytes": h2d * nl, "d2h_bytes": d2h},
                     "pipeline": "step i+1's input copies run on a second stream during step i; one timed region over "
